@@ -1,0 +1,168 @@
+"""CPU oracle for batched descriptor building -- test infrastructure only.
+
+A ctypes front end over ``oracle.cpp``: plain single-threaded C++ written
+from the source pages' definitions. Only the tests, ``__graft_entry__``'s
+smoke check and the benchmark's CPU-baseline leg may import this package;
+the CUDA library never does, and this package never imports the library.
+
+All functions take and return numpy arrays (host memory).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PRP_OK, PRP_INVALID, PRP_OVERFLOW = 0, 1, 2
+MR_MISS, MR_EXACT, MR_CONTAINED, MR_INVALID = 0, 1, 2, 3
+ERR_RING_OVERFLOW = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so beside its source (plain g++, no GPU needed)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-o", tmp, _SRC],
+                       check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # A test may point this at a deliberately broken build of the
+            # oracle to check that the pins notice (tests/test_oracle_mutations.py).
+            path = os.environ.get("DB_ORACLE_LIB") or build()
+            lib = ctypes.CDLL(path)
+            u64, u32, i32, vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p
+            lib.oracle_prp_list_pages.restype = u64
+            lib.oracle_prp_list_pages.argtypes = [u64, u64, u64]
+            lib.oracle_prp_one.restype = u64
+            lib.oracle_prp_one.argtypes = [u64, u64, vp, u64, u64, u64, u64, vp, vp, i32]
+            lib.oracle_prp_build.restype = None
+            lib.oracle_prp_build.argtypes = [vp, u64, vp, u64, u64, u64, u64, vp, vp, vp, vp,
+                                             vp, i32]
+            lib.oracle_mr_round.restype = None
+            lib.oracle_mr_round.argtypes = [u64, u64, vp]
+            for name in ("oracle_mr_linear", "oracle_mr_bsearch"):
+                fn = getattr(lib, name)
+                fn.restype = None
+                fn.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp]
+            lib.oracle_wqe_bucket.restype = None
+            lib.oracle_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64,
+                                              vp, vp, vp]
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _u64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint64)
+
+
+# ----------------------------------------------------------------------- PRP
+def prp_list_pages(off: int, length: int, heap_size: int) -> int:
+    """List pages one request needs (0 for no list or an invalid request)."""
+    return int(_load().oracle_prp_list_pages(off, length, heap_size))
+
+
+def prp_one(off: int, length: int, lut: np.ndarray, heap_size: int, arena_base: int,
+            page_base: int, zero_tail: bool = False, fill: int = 0):
+    """Descriptors of one request placed at list page ``page_base``.
+
+    Returns (prp1, prp2, list) where ``list`` is [list_pages, 512] uint64
+    (slots the request leaves unwritten hold ``fill``).
+    """
+    lut = _u64(lut)
+    pages = prp_list_pages(off, length, heap_size)
+    lst = np.full((max(pages, 1), 512), fill, dtype=np.uint64)
+    prp = np.zeros(2, dtype=np.uint64)
+    got = _load().oracle_prp_one(off, length, _p(lut), lut.shape[0], heap_size, arena_base,
+                                 page_base, _p(prp), _p(lst), int(zero_tail))
+    assert got == pages
+    return int(prp[0]), int(prp[1]), lst[:pages]
+
+
+def prp_build(req: np.ndarray, lut: np.ndarray, heap_size: int, arena_base: int,
+              arena_cap_pages: int, zero_tail: bool = False, fill: int = 0) -> dict:
+    """Whole batch; returns prp [n,2], page_base [n], status [n], ctr [4], arena."""
+    req = _u64(req).reshape(-1, 2)
+    lut = _u64(lut)
+    n = req.shape[0]
+    arena = np.full((max(arena_cap_pages, 1), 512), fill, dtype=np.uint64)
+    prp = np.zeros((n, 2), dtype=np.uint64)
+    page_base = np.zeros(n, dtype=np.uint64)
+    status = np.zeros(n, dtype=np.uint8)
+    ctr = np.zeros(4, dtype=np.uint64)
+    _load().oracle_prp_build(_p(req), n, _p(lut), lut.shape[0], heap_size, arena_base,
+                             arena_cap_pages, _p(arena), _p(prp), _p(page_base), _p(status),
+                             _p(ctr), int(zero_tail))
+    return dict(prp=prp, page_base=page_base, status=status, ctr=ctr,
+                arena=arena[:arena_cap_pages])
+
+
+# ------------------------------------------------------------------------ MR
+def mr_round(addr: int, size: int):
+    """(valid, base, aend) of one range rounded to whole 4 KiB pages."""
+    out = np.zeros(3, dtype=np.uint64)
+    _load().oracle_mr_round(addr, size, _p(out))
+    return bool(out[0]), int(out[1]), int(out[2])
+
+
+def _mr(fn_name, queries, start, end, lkey):
+    q = _u64(queries).reshape(-1, 2)
+    start, end = _u64(start), _u64(end)
+    lkey = np.ascontiguousarray(lkey, dtype=np.uint32)
+    n = q.shape[0]
+    idx = np.zeros(n, dtype=np.int32)
+    lk = np.zeros(n, dtype=np.uint32)
+    kind = np.zeros(n, dtype=np.uint8)
+    getattr(_load(), fn_name)(_p(q), n, _p(start), _p(end), _p(lkey), start.shape[0],
+                              _p(idx), _p(lk), _p(kind))
+    return dict(idx=idx, lkey=lk, kind=kind)
+
+
+def mr_linear(queries, start, end, lkey) -> dict:
+    """The definition: first containing range by index, for every query."""
+    return _mr("oracle_mr_linear", queries, start, end, lkey)
+
+
+def mr_bsearch(queries, start, end, lkey) -> dict:
+    """Same result for sorted non-overlapping tables, by binary search."""
+    return _mr("oracle_mr_bsearch", queries, start, end, lkey)
+
+
+# ----------------------------------------------------------------------- WQE
+def wqe_bucket(req, peer_ptrs, rkeys, world: int, n_qp: int, local_base: int, lkey: int,
+               heap_size: int, depth: int, head, fill: int = 0) -> dict:
+    """Whole batch; returns rings [R, depth, 64] u8, head, count, ctr."""
+    req = _u64(req).reshape(-1, 2)
+    peer_ptrs = _u64(peer_ptrs)
+    rkeys = np.ascontiguousarray(rkeys, dtype=np.uint32)
+    n_rings = world * n_qp
+    rings = np.full((n_rings, depth, 64), fill, dtype=np.uint8)
+    head = _u64(head).copy()
+    count = np.zeros(n_rings, dtype=np.uint32)
+    ctr = np.zeros(4, dtype=np.uint64)
+    _load().oracle_wqe_bucket(_p(req), req.shape[0], _p(peer_ptrs), _p(rkeys), world, n_qp,
+                              local_base, lkey, heap_size, _p(rings), depth, _p(head),
+                              _p(count), _p(ctr))
+    return dict(rings=rings, head=head, count=count, ctr=ctr)

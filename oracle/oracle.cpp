@@ -1,0 +1,372 @@
+// CPU oracle for batched descriptor building -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, single-threaded statement of the three definitions that the CUDA
+// library computes, written for a reader to check by eye against the source
+// pages. Only the tests and the benchmark's CPU-baseline leg load it. It
+// shares no code, header, table or constant with the CUDA library.
+//
+// Sources (page title, section):
+//  * PRP building -- xNVMe "uPCIe CUDA" backend page: the introduction (the
+//    CUDA driver exports device memory at 64 KiB granularity, the physical
+//    address of each 64 KiB chunk sits in a lookup table, PRP entries are
+//    built at 4 KiB from sub-page offsets within a chunk), "Memory
+//    Architecture" (PRP lists live in a separate host-memory region) and
+//    "Limitations" (one 4 KiB list page holds 512 entries; with PRP1 that is
+//    513 x 4 KiB per command).
+//  * MR lookup -- "NCCL expert course 26: GPUDirect RDMA, DMA-BUF, MR and the
+//    registration cache": "IB Backend MR Cache" (rounding a range down/up to
+//    whole pages, worked table; reuse only if an existing MR fully contains
+//    the range, partial overlap is no hit) and "Communicator User
+//    Registration Cache" (page_floor / page_cover, sorted records).
+//  * Put translation -- "mori communication library analysis (1)": static
+//    heap address/key computation (raddr = peerPtrs[pe] + offset,
+//    rkey = peerRkeys[pe], lkey = the source object's lkey) and the
+//    warp-level WQE slot reservation (a post index per send queue).
+//
+// Readings where the pages are silent are listed with each function.
+//
+// Parity status: every function here is pinned by tests under tests/
+// (worked examples from the pages, brute force on tiny inputs, invariants,
+// library-routine equivalences).
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+typedef unsigned __int128 u128;
+
+const uint64_t kPage = 4096;        // NVMe memory page (host page size used for PRPs)
+const uint64_t kChunk = 65536;      // dma-buf export granule, one LUT entry each
+const uint64_t kListSlots = 512;    // 8-byte entries in one 4 KiB PRP list page
+
+[[noreturn]] void fail(const char* what) {
+  std::fprintf(stderr, "oracle: %s\n", what);
+  std::abort();
+}
+
+// Bus address of heap offset x: the LUT entry of the 64 KiB chunk that holds
+// x, plus x's offset inside that chunk.
+uint64_t bus_address(const uint64_t* lut, uint64_t n_lut, uint64_t x) {
+  uint64_t chunk = x / kChunk;
+  if (chunk >= n_lut) fail("heap offset beyond the LUT");
+  uint64_t chunk_base = lut[chunk];
+  if (chunk_base == 0 || chunk_base % kChunk != 0)
+    fail("LUT entry is not a non-zero 64 KiB-aligned address");
+  uint64_t inside = x % kChunk;
+  if (chunk_base + inside < chunk_base) fail("bus address wraps");
+  return chunk_base + inside;
+}
+
+// A request is well formed when it moves at least one byte, starts on a
+// dword boundary, and ends inside the heap.
+bool prp_request_valid(uint64_t off, uint64_t len, uint64_t heap_size) {
+  if (len == 0) return false;
+  if (off % 4 != 0) return false;
+  if ((u128)off + (u128)len > (u128)heap_size) return false;
+  return true;
+}
+
+// Number of 4 KiB memory pages that [off, off + len) touches.
+uint64_t pages_touched(uint64_t off, uint64_t len) {
+  uint64_t first = off / kPage;
+  uint64_t last = (off + len - 1) / kPage;
+  return last - first + 1;
+}
+
+// List pages needed for `entries` list entries when every page but the last
+// gives its final slot to a pointer to the next page.
+uint64_t list_pages_for(uint64_t entries) {
+  if (entries == 0) return 0;
+  uint64_t pages = 0;
+  uint64_t left = entries;
+  while (left > kListSlots) {   // this page cannot be the last one
+    pages += 1;
+    left -= kListSlots - 1;     // 511 entries + the chain pointer
+  }
+  return pages + 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Per-request list-page count (0 when no list is used or when invalid).
+// PRP1 covers the first page; a second page goes in PRP2; three or more
+// pages put every page after the first into a PRP list.
+uint64_t oracle_prp_list_pages(uint64_t off, uint64_t len, uint64_t heap_size) {
+  if (!prp_request_valid(off, len, heap_size)) return 0;
+  uint64_t n = pages_touched(off, len);
+  if (n < 3) return 0;
+  return list_pages_for(n - 1);
+}
+
+// Descriptors of ONE request whose list (if any) starts at list page
+// `page_base` of the arena. `list` receives the request's list pages
+// (list_pages * 512 words, laid out as they sit in the arena); untouched
+// slots are left as they are unless `zero_tail`. Returns the list-page count.
+uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_t n_lut,
+                        uint64_t heap_size, uint64_t arena_base, uint64_t page_base,
+                        uint64_t* prp /*[2]*/, uint64_t* list, int zero_tail) {
+  prp[0] = 0;
+  prp[1] = 0;
+  if (!prp_request_valid(off, len, heap_size)) return 0;
+  uint64_t n = pages_touched(off, len);
+  uint64_t first_page = off - off % kPage;        // heap offset of the first page
+  prp[0] = bus_address(lut, n_lut, off);          // PRP1 keeps the in-page offset
+  if (n == 1) return 0;
+  if (n == 2) {
+    prp[1] = bus_address(lut, n_lut, first_page + kPage);
+    return 0;
+  }
+  // n >= 3: PRP2 points at the first list page; the list holds pages 1..n-1.
+  if (arena_base % kPage != 0) fail("arena base not page aligned");
+  uint64_t n_list = list_pages_for(n - 1);
+  prp[1] = arena_base + page_base * kPage;
+  uint64_t page = 0;   // list page being filled, relative to page_base
+  uint64_t slot = 0;   // next free slot on it
+  for (uint64_t k = 1; k < n; ++k) {
+    bool more_after_this = (k + 1 < n);
+    if (slot == kListSlots - 1 && more_after_this) {
+      // Last slot of a full page with entries still to come: chain.
+      list[page * kListSlots + slot] = arena_base + (page_base + page + 1) * kPage;
+      page += 1;
+      slot = 0;
+    }
+    list[page * kListSlots + slot] = bus_address(lut, n_lut, first_page + k * kPage);
+    slot += 1;
+  }
+  if (page + 1 != n_list) fail("list page count mismatch");
+  if (zero_tail)
+    for (; slot < kListSlots; ++slot) list[page * kListSlots + slot] = 0;
+  return n_list;
+}
+
+// Whole batch, in request order.
+//  req        [n][2]: word 0 = heap offset, word 1 low 32 bits = length
+//  arena      host copy of the list arena, arena_cap_pages * 512 words
+//  prp        [n][2] out: PRP1, PRP2
+//  page_base  [n] out (nullable): first list page of each request (exclusive
+//             running sum of list pages, in request order)
+//  status     [n] out (nullable): 0 ok, 1 invalid, 2 list would not fit
+//  ctr        [4] out: total list pages, invalid count, overflow count, error bits (0)
+// A request whose list would end past the arena gets status 2, PRP {0,0}
+// and no list; it still advances the running page count.
+void oracle_prp_build(const uint64_t* req, uint64_t n, const uint64_t* lut, uint64_t n_lut,
+                      uint64_t heap_size, uint64_t arena_base, uint64_t arena_cap_pages,
+                      uint64_t* arena, uint64_t* prp, uint64_t* page_base, uint8_t* status,
+                      uint64_t* ctr, int zero_tail) {
+  uint64_t running = 0;
+  uint64_t n_invalid = 0, n_overflow = 0;
+  std::vector<uint64_t> scratch;
+  for (uint64_t i = 0; i < n; ++i) {
+    uint64_t off = req[2 * i];
+    uint64_t len = req[2 * i + 1] & 0xFFFFFFFFull;
+    uint8_t st = 0;
+    uint64_t pages = 0;
+    prp[2 * i] = 0;
+    prp[2 * i + 1] = 0;
+    if (page_base) page_base[i] = running;
+    if (!prp_request_valid(off, len, heap_size)) {
+      st = 1;
+      n_invalid += 1;
+    } else {
+      pages = oracle_prp_list_pages(off, len, heap_size);
+      // Only a request that needs list pages can run out of arena.
+      if (pages > 0 && running + pages > arena_cap_pages) {
+        st = 2;
+        n_overflow += 1;
+      } else {
+        uint64_t* list = pages ? arena + running * kListSlots : nullptr;
+        uint64_t got = oracle_prp_one(off, len, lut, n_lut, heap_size, arena_base, running,
+                                      prp + 2 * i, list, zero_tail);
+        if (got != pages) fail("list page count disagrees");
+      }
+    }
+    if (status) status[i] = st;
+    running += pages;
+  }
+  ctr[0] = running;
+  ctr[1] = n_invalid;
+  ctr[2] = n_overflow;
+  ctr[3] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// MR lookup.
+//
+// Rounding: the range [addr, addr + size) widens to whole 4 KiB pages,
+// base = page floor of addr, aend = base + pages * 4096 with
+// pages = ceil((addr + size - base) / 4096).
+// Reading: a range is INVALID (kind 3) when size == 0 or when the rounded end
+// would not fit in 64 bits (addr + size > 2^64 - 4096).
+// Classification: the lowest-index registered range [start_i, end_i) with
+// start_i <= base and aend <= end_i is the hit; EXACT (1) when both ends
+// match, CONTAINED (2) otherwise. No such range: MISS (0). Partial overlap
+// is a miss. Ranges are end-exclusive.
+
+static bool mr_round(uint64_t addr, uint64_t size, uint64_t* base, uint64_t* aend) {
+  if (size == 0) return false;
+  u128 stop = (u128)addr + (u128)size;
+  if (stop > (u128)(UINT64_MAX - kPage + 1)) return false;
+  uint64_t b = addr - addr % kPage;
+  uint64_t pages = (uint64_t)((stop - b + kPage - 1) / kPage);
+  *base = b;
+  *aend = b + pages * kPage;
+  return true;
+}
+
+void oracle_mr_round(uint64_t addr, uint64_t size, uint64_t* out /*[3]: valid, base, aend*/) {
+  uint64_t b = 0, e = 0;
+  out[0] = mr_round(addr, size, &b, &e) ? 1 : 0;
+  out[1] = b;
+  out[2] = e;
+}
+
+// The definition: a scan over the whole table for every query.
+void oracle_mr_linear(const uint64_t* q, uint64_t n_q, const uint64_t* start,
+                      const uint64_t* end, const uint32_t* lkey, uint64_t n_mr,
+                      int32_t* idx, uint32_t* lkey_out, uint8_t* kind) {
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t base, aend;
+    idx[k] = -1;
+    lkey_out[k] = 0;
+    if (!mr_round(q[2 * k], q[2 * k + 1], &base, &aend)) {
+      kind[k] = 3;
+      continue;
+    }
+    kind[k] = 0;
+    for (uint64_t i = 0; i < n_mr; ++i) {
+      if (start[i] <= base && aend <= end[i]) {
+        idx[k] = (int32_t)i;
+        lkey_out[k] = lkey[i];
+        kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;
+        break;
+      }
+    }
+  }
+}
+
+// For tables sorted by start with no two ranges overlapping: the only range
+// that can contain [base, aend) is the last one starting at or below base.
+void oracle_mr_bsearch(const uint64_t* q, uint64_t n_q, const uint64_t* start,
+                       const uint64_t* end, const uint32_t* lkey, uint64_t n_mr,
+                       int32_t* idx, uint32_t* lkey_out, uint8_t* kind) {
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t base, aend;
+    idx[k] = -1;
+    lkey_out[k] = 0;
+    if (!mr_round(q[2 * k], q[2 * k + 1], &base, &aend)) {
+      kind[k] = 3;
+      continue;
+    }
+    kind[k] = 0;
+    const uint64_t* it = std::upper_bound(start, start + n_mr, base);
+    if (it == start) continue;
+    uint64_t j = (uint64_t)(it - start) - 1;
+    if (aend <= end[j]) {
+      idx[k] = (int32_t)j;
+      lkey_out[k] = lkey[j];
+      kind[k] = (start[j] == base && end[j] == aend) ? 1 : 2;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Put translation and stable bucketing into per-queue WQE rings.
+//
+// Request word 0 = heap offset, word 1 = bytes | pe << 32 | qp << 48.
+// A request is valid when pe < world, qp < n_qp, bytes >= 1 and
+// offset + bytes <= heap_size. Valid requests go to ring r = pe * n_qp + qp
+// (PE-major), in request order; the k-th one of ring r (k from 0) takes
+// sequence number seq = head[r] + k and slot seq mod depth.
+// A ring asked to take more than `depth` entries in one batch overflows: it
+// gets no entry, its head stays, its requests count in ctr[2] and ctr[3]
+// gets bit 2. count[r] is the number of valid requests routed to ring r.
+// ctr = {entries posted, invalid count, overflow count, error bits}.
+//
+// WQE (64 bytes, little-endian): +0 raddr, +8 laddr, +16 u32 len,
+// +20 u32 lkey, +24 u32 rkey, +28 u32 flags (0), +32 u64 seq,
+// +40 u32 request index, +44..63 zero.
+// raddr = peer_ptrs[pe] + offset, rkey = rkeys[pe];
+// laddr = local_base + offset (the source sits at the same symmetric offset
+// in the local heap), lkey = the local object's single lkey.
+
+static void put_u64(uint8_t* p, uint64_t v) { std::memcpy(p, &v, 8); }
+static void put_u32(uint8_t* p, uint32_t v) { std::memcpy(p, &v, 4); }
+
+void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptrs,
+                       const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
+                       uint64_t local_base, uint32_t lkey, uint64_t heap_size,
+                       uint8_t* rings, uint64_t depth, uint64_t* head, uint32_t* count,
+                       uint64_t* ctr) {
+  uint64_t n_rings = (uint64_t)world * n_qp;
+  std::vector<uint64_t> demand(n_rings, 0);
+  std::vector<int> ring_of(n);
+  uint64_t n_invalid = 0;
+  // 1. Validate and count per ring.
+  for (uint64_t i = 0; i < n; ++i) {
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint64_t bytes = w1 & 0xFFFFFFFFull;
+    uint64_t pe = (w1 >> 32) & 0xFFFF;
+    uint64_t qp = (w1 >> 48) & 0xFFFF;
+    bool ok = pe < world && qp < n_qp && bytes >= 1 &&
+              (u128)off + (u128)bytes <= (u128)heap_size;
+    if (!ok) {
+      ring_of[i] = -1;
+      n_invalid += 1;
+      continue;
+    }
+    ring_of[i] = (int)(pe * n_qp + qp);
+    demand[ring_of[i]] += 1;
+  }
+  // 2. Overflowing rings take nothing.
+  uint64_t n_overflow = 0, posted = 0, err = 0;
+  std::vector<bool> full(n_rings, false);
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    if (demand[r] > depth) {
+      full[r] = true;
+      n_overflow += demand[r];
+      err |= 2;
+    }
+  }
+  // 3. Post in request order.
+  std::vector<uint64_t> taken(n_rings, 0);
+  for (uint64_t i = 0; i < n; ++i) {
+    int r = ring_of[i];
+    if (r < 0 || full[r]) continue;
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint32_t bytes = (uint32_t)(w1 & 0xFFFFFFFFull);
+    uint32_t pe = (uint32_t)((w1 >> 32) & 0xFFFF);
+    uint64_t seq = head[r] + taken[r];
+    taken[r] += 1;
+    uint8_t* wqe = rings + ((uint64_t)r * depth + (seq % depth)) * 64;
+    std::memset(wqe, 0, 64);
+    put_u64(wqe + 0, peer_ptrs[pe] + off);
+    put_u64(wqe + 8, local_base + off);
+    put_u32(wqe + 16, bytes);
+    put_u32(wqe + 20, lkey);
+    put_u32(wqe + 24, rkeys[pe]);
+    put_u32(wqe + 28, 0);
+    put_u64(wqe + 32, seq);
+    put_u32(wqe + 40, (uint32_t)i);
+    posted += 1;
+  }
+  // 4. Advance heads of the rings that took their batch.
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    count[r] = (uint32_t)demand[r];
+    if (!full[r]) head[r] += demand[r];
+  }
+  ctr[0] = posted;
+  ctr[1] = n_invalid;
+  ctr[2] = n_overflow;
+  ctr[3] = err;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle.cpp (a dropped term, a wrong
+index, an off-by-one, a transposed operand), builds it on the CPU, and runs
+the oracle pin tests against it in a subprocess: they must fail.
+"""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.cpp")
+
+MUTANTS = [
+    ("prp2 drops the in-chunk offset",
+     "prp[1] = bus_address(lut, n_lut, first_page + kPage);",
+     "prp[1] = lut[(first_page + kPage) / kChunk];"),
+    ("prp1 loses its in-page offset",
+     "prp[0] = bus_address(lut, n_lut, off);",
+     "prp[0] = bus_address(lut, n_lut, first_page);"),
+    ("chain pointer names the current page",
+     "arena_base + (page_base + page + 1) * kPage;",
+     "arena_base + (page_base + page) * kPage;"),
+    ("list page holds 512 data entries before chaining",
+     "left -= kListSlots - 1;", "left -= kListSlots;"),
+    ("page count off by one at the end",
+     "uint64_t last = (off + len - 1) / kPage;", "uint64_t last = (off + len) / kPage;"),
+    ("list used from two pages on",
+     "if (n < 3) return 0;\n  return list_pages_for(n - 1);",
+     "if (n < 2) return 0;\n  return list_pages_for(n - 1);"),
+    ("list entries start at the first page",
+     "bus_address(lut, n_lut, first_page + k * kPage);",
+     "bus_address(lut, n_lut, first_page + (k - 1) * kPage);"),
+    ("mr containment uses a strict end",
+     "if (start[i] <= base && aend <= end[i]) {", "if (start[i] <= base && aend < end[i]) {"),
+    ("mr rounding truncates the end",
+     "uint64_t pages = (uint64_t)((stop - b + kPage - 1) / kPage);",
+     "uint64_t pages = (uint64_t)((stop - b) / kPage);"),
+    ("mr exact compares one end only",
+     "kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;",
+     "kind[k] = (start[i] == base) ? 1 : 2;"),
+    ("mr bsearch takes lower_bound",
+     "std::upper_bound(start, start + n_mr, base);", "std::lower_bound(start, start + n_mr, base);"),
+    ("wqe ring order is qp-major",
+     "ring_of[i] = (int)(pe * n_qp + qp);", "ring_of[i] = (int)(qp * world + pe);"),
+    ("wqe seq ignores the head",
+     "uint64_t seq = head[r] + taken[r];", "uint64_t seq = taken[r];"),
+    ("wqe rkey of the local PE",
+     "put_u32(wqe + 24, rkeys[pe]);", "put_u32(wqe + 24, rkeys[0]);"),
+    ("wqe ring full one early",
+     "if (demand[r] > depth) {", "if (demand[r] >= depth) {"),
+    ("wqe raddr from the local base",
+     "put_u64(wqe + 0, peer_ptrs[pe] + off);", "put_u64(wqe + 0, local_base + off);"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    mutated = tmp_path / "oracle_mutant.cpp"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mutant.so"
+    subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-o", str(lib), str(mutated)],
+                   check=True)
+    env = dict(os.environ, DB_ORACLE_LIB=str(lib))
+    tests = [os.path.join(ROOT, "tests", f) for f in
+             ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py")]
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
