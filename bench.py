@@ -1,0 +1,483 @@
+"""Throughput of batched GPU-range -> DMA-descriptor translation on one GB300.
+
+One step runs every part of the hot path once, each on its full-size seeded
+synthetic workload, all on one CUDA stream:
+
+  prp_small   db_prp_build, 1,048,576 small requests (1 GiB heap)
+  prp_large   db_prp_build, 4,194,304 requests, chained lists (16 GiB heap)
+  mr_lookup   db_mr_lookup, 16,777,216 queries over 1,048,576 records
+  put_bucket  db_wqe_bucket, 8,388,608 puts into 32 rings of 2^19 WQEs
+
+``value`` is requests translated per second over the whole step (all four
+batches), with inputs resident in HBM. Each kernel call is also timed alone
+with CUDA events on the launch stream; the dominant one (prp_large) gives the
+roofline line. ``e2e`` repeats the step through the same API with inputs in
+pinned host memory and every descriptor copied back to the host.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica (the batches are independent);
+the step time is the maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "M requests/s translated + achieved HBM GB/s as % of GB300 peak"
+UNIT = "M requests/s"
+WORKLOAD = "descriptor batch: prp_small + prp_large + mr_lookup + put_bucket (full sizes)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- inputs
+def make_inputs():
+    import synth
+    return dict(prp_small=synth.prp_small(), prp_large=synth.prp_large(),
+                mr_lookup=synth.mr_lookup(), put_bucket=synth.put_bucket())
+
+
+def list_words(req: np.ndarray) -> int:
+    """8-byte words a PRP batch writes into list pages (data entries plus
+    chain pointers), counted from the requests -- measurement bookkeeping."""
+    off = req[:, 0]
+    ln = req[:, 1] & np.uint64(0xFFFFFFFF)
+    n = ((off & np.uint64(4095)) + ln + np.uint64(4095)) >> np.uint64(12)
+    n = n[n >= 3].astype(np.int64)
+    entries = n - 1
+    pages = -(-(entries - 1) // 511)
+    return int((entries + pages - 1).sum())
+
+
+def algorithmic_bytes(inp) -> dict:
+    """Bytes each call must move at minimum (read inputs once, write outputs once)."""
+    s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
+    return {
+        "prp_small": 32 * s["req"].shape[0] + 8 * list_words(s["req"]) + 8 * s["lut"].shape[0],
+        "prp_large": 32 * l["req"].shape[0] + 8 * list_words(l["req"]) + 8 * l["lut"].shape[0],
+        "mr_lookup": 25 * m["queries"].shape[0] + 20 * m["mr_start"].shape[0],
+        "put_bucket": 80 * p["req"].shape[0],
+    }
+
+
+def units(inp) -> dict:
+    return {"prp_small": inp["prp_small"]["req"].shape[0],
+            "prp_large": inp["prp_large"]["req"].shape[0],
+            "mr_lookup": inp["mr_lookup"]["queries"].shape[0],
+            "put_bucket": inp["put_bucket"]["req"].shape[0]}
+
+
+def peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel_src: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        src = open(os.path.join(ROOT, "descriptor_build_gb300", "csrc", kernel_src), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# -------------------------------------------------------------- clock sampler
+class Clocks:
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9:
+                self.rows.append(parts)
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4)
+                          if r[5 + k].lower() == "active"})
+        load = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def smi_index(device) -> int:
+    """nvidia-smi's index of a CUDA device (honours CUDA_VISIBLE_DEVICES)."""
+    local = device.index or 0
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",")]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+# ----------------------------------------------------------------- our arm
+class Step:
+    """Device buffers for one replica and the calls of one step."""
+
+    def __init__(self, db, torch, inp, device):
+        self.db, self.torch, self.inp = db, torch, inp
+        t = torch
+        d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+        d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+        self.d64, self.d32 = d64, d32
+        s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
+        self.small = dict(req=d64(s["req"]), lut=d64(s["lut"]), heap=s["heap_size"],
+                          base=s["arena_base"], cap=1, arena=t.zeros((1, 512), dtype=t.int64,
+                                                                   device=device),
+                          prp=t.empty((s["req"].shape[0], 2), dtype=t.int64, device=device),
+                          ctr=t.zeros(4, dtype=t.int64, device=device),
+                          ws=db.workspace(db.prp_workspace_size(s["req"].shape[0]), device))
+        self.large = dict(req=d64(l["req"]), lut=d64(l["lut"]), heap=l["heap_size"],
+                          base=l["arena_base"], cap=0, arena=None,
+                          prp=t.empty((l["req"].shape[0], 2), dtype=t.int64, device=device),
+                          ctr=t.zeros(4, dtype=t.int64, device=device),
+                          ws=db.workspace(db.prp_workspace_size(l["req"].shape[0]), device))
+        # Size the list arena the way a caller would: a call with no arena
+        # reports, in its counters, the list pages the batch needs.
+        self.prp(self.large, t.cuda.current_stream(device))
+        t.cuda.synchronize(device)
+        cap = int(self.large["ctr"][0].item())
+        self.large["cap"] = cap
+        self.large["arena"] = t.empty((cap, 512), dtype=t.int64, device=device)
+        nq = m["queries"].shape[0]
+        self.mr = dict(q=d64(m["queries"]), start=d64(m["mr_start"]), end=d64(m["mr_end"]),
+                       lkey=d32(m["mr_lkey"]),
+                       idx=t.empty(nq, dtype=t.int32, device=device),
+                       olkey=t.empty(nq, dtype=t.int32, device=device),
+                       kind=t.empty(nq, dtype=t.uint8, device=device),
+                       ctr=t.zeros(4, dtype=t.int64, device=device),
+                       ws=db.workspace(db.mr_workspace_size(m["mr_start"].shape[0]), device))
+        R = p["world"] * p["n_qp"]
+        self.put = dict(req=d64(p["req"]), peer=d64(p["peer_ptrs"]), rkeys=d32(p["rkeys"]),
+                        rings=t.empty((R, p["depth"], 64), dtype=t.uint8, device=device),
+                        head=d64(p["head"]), count=t.empty(R, dtype=t.int32, device=device),
+                        ctr=t.zeros(4, dtype=t.int64, device=device),
+                        ws=db.workspace(db.wqe_workspace_size(p["req"].shape[0], R), device))
+
+    def prp(self, a, stream):
+        self.db.prp_build(a["req"], a["lut"], a["heap"], a["base"], a["cap"], a["arena"],
+                          a["prp"], a["ws"], ctr=a["ctr"], stream=stream)
+
+    def mr_call(self, stream):
+        m = self.mr
+        self.db.mr_lookup(m["q"], m["start"], m["end"], m["lkey"], m["idx"], m["olkey"],
+                          m["kind"], m["ws"], ctr=m["ctr"], stream=stream)
+
+    def put_call(self, stream):
+        p, P = self.put, self.inp["put_bucket"]
+        self.db.wqe_bucket(p["req"], p["peer"], p["rkeys"], P["world"], P["n_qp"],
+                           P["local_base"], P["lkey"], P["heap_size"], p["rings"], P["depth"],
+                           p["head"], p["count"], p["ws"], ctr=p["ctr"], stream=stream)
+
+    def calls(self):
+        return [("prp_small", lambda s: self.prp(self.small, s)),
+                ("prp_large", lambda s: self.prp(self.large, s)),
+                ("mr_lookup", self.mr_call),
+                ("put_bucket", self.put_call)]
+
+    LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 2}
+
+    def check_counters(self):
+        t = self.torch
+        for name, c in (("prp_small", self.small["ctr"]), ("prp_large", self.large["ctr"]),
+                        ("mr_lookup", self.mr["ctr"]), ("put_bucket", self.put["ctr"])):
+            err = int(c[3].item())
+            if err:
+                raise RuntimeError(f"{name}: device error bits {err}")
+        assert int(self.large["ctr"][2].item()) == 0, "arena overflow in the benchmark"
+
+
+def run_ours(args, inp, world, device, dist):
+    import torch
+    import descriptor_build_gb300 as db
+
+    torch.cuda.set_device(device)
+    st = Step(db, torch, inp, device)
+    stream = torch.cuda.Stream(device=device)
+    calls = st.calls()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    for _ in range(args.warmup):
+        for _, fn in calls:
+            fn(stream)
+    torch.cuda.synchronize(device)
+    st.check_counters()
+
+    K = args.steps
+    evs = [[(ev(), ev()) for _ in calls] for _ in range(K)]
+    step_ev = [(ev(), ev()) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    with Clocks(smi_index(device)) as clk:
+        t0 = ev()
+        t1 = ev()
+        t0.record(stream)
+        for k in range(K):
+            step_ev[k][0].record(stream)
+            for j, (_, fn) in enumerate(calls):
+                evs[k][j][0].record(stream)
+                fn(stream)
+                evs[k][j][1].record(stream)
+            step_ev[k][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+    total_ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([total_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+        dist.barrier()
+    st.check_counters()
+    per_kernel_ms = {name: statistics.mean(evs[k][j][0].elapsed_time(evs[k][j][1])
+                                           for k in range(K))
+                     for j, (name, _) in enumerate(calls)}
+
+    u = units(inp)
+    alg = algorithmic_bytes(inp)
+    peak, peak_kind = peak_gbs()
+    reqs_per_step = sum(u.values())
+    ms_per_step = total_ms / K
+    value = world * reqs_per_step / (ms_per_step * 1e-3) / 1e6
+    kernels = {}
+    for name in u:
+        ms = per_kernel_ms[name]
+        gbs = alg[name] / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": round(ms, 4), "M_req_per_s": round(u[name] / ms / 1e3, 2),
+                         "algorithmic_bytes": alg[name], "GB_per_s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4), "launches": Step.LAUNCHES[name]}
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    traffic = recorded_traffic("prp_build.cu", "prp_build_kernel") if dom.startswith("prp") \
+        else None
+    roof = {"bound": "hbm", "kernel": "prp_build_kernel" if dom.startswith("prp") else dom,
+            "workload": dom, "achieved": kernels[dom]["GB_per_s"], "peak": peak,
+            "peak_source": peak_kind, "unit": "GB/s",
+            "frac": round(kernels[dom]["GB_per_s"] / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg[dom]}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+           "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+           "data": "synthetic (seeded generators of the five study workloads)",
+           "config": {"workload": WORKLOAD, "requests_per_step": reqs_per_step,
+                      "per_workload_requests": u,
+                      "l2": "inputs larger than L2: each step streams ~6 GB, so every "
+                            "kernel's inputs are evicted before its next launch",
+                      "parallelism": f"replicas x{world}"},
+           "kernels": kernels, "roofline": roof,
+           "gpu_launches": K * sum(Step.LAUNCHES.values()),
+           "clocks": clk.summary()}
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world)
+    return out
+
+
+def run_e2e(st, stream, inp, K, device, dist, world):
+    """The same step through the API with host buffers: pinned host inputs are
+    copied in, every descriptor the step produces is copied back out."""
+    import torch
+    t = torch
+    pin = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).pin_memory()
+    pin32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).pin_memory()
+    s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
+    h_in = [(pin(s["req"]), st.small["req"]), (pin(s["lut"]), st.small["lut"]),
+            (pin(l["req"]), st.large["req"]), (pin(l["lut"]), st.large["lut"]),
+            (pin(m["queries"]), st.mr["q"]), (pin(m["mr_start"]), st.mr["start"]),
+            (pin(m["mr_end"]), st.mr["end"]), (pin32(m["mr_lkey"]), st.mr["lkey"]),
+            (pin(p["req"]), st.put["req"]), (pin(p["peer_ptrs"]), st.put["peer"]),
+            (pin32(p["rkeys"]), st.put["rkeys"])]
+    used = st.large["cap"]
+    outs = [st.small["prp"], st.large["prp"], st.large["arena"][:used], st.mr["idx"],
+            st.mr["olkey"], st.mr["kind"], st.put["rings"], st.put["head"], st.put["count"],
+            st.small["ctr"], st.large["ctr"], st.mr["ctr"], st.put["ctr"]]
+    h_out = [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    bi = sum(h.numel() * h.element_size() for h, _ in h_in)
+    bo = sum(o.numel() * o.element_size() for o in outs)
+    calls = st.calls()
+
+    def one():
+        with t.cuda.stream(stream):
+            for h, d in h_in:
+                d.copy_(h, non_blocking=True)
+            for _, fn in calls:
+                fn(stream)
+            for o, h in zip(outs, h_out):
+                h.copy_(o, non_blocking=True)
+
+    one()
+    t.cuda.synchronize(device)
+    if dist:
+        dist.barrier()
+    a, b = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        one()
+    b.record(stream)
+    t.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / K
+    if dist:
+        tt = t.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    reqs = sum(units(inp).values())
+    return {"value": round(world * reqs / (ms * 1e-3) / 1e6, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "steps": K, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo}
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_baseline(inp, scale: int = 1) -> dict:
+    """The oracle as it stands (single-threaded C++) on a bounded sample of
+    each workload; value in the same unit, scaled by the sample sizes.
+    ``scale`` divides the sample sizes."""
+    import oracle
+    s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
+    samples = {"prp_small": 262_144 // scale, "prp_large": 65_536 // scale,
+               "mr_lookup": 1_048_576 // scale, "put_bucket": 1_048_576 // scale}
+    secs = {}
+    t = time.perf_counter()
+    oracle.prp_build(s["req"][:samples["prp_small"]], s["lut"], s["heap_size"],
+                     s["arena_base"], 1, lists=False)
+    secs["prp_small"] = time.perf_counter() - t
+    req = l["req"][:samples["prp_large"]]
+    need = oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], 1 << 40,
+                            lists=False)
+    t = time.perf_counter()
+    oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], int(need["ctr"][0]))
+    secs["prp_large"] = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.mr_bsearch(m["queries"][:samples["mr_lookup"]], m["mr_start"], m["mr_end"],
+                      m["mr_lkey"])
+    secs["mr_lookup"] = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.wqe_bucket(p["req"][:samples["put_bucket"]], p["peer_ptrs"], p["rkeys"], p["world"],
+                      p["n_qp"], p["local_base"], p["lkey"], p["heap_size"], p["depth"],
+                      p["head"])
+    secs["put_bucket"] = time.perf_counter() - t
+    # Time for one full step's requests at the sampled per-request rates.
+    u = units(inp)
+    step_s = sum(secs[k] * u[k] / samples[k] for k in u)
+    return {"value": round(sum(u.values()) / step_s / 1e6, 3), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": "first %d prp_small, %d prp_large (lists written), %d mr_lookup "
+                      "(binary-search oracle), %d put_bucket requests; per-workload rates "
+                      "scaled to one full step" % tuple(samples[k] for k in u),
+            "seconds": {k: round(v, 3) for k, v in secs.items()}}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The oracle as the reference arm: each step a bounded sample of the
+    workload on the host cores, same metric and unit as our arm."""
+    inp = make_inputs()
+    for _ in range(args.warmup):
+        cpu_baseline(inp, scale=8)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(inp, scale=8))
+    wall = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    reqs = sum(units(inp).values())
+    ms = reqs / (v * 1e6) * 1e3
+    cb = dict(vals[0])
+    cb["value"] = v
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+            "data": "synthetic (seeded generators of the five study workloads)",
+            "config": {"workload": WORKLOAD, "requests_per_step": reqs},
+            "cpu_baseline": cb, "wall_s": round(wall, 2),
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(device)
+        dist.init_process_group("nccl", device_id=device)
+    inp = make_inputs()
+    out = run_ours(args, inp, world, device, dist)
+    if rank == 0:
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(inp)
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

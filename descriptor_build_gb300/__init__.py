@@ -1,0 +1,172 @@
+"""Python binding of libdescbuild.so: batched GPU-range -> DMA-descriptor translation.
+
+The functions here have the names of the C ABI in ``include/descbuild.h``
+(without the ``db_`` prefix) and only marshal arguments: torch CUDA tensors
+become device pointers, the stream becomes a ``cudaStream_t``, and a negative
+return code becomes a ``DescBuildError``. Every step of the computation runs
+in the library's CUDA kernels; there is no fallback. Importing this package
+fails loudly when the library has not been built.
+
+Record layouts (all tensors contiguous, on the GPU):
+  PRP request  16 B  {u64 off; u32 len; u32 rsvd}     -> int64 [n, 2]
+  PRP output   16 B  {u64 prp1; u64 prp2}             -> int64 [n, 2]
+  range        16 B  {u64 addr; u64 size}             -> int64 [n, 2]
+  put          16 B  {u64 off; u32 bytes; u16 pe; u16 qp} -> int64 [n, 2]
+  WQE          64 B                                    -> uint8 [rings, depth, 64]
+  counters     32 B  {total, n_invalid, n_overflow, err} -> int64 [4]
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
+    "mr_workspace_size", "mr_lookup", "wqe_workspace_size", "wqe_bucket", "strerror",
+    "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
+    "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
+]
+
+PRP_OK, PRP_INVALID, PRP_OVERFLOW = 0, 1, 2
+MR_MISS, MR_EXACT, MR_CONTAINED, MR_INVALID = 0, 1, 2, 3
+ERR_TIMEOUT, ERR_RING_OVERFLOW, ERR_TABLE_ORDER = 1, 2, 4
+PRP_ZERO_TAIL = 1
+
+lib_path = _build.LIB
+
+
+class DescBuildError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = _lib.db_strerror(code).decode()
+        if code == -5:
+            msg += f" (cudaError {_lib.db_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [{code}]")
+
+
+def _load():
+    if not os.path.exists(lib_path):
+        raise ImportError(
+            f"{lib_path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+            f"g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(lib_path)
+    vp, u64, u32, i32, sz = (ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int,
+                             ctypes.c_size_t)
+    psz = ctypes.POINTER(ctypes.c_size_t)
+    lib.db_prp_workspace_size.argtypes = [u64, psz]
+    lib.db_prp_build.argtypes = [vp, u64, vp, u64, u64, u64, vp, vp, vp, vp, vp, u32, vp, sz, vp]
+    lib.db_mr_workspace_size.argtypes = [u64, psz]
+    lib.db_mr_lookup.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp, vp, vp, sz, vp]
+    lib.db_wqe_workspace_size.argtypes = [u64, u32, psz]
+    lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
+                                  vp, sz, vp]
+    for name in ("db_prp_workspace_size", "db_prp_build", "db_mr_workspace_size",
+                 "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket",
+                 "db_last_cuda_error"):
+        getattr(lib, name).restype = i32
+    lib.db_strerror.argtypes = [i32]
+    lib.db_strerror.restype = ctypes.c_char_p
+    lib.db_last_cuda_error.argtypes = []
+    return lib
+
+
+_lib = _load()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise DescBuildError(fn, rc)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdescbuild must be contiguous")
+    return t.data_ptr()
+
+
+def _records(t: torch.Tensor, size: int) -> int:
+    nbytes = t.numel() * t.element_size()
+    if nbytes % size:
+        raise ValueError(f"buffer of {nbytes} bytes is not a whole number of {size}-byte records")
+    return nbytes // size
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _size(fn, *args) -> int:
+    out = ctypes.c_size_t(0)
+    _check(fn.__name__, fn(*args, ctypes.byref(out)))
+    return out.value
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace of ``nbytes`` (256-byte aligned by torch)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def strerror(code: int) -> str:
+    return _lib.db_strerror(code).decode()
+
+
+# ------------------------------------------------------------------ PRP build
+def prp_workspace_size(n: int) -> int:
+    return _size(_lib.db_prp_workspace_size, n)
+
+
+def prp_build(req: torch.Tensor, lut: torch.Tensor, heap_size: int, arena_base: int,
+              arena_cap_pages: int, arena: torch.Tensor | None, prp: torch.Tensor,
+              ws: torch.Tensor, page_base: torch.Tensor | None = None,
+              status: torch.Tensor | None = None, ctr: torch.Tensor | None = None,
+              flags: int = 0, stream=None) -> None:
+    """db_prp_build: PRP1/PRP2 per request and the chained list pages in ``arena``."""
+    n = _records(req, 16)
+    _check("db_prp_build", _lib.db_prp_build(
+        _ptr(req), n, _ptr(lut), heap_size, arena_base, arena_cap_pages, _ptr(arena), _ptr(prp),
+        _ptr(page_base), _ptr(status), _ptr(ctr), flags, _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ MR lookup
+def mr_workspace_size(n_mr: int) -> int:
+    return _size(_lib.db_mr_workspace_size, n_mr)
+
+
+def mr_lookup(q: torch.Tensor, mr_start: torch.Tensor, mr_end: torch.Tensor,
+              mr_lkey: torch.Tensor, idx: torch.Tensor, lkey: torch.Tensor, kind: torch.Tensor,
+              ws: torch.Tensor, ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_mr_lookup: classify each range against a sorted registration table."""
+    n_q = _records(q, 16)
+    n_mr = _records(mr_start, 8)
+    _check("db_mr_lookup", _lib.db_mr_lookup(
+        _ptr(q), n_q, _ptr(mr_start), _ptr(mr_end), _ptr(mr_lkey), n_mr, _ptr(idx), _ptr(lkey),
+        _ptr(kind), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# --------------------------------------------------------------- WQE bucketing
+def wqe_workspace_size(n: int, n_rings: int) -> int:
+    return _size(_lib.db_wqe_workspace_size, n, n_rings)
+
+
+def wqe_bucket(req: torch.Tensor, peer_ptrs: torch.Tensor, rkeys: torch.Tensor, world: int,
+               n_qp: int, local_base: int, lkey: int, heap_size: int, rings: torch.Tensor,
+               depth: int, head: torch.Tensor, count: torch.Tensor, ws: torch.Tensor,
+               ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_wqe_bucket: translate puts and stable-partition them into WQE rings."""
+    n = _records(req, 16)
+    _check("db_wqe_bucket", _lib.db_wqe_bucket(
+        _ptr(req), n, _ptr(peer_ptrs), _ptr(rkeys), world, n_qp, local_base, lkey, heap_size,
+        _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(ctr), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))

@@ -1,0 +1,458 @@
+// Symmetric-heap put translation and stable bucketing into WQE rings (sm_103a).
+//
+// Source: "mori communication library analysis (1)". Static-heap put:
+// raddr = peerPtrs[pe] + offset, rkey = peerRkeys[pe], lkey of the source
+// object, one WQE for the whole transfer. Warp-level slot reservation: each
+// entry takes the next post index of its send queue, which here is
+// head[ring] + (valid puts of the same ring earlier in the batch).
+//
+// A ring asked for more than `depth` entries takes none of the batch, so the
+// per-ring totals must be known before any entry is written. Two launches:
+//   count    (persistent, tickets) per tile of 1024 puts: a shared-memory
+//            histogram over the rings (+1 bin for invalid puts), published
+//            as one status word per (tile, ring) and scanned across tiles by
+//            a decoupled lookback, one ring per thread. Each word ends as the
+//            tile's inclusive prefix, which is the next tile's exclusive one.
+//            The CTA of the last tile sees the totals: it writes count[],
+//            decides which rings overflow and advances head[] (old heads are
+//            kept in the workspace).
+//   scatter  per tile: stable rank of each put inside its warp with
+//            __match_any_sync, then across the tile's 32 warp-rows; WQEs are
+//            built into shared memory in ring order and each ring's run is
+//            written out contiguously with 16-byte stores.
+#include "common.cuh"
+
+namespace db {
+namespace wqe {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kItems = 2;
+constexpr int kTile = kThreads * kItems;  // 1024 puts per tile
+constexpr int kUnits = kItems * kWarps;   // warp-rows of 32 puts, in batch order
+constexpr uint32_t kMaxRings = 1024;
+
+// Workspace: ScanHeader (acc[0] posted, acc[1] invalid, acc[2] overflow;
+// aux = count pass failed), old heads [1024] u64, overflow flags [1024] u32,
+// then the status words [tiles][R + 1].
+constexpr size_t kHeadOldOff = kScanHeaderBytes;
+constexpr size_t kFullOff = kHeadOldOff + 8 * kMaxRings;
+constexpr size_t kStatusOff = kFullOff + 4 * kMaxRings;
+inline uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
+inline size_t ws_bytes_for(uint64_t n, uint32_t R) {
+  return kStatusOff + ((tiles_for(n) * ((uint64_t)R + 1) * 8 + 255) & ~(uint64_t)255);
+}
+
+struct Params {
+  const ulonglong2* req;
+  uint64_t n;
+  uint64_t n_tiles;
+  const uint64_t* peer_ptrs;
+  const uint32_t* rkeys;
+  uint32_t world, n_qp, R, V;
+  uint64_t local_base;
+  uint32_t lkey;
+  uint64_t heap_size;
+  unsigned char* rings;
+  uint64_t depth;
+  uint64_t* head;
+  uint32_t* count;
+  db_counters* ctr;
+  ScanHeader* hdr;
+  uint64_t* head_old;
+  uint32_t* full;
+  unsigned long long* status;  // [cap_words]
+  uint64_t cap_words;
+};
+
+// Ring of a put, or R for an invalid one.
+__device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) {
+  const uint64_t off = r.x;
+  const uint32_t bytes = (uint32_t)r.y;
+  const uint32_t pe = (uint32_t)(r.y >> 32) & 0xFFFFu;
+  const uint32_t qp = (uint32_t)(r.y >> 48);
+  const bool ok = pe < p.world && qp < p.n_qp && bytes != 0 && off <= p.heap_size &&
+                  (uint64_t)bytes <= p.heap_size - off;
+  return ok ? pe * p.n_qp + qp : p.R;
+}
+
+__device__ __forceinline__ uint64_t block_sum64(uint64_t v, uint64_t* s_red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum64(v);
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  uint64_t t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += s_red[w];
+  __syncthreads();
+  return t;
+}
+
+// ---------------------------------------------------------------- count pass
+__global__ void __launch_bounds__(kThreads, 2) wqe_count_kernel(const Params p) {
+  extern __shared__ uint32_t s_hist[];  // [V]
+  __shared__ unsigned long long s_ticket;
+  __shared__ int s_failed;
+  __shared__ int s_last;
+  __shared__ uint64_t s_red[kWarps];
+
+  const uint64_t pol_first = policy_evict_first();
+  const uint32_t epoch = *(volatile unsigned int*)&p.hdr->epoch;
+  const uint32_t V = p.V;
+  bool any_failed = false;
+
+  for (;;) {
+    if (threadIdx.x == 0) {
+      s_ticket = atomicAdd(&p.hdr->ticket, 1ull);
+      s_failed = 0;
+    }
+    for (uint32_t v = threadIdx.x; v < V; v += kThreads) s_hist[v] = 0;
+    __syncthreads();
+    const uint64_t tile = s_ticket;
+    if (tile >= p.n_tiles) break;
+
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      if (i < p.n) atomicAdd(&s_hist[bin_of(p, ld_stream16(p.req + i, pol_first))], 1u);
+    }
+    __syncthreads();
+
+    // Publish every aggregate before waiting on any predecessor.
+    unsigned long long* row = p.status + tile * V;
+    for (uint32_t v = threadIdx.x; v < V; v += kThreads)
+      st_release(row + v, status_word(tile == 0 ? kPrefix : kAggregate, epoch, s_hist[v]));
+    for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
+      const uint64_t agg = s_hist[v];
+      uint64_t excl = 0;
+      if (tile != 0) {
+        bool failed = false;
+        int64_t pos = (int64_t)tile - 1;
+        Backoff backoff;
+        while (pos >= 0) {
+          const uint64_t w = ld_acquire(p.status + (uint64_t)pos * V + v);
+          const uint32_t f = status_flag(w, epoch);
+          if (f == kEmpty) {
+            if (!backoff.wait()) {
+              failed = true;
+              break;
+            }
+            continue;
+          }
+          if (f == kFailed) {
+            failed = true;
+            break;
+          }
+          excl += w & kValueMask;
+          if (f == kPrefix) break;
+          --pos;
+        }
+        st_release(row + v, failed ? status_word(kFailed, epoch, 0)
+                                   : status_word(kPrefix, epoch, excl + agg));
+        if (failed) s_failed = 1;
+      }
+      if (tile + 1 == p.n_tiles) s_hist[v] = (uint32_t)(excl + agg);  // batch totals
+    }
+    __syncthreads();
+    const bool failed = s_failed != 0;
+    any_failed |= failed;
+
+    if (tile + 1 == p.n_tiles) {
+      // Totals are known: counts, overflow decision, heads.
+      uint64_t posted = 0, overflow = 0;
+      for (uint32_t r = threadIdx.x; r < p.R; r += kThreads) {
+        const uint64_t tot = s_hist[r];
+        const uint64_t h = p.head[r];
+        const bool over = tot > p.depth;
+        const bool skip = over || failed;
+        p.count[r] = (uint32_t)tot;
+        p.head_old[r] = h;
+        p.full[r] = skip ? 1u : 0u;
+        if (!skip) p.head[r] = h + tot;
+        posted += skip ? 0 : tot;
+        overflow += over ? tot : 0;
+      }
+      posted = block_sum64(posted, s_red);
+      overflow = block_sum64(overflow, s_red);
+      if (threadIdx.x == 0) {
+        p.hdr->acc[0] = posted;
+        p.hdr->acc[1] = s_hist[p.R];
+        p.hdr->acc[2] = overflow;
+        if (overflow) atomicOr(&p.hdr->err, DB_ERR_RING_OVERFLOW);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (threadIdx.x == 0) {
+    if (any_failed) atomicOr(&p.hdr->err, DB_ERR_TIMEOUT);
+    __threadfence();
+    s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    if (threadIdx.x == 0) {
+      const unsigned int err = atomicExch(&p.hdr->err, 0u);
+      const unsigned long long posted = atomicExch(&p.hdr->acc[0], 0ull);
+      const unsigned long long invalid = atomicExch(&p.hdr->acc[1], 0ull);
+      const unsigned long long overflow = atomicExch(&p.hdr->acc[2], 0ull);
+      p.hdr->aux = (err & DB_ERR_TIMEOUT) ? kAuxFailed : 0u;
+      if (p.ctr) {
+        p.ctr->total = (err & DB_ERR_TIMEOUT) ? 0 : posted;
+        p.ctr->n_invalid = invalid;
+        p.ctr->n_overflow = overflow;
+        p.ctr->err = err;
+      }
+    }
+    end_of_call(p.hdr, p.status, p.n_tiles * V, p.cap_words, false);
+  }
+}
+
+// -------------------------------------------------------------- scatter pass
+inline size_t scatter_smem(uint32_t V) {
+  size_t b = (size_t)kTile * 64;    // staged WQEs
+  b += (size_t)kTile * 8;           // destination of each staged WQE
+  b += (size_t)V * 8;               // old heads
+  b += (size_t)V * 4 * 4;           // run start, tile count, tile prefix, full flag
+  b += (size_t)kUnits * V * 2;      // per warp-row counts
+  return (b + 15) & ~(size_t)15;
+}
+
+// The exclusive prefix of (tile, v) is the inclusive prefix the count pass
+// left in the status word of (tile - 1, v).
+__device__ __forceinline__ uint32_t tile_prefix(const Params& p, uint64_t tile, uint32_t v) {
+  if (tile == 0) return 0;
+  return (uint32_t)(p.status[(tile - 1) * p.V + v] & kValueMask);
+}
+
+// One tile: rank, stage in ring order, write out.
+__device__ __forceinline__ void scatter_tile(const Params& p, unsigned char* smem,
+                                             uint32_t* s_scan) {
+  const uint32_t V = p.V, R = p.R;
+  ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);
+  uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 64);
+  uint64_t* s_head = s_dst + kTile;
+  uint32_t* s_run = reinterpret_cast<uint32_t*>(s_head + V);
+  uint32_t* s_tot = s_run + V;
+  uint32_t* s_pre = s_tot + V;
+  uint32_t* s_full = s_pre + V;
+  uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_full + V);
+  const int warp = threadIdx.x >> 5;
+  const uint64_t tile = blockIdx.x;
+  const uint64_t pol_first = policy_evict_first();
+
+  for (uint32_t x = threadIdx.x; x < kUnits * V; x += kThreads) s_cnt[x] = 0;
+  for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
+    s_pre[v] = tile_prefix(p, tile, v);
+    if (v < R) {
+      s_head[v] = p.head_old[v];
+      s_full[v] = p.full[v];
+    }
+  }
+  ulonglong2 r[kItems];
+  uint32_t bin[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+    r[k] = make_ulonglong2(0, 0);
+    bin[k] = V;  // outside the tile: no bin
+    if (i < p.n) {
+      r[k] = ld_stream16(p.req + i, pol_first);
+      bin[k] = bin_of(p, r[k]);
+    }
+  }
+  __syncthreads();
+
+  // Rank inside each warp-row (stable: lower lanes are earlier puts).
+  uint32_t lrank[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint32_t peers = __match_any_sync(kFull, bin[k]);
+    const uint32_t before = peers & lanemask_lt();
+    lrank[k] = __popc(before);
+    if (bin[k] < V && before == 0) s_cnt[(k * kWarps + warp) * V + bin[k]] = (uint16_t)__popc(peers);
+  }
+  __syncthreads();
+  // Across warp-rows, in batch order.
+  for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
+    uint32_t run = 0;
+    for (int u = 0; u < kUnits; ++u) {
+      const uint32_t c = s_cnt[u * V + v];
+      s_cnt[u * V + v] = (uint16_t)run;
+      run += c;
+    }
+    s_tot[v] = run;
+  }
+  __syncthreads();
+  // Where each ring's run starts in the staging buffer (ring order; the
+  // invalid bin is left out). Thread t owns a chunk of consecutive rings.
+  const uint32_t chunk = (R + kThreads - 1) / kThreads;
+  const uint32_t r0 = threadIdx.x * chunk;
+  uint32_t mine = 0;
+  for (uint32_t v = r0; v < r0 + chunk && v < R; ++v) mine += s_tot[v];
+  uint32_t excl, n_staged;
+  block_excl_scan<kWarps>(mine, excl, n_staged, s_scan);
+  for (uint32_t v = r0; v < r0 + chunk && v < R; ++v) {
+    s_run[v] = excl;
+    excl += s_tot[v];
+  }
+  __syncthreads();
+
+  // Build the WQEs in ring order.
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint32_t v = bin[k];
+    if (v >= R) continue;
+    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+    const uint32_t local = s_cnt[(k * kWarps + warp) * V + v] + lrank[k];
+    const uint32_t pos = s_run[v] + local;
+    const uint64_t seq = s_head[v] + s_pre[v] + local;
+    const uint64_t off = r[k].x;
+    const uint32_t bytes = (uint32_t)r[k].y;
+    const uint32_t pe = (uint32_t)(r[k].y >> 32) & 0xFFFFu;
+    const uint64_t raddr = __ldg(p.peer_ptrs + pe) + off;
+    const uint32_t rkey = __ldg(p.rkeys + pe);
+    s_stage[pos * 4 + 0] = make_ulonglong2(raddr, p.local_base + off);
+    s_stage[pos * 4 + 1] = make_ulonglong2((uint64_t)bytes | ((uint64_t)p.lkey << 32), (uint64_t)rkey);
+    s_stage[pos * 4 + 2] = make_ulonglong2(seq, (uint64_t)(uint32_t)i);
+    s_stage[pos * 4 + 3] = make_ulonglong2(0, 0);
+    s_dst[pos] = s_full[v] ? 0ull
+                           : (uint64_t)(p.rings + (((uint64_t)v * p.depth + (seq & (p.depth - 1))) << 6));
+  }
+  __syncthreads();
+
+  // Each ring's run is contiguous in the ring (up to one wrap): 16-byte stores.
+  for (uint32_t f = threadIdx.x; f < n_staged * 4; f += kThreads) {
+    const uint64_t d = s_dst[f >> 2];
+    if (d) {
+      const ulonglong2 x = s_stage[f];
+      st_stream16(reinterpret_cast<void*>(d + (f & 3) * 16), x.x, x.y, pol_first);
+    }
+  }
+}
+
+
+__global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ uint32_t s_scan[kWarps];
+  __shared__ int s_last;
+  if (!(*(volatile unsigned int*)&p.hdr->aux & kAuxFailed)) scatter_tile(p, smem, s_scan);
+
+  // The last CTA performs a status clear that the count pass left pending.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    if (p.hdr->aux & kAuxClearPending) clear_status(p.hdr, p.status, p.cap_words);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      p.hdr->aux &= ~kAuxClearPending;
+      p.hdr->done = 0;
+    }
+    __threadfence();
+  }
+}
+
+int count_grid(uint64_t n_tiles, uint32_t V) {
+  static int per_sm[64][2] = {{0}};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& occ = per_sm[dev & 63][V > 256 ? 1 : 0];
+  if (occ == 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, wqe_count_kernel, kThreads,
+                                                      (size_t)(kMaxRings + 1) * 4) != cudaSuccess ||
+        o < 1)
+      o = 1;
+    occ = o;
+  }
+  const uint64_t g = (uint64_t)num_sms() * (uint64_t)occ;
+  return (int)(n_tiles < g ? n_tiles : g);
+}
+
+// Allow the scatter kernel its largest shared-memory footprint (once per device).
+int prepare_scatter() {
+  static bool done_for[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!done_for[dev & 63]) {
+    if (cudaFuncSetAttribute(wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)scatter_smem(kMaxRings + 1)) != cudaSuccess)
+      return launch_result();
+    done_for[dev & 63] = true;
+  }
+  return 0;
+}
+
+}  // namespace wqe
+}  // namespace db
+
+using namespace db;
+
+extern "C" int db_wqe_workspace_size(uint64_t n, uint32_t n_rings, size_t* bytes) {
+  if (!bytes || n_rings == 0 || n_rings > wqe::kMaxRings || n >= (1ull << 32)) return -EINVAL;
+  *bytes = wqe::ws_bytes_for(n, n_rings);
+  return 0;
+}
+
+extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
+                             const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
+                             uint64_t local_base, uint32_t lkey, uint64_t heap_size,
+                             db_wqe* rings, uint64_t depth, uint64_t* head, uint32_t* count,
+                             db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (world == 0 || n_qp == 0 || (uint64_t)world * n_qp > wqe::kMaxRings) return -EINVAL;
+  if (depth == 0 || (depth & (depth - 1)) != 0) return -EINVAL;
+  if (n >= (1ull << 32)) return -EINVAL;
+  const uint32_t R = world * n_qp;
+  if (!count || !aligned(count, 4)) return -EINVAL;
+  if (ctr && !aligned(ctr, 8)) return -EINVAL;
+  if (n == 0) {
+    cudaMemsetAsync(count, 0, (size_t)R * 4, s);
+    if (ctr) cudaMemsetAsync(ctr, 0, sizeof(db_counters), s);
+    return launch_result();
+  }
+  if (!req || !peer_ptrs || !rkeys || !rings || !head || !ws) return -EINVAL;
+  if (!aligned(req, 16) || !aligned(peer_ptrs, 8) || !aligned(rkeys, 4) || !aligned(rings, 64) ||
+      !aligned(head, 8) || !aligned(ws, 256))
+    return -EINVAL;
+  const uint64_t n_tiles = wqe::tiles_for(n);
+  if (ws_bytes < wqe::ws_bytes_for(n, R)) return -ENOSPC;
+
+  char* w = static_cast<char*>(ws);
+  wqe::Params p;
+  p.req = reinterpret_cast<const ulonglong2*>(req);
+  p.n = n;
+  p.n_tiles = n_tiles;
+  p.peer_ptrs = peer_ptrs;
+  p.rkeys = rkeys;
+  p.world = world;
+  p.n_qp = n_qp;
+  p.R = R;
+  p.V = R + 1;
+  p.local_base = local_base;
+  p.lkey = lkey;
+  p.heap_size = heap_size;
+  p.rings = reinterpret_cast<unsigned char*>(rings);
+  p.depth = depth;
+  p.head = head;
+  p.count = count;
+  p.ctr = ctr;
+  p.hdr = reinterpret_cast<ScanHeader*>(w);
+  p.head_old = reinterpret_cast<uint64_t*>(w + wqe::kHeadOldOff);
+  p.full = reinterpret_cast<uint32_t*>(w + wqe::kFullOff);
+  p.status = reinterpret_cast<unsigned long long*>(w + wqe::kStatusOff);
+  p.cap_words = (ws_bytes - wqe::kStatusOff) / 8;
+
+  int rc = wqe::prepare_scatter();
+  if (rc) return rc;
+  wqe::wqe_count_kernel<<<wqe::count_grid(n_tiles, p.V), wqe::kThreads, (size_t)p.V * 4, s>>>(p);
+  rc = launch_result();
+  if (rc) return rc;
+  wqe::wqe_scatter_kernel<<<(unsigned)n_tiles, wqe::kThreads, wqe::scatter_smem(p.V), s>>>(p);
+  return launch_result();
+}

@@ -1,0 +1,239 @@
+/*
+ * descbuild.h -- batched translation of GPU buffer ranges into DMA descriptors.
+ *
+ * C ABI of libdescbuild.so (CUDA, sm_103a). Three batched operations:
+ *
+ *   db_prp_build   NVMe PRP1/PRP2 and chained 4 KiB PRP lists from heap
+ *                  offsets and a 64 KiB-granular bus-address LUT.
+ *   db_mr_lookup   classify ranges against a sorted registration (MR) table
+ *                  after rounding them to whole 4 KiB pages.
+ *   db_wqe_bucket  translate symmetric-heap puts and stable-partition them
+ *                  into per-queue rings of 64-byte work-queue entries.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every data pointer is a DEVICE pointer (cudaMalloc / torch), owned by the
+ *    caller, unless its comment says "host". The library allocates nothing
+ *    and keeps no state between calls other than what it leaves in the
+ *    caller's workspace.
+ *  - `stream` is a cudaStream_t passed as void*. Work is enqueued on it and the
+ *    call returns without waiting: results are valid once the caller has
+ *    synchronised with that stream. Inputs must stay alive and unchanged
+ *    until then.
+ *  - Return value: 0 on success, or a negative errno:
+ *      -EINVAL  a null or misaligned pointer, or an argument outside its range
+ *      -ENOSPC  the workspace is smaller than *_workspace_size reports
+ *      -EIO     the CUDA launch failed (db_last_cuda_error() gives the code)
+ *    The return covers argument checks and the launch only. Errors that
+ *    depend on the data are reported in device memory (per-request status,
+ *    db_counters) and are read after synchronising.
+ *  - n == 0 is a successful call that only zeroes the counters it would
+ *    otherwise fill.
+ *  - Workspaces: `ws` is device memory of at least *_workspace_size() bytes,
+ *    256-byte aligned, ZERO-FILLED when first allocated. Each call leaves it
+ *    ready for the next one, so it is never cleared again. One workspace
+ *    serves one call at a time: calls sharing a workspace must be ordered on
+ *    one stream.
+ */
+#ifndef DESCBUILD_H
+#define DESCBUILD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- records ------------------------------------------------------------ */
+
+/* One NVMe transfer: `len` bytes at byte offset `off` of the device heap. */
+typedef struct db_prp_req {
+  uint64_t off;
+  uint32_t len;
+  uint32_t rsvd; /* ignored */
+} db_prp_req;    /* 16 bytes */
+
+typedef struct db_prp_out {
+  uint64_t prp1;
+  uint64_t prp2;
+} db_prp_out;    /* 16 bytes */
+
+/* A byte range [addr, addr + size). */
+typedef struct db_range {
+  uint64_t addr;
+  uint64_t size;
+} db_range;      /* 16 bytes */
+
+/* One put: `bytes` bytes at symmetric-heap offset `off` to PE `pe` on its
+ * queue pair `qp`. */
+typedef struct db_put_req {
+  uint64_t off;
+  uint32_t bytes;
+  uint16_t pe;
+  uint16_t qp;
+} db_put_req;    /* 16 bytes */
+
+/* A work-queue entry as written into a ring. */
+typedef struct db_wqe {
+  uint64_t raddr;     /* peer_ptrs[pe] + off               */
+  uint64_t laddr;     /* local_base + off                  */
+  uint32_t len;       /* bytes                             */
+  uint32_t lkey;      /* the local object's lkey           */
+  uint32_t rkey;      /* rkeys[pe]                         */
+  uint32_t flags;     /* 0                                 */
+  uint64_t seq;       /* post index in its ring            */
+  uint32_t req_index; /* position of the put in the batch  */
+  uint32_t rsvd[5];   /* 0                                 */
+} db_wqe;             /* 64 bytes */
+
+/* Batch counters, written by the device at the end of a call. */
+typedef struct db_counters {
+  uint64_t total;      /* prp: list pages the batch needs; wqe: entries posted */
+  uint64_t n_invalid;  /* malformed requests                                  */
+  uint64_t n_overflow; /* prp: lists that did not fit; wqe: puts refused      */
+  uint64_t err;        /* DB_ERR_* bits                                       */
+} db_counters;
+
+/* ---- codes ----------------------------------------------------------------*/
+
+#define DB_PRP_OK 0
+#define DB_PRP_INVALID 1  /* len == 0, off % 4 != 0, or off + len > heap_size */
+#define DB_PRP_OVERFLOW 2 /* the request's list pages would end past the arena */
+
+#define DB_MR_MISS 0
+#define DB_MR_EXACT 1
+#define DB_MR_CONTAINED 2
+#define DB_MR_INVALID 3
+
+#define DB_ERR_TIMEOUT 1u       /* a bounded wait for another CTA ran out; outputs undefined */
+#define DB_ERR_RING_OVERFLOW 2u /* a ring was asked for more than `depth` entries            */
+#define DB_ERR_TABLE_ORDER 4u   /* the MR table is not sorted and non-overlapping            */
+
+#define DB_PRP_ZERO_TAIL 1u     /* db_prp_build: zero the unused slots of each last list page */
+
+/* ---- PRP build ------------------------------------------------------------
+ * Source: xNVMe "uPCIe CUDA" backend page. Introduction: the CUDA driver
+ * exports device memory at 64 KiB granularity; the bus address of each
+ * 64 KiB chunk sits in a LUT indexed by chunk, and PRP entries are built at
+ * 4 KiB from sub-page offsets inside a chunk. "Memory Architecture": PRP
+ * lists live in their own memory region. "Limitations": one 4 KiB list page
+ * holds 512 entries (513 x 4 KiB with PRP1); longer lists chain through the
+ * last slot of each full page (NVMe convention, required by the large
+ * workload). List pages are placed by an exclusive scan of per-request
+ * list-page counts in request order.
+ *
+ * For request i (off, len), n = pages of 4 KiB that [off, off+len) touches,
+ * bus(x) = lut[x >> 16] + (x & 0xFFFF):
+ *   prp1 = bus(off)
+ *   n == 1: prp2 = 0
+ *   n == 2: prp2 = bus(page_floor(off) + 4096)
+ *   n >= 3: prp2 = arena_base + 4096 * page_base[i], and list pages
+ *           page_base[i] .. page_base[i] + L_i - 1 of the arena hold the
+ *           n - 1 entries bus(page_floor(off) + 4096 k), k = 1 .. n-1;
+ *           every page but the last holds 511 entries and, in slot 511,
+ *           the bus address of the next page; the last holds up to 512.
+ *   page_base[i] = sum of L_j over j < i (valid requests only).
+ *
+ * Arguments
+ *   req              [n] requests (16-byte aligned)
+ *   lut              [heap_size / 65536] bus addresses, 64 KiB-aligned, non-zero
+ *   heap_size        bytes of device heap; a multiple of 65536
+ *   arena_base       bus address of list page 0; a multiple of 4096
+ *   arena_cap_pages  pages the arena holds
+ *   arena            [arena_cap_pages][512] uint64: the arena's contents (16-byte aligned).
+ *                    Unused slots are left as they were unless DB_PRP_ZERO_TAIL.
+ *   prp              [n] output (16-byte aligned)
+ *   page_base        [n] output or NULL
+ *   status           [n] output (DB_PRP_*) or NULL
+ *   ctr              output counters or NULL: total list pages (including
+ *                    those of requests that did not fit), n_invalid,
+ *                    n_overflow, err
+ *   flags            0 or DB_PRP_ZERO_TAIL
+ * A request that is invalid or whose list does not fit gets prp = {0, 0}
+ * and writes no list; one that does not fit still advances page_base.
+ * Limits: n <= 2^29.
+ */
+int db_prp_workspace_size(uint64_t n, size_t* bytes);
+int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* lut, uint64_t heap_size,
+                 uint64_t arena_base, uint64_t arena_cap_pages, uint64_t* arena,
+                 db_prp_out* prp, uint64_t* page_base, uint8_t* status, db_counters* ctr,
+                 uint32_t flags, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- MR lookup ------------------------------------------------------------
+ * Source: "NCCL expert course 26: GPUDirect RDMA, DMA-BUF, MR and the
+ * registration cache". "IB Backend MR Cache": a range is widened to whole
+ * pages (addr = data & -pageSize; pages = ceil((data + size - addr) /
+ * pageSize)); an existing MR is reused only if it fully contains the widened
+ * range; partial overlap is not a hit. "Communicator User Registration
+ * Cache": the same rounding over records kept sorted by address.
+ *
+ * For query k: base = addr & ~4095, aend = base + 4096 * pages.
+ *   invalid (size == 0, or addr + size > 2^64 - 4096): kind = DB_MR_INVALID
+ *   the lowest i with mr_start[i] <= base and aend <= mr_end[i]:
+ *     kind = DB_MR_EXACT if both ends are equal, else DB_MR_CONTAINED;
+ *     idx = i, lkey = mr_lkey[i]
+ *   none: kind = DB_MR_MISS, idx = -1, lkey = 0
+ *
+ * Arguments
+ *   q         [n_q] query ranges (16-byte aligned)
+ *   mr_start  [n_mr] record starts, sorted ascending
+ *   mr_end    [n_mr] record ends (exclusive); records must not overlap and
+ *             must not be empty (mr_start[i] < mr_end[i] <= mr_start[i+1])
+ *   mr_lkey   [n_mr]
+ *   idx, lkey, kind  [n_q] outputs
+ *   ctr       NULL or counters: err gets DB_ERR_TABLE_ORDER when the table
+ *             breaks the ordering rule (results are then undefined);
+ *             n_invalid counts invalid queries; total = hits
+ * Limits: n_mr < 2^31.
+ */
+int db_mr_workspace_size(uint64_t n_mr, size_t* bytes);
+int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
+                 const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr, int32_t* idx,
+                 uint32_t* lkey, uint8_t* kind, db_counters* ctr, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/* ---- put translation and WQE bucketing ------------------------------------
+ * Source: "mori communication library analysis (1)". Static-heap put:
+ * raddr = peerPtrs[pe] + offset with rkey = peerRkeys[pe] and the source
+ * object's lkey, the whole transfer in one WQE. Warp-level WQE slot
+ * reservation: each entry takes the next post index of its send queue.
+ *
+ * Put i is valid when pe < world, qp < n_qp, bytes >= 1 and
+ * off + bytes <= heap_size. Valid puts go to ring r = pe * n_qp + qp in
+ * batch order: the k-th of ring r takes seq = head[r] + k and lands in
+ * slot seq & (depth - 1) of ring r, i.e. at
+ * rings + (r * depth + (seq & (depth - 1))) * 64.
+ * A ring asked for more than `depth` entries by one batch takes none of
+ * them: its head stays, its puts count in n_overflow and err gets
+ * DB_ERR_RING_OVERFLOW. Otherwise head[r] += count[r].
+ *
+ * Arguments
+ *   req         [n] puts (16-byte aligned)
+ *   peer_ptrs   [world] heap base of each PE
+ *   rkeys       [world]
+ *   world, n_qp PEs and queue pairs per PE; 1 <= world * n_qp <= 1024
+ *   local_base, lkey, heap_size  the local object
+ *   rings       [world * n_qp][depth] db_wqe (64-byte aligned)
+ *   depth       entries per ring, a power of two
+ *   head        [world * n_qp] in/out post indices
+ *   count       [world * n_qp] output: valid puts per ring in this batch
+ *   ctr         NULL or counters: total = entries posted
+ * Limits: n < 2^32.
+ */
+int db_wqe_workspace_size(uint64_t n, uint32_t n_rings, size_t* bytes);
+int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
+                  const uint32_t* rkeys, uint32_t world, uint32_t n_qp, uint64_t local_base,
+                  uint32_t lkey, uint64_t heap_size, db_wqe* rings, uint64_t depth,
+                  uint64_t* head, uint32_t* count, db_counters* ctr, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* ---- misc ----------------------------------------------------------------- */
+const char* db_strerror(int code);
+/* The cudaError_t of the last -EIO on this thread (0 if none). */
+int db_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DESCBUILD_H */

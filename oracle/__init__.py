@@ -102,12 +102,16 @@ def prp_one(off: int, length: int, lut: np.ndarray, heap_size: int, arena_base: 
 
 
 def prp_build(req: np.ndarray, lut: np.ndarray, heap_size: int, arena_base: int,
-              arena_cap_pages: int, zero_tail: bool = False, fill: int = 0) -> dict:
-    """Whole batch; returns prp [n,2], page_base [n], status [n], ctr [4], arena."""
+              arena_cap_pages: int, zero_tail: bool = False, fill: int = 0,
+              lists: bool = True) -> dict:
+    """Whole batch; returns prp [n,2], page_base [n], status [n], ctr [4], arena.
+
+    With ``lists=False`` no arena is allocated or written (everything else is
+    computed as if the lists had been written)."""
     req = _u64(req).reshape(-1, 2)
     lut = _u64(lut)
     n = req.shape[0]
-    arena = np.full((max(arena_cap_pages, 1), 512), fill, dtype=np.uint64)
+    arena = np.full((max(arena_cap_pages, 1), 512), fill, dtype=np.uint64) if lists else None
     prp = np.zeros((n, 2), dtype=np.uint64)
     page_base = np.zeros(n, dtype=np.uint64)
     status = np.zeros(n, dtype=np.uint8)
@@ -116,7 +120,7 @@ def prp_build(req: np.ndarray, lut: np.ndarray, heap_size: int, arena_base: int,
                              arena_cap_pages, _p(arena), _p(prp), _p(page_base), _p(status),
                              _p(ctr), int(zero_tail))
     return dict(prp=prp, page_base=page_base, status=status, ctr=ctr,
-                arena=arena[:arena_cap_pages])
+                arena=arena[:arena_cap_pages] if lists else None)
 
 
 # ------------------------------------------------------------------------ MR

@@ -108,7 +108,8 @@ uint64_t oracle_prp_list_pages(uint64_t off, uint64_t len, uint64_t heap_size) {
 // Descriptors of ONE request whose list (if any) starts at list page
 // `page_base` of the arena. `list` receives the request's list pages
 // (list_pages * 512 words, laid out as they sit in the arena); untouched
-// slots are left as they are unless `zero_tail`. Returns the list-page count.
+// slots are left as they are unless `zero_tail`. A NULL `list` computes
+// PRP1/PRP2 only. Returns the list-page count.
 uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_t n_lut,
                         uint64_t heap_size, uint64_t arena_base, uint64_t page_base,
                         uint64_t* prp /*[2]*/, uint64_t* list, int zero_tail) {
@@ -127,6 +128,7 @@ uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_
   if (arena_base % kPage != 0) fail("arena base not page aligned");
   uint64_t n_list = list_pages_for(n - 1);
   prp[1] = arena_base + page_base * kPage;
+  if (!list) return n_list;
   uint64_t page = 0;   // list page being filled, relative to page_base
   uint64_t slot = 0;   // next free slot on it
   for (uint64_t k = 1; k < n; ++k) {
@@ -148,7 +150,8 @@ uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_
 
 // Whole batch, in request order.
 //  req        [n][2]: word 0 = heap offset, word 1 low 32 bits = length
-//  arena      host copy of the list arena, arena_cap_pages * 512 words
+//  arena      host copy of the list arena, arena_cap_pages * 512 words, or
+//             NULL to compute everything but the list pages
 //  prp        [n][2] out: PRP1, PRP2
 //  page_base  [n] out (nullable): first list page of each request (exclusive
 //             running sum of list pages, in request order)
@@ -181,7 +184,7 @@ void oracle_prp_build(const uint64_t* req, uint64_t n, const uint64_t* lut, uint
         st = 2;
         n_overflow += 1;
       } else {
-        uint64_t* list = pages ? arena + running * kListSlots : nullptr;
+        uint64_t* list = (pages && arena) ? arena + running * kListSlots : nullptr;
         uint64_t got = oracle_prp_one(off, len, lut, n_lut, heap_size, arena_base, running,
                                       prp + 2 * i, list, zero_tail);
         if (got != pages) fail("list page count disagrees");

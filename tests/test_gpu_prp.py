@@ -1,0 +1,241 @@
+"""db_prp_build on the GPU against the oracle, bit for bit.
+
+Integer work: every output word must equal the oracle's.
+"""
+
+import numpy as np
+import pytest
+
+from conftest import h, load_golden
+from gpu_util import dev64, host64, lib, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+FILL = -0x2152411021524111  # 0xDEADBEEFDEADBEEF as int64
+
+
+@pytest.fixture(scope="module")
+def db():
+    need_gpu()
+    return lib()
+
+
+def run_gpu(db, req, lut, heap, arena_base, cap, flags=0, ws=None, with_arena=True):
+    n = req.shape[0]
+    d_req = dev64(req) if n else torch.zeros((0, 2), dtype=torch.int64, device="cuda")
+    arena = torch.full((max(cap, 1), 512), FILL, dtype=torch.int64, device="cuda") \
+        if with_arena else None
+    prp = torch.full((max(n, 1), 2), FILL, dtype=torch.int64, device="cuda")
+    pb = torch.full((max(n, 1),), FILL, dtype=torch.int64, device="cuda")
+    st = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device="cuda")
+    ctr = torch.full((4,), FILL, dtype=torch.int64, device="cuda")
+    if ws is None:
+        ws = db.workspace(db.prp_workspace_size(n))
+    db.prp_build(d_req, dev64(lut), heap, arena_base, cap, arena, prp, ws, page_base=pb,
+                 status=st, ctr=ctr, flags=flags)
+    torch.cuda.synchronize()
+    return dict(prp=host64(prp)[:n], page_base=host64(pb)[:n], status=st.cpu().numpy()[:n],
+                ctr=host64(ctr), arena=arena)
+
+
+def compare(oracle, got, want, cap, zero_tail):
+    assert (got["prp"] == want["prp"]).all()
+    assert (got["page_base"] == want["page_base"]).all()
+    assert (got["status"] == want["status"]).all()
+    assert (got["ctr"] == want["ctr"]).all(), (got["ctr"], want["ctr"])
+    if got["arena"] is not None:
+        used = min(int(want["ctr"][0]), cap)
+        a = host64(got["arena"][:max(used, 1)])[:used]
+        # The oracle's arena was filled with the same marker: untouched slots agree too.
+        assert (a == want["arena"][:used]).all()
+        if used < cap:
+            rest = host64(got["arena"][used:used + 4])
+            assert (rest == np.uint64(FILL & (2**64 - 1))).all()
+
+
+def test_golden_hand_cases(db):
+    fx = load_golden("prp_hand_cases.json")
+    n_lut = fx["heap_size"] // 65536
+    lut = np.array([0x900000000 + c * 0x30000 for c in range(n_lut)], dtype=np.uint64)
+    for c, v in enumerate(fx["lut_explicit"]):
+        lut[c] = h(v)
+    for case in fx["cases"]:
+        cap = case.get("arena_cap_pages", fx["arena_cap_pages"])
+        req = np.array([[h(o), int(n)] for o, n in case["req"]], dtype=np.uint64)
+        got = run_gpu(db, req, lut, fx["heap_size"], h(fx["arena_base"]), cap)
+        want = np.array([[h(a), h(b)] for a, b in case["prp"]], dtype=np.uint64)
+        assert (got["prp"] == want).all(), case["name"]
+        assert got["page_base"].tolist() == case["page_base"], case["name"]
+        assert got["status"].tolist() == case["status"], case["name"]
+        assert int(got["ctr"][0]) == case["total_pages"], case["name"]
+        arena = host64(got["arena"])
+        for lp in case["lists"]:
+            for slot, val in lp["slots"].items():
+                assert int(arena[lp["page"], int(slot)]) == h(val), (case["name"], lp, slot)
+
+
+@pytest.mark.parametrize("zero_tail", [False, True])
+def test_tiny_workload(db, oracle, zero_tail):
+    import synth
+    w = synth.prp_tiny()
+    cap = 4096
+    want = oracle.prp_build(w["req"], w["lut"], w["heap_size"], w["arena_base"], cap,
+                            zero_tail=zero_tail, fill=FILL & (2**64 - 1))
+    got = run_gpu(db, w["req"], w["lut"], w["heap_size"], w["arena_base"], cap,
+                  flags=db.PRP_ZERO_TAIL if zero_tail else 0)
+    compare(oracle, got, want, cap, zero_tail)
+
+
+def random_batch(rng, n, heap, max_len, invalid_frac=0.02):
+    off = 4 * rng.integers(0, heap // 4, size=n).astype(np.uint64)
+    length = rng.integers(1, max_len + 1, size=n).astype(np.uint64)
+    length = np.minimum(length, np.uint64(heap) - off)
+    bad = rng.random(n) < invalid_frac
+    kind = rng.integers(0, 3, size=n)
+    length = np.where(bad & (kind == 0), 0, length)
+    off = np.where(bad & (kind == 1), off + np.uint64(2), off)
+    length = np.where(bad & (kind == 2), np.uint64(heap), length)
+    length[length == 0] = np.where(bad[length == 0], 0, 1)
+    return np.stack([off, length], axis=1).astype(np.uint64)
+
+
+@pytest.mark.parametrize("n", [1, 2, 511, 512, 513, 1023, 1025, 4999, 70001])
+def test_random_batches_ragged(db, oracle, n):
+    """Several tiles of 512 and a ragged tail, lists of all lengths."""
+    import synth
+    rng = np.random.default_rng(1000 + n)
+    heap = 64 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    req = random_batch(rng, n, heap, 5 * 1024 * 1024 if n < 5000 else 300 * 1024)
+    need = oracle.prp_build(req, lut, heap, 0x7_0000_0000, 1 << 40, lists=False)
+    cap = max(1, int(need["ctr"][0]))
+    want = oracle.prp_build(req, lut, heap, 0x7_0000_0000, cap, fill=FILL & (2**64 - 1))
+    got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap)
+    compare(oracle, got, want, cap, False)
+
+
+def test_arena_overflow_and_capacity_edges(db, oracle):
+    import synth
+    rng = np.random.default_rng(7)
+    heap = 16 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    req = random_batch(rng, 3000, heap, 3 * 1024 * 1024)
+    full = oracle.prp_build(req, lut, heap, 0x10000000, 1 << 20, lists=False)
+    total = int(full["ctr"][0])
+    for cap in (0, 1, total // 3, total - 1, total, total + 5):
+        want = oracle.prp_build(req, lut, heap, 0x10000000, cap, fill=FILL & (2**64 - 1))
+        got = run_gpu(db, req, lut, heap, 0x10000000, cap)
+        compare(oracle, got, want, cap, False)
+
+
+def test_empty_and_all_invalid(db, oracle):
+    import synth
+    lut = synth.physical_lut(np.random.default_rng(1), 16)
+    got = run_gpu(db, np.zeros((0, 2), dtype=np.uint64), lut, 1 << 20, 0, 4)
+    assert got["ctr"].tolist() == [0, 0, 0, 0]
+    req = np.array([[0, 0], [3, 100], [1 << 20, 1], [(1 << 20) - 4, 8]] * 300, dtype=np.uint64)
+    want = oracle.prp_build(req, lut, 1 << 20, 0, 4)
+    got = run_gpu(db, req, lut, 1 << 20, 0, 4)
+    compare(oracle, got, want, 4, False)
+    assert int(got["ctr"][1]) == 1200
+
+
+def test_largest_requests(db, oracle):
+    """Lengths up to 2^32 - 1 bytes (1,048,577 pages, 2053 list pages)."""
+    import synth
+    rng = np.random.default_rng(3)
+    heap = 8 * 1024**3
+    lut = synth.physical_lut(rng, heap // 65536)
+    req = np.array([[0, 0xFFFFFFFF], [4092, 0xFFFFFFFF], [4 << 30, 0xFFFFF000],
+                    [12, 513 * 4096]], dtype=np.uint64)
+    want = oracle.prp_build(req, lut, heap, 0x1_0000_0000, 8192, fill=FILL & (2**64 - 1))
+    assert int(want["ctr"][0]) > 6000
+    got = run_gpu(db, req, lut, heap, 0x1_0000_0000, 8192)
+    compare(oracle, got, want, 8192, False)
+
+
+def test_workspace_reuse_across_calls(db, oracle):
+    """One workspace, many calls of different sizes: results stay exact."""
+    import synth
+    rng = np.random.default_rng(11)
+    heap = 32 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    ws = db.workspace(db.prp_workspace_size(40000))
+    for n in (40000, 100, 7, 40000, 513, 20000):
+        req = random_batch(rng, n, heap, 1024 * 1024)
+        want = oracle.prp_build(req, lut, heap, 0x40000000, 1 << 16, fill=FILL & (2**64 - 1))
+        got = run_gpu(db, req, lut, heap, 0x40000000, 1 << 16, ws=ws)
+        compare(oracle, got, want, 1 << 16, False)
+
+
+def test_bad_arguments(db):
+    t = torch.zeros((4, 2), dtype=torch.int64, device="cuda")
+    lut = torch.ones(16, dtype=torch.int64, device="cuda") << 16
+    ws = db.workspace(db.prp_workspace_size(4))
+    with pytest.raises(db.DescBuildError, match="invalid"):
+        db.prp_build(t, lut, 1000, 0, 1, t, t, ws)           # heap not a multiple of 64 KiB
+    with pytest.raises(db.DescBuildError, match="invalid"):
+        db.prp_build(t, lut, 1 << 20, 100, 1, t, t, ws)      # arena base not page aligned
+    with pytest.raises(db.DescBuildError, match="workspace"):
+        db.prp_build(t, lut, 1 << 20, 0, 1, t, t, ws[:16])
+    with pytest.raises(db.DescBuildError, match="invalid"):
+        db.prp_build(t, lut, 1 << 20, 0, 1, t, t, ws, flags=8)
+
+
+def test_lookback_timeout_is_reported(db, oracle):
+    """A predecessor tile that never publishes: the bounded wait gives up,
+    the call reports DB_ERR_TIMEOUT, and the workspace works again after."""
+    import synth
+    rng = np.random.default_rng(5)
+    heap = 16 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    req = random_batch(rng, 4 * 512, heap, 64 * 1024)
+    ws = db.workspace(db.prp_workspace_size(req.shape[0]))
+    # The first 8 bytes of the workspace hold the next tile ticket, 0 between
+    # calls. Starting at 1 means no CTA ever takes tile 0.
+    ws[:8].view(torch.int64).fill_(1)
+    got = run_gpu(db, req, lut, heap, 0, 1 << 14, ws=ws)
+    assert int(got["ctr"][3]) & db.ERR_TIMEOUT
+    want = oracle.prp_build(req, lut, heap, 0, 1 << 14, fill=FILL & (2**64 - 1))
+    got = run_gpu(db, req, lut, heap, 0, 1 << 14, ws=ws)
+    compare(oracle, got, want, 1 << 14, False)
+
+
+def test_small_io_workload_full(db, oracle):
+    """1,048,576 small requests: every output against the oracle."""
+    import synth
+    w = synth.prp_small()
+    want = oracle.prp_build(w["req"], w["lut"], w["heap_size"], w["arena_base"], 1024)
+    assert int(want["ctr"][0]) == 0  # the list path is never taken here
+    got = run_gpu(db, w["req"], w["lut"], w["heap_size"], w["arena_base"], 1024)
+    compare(oracle, got, want, 1024, False)
+
+
+def test_large_workload_full_size(db, oracle):
+    """4,194,304 requests on a 16 GiB heap: PRPs, page bases and counters of
+    every request against the oracle; list pages of a sample, one by one."""
+    import synth
+    w = synth.prp_large()
+    req, lut = w["req"], w["lut"]
+    n = req.shape[0]
+    full = oracle.prp_build(req, lut, w["heap_size"], w["arena_base"], 1 << 40, lists=False)
+    cap = int(full["ctr"][0])
+    want = oracle.prp_build(req, lut, w["heap_size"], w["arena_base"], cap, lists=False)
+    got = run_gpu(db, req, lut, w["heap_size"], w["arena_base"], cap)
+    assert (got["prp"] == want["prp"]).all()
+    assert (got["page_base"] == want["page_base"]).all()
+    assert (got["status"] == want["status"]).all()
+    assert (got["ctr"] == want["ctr"]).all()
+    rng = np.random.default_rng(0)
+    pages = np.diff(np.append(want["page_base"], np.uint64(cap))).astype(np.int64)
+    with_list = np.flatnonzero(pages > 0)
+    sample = np.concatenate([rng.choice(with_list, 3000, replace=False),
+                             with_list[-5:], np.flatnonzero(pages >= 3)[:20]])
+    arena = got["arena"]
+    for i in sample:
+        pb, L = int(want["page_base"][i]), int(pages[i])
+        prp1, prp2, lst = oracle.prp_one(int(req[i, 0]), int(req[i, 1]), lut, w["heap_size"],
+                                         w["arena_base"], pb, fill=FILL & (2**64 - 1))
+        g = host64(arena[pb:pb + L])
+        used = lst != np.uint64(FILL & (2**64 - 1))
+        assert (g[used] == lst[used]).all(), i
