@@ -48,14 +48,24 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", choices=["prp_small", "prp_large", "mr_lookup", "put_bucket"],
+                    help="profiling aid: run one workload only (not a bench line)")
+    ap.add_argument("--fraction", type=float, default=1.0,
+                    help="profiling aid: keep this leading fraction of each batch")
     return ap.parse_args()
 
 
 # --------------------------------------------------------------------- inputs
-def make_inputs():
+def make_inputs(only=None, fraction=1.0):
     import synth
-    return dict(prp_small=synth.prp_small(), prp_large=synth.prp_large(),
-                mr_lookup=synth.mr_lookup(), put_bucket=synth.put_bucket())
+    gens = {"prp_small": synth.prp_small, "prp_large": synth.prp_large,
+            "mr_lookup": synth.mr_lookup, "put_bucket": synth.put_bucket}
+    inp = {k: g() for k, g in gens.items() if only in (None, k)}
+    if fraction < 1.0:
+        for k, w in inp.items():
+            key = "queries" if k == "mr_lookup" else "req"
+            w[key] = w[key][: max(1, int(w[key].shape[0] * fraction))]
+    return inp
 
 
 def list_words(req: np.ndarray) -> int:
@@ -71,21 +81,25 @@ def list_words(req: np.ndarray) -> int:
 
 
 def algorithmic_bytes(inp) -> dict:
-    """Bytes each call must move at minimum (read inputs once, write outputs once)."""
-    s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
-    return {
-        "prp_small": 32 * s["req"].shape[0] + 8 * list_words(s["req"]) + 8 * s["lut"].shape[0],
-        "prp_large": 32 * l["req"].shape[0] + 8 * list_words(l["req"]) + 8 * l["lut"].shape[0],
-        "mr_lookup": 25 * m["queries"].shape[0] + 20 * m["mr_start"].shape[0],
-        "put_bucket": 80 * p["req"].shape[0],
-    }
+    """Bytes each call must move at minimum (read inputs once, write outputs once):
+    PRP 16 B request + 16 B PRP pair + 8 B per list word + the LUT once;
+    MR 16 B query + 9 B result + the 20 B/record table once; put 16 B + 64 B WQE."""
+    out = {}
+    for k in ("prp_small", "prp_large"):
+        if k in inp:
+            w = inp[k]
+            out[k] = 32 * w["req"].shape[0] + 8 * list_words(w["req"]) + 8 * w["lut"].shape[0]
+    if "mr_lookup" in inp:
+        m = inp["mr_lookup"]
+        out["mr_lookup"] = 25 * m["queries"].shape[0] + 20 * m["mr_start"].shape[0]
+    if "put_bucket" in inp:
+        out["put_bucket"] = 80 * inp["put_bucket"]["req"].shape[0]
+    return out
 
 
 def units(inp) -> dict:
-    return {"prp_small": inp["prp_small"]["req"].shape[0],
-            "prp_large": inp["prp_large"]["req"].shape[0],
-            "mr_lookup": inp["mr_lookup"]["queries"].shape[0],
-            "put_bucket": inp["put_bucket"]["req"].shape[0]}
+    return {k: (w["queries"] if k == "mr_lookup" else w["req"]).shape[0]
+            for k, w in inp.items()}
 
 
 def peak_gbs():
@@ -176,77 +190,80 @@ def smi_index(device) -> int:
 class Step:
     """Device buffers for one replica and the calls of one step."""
 
+    LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 2}
+
     def __init__(self, db, torch, inp, device):
         self.db, self.torch, self.inp = db, torch, inp
         t = torch
         d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
         d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
-        self.d64, self.d32 = d64, d32
-        s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
-        self.small = dict(req=d64(s["req"]), lut=d64(s["lut"]), heap=s["heap_size"],
-                          base=s["arena_base"], cap=1, arena=t.zeros((1, 512), dtype=t.int64,
-                                                                   device=device),
-                          prp=t.empty((s["req"].shape[0], 2), dtype=t.int64, device=device),
-                          ctr=t.zeros(4, dtype=t.int64, device=device),
-                          ws=db.workspace(db.prp_workspace_size(s["req"].shape[0]), device))
-        self.large = dict(req=d64(l["req"]), lut=d64(l["lut"]), heap=l["heap_size"],
-                          base=l["arena_base"], cap=0, arena=None,
-                          prp=t.empty((l["req"].shape[0], 2), dtype=t.int64, device=device),
-                          ctr=t.zeros(4, dtype=t.int64, device=device),
-                          ws=db.workspace(db.prp_workspace_size(l["req"].shape[0]), device))
-        # Size the list arena the way a caller would: a call with no arena
-        # reports, in its counters, the list pages the batch needs.
-        self.prp(self.large, t.cuda.current_stream(device))
-        t.cuda.synchronize(device)
-        cap = int(self.large["ctr"][0].item())
-        self.large["cap"] = cap
-        self.large["arena"] = t.empty((cap, 512), dtype=t.int64, device=device)
-        nq = m["queries"].shape[0]
-        self.mr = dict(q=d64(m["queries"]), start=d64(m["mr_start"]), end=d64(m["mr_end"]),
-                       lkey=d32(m["mr_lkey"]),
-                       idx=t.empty(nq, dtype=t.int32, device=device),
-                       olkey=t.empty(nq, dtype=t.int32, device=device),
-                       kind=t.empty(nq, dtype=t.uint8, device=device),
-                       ctr=t.zeros(4, dtype=t.int64, device=device),
-                       ws=db.workspace(db.mr_workspace_size(m["mr_start"].shape[0]), device))
-        R = p["world"] * p["n_qp"]
-        self.put = dict(req=d64(p["req"]), peer=d64(p["peer_ptrs"]), rkeys=d32(p["rkeys"]),
-                        rings=t.empty((R, p["depth"], 64), dtype=t.uint8, device=device),
-                        head=d64(p["head"]), count=t.empty(R, dtype=t.int32, device=device),
-                        ctr=t.zeros(4, dtype=t.int64, device=device),
-                        ws=db.workspace(db.wqe_workspace_size(p["req"].shape[0], R), device))
+        self.bufs = {}
+        for k in ("prp_small", "prp_large"):
+            if k not in inp:
+                continue
+            w = inp[k]
+            n = w["req"].shape[0]
+            a = dict(req=d64(w["req"]), lut=d64(w["lut"]), heap=w["heap_size"],
+                     base=w["arena_base"], cap=0, arena=None,
+                     prp=t.empty((n, 2), dtype=t.int64, device=device),
+                     ctr=t.zeros(4, dtype=t.int64, device=device),
+                     ws=db.workspace(db.prp_workspace_size(n), device))
+            # Size the list arena the way a caller would: a call with no arena
+            # reports, in its counters, the list pages the batch needs.
+            self.prp(a, t.cuda.current_stream(device))
+            t.cuda.synchronize(device)
+            a["cap"] = int(a["ctr"][0].item())
+            a["arena"] = t.empty((max(a["cap"], 1), 512), dtype=t.int64, device=device)
+            self.bufs[k] = a
+        if "mr_lookup" in inp:
+            m = inp["mr_lookup"]
+            nq = m["queries"].shape[0]
+            self.bufs["mr_lookup"] = dict(
+                q=d64(m["queries"]), start=d64(m["mr_start"]), end=d64(m["mr_end"]),
+                lkey=d32(m["mr_lkey"]), idx=t.empty(nq, dtype=t.int32, device=device),
+                olkey=t.empty(nq, dtype=t.int32, device=device),
+                kind=t.empty(nq, dtype=t.uint8, device=device),
+                ctr=t.zeros(4, dtype=t.int64, device=device),
+                ws=db.workspace(db.mr_workspace_size(m["mr_start"].shape[0]), device))
+        if "put_bucket" in inp:
+            p = inp["put_bucket"]
+            R = p["world"] * p["n_qp"]
+            self.bufs["put_bucket"] = dict(
+                req=d64(p["req"]), peer=d64(p["peer_ptrs"]), rkeys=d32(p["rkeys"]),
+                rings=t.empty((R, p["depth"], 64), dtype=t.uint8, device=device),
+                head=d64(p["head"]), count=t.empty(R, dtype=t.int32, device=device),
+                ctr=t.zeros(4, dtype=t.int64, device=device),
+                ws=db.workspace(db.wqe_workspace_size(p["req"].shape[0], R), device))
 
     def prp(self, a, stream):
         self.db.prp_build(a["req"], a["lut"], a["heap"], a["base"], a["cap"], a["arena"],
                           a["prp"], a["ws"], ctr=a["ctr"], stream=stream)
 
     def mr_call(self, stream):
-        m = self.mr
+        m = self.bufs["mr_lookup"]
         self.db.mr_lookup(m["q"], m["start"], m["end"], m["lkey"], m["idx"], m["olkey"],
                           m["kind"], m["ws"], ctr=m["ctr"], stream=stream)
 
     def put_call(self, stream):
-        p, P = self.put, self.inp["put_bucket"]
+        p, P = self.bufs["put_bucket"], self.inp["put_bucket"]
         self.db.wqe_bucket(p["req"], p["peer"], p["rkeys"], P["world"], P["n_qp"],
                            P["local_base"], P["lkey"], P["heap_size"], p["rings"], P["depth"],
                            p["head"], p["count"], p["ws"], ctr=p["ctr"], stream=stream)
 
     def calls(self):
-        return [("prp_small", lambda s: self.prp(self.small, s)),
-                ("prp_large", lambda s: self.prp(self.large, s)),
-                ("mr_lookup", self.mr_call),
-                ("put_bucket", self.put_call)]
-
-    LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 2}
+        fns = {"prp_small": lambda s: self.prp(self.bufs["prp_small"], s),
+               "prp_large": lambda s: self.prp(self.bufs["prp_large"], s),
+               "mr_lookup": self.mr_call, "put_bucket": self.put_call}
+        return [(k, fns[k]) for k in ("prp_small", "prp_large", "mr_lookup", "put_bucket")
+                if k in self.bufs]
 
     def check_counters(self):
-        t = self.torch
-        for name, c in (("prp_small", self.small["ctr"]), ("prp_large", self.large["ctr"]),
-                        ("mr_lookup", self.mr["ctr"]), ("put_bucket", self.put["ctr"])):
-            err = int(c[3].item())
+        for name, b in self.bufs.items():
+            err = int(b["ctr"][3].item())
             if err:
                 raise RuntimeError(f"{name}: device error bits {err}")
-        assert int(self.large["ctr"][2].item()) == 0, "arena overflow in the benchmark"
+            if name.startswith("prp"):
+                assert int(b["ctr"][2].item()) == 0, "arena overflow in the benchmark"
 
 
 def run_ours(args, inp, world, device, dist):
@@ -327,7 +344,7 @@ def run_ours(args, inp, world, device, dist):
                             "kernel's inputs are evicted before its next launch",
                       "parallelism": f"replicas x{world}"},
            "kernels": kernels, "roofline": roof,
-           "gpu_launches": K * sum(Step.LAUNCHES.values()),
+           "gpu_launches": K * sum(Step.LAUNCHES[k] for k in u),
            "clocks": clk.summary()}
     if not args.no_e2e:
         out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world)
@@ -341,17 +358,22 @@ def run_e2e(st, stream, inp, K, device, dist, world):
     t = torch
     pin = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).pin_memory()
     pin32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).pin_memory()
-    s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
-    h_in = [(pin(s["req"]), st.small["req"]), (pin(s["lut"]), st.small["lut"]),
-            (pin(l["req"]), st.large["req"]), (pin(l["lut"]), st.large["lut"]),
-            (pin(m["queries"]), st.mr["q"]), (pin(m["mr_start"]), st.mr["start"]),
-            (pin(m["mr_end"]), st.mr["end"]), (pin32(m["mr_lkey"]), st.mr["lkey"]),
-            (pin(p["req"]), st.put["req"]), (pin(p["peer_ptrs"]), st.put["peer"]),
-            (pin32(p["rkeys"]), st.put["rkeys"])]
-    used = st.large["cap"]
-    outs = [st.small["prp"], st.large["prp"], st.large["arena"][:used], st.mr["idx"],
-            st.mr["olkey"], st.mr["kind"], st.put["rings"], st.put["head"], st.put["count"],
-            st.small["ctr"], st.large["ctr"], st.mr["ctr"], st.put["ctr"]]
+    h_in, outs = [], []
+    for k in ("prp_small", "prp_large"):
+        if k in st.bufs:
+            b, w = st.bufs[k], inp[k]
+            h_in += [(pin(w["req"]), b["req"]), (pin(w["lut"]), b["lut"])]
+            outs += [b["prp"], b["ctr"]] + ([b["arena"][:b["cap"]]] if b["cap"] else [])
+    if "mr_lookup" in st.bufs:
+        b, m = st.bufs["mr_lookup"], inp["mr_lookup"]
+        h_in += [(pin(m["queries"]), b["q"]), (pin(m["mr_start"]), b["start"]),
+                 (pin(m["mr_end"]), b["end"]), (pin32(m["mr_lkey"]), b["lkey"])]
+        outs += [b["idx"], b["olkey"], b["kind"], b["ctr"]]
+    if "put_bucket" in st.bufs:
+        b, p = st.bufs["put_bucket"], inp["put_bucket"]
+        h_in += [(pin(p["req"]), b["req"]), (pin(p["peer_ptrs"]), b["peer"]),
+                 (pin32(p["rkeys"]), b["rkeys"])]
+        outs += [b["rings"], b["head"], b["count"], b["ctr"]]
     h_out = [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     bi = sum(h.numel() * h.element_size() for h, _ in h_in)
     bo = sum(o.numel() * o.element_size() for o in outs)
@@ -391,7 +413,8 @@ def run_e2e(st, stream, inp, K, device, dist, world):
 def cpu_baseline(inp, scale: int = 1) -> dict:
     """The oracle as it stands (single-threaded C++) on a bounded sample of
     each workload; value in the same unit, scaled by the sample sizes.
-    ``scale`` divides the sample sizes."""
+    ``scale`` divides the sample sizes. Output buffers that scale with the
+    ring or arena size are allocated outside the timed calls."""
     import oracle
     s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
     samples = {"prp_small": 262_144 // scale, "prp_large": 65_536 // scale,
@@ -402,19 +425,21 @@ def cpu_baseline(inp, scale: int = 1) -> dict:
                      s["arena_base"], 1, lists=False)
     secs["prp_small"] = time.perf_counter() - t
     req = l["req"][:samples["prp_large"]]
-    need = oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], 1 << 40,
-                            lists=False)
+    need = int(oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], 1 << 40,
+                                lists=False)["ctr"][0])
+    arena = np.zeros((need, 512), dtype=np.uint64)
     t = time.perf_counter()
-    oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], int(need["ctr"][0]))
+    oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], need, arena=arena)
     secs["prp_large"] = time.perf_counter() - t
     t = time.perf_counter()
     oracle.mr_bsearch(m["queries"][:samples["mr_lookup"]], m["mr_start"], m["mr_end"],
                       m["mr_lkey"])
     secs["mr_lookup"] = time.perf_counter() - t
+    rings = np.zeros((p["world"] * p["n_qp"], p["depth"], 64), dtype=np.uint8)
     t = time.perf_counter()
     oracle.wqe_bucket(p["req"][:samples["put_bucket"]], p["peer_ptrs"], p["rkeys"], p["world"],
                       p["n_qp"], p["local_base"], p["lkey"], p["heap_size"], p["depth"],
-                      p["head"])
+                      p["head"], rings=rings)
     secs["put_bucket"] = time.perf_counter() - t
     # Time for one full step's requests at the sampled per-request rates.
     u = units(inp)
@@ -424,7 +449,7 @@ def cpu_baseline(inp, scale: int = 1) -> dict:
             "sample": "first %d prp_small, %d prp_large (lists written), %d mr_lookup "
                       "(binary-search oracle), %d put_bucket requests; per-workload rates "
                       "scaled to one full step" % tuple(samples[k] for k in u),
-            "seconds": {k: round(v, 3) for k, v in secs.items()}}
+            "seconds": {k: round(v, 4) for k, v in secs.items()}}
 
 
 # ------------------------------------------------------------ reference arm
@@ -433,13 +458,13 @@ def run_reference(args):
     workload on the host cores, same metric and unit as our arm."""
     inp = make_inputs()
     for _ in range(args.warmup):
-        cpu_baseline(inp, scale=8)
+        cpu_baseline(inp)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(inp, scale=8))
+        vals.append(cpu_baseline(inp))
     wall = time.perf_counter() - t0
-    v = statistics.median(x["value"] for x in vals)
+    v = round(statistics.median(x["value"] for x in vals), 3)
     reqs = sum(units(inp).values())
     ms = reqs / (v * 1e6) * 1e3
     cb = dict(vals[0])
@@ -469,10 +494,12 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
-    inp = make_inputs()
+    inp = make_inputs(args.only, args.fraction)
     out = run_ours(args, inp, world, device, dist)
     if rank == 0:
-        if not args.no_cpu:
+        if args.only or args.fraction < 1.0:
+            out["note"] = "profiling run on a subset: not a bench line"
+        if not args.no_cpu and not args.only and args.fraction >= 1.0:
             out["cpu_baseline"] = cpu_baseline(inp)
         print(json.dumps(out), flush=True)
     if dist:

@@ -103,15 +103,21 @@ def prp_one(off: int, length: int, lut: np.ndarray, heap_size: int, arena_base: 
 
 def prp_build(req: np.ndarray, lut: np.ndarray, heap_size: int, arena_base: int,
               arena_cap_pages: int, zero_tail: bool = False, fill: int = 0,
-              lists: bool = True) -> dict:
+              lists: bool = True, arena: np.ndarray | None = None) -> dict:
     """Whole batch; returns prp [n,2], page_base [n], status [n], ctr [4], arena.
 
     With ``lists=False`` no arena is allocated or written (everything else is
-    computed as if the lists had been written)."""
+    computed as if the lists had been written). ``arena`` may be given as a
+    preallocated uint64 [>= arena_cap_pages, 512] array."""
     req = _u64(req).reshape(-1, 2)
     lut = _u64(lut)
     n = req.shape[0]
-    arena = np.full((max(arena_cap_pages, 1), 512), fill, dtype=np.uint64) if lists else None
+    if not lists:
+        arena = None
+    elif arena is None:
+        arena = np.full((max(arena_cap_pages, 1), 512), fill, dtype=np.uint64)
+    else:
+        assert arena.dtype == np.uint64 and arena.shape[0] >= arena_cap_pages
     prp = np.zeros((n, 2), dtype=np.uint64)
     page_base = np.zeros(n, dtype=np.uint64)
     status = np.zeros(n, dtype=np.uint8)
@@ -156,13 +162,18 @@ def mr_bsearch(queries, start, end, lkey) -> dict:
 
 # ----------------------------------------------------------------------- WQE
 def wqe_bucket(req, peer_ptrs, rkeys, world: int, n_qp: int, local_base: int, lkey: int,
-               heap_size: int, depth: int, head, fill: int = 0) -> dict:
-    """Whole batch; returns rings [R, depth, 64] u8, head, count, ctr."""
+               heap_size: int, depth: int, head, fill: int = 0,
+               rings: np.ndarray | None = None) -> dict:
+    """Whole batch; returns rings [R, depth, 64] u8, head, count, ctr.
+    ``rings`` may be given preallocated."""
     req = _u64(req).reshape(-1, 2)
     peer_ptrs = _u64(peer_ptrs)
     rkeys = np.ascontiguousarray(rkeys, dtype=np.uint32)
     n_rings = world * n_qp
-    rings = np.full((n_rings, depth, 64), fill, dtype=np.uint8)
+    if rings is None:
+        rings = np.full((n_rings, depth, 64), fill, dtype=np.uint8)
+    else:
+        assert rings.dtype == np.uint8 and rings.shape == (n_rings, depth, 64)
     head = _u64(head).copy()
     count = np.zeros(n_rings, dtype=np.uint32)
     ctr = np.zeros(4, dtype=np.uint64)
