@@ -27,6 +27,7 @@ from . import build as _build
 
 __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
+    "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
     "mr_workspace_size", "mr_lookup", "wqe_workspace_size", "wqe_bucket", "strerror",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
@@ -60,12 +61,14 @@ def _load():
     psz = ctypes.POINTER(ctypes.c_size_t)
     lib.db_prp_workspace_size.argtypes = [u64, psz]
     lib.db_prp_build.argtypes = [vp, u64, vp, u64, u64, u64, vp, vp, vp, vp, vp, u32, vp, sz, vp]
+    lib.db_prp_build_static.argtypes = [vp, u64, vp, u64, u64, u64, vp, vp, vp, vp, vp, u32, vp]
     lib.db_mr_workspace_size.argtypes = [u64, psz]
     lib.db_mr_lookup.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp, vp, vp, sz, vp]
     lib.db_wqe_workspace_size.argtypes = [u64, u32, psz]
     lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
                                   vp, sz, vp]
-    for name in ("db_prp_workspace_size", "db_prp_build", "db_mr_workspace_size",
+    for name in ("db_prp_workspace_size", "db_prp_build", "db_prp_build_static",
+                 "db_mr_workspace_size",
                  "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket",
                  "db_last_cuda_error"):
         getattr(lib, name).restype = i32
@@ -137,6 +140,25 @@ def prp_build(req: torch.Tensor, lut: torch.Tensor, heap_size: int, arena_base: 
         _ptr(req), n, _ptr(lut), heap_size, arena_base, arena_cap_pages, _ptr(arena), _ptr(prp),
         _ptr(page_base), _ptr(status), _ptr(ctr), flags, _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+PRP_STATIC_MAX_REQUESTS = 1 << 24
+
+
+def prp_build_static(req: torch.Tensor, lut: torch.Tensor, heap_size: int, arena_base: int,
+                     arena_cap_pages: int, arena: torch.Tensor | None, prp: torch.Tensor,
+                     page_base: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     ctr: torch.Tensor | None = None, flags: int = 0, stream=None) -> None:
+    """db_prp_build_static: prp_build with the library's own static scratch
+    array, for callers that must not allocate device memory while submitting
+    (cudaMalloc may wait on queued device work and takes driver locks).
+    At most PRP_STATIC_MAX_REQUESTS requests per call; calls that may overlap
+    on the GPU share the array and must be ordered by the caller. The first
+    call on a device looks the array up, so make it before any stream capture."""
+    n = _records(req, 16)
+    _check("db_prp_build_static", _lib.db_prp_build_static(
+        _ptr(req), n, _ptr(lut), heap_size, arena_base, arena_cap_pages, _ptr(arena), _ptr(prp),
+        _ptr(page_base), _ptr(status), _ptr(ctr), flags, _stream(stream)))
 
 
 # ------------------------------------------------------------------ MR lookup

@@ -14,6 +14,12 @@ int launch_result() {
   return -EIO;
 }
 
+int cuda_failure(cudaError_t e) {
+  cudaGetLastError();  // clear it: the code is returned through db_last_cuda_error
+  g_last_cuda_error = (int)e;
+  return -EIO;
+}
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -40,6 +46,8 @@ extern "C" const char* db_strerror(int code) {
       return "workspace too small";
     case -EIO:
       return "CUDA launch failed (see db_last_cuda_error)";
+    case -E2BIG:
+      return "batch larger than the built-in workspace allows (DB_PRP_STATIC_MAX_REQUESTS)";
     default:
       return "unknown error";
   }

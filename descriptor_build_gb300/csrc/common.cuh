@@ -224,6 +224,8 @@ inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 
 // Record and map a CUDA error from the most recent launch.
 int launch_result();
+// Record a failed CUDA runtime call and return -EIO.
+int cuda_failure(cudaError_t e);
 int num_sms();
 
 }  // namespace db

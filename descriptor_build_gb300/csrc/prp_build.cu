@@ -30,8 +30,8 @@ constexpr uint32_t kPackShift = 21;  // list pages of a tile < 2^21
 
 // Workspace: ScanHeader (acc[0] invalid, acc[1] overflow), then one status
 // word per tile.
-inline uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
-inline size_t ws_bytes_for(uint64_t n) {
+constexpr uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
+constexpr size_t ws_bytes_for(uint64_t n) {
   return kScanHeaderBytes + ((tiles_for(n) * 8 + 255) & ~(uint64_t)255);
 }
 
@@ -342,4 +342,54 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
   p.cap_tiles = (ws_bytes - kScanHeaderBytes) / 8;
   prp::prp_build_kernel<<<prp::grid_for(p.n_tiles), prp::kThreads, 0, s>>>(p);
   return launch_result();
+}
+
+// ---------------------------------------------------------------------------
+// db_prp_build_static: the same build with its scratch in a static device
+// array instead of a caller workspace (for callers that must not allocate).
+#include <mutex>
+
+namespace db {
+namespace prp {
+
+constexpr size_t kStaticWsBytes = ws_bytes_for(DB_PRP_STATIC_MAX_REQUESTS);
+
+// Zero when the module loads; every call leaves it ready for the next call.
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+// Device address of g_static_ws on the current device. Host code cannot use
+// the symbol itself (on the host it names a stand-in, not device memory), so
+// the address is looked up once per device, with that device current.
+int static_ws_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_failure(e);
+  if (dev < 0 || dev >= 64) return -EINVAL;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return cuda_failure(e);
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return 0;
+}
+
+}  // namespace prp
+}  // namespace db
+
+extern "C" int db_prp_build_static(const db_prp_req* req, uint64_t n, const uint64_t* lut,
+                                   uint64_t heap_size, uint64_t arena_base,
+                                   uint64_t arena_cap_pages, uint64_t* arena, db_prp_out* prp,
+                                   uint64_t* page_base, uint8_t* status, db_counters* ctr,
+                                   uint32_t flags, void* stream) {
+  if (n > DB_PRP_STATIC_MAX_REQUESTS) return -E2BIG;
+  void* ws = nullptr;
+  const int rc = prp::static_ws_address(&ws);
+  if (rc) return rc;
+  return db_prp_build(req, n, lut, heap_size, arena_base, arena_cap_pages, arena, prp, page_base,
+                      status, ctr, flags, ws, prp::kStaticWsBytes, stream);
 }

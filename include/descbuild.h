@@ -228,6 +228,37 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
                   uint64_t* head, uint32_t* count, db_counters* ctr, void* ws,
                   size_t ws_bytes, void* stream);
 
+/* ---- PRP build with no caller workspace ------------------------------------
+ * The source pages have no counterpart to this entry point; it is an addition
+ * for callers that must not allocate device memory on their submission path:
+ * cudaMalloc can wait for work already queued on the device and takes driver
+ * locks, so a latency-bound I/O submitter cannot afford it, and a process
+ * whose device memory is handed out up front by its own allocator may have no
+ * room for an extra cudaMalloc at all.
+ *
+ * Same arguments and results as db_prp_build, without `ws`/`ws_bytes`: the
+ * scratch memory (a header and one status word per tile of requests) is a
+ * static device array inside libdescbuild.so, sized for at most
+ * DB_PRP_STATIC_MAX_REQUESTS (16,777,216) requests per call: 256 B of header
+ * plus 8 B per tile of 512 requests, 256.25 KiB in all. Every GPU that loads
+ * the library holds that array until the process exits.
+ *
+ *  - n > DB_PRP_STATIC_MAX_REQUESTS returns -E2BIG before any GPU work.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture on the device.
+ *  - The array starts zeroed and every call leaves it ready for the next one,
+ *    so no call has to clear it. All calls share it: calls whose work can
+ *    overlap on the GPU (different streams without ordering between them, or
+ *    different host threads) race on it and must be serialised by the caller.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define DB_PRP_STATIC_MAX_REQUESTS (1u << 24)
+int db_prp_build_static(const db_prp_req* req, uint64_t n, const uint64_t* lut,
+                        uint64_t heap_size, uint64_t arena_base, uint64_t arena_cap_pages,
+                        uint64_t* arena, db_prp_out* prp, uint64_t* page_base, uint8_t* status,
+                        db_counters* ctr, uint32_t flags, void* stream);
+
 /* ---- misc ----------------------------------------------------------------- */
 const char* db_strerror(int code);
 /* The cudaError_t of the last -EIO on this thread (0 if none). */
