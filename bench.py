@@ -190,7 +190,7 @@ def smi_index(device) -> int:
 class Step:
     """Device buffers for one replica and the calls of one step."""
 
-    LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 2}
+    LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 3}
 
     def __init__(self, db, torch, inp, device):
         self.db, self.torch, self.inp = db, torch, inp

@@ -7,11 +7,11 @@
 // rounding over records kept sorted by address).
 //
 // Two launches per call:
-//   index build  one thread per record: copies (start, end, lkey) into
-//                32-byte records (one L2 sector each) and fills a directory
-//                D[b] = number of records starting below lo + b * 2^shift,
-//                with 2^shift chosen so that the records' span fits nb
-//                buckets; also checks the table is sorted and disjoint.
+//   index build  copies (start, end, lkey) into 32-byte records (one L2
+//                sector each), checks the table is sorted and disjoint, and
+//                fills a directory D[b] = number of records starting below
+//                lo + b * 2^shift (2^shift chosen so that the records' span
+//                fits nb buckets) by a merge path over records and buckets.
 //   lookup       kQPT queries per thread: round to pages, read D[b], D[b+1]
 //                (adjacent words), binary-search the few records of the
 //                bucket, read the one candidate record, classify. Queries of
@@ -73,37 +73,65 @@ __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t 
   return b < nb ? b : nb;
 }
 
+constexpr int kMergeChunk = 32;  // merged elements per thread in the directory build
+
+// Records: 32-byte copies and the ordering check. Directory: D[b] = number of
+// records whose bucket key is below b, for b = 0..nb -- the merge of the
+// (sorted) record keys with the bucket numbers, split into equal chunks of
+// the merged sequence ("merge path"), so every thread does the same work
+// however the records fall into buckets.
 __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildParams p) {
   const uint64_t lo = p.start[0];
   const uint64_t hi = p.start[p.n_mr - 1];
   const uint64_t span = hi > lo ? hi - lo : 0;
   const uint32_t bits = span ? 64u - (uint32_t)__clzll((long long)span) : 0u;
   const uint32_t shift = bits > p.log_nb ? bits - p.log_nb : 0u;
+  const uint64_t nb = p.nb;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     p.hdr->lo = lo;
     p.hdr->shift = shift;
     p.hdr->nb = p.nb;
   }
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+
   bool bad = false;
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i <= p.n_mr;
-       i += (uint64_t)gridDim.x * blockDim.x) {
-    // Buckets (prev, cur] start at record i: D[b] = i for those b.
-    const int64_t prev = i == 0 ? -1 : (int64_t)bucket_of(p.start[i - 1], lo, shift, p.nb);
-    const int64_t cur = i == p.n_mr ? (int64_t)p.nb : (int64_t)bucket_of(p.start[i], lo, shift, p.nb);
-    for (int64_t b = prev + 1; b <= cur; ++b) p.dir[b] = (uint32_t)i;
-    if (i < p.n_mr) {
-      const uint64_t s = p.start[i], e = p.end[i];
-      Rec r;
-      r.start = s;
-      r.end = e;
-      r.lkey = p.lkey[i];
-      r.pad0 = 0;
-      r.pad1 = 0;
-      p.rec[i] = r;
-      if (!(s < e) || (i > 0 && p.end[i - 1] > s)) bad = true;
-    }
+  for (uint64_t i = tid; i < p.n_mr; i += nthreads) {
+    const uint64_t s = p.start[i], e = p.end[i];
+    Rec r;
+    r.start = s;
+    r.end = e;
+    r.lkey = p.lkey[i];
+    r.pad0 = 0;
+    r.pad1 = 0;
+    p.rec[i] = r;
+    if (!(s < e) || (i > 0 && p.end[i - 1] > s)) bad = true;
   }
   if (bad) atomicOr(&p.hdr->err, DB_ERR_TABLE_ORDER);
+
+  // Merge order: record i comes before bucket number b iff key(i) < b.
+  const uint64_t n = p.n_mr;
+  const uint64_t merged = n + nb + 1;
+  for (uint64_t k = tid * kMergeChunk; k < merged; k += nthreads * kMergeChunk) {
+    // m = records among the first k merged elements: the largest m with
+    // key(m - 1) < k - m.
+    uint64_t mlo = k > nb + 1 ? k - (nb + 1) : 0;
+    uint64_t mhi = k < n ? k : n;
+    while (mlo < mhi) {
+      const uint64_t mid = (mlo + mhi + 1) >> 1;
+      if (bucket_of(p.start[mid - 1], lo, shift, p.nb) < k - mid)
+        mlo = mid;
+      else
+        mhi = mid - 1;
+    }
+    uint64_t i = mlo, b = k - mlo;
+    for (int step = 0; step < kMergeChunk && (i < n || b <= nb); ++step) {
+      if (i < n && (b > nb || bucket_of(p.start[i], lo, shift, p.nb) < b))
+        ++i;
+      else
+        p.dir[b++] = (uint32_t)i;
+    }
+  }
 }
 
 struct LookupParams {
@@ -286,9 +314,10 @@ extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_
 
   if (n_mr > 0) {
     mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb};
-    const uint64_t work = n_mr + 1;
-    uint64_t grid = (work + mr::kBuildThreads - 1) / mr::kBuildThreads;
-    const uint64_t cap = (uint64_t)num_sms() * 8;
+    const uint64_t merged = n_mr + nb + 1;
+    const uint64_t threads = (merged + mr::kMergeChunk - 1) / mr::kMergeChunk;
+    uint64_t grid = (threads + mr::kBuildThreads - 1) / mr::kBuildThreads;
+    const uint64_t cap = (uint64_t)num_sms() * 16;
     if (grid > cap) grid = cap;
     mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
     int rc = launch_result();

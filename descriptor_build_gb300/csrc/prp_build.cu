@@ -25,8 +25,8 @@ namespace prp {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTile = kThreads;  // requests per tile
-constexpr uint32_t kPackShift = 21;  // list pages of a tile < 2^21
+constexpr int kItems = 4;                  // requests per thread per tile
+constexpr int kTile = kThreads * kItems;   // 2048 requests per tile
 
 // Workspace: ScanHeader (acc[0] invalid, acc[1] overflow), then one status
 // word per tile.
@@ -54,7 +54,7 @@ struct Params {
   uint64_t cap_tiles;
 };
 
-// A request that owns list pages, queued for the emission phase.
+// A request that owns list pages, as the emission phase sees it.
 struct ListItem {
   uint64_t pb;    // first list page (arena page index)
   uint64_t hb;    // heap offset of the request's first 4 KiB page
@@ -62,20 +62,125 @@ struct ListItem {
   uint32_t pages; // list pages (0: skip, the list did not fit)
 };
 
+// Queued form, 16 bytes: w0 = hb | pages (hb is page aligned, pages < 4096),
+// w1 = pb | n << 40 (pb < 2^40 by the host check, n < 2^21).
+__device__ __forceinline__ ulonglong2 pack_item(uint64_t hb, uint32_t pages, uint64_t pb,
+                                                uint32_t npg) {
+  return make_ulonglong2(hb | pages, (pb & ((1ull << 40) - 1)) | ((uint64_t)npg << 40));
+}
+__device__ __forceinline__ ListItem unpack_item(ulonglong2 q) {
+  ListItem it;
+  it.hb = q.x & ~4095ull;
+  it.pages = (uint32_t)(q.x & 4095ull);
+  it.pb = q.y & ((1ull << 40) - 1);
+  const uint32_t npg = (uint32_t)(q.y >> 40);
+  it.words = it.pages ? (npg - 1) + (it.pages - 1) : 0;
+  return it;
+}
+
 __device__ __forceinline__ uint64_t bus(const uint64_t* lut, uint64_t x, uint64_t pol) {
   return ld_table8(lut + (x >> 16), pol) + (x & 0xFFFFull);
 }
 
-// Word w of a list: slot 511 of every page but the last points at the next
-// page; every other word is data entry e = w - (pointers before w), which
-// names the heap page hb + 4096 (e + 1).
+// LUT window of a warp: lane l holds lut[wb + l] (0 past the request's last
+// chunk). Issued as a volatile load so that it is not moved behind the stores
+// of the previous request (it is the prefetch of the next one).
+__device__ __forceinline__ uint64_t lut_window(const uint64_t* lut, uint64_t wb, uint64_t c_last,
+                                               int lane, uint64_t pol) {
+  uint64_t v = 0;
+  const uint64_t c = wb + (uint64_t)lane;
+  if (c <= c_last)
+    asm volatile("ld.global.nc.L2::cache_hint.u64 %0, [%1], %2;" : "=l"(v) : "l"(lut + c), "l"(pol));
+  return v;
+}
+
+// Chunk (64 KiB LUT index) of data entry e (0-based): heap page hb + 4096 (e + 1).
+__device__ __forceinline__ uint64_t entry_chunk(const ListItem& it, uint32_t e) {
+  return (it.hb + ((uint64_t)(e + 1) << 12)) >> 16;
+}
+__device__ __forceinline__ uint64_t last_chunk(const ListItem& it) {
+  return entry_chunk(it, it.words - (it.pages - 1) - 1);
+}
+
+// Word w of a list (w < words): slot 511 of every page but the last points at
+// the next page; every other word is data entry e = w - (pointers before w),
+// the bus address of heap page hb + 4096 (e + 1). The LUT value comes from the
+// warp's window by shuffle, so all lanes execute this.
 __device__ __forceinline__ uint64_t list_word(const Params& p, const ListItem& it, uint32_t w,
-                                              uint64_t pol) {
-  if (w >= it.words) return 0;  // zeroed tail
+                                              uint64_t lutv, uint64_t wb) {
   const uint32_t j = w >> 9;
-  if ((w & 511u) == 511u && j + 1 < it.pages) return p.arena_base + ((it.pb + j + 1) << 12);
+  const bool ptr = (w & 511u) == 511u && j + 1 < it.pages;
   const uint64_t x = it.hb + ((uint64_t)(w - j + 1) << 12);
-  return bus(p.lut, x, pol);
+  const int src = (int)(((x >> 16) - wb) & 31u);
+  const uint64_t base = __shfl_sync(kFull, lutv, src);
+  if (w >= it.words) return 0;  // zeroed tail
+  if (ptr) return p.arena_base + ((it.pb + j + 1) << 12);
+  return base + (x & 0xFFFFull);
+}
+
+// One request's list run, written by a whole warp: 64 words per iteration as
+// 16-byte stores (a warp store covers 512 contiguous bytes). A 64-word step
+// spans at most 5 LUT chunks; the window moves when the next step could leave it.
+__device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, uint64_t lutv,
+                                          uint64_t wb, int lane, uint64_t pol_lut,
+                                          uint64_t pol_out) {
+  uint64_t* dst = p.arena + (it.pb << 9);
+  const uint32_t total = p.zero_tail ? (it.pages << 9) : it.words;
+  const uint64_t c_last = last_chunk(it);
+  for (uint32_t ib = 0; ib < total; ib += 64) {
+    if (ib < it.words) {
+      const uint64_t c_min = entry_chunk(it, ib - (ib >> 9));
+      if (c_min + 4 >= wb + 32) {
+        wb = c_min;
+        lutv = lut_window(p.lut, wb, c_last, lane, pol_lut);
+      }
+    }
+    const uint32_t w = ib + 2 * lane;
+    const uint64_t v0 = list_word(p, it, w, lutv, wb);
+    const uint64_t v1 = list_word(p, it, w + 1, lutv, wb);
+    if (w + 1 < total)
+      st_stream16(dst + w, v0, v1, pol_out);
+    else if (w < total)
+      st_stream8(dst + w, v0, pol_out);
+  }
+}
+
+// Exclusive scan over a tile held as kItems rows of kThreads values, in
+// request order (row-major: request k * kThreads + thread). s_scan holds
+// kItems * kWarps values.
+__device__ __forceinline__ void tile_excl_scan(const uint64_t (&v)[kItems], uint64_t (&excl)[kItems],
+                                               uint64_t& total, uint64_t* s_scan) {
+  static_assert(kItems * kWarps == 64, "two scan totals per lane");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    x[k] = v[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(kFull, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+    if (lane == 31) s_scan[k * kWarps + warp] = x[k];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint64_t a = s_scan[2 * lane], b = s_scan[2 * lane + 1];
+    uint64_t t = a + b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(kFull, t, o);
+      if (lane >= o) t += y;
+    }
+    const uint64_t before = t - a - b;
+    s_scan[2 * lane] = before;
+    s_scan[2 * lane + 1] = before + a;
+    if (lane == 31) s_scan[64] = t;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) excl[k] = s_scan[k * kWarps + warp] + x[k] - v[k];
+  total = s_scan[64];
 }
 
 // Decoupled lookback for tile t (warp 0 only). Publishes the tile's
@@ -130,11 +235,11 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
 
 __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) {
   __shared__ unsigned long long s_ticket;
-  __shared__ uint32_t s_scan[kWarps];
+  __shared__ uint64_t s_scan[kItems * kWarps + 1];
   __shared__ unsigned long long s_excl;
   __shared__ int s_failed;
   __shared__ uint32_t s_next;
-  __shared__ ListItem s_list[kTile];
+  __shared__ ulonglong2 s_list[kTile];
 
   const int lane = threadIdx.x & 31;
   const uint64_t pol_first = policy_evict_first();
@@ -149,24 +254,35 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
     const uint64_t tile = s_ticket;
     if (tile >= p.n_tiles) break;
 
-    // 1-2. One request per thread: validity, pages touched, list pages.
-    const uint64_t i = tile * kTile + threadIdx.x;
-    const bool in = i < p.n;
-    uint64_t off = 0;
-    uint32_t len = 0;
-    if (in) {
-      const ulonglong2 r = ld_stream16(p.req + i, pol_first);
-      off = r.x;
-      len = (uint32_t)r.y;
+    // 1-2. Four requests per thread (rows of the tile): validity, pages
+    //      touched, list pages; scan of (list pages, has-a-list) in request order.
+    uint64_t off[kItems];
+    uint32_t len[kItems], npg[kItems], L[kItems];
+    bool valid[kItems];
+    uint64_t v[kItems], ex[kItems], tile_v;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      off[k] = 0;
+      len[k] = 0;
+      if (i < p.n) {
+        const ulonglong2 r = ld_stream16(p.req + i, pol_first);
+        off[k] = r.x;
+        len[k] = (uint32_t)r.y;
+      }
     }
-    const bool valid = in && len != 0 && (off & 3) == 0 && off <= p.heap_size &&
-                       (uint64_t)len <= p.heap_size - off;
-    const uint32_t npg = valid ? (uint32_t)(((off & 4095) + len + 4095) >> 12) : 0;
-    const uint32_t L = npg >= 3 ? (npg - 2 + 510) / 511 : 0;  // ceil((list entries - 1) / 511)
-    uint32_t excl_pack, tile_pack;
-    block_excl_scan<kWarps>(L | ((L ? 1u : 0u) << kPackShift), excl_pack, tile_pack, s_scan);
-    const uint32_t tile_L = tile_pack & ((1u << kPackShift) - 1);
-    const uint32_t n_list = tile_pack >> kPackShift;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      valid[k] = i < p.n && len[k] != 0 && (off[k] & 3) == 0 && off[k] <= p.heap_size &&
+                 (uint64_t)len[k] <= p.heap_size - off[k];
+      npg[k] = valid[k] ? (uint32_t)(((off[k] & 4095) + len[k] + 4095) >> 12) : 0;
+      L[k] = npg[k] >= 3 ? (npg[k] - 2 + 510) / 511 : 0;  // ceil((list entries - 1) / 511)
+      v[k] = (uint64_t)L[k] | ((uint64_t)(L[k] ? 1 : 0) << 32);
+    }
+    tile_excl_scan(v, ex, tile_v, s_scan);
+    const uint64_t tile_L = tile_v & 0xFFFFFFFFull;
+    const uint32_t n_list = (uint32_t)(tile_v >> 32);
 
     // 3. First list page of this tile.
     if (threadIdx.x < 32) {
@@ -182,56 +298,68 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
     __syncthreads();
     const bool failed = s_failed != 0;
     any_failed |= failed;
-    const uint64_t pb = s_excl + (excl_pack & ((1u << kPackShift) - 1));
 
-    // 4. PRP1 / PRP2.
-    const bool ovf = L != 0 && pb + L > p.cap;
-    uint64_t prp1 = 0, prp2 = 0;
-    if (valid && !ovf && !failed) {
-      prp1 = bus(p.lut, off, pol_last);
-      if (npg == 2)
-        prp2 = bus(p.lut, (off & ~4095ull) + 4096, pol_last);
-      else if (npg >= 3)
-        prp2 = p.arena_base + (pb << 12);
-    }
-    if (in) {
-      st_stream16(p.prp + i, prp1, prp2, pol_first);
-      if (p.page_base) p.page_base[i] = pb;
-      if (p.status) p.status[i] = !valid ? DB_PRP_INVALID : (ovf ? DB_PRP_OVERFLOW : DB_PRP_OK);
-      my_invalid += !valid;
-      my_overflow += ovf;
-    }
-    if (L) {
-      ListItem it;
-      it.pb = pb;
-      it.hb = off & ~4095ull;
-      it.words = (npg - 1) + (L - 1);
-      it.pages = (ovf || failed) ? 0 : L;
-      s_list[excl_pack >> kPackShift] = it;
+    // 4. PRP1 / PRP2, page_base, status; queue the lists.
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      const uint64_t pb = s_excl + (ex[k] & 0xFFFFFFFFull);
+      const bool ovf = L[k] != 0 && pb + L[k] > p.cap;
+      uint64_t prp1 = 0, prp2 = 0;
+      if (valid[k] && !ovf && !failed) {
+        prp1 = bus(p.lut, off[k], pol_last);
+        if (npg[k] == 2)
+          prp2 = bus(p.lut, (off[k] & ~4095ull) + 4096, pol_last);
+        else if (npg[k] >= 3)
+          prp2 = p.arena_base + (pb << 12);
+      }
+      if (i < p.n) {
+        st_stream16(p.prp + i, prp1, prp2, pol_first);
+        if (p.page_base) p.page_base[i] = pb;
+        if (p.status)
+          p.status[i] = !valid[k] ? DB_PRP_INVALID : (ovf ? DB_PRP_OVERFLOW : DB_PRP_OK);
+        my_invalid += !valid[k];
+        my_overflow += ovf;
+      }
+      if (L[k])
+        s_list[ex[k] >> 32] = pack_item(off[k] & ~4095ull, (ovf || failed) ? 0 : L[k], pb, npg[k]);
     }
     if (tile + 1 == p.n_tiles && threadIdx.x == 0 && p.ctr && !failed)
       p.ctr->total = s_excl + tile_L;
     __syncthreads();
 
-    // 5. Lists: a warp takes the next queued request and writes its run.
-    for (;;) {
-      uint32_t j = 0;
-      if (lane == 0) j = atomicAdd(&s_next, 1u);
-      j = __shfl_sync(kFull, j, 0);
-      if (j >= n_list) break;
-      const ListItem it = s_list[j];
-      if (it.pages == 0) continue;
-      uint64_t* dst = p.arena + (it.pb << 9);
-      const uint32_t total = p.zero_tail ? (it.pages << 9) : it.words;
-      for (uint32_t w = 2 * lane; w < total; w += 64) {
-        const uint64_t v0 = list_word(p, it, w, pol_last);
-        if (w + 1 < total) {
-          const uint64_t v1 = list_word(p, it, w + 1, pol_last);
-          st_stream16(dst + w, v0, v1, pol_first);
-        } else {
-          st_stream8(dst + w, v0, pol_first);
+    // 5. Lists: a warp takes the next queued request and writes its run,
+    //    with the LUT window of the request after it already in flight.
+    uint32_t j = 0;
+    if (lane == 0) j = atomicAdd(&s_next, 1u);
+    j = __shfl_sync(kFull, j, 0);
+    ListItem it{};
+    uint64_t lutv = 0, wb = 0;
+    if (j < n_list) {
+      it = unpack_item(s_list[j]);
+      if (it.pages) {
+        wb = entry_chunk(it, 0);
+        lutv = lut_window(p.lut, wb, last_chunk(it), lane, pol_last);
+      }
+    }
+    while (j < n_list) {
+      uint32_t jn = 0;
+      if (lane == 0) jn = atomicAdd(&s_next, 1u);
+      jn = __shfl_sync(kFull, jn, 0);
+      ListItem nx{};
+      uint64_t nlutv = 0, nwb = 0;
+      if (jn < n_list) {
+        nx = unpack_item(s_list[jn]);
+        if (nx.pages) {
+          nwb = entry_chunk(nx, 0);
+          nlutv = lut_window(p.lut, nwb, last_chunk(nx), lane, pol_last);
         }
       }
+      if (it.pages) emit_list(p, it, lutv, wb, lane, pol_last, pol_first);
+      j = jn;
+      it = nx;
+      lutv = nlutv;
+      wb = nwb;
     }
     __syncthreads();
   }
@@ -293,7 +421,7 @@ using namespace db;
 extern "C" int db_prp_workspace_size(uint64_t n, size_t* bytes) {
   (void)n;
   if (!bytes) return -EINVAL;
-  if (n > (1ull << 29)) return -EINVAL;
+  if (n > (1ull << 28)) return -EINVAL;
   *bytes = prp::ws_bytes_for(n);
   return 0;
 }
@@ -304,7 +432,7 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
                             uint8_t* status, db_counters* ctr, uint32_t flags, void* ws,
                             size_t ws_bytes, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  if (n > (1ull << 29)) return -EINVAL;
+  if (n > (1ull << 28)) return -EINVAL;
   if (heap_size == 0 || heap_size % 65536 != 0) return -EINVAL;
   if (arena_base % 4096 != 0) return -EINVAL;
   if (arena_cap_pages > ((~0ull - arena_base) >> 12)) return -EINVAL;  // bus addresses must not wrap

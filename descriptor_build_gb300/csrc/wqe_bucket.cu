@@ -7,19 +7,19 @@
 // head[ring] + (valid puts of the same ring earlier in the batch).
 //
 // A ring asked for more than `depth` entries takes none of the batch, so the
-// per-ring totals must be known before any entry is written. Two launches:
-//   count    (persistent, tickets) per tile of 1024 puts: a shared-memory
-//            histogram over the rings (+1 bin for invalid puts), published
-//            as one status word per (tile, ring) and scanned across tiles by
-//            a decoupled lookback, one ring per thread. Each word ends as the
-//            tile's inclusive prefix, which is the next tile's exclusive one.
-//            The CTA of the last tile sees the totals: it writes count[],
-//            decides which rings overflow and advances head[] (old heads are
-//            kept in the workspace).
-//   scatter  per tile: stable rank of each put inside its warp with
+// per-ring totals must be known before any entry is written. Three launches,
+// reduce-then-scan:
+//   count    one CTA per tile of 1024 puts: a shared-memory histogram over
+//            the R rings plus one bin for invalid puts (warp-aggregated with
+//            __match_any_sync), written column-major: counts[ring][tile].
+//   scan     one CTA per ring: exclusive scan of its column in place, the
+//            ring's batch total, count[], the overflow decision, the head;
+//            the last CTA publishes the counters.
+//   scatter  one CTA per tile: stable rank of each put inside its warp with
 //            __match_any_sync, then across the tile's 32 warp-rows; WQEs are
 //            built into shared memory in ring order and each ring's run is
 //            written out contiguously with 16-byte stores.
+// No kernel waits on another CTA.
 #include "common.cuh"
 
 namespace db {
@@ -31,16 +31,23 @@ constexpr int kItems = 2;
 constexpr int kTile = kThreads * kItems;  // 1024 puts per tile
 constexpr int kUnits = kItems * kWarps;   // warp-rows of 32 puts, in batch order
 constexpr uint32_t kMaxRings = 1024;
+constexpr int kScanThreads = 256;
 
-// Workspace: ScanHeader (acc[0] posted, acc[1] invalid, acc[2] overflow;
-// aux = count pass failed), old heads [1024] u64, overflow flags [1024] u32,
-// then the status words [tiles][R + 1].
-constexpr size_t kHeadOldOff = kScanHeaderBytes;
+// Workspace: Header, old heads [1024] u64, overflow flags [1024] u32,
+// counts [R + 1][tiles] u32 (per-tile counts, then their exclusive prefixes).
+struct Header {
+  unsigned int done;           // scan CTAs finished in the current call
+  unsigned int pad;
+  unsigned long long posted;   // accumulators, zero between calls
+  unsigned long long invalid;
+  unsigned long long overflow;
+};
+constexpr size_t kHeadOldOff = 256;
 constexpr size_t kFullOff = kHeadOldOff + 8 * kMaxRings;
-constexpr size_t kStatusOff = kFullOff + 4 * kMaxRings;
+constexpr size_t kCountsOff = kFullOff + 4 * kMaxRings;
 inline uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
 inline size_t ws_bytes_for(uint64_t n, uint32_t R) {
-  return kStatusOff + ((tiles_for(n) * ((uint64_t)R + 1) * 8 + 255) & ~(uint64_t)255);
+  return kCountsOff + ((tiles_for(n) * ((uint64_t)R + 1) * 4 + 255) & ~(uint64_t)255);
 }
 
 struct Params {
@@ -58,11 +65,10 @@ struct Params {
   uint64_t* head;
   uint32_t* count;
   db_counters* ctr;
-  ScanHeader* hdr;
+  Header* hdr;
   uint64_t* head_old;
   uint32_t* full;
-  unsigned long long* status;  // [cap_words]
-  uint64_t cap_words;
+  uint32_t* counts;  // [V][n_tiles]
 };
 
 // Ring of a put, or R for an invalid one.
@@ -76,136 +82,81 @@ __device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) 
   return ok ? pe * p.n_qp + qp : p.R;
 }
 
-__device__ __forceinline__ uint64_t block_sum64(uint64_t v, uint64_t* s_red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum64(v);
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  uint64_t t = 0;
+// ---------------------------------------------------------------- count pass
+__global__ void __launch_bounds__(kThreads) wqe_count_kernel(const Params p) {
+  extern __shared__ uint32_t s_hist[];  // [V]
+  const uint32_t V = p.V;
+  const uint64_t tile = blockIdx.x;
+  const uint64_t pol_first = policy_evict_first();
+  for (uint32_t v = threadIdx.x; v < V; v += kThreads) s_hist[v] = 0;
+  uint32_t bin[kItems];
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += s_red[w];
+  for (int k = 0; k < kItems; ++k) {
+    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+    bin[k] = i < p.n ? bin_of(p, ld_stream16(p.req + i, pol_first)) : V;
+  }
   __syncthreads();
-  return t;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint32_t peers = __match_any_sync(kFull, bin[k]);
+    if (bin[k] < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin[k]], __popc(peers));
+  }
+  __syncthreads();
+  for (uint32_t v = threadIdx.x; v < V; v += kThreads) p.counts[v * p.n_tiles + tile] = s_hist[v];
 }
 
-// ---------------------------------------------------------------- count pass
-__global__ void __launch_bounds__(kThreads, 2) wqe_count_kernel(const Params p) {
-  extern __shared__ uint32_t s_hist[];  // [V]
-  __shared__ unsigned long long s_ticket;
-  __shared__ int s_failed;
+// ----------------------------------------------------------------- scan pass
+__global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) {
+  constexpr int kW = kScanThreads / 32;
+  __shared__ uint32_t s_scan[kW];
   __shared__ int s_last;
-  __shared__ uint64_t s_red[kWarps];
-
-  const uint64_t pol_first = policy_evict_first();
-  const uint32_t epoch = *(volatile unsigned int*)&p.hdr->epoch;
-  const uint32_t V = p.V;
-  bool any_failed = false;
-
-  for (;;) {
-    if (threadIdx.x == 0) {
-      s_ticket = atomicAdd(&p.hdr->ticket, 1ull);
-      s_failed = 0;
-    }
-    for (uint32_t v = threadIdx.x; v < V; v += kThreads) s_hist[v] = 0;
-    __syncthreads();
-    const uint64_t tile = s_ticket;
-    if (tile >= p.n_tiles) break;
-
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-      if (i < p.n) atomicAdd(&s_hist[bin_of(p, ld_stream16(p.req + i, pol_first))], 1u);
-    }
-    __syncthreads();
-
-    // Publish every aggregate before waiting on any predecessor.
-    unsigned long long* row = p.status + tile * V;
-    for (uint32_t v = threadIdx.x; v < V; v += kThreads)
-      st_release(row + v, status_word(tile == 0 ? kPrefix : kAggregate, epoch, s_hist[v]));
-    for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
-      const uint64_t agg = s_hist[v];
-      uint64_t excl = 0;
-      if (tile != 0) {
-        bool failed = false;
-        int64_t pos = (int64_t)tile - 1;
-        Backoff backoff;
-        while (pos >= 0) {
-          const uint64_t w = ld_acquire(p.status + (uint64_t)pos * V + v);
-          const uint32_t f = status_flag(w, epoch);
-          if (f == kEmpty) {
-            if (!backoff.wait()) {
-              failed = true;
-              break;
-            }
-            continue;
-          }
-          if (f == kFailed) {
-            failed = true;
-            break;
-          }
-          excl += w & kValueMask;
-          if (f == kPrefix) break;
-          --pos;
-        }
-        st_release(row + v, failed ? status_word(kFailed, epoch, 0)
-                                   : status_word(kPrefix, epoch, excl + agg));
-        if (failed) s_failed = 1;
-      }
-      if (tile + 1 == p.n_tiles) s_hist[v] = (uint32_t)(excl + agg);  // batch totals
-    }
-    __syncthreads();
-    const bool failed = s_failed != 0;
-    any_failed |= failed;
-
-    if (tile + 1 == p.n_tiles) {
-      // Totals are known: counts, overflow decision, heads.
-      uint64_t posted = 0, overflow = 0;
-      for (uint32_t r = threadIdx.x; r < p.R; r += kThreads) {
-        const uint64_t tot = s_hist[r];
-        const uint64_t h = p.head[r];
-        const bool over = tot > p.depth;
-        const bool skip = over || failed;
-        p.count[r] = (uint32_t)tot;
-        p.head_old[r] = h;
-        p.full[r] = skip ? 1u : 0u;
-        if (!skip) p.head[r] = h + tot;
-        posted += skip ? 0 : tot;
-        overflow += over ? tot : 0;
-      }
-      posted = block_sum64(posted, s_red);
-      overflow = block_sum64(overflow, s_red);
-      if (threadIdx.x == 0) {
-        p.hdr->acc[0] = posted;
-        p.hdr->acc[1] = s_hist[p.R];
-        p.hdr->acc[2] = overflow;
-        if (overflow) atomicOr(&p.hdr->err, DB_ERR_RING_OVERFLOW);
-      }
-    }
-    __syncthreads();
+  const uint32_t v = blockIdx.x;
+  uint32_t* col = p.counts + (uint64_t)v * p.n_tiles;
+  const uint64_t T = p.n_tiles;
+  const uint64_t chunk = (T + kScanThreads - 1) / kScanThreads;
+  const uint64_t r0 = threadIdx.x * chunk;
+  const uint64_t r1 = r0 + chunk < T ? r0 + chunk : T;
+  uint32_t mine = 0;
+  for (uint64_t r = r0; r < r1; ++r) mine += col[r];
+  uint32_t excl, total;
+  block_excl_scan<kW>(mine, excl, total, s_scan);
+  for (uint64_t r = r0; r < r1; ++r) {
+    const uint32_t c = col[r];
+    col[r] = excl;
+    excl += c;
   }
-
   if (threadIdx.x == 0) {
-    if (any_failed) atomicOr(&p.hdr->err, DB_ERR_TIMEOUT);
+    if (v < p.R) {
+      const uint64_t h = p.head[v];
+      const bool over = total > p.depth;
+      p.count[v] = total;
+      p.head_old[v] = h;
+      p.full[v] = over ? 1u : 0u;
+      if (!over) p.head[v] = h + total;
+      if (over)
+        atomicAdd(&p.hdr->overflow, (unsigned long long)total);
+      else if (total)
+        atomicAdd(&p.hdr->posted, (unsigned long long)total);
+    } else if (total) {
+      atomicAdd(&p.hdr->invalid, (unsigned long long)total);
+    }
     __threadfence();
     s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (s_last) {
+  if (s_last && threadIdx.x == 0) {
     __threadfence();
-    if (threadIdx.x == 0) {
-      const unsigned int err = atomicExch(&p.hdr->err, 0u);
-      const unsigned long long posted = atomicExch(&p.hdr->acc[0], 0ull);
-      const unsigned long long invalid = atomicExch(&p.hdr->acc[1], 0ull);
-      const unsigned long long overflow = atomicExch(&p.hdr->acc[2], 0ull);
-      p.hdr->aux = (err & DB_ERR_TIMEOUT) ? kAuxFailed : 0u;
-      if (p.ctr) {
-        p.ctr->total = (err & DB_ERR_TIMEOUT) ? 0 : posted;
-        p.ctr->n_invalid = invalid;
-        p.ctr->n_overflow = overflow;
-        p.ctr->err = err;
-      }
+    const unsigned long long posted = atomicExch(&p.hdr->posted, 0ull);
+    const unsigned long long invalid = atomicExch(&p.hdr->invalid, 0ull);
+    const unsigned long long overflow = atomicExch(&p.hdr->overflow, 0ull);
+    if (p.ctr) {
+      p.ctr->total = posted;
+      p.ctr->n_invalid = invalid;
+      p.ctr->n_overflow = overflow;
+      p.ctr->err = overflow ? DB_ERR_RING_OVERFLOW : 0u;
     }
-    end_of_call(p.hdr, p.status, p.n_tiles * V, p.cap_words, false);
+    p.hdr->done = 0;
+    __threadfence();
   }
 }
 
@@ -219,16 +170,9 @@ inline size_t scatter_smem(uint32_t V) {
   return (b + 15) & ~(size_t)15;
 }
 
-// The exclusive prefix of (tile, v) is the inclusive prefix the count pass
-// left in the status word of (tile - 1, v).
-__device__ __forceinline__ uint32_t tile_prefix(const Params& p, uint64_t tile, uint32_t v) {
-  if (tile == 0) return 0;
-  return (uint32_t)(p.status[(tile - 1) * p.V + v] & kValueMask);
-}
-
-// One tile: rank, stage in ring order, write out.
-__device__ __forceinline__ void scatter_tile(const Params& p, unsigned char* smem,
-                                             uint32_t* s_scan) {
+__global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ uint32_t s_scan[kWarps];
   const uint32_t V = p.V, R = p.R;
   ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);
   uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 64);
@@ -244,7 +188,7 @@ __device__ __forceinline__ void scatter_tile(const Params& p, unsigned char* sme
 
   for (uint32_t x = threadIdx.x; x < kUnits * V; x += kThreads) s_cnt[x] = 0;
   for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
-    s_pre[v] = tile_prefix(p, tile, v);
+    s_pre[v] = p.counts[v * p.n_tiles + tile];
     if (v < R) {
       s_head[v] = p.head_old[v];
       s_full[v] = p.full[v];
@@ -256,7 +200,7 @@ __device__ __forceinline__ void scatter_tile(const Params& p, unsigned char* sme
   for (int k = 0; k < kItems; ++k) {
     const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
     r[k] = make_ulonglong2(0, 0);
-    bin[k] = V;  // outside the tile: no bin
+    bin[k] = V;  // outside the batch: no bin
     if (i < p.n) {
       r[k] = ld_stream16(p.req + i, pol_first);
       bin[k] = bin_of(p, r[k]);
@@ -332,57 +276,16 @@ __device__ __forceinline__ void scatter_tile(const Params& p, unsigned char* sme
   }
 }
 
-
-__global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ uint32_t s_scan[kWarps];
-  __shared__ int s_last;
-  if (!(*(volatile unsigned int*)&p.hdr->aux & kAuxFailed)) scatter_tile(p, smem, s_scan);
-
-  // The last CTA performs a status clear that the count pass left pending.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (s_last) {
-    if (p.hdr->aux & kAuxClearPending) clear_status(p.hdr, p.status, p.cap_words);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      p.hdr->aux &= ~kAuxClearPending;
-      p.hdr->done = 0;
-    }
-    __threadfence();
-  }
-}
-
-int count_grid(uint64_t n_tiles, uint32_t V) {
-  static int per_sm[64][2] = {{0}};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int& occ = per_sm[dev & 63][V > 256 ? 1 : 0];
-  if (occ == 0) {
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, wqe_count_kernel, kThreads,
-                                                      (size_t)(kMaxRings + 1) * 4) != cudaSuccess ||
-        o < 1)
-      o = 1;
-    occ = o;
-  }
-  const uint64_t g = (uint64_t)num_sms() * (uint64_t)occ;
-  return (int)(n_tiles < g ? n_tiles : g);
-}
-
 // Allow the scatter kernel its largest shared-memory footprint (once per device).
 int prepare_scatter() {
   static bool done_for[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (!done_for[dev & 63]) {
-    if (cudaFuncSetAttribute(wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)scatter_smem(kMaxRings + 1)) != cudaSuccess)
-      return launch_result();
+    const cudaError_t e = cudaFuncSetAttribute(
+        wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)scatter_smem(kMaxRings + 1));
+    if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
   }
   return 0;
@@ -442,15 +345,17 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   p.head = head;
   p.count = count;
   p.ctr = ctr;
-  p.hdr = reinterpret_cast<ScanHeader*>(w);
+  p.hdr = reinterpret_cast<wqe::Header*>(w);
   p.head_old = reinterpret_cast<uint64_t*>(w + wqe::kHeadOldOff);
   p.full = reinterpret_cast<uint32_t*>(w + wqe::kFullOff);
-  p.status = reinterpret_cast<unsigned long long*>(w + wqe::kStatusOff);
-  p.cap_words = (ws_bytes - wqe::kStatusOff) / 8;
+  p.counts = reinterpret_cast<uint32_t*>(w + wqe::kCountsOff);
 
   int rc = wqe::prepare_scatter();
   if (rc) return rc;
-  wqe::wqe_count_kernel<<<wqe::count_grid(n_tiles, p.V), wqe::kThreads, (size_t)p.V * 4, s>>>(p);
+  wqe::wqe_count_kernel<<<(unsigned)n_tiles, wqe::kThreads, (size_t)p.V * 4, s>>>(p);
+  rc = launch_result();
+  if (rc) return rc;
+  wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
   wqe::wqe_scatter_kernel<<<(unsigned)n_tiles, wqe::kThreads, wqe::scatter_smem(p.V), s>>>(p);

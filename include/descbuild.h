@@ -152,7 +152,7 @@ typedef struct db_counters {
  *   flags            0 or DB_PRP_ZERO_TAIL
  * A request that is invalid or whose list does not fit gets prp = {0, 0}
  * and writes no list; one that does not fit still advances page_base.
- * Limits: n <= 2^29.
+ * Limits: n <= 2^28, arena_cap_pages <= 2^40.
  */
 int db_prp_workspace_size(uint64_t n, size_t* bytes);
 int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* lut, uint64_t heap_size,
@@ -240,7 +240,7 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
  * scratch memory (a header and one status word per tile of requests) is a
  * static device array inside libdescbuild.so, sized for at most
  * DB_PRP_STATIC_MAX_REQUESTS (16,777,216) requests per call: 256 B of header
- * plus 8 B per tile of 512 requests, 256.25 KiB in all. Every GPU that loads
+ * plus 8 B per tile of 2048 requests, 64.25 KiB in all. Every GPU that loads
  * the library holds that array until the process exits.
  *
  *  - n > DB_PRP_STATIC_MAX_REQUESTS returns -E2BIG before any GPU work.

@@ -54,18 +54,18 @@ def test_workspace_sizes(libpath):
     lib = ctypes.CDLL(libpath)
     out = ctypes.c_size_t()
     assert lib.db_prp_workspace_size(ctypes.c_uint64(4_194_304), ctypes.byref(out)) == 0
-    assert out.value >= 256 + 8 * (4_194_304 // 512)
+    assert out.value >= 256 + 8 * (4_194_304 // 2048)   # a status word per tile
     assert lib.db_mr_workspace_size(ctypes.c_uint64(1 << 20), ctypes.byref(out)) == 0
     assert out.value >= 32 * (1 << 20)
     assert lib.db_wqe_workspace_size(ctypes.c_uint64(8 << 20), ctypes.c_uint32(32),
                                      ctypes.byref(out)) == 0
-    assert out.value >= 8 * 33 * ((8 << 20) // 1024)
+    assert out.value >= 4 * 33 * ((8 << 20) // 1024)   # a count per (ring + invalid, tile)
     # out of range
     assert lib.db_wqe_workspace_size(ctypes.c_uint64(10), ctypes.c_uint32(0),
                                      ctypes.byref(out)) == -22
     assert lib.db_wqe_workspace_size(ctypes.c_uint64(10), ctypes.c_uint32(1025),
                                      ctypes.byref(out)) == -22
-    assert lib.db_prp_workspace_size(ctypes.c_uint64((1 << 29) + 1), ctypes.byref(out)) == -22
+    assert lib.db_prp_workspace_size(ctypes.c_uint64((1 << 28) + 1), ctypes.byref(out)) == -22
     assert lib.db_prp_workspace_size(ctypes.c_uint64(1), None) == -22
 
 

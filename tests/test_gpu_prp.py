@@ -189,7 +189,7 @@ def test_lookback_timeout_is_reported(db, oracle):
     rng = np.random.default_rng(5)
     heap = 16 * 1024 * 1024
     lut = synth.physical_lut(rng, heap // 65536)
-    req = random_batch(rng, 4 * 512, heap, 64 * 1024)
+    req = random_batch(rng, 4 * 2048, heap, 64 * 1024)   # four tiles of 2048 requests
     ws = db.workspace(db.prp_workspace_size(req.shape[0]))
     # The first 8 bytes of the workspace hold the next tile ticket, 0 between
     # calls. Starting at 1 means no CTA ever takes tile 0.

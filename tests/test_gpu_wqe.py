@@ -150,26 +150,6 @@ def test_bad_arguments(db):
         db.wqe_bucket(t, p, k, 8, 4, 0, 0, 1 << 20, rings, 8, head, cnt, ws[:256])
 
 
-def test_count_pass_timeout_is_reported(db, oracle):
-    """A predecessor tile that never publishes its counts: the bounded wait
-    gives up, DB_ERR_TIMEOUT is reported, no ring or head is touched, and the
-    workspace works again on the next call."""
-    rng = np.random.default_rng(8)
-    world, n_qp, depth, heap = 8, 4, 1024, 1 << 30
-    req = random_puts(rng, 4 * 1024, world, n_qp, heap)
-    peer = (rng.integers(1 << 19, 1 << 26, size=world) << 21).astype(np.uint64)
-    rkeys = rng.integers(0, 2**32, size=world, dtype=np.uint64).astype(np.uint32)
-    head = np.arange(32, dtype=np.uint64)
-    ws = db.workspace(db.wqe_workspace_size(req.shape[0], 32))
-    ws[:8].view(torch.int64).fill_(1)   # next tile ticket: tile 0 is never taken
-    got = run_gpu(db, req, peer, rkeys, world, n_qp, 0, 0, heap, depth, head, ws=ws)
-    assert int(got["ctr"][3]) & db.ERR_TIMEOUT
-    assert got["head"].tolist() == head.tolist()
-    assert (got["rings"].cpu().numpy() == 0xCD).all()
-    want = oracle.wqe_bucket(req, peer, rkeys, world, n_qp, 0, 0, heap, depth, head, fill=0xCD)
-    check(run_gpu(db, req, peer, rkeys, world, n_qp, 0, 0, heap, depth, head, ws=ws), want)
-
-
 def test_full_size_workload(db, oracle):
     """8,388,608 puts into 32 rings of 2^19 entries, every byte against the oracle."""
     import synth
