@@ -67,6 +67,20 @@ __device__ __forceinline__ void st_stream16(void* p, uint64_t a, uint64_t b, uin
                "l"(a), "l"(b), "l"(pol)
                : "memory");
 }
+// 32-byte store (sm_100+): p must be 32-byte aligned.
+__device__ __forceinline__ void st_stream32(void* p, uint64_t a, uint64_t b, uint64_t c, uint64_t d,
+                                            uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u64 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+               "l"(a), "l"(b), "l"(c), "l"(d), "l"(pol)
+               : "memory");
+}
+// 32-byte read-only load (sm_100+): p must be 32-byte aligned.
+__device__ __forceinline__ void ld_table32(const void* p, uint64_t pol, uint64_t& a, uint64_t& b,
+                                           uint64_t& c, uint64_t& d) {
+  asm("ld.global.nc.L2::cache_hint.v4.u64 {%0, %1, %2, %3}, [%4], %5;"
+      : "=l"(a), "=l"(b), "=l"(c), "=l"(d)
+      : "l"(p), "l"(pol));
+}
 __device__ __forceinline__ void st_stream8(void* p, uint64_t a, uint64_t pol) {
   asm volatile("st.global.L1::no_allocate.L2::cache_hint.u64 [%0], %1, %2;" ::"l"(p), "l"(a),
                "l"(pol)

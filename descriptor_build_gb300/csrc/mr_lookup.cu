@@ -11,11 +11,15 @@
 //                sector each), checks the table is sorted and disjoint, and
 //                fills a directory D[b] = number of records starting below
 //                lo + b * 2^shift (2^shift chosen so that the records' span
-//                fits nb buckets) by a merge path over records and buckets.
-//   lookup       kQPT queries per thread: round to pages, read D[b], D[b+1]
-//                (adjacent words), binary-search the few records of the
-//                bucket, read the one candidate record, classify. Queries of
-//                a thread advance in lockstep so their L2 misses overlap.
+//                fits nb buckets): each record fills the buckets between its
+//                predecessor's and its own; entry b also holds D[b+1] and the
+//                start of record D[b].
+//   lookup       persistent CTAs, 4 queries per thread per step: round to
+//                pages; one 16-byte directory entry gives D[b], D[b+1] and
+//                the start of record D[b], which decides the candidate when
+//                the bucket holds at most one record start (binary steps
+//                otherwise); read the candidate's 32-byte record and
+//                classify. The next step's queries load meanwhile.
 // For a sorted table of disjoint non-empty records the only record that can
 // contain [base, aend) is the last one starting at or below base, so the
 // lowest containing index is that record or none.
@@ -24,9 +28,24 @@
 namespace db {
 namespace mr {
 
+// Launch shape of the lookup (tunable at build time; the defaults are the
+// measured best on GB300): threads per CTA, queries per thread, minimum CTAs
+// per SM for the register budget, and log2 of buckets per record.
+#ifndef DB_MR_THREADS
+#define DB_MR_THREADS 256
+#endif
+#ifndef DB_MR_QPT
+#define DB_MR_QPT 4
+#endif
+#ifndef DB_MR_MIN_CTAS
+#define DB_MR_MIN_CTAS 4
+#endif
+#ifndef DB_MR_BUCKET_SHIFT
+#define DB_MR_BUCKET_SHIFT 0
+#endif
 constexpr int kBuildThreads = 256;
-constexpr int kThreads = 256;
-constexpr int kQPT = 4;
+constexpr int kThreads = DB_MR_THREADS;
+constexpr int kQPT = DB_MR_QPT;
 
 struct Header {        // first 256 bytes of the workspace
   uint64_t lo;         // start of record 0
@@ -46,12 +65,21 @@ constexpr size_t kHeaderBytes = 256;
 
 inline uint32_t buckets_for(uint64_t n_mr) {
   uint64_t nb = 1024;
-  while (nb < n_mr && nb < (1u << 22)) nb <<= 1;
+  while (nb < (n_mr << DB_MR_BUCKET_SHIFT) && nb < (1u << 22)) nb <<= 1;
   return (uint32_t)nb;
 }
-inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * 4 + 255) & ~(size_t)255; }
+// Directory entry of bucket b: the records starting below the bucket
+// (D[b]), the same count for bucket b + 1 (D[b+1]), and the start of record
+// D[b] -- one 16-byte load answers a bucket holding at most one record start.
+struct alignas(16) Dir {
+  uint32_t first;        // D[b]
+  uint32_t next;         // D[b + 1] (entry nb: n_mr)
+  uint64_t first_start;  // start of record D[b]; ~0 when D[b] == n_mr
+};
+inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * sizeof(Dir) + 255) & ~(size_t)255; }
 inline size_t ws_bytes_for(uint64_t n_mr) {
-  return kHeaderBytes + dir_bytes(buckets_for(n_mr)) + (size_t)n_mr * sizeof(Rec);
+  const uint32_t nb = buckets_for(n_mr);
+  return kHeaderBytes + dir_bytes(nb) + (size_t)n_mr * sizeof(Rec);
 }
 
 struct BuildParams {
@@ -60,7 +88,7 @@ struct BuildParams {
   const uint32_t* lkey;
   uint64_t n_mr;
   Header* hdr;
-  uint32_t* dir;
+  Dir* dir;  // [nb + 1]
   Rec* rec;
   uint32_t nb;
   uint32_t log_nb;
@@ -73,65 +101,71 @@ __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t 
   return b < nb ? b : nb;
 }
 
-constexpr int kMergeChunk = 32;  // merged elements per thread in the directory build
+// Records: 32-byte copies and the ordering check. Directory: D[b] = number
+// of records whose bucket key is below b, for b = 0..nb. Record i owns the
+// buckets (key(i-1), key(i)] (all with D = i); a short range is written by
+// its thread, a longer one (a wide gap before the record) by its whole warp.
+// The buckets after the last record's (D = n) are written by a grid-stride
+// loop of their own. Entry b also gets the start of record D[b] and entry
+// b - 1 its "next" count.
+__device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32_t x,
+                                        uint64_t x_start) {
+  p.dir[b].first = x;
+  p.dir[b].first_start = x_start;
+  if (b > 0) p.dir[b - 1].next = x;
+}
 
-// Records: 32-byte copies and the ordering check. Directory: D[b] = number of
-// records whose bucket key is below b, for b = 0..nb -- the merge of the
-// (sorted) record keys with the bucket numbers, split into equal chunks of
-// the merged sequence ("merge path"), so every thread does the same work
-// however the records fall into buckets.
 __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildParams p) {
   const uint64_t lo = p.start[0];
   const uint64_t hi = p.start[p.n_mr - 1];
   const uint64_t span = hi > lo ? hi - lo : 0;
   const uint32_t bits = span ? 64u - (uint32_t)__clzll((long long)span) : 0u;
   const uint32_t shift = bits > p.log_nb ? bits - p.log_nb : 0u;
-  const uint64_t nb = p.nb;
+  const uint64_t nb = p.nb, n = p.n_mr;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     p.hdr->lo = lo;
     p.hdr->shift = shift;
     p.hdr->nb = p.nb;
+    p.dir[nb].next = (uint32_t)n;
   }
-  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
+  const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint64_t n_round = (n + 31) & ~31ull;  // whole warps stay in the loop together
 
   bool bad = false;
-  for (uint64_t i = tid; i < p.n_mr; i += nthreads) {
-    const uint64_t s = p.start[i], e = p.end[i];
-    Rec r;
-    r.start = s;
-    r.end = e;
-    r.lkey = p.lkey[i];
-    r.pad0 = 0;
-    r.pad1 = 0;
-    p.rec[i] = r;
-    if (!(s < e) || (i > 0 && p.end[i - 1] > s)) bad = true;
+  for (uint64_t i = tid; i < n_round; i += nthreads) {
+    uint64_t b0 = 1, b1 = 0, s = 0;  // buckets [b0, b1] get D = i
+    if (i < n) {
+      s = p.start[i];
+      const uint64_t e = p.end[i];
+      Rec r;
+      r.start = s;
+      r.end = e;
+      r.lkey = p.lkey[i];
+      r.pad0 = 0;
+      r.pad1 = 0;
+      p.rec[i] = r;
+      if (!(s < e) || (i > 0 && p.end[i - 1] > s)) bad = true;
+      b0 = i == 0 ? 0 : bucket_of(p.start[i - 1], lo, shift, p.nb) + 1;
+      b1 = bucket_of(s, lo, shift, p.nb);
+    }
+    const bool wide = b1 >= b0 && b1 - b0 >= 32;
+    if (!wide)
+      for (uint64_t b = b0; b <= b1 && b1 >= b0; ++b) set_dir(p, b, (uint32_t)i, s);
+    uint32_t todo = __ballot_sync(kFull, wide);
+    while (todo) {
+      const int l = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const uint64_t wb0 = __shfl_sync(kFull, b0, l), wb1 = __shfl_sync(kFull, b1, l);
+      const uint64_t wi = __shfl_sync(kFull, i, l), ws = __shfl_sync(kFull, s, l);
+      for (uint64_t b = wb0 + lane; b <= wb1; b += 32) set_dir(p, b, (uint32_t)wi, ws);
+    }
   }
   if (bad) atomicOr(&p.hdr->err, DB_ERR_TABLE_ORDER);
-
-  // Merge order: record i comes before bucket number b iff key(i) < b.
-  const uint64_t n = p.n_mr;
-  const uint64_t merged = n + nb + 1;
-  for (uint64_t k = tid * kMergeChunk; k < merged; k += nthreads * kMergeChunk) {
-    // m = records among the first k merged elements: the largest m with
-    // key(m - 1) < k - m.
-    uint64_t mlo = k > nb + 1 ? k - (nb + 1) : 0;
-    uint64_t mhi = k < n ? k : n;
-    while (mlo < mhi) {
-      const uint64_t mid = (mlo + mhi + 1) >> 1;
-      if (bucket_of(p.start[mid - 1], lo, shift, p.nb) < k - mid)
-        mlo = mid;
-      else
-        mhi = mid - 1;
-    }
-    uint64_t i = mlo, b = k - mlo;
-    for (int step = 0; step < kMergeChunk && (i < n || b <= nb); ++step) {
-      if (i < n && (b > nb || bucket_of(p.start[i], lo, shift, p.nb) < b))
-        ++i;
-      else
-        p.dir[b++] = (uint32_t)i;
-    }
-  }
+  // Buckets after the last record's: D = n.
+  const uint64_t tail0 = bucket_of(hi, lo, shift, p.nb) + 1;
+  for (uint64_t b = tail0 + tid; b <= nb; b += nthreads) set_dir(p, b, (uint32_t)n, ~0ull);
 }
 
 struct LookupParams {
@@ -140,7 +174,7 @@ struct LookupParams {
   uint64_t n_mr;
   const Header* hdr_ro;
   Header* hdr;
-  const uint32_t* dir;
+  const Dir* dir;
   const Rec* rec;
   int32_t* idx;
   uint32_t* lkey;
@@ -148,100 +182,132 @@ struct LookupParams {
   db_counters* ctr;
 };
 
-__global__ void __launch_bounds__(kThreads) mr_lookup_kernel(const LookupParams p) {
+__global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(const LookupParams p) {
   const uint64_t pol_first = policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
   const uint64_t lo = p.hdr_ro->lo;
   const uint32_t shift = p.hdr_ro->shift;
   const uint32_t nb = p.hdr_ro->nb;
   const uint64_t n_mr = p.n_mr;
-  const uint64_t first = (uint64_t)blockIdx.x * (kThreads * kQPT) + threadIdx.x;
+  constexpr uint64_t kGroup = (uint64_t)kThreads * kQPT;  // queries per CTA step
+  const uint64_t n_groups = (p.n_q + kGroup - 1) / kGroup;
+  uint32_t hits = 0, invalid = 0;
 
-  uint64_t base[kQPT], aend[kQPT];
-  uint32_t a[kQPT], z[kQPT];
-  uint8_t state[kQPT];  // 0 done (miss), 1 searching, 2 invalid, 3 out of range
-  // Load and round.
+  // Persistent: CTAs stride over groups of queries; the next group's queries
+  // are loaded while the current group's table lookups are in flight.
+  ulonglong2 nq[kQPT];
+  uint64_t g = blockIdx.x;
 #pragma unroll
   for (int k = 0; k < kQPT; ++k) {
-    const uint64_t i = first + (uint64_t)k * kThreads;
-    state[k] = 3;
-    base[k] = 0;
-    aend[k] = 0;
-    if (i < p.n_q) {
-      const ulonglong2 r = ld_stream16(p.q + i, pol_first);
-      const uint64_t addr = r.x, size = r.y;
-      // valid iff size >= 1 and addr + size <= 2^64 - 4096 (the widened end fits)
-      constexpr uint64_t kTop = ~0ull - 4095ull;
-      const bool ok = size != 0 && size <= kTop && addr <= kTop - size;
-      if (!ok) {
-        state[k] = 2;
-      } else {
-        base[k] = addr & ~4095ull;
-        aend[k] = (addr + size + 4095ull) & ~4095ull;
-        state[k] = (n_mr == 0 || base[k] < lo) ? 0 : 1;
-      }
-    }
+    const uint64_t i = g * kGroup + (uint64_t)k * kThreads + threadIdx.x;
+    nq[k] = (g < n_groups && i < p.n_q) ? ld_stream16(p.q + i, pol_first) : make_ulonglong2(0, 0);
   }
-  // Directory: candidate records [a, z).
-#pragma unroll
-  for (int k = 0; k < kQPT; ++k) {
-    a[k] = 0;
-    z[k] = 0;
-    if (state[k] == 1) {
-      const uint64_t b = (base[k] - lo) >> shift;
-      if (b >= nb) {
-        a[k] = (uint32_t)n_mr;
-        z[k] = (uint32_t)n_mr;
-      } else {
-        uint32_t x = ld_table4(p.dir + b, pol_last), y = ld_table4(p.dir + b + 1, pol_last);
-        x = x < n_mr ? x : (uint32_t)n_mr;
-        y = y < n_mr ? y : (uint32_t)n_mr;
-        a[k] = x;
-        z[k] = y > x ? y : x;
-      }
-    }
-  }
-  // Binary search, all queries of the thread in lockstep: first record in
-  // [a, z) starting above base.
-  bool more = true;
-  while (more) {
-    more = false;
+  for (; g < n_groups; g += gridDim.x) {
+    const uint64_t first = g * kGroup + threadIdx.x;
+    uint64_t base[kQPT], aend[kQPT];
+    uint32_t a[kQPT], z[kQPT];
+    uint8_t state[kQPT];  // 0 miss, 1 searching, 2 invalid, 3 outside the batch
+    // Round.
 #pragma unroll
     for (int k = 0; k < kQPT; ++k) {
-      if (state[k] == 1 && a[k] < z[k]) {
-        const uint32_t mid = (a[k] + z[k]) >> 1;
-        const uint64_t s = ld_table8(&p.rec[mid].start, pol_last);
-        if (s <= base[k])
-          a[k] = mid + 1;
-        else
-          z[k] = mid;
-        more |= a[k] < z[k];
+      const uint64_t i = first + (uint64_t)k * kThreads;
+      state[k] = 3;
+      base[k] = 0;
+      aend[k] = 0;
+      if (i < p.n_q) {
+        const uint64_t addr = nq[k].x, size = nq[k].y;
+        // valid iff size >= 1 and addr + size <= 2^64 - 4096 (the widened end fits)
+        constexpr uint64_t kTop = ~0ull - 4095ull;
+        const bool ok = size != 0 && size <= kTop && addr <= kTop - size;
+        if (!ok) {
+          state[k] = 2;
+        } else {
+          base[k] = addr & ~4095ull;
+          aend[k] = (addr + size + 4095ull) & ~4095ull;
+          state[k] = (n_mr == 0 || base[k] < lo) ? 0 : 1;
+        }
       }
     }
-  }
-  // The candidate is record a - 1: the last one starting at or below base.
-  uint32_t hits = 0, invalid = 0;
+    // Directory: the number of records starting at or below base lies in
+    // [first, next]; first_start settles a bucket with one record start.
 #pragma unroll
-  for (int k = 0; k < kQPT; ++k) {
-    const uint64_t i = first + (uint64_t)k * kThreads;
-    if (state[k] == 3) continue;
-    int32_t out_idx = -1;
-    uint32_t out_lkey = 0;
-    uint8_t out_kind = state[k] == 2 ? DB_MR_INVALID : DB_MR_MISS;
-    invalid += state[k] == 2;
-    if (state[k] == 1 && a[k] > 0) {
-      const uint32_t j = a[k] - 1;
-      const ulonglong2 se = ld_table16(&p.rec[j], pol_last);
-      if (se.x <= base[k] && aend[k] <= se.y) {
-        out_idx = (int32_t)j;
-        out_lkey = ld_table4(&p.rec[j].lkey, pol_last);
-        out_kind = (se.x == base[k] && se.y == aend[k]) ? DB_MR_EXACT : DB_MR_CONTAINED;
-        hits += 1;
+    for (int k = 0; k < kQPT; ++k) {
+      a[k] = 0;
+      z[k] = 0;
+      if (state[k] == 1) {
+        const uint64_t b = (base[k] - lo) >> shift;
+        if (b >= nb) {
+          a[k] = (uint32_t)n_mr;
+          z[k] = (uint32_t)n_mr;
+        } else {
+          uint64_t w0, w1;
+          {
+            const ulonglong2 d = ld_table16(p.dir + b, pol_last);
+            w0 = d.x;
+            w1 = d.y;
+          }
+          uint32_t x = (uint32_t)w0, y = (uint32_t)(w0 >> 32);
+          x = x < n_mr ? x : (uint32_t)n_mr;
+          y = y < n_mr ? y : (uint32_t)n_mr;
+          y = y > x ? y : x;
+          if (x < y && w1 <= base[k])
+            ++x;    // record x starts at or below base
+          else
+            y = x;  // it does not (or there is none)
+          a[k] = x;
+          z[k] = y;
+        }
       }
     }
-    __stcs(p.idx + i, out_idx);
-    __stcs(reinterpret_cast<unsigned int*>(p.lkey + i), out_lkey);
-    __stcs(reinterpret_cast<unsigned char*>(p.kind + i), out_kind);
+    // Prefetch the next group's queries.
+    const uint64_t gn = g + gridDim.x;
+#pragma unroll
+    for (int k = 0; k < kQPT; ++k) {
+      const uint64_t i = gn * kGroup + (uint64_t)k * kThreads + threadIdx.x;
+      nq[k] = (gn < n_groups && i < p.n_q) ? ld_stream16(p.q + i, pol_first)
+                                            : make_ulonglong2(0, 0);
+    }
+    // Binary steps over any records still undecided (a bucket with two or
+    // more record starts; all queries of the thread in lockstep).
+    bool more = true;
+    while (more) {
+      more = false;
+#pragma unroll
+      for (int k = 0; k < kQPT; ++k) {
+        if (state[k] == 1 && a[k] < z[k]) {
+          const uint32_t mid = (a[k] + z[k]) >> 1;
+          if (ld_table8(&p.rec[mid].start, pol_last) <= base[k])
+            a[k] = mid + 1;
+          else
+            z[k] = mid;
+          more |= a[k] < z[k];
+        }
+      }
+    }
+    // The candidate is record a - 1: the last one starting at or below base.
+#pragma unroll
+    for (int k = 0; k < kQPT; ++k) {
+      const uint64_t i = first + (uint64_t)k * kThreads;
+      if (state[k] == 3) continue;
+      int32_t out_idx = -1;
+      uint32_t out_lkey = 0;
+      uint8_t out_kind = state[k] == 2 ? DB_MR_INVALID : DB_MR_MISS;
+      invalid += state[k] == 2;
+      if (state[k] == 1 && a[k] > 0) {
+        const uint32_t j = a[k] - 1;
+        uint64_t rs, re, rk, pad;
+        ld_table32(&p.rec[j], pol_last, rs, re, rk, pad);
+        if (rs <= base[k] && aend[k] <= re) {
+          out_idx = (int32_t)j;
+          out_lkey = (uint32_t)rk;
+          out_kind = (rs == base[k] && re == aend[k]) ? DB_MR_EXACT : DB_MR_CONTAINED;
+          hits += 1;
+        }
+      }
+      __stcs(p.idx + i, out_idx);
+      __stcs(reinterpret_cast<unsigned int*>(p.lkey + i), out_lkey);
+      __stcs(reinterpret_cast<unsigned char*>(p.kind + i), out_kind);
+    }
   }
   // Counters and hand-off to the next call.
   if (p.ctr) {
@@ -271,6 +337,22 @@ __global__ void __launch_bounds__(kThreads) mr_lookup_kernel(const LookupParams 
       __threadfence();
     }
   }
+}
+
+int lookup_ctas_per_sm() {
+  static int per_sm[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& occ = per_sm[dev & 63];
+  if (occ == 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, mr_lookup_kernel, kThreads, 0) !=
+            cudaSuccess ||
+        o < 1)
+      o = 1;
+    occ = o;
+  }
+  return occ;
 }
 
 }  // namespace mr
@@ -309,15 +391,13 @@ extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_
   while ((1u << log_nb) < nb) ++log_nb;
   char* w = static_cast<char*>(ws);
   mr::Header* hdr = reinterpret_cast<mr::Header*>(w);
-  uint32_t* dir = reinterpret_cast<uint32_t*>(w + mr::kHeaderBytes);
+  mr::Dir* dir = reinterpret_cast<mr::Dir*>(w + mr::kHeaderBytes);
   mr::Rec* rec = reinterpret_cast<mr::Rec*>(w + mr::kHeaderBytes + mr::dir_bytes(nb));
 
   if (n_mr > 0) {
     mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb};
-    const uint64_t merged = n_mr + nb + 1;
-    const uint64_t threads = (merged + mr::kMergeChunk - 1) / mr::kMergeChunk;
-    uint64_t grid = (threads + mr::kBuildThreads - 1) / mr::kBuildThreads;
-    const uint64_t cap = (uint64_t)num_sms() * 16;
+    uint64_t grid = (n_mr + mr::kBuildThreads - 1) / mr::kBuildThreads;
+    const uint64_t cap = (uint64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
     int rc = launch_result();
@@ -326,8 +406,9 @@ extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_
   mr::LookupParams l{reinterpret_cast<const ulonglong2*>(q), n_q, n_mr, hdr, hdr, dir, rec,
                      idx, lkey, kind, ctr};
   const uint64_t per_cta = (uint64_t)mr::kThreads * mr::kQPT;
-  const uint64_t grid = (n_q + per_cta - 1) / per_cta;
-  if (grid > 0x7FFFFFFFull) return -EINVAL;
+  uint64_t grid = (n_q + per_cta - 1) / per_cta;
+  const uint64_t resident = (uint64_t)num_sms() * mr::lookup_ctas_per_sm();
+  if (grid > resident) grid = resident;
   mr::mr_lookup_kernel<<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
   return launch_result();
 }

@@ -82,66 +82,156 @@ __device__ __forceinline__ uint64_t bus(const uint64_t* lut, uint64_t x, uint64_
   return ld_table8(lut + (x >> 16), pol) + (x & 0xFFFFull);
 }
 
-// LUT window of a warp: lane l holds lut[wb + l] (0 past the request's last
-// chunk). Issued as a volatile load so that it is not moved behind the stores
-// of the previous request (it is the prefetch of the next one).
-__device__ __forceinline__ uint64_t lut_window(const uint64_t* lut, uint64_t wb, uint64_t c_last,
-                                               int lane, uint64_t pol) {
+// LUT window of a warp: lane l holds lut[c0 + wrel + l] (0 past the
+// request's last chunk). Issued as a volatile load so that it is not moved
+// behind the stores of the previous request (it is the prefetch of the next).
+__device__ __forceinline__ uint64_t lut_window(const uint64_t* lut, uint64_t c, uint64_t c_last,
+                                               uint64_t pol) {
   uint64_t v = 0;
-  const uint64_t c = wb + (uint64_t)lane;
   if (c <= c_last)
     asm volatile("ld.global.nc.L2::cache_hint.u64 %0, [%1], %2;" : "=l"(v) : "l"(lut + c), "l"(pol));
   return v;
 }
 
-// Chunk (64 KiB LUT index) of data entry e (0-based): heap page hb + 4096 (e + 1).
-__device__ __forceinline__ uint64_t entry_chunk(const ListItem& it, uint32_t e) {
-  return (it.hb + ((uint64_t)(e + 1) << 12)) >> 16;
+// Page positions are counted from the start of the request's first 64 KiB
+// chunk c0: data entry e (0-based) names heap page hb + 4096 (e + 1), which
+// is page t = p0 + e + 1 of that count (p0 = position of hb in its chunk),
+// i.e. chunk c0 + (t >> 4) at offset (t & 15) * 4096.
+__device__ __forceinline__ uint32_t first_pos(const ListItem& it) {
+  return (uint32_t)((it.hb >> 12) & 15u);
 }
 __device__ __forceinline__ uint64_t last_chunk(const ListItem& it) {
-  return entry_chunk(it, it.words - (it.pages - 1) - 1);
+  const uint32_t m = it.words - (it.pages - 1);  // data entries
+  return (it.hb >> 16) + ((first_pos(it) + m) >> 4);
 }
 
-// Word w of a list (w < words): slot 511 of every page but the last points at
-// the next page; every other word is data entry e = w - (pointers before w),
-// the bus address of heap page hb + 4096 (e + 1). The LUT value comes from the
-// warp's window by shuffle, so all lanes execute this.
-__device__ __forceinline__ uint64_t list_word(const Params& p, const ListItem& it, uint32_t w,
-                                              uint64_t lutv, uint64_t wb) {
-  const uint32_t j = w >> 9;
-  const bool ptr = (w & 511u) == 511u && j + 1 < it.pages;
-  const uint64_t x = it.hb + ((uint64_t)(w - j + 1) << 12);
-  const int src = (int)(((x >> 16) - wb) & 31u);
-  const uint64_t base = __shfl_sync(kFull, lutv, src);
-  if (w >= it.words) return 0;  // zeroed tail
-  if (ptr) return p.arena_base + ((it.pb + j + 1) << 12);
-  return base + (x & 0xFFFFull);
+// Four consecutive data words of a lane, from the page position t of the
+// first: words s < 16 - (t & 15) lie in the chunk whose LUT value is
+// (hi_a, lo_a), the others in the next chunk (hi_b, lo_b). LUT values are
+// 64 KiB aligned, so adding the in-chunk offset to the low word never carries.
+__device__ __forceinline__ void four_words(uint32_t t, uint32_t lo_a, uint32_t hi_a, uint32_t lo_b,
+                                           uint32_t hi_b, uint64_t (&v)[4]) {
+  const uint32_t off0 = (t & 15u) << 12;
+  const uint32_t nsame = 16u - (t & 15u);
+  const uint32_t A = lo_a + off0, B = lo_b + off0 - 65536u;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const bool same = (uint32_t)s < nsame;
+    const uint32_t lo = (same ? A : B) + ((uint32_t)s << 12);
+    v[s] = ((uint64_t)(same ? hi_a : hi_b) << 32) | lo;
+  }
 }
 
-// One request's list run, written by a whole warp: 64 words per iteration as
-// 16-byte stores (a warp store covers 512 contiguous bytes). A 64-word step
-// spans at most 5 LUT chunks; the window moves when the next step could leave it.
-__device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, uint64_t lutv,
-                                          uint64_t wb, int lane, uint64_t pol_lut,
+// One long request's list run, written by a whole warp, 128 words per step:
+// lane l writes words 4l .. 4l+3 of the step with one 32-byte store, so a
+// warp store covers 1 KiB of contiguous arena. A step never leaves its 4 KiB
+// page (128 divides 512); the only chain-pointer slot a step can hold is word
+// 127 of the last step of a page. LUT values come by shuffle from two
+// windows of 32 chunks (lane l holds chunks c0 + wrel + l and c0 + wrel +
+// 32 + l); a step spans at most 9 chunks. Once a step lies wholly in the
+// second window the windows move on by 32 and the next 32 chunks are loaded,
+// about four steps before they are needed.
+__device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, uint64_t win0,
+                                          uint64_t win1, int lane, uint64_t pol_lut,
                                           uint64_t pol_out) {
   uint64_t* dst = p.arena + (it.pb << 9);
   const uint32_t total = p.zero_tail ? (it.pages << 9) : it.words;
+  const uint64_t c0 = it.hb >> 16;
   const uint64_t c_last = last_chunk(it);
-  for (uint32_t ib = 0; ib < total; ib += 64) {
-    if (ib < it.words) {
-      const uint64_t c_min = entry_chunk(it, ib - (ib >> 9));
-      if (c_min + 4 >= wb + 32) {
-        wb = c_min;
-        lutv = lut_window(p.lut, wb, c_last, lane, pol_lut);
+  const uint32_t p0 = first_pos(it);
+  uint32_t wrel = 0;
+  for (uint32_t ib = 0; ib < total; ib += 128) {
+    const uint32_t j = ib >> 9;                // list page of this step
+    const uint32_t t_min = p0 + 1 + ib - j;    // page position of the step's first word
+    if ((t_min >> 4) >= wrel + 32) {           // uniform across the warp
+      wrel += 32;
+      win0 = win1;
+      win1 = lut_window(p.lut, c0 + wrel + 32 + lane, c_last, pol_lut);
+    }
+    const uint32_t w = ib + 4 * lane;
+    const uint32_t t = t_min + 4 * lane;
+    const uint32_t ra = (t >> 4) - wrel, rb = ((t + 3) >> 4) - wrel;  // < 64
+    uint32_t lo_a, hi_a, lo_b, hi_b;
+    if (((t_min + 127) >> 4) < wrel + 32) {    // the step lies in the first window
+      lo_a = __shfl_sync(kFull, (uint32_t)win0, ra & 31);
+      hi_a = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ra & 31);
+      lo_b = __shfl_sync(kFull, (uint32_t)win0, rb & 31);
+      hi_b = __shfl_sync(kFull, (uint32_t)(win0 >> 32), rb & 31);
+    } else {                                   // it straddles the two windows
+      const uint32_t lo_a0 = __shfl_sync(kFull, (uint32_t)win0, ra & 31);
+      const uint32_t hi_a0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ra & 31);
+      const uint32_t lo_b0 = __shfl_sync(kFull, (uint32_t)win0, rb & 31);
+      const uint32_t hi_b0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), rb & 31);
+      const uint32_t lo_a1 = __shfl_sync(kFull, (uint32_t)win1, ra & 31);
+      const uint32_t hi_a1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), ra & 31);
+      const uint32_t lo_b1 = __shfl_sync(kFull, (uint32_t)win1, rb & 31);
+      const uint32_t hi_b1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), rb & 31);
+      lo_a = ra < 32 ? lo_a0 : lo_a1;
+      hi_a = ra < 32 ? hi_a0 : hi_a1;
+      lo_b = rb < 32 ? lo_b0 : lo_b1;
+      hi_b = rb < 32 ? hi_b0 : hi_b1;
+    }
+    uint64_t v[4];
+    four_words(t, lo_a, hi_a, lo_b, hi_b, v);
+    if (lane == 31 && (ib & 511u) == 384u && j + 1 < it.pages)
+      v[3] = p.arena_base + ((it.pb + j + 1) << 12);  // slot 511: next list page
+    if (ib + 128 <= it.words) {                       // a full step of data (uniform)
+      st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
+    } else {
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        if (w + s >= it.words) v[s] = 0;  // zeroed tail
+      if (w + 3 < total) {
+        st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (w + s < total) st_stream8(dst + w + s, v[s], pol_out);
       }
     }
-    const uint32_t w = ib + 2 * lane;
-    const uint64_t v0 = list_word(p, it, w, lutv, wb);
-    const uint64_t v1 = list_word(p, it, w + 1, lutv, wb);
-    if (w + 1 < total)
-      st_stream16(dst + w, v0, v1, pol_out);
-    else if (w < total)
-      st_stream8(dst + w, v0, pol_out);
+  }
+}
+
+// Short lists (at most kShortWords entries, one list page) are written by
+// 8-lane groups, four lists per warp step: lane g of a group writes words
+// 4g .. 4g+3 (one 32-byte store). Such a list touches at most 3 LUT chunks,
+// loaded by lanes 0..2 of the group. With zeroed tails every list fills its
+// whole page, 32 words per group step.
+constexpr uint32_t kShortWords = 32;
+__device__ __forceinline__ uint64_t short_window(const Params& p, const ListItem& it, bool valid,
+                                                 int lane, uint64_t pol_lut) {
+  return valid ? lut_window(p.lut, (it.hb >> 16) + (uint64_t)(lane & 7), last_chunk(it), pol_lut)
+               : 0;
+}
+__device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, bool valid,
+                                           uint64_t lutv, int lane, uint64_t pol_out) {
+  const int g = lane & 7, g0 = lane & ~7;
+  const uint32_t p0 = first_pos(it);
+  uint64_t* dst = p.arena + (it.pb << 9);
+  const uint32_t total = p.zero_tail ? 512u : it.words;
+  const uint32_t steps = p.zero_tail ? 16u : 1u;  // the same for every group of the warp
+  for (uint32_t st = 0; st < steps; ++st) {
+    const uint32_t w = st * 32 + 4 * g;
+    const uint32_t t = p0 + 1 + w;
+    const int sa = g0 + (int)((t >> 4) & 7u), sb = g0 + (int)(((t + 3) >> 4) & 7u);
+    const uint32_t lo_a = __shfl_sync(kFull, (uint32_t)lutv, sa);
+    const uint32_t hi_a = __shfl_sync(kFull, (uint32_t)(lutv >> 32), sa);
+    const uint32_t lo_b = __shfl_sync(kFull, (uint32_t)lutv, sb);
+    const uint32_t hi_b = __shfl_sync(kFull, (uint32_t)(lutv >> 32), sb);
+    uint64_t v[4];
+    four_words(t, lo_a, hi_a, lo_b, hi_b, v);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      if (w + s >= it.words) v[s] = 0;  // zeroed tail
+    if (valid) {
+      if (w + 3 < total) {
+        st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (w + s < total) st_stream8(dst + w + s, v[s], pol_out);
+      }
+    }
   }
 }
 
@@ -238,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
   __shared__ uint64_t s_scan[kItems * kWarps + 1];
   __shared__ unsigned long long s_excl;
   __shared__ int s_failed;
-  __shared__ uint32_t s_next;
+  __shared__ uint32_t s_next, s_next_short;
   __shared__ ulonglong2 s_list[kTile];
 
   const int lane = threadIdx.x & 31;
@@ -255,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
     if (tile >= p.n_tiles) break;
 
     // 1-2. Four requests per thread (rows of the tile): validity, pages
-    //      touched, list pages; scan of (list pages, has-a-list) in request order.
+    //      touched, list pages; one scan in request order of the list pages
+    //      (bits 0..22), short lists (bits 23..34) and long lists (35..46).
     uint64_t off[kItems];
     uint32_t len[kItems], npg[kItems], L[kItems];
     bool valid[kItems];
@@ -278,11 +369,14 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
                  (uint64_t)len[k] <= p.heap_size - off[k];
       npg[k] = valid[k] ? (uint32_t)(((off[k] & 4095) + len[k] + 4095) >> 12) : 0;
       L[k] = npg[k] >= 3 ? (npg[k] - 2 + 510) / 511 : 0;  // ceil((list entries - 1) / 511)
-      v[k] = (uint64_t)L[k] | ((uint64_t)(L[k] ? 1 : 0) << 32);
+      const bool is_short = L[k] != 0 && npg[k] - 1 <= kShortWords;  // then L = 1, words = n - 1
+      v[k] = (uint64_t)L[k] | ((uint64_t)(is_short ? 1 : 0) << 23) |
+             ((uint64_t)(L[k] != 0 && !is_short ? 1 : 0) << 35);
     }
     tile_excl_scan(v, ex, tile_v, s_scan);
-    const uint64_t tile_L = tile_v & 0xFFFFFFFFull;
-    const uint32_t n_list = (uint32_t)(tile_v >> 32);
+    const uint64_t tile_L = tile_v & ((1ull << 23) - 1);
+    const uint32_t n_short = (uint32_t)(tile_v >> 23) & 4095u;
+    const uint32_t n_long = (uint32_t)(tile_v >> 35) & 4095u;
 
     // 3. First list page of this tile.
     if (threadIdx.x < 32) {
@@ -293,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
         s_excl = excl;
         s_failed = failed;
         s_next = 0;
+        s_next_short = 0;
       }
     }
     __syncthreads();
@@ -303,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
       const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-      const uint64_t pb = s_excl + (ex[k] & 0xFFFFFFFFull);
+      const uint64_t pb = s_excl + (ex[k] & ((1ull << 23) - 1));
       const bool ovf = L[k] != 0 && pb + L[k] > p.cap;
       uint64_t prp1 = 0, prp2 = 0;
       if (valid[k] && !ovf && !failed) {
@@ -321,45 +416,82 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
         my_invalid += !valid[k];
         my_overflow += ovf;
       }
-      if (L[k])
-        s_list[ex[k] >> 32] = pack_item(off[k] & ~4095ull, (ovf || failed) ? 0 : L[k], pb, npg[k]);
+      if (L[k]) {  // long lists from the front of the queue, short ones from the back
+        const bool is_short = npg[k] - 1 <= kShortWords;
+        const uint32_t q = is_short ? kTile - 1 - ((uint32_t)(ex[k] >> 23) & 4095u)
+                                    : (uint32_t)(ex[k] >> 35) & 4095u;
+        s_list[q] = pack_item(off[k] & ~4095ull, (ovf || failed) ? 0 : L[k], pb, npg[k]);
+      }
     }
     if (tile + 1 == p.n_tiles && threadIdx.x == 0 && p.ctr && !failed)
       p.ctr->total = s_excl + tile_L;
     __syncthreads();
 
-    // 5. Lists: a warp takes the next queued request and writes its run,
-    //    with the LUT window of the request after it already in flight.
+    // 5. Lists. Long ones: a warp takes the next queued request and writes
+    //    its run, with the LUT window of the request after it already in
+    //    flight. Then short ones, four per warp.
     uint32_t j = 0;
     if (lane == 0) j = atomicAdd(&s_next, 1u);
     j = __shfl_sync(kFull, j, 0);
     ListItem it{};
-    uint64_t lutv = 0, wb = 0;
-    if (j < n_list) {
+    uint64_t win0 = 0, win1 = 0;
+    if (j < n_long) {
       it = unpack_item(s_list[j]);
       if (it.pages) {
-        wb = entry_chunk(it, 0);
-        lutv = lut_window(p.lut, wb, last_chunk(it), lane, pol_last);
+        win0 = lut_window(p.lut, (it.hb >> 16) + lane, last_chunk(it), pol_last);
+        win1 = lut_window(p.lut, (it.hb >> 16) + 32 + lane, last_chunk(it), pol_last);
       }
     }
-    while (j < n_list) {
+    while (j < n_long) {
       uint32_t jn = 0;
       if (lane == 0) jn = atomicAdd(&s_next, 1u);
       jn = __shfl_sync(kFull, jn, 0);
       ListItem nx{};
-      uint64_t nlutv = 0, nwb = 0;
-      if (jn < n_list) {
+      uint64_t nwin0 = 0, nwin1 = 0;
+      if (jn < n_long) {
         nx = unpack_item(s_list[jn]);
         if (nx.pages) {
-          nwb = entry_chunk(nx, 0);
-          nlutv = lut_window(p.lut, nwb, last_chunk(nx), lane, pol_last);
+          nwin0 = lut_window(p.lut, (nx.hb >> 16) + lane, last_chunk(nx), pol_last);
+          nwin1 = lut_window(p.lut, (nx.hb >> 16) + 32 + lane, last_chunk(nx), pol_last);
         }
       }
-      if (it.pages) emit_list(p, it, lutv, wb, lane, pol_last, pol_first);
+      if (it.pages) emit_list(p, it, win0, win1, lane, pol_last, pol_first);
       j = jn;
       it = nx;
-      lutv = nlutv;
-      wb = nwb;
+      win0 = nwin0;
+      win1 = nwin1;
+    }
+    // Short lists, four per warp step, the next four already loading.
+    uint32_t q0 = 0;
+    if (lane == 0) q0 = atomicAdd(&s_next_short, 4u);
+    q0 = __shfl_sync(kFull, q0, 0);
+    ListItem sh{};
+    bool sv = false;
+    uint64_t swin = 0;
+    if (q0 < n_short) {
+      const uint32_t q = q0 + (uint32_t)(lane >> 3);
+      if (q < n_short) sh = unpack_item(s_list[kTile - 1 - q]);
+      sv = q < n_short && sh.pages != 0;
+      swin = short_window(p, sh, sv, lane, pol_last);
+    }
+    while (q0 < n_short) {
+      uint32_t q1 = 0;
+      if (lane == 0) q1 = atomicAdd(&s_next_short, 4u);
+      q1 = __shfl_sync(kFull, q1, 0);
+      ListItem nsh{};
+      bool nsv = false;
+      uint64_t nswin = 0;
+      if (q1 < n_short) {
+        const uint32_t q = q1 + (uint32_t)(lane >> 3);
+        if (q < n_short) nsh = unpack_item(s_list[kTile - 1 - q]);
+        nsv = q < n_short && nsh.pages != 0;
+        nswin = short_window(p, nsh, nsv, lane, pol_last);
+      }
+      emit_short(p, sh, sv, swin, lane, pol_first);
+      q0 = q1;
+      sh = nsh;
+      sv = nsv;
+      swin = nswin;
     }
     __syncthreads();
   }
@@ -447,7 +579,7 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
   if (arena_cap_pages != 0 && !arena) return -EINVAL;
   if (!aligned(req, 16) || !aligned(prp, 16) || !aligned(lut, 8) || !aligned(ws, 256))
     return -EINVAL;
-  if (arena && !aligned(arena, 16)) return -EINVAL;
+  if (arena && !aligned(arena, 32)) return -EINVAL;
   if (page_base && !aligned(page_base, 8)) return -EINVAL;
   if (ws_bytes < prp::ws_bytes_for(n)) return -ENOSPC;
 

@@ -9,16 +9,19 @@
 // A ring asked for more than `depth` entries takes none of the batch, so the
 // per-ring totals must be known before any entry is written. Three launches,
 // reduce-then-scan:
-//   count    one CTA per tile of 1024 puts: a shared-memory histogram over
-//            the R rings plus one bin for invalid puts (warp-aggregated with
-//            __match_any_sync), written column-major: counts[ring][tile].
-//   scan     one CTA per ring: exclusive scan of its column in place, the
-//            ring's batch total, count[], the overflow decision, the head;
-//            the last CTA publishes the counters.
+//   count    warps stride over tiles of 1024 puts: a per-warp shared-memory
+//            histogram over the R rings plus one bin for invalid puts
+//            (aggregated with __match_any_sync), written column-major:
+//            counts[ring][tile].
+//   scan     one CTA per ring: exclusive scan of its column in place (staged
+//            through shared memory), the ring's batch total, count[], the
+//            overflow decision, the head; the last CTA publishes the counters.
 //   scatter  one CTA per tile: stable rank of each put inside its warp with
-//            __match_any_sync, then across the tile's 32 warp-rows; WQEs are
-//            built into shared memory in ring order and each ring's run is
-//            written out contiguously with 16-byte stores.
+//            __match_any_sync, then across the tile's 32 warp-rows (a warp
+//            scan per ring); the first 48 bytes of each WQE are built into
+//            shared memory in ring order (48-byte stride, conflict-free
+//            read-out) and each ring's run is written out contiguously with
+//            16-byte stores, the zero last quarter straight from registers.
 // No kernel waits on another CTA.
 #include "common.cuh"
 
@@ -31,7 +34,6 @@ constexpr int kItems = 2;
 constexpr int kTile = kThreads * kItems;  // 1024 puts per tile
 constexpr int kUnits = kItems * kWarps;   // warp-rows of 32 puts, in batch order
 constexpr uint32_t kMaxRings = 1024;
-constexpr int kScanThreads = 256;
 
 // Workspace: Header, old heads [1024] u64, overflow flags [1024] u32,
 // counts [R + 1][tiles] u32 (per-tile counts, then their exclusive prefixes).
@@ -83,53 +85,87 @@ __device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) 
 }
 
 // ---------------------------------------------------------------- count pass
-__global__ void __launch_bounds__(kThreads) wqe_count_kernel(const Params p) {
-  extern __shared__ uint32_t s_hist[];  // [V]
+// One warp counts a whole tile (32 rows of 32 puts) into its own shared
+// histogram; warps stride over tiles, so no block-wide barrier is needed.
+constexpr int kCountThreads = 256;
+constexpr int kCountWarps = kCountThreads / 32;
+constexpr int kCountUnroll = 4;  // rows of 32 puts loaded at once
+
+__global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
+  extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V]
   const uint32_t V = p.V;
-  const uint64_t tile = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t* s_hist = s_hist_all + (size_t)warp * V;
   const uint64_t pol_first = policy_evict_first();
-  for (uint32_t v = threadIdx.x; v < V; v += kThreads) s_hist[v] = 0;
-  uint32_t bin[kItems];
+  const uint64_t n_warps = (uint64_t)gridDim.x * kCountWarps;
+  for (uint64_t tile = (uint64_t)blockIdx.x * kCountWarps + warp; tile < p.n_tiles;
+       tile += n_warps) {
+    for (uint32_t v = lane; v < V; v += 32) s_hist[v] = 0;
+    __syncwarp();
+    for (int row = 0; row < kTile / 32; row += kCountUnroll) {
+      ulonglong2 r[kCountUnroll];
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-    bin[k] = i < p.n ? bin_of(p, ld_stream16(p.req + i, pol_first)) : V;
-  }
-  __syncthreads();
+      for (int u = 0; u < kCountUnroll; ++u) {
+        const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
+        r[u] = i < p.n ? ld_stream16(p.req + i, pol_first) : make_ulonglong2(0, 0);
+      }
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const uint32_t peers = __match_any_sync(kFull, bin[k]);
-    if (bin[k] < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin[k]], __popc(peers));
+      for (int u = 0; u < kCountUnroll; ++u) {
+        const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
+        const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
+        const uint32_t peers = __match_any_sync(kFull, bin);
+        if (bin < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+      }
+    }
+    __syncwarp();
+    for (uint32_t v = lane; v < V; v += 32) p.counts[v * p.n_tiles + tile] = s_hist[v];
+    __syncwarp();
   }
-  __syncthreads();
-  for (uint32_t v = threadIdx.x; v < V; v += kThreads) p.counts[v * p.n_tiles + tile] = s_hist[v];
 }
 
 // ----------------------------------------------------------------- scan pass
+constexpr int kScanThreads = 1024;
+constexpr int kScanSeg = 4 * kScanThreads;  // column entries staged per round
+
 __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) {
   constexpr int kW = kScanThreads / 32;
   __shared__ uint32_t s_scan[kW];
+  __shared__ uint32_t s_col[kScanSeg];
   __shared__ int s_last;
   const uint32_t v = blockIdx.x;
   uint32_t* col = p.counts + (uint64_t)v * p.n_tiles;
   const uint64_t T = p.n_tiles;
-  const uint64_t chunk = (T + kScanThreads - 1) / kScanThreads;
-  const uint64_t r0 = threadIdx.x * chunk;
-  const uint64_t r1 = r0 + chunk < T ? r0 + chunk : T;
-  uint32_t mine = 0;
-  for (uint64_t r = r0; r < r1; ++r) mine += col[r];
-  uint32_t excl, total;
-  block_excl_scan<kW>(mine, excl, total, s_scan);
-  for (uint64_t r = r0; r < r1; ++r) {
-    const uint32_t c = col[r];
-    col[r] = excl;
-    excl += c;
+  uint64_t carry = 0;
+  for (uint64_t s0 = 0; s0 < T; s0 += kScanSeg) {
+    const uint32_t len = (uint32_t)(T - s0 < (uint64_t)kScanSeg ? T - s0 : kScanSeg);
+    for (uint32_t x = threadIdx.x; x < len; x += kScanThreads) s_col[x] = col[s0 + x];
+    __syncthreads();
+    uint32_t c[4], mine = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t x = 4 * threadIdx.x + q;
+      c[q] = x < len ? s_col[x] : 0u;
+      mine += c[q];
+    }
+    uint32_t excl, seg_total;
+    block_excl_scan<kW>(mine, excl, seg_total, s_scan);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t x = 4 * threadIdx.x + q;
+      if (x < len) s_col[x] = (uint32_t)carry + excl;
+      excl += c[q];
+    }
+    __syncthreads();
+    for (uint32_t x = threadIdx.x; x < len; x += kScanThreads) col[s0 + x] = s_col[x];
+    carry += seg_total;
+    __syncthreads();
   }
+  const uint64_t total = carry;
   if (threadIdx.x == 0) {
     if (v < p.R) {
       const uint64_t h = p.head[v];
       const bool over = total > p.depth;
-      p.count[v] = total;
+      p.count[v] = (uint32_t)total;
       p.head_old[v] = h;
       p.full[v] = over ? 1u : 0u;
       if (!over) p.head[v] = h + total;
@@ -162,7 +198,7 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
 
 // -------------------------------------------------------------- scatter pass
 inline size_t scatter_smem(uint32_t V) {
-  size_t b = (size_t)kTile * 64;    // staged WQEs
+  size_t b = (size_t)kTile * 48;    // staged WQEs (bytes 48..63 are zero: not staged)
   b += (size_t)kTile * 8;           // destination of each staged WQE
   b += (size_t)V * 8;               // old heads
   b += (size_t)V * 4 * 4;           // run start, tile count, tile prefix, full flag
@@ -170,19 +206,19 @@ inline size_t scatter_smem(uint32_t V) {
   return (b + 15) & ~(size_t)15;
 }
 
-__global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 3) wqe_scatter_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ uint32_t s_scan[kWarps];
   const uint32_t V = p.V, R = p.R;
-  ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);
-  uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 64);
+  ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);  // WQE pos, part k at 3 pos + k
+  uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 48);
   uint64_t* s_head = s_dst + kTile;
   uint32_t* s_run = reinterpret_cast<uint32_t*>(s_head + V);
   uint32_t* s_tot = s_run + V;
   uint32_t* s_pre = s_tot + V;
   uint32_t* s_full = s_pre + V;
   uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_full + V);
-  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t tile = blockIdx.x;
   const uint64_t pol_first = policy_evict_first();
 
@@ -218,15 +254,18 @@ __global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
     if (bin[k] < V && before == 0) s_cnt[(k * kWarps + warp) * V + bin[k]] = (uint16_t)__popc(peers);
   }
   __syncthreads();
-  // Across warp-rows, in batch order.
-  for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
-    uint32_t run = 0;
-    for (int u = 0; u < kUnits; ++u) {
-      const uint32_t c = s_cnt[u * V + v];
-      s_cnt[u * V + v] = (uint16_t)run;
-      run += c;
+  // Across warp-rows, in batch order: one warp per ring, lane u = warp-row u.
+  static_assert(kUnits == 32, "one lane per warp-row");
+  for (uint32_t v = warp; v < V; v += kWarps) {
+    const uint32_t c = s_cnt[lane * V + v];
+    uint32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
     }
-    s_tot[v] = run;
+    s_cnt[lane * V + v] = (uint16_t)(x - c);
+    if (lane == 31) s_tot[v] = x;
   }
   __syncthreads();
   // Where each ring's run starts in the staging buffer (ring order; the
@@ -243,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
   }
   __syncthreads();
 
-  // Build the WQEs in ring order.
+  // Build the first 48 bytes of each WQE in ring order.
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const uint32_t v = bin[k];
@@ -257,10 +296,9 @@ __global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
     const uint32_t pe = (uint32_t)(r[k].y >> 32) & 0xFFFFu;
     const uint64_t raddr = __ldg(p.peer_ptrs + pe) + off;
     const uint32_t rkey = __ldg(p.rkeys + pe);
-    s_stage[pos * 4 + 0] = make_ulonglong2(raddr, p.local_base + off);
-    s_stage[pos * 4 + 1] = make_ulonglong2((uint64_t)bytes | ((uint64_t)p.lkey << 32), (uint64_t)rkey);
-    s_stage[pos * 4 + 2] = make_ulonglong2(seq, (uint64_t)(uint32_t)i);
-    s_stage[pos * 4 + 3] = make_ulonglong2(0, 0);
+    s_stage[pos * 3 + 0] = make_ulonglong2(raddr, p.local_base + off);
+    s_stage[pos * 3 + 1] = make_ulonglong2((uint64_t)bytes | ((uint64_t)p.lkey << 32), (uint64_t)rkey);
+    s_stage[pos * 3 + 2] = make_ulonglong2(seq, (uint64_t)(uint32_t)i);
     s_dst[pos] = s_full[v] ? 0ull
                            : (uint64_t)(p.rings + (((uint64_t)v * p.depth + (seq & (p.depth - 1))) << 6));
   }
@@ -268,10 +306,11 @@ __global__ void __launch_bounds__(kThreads) wqe_scatter_kernel(const Params p) {
 
   // Each ring's run is contiguous in the ring (up to one wrap): 16-byte stores.
   for (uint32_t f = threadIdx.x; f < n_staged * 4; f += kThreads) {
-    const uint64_t d = s_dst[f >> 2];
+    const uint32_t q = f >> 2, part = f & 3;
+    const uint64_t d = s_dst[q];
     if (d) {
-      const ulonglong2 x = s_stage[f];
-      st_stream16(reinterpret_cast<void*>(d + (f & 3) * 16), x.x, x.y, pol_first);
+      const ulonglong2 x = part < 3 ? s_stage[q * 3 + part] : make_ulonglong2(0, 0);
+      st_stream16(reinterpret_cast<void*>(d + part * 16), x.x, x.y, pol_first);
     }
   }
 }
@@ -352,7 +391,11 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
 
   int rc = wqe::prepare_scatter();
   if (rc) return rc;
-  wqe::wqe_count_kernel<<<(unsigned)n_tiles, wqe::kThreads, (size_t)p.V * 4, s>>>(p);
+  uint64_t count_grid = (uint64_t)num_sms() * 8;
+  const uint64_t count_need = (n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
+  if (count_grid > count_need) count_grid = count_need;
+  wqe::wqe_count_kernel<<<(unsigned)count_grid, wqe::kCountThreads,
+                          (size_t)wqe::kCountWarps * p.V * 4, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
   wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);

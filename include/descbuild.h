@@ -141,7 +141,7 @@ typedef struct db_counters {
  *   heap_size        bytes of device heap; a multiple of 65536
  *   arena_base       bus address of list page 0; a multiple of 4096
  *   arena_cap_pages  pages the arena holds
- *   arena            [arena_cap_pages][512] uint64: the arena's contents (16-byte aligned).
+ *   arena            [arena_cap_pages][512] uint64: the arena's contents (32-byte aligned).
  *                    Unused slots are left as they were unless DB_PRP_ZERO_TAIL.
  *   prp              [n] output (16-byte aligned)
  *   page_base        [n] output or NULL
