@@ -69,13 +69,19 @@ inline uint32_t buckets_for(uint64_t n_mr) {
   return (uint32_t)nb;
 }
 // Directory entry of bucket b: the records starting below the bucket
-// (D[b]), the same count for bucket b + 1 (D[b+1]), and the start of record
-// D[b] -- one 16-byte load answers a bucket holding at most one record start.
+// (D[b]), the same count for bucket b + 1 (D[b+1]), and where records D[b]
+// and D[b] + 1 start, as page offsets from the bucket's first page
+// (rounded up: a start s lies at or below a page-aligned base exactly when
+// ceil(s / 4096) <= base / 4096). One 16-byte load settles a bucket holding
+// at most two record starts.
 struct alignas(16) Dir {
-  uint32_t first;        // D[b]
-  uint32_t next;         // D[b + 1] (entry nb: n_mr)
-  uint64_t first_start;  // start of record D[b]; ~0 when D[b] == n_mr
+  uint32_t first;  // D[b]
+  uint32_t next;   // D[b + 1] (entry nb: n_mr)
+  uint32_t off1;   // page offset of record D[b]'s start (kNoOff if none or too far)
+  uint32_t off2;   // page offset of record D[b] + 1's start (kNoOff likewise)
 };
+constexpr uint32_t kNoOff = 0xFFFFFFFFu;
+constexpr uint32_t kMaxOffsetShift = 43;  // bucket widths up to 2^43 bytes keep offsets in 32 bits
 inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * sizeof(Dir) + 255) & ~(size_t)255; }
 inline size_t ws_bytes_for(uint64_t n_mr) {
   const uint32_t nb = buckets_for(n_mr);
@@ -108,10 +114,19 @@ __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t 
 // The buckets after the last record's (D = n) are written by a grid-stride
 // loop of their own. Entry b also gets the start of record D[b] and entry
 // b - 1 its "next" count.
-__device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32_t x,
-                                        uint64_t x_start) {
+__device__ __forceinline__ uint32_t page_offset(uint64_t s, uint64_t bpage0) {
+  const uint64_t sp = (s >> 12) + ((s & 4095u) ? 1 : 0);  // ceil(s / 4096), s < 2^64
+  const uint64_t d = sp - bpage0;
+  return d < kNoOff ? (uint32_t)d : kNoOff;
+}
+__device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32_t x, uint64_t s1,
+                                        uint64_t s2, bool have1, bool have2, uint64_t lo,
+                                        uint32_t shift) {
+  const uint64_t bpage0 = (lo + (b << shift)) >> 12;
+  const bool offs = shift <= kMaxOffsetShift;
   p.dir[b].first = x;
-  p.dir[b].first_start = x_start;
+  p.dir[b].off1 = (offs && have1) ? page_offset(s1, bpage0) : kNoOff;
+  p.dir[b].off2 = (offs && have2) ? page_offset(s2, bpage0) : kNoOff;
   if (b > 0) p.dir[b - 1].next = x;
 }
 
@@ -135,9 +150,10 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
 
   bool bad = false;
   for (uint64_t i = tid; i < n_round; i += nthreads) {
-    uint64_t b0 = 1, b1 = 0, s = 0;  // buckets [b0, b1] get D = i
+    uint64_t b0 = 1, b1 = 0, s = 0, s_next = 0;  // buckets [b0, b1] get D = i
     if (i < n) {
       s = p.start[i];
+      s_next = i + 1 < n ? p.start[i + 1] : 0;
       const uint64_t e = p.end[i];
       Rec r;
       r.start = s;
@@ -151,21 +167,27 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
       b1 = bucket_of(s, lo, shift, p.nb);
     }
     const bool wide = b1 >= b0 && b1 - b0 >= 32;
+    const bool has_next = i + 1 < n;
     if (!wide)
-      for (uint64_t b = b0; b <= b1 && b1 >= b0; ++b) set_dir(p, b, (uint32_t)i, s);
+      for (uint64_t b = b0; b <= b1 && b1 >= b0; ++b)
+        set_dir(p, b, (uint32_t)i, s, s_next, true, has_next, lo, shift);
     uint32_t todo = __ballot_sync(kFull, wide);
     while (todo) {
       const int l = __ffs(todo) - 1;
       todo &= todo - 1;
       const uint64_t wb0 = __shfl_sync(kFull, b0, l), wb1 = __shfl_sync(kFull, b1, l);
       const uint64_t wi = __shfl_sync(kFull, i, l), ws = __shfl_sync(kFull, s, l);
-      for (uint64_t b = wb0 + lane; b <= wb1; b += 32) set_dir(p, b, (uint32_t)wi, ws);
+      const uint64_t wsn = __shfl_sync(kFull, s_next, l);
+      const bool whn = __shfl_sync(kFull, has_next, l);
+      for (uint64_t b = wb0 + lane; b <= wb1; b += 32)
+        set_dir(p, b, (uint32_t)wi, ws, wsn, true, whn, lo, shift);
     }
   }
   if (bad) atomicOr(&p.hdr->err, DB_ERR_TABLE_ORDER);
   // Buckets after the last record's: D = n.
   const uint64_t tail0 = bucket_of(hi, lo, shift, p.nb) + 1;
-  for (uint64_t b = tail0 + tid; b <= nb; b += nthreads) set_dir(p, b, (uint32_t)n, ~0ull);
+  for (uint64_t b = tail0 + tid; b <= nb; b += nthreads)
+    set_dir(p, b, (uint32_t)n, 0, 0, false, false, lo, shift);
 }
 
 struct LookupParams {
@@ -229,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
       }
     }
     // Directory: the number of records starting at or below base lies in
-    // [first, next]; first_start settles a bucket with one record start.
+    // [first, next]; the two start offsets settle up to two of them.
 #pragma unroll
     for (int k = 0; k < kQPT; ++k) {
       a[k] = 0;
@@ -240,20 +262,24 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
           a[k] = (uint32_t)n_mr;
           z[k] = (uint32_t)n_mr;
         } else {
-          uint64_t w0, w1;
-          {
-            const ulonglong2 d = ld_table16(p.dir + b, pol_last);
-            w0 = d.x;
-            w1 = d.y;
-          }
-          uint32_t x = (uint32_t)w0, y = (uint32_t)(w0 >> 32);
+          const ulonglong2 d = ld_table16(p.dir + b, pol_last);
+          uint32_t x = (uint32_t)d.x, y = (uint32_t)(d.x >> 32);
+          const uint32_t off1 = (uint32_t)d.y, off2 = (uint32_t)(d.y >> 32);
           x = x < n_mr ? x : (uint32_t)n_mr;
           y = y < n_mr ? y : (uint32_t)n_mr;
           y = y > x ? y : x;
-          if (x < y && w1 <= base[k])
-            ++x;    // record x starts at or below base
-          else
-            y = x;  // it does not (or there is none)
+          const uint64_t bo = (base[k] >> 12) - ((lo + (b << shift)) >> 12);  // base's page offset
+          if (x < y && off1 != kNoOff) {
+            if (bo < off1) {
+              y = x;                    // record x starts above base
+            } else if (x + 1 < y && off2 != kNoOff) {
+              if (bo < off2) { ++x; y = x; }            // x starts at or below, x + 1 above
+              else { x += 2; }                          // both at or below: search the rest
+            } else {
+              ++x;                      // record x starts at or below base
+              if (x + 1 > y) y = x;
+            }
+          }
           a[k] = x;
           z[k] = y;
         }

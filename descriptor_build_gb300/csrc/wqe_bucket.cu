@@ -10,13 +10,13 @@
 // per-ring totals must be known before any entry is written. Three launches,
 // reduce-then-scan:
 //   count    warps stride over tiles of 1024 puts: a per-warp shared-memory
-//            histogram over the R rings plus one bin for invalid puts
-//            (aggregated with __match_any_sync), written column-major:
-//            counts[ring][tile].
+//            histogram over the R rings plus one bin for invalid puts,
+//            written column-major: counts[ring][tile].
 //   scan     one CTA per ring: exclusive scan of its column in place (staged
 //            through shared memory), the ring's batch total, count[], the
 //            overflow decision, the head; the last CTA publishes the counters.
-//   scatter  one CTA per tile: stable rank of each put inside its warp with
+//   scatter  persistent CTAs, a tile at a time (the next tile's puts load
+//            meanwhile): stable rank of each put inside its warp with
 //            __match_any_sync, then across the tile's 32 warp-rows (a warp
 //            scan per ring); the first 48 bytes of each WQE are built into
 //            shared memory in ring order (48-byte stride, conflict-free
@@ -34,6 +34,17 @@ constexpr int kItems = 2;
 constexpr int kTile = kThreads * kItems;  // 1024 puts per tile
 constexpr int kUnits = kItems * kWarps;   // warp-rows of 32 puts, in batch order
 constexpr uint32_t kMaxRings = 1024;
+
+// Build-time tuning (defaults measured best on GB300): how the count pass
+// histograms a row of 32 puts (0: __match_any_sync + one shared atomic per
+// distinct ring, 1: one shared atomic per put), and whether the scatter pass
+// runs persistent CTAs (3 per SM) that load their next tile early.
+#ifndef DB_WQE_COUNT_MODE
+#define DB_WQE_COUNT_MODE 1
+#endif
+#ifndef DB_WQE_SCATTER_PERSIST
+#define DB_WQE_SCATTER_PERSIST 1
+#endif
 
 // Workspace: Header, old heads [1024] u64, overflow flags [1024] u32,
 // counts [R + 1][tiles] u32 (per-tile counts, then their exclusive prefixes).
@@ -113,8 +124,12 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
       for (int u = 0; u < kCountUnroll; ++u) {
         const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
         const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
-        const uint32_t peers = __match_any_sync(kFull, bin);
-        if (bin < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+        if (DB_WQE_COUNT_MODE == 1) {
+          if (bin < V) atomicAdd(&s_hist[bin], 1u);
+        } else {
+          const uint32_t peers = __match_any_sync(kFull, bin);
+          if (bin < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+        }
       }
     }
     __syncwarp();
@@ -206,9 +221,37 @@ inline size_t scatter_smem(uint32_t V) {
   return (b + 15) & ~(size_t)15;
 }
 
+__device__ __forceinline__ void scatter_tile(const Params& p, uint64_t tile, const ulonglong2 (&r)[kItems],
+                                             unsigned char* smem, uint32_t* s_scan);
+
 __global__ void __launch_bounds__(kThreads, 3) wqe_scatter_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ uint32_t s_scan[kWarps];
+  const uint64_t pol_first = policy_evict_first();
+  auto load = [&](uint64_t tile, ulonglong2 (&r)[kItems]) {
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      r[k] = (tile < p.n_tiles && i < p.n) ? ld_stream16(p.req + i, pol_first)
+                                             : make_ulonglong2(0, 0);
+    }
+  };
+  ulonglong2 cur[kItems];
+  load(blockIdx.x, cur);
+  const uint64_t stride = DB_WQE_SCATTER_PERSIST ? gridDim.x : p.n_tiles;
+  for (uint64_t tile = blockIdx.x; tile < p.n_tiles; tile += stride) {
+    ulonglong2 nxt[kItems];
+    if (DB_WQE_SCATTER_PERSIST) load(tile + stride, nxt);
+    scatter_tile(p, tile, cur, smem, s_scan);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) cur[k] = DB_WQE_SCATTER_PERSIST ? nxt[k] : cur[k];
+  }
+}
+
+__device__ __forceinline__ void scatter_tile(const Params& p, uint64_t tile,
+                                             const ulonglong2 (&rin)[kItems], unsigned char* smem,
+                                             uint32_t* s_scan) {
   const uint32_t V = p.V, R = p.R;
   ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);  // WQE pos, part k at 3 pos + k
   uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 48);
@@ -219,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 3) wqe_scatter_kernel(const Params p
   uint32_t* s_full = s_pre + V;
   uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_full + V);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint64_t tile = blockIdx.x;
   const uint64_t pol_first = policy_evict_first();
 
   for (uint32_t x = threadIdx.x; x < kUnits * V; x += kThreads) s_cnt[x] = 0;
@@ -235,12 +277,8 @@ __global__ void __launch_bounds__(kThreads, 3) wqe_scatter_kernel(const Params p
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-    r[k] = make_ulonglong2(0, 0);
-    bin[k] = V;  // outside the batch: no bin
-    if (i < p.n) {
-      r[k] = ld_stream16(p.req + i, pol_first);
-      bin[k] = bin_of(p, r[k]);
-    }
+    r[k] = rin[k];
+    bin[k] = i < p.n ? bin_of(p, r[k]) : V;  // outside the batch: no bin
   }
   __syncthreads();
 
@@ -401,6 +439,9 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
-  wqe::wqe_scatter_kernel<<<(unsigned)n_tiles, wqe::kThreads, wqe::scatter_smem(p.V), s>>>(p);
+  uint64_t scatter_grid = n_tiles;
+  if (DB_WQE_SCATTER_PERSIST && scatter_grid > (uint64_t)num_sms() * 3)
+    scatter_grid = (uint64_t)num_sms() * 3;
+  wqe::wqe_scatter_kernel<<<(unsigned)scatter_grid, wqe::kThreads, wqe::scatter_smem(p.V), s>>>(p);
   return launch_result();
 }
