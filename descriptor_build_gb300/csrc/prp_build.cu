@@ -23,14 +23,32 @@
 namespace db {
 namespace prp {
 
-constexpr int kThreads = 512;
+// Build-time tuning: gather the PRP1/PRP2 LUT entries before the tile's
+// scan and lookback (1) or after them (0).
+#ifndef DB_PRP_EARLY_LUT
+#define DB_PRP_EARLY_LUT 0
+#endif
+
+// Tile shape (tunable at build time; defaults measured best on GB300):
+// threads per CTA, requests per thread, minimum resident CTAs per SM.
+#ifndef DB_PRP_THREADS
+#define DB_PRP_THREADS 512
+#endif
+#ifndef DB_PRP_ITEMS
+#define DB_PRP_ITEMS 4
+#endif
+#ifndef DB_PRP_MIN_CTAS
+#define DB_PRP_MIN_CTAS 2
+#endif
+constexpr int kThreads = DB_PRP_THREADS;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 4;                  // requests per thread per tile
-constexpr int kTile = kThreads * kItems;   // 2048 requests per tile
+constexpr int kItems = DB_PRP_ITEMS;       // requests per thread per tile
+constexpr int kTile = kThreads * kItems;   // requests per tile
 
 // Workspace: ScanHeader (acc[0] invalid, acc[1] overflow), then one status
 // word per tile.
 constexpr uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
+constexpr uint64_t kMaxRequests = 1ull << 28;
 constexpr size_t ws_bytes_for(uint64_t n) {
   return kScanHeaderBytes + ((tiles_for(n) * 8 + 255) & ~(uint64_t)255);
 }
@@ -240,7 +258,7 @@ __device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, 
 // kItems * kWarps values.
 __device__ __forceinline__ void tile_excl_scan(const uint64_t (&v)[kItems], uint64_t (&excl)[kItems],
                                                uint64_t& total, uint64_t* s_scan) {
-  static_assert(kItems * kWarps == 64, "two scan totals per lane");
+  static_assert(kItems * kWarps <= 64, "at most two scan totals per lane");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t x[kItems];
 #pragma unroll
@@ -255,7 +273,8 @@ __device__ __forceinline__ void tile_excl_scan(const uint64_t (&v)[kItems], uint
   }
   __syncthreads();
   if (warp == 0) {
-    const uint64_t a = s_scan[2 * lane], b = s_scan[2 * lane + 1];
+    const uint64_t a = 2 * lane < kItems * kWarps ? s_scan[2 * lane] : 0;
+    const uint64_t b = 2 * lane + 1 < kItems * kWarps ? s_scan[2 * lane + 1] : 0;
     uint64_t t = a + b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -263,19 +282,20 @@ __device__ __forceinline__ void tile_excl_scan(const uint64_t (&v)[kItems], uint
       if (lane >= o) t += y;
     }
     const uint64_t before = t - a - b;
-    s_scan[2 * lane] = before;
-    s_scan[2 * lane + 1] = before + a;
-    if (lane == 31) s_scan[64] = t;
+    if (2 * lane < kItems * kWarps) s_scan[2 * lane] = before;
+    if (2 * lane + 1 < kItems * kWarps) s_scan[2 * lane + 1] = before + a;
+    if (lane == 31) s_scan[kItems * kWarps] = t;
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < kItems; ++k) excl[k] = s_scan[k * kWarps + warp] + x[k] - v[k];
-  total = s_scan[64];
+  total = s_scan[kItems * kWarps];
 }
 
 // Decoupled lookback for tile t (warp 0 only). Publishes the tile's
-// aggregate, then sums predecessors 32 at a time until an inclusive prefix
-// (or the start of the batch) is found, then publishes its own prefix.
+// aggregate, then sums predecessors 128 at a time (4 per lane, nearest
+// first) until an inclusive prefix (or the start of the batch) is found,
+// then publishes its own prefix.
 __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t epoch, uint64_t agg,
                                          uint64_t& excl_out, bool& failed) {
   const int lane = threadIdx.x & 31;
@@ -291,31 +311,47 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
   int64_t top = (int64_t)t - 1;  // newest tile of the window
   Backoff backoff;
   while (true) {
-    const int64_t u = top - lane;
-    uint32_t flag = kPrefix;  // before tile 0: an inclusive prefix of 0
-    uint64_t val = 0;
-    if (u >= 0) {
-      const uint64_t w = ld_acquire(p.tile_status + u);
-      flag = status_flag(w, epoch);
-      val = w & kValueMask;
+    // This lane's four tiles, nearest first: top - 4 lane - s.
+    uint32_t stop_s = 4;           // first of them holding a prefix (or a failure)
+    bool empty_before = false;     // an unpublished tile before that
+    bool stop_failed = false;
+    uint64_t sum = 0;              // values up to and including the stop
+#pragma unroll
+    for (int sidx = 0; sidx < 4; ++sidx) {
+      const int64_t u = top - 4 * lane - sidx;
+      uint32_t flag = kPrefix;     // before tile 0: an inclusive prefix of 0
+      uint64_t val = 0;
+      if (u >= 0) {
+        const uint64_t w = ld_acquire(p.tile_status + u);
+        flag = status_flag(w, epoch);
+        val = w & kValueMask;
+      }
+      if (stop_s == 4) {
+        if (flag == kEmpty) empty_before = true;
+        sum += val;
+        if (flag == kPrefix || flag == kFailed) {
+          stop_s = (uint32_t)sidx;
+          stop_failed = flag == kFailed;
+        }
+      }
     }
-    const uint32_t stop_mask = __ballot_sync(kFull, flag == kPrefix || flag == kFailed);
-    const int stop = stop_mask ? __ffs(stop_mask) - 1 : 31;
-    const uint32_t upto = stop == 31 ? kFull : ((2u << stop) - 1u);
-    if (__ballot_sync(kFull, flag == kEmpty) & upto) {
+    const uint32_t stop_mask = __ballot_sync(kFull, stop_s < 4);
+    const int stop_lane = stop_mask ? __ffs(stop_mask) - 1 : 31;
+    const bool counts = lane <= stop_lane;
+    if (__ballot_sync(kFull, counts && empty_before)) {
       if (!backoff.wait()) {
         failed = true;
         break;
       }
       continue;
     }
-    if (__ballot_sync(kFull, flag == kFailed) & upto) {
+    if (__shfl_sync(kFull, stop_failed ? 1 : 0, stop_lane) && stop_mask) {
       failed = true;
       break;
     }
-    excl += warp_sum64(lane <= stop ? val : 0);
+    excl += warp_sum64(counts ? sum : 0);
     if (stop_mask) break;
-    top -= 32;
+    top -= 128;
   }
   if (lane == 0)
     st_release(mine, failed ? status_word(kFailed, epoch, 0)
@@ -323,7 +359,7 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
   excl_out = excl;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(const Params p) {
   __shared__ unsigned long long s_ticket;
   __shared__ uint64_t s_scan[kItems * kWarps + 1];
   __shared__ unsigned long long s_excl;
@@ -373,6 +409,16 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
       v[k] = (uint64_t)L[k] | ((uint64_t)(is_short ? 1 : 0) << 23) |
              ((uint64_t)(L[k] != 0 && !is_short ? 1 : 0) << 35);
     }
+    // The PRP1 / PRP2 gathers do not depend on the scan: optionally start
+    // them before it (DB_PRP_EARLY_LUT).
+    uint64_t g1[kItems], g2[kItems];
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      g1[k] = (DB_PRP_EARLY_LUT && valid[k]) ? lut_window(p.lut, off[k] >> 16, ~0ull, pol_last) : 0;
+      g2[k] = (DB_PRP_EARLY_LUT && npg[k] == 2)
+                  ? lut_window(p.lut, ((off[k] & ~4095ull) + 4096) >> 16, ~0ull, pol_last)
+                  : 0;
+    }
     tile_excl_scan(v, ex, tile_v, s_scan);
     const uint64_t tile_L = tile_v & ((1ull << 23) - 1);
     const uint32_t n_short = (uint32_t)(tile_v >> 23) & 4095u;
@@ -402,9 +448,10 @@ __global__ void __launch_bounds__(kThreads, 2) prp_build_kernel(const Params p) 
       const bool ovf = L[k] != 0 && pb + L[k] > p.cap;
       uint64_t prp1 = 0, prp2 = 0;
       if (valid[k] && !ovf && !failed) {
-        prp1 = bus(p.lut, off[k], pol_last);
+        const uint64_t x2 = (off[k] & ~4095ull) + 4096;  // the second page
+        prp1 = DB_PRP_EARLY_LUT ? g1[k] + (off[k] & 0xFFFFull) : bus(p.lut, off[k], pol_last);
         if (npg[k] == 2)
-          prp2 = bus(p.lut, (off[k] & ~4095ull) + 4096, pol_last);
+          prp2 = DB_PRP_EARLY_LUT ? g2[k] + (x2 & 0xFFFFull) : bus(p.lut, x2, pol_last);
         else if (npg[k] >= 3)
           prp2 = p.arena_base + (pb << 12);
       }
@@ -551,9 +598,8 @@ int grid_for(uint64_t n_tiles) {
 using namespace db;
 
 extern "C" int db_prp_workspace_size(uint64_t n, size_t* bytes) {
-  (void)n;
   if (!bytes) return -EINVAL;
-  if (n > (1ull << 28)) return -EINVAL;
+  if (n > prp::kMaxRequests) return -EINVAL;
   *bytes = prp::ws_bytes_for(n);
   return 0;
 }
@@ -564,7 +610,7 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
                             uint8_t* status, db_counters* ctr, uint32_t flags, void* ws,
                             size_t ws_bytes, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  if (n > (1ull << 28)) return -EINVAL;
+  if (n > prp::kMaxRequests) return -EINVAL;
   if (heap_size == 0 || heap_size % 65536 != 0) return -EINVAL;
   if (arena_base % 4096 != 0) return -EINVAL;
   if (arena_cap_pages > ((~0ull - arena_base) >> 12)) return -EINVAL;  // bus addresses must not wrap

@@ -99,9 +99,9 @@ def random_batch(rng, n, heap, max_len, invalid_frac=0.02):
     return np.stack([off, length], axis=1).astype(np.uint64)
 
 
-@pytest.mark.parametrize("n", [1, 2, 511, 512, 513, 1023, 1025, 4999, 70001])
+@pytest.mark.parametrize("n", [1, 2, 511, 512, 513, 2047, 2048, 2049, 4999, 70001])
 def test_random_batches_ragged(db, oracle, n):
-    """Several tiles of 512 and a ragged tail, lists of all lengths."""
+    """Several tiles of 2048 and a ragged tail, lists of all lengths."""
     import synth
     rng = np.random.default_rng(1000 + n)
     heap = 64 * 1024 * 1024
