@@ -9,17 +9,18 @@
 // Two launches per call:
 //   index build  copies (start, end, lkey) into 32-byte records (one L2
 //                sector each), checks the table is sorted and disjoint, and
-//                fills a directory D[b] = number of records starting below
-//                lo + b * 2^shift (2^shift chosen so that the records' span
-//                fits nb buckets): each record fills the buckets between its
-//                predecessor's and its own; entry b also holds D[b+1] and the
-//                start of record D[b].
+//                fills a directory of 32-byte entries (one sector each):
+//                D[b] = number of records starting below lo + b * 2^shift
+//                (2^shift chosen so that the records' span fits nb buckets)
+//                and the page offsets, from the bucket's first page, of the
+//                starts of records D[b] .. D[b] + 6. Each record fills the
+//                buckets between its predecessor's and its own.
 //   lookup       persistent CTAs, 4 queries per thread per step: round to
-//                pages; one 16-byte directory entry gives D[b], D[b+1] and
-//                the start of record D[b], which decides the candidate when
-//                the bucket holds at most one record start (binary steps
-//                otherwise); read the candidate's 32-byte record and
-//                classify. The next step's queries load meanwhile.
+//                pages; the directory entry of the base's bucket names the
+//                candidate unless seven or more records start in the bucket
+//                at or below the base (then binary steps over the records up
+//                to D[b+1]); read the candidate's 32-byte record and classify.
+//                The next step's queries load meanwhile.
 // For a sorted table of disjoint non-empty records the only record that can
 // contain [base, aend) is the last one starting at or below base, so the
 // lowest containing index is that record or none.
@@ -35,10 +36,10 @@ namespace mr {
 #define DB_MR_THREADS 256
 #endif
 #ifndef DB_MR_QPT
-#define DB_MR_QPT 4
+#define DB_MR_QPT 3
 #endif
 #ifndef DB_MR_MIN_CTAS
-#define DB_MR_MIN_CTAS 4
+#define DB_MR_MIN_CTAS 5
 #endif
 #ifndef DB_MR_BUCKET_SHIFT
 #define DB_MR_BUCKET_SHIFT 0
@@ -46,6 +47,7 @@ namespace mr {
 constexpr int kBuildThreads = 256;
 constexpr int kThreads = DB_MR_THREADS;
 constexpr int kQPT = DB_MR_QPT;
+
 
 struct Header {        // first 256 bytes of the workspace
   uint64_t lo;         // start of record 0
@@ -69,20 +71,23 @@ inline uint32_t buckets_for(uint64_t n_mr) {
   return (uint32_t)nb;
 }
 // Directory entry of bucket b: the records starting below the bucket
-// (D[b]), the same count for bucket b + 1 (D[b+1]), and where records D[b]
-// and D[b] + 1 start, as page offsets from the bucket's first page
-// (rounded up: a start s lies at or below a page-aligned base exactly when
-// ceil(s / 4096) <= base / 4096). One 16-byte load settles a bucket holding
-// at most two record starts.
-struct alignas(16) Dir {
-  uint32_t first;  // D[b]
-  uint32_t next;   // D[b + 1] (entry nb: n_mr)
-  uint32_t off1;   // page offset of record D[b]'s start (kNoOff if none or too far)
-  uint32_t off2;   // page offset of record D[b] + 1's start (kNoOff likewise)
+// (D[b]) and where records D[b] .. D[b] + 6 start, as page offsets from the
+// bucket's first page, rounded up (a start s lies at or below a
+// page-aligned base exactly when ceil(s / 4096) <= base / 4096). The starts
+// are increasing, so the offsets at or below a base's offset form a prefix
+// and their count says which record is the candidate; kNoOff stands for a
+// record that does not exist or starts more than 2^32 - 2 pages on. One
+// 32-byte load settles every query whose bucket holds fewer than seven
+// record starts at or below it.
+constexpr int kOffs = 7;
+struct alignas(32) Dir {
+  uint32_t first;        // D[b]
+  uint32_t off[kOffs];   // page offsets of records D[b] .. D[b] + 6
 };
 constexpr uint32_t kNoOff = 0xFFFFFFFFu;
 constexpr uint32_t kMaxOffsetShift = 43;  // bucket widths up to 2^43 bytes keep offsets in 32 bits
 inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * sizeof(Dir) + 255) & ~(size_t)255; }
+static_assert(sizeof(Dir) == 32, "one L2 sector per directory entry");
 inline size_t ws_bytes_for(uint64_t n_mr) {
   const uint32_t nb = buckets_for(n_mr);
   return kHeaderBytes + dir_bytes(nb) + (size_t)n_mr * sizeof(Rec);
@@ -112,22 +117,29 @@ __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t 
 // buckets (key(i-1), key(i)] (all with D = i); a short range is written by
 // its thread, a longer one (a wide gap before the record) by its whole warp.
 // The buckets after the last record's (D = n) are written by a grid-stride
-// loop of their own. Entry b also gets the start of record D[b] and entry
-// b - 1 its "next" count.
+// loop of their own. Each entry is written whole, by one 32-byte store, by
+// its owner: the starts of records D[b] .. D[b] + 6 are all it needs.
+// ss[k] is the start of record x + k, or ~0 when that record does not exist.
 __device__ __forceinline__ uint32_t page_offset(uint64_t s, uint64_t bpage0) {
+  if (s == ~0ull) return kNoOff;
   const uint64_t sp = (s >> 12) + ((s & 4095u) ? 1 : 0);  // ceil(s / 4096), s < 2^64
-  const uint64_t d = sp - bpage0;
+  const uint64_t d = sp - bpage0;  // the record starts in or after the bucket: d >= 0
   return d < kNoOff ? (uint32_t)d : kNoOff;
 }
-__device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32_t x, uint64_t s1,
-                                        uint64_t s2, bool have1, bool have2, uint64_t lo,
-                                        uint32_t shift) {
+__device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32_t x,
+                                        const uint64_t (&ss)[kOffs], uint64_t lo, uint32_t shift) {
   const uint64_t bpage0 = (lo + (b << shift)) >> 12;
   const bool offs = shift <= kMaxOffsetShift;
-  p.dir[b].first = x;
-  p.dir[b].off1 = (offs && have1) ? page_offset(s1, bpage0) : kNoOff;
-  p.dir[b].off2 = (offs && have2) ? page_offset(s2, bpage0) : kNoOff;
-  if (b > 0) p.dir[b - 1].next = x;
+  uint32_t o[kOffs];
+#pragma unroll
+  for (int k = 0; k < kOffs; ++k) o[k] = offs ? page_offset(ss[k], bpage0) : kNoOff;
+  const uint64_t w0 = (uint64_t)x | ((uint64_t)o[0] << 32);
+  const uint64_t w1 = (uint64_t)o[1] | ((uint64_t)o[2] << 32);
+  const uint64_t w2 = (uint64_t)o[3] | ((uint64_t)o[4] << 32);
+  const uint64_t w3 = (uint64_t)o[5] | ((uint64_t)o[6] << 32);
+  asm volatile("st.global.v4.u64 [%0], {%1, %2, %3, %4};" ::"l"(p.dir + b), "l"(w0), "l"(w1),
+               "l"(w2), "l"(w3)
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildParams p) {
@@ -141,7 +153,6 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
     p.hdr->lo = lo;
     p.hdr->shift = shift;
     p.hdr->nb = p.nb;
-    p.dir[nb].next = (uint32_t)n;
   }
   const int lane = threadIdx.x & 31;
   const uint64_t nthreads = (uint64_t)gridDim.x * blockDim.x;
@@ -150,10 +161,12 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
 
   bool bad = false;
   for (uint64_t i = tid; i < n_round; i += nthreads) {
-    uint64_t b0 = 1, b1 = 0, s = 0, s_next = 0;  // buckets [b0, b1] get D = i
+    uint64_t b0 = 1, b1 = 0, s = 0;  // buckets [b0, b1] get D = i
+    uint64_t ss[kOffs];              // starts of records i .. i + 6
+#pragma unroll
+    for (int k = 0; k < kOffs; ++k) ss[k] = i + k < n ? p.start[i + k] : ~0ull;
     if (i < n) {
-      s = p.start[i];
-      s_next = i + 1 < n ? p.start[i + 1] : 0;
+      s = ss[0];
       const uint64_t e = p.end[i];
       Rec r;
       r.start = s;
@@ -167,27 +180,27 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
       b1 = bucket_of(s, lo, shift, p.nb);
     }
     const bool wide = b1 >= b0 && b1 - b0 >= 32;
-    const bool has_next = i + 1 < n;
     if (!wide)
-      for (uint64_t b = b0; b <= b1 && b1 >= b0; ++b)
-        set_dir(p, b, (uint32_t)i, s, s_next, true, has_next, lo, shift);
+      for (uint64_t b = b0; b <= b1 && b1 >= b0; ++b) set_dir(p, b, (uint32_t)i, ss, lo, shift);
     uint32_t todo = __ballot_sync(kFull, wide);
     while (todo) {
       const int l = __ffs(todo) - 1;
       todo &= todo - 1;
       const uint64_t wb0 = __shfl_sync(kFull, b0, l), wb1 = __shfl_sync(kFull, b1, l);
-      const uint64_t wi = __shfl_sync(kFull, i, l), ws = __shfl_sync(kFull, s, l);
-      const uint64_t wsn = __shfl_sync(kFull, s_next, l);
-      const bool whn = __shfl_sync(kFull, has_next, l);
-      for (uint64_t b = wb0 + lane; b <= wb1; b += 32)
-        set_dir(p, b, (uint32_t)wi, ws, wsn, true, whn, lo, shift);
+      const uint64_t wi = __shfl_sync(kFull, i, l);
+      uint64_t wss[kOffs];
+#pragma unroll
+      for (int k = 0; k < kOffs; ++k) wss[k] = __shfl_sync(kFull, ss[k], l);
+      for (uint64_t b = wb0 + lane; b <= wb1; b += 32) set_dir(p, b, (uint32_t)wi, wss, lo, shift);
     }
   }
   if (bad) atomicOr(&p.hdr->err, DB_ERR_TABLE_ORDER);
-  // Buckets after the last record's: D = n.
+  // Buckets after the last record's: D = n, no record starts in or after them.
   const uint64_t tail0 = bucket_of(hi, lo, shift, p.nb) + 1;
-  for (uint64_t b = tail0 + tid; b <= nb; b += nthreads)
-    set_dir(p, b, (uint32_t)n, 0, 0, false, false, lo, shift);
+  uint64_t none[kOffs];
+#pragma unroll
+  for (int k = 0; k < kOffs; ++k) none[k] = ~0ull;
+  for (uint64_t b = tail0 + tid; b <= nb; b += nthreads) set_dir(p, b, (uint32_t)n, none, lo, shift);
 }
 
 struct LookupParams {
@@ -211,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
   const uint32_t shift = p.hdr_ro->shift;
   const uint32_t nb = p.hdr_ro->nb;
   const uint64_t n_mr = p.n_mr;
+  const bool offsets_kept = shift <= kMaxOffsetShift;
   constexpr uint64_t kGroup = (uint64_t)kThreads * kQPT;  // queries per CTA step
   const uint64_t n_groups = (p.n_q + kGroup - 1) / kGroup;
   uint32_t hits = 0, invalid = 0;
@@ -250,38 +264,41 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
         }
       }
     }
-    // Directory: the number of records starting at or below base lies in
-    // [first, next]; the two start offsets settle up to two of them.
+    // Directory: the number of records starting at or below base is
+    // D[b] plus the count of start offsets at or below base's offset; only
+    // when all seven are (or the offsets are not kept) does it take binary
+    // steps over records up to D[b+1]. [a, z) is the range still open.
+    bool wide_search = false;
 #pragma unroll
     for (int k = 0; k < kQPT; ++k) {
       a[k] = 0;
       z[k] = 0;
       if (state[k] == 1) {
-        const uint64_t b = (base[k] - lo) >> shift;
-        if (b >= nb) {
-          a[k] = (uint32_t)n_mr;
-          z[k] = (uint32_t)n_mr;
-        } else {
-          const ulonglong2 d = ld_table16(p.dir + b, pol_last);
-          uint32_t x = (uint32_t)d.x, y = (uint32_t)(d.x >> 32);
-          const uint32_t off1 = (uint32_t)d.y, off2 = (uint32_t)(d.y >> 32);
+        uint64_t b = (base[k] - lo) >> shift;
+        b = b < nb ? b : nb;
+        uint64_t w0, w1, w2, w3;
+        ld_table32(p.dir + b, pol_last, w0, w1, w2, w3);
+        uint32_t x = (uint32_t)w0;
+        x = x < n_mr ? x : (uint32_t)n_mr;
+        // base's page offset in the bucket, capped below kNoOff
+        const uint64_t bo64 = (base[k] >> 12) - ((lo + (b << shift)) >> 12);
+        const uint32_t bo = bo64 < kNoOff - 1 ? (uint32_t)bo64 : kNoOff - 1;
+        const uint32_t o[kOffs] = {(uint32_t)(w0 >> 32), (uint32_t)w1, (uint32_t)(w1 >> 32),
+                                   (uint32_t)w2, (uint32_t)(w2 >> 32), (uint32_t)w3,
+                                   (uint32_t)(w3 >> 32)};
+        uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < kOffs; ++j) c += o[j] <= bo;
+        if (offsets_kept && c < kOffs) {
+          x += c;
           x = x < n_mr ? x : (uint32_t)n_mr;
-          y = y < n_mr ? y : (uint32_t)n_mr;
-          y = y > x ? y : x;
-          const uint64_t bo = (base[k] >> 12) - ((lo + (b << shift)) >> 12);  // base's page offset
-          if (x < y && off1 != kNoOff) {
-            if (bo < off1) {
-              y = x;                    // record x starts above base
-            } else if (x + 1 < y && off2 != kNoOff) {
-              if (bo < off2) { ++x; y = x; }            // x starts at or below, x + 1 above
-              else { x += 2; }                          // both at or below: search the rest
-            } else {
-              ++x;                      // record x starts at or below base
-              if (x + 1 > y) y = x;
-            }
-          }
           a[k] = x;
-          z[k] = y;
+          z[k] = x;
+        } else {
+          a[k] = offsets_kept ? x + kOffs : x;   // the rest lies in [a, D[b+1])
+          a[k] = a[k] < n_mr ? a[k] : (uint32_t)n_mr;
+          z[k] = b < nb ? ~0u : (uint32_t)n_mr;  // D[b+1], read below
+          wide_search = true;
         }
       }
     }
@@ -292,6 +309,18 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
       const uint64_t i = gn * kGroup + (uint64_t)k * kThreads + threadIdx.x;
       nq[k] = (gn < n_groups && i < p.n_q) ? ld_stream16(p.q + i, pol_first)
                                             : make_ulonglong2(0, 0);
+    }
+    // Rare: the upper bound D[b+1] of a bucket holding many record starts.
+    if (wide_search) {
+#pragma unroll
+      for (int k = 0; k < kQPT; ++k) {
+        if (state[k] == 1 && z[k] == ~0u) {
+          const uint64_t b = (base[k] - lo) >> shift;
+          uint32_t y = ld_table4(&p.dir[b + 1].first, pol_last);
+          y = y < n_mr ? y : (uint32_t)n_mr;
+          z[k] = y > a[k] ? y : a[k];
+        }
+      }
     }
     // Binary steps over any records still undecided (a bucket with two or
     // more record starts; all queries of the thread in lockstep).

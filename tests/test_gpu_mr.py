@@ -108,6 +108,91 @@ def test_extreme_addresses(db, oracle):
     check(run_gpu(db, q, start, end, lkey), oracle.mr_linear(q, start, end, lkey))
 
 
+def byte_table(rng, n, span_pages, granule):
+    """n disjoint records inside span_pages pages, with starts and ends on
+    multiples of granule bytes (64: byte-granular records; 4096: pages)."""
+    cuts = np.sort(rng.choice(np.arange(1, span_pages * 4096 // granule, dtype=np.int64),
+                              size=2 * n, replace=False)).astype(np.uint64) * np.uint64(granule)
+    if granule < 4096:
+        cuts += rng.integers(0, granule, size=2 * n).astype(np.uint64)
+    start, end = cuts[0::2], cuts[1::2]
+    keep = start < end
+    return start[keep], end[keep]
+
+
+@pytest.mark.parametrize("case", ["unaligned", "clustered", "clustered_far", "long_queries"])
+def test_directory_paths(db, oracle, case):
+    """Byte-granular starts and ends (exact versus contained), many records
+    in one bucket (the binary-step path), queries spanning more than 2^31
+    pages and queries past the last record."""
+    rng = np.random.default_rng({"unaligned": 1, "clustered": 2, "clustered_far": 3,
+                                 "long_queries": 4}[case])
+    if case == "unaligned":
+        start, end = byte_table(rng, 3000, 200000, 64)
+        # a quarter of the records page aligned at both ends, so exact hits exist
+        al = rng.random(start.shape[0]) < 0.25
+        start = np.where(al, (start + np.uint64(4095)) & ~np.uint64(4095), start)
+        end = np.where(al, end & ~np.uint64(4095), end)
+        ok = start < end
+        ok[1:] &= end[:-1] <= start[1:]
+        start, end = start[ok], end[ok]
+    elif case == "clustered":
+        # ten dense groups of 200 records, far apart: each group shares a bucket
+        parts = []
+        for base in np.sort(rng.choice(1 << 28, size=10, replace=False)).astype(np.uint64):
+            s_, e_ = byte_table(rng, 200, 3000, 4096)
+            parts.append((s_ + (base << np.uint64(12)), e_ + (base << np.uint64(12))))
+        start = np.concatenate([x[0] for x in parts])
+        end = np.concatenate([x[1] for x in parts])
+        ok = np.ones(start.shape[0], dtype=bool)
+        ok[1:] = end[:-1] <= start[1:]
+        start, end = start[ok], end[ok]
+    elif case == "clustered_far":
+        start, end = byte_table(rng, 1500, 20000, 4096)
+        start = np.append(start, np.uint64(1) << np.uint64(46))  # one record far away:
+        end = np.append(end, (np.uint64(1) << np.uint64(46)) + np.uint64(1 << 20))  # every other bucket empty
+    else:
+        start = np.array([0x1000, 1 << 40, (1 << 60) + 0x3000], dtype=np.uint64)
+        end = np.array([0x5000, 1 << 59, (1 << 61)], dtype=np.uint64)
+    n = start.shape[0]
+    lkey = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    hi = int(end[-1])
+    m = 60000
+    pick = rng.integers(0, n, size=m)
+    mode = rng.integers(0, 4, size=m)
+    a = np.empty(m, dtype=np.uint64)
+    sz = np.empty(m, dtype=np.uint64)
+    span = (end[pick] - start[pick]).astype(np.float64)
+    # 0: exactly the record; 1: inside it; 2: anywhere; 3: past the last record
+    a[mode == 0] = start[pick][mode == 0]
+    sz[mode == 0] = (end[pick] - start[pick])[mode == 0]
+    off = (rng.random(m) * span).astype(np.uint64)
+    a[mode == 1] = (start[pick] + off)[mode == 1]
+    sz[mode == 1] = np.maximum(np.uint64(1), ((end[pick] - start[pick] - off).astype(np.float64)
+                                               * rng.random(m)).astype(np.uint64))[mode == 1]
+    a[mode == 2] = (rng.random(m) * float(hi)).astype(np.uint64)[mode == 2]
+    sz[mode == 2] = rng.integers(1, 1 << 16, size=m).astype(np.uint64)[mode == 2]
+    a[mode == 3] = np.uint64(hi) + rng.integers(0, 1 << 30, size=m).astype(np.uint64)[mode == 3]
+    sz[mode == 3] = rng.integers(1, 1 << 20, size=m).astype(np.uint64)[mode == 3]
+    if case == "long_queries":
+        # ranges of 2^43 .. 2^50 bytes inside the second record and across the third
+        big = np.uint64(1) << rng.integers(43, 51, size=m).astype(np.uint64)
+        a = np.where(mode == 1, np.uint64(1 << 41), a)
+        sz = np.where(mode == 1, big, sz)
+        a = np.where(mode == 0, np.uint64((1 << 60) + 0x3000), a)
+        sz = np.where(mode == 0, big, sz)
+    top = np.uint64(2**64 - 4096)
+    sz = np.minimum(sz, top - np.minimum(a, top))
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    want = oracle.mr_linear(q, start, end, lkey)
+    got = run_gpu(db, q, start, end, lkey)
+    check(got, want)
+    kinds = np.bincount(want["kind"].astype(np.int64), minlength=4)
+    assert kinds[2] > 0 and kinds[0] > 0, kinds
+    if case == "unaligned":
+        assert kinds[1] > 0, kinds
+
+
 def test_empty_table_and_empty_batch(db, oracle):
     q = np.array([[0x1000, 10], [0, 0]], dtype=np.uint64)
     e = np.zeros(0, dtype=np.uint64)
