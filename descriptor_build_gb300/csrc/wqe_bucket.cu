@@ -8,42 +8,41 @@
 //
 // A ring asked for more than `depth` entries takes none of the batch, so the
 // per-ring totals must be known before any entry is written. Three launches,
-// reduce-then-scan:
-//   count    warps stride over tiles of 1024 puts: a per-warp shared-memory
-//            histogram over the R rings plus one bin for invalid puts,
-//            written column-major: counts[ring][tile].
+// reduce-then-scan over tiles of 256 puts (8 rows of 32):
+//   count    a warp per tile: a warp-private shared-memory histogram over
+//            the R rings plus one bin for invalid puts, written column-major:
+//            counts[ring][tile].
 //   scan     one CTA per ring: exclusive scan of its column in place (staged
 //            through shared memory), the ring's batch total, count[], the
 //            overflow decision, the head; the last CTA publishes the counters.
-//   scatter  persistent CTAs, a tile at a time (the next tile's puts load
-//            meanwhile): stable rank of each put inside its warp with
-//            __match_any_sync, then across the tile's 32 warp-rows (a warp
-//            scan per ring); the first 48 bytes of each WQE are built into
-//            shared memory in ring order (48-byte stride, conflict-free
-//            read-out) and each ring's run is written out contiguously with
-//            16-byte stores, the zero last quarter straight from registers.
+//   scatter  a warp per tile, with no CTA-wide barrier: the tile's puts go to
+//            warp-private shared memory; stable rank of each put inside its
+//            row with __match_any_sync and across the 8 rows by a per-ring
+//            prefix; a 2-byte permutation puts the tile in ring order, and
+//            each ring's run is written out contiguously, two 32-byte stores
+//            per WQE from a pair of lanes.
 // No kernel waits on another CTA.
 #include "common.cuh"
 
 namespace db {
 namespace wqe {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 2;
-constexpr int kTile = kThreads * kItems;  // 1024 puts per tile
-constexpr int kUnits = kItems * kWarps;   // warp-rows of 32 puts, in batch order
+constexpr int kRows = 8;
+constexpr int kTile = kRows * 32;  // 256 puts per tile, one warp each
 constexpr uint32_t kMaxRings = 1024;
+// Warps per scatter CTA (build-time tunable; fewer when many rings make a
+// warp's shared memory large).
+#ifndef DB_WQE_SCATTER_WARPS
+#define DB_WQE_SCATTER_WARPS 4
+#endif
+constexpr int kSWarps = DB_WQE_SCATTER_WARPS;
+constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per CTA
 
 // Build-time tuning (defaults measured best on GB300): how the count pass
 // histograms a row of 32 puts (0: __match_any_sync + one shared atomic per
-// distinct ring, 1: one shared atomic per put), and whether the scatter pass
-// runs persistent CTAs (3 per SM) that load their next tile early.
+// distinct ring, 1: one shared atomic per put).
 #ifndef DB_WQE_COUNT_MODE
 #define DB_WQE_COUNT_MODE 1
-#endif
-#ifndef DB_WQE_SCATTER_PERSIST
-#define DB_WQE_SCATTER_PERSIST 1
 #endif
 
 // Workspace: Header, old heads [1024] u64, overflow flags [1024] u32,
@@ -59,14 +58,17 @@ constexpr size_t kHeadOldOff = 256;
 constexpr size_t kFullOff = kHeadOldOff + 8 * kMaxRings;
 constexpr size_t kCountsOff = kFullOff + 4 * kMaxRings;
 inline uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
+// Column stride of counts: tiles rounded up to 8 (32-byte aligned columns).
+inline uint64_t stride_for(uint64_t n) { return (tiles_for(n) + 7) & ~7ull; }
 inline size_t ws_bytes_for(uint64_t n, uint32_t R) {
-  return kCountsOff + ((tiles_for(n) * ((uint64_t)R + 1) * 4 + 255) & ~(uint64_t)255);
+  return kCountsOff + ((stride_for(n) * ((uint64_t)R + 1) * 4 + 255) & ~(uint64_t)255);
 }
 
 struct Params {
   const ulonglong2* req;
   uint64_t n;
   uint64_t n_tiles;
+  uint64_t stride;  // column stride of counts
   const uint64_t* peer_ptrs;
   const uint32_t* rkeys;
   uint32_t world, n_qp, R, V;
@@ -81,7 +83,7 @@ struct Params {
   Header* hdr;
   uint64_t* head_old;
   uint32_t* full;
-  uint32_t* counts;  // [V][n_tiles]
+  uint32_t* counts;  // [V][stride], first n_tiles of each column used
 };
 
 // Ring of a put, or R for an invalid one.
@@ -96,11 +98,14 @@ __device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) 
 }
 
 // ---------------------------------------------------------------- count pass
-// One warp counts a whole tile (32 rows of 32 puts) into its own shared
+// One warp counts a whole tile (8 rows of 32 puts) into its own shared
 // histogram; warps stride over tiles, so no block-wide barrier is needed.
 constexpr int kCountThreads = 256;
 constexpr int kCountWarps = kCountThreads / 32;
-constexpr int kCountUnroll = 4;  // rows of 32 puts loaded at once
+#ifndef DB_WQE_COUNT_UNROLL
+#define DB_WQE_COUNT_UNROLL 8
+#endif
+constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at once
 
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
   extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V]
@@ -133,47 +138,65 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
       }
     }
     __syncwarp();
-    for (uint32_t v = lane; v < V; v += 32) p.counts[v * p.n_tiles + tile] = s_hist[v];
+    for (uint32_t v = lane; v < V; v += 32) p.counts[v * p.stride + tile] = s_hist[v];
     __syncwarp();
   }
 }
 
 // ----------------------------------------------------------------- scan pass
+// One CTA per bin: each thread takes 32 consecutive column entries (16-byte
+// loads and stores), so a column of up to 32768 tiles is one round.
 constexpr int kScanThreads = 1024;
-constexpr int kScanSeg = 4 * kScanThreads;  // column entries staged per round
+constexpr int kScanPer = 32;
+constexpr uint64_t kScanSeg = (uint64_t)kScanThreads * kScanPer;
 
 __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) {
   constexpr int kW = kScanThreads / 32;
   __shared__ uint32_t s_scan[kW];
-  __shared__ uint32_t s_col[kScanSeg];
   __shared__ int s_last;
   const uint32_t v = blockIdx.x;
-  uint32_t* col = p.counts + (uint64_t)v * p.n_tiles;
+  uint32_t* col = p.counts + (uint64_t)v * p.stride;
   const uint64_t T = p.n_tiles;
   uint64_t carry = 0;
   for (uint64_t s0 = 0; s0 < T; s0 += kScanSeg) {
-    const uint32_t len = (uint32_t)(T - s0 < (uint64_t)kScanSeg ? T - s0 : kScanSeg);
-    for (uint32_t x = threadIdx.x; x < len; x += kScanThreads) s_col[x] = col[s0 + x];
-    __syncthreads();
-    uint32_t c[4], mine = 0;
+    const uint64_t b = s0 + (uint64_t)threadIdx.x * kScanPer;
+    uint32_t c[kScanPer];
+    if (b + kScanPer <= T) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t x = 4 * threadIdx.x + q;
-      c[q] = x < len ? s_col[x] : 0u;
-      mine += c[q];
+      for (int j = 0; j < kScanPer; j += 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(col + b + j);
+        c[j] = x.x;
+        c[j + 1] = x.y;
+        c[j + 2] = x.z;
+        c[j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kScanPer; ++j) c[j] = b + j < T ? col[b + j] : 0u;
     }
+    uint32_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < kScanPer; ++j) mine += c[j];
     uint32_t excl, seg_total;
     block_excl_scan<kW>(mine, excl, seg_total, s_scan);
+    uint32_t run = (uint32_t)carry + excl;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t x = 4 * threadIdx.x + q;
-      if (x < len) s_col[x] = (uint32_t)carry + excl;
-      excl += c[q];
+    for (int j = 0; j < kScanPer; ++j) {
+      const uint32_t x = c[j];
+      c[j] = run;
+      run += x;
     }
-    __syncthreads();
-    for (uint32_t x = threadIdx.x; x < len; x += kScanThreads) col[s0 + x] = s_col[x];
+    if (b + kScanPer <= T) {
+#pragma unroll
+      for (int j = 0; j < kScanPer; j += 4)
+        *reinterpret_cast<uint4*>(col + b + j) = make_uint4(c[j], c[j + 1], c[j + 2], c[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kScanPer; ++j)
+        if (b + j < T) col[b + j] = c[j];
+    }
     carry += seg_total;
-    __syncthreads();
+    __syncthreads();  // s_scan is reused by the next round
   }
   const uint64_t total = carry;
   if (threadIdx.x == 0) {
@@ -212,144 +235,130 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
 }
 
 // -------------------------------------------------------------- scatter pass
-inline size_t scatter_smem(uint32_t V) {
-  size_t b = (size_t)kTile * 48;    // staged WQEs (bytes 48..63 are zero: not staged)
-  b += (size_t)kTile * 8;           // destination of each staged WQE
-  b += (size_t)V * 8;               // old heads
-  b += (size_t)V * 4 * 4;           // run start, tile count, tile prefix, full flag
-  b += (size_t)kUnits * V * 2;      // per warp-row counts
+// Shared memory of a scatter CTA: per CTA, for each ring its slot array (0
+// when the ring overflowed) and for each PE its peer pointer and rkey; per
+// warp, the tile's puts, the ring-order permutation, the per-row ring counts
+// (then their prefixes over rows), and per ring the tile's first sequence
+// number and where its run starts.
+__host__ __device__ inline size_t warp_smem(uint32_t V) {
+  size_t b = (size_t)kTile * 16;      // puts
+  b += (size_t)V * 8;                 // first sequence number per ring
+  b += (size_t)V * 4;                 // run start per ring
+  b += (size_t)kRows * V * 2;         // per-row counts
+  b += (size_t)kTile * 2;             // permutation
   return (b + 15) & ~(size_t)15;
 }
-
-__device__ __forceinline__ void scatter_tile(const Params& p, uint64_t tile, const ulonglong2 (&r)[kItems],
-                                             unsigned char* smem, uint32_t* s_scan);
-
-__global__ void __launch_bounds__(kThreads, 3) wqe_scatter_kernel(const Params p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ uint32_t s_scan[kWarps];
-  const uint64_t pol_first = policy_evict_first();
-  auto load = [&](uint64_t tile, ulonglong2 (&r)[kItems]) {
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-      r[k] = (tile < p.n_tiles && i < p.n) ? ld_stream16(p.req + i, pol_first)
-                                             : make_ulonglong2(0, 0);
-    }
-  };
-  ulonglong2 cur[kItems];
-  load(blockIdx.x, cur);
-  const uint64_t stride = DB_WQE_SCATTER_PERSIST ? gridDim.x : p.n_tiles;
-  for (uint64_t tile = blockIdx.x; tile < p.n_tiles; tile += stride) {
-    ulonglong2 nxt[kItems];
-    if (DB_WQE_SCATTER_PERSIST) load(tile + stride, nxt);
-    scatter_tile(p, tile, cur, smem, s_scan);
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) cur[k] = DB_WQE_SCATTER_PERSIST ? nxt[k] : cur[k];
-  }
+__host__ __device__ inline size_t cta_smem(uint32_t V) { return ((size_t)V * 20 + 15) & ~(size_t)15; }
+// Warps of a scatter CTA for V bins, and its shared memory.
+inline int scatter_warps(uint32_t V) {
+  const size_t fit = (kMaxSmem - cta_smem(V)) / warp_smem(V);
+  return (int)(fit < (size_t)kSWarps ? fit : (size_t)kSWarps);
 }
+inline size_t scatter_smem(uint32_t V) { return cta_smem(V) + scatter_warps(V) * warp_smem(V); }
 
-__device__ __forceinline__ void scatter_tile(const Params& p, uint64_t tile,
-                                             const ulonglong2 (&rin)[kItems], unsigned char* smem,
-                                             uint32_t* s_scan) {
+__global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
   const uint32_t V = p.V, R = p.R;
-  ulonglong2* s_stage = reinterpret_cast<ulonglong2*>(smem);  // WQE pos, part k at 3 pos + k
-  uint64_t* s_dst = reinterpret_cast<uint64_t*>(smem + (size_t)kTile * 48);
-  uint64_t* s_head = s_dst + kTile;
-  uint32_t* s_run = reinterpret_cast<uint32_t*>(s_head + V);
-  uint32_t* s_tot = s_run + V;
-  uint32_t* s_pre = s_tot + V;
-  uint32_t* s_full = s_pre + V;
-  uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_full + V);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t pol_first = policy_evict_first();
+  uint64_t* s_slots = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* s_peer = s_slots + V;
+  uint32_t* s_rkey = reinterpret_cast<uint32_t*>(s_peer + V);
+  unsigned char* w = smem + cta_smem(V) + warp * warp_smem(V);
+  ulonglong2* s_put = reinterpret_cast<ulonglong2*>(w);
+  uint64_t* s_seq0 = reinterpret_cast<uint64_t*>(s_put + kTile);
+  uint32_t* s_run = reinterpret_cast<uint32_t*>(s_seq0 + V);
+  uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_run + V);  // [kRows][V]
+  uint16_t* s_perm = s_cnt + kRows * V;
 
-  for (uint32_t x = threadIdx.x; x < kUnits * V; x += kThreads) s_cnt[x] = 0;
-  for (uint32_t v = threadIdx.x; v < V; v += kThreads) {
-    s_pre[v] = p.counts[v * p.n_tiles + tile];
-    if (v < R) {
-      s_head[v] = p.head_old[v];
-      s_full[v] = p.full[v];
+  for (uint32_t v = threadIdx.x; v < R; v += blockDim.x) {
+    s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
+    if (v < p.world) {
+      s_peer[v] = __ldg(p.peer_ptrs + v);
+      s_rkey[v] = __ldg(p.rkeys + v);
     }
   }
-  ulonglong2 r[kItems];
-  uint32_t bin[kItems];
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-    r[k] = rin[k];
-    bin[k] = i < p.n ? bin_of(p, r[k]) : V;  // outside the batch: no bin
-  }
-  __syncthreads();
+  __syncthreads();  // the only CTA-wide barrier
+  const uint64_t tile = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  if (tile >= p.n_tiles) return;
+  const uint64_t t0 = tile * kTile;
 
-  // Rank inside each warp-row (stable: lower lanes are earlier puts).
-  uint32_t lrank[kItems];
+  // 1. Load the tile (all rows in flight at once); ring of each put; rank
+  //    inside its row; per-row counts by the row's first put of each ring.
+  for (uint32_t x = lane; x < kRows * V; x += 32) s_cnt[x] = 0;
+  ulonglong2 r[kRows];
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const uint32_t peers = __match_any_sync(kFull, bin[k]);
-    const uint32_t before = peers & lanemask_lt();
-    lrank[k] = __popc(before);
-    if (bin[k] < V && before == 0) s_cnt[(k * kWarps + warp) * V + bin[k]] = (uint16_t)__popc(peers);
+  for (int u = 0; u < kRows; ++u) {
+    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
+    r[u] = i < p.n ? ld_stream16(p.req + i, pol_first) : make_ulonglong2(0, 0);
   }
-  __syncthreads();
-  // Across warp-rows, in batch order: one warp per ring, lane u = warp-row u.
-  static_assert(kUnits == 32, "one lane per warp-row");
-  for (uint32_t v = warp; v < V; v += kWarps) {
-    const uint32_t c = s_cnt[lane * V + v];
-    uint32_t x = c;
+  __syncwarp();
+  uint32_t bin_rank[kRows];  // ring | rank << 16
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
+    const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;  // outside the batch: no bin
+    s_put[u * 32 + lane] = r[u];
+    const uint32_t peers = __match_any_sync(kFull, bin);
+    const uint32_t before = peers & lanemask_lt();
+    if (bin < V && before == 0) s_cnt[u * V + bin] = (uint16_t)__popc(peers);
+    bin_rank[u] = bin | ((uint32_t)__popc(before) << 16);
+  }
+  __syncwarp();
+  // 2. Per ring: prefix of its counts over the rows, the tile's total, where
+  //    its run starts (rings in order, the invalid bin left out) and the
+  //    tile's first sequence number (the count pass's scan).
+  uint32_t carry = 0;
+  for (uint32_t v0 = 0; v0 < R; v0 += 32) {
+    const uint32_t v = v0 + lane;
+    uint32_t tot = 0;
+    if (v < R) {
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        const uint32_t c = s_cnt[u * V + v];
+        s_cnt[u * V + v] = (uint16_t)tot;
+        tot += c;
+      }
+    }
+    uint32_t x = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(kFull, x, o);
       if (lane >= o) x += y;
     }
-    s_cnt[lane * V + v] = (uint16_t)(x - c);
-    if (lane == 31) s_tot[v] = x;
-  }
-  __syncthreads();
-  // Where each ring's run starts in the staging buffer (ring order; the
-  // invalid bin is left out). Thread t owns a chunk of consecutive rings.
-  const uint32_t chunk = (R + kThreads - 1) / kThreads;
-  const uint32_t r0 = threadIdx.x * chunk;
-  uint32_t mine = 0;
-  for (uint32_t v = r0; v < r0 + chunk && v < R; ++v) mine += s_tot[v];
-  uint32_t excl, n_staged;
-  block_excl_scan<kWarps>(mine, excl, n_staged, s_scan);
-  for (uint32_t v = r0; v < r0 + chunk && v < R; ++v) {
-    s_run[v] = excl;
-    excl += s_tot[v];
-  }
-  __syncthreads();
-
-  // Build the first 48 bytes of each WQE in ring order.
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    const uint32_t v = bin[k];
-    if (v >= R) continue;
-    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-    const uint32_t local = s_cnt[(k * kWarps + warp) * V + v] + lrank[k];
-    const uint32_t pos = s_run[v] + local;
-    const uint64_t seq = s_head[v] + s_pre[v] + local;
-    const uint64_t off = r[k].x;
-    const uint32_t bytes = (uint32_t)r[k].y;
-    const uint32_t pe = (uint32_t)(r[k].y >> 32) & 0xFFFFu;
-    const uint64_t raddr = __ldg(p.peer_ptrs + pe) + off;
-    const uint32_t rkey = __ldg(p.rkeys + pe);
-    s_stage[pos * 3 + 0] = make_ulonglong2(raddr, p.local_base + off);
-    s_stage[pos * 3 + 1] = make_ulonglong2((uint64_t)bytes | ((uint64_t)p.lkey << 32), (uint64_t)rkey);
-    s_stage[pos * 3 + 2] = make_ulonglong2(seq, (uint64_t)(uint32_t)i);
-    s_dst[pos] = s_full[v] ? 0ull
-                           : (uint64_t)(p.rings + (((uint64_t)v * p.depth + (seq & (p.depth - 1))) << 6));
-  }
-  __syncthreads();
-
-  // Each ring's run is contiguous in the ring (up to one wrap): 16-byte stores.
-  for (uint32_t f = threadIdx.x; f < n_staged * 4; f += kThreads) {
-    const uint32_t q = f >> 2, part = f & 3;
-    const uint64_t d = s_dst[q];
-    if (d) {
-      const ulonglong2 x = part < 3 ? s_stage[q * 3 + part] : make_ulonglong2(0, 0);
-      st_stream16(reinterpret_cast<void*>(d + part * 16), x.x, x.y, pol_first);
+    if (v < R) {
+      s_run[v] = carry + x - tot;
+      s_seq0[v] = p.head_old[v] + p.counts[(uint64_t)v * p.stride + tile];
     }
+    carry += __shfl_sync(kFull, x, 31);
+  }
+  __syncwarp();
+  // 3. Ring-order permutation of the valid puts.
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint32_t bin = bin_rank[u] & 0xFFFFu;
+    if (bin < R) s_perm[s_run[bin] + s_cnt[u * V + bin] + (bin_rank[u] >> 16)] = (uint16_t)(u * 32 + lane);
+  }
+  __syncwarp();
+  // 4. Write-out, each ring's run contiguous in its ring (up to one wrap):
+  //    lanes 2q and 2q + 1 write the two halves of the WQE of position q.
+  const uint32_t n_out = 2 * carry;
+  const uint64_t slot_mask = p.depth - 1;
+  for (uint32_t f = lane; f < n_out; f += 32) {
+    const uint32_t q = f >> 1, h = f & 1;
+    const uint32_t o = s_perm[q];
+    const ulonglong2 x = s_put[o];
+    const uint32_t pe = (uint32_t)(x.y >> 32) & 0xFFFFu, qp = (uint32_t)(x.y >> 48);
+    const uint32_t v = pe * p.n_qp + qp;
+    const uint64_t slots = s_slots[v];
+    if (!slots) continue;
+    const uint64_t seq = s_seq0[v] + (q - s_run[v]);
+    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6)) + 32 * h;
+    if (h == 0)
+      st_stream32(d, s_peer[pe] + x.x, p.local_base + x.x,
+                  (uint64_t)(uint32_t)x.y | ((uint64_t)p.lkey << 32), (uint64_t)s_rkey[pe], pol_first);
+    else
+      st_stream32(d, seq, t0 + o, 0ull, 0ull, pol_first);
   }
 }
 
@@ -360,8 +369,7 @@ int prepare_scatter() {
   cudaGetDevice(&dev);
   if (!done_for[dev & 63]) {
     const cudaError_t e = cudaFuncSetAttribute(
-        wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)scatter_smem(kMaxRings + 1));
+        wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
   }
@@ -408,6 +416,7 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   p.req = reinterpret_cast<const ulonglong2*>(req);
   p.n = n;
   p.n_tiles = n_tiles;
+  p.stride = wqe::stride_for(n);
   p.peer_ptrs = peer_ptrs;
   p.rkeys = rkeys;
   p.world = world;
@@ -439,9 +448,8 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
-  uint64_t scatter_grid = n_tiles;
-  if (DB_WQE_SCATTER_PERSIST && scatter_grid > (uint64_t)num_sms() * 3)
-    scatter_grid = (uint64_t)num_sms() * 3;
-  wqe::wqe_scatter_kernel<<<(unsigned)scatter_grid, wqe::kThreads, wqe::scatter_smem(p.V), s>>>(p);
+  const int sw = wqe::scatter_warps(p.V);  // at least 6 for the largest ring count
+  const uint64_t scatter_grid = (n_tiles + sw - 1) / sw;
+  wqe::wqe_scatter_kernel<<<(unsigned)scatter_grid, sw * 32, wqe::scatter_smem(p.V), s>>>(p);
   return launch_result();
 }

@@ -81,7 +81,8 @@ def random_puts(rng, n, world, n_qp, heap, invalid_frac=0.03):
 
 
 @pytest.mark.parametrize("n,world,n_qp,depth", [
-    (1, 8, 4, 64), (1023, 8, 4, 64), (1024, 8, 4, 64), (1025, 8, 4, 64),
+    (1, 8, 4, 64), (255, 8, 4, 64), (256, 8, 4, 64), (257, 8, 4, 64), (2049, 8, 4, 64),
+    (1023, 8, 4, 64), (1024, 8, 4, 64), (1025, 8, 4, 64),
     (5000, 8, 4, 256), (5000, 8, 4, 128),       # 128: some rings overflow
     (20000, 3, 5, 2048), (20000, 1, 1, 32768), (7777, 16, 2, 512),
     (100000, 256, 4, 256), (60000, 1024, 1, 128), (300000, 8, 4, 16384)])
