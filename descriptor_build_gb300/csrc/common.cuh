@@ -61,18 +61,30 @@ __device__ __forceinline__ uint32_t ld_table4(const uint32_t* p, uint64_t pol) {
   return v;
 }
 
-// Output stores this kernel never reads back: no L1 allocation, L2 hint `pol`.
+// Output stores this kernel never reads back. DB_STORE_HINT 1: no L1
+// allocation and the L2 policy `pol`; 0: plain stores (`pol` unused).
+#ifndef DB_STORE_HINT
+#define DB_STORE_HINT 1
+#endif
 __device__ __forceinline__ void st_stream16(void* p, uint64_t a, uint64_t b, uint64_t pol) {
-  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u64 [%0], {%1, %2}, %3;" ::"l"(p),
-               "l"(a), "l"(b), "l"(pol)
-               : "memory");
+  if (DB_STORE_HINT)
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u64 [%0], {%1, %2}, %3;" ::"l"(p),
+                 "l"(a), "l"(b), "l"(pol)
+                 : "memory");
+  else
+    asm volatile("st.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 // 32-byte store (sm_100+): p must be 32-byte aligned.
 __device__ __forceinline__ void st_stream32(void* p, uint64_t a, uint64_t b, uint64_t c, uint64_t d,
                                             uint64_t pol) {
-  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u64 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
-               "l"(a), "l"(b), "l"(c), "l"(d), "l"(pol)
-               : "memory");
+  if (DB_STORE_HINT)
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u64 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "l"(a), "l"(b), "l"(c), "l"(d), "l"(pol)
+                 : "memory");
+  else
+    asm volatile("st.global.v4.u64 [%0], {%1, %2, %3, %4};" ::"l"(p), "l"(a), "l"(b), "l"(c),
+                 "l"(d)
+                 : "memory");
 }
 // 32-byte read-only load (sm_100+): p must be 32-byte aligned.
 __device__ __forceinline__ void ld_table32(const void* p, uint64_t pol, uint64_t& a, uint64_t& b,
@@ -82,9 +94,12 @@ __device__ __forceinline__ void ld_table32(const void* p, uint64_t pol, uint64_t
       : "l"(p), "l"(pol));
 }
 __device__ __forceinline__ void st_stream8(void* p, uint64_t a, uint64_t pol) {
-  asm volatile("st.global.L1::no_allocate.L2::cache_hint.u64 [%0], %1, %2;" ::"l"(p), "l"(a),
-               "l"(pol)
-               : "memory");
+  if (DB_STORE_HINT)
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.u64 [%0], %1, %2;" ::"l"(p), "l"(a),
+                 "l"(pol)
+                 : "memory");
+  else
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
 }
 
 __device__ __forceinline__ uint64_t ld_acquire(const unsigned long long* p) {

@@ -359,9 +359,15 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
           hits += 1;
         }
       }
-      __stcs(p.idx + i, out_idx);
-      __stcs(reinterpret_cast<unsigned int*>(p.lkey + i), out_lkey);
-      __stcs(reinterpret_cast<unsigned char*>(p.kind + i), out_kind);
+      if (DB_STORE_HINT) {
+        __stcs(p.idx + i, out_idx);
+        __stcs(reinterpret_cast<unsigned int*>(p.lkey + i), out_lkey);
+        __stcs(reinterpret_cast<unsigned char*>(p.kind + i), out_kind);
+      } else {
+        p.idx[i] = out_idx;
+        p.lkey[i] = out_lkey;
+        p.kind[i] = out_kind;
+      }
     }
   }
   // Counters and hand-off to the next call.

@@ -28,6 +28,10 @@ namespace prp {
 #ifndef DB_PRP_EARLY_LUT
 #define DB_PRP_EARLY_LUT 0
 #endif
+// List words: 32-byte stores with the evict-first L2 hint (1) or plain (0).
+#ifndef DB_PRP_LIST_HINT
+#define DB_PRP_LIST_HINT 0
+#endif
 
 // Tile shape (tunable at build time; defaults measured best on GB300):
 // threads per CTA, requests per thread, minimum resident CTAs per SM.
@@ -140,73 +144,120 @@ __device__ __forceinline__ void four_words(uint32_t t, uint32_t lo_a, uint32_t h
   }
 }
 
-// One long request's list run, written by a whole warp, 128 words per step:
-// lane l writes words 4l .. 4l+3 of the step with one 32-byte store, so a
-// warp store covers 1 KiB of contiguous arena. A step never leaves its 4 KiB
-// page (128 divides 512); the only chain-pointer slot a step can hold is word
-// 127 of the last step of a page. LUT values come by shuffle from two
-// windows of 32 chunks (lane l holds chunks c0 + wrel + l and c0 + wrel +
-// 32 + l); a step spans at most 9 chunks. Once a step lies wholly in the
-// second window the windows move on by 32 and the next 32 chunks are loaded,
-// about four steps before they are needed.
+// List-word stores. Plain stores measured faster than evict-first hinted
+// ones for this pattern (runs at page starts across the whole arena).
+__device__ __forceinline__ void st_list32(void* a, uint64_t x, uint64_t y, uint64_t z, uint64_t w,
+                                          uint64_t pol) {
+  if (DB_PRP_LIST_HINT) {
+    st_stream32(a, x, y, z, w, pol);
+  } else {
+    asm volatile("st.global.v4.u64 [%0], {%1, %2, %3, %4};" ::"l"(a), "l"(x), "l"(y), "l"(z),
+                 "l"(w)
+                 : "memory");
+  }
+}
+__device__ __forceinline__ void st_list8(void* a, uint64_t x, uint64_t pol) {
+  if (DB_PRP_LIST_HINT)
+    st_stream8(a, x, pol);
+  else
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(a), "l"(x) : "memory");
+}
+
+// One long request's list, written by a whole warp a list page (512 words)
+// at a time, in four steps of 128 words: lane l writes words 4l .. 4l+3 of a
+// step with one 32-byte store, so a warp store covers 1 KiB of contiguous
+// arena. Word w of list page j is data entry 511 j + w, which names page
+// position t = p0 + 1 + 511 j + w (w = 511 of a page with a successor is the
+// chain pointer instead). Step k moves a lane's words 128 k positions on,
+// exactly 8 chunks, so a lane's chunk offset and where its four words cross
+// into the next chunk are worked out once per page. The page's LUT values
+// come by shuffle from two windows of 32 chunks anchored at the page's first
+// chunk (lane l holds chunks anchor + l and anchor + 32 + l; the first page
+// is anchored at c0); a page spans at most 34 of them, and the next page's
+// windows load while this one is written.
 __device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, uint64_t win0,
                                           uint64_t win1, int lane, uint64_t pol_lut,
                                           uint64_t pol_out) {
-  uint64_t* dst = p.arena + (it.pb << 9);
-  const uint32_t total = p.zero_tail ? (it.pages << 9) : it.words;
+  uint64_t* const dst0 = p.arena + (it.pb << 9) + 4 * lane;
+  const uint32_t W = it.words;
+  const uint32_t total = p.zero_tail ? (it.pages << 9) : W;
   const uint64_t c0 = it.hb >> 16;
   const uint64_t c_last = last_chunk(it);
   const uint32_t p0 = first_pos(it);
-  uint32_t wrel = 0;
-  for (uint32_t ib = 0; ib < total; ib += 128) {
-    const uint32_t j = ib >> 9;                // list page of this step
-    const uint32_t t_min = p0 + 1 + ib - j;    // page position of the step's first word
-    if ((t_min >> 4) >= wrel + 32) {           // uniform across the warp
-      wrel += 32;
-      win0 = win1;
-      win1 = lut_window(p.lut, c0 + wrel + 32 + lane, c_last, pol_lut);
+  for (uint32_t j = 0; j < it.pages; ++j) {
+    const uint32_t tp = p0 + 1 + 511 * j;            // position of the page's word 0
+    const uint32_t anchor = j == 0 ? 0u : (tp >> 4);  // chunk of window lane 0, from c0
+    const bool last = j + 1 == it.pages;              // uniform across the warp
+    uint64_t nwin0 = 0, nwin1 = 0;
+    if (!last) {
+      const uint64_t na = c0 + ((tp + 511) >> 4);
+      nwin0 = lut_window(p.lut, na + lane, c_last, pol_lut);
+      nwin1 = lut_window(p.lut, na + 32 + lane, c_last, pol_lut);
     }
-    const uint32_t w = ib + 4 * lane;
-    const uint32_t t = t_min + 4 * lane;
-    const uint32_t ra = (t >> 4) - wrel, rb = ((t + 3) >> 4) - wrel;  // < 64
-    uint32_t lo_a, hi_a, lo_b, hi_b;
-    if (((t_min + 127) >> 4) < wrel + 32) {    // the step lies in the first window
-      lo_a = __shfl_sync(kFull, (uint32_t)win0, ra & 31);
-      hi_a = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ra & 31);
-      lo_b = __shfl_sync(kFull, (uint32_t)win0, rb & 31);
-      hi_b = __shfl_sync(kFull, (uint32_t)(win0 >> 32), rb & 31);
-    } else {                                   // it straddles the two windows
-      const uint32_t lo_a0 = __shfl_sync(kFull, (uint32_t)win0, ra & 31);
-      const uint32_t hi_a0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ra & 31);
-      const uint32_t lo_b0 = __shfl_sync(kFull, (uint32_t)win0, rb & 31);
-      const uint32_t hi_b0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), rb & 31);
-      const uint32_t lo_a1 = __shfl_sync(kFull, (uint32_t)win1, ra & 31);
-      const uint32_t hi_a1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), ra & 31);
-      const uint32_t lo_b1 = __shfl_sync(kFull, (uint32_t)win1, rb & 31);
-      const uint32_t hi_b1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), rb & 31);
-      lo_a = ra < 32 ? lo_a0 : lo_a1;
-      hi_a = ra < 32 ? hi_a0 : hi_a1;
-      lo_b = rb < 32 ? lo_b0 : lo_b1;
-      hi_b = rb < 32 ? hi_b0 : hi_b1;
+    const uint32_t tl = tp + 4 * lane;
+    const uint32_t ql = tl & 15;
+    const uint32_t al = (tl >> 4) - anchor;  // at most 8
+    // LUT values are 64 KiB aligned: the in-chunk offset is OR-ed into the low word.
+    uint32_t offs[4];
+    bool useb[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      offs[s] = ((ql + s) & 15u) << 12;
+      useb[s] = ql + s >= 16;
     }
-    uint64_t v[4];
-    four_words(t, lo_a, hi_a, lo_b, hi_b, v);
-    if (lane == 31 && (ib & 511u) == 384u && j + 1 < it.pages)
-      v[3] = p.arena_base + ((it.pb + j + 1) << 12);  // slot 511: next list page
-    if (ib + 128 <= it.words) {                       // a full step of data (uniform)
-      st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
-    } else {
+    const uint32_t wpage = j << 9;
+    uint64_t* const dst = dst0 + wpage;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (last && wpage + 128 * k >= total) break;  // uniform
+      const uint32_t ca = al + 8 * k, cb = ca + 1;   // ca <= 32, cb <= 33
+      uint32_t alo, ahi, blo, bhi;
+      if (k < 3) {                                   // ca <= 24, cb <= 25: first window
+        alo = __shfl_sync(kFull, (uint32_t)win0, ca);
+        ahi = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ca);
+        blo = __shfl_sync(kFull, (uint32_t)win0, cb);
+        bhi = __shfl_sync(kFull, (uint32_t)(win0 >> 32), cb);
+      } else {
+        const uint32_t alo0 = __shfl_sync(kFull, (uint32_t)win0, ca & 31);
+        const uint32_t ahi0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), ca & 31);
+        const uint32_t blo0 = __shfl_sync(kFull, (uint32_t)win0, cb & 31);
+        const uint32_t bhi0 = __shfl_sync(kFull, (uint32_t)(win0 >> 32), cb & 31);
+        const uint32_t alo1 = __shfl_sync(kFull, (uint32_t)win1, ca & 31);
+        const uint32_t ahi1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), ca & 31);
+        const uint32_t blo1 = __shfl_sync(kFull, (uint32_t)win1, cb & 31);
+        const uint32_t bhi1 = __shfl_sync(kFull, (uint32_t)(win1 >> 32), cb & 31);
+        alo = ca < 32 ? alo0 : alo1;
+        ahi = ca < 32 ? ahi0 : ahi1;
+        blo = cb < 32 ? blo0 : blo1;
+        bhi = cb < 32 ? bhi0 : bhi1;
+      }
+      uint64_t v[4];
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        if (w + s >= it.words) v[s] = 0;  // zeroed tail
-      if (w + 3 < total) {
-        st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
+        v[s] = ((uint64_t)(useb[s] ? bhi : ahi) << 32) | ((useb[s] ? blo : alo) | offs[s]);
+      if (!last) {
+        if (k == 3 && lane == 31) v[3] = p.arena_base + ((it.pb + j + 1) << 12);  // chain pointer
+        st_list32(dst + 128 * k, v[0], v[1], v[2], v[3], pol_out);
       } else {
+        const uint32_t w = wpage + 128 * k + 4 * lane;
+        if (wpage + 128 * k + 128 <= W) {            // a full step of data (uniform)
+          st_list32(dst + 128 * k, v[0], v[1], v[2], v[3], pol_out);
+        } else {
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          if (w + s < total) st_stream8(dst + w + s, v[s], pol_out);
+          for (int s = 0; s < 4; ++s)
+            if (w + s >= W) v[s] = 0;  // zeroed tail
+          if (w + 3 < total) {
+            st_list32(dst + 128 * k, v[0], v[1], v[2], v[3], pol_out);
+          } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              if (w + s < total) st_list8(dst + 128 * k + s, v[s], pol_out);
+          }
+        }
       }
     }
+    win0 = nwin0;
+    win1 = nwin1;
   }
 }
 
@@ -243,11 +294,11 @@ __device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, 
       if (w + s >= it.words) v[s] = 0;  // zeroed tail
     if (valid) {
       if (w + 3 < total) {
-        st_stream32(dst + w, v[0], v[1], v[2], v[3], pol_out);
+        st_list32(dst + w, v[0], v[1], v[2], v[3], pol_out);
       } else {
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          if (w + s < total) st_stream8(dst + w + s, v[s], pol_out);
+          if (w + s < total) st_list8(dst + w + s, v[s], pol_out);
       }
     }
   }
