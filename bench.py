@@ -111,15 +111,26 @@ def peak_gbs():
         return 6800.0, "fallback"
 
 
+def source_sha256(kernel_src: str) -> str:
+    """Hash of what a kernel is built from: its file, the shared device
+    header and the public header."""
+    h = hashlib.sha256()
+    for path in (os.path.join(ROOT, "descriptor_build_gb300", "csrc", kernel_src),
+                 os.path.join(ROOT, "descriptor_build_gb300", "csrc", "common.cuh"),
+                 os.path.join(ROOT, "include", "descbuild.h")):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def recorded_traffic(kernel_src: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernel source as it is now (else None)."""
+    on the kernel sources as they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
-        src = open(os.path.join(ROOT, "descriptor_build_gb300", "csrc", kernel_src), "rb").read()
-        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+        if source_sha256(kernel_src) != rec["source_sha256"]:
             return None
         return int(rec["dram_bytes_per_launch"])
     except Exception:
