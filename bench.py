@@ -102,6 +102,22 @@ def units(inp) -> dict:
             for k, w in inp.items()}
 
 
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """The largest of every rank's value, on every rank (the value itself
+    without a process group). NCCL wants a device tensor, gloo a host one."""
+    if not dist:
+        return value
+    import torch
+    tt = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(world: int, reqs_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job M requests/s: every rank's requests over the slowest rank's step."""
+    return world * reqs_per_rank_step / (ms_per_step * 1e-3) / 1e6
+
+
 def peak_gbs():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -312,11 +328,8 @@ def run_ours(args, inp, world, device, dist):
             step_ev[k][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(device)
-    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(dist, t0.elapsed_time(t1), device)
     if dist:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
         dist.barrier()
     st.check_counters()
     per_kernel_ms = {name: statistics.mean(evs[k][j][0].elapsed_time(evs[k][j][1])
@@ -328,7 +341,7 @@ def run_ours(args, inp, world, device, dist):
     peak, peak_kind = peak_gbs()
     reqs_per_step = sum(u.values())
     ms_per_step = total_ms / K
-    value = world * reqs_per_step / (ms_per_step * 1e-3) / 1e6
+    value = job_throughput(world, reqs_per_step, ms_per_step)
     kernels = {}
     for name in u:
         ms = per_kernel_ms[name]
@@ -409,13 +422,9 @@ def run_e2e(st, stream, inp, K, device, dist, world):
         one()
     b.record(stream)
     t.cuda.synchronize(device)
-    ms = a.elapsed_time(b) / K
-    if dist:
-        tt = t.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(dist, a.elapsed_time(b) / K, device)
     reqs = sum(units(inp).values())
-    return {"value": round(world * reqs / (ms * 1e-3) / 1e6, 2), "unit": UNIT,
+    return {"value": round(job_throughput(world, reqs, ms), 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "steps": K, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo}
 
