@@ -63,6 +63,9 @@ def _load():
             lib.oracle_wqe_bucket.restype = None
             lib.oracle_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64,
                                               vp, vp, vp]
+            lib.oracle_wqe_bucket_vmm.restype = None
+            lib.oracle_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64,
+                                                  vp, u64, vp, vp, vp]
             _lib = lib
     return _lib
 
@@ -180,4 +183,30 @@ def wqe_bucket(req, peer_ptrs, rkeys, world: int, n_qp: int, local_base: int, lk
     _load().oracle_wqe_bucket(_p(req), req.shape[0], _p(peer_ptrs), _p(rkeys), world, n_qp,
                               local_base, lkey, heap_size, _p(rings), depth, _p(head),
                               _p(count), _p(ctr))
+    return dict(rings=rings, head=head, count=count, ctr=ctr)
+
+
+def wqe_bucket_vmm(req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift: int, world: int,
+                   n_qp: int, local_base: int, heap_size: int, depth: int, head,
+                   fill: int = 0, rings: np.ndarray | None = None) -> dict:
+    """Put translation on a VMM heap: one WQE per chunk a put touches.
+    chunk_raddr / chunk_rkey are [world, n_chunks], chunk_lkey [n_chunks]."""
+    req = _u64(req).reshape(-1, 2)
+    n_chunks = -(-heap_size // (1 << chunk_shift))
+    chunk_raddr = _u64(chunk_raddr).reshape(-1)
+    chunk_rkey = np.ascontiguousarray(chunk_rkey, dtype=np.uint32).reshape(-1)
+    chunk_lkey = np.ascontiguousarray(chunk_lkey, dtype=np.uint32).reshape(-1)
+    assert chunk_raddr.shape[0] == world * n_chunks and chunk_rkey.shape[0] == world * n_chunks
+    assert chunk_lkey.shape[0] == n_chunks
+    n_rings = world * n_qp
+    if rings is None:
+        rings = np.full((n_rings, depth, 64), fill, dtype=np.uint8)
+    else:
+        assert rings.dtype == np.uint8 and rings.shape == (n_rings, depth, 64)
+    head = _u64(head).copy()
+    count = np.zeros(n_rings, dtype=np.uint32)
+    ctr = np.zeros(4, dtype=np.uint64)
+    _load().oracle_wqe_bucket_vmm(_p(req), req.shape[0], _p(chunk_raddr), _p(chunk_rkey),
+                                  _p(chunk_lkey), chunk_shift, world, n_qp, local_base,
+                                  heap_size, _p(rings), depth, _p(head), _p(count), _p(ctr))
     return dict(rings=rings, head=head, count=count, ctr=ctr)

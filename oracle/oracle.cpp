@@ -20,8 +20,10 @@
 //    Registration Cache" (page_floor / page_cover, sorted records).
 //  * Put translation -- "mori communication library analysis (1)": static
 //    heap address/key computation (raddr = peerPtrs[pe] + offset,
-//    rkey = peerRkeys[pe], lkey = the source object's lkey) and the
-//    warp-level WQE slot reservation (a post index per send queue).
+//    rkey = peerRkeys[pe], lkey = the source object's lkey), the VMM-heap
+//    branch (one WQE per chunk: min of the source and destination chunk
+//    remainders and the bytes left) and the warp-level WQE slot reservation
+//    (a post index per send queue).
 //
 // Readings where the pages are silent are listed with each function.
 //
@@ -360,6 +362,123 @@ void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptr
     put_u64(wqe + 32, seq);
     put_u32(wqe + 40, (uint32_t)i);
     posted += 1;
+  }
+  // 4. Advance heads of the rings that took their batch.
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    count[r] = (uint32_t)demand[r];
+    if (!full[r]) head[r] += demand[r];
+  }
+  ctr[0] = posted;
+  ctr[1] = n_invalid;
+  ctr[2] = n_overflow;
+  ctr[3] = err;
+}
+
+// Put translation on a VMM heap -- "mori communication library analysis
+// (1)", the VMM-heap branch of the put path: while bytes remain, look up the
+// chunk holding the current source address (its lkey and how many bytes of
+// it remain) and the chunk holding the current destination address on the
+// target PE (its remote address, rkey and remainder); send
+// min(source remainder, destination remainder, remaining) bytes as one WQE;
+// advance. Readings (the page does not give the chunk layout):
+//  * the heap is cut into chunks of 2^chunk_shift bytes at the same offsets
+//    on every PE; local chunk c has lkey chunk_lkey[c]; chunk c of PE pe sits
+//    at remote address chunk_raddr[pe * n_chunks + c] with rkey
+//    chunk_rkey[pe * n_chunks + c] (n_chunks = ceil(heap_size / 2^chunk_shift));
+//  * a put covers the same symmetric range [off, off + bytes) on both sides,
+//    and laddr is local_base + the fragment's offset;
+//  * a put's fragments take consecutive post indices in its ring, in address
+//    order, each carrying the put's batch index; validity and ring order are
+//    those of the static heap;
+//  * a ring asked for more than `depth` WQEs by the batch takes none;
+//    counters: WQEs posted, invalid puts, WQEs of overflowing rings, err.
+void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chunk_raddr,
+                           const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
+                           uint32_t chunk_shift, uint32_t world, uint32_t n_qp,
+                           uint64_t local_base, uint64_t heap_size, uint8_t* rings,
+                           uint64_t depth, uint64_t* head, uint32_t* count, uint64_t* ctr) {
+  const uint64_t C = 1ull << chunk_shift;
+  const uint64_t n_chunks = (heap_size + C - 1) / C;
+  uint64_t n_rings = (uint64_t)world * n_qp;
+  std::vector<uint64_t> demand(n_rings, 0);
+  std::vector<int> ring_of(n);
+  uint64_t n_invalid = 0;
+  // One pass of the page's loop, emitting nothing: how many WQEs a put makes.
+  auto fragments = [&](uint64_t off, uint64_t bytes) {
+    uint64_t cur = 0, remaining = bytes, k = 0;
+    while (remaining > 0) {
+      const uint64_t src = off + cur, dst = off + cur;
+      const uint64_t src_left = C - (src % C), dst_left = C - (dst % C);
+      const uint64_t t = std::min(std::min(src_left, dst_left), remaining);
+      cur += t;
+      remaining -= t;
+      k += 1;
+    }
+    return k;
+  };
+  // 1. Validate and count WQEs per ring.
+  for (uint64_t i = 0; i < n; ++i) {
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint64_t bytes = w1 & 0xFFFFFFFFull;
+    uint64_t pe = (w1 >> 32) & 0xFFFF;
+    uint64_t qp = (w1 >> 48) & 0xFFFF;
+    bool ok = pe < world && qp < n_qp && bytes >= 1 &&
+              (u128)off + (u128)bytes <= (u128)heap_size;
+    if (!ok) {
+      ring_of[i] = -1;
+      n_invalid += 1;
+      continue;
+    }
+    const int ring = (int)(pe * n_qp + qp);  // PE-major, as for the static heap
+    ring_of[i] = ring;
+    demand[ring] += fragments(off, bytes);
+  }
+  // 2. Overflowing rings take nothing.
+  uint64_t n_overflow = 0, posted = 0, err = 0;
+  std::vector<bool> full(n_rings, false);
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    if (depth < demand[r]) {
+      full[r] = true;
+      n_overflow += demand[r];
+      err |= 2;
+    }
+  }
+  // 3. Post in request order, each put's fragments in address order.
+  std::vector<uint64_t> taken(n_rings, 0);
+  for (uint64_t i = 0; i < n; ++i) {
+    int r = ring_of[i];
+    if (r < 0 || full[r]) continue;
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint64_t bytes = w1 & 0xFFFFFFFFull;
+    uint32_t pe = (uint32_t)((w1 >> 32) & 0xFFFF);
+    uint64_t cur = 0, remaining = bytes;
+    while (remaining > 0) {
+      const uint64_t src = off + cur, dst = off + cur;
+      const uint64_t src_chunk = src / C, dst_chunk = dst / C;
+      if (src_chunk >= n_chunks || dst_chunk >= n_chunks) std::abort();  // inside the heap
+      const uint32_t lkey = chunk_lkey[src_chunk];
+      const uint64_t raddr = chunk_raddr[pe * n_chunks + dst_chunk] + (dst % C);
+      const uint32_t rkey = chunk_rkey[pe * n_chunks + dst_chunk];
+      const uint64_t src_left = C - (src % C), dst_left = C - (dst % C);
+      const uint64_t t = std::min(std::min(src_left, dst_left), remaining);
+      const uint64_t post = head[r] + taken[r];  // the ring's next post index
+      taken[r] += 1;
+      uint8_t* wqe = rings + ((uint64_t)r * depth + (post % depth)) * 64;
+      std::memset(wqe, 0, 64);
+      put_u64(wqe + 0, raddr);
+      put_u64(wqe + 8, local_base + src);
+      put_u32(wqe + 16, (uint32_t)t);
+      put_u32(wqe + 20, lkey);
+      put_u32(wqe + 24, rkey);
+      put_u32(wqe + 28, 0);
+      put_u64(wqe + 32, post);
+      put_u32(wqe + 40, (uint32_t)i);
+      posted += 1;
+      cur += t;
+      remaining -= t;
+    }
   }
   // 4. Advance heads of the rings that took their batch.
   for (uint64_t r = 0; r < n_rings; ++r) {

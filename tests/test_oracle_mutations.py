@@ -54,6 +54,19 @@ MUTANTS = [
      "if (demand[r] > depth) {", "if (demand[r] >= depth) {"),
     ("wqe raddr from the local base",
      "put_u64(wqe + 0, peer_ptrs[pe] + off);", "put_u64(wqe + 0, local_base + off);"),
+    ("vmm raddr adds the heap offset, not the chunk offset",
+     "chunk_raddr[pe * n_chunks + dst_chunk] + (dst % C);",
+     "chunk_raddr[pe * n_chunks + dst_chunk] + dst;"),
+    ("vmm lkey of chunk 0",
+     "const uint32_t lkey = chunk_lkey[src_chunk];", "const uint32_t lkey = chunk_lkey[0];"),
+    ("vmm rkey of the PE's first chunk",
+     "const uint32_t rkey = chunk_rkey[pe * n_chunks + dst_chunk];",
+     "const uint32_t rkey = chunk_rkey[pe * n_chunks];"),
+    ("vmm laddr does not advance per fragment",
+     "put_u64(wqe + 8, local_base + src);", "put_u64(wqe + 8, local_base + off);"),
+    ("vmm fragment runs 16 bytes past its chunk",
+     "const uint64_t t = std::min(std::min(src_left, dst_left), remaining);\n      const uint64_t post",
+     "const uint64_t t = std::min(src_left + 16, remaining);\n      const uint64_t post"),
 ]
 
 
@@ -68,7 +81,8 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
                    check=True)
     env = dict(os.environ, DB_ORACLE_LIB=str(lib))
     tests = [os.path.join(ROOT, "tests", f) for f in
-             ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py")]
+             ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
+              "test_oracle_vmm.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
