@@ -28,7 +28,8 @@ from . import build as _build
 __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
-    "mr_workspace_size", "mr_lookup", "wqe_workspace_size", "wqe_bucket", "strerror",
+    "mr_workspace_size", "mr_lookup", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
+    "strerror",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
 ]
@@ -67,9 +68,11 @@ def _load():
     lib.db_wqe_workspace_size.argtypes = [u64, u32, psz]
     lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
                                   vp, sz, vp]
+    lib.db_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64, vp, u64, vp,
+                                      vp, vp, vp, sz, vp]
     for name in ("db_prp_workspace_size", "db_prp_build", "db_prp_build_static",
                  "db_mr_workspace_size",
-                 "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket",
+                 "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
                  "db_last_cuda_error"):
         getattr(lib, name).restype = i32
     lib.db_strerror.argtypes = [i32]
@@ -192,3 +195,16 @@ def wqe_bucket(req: torch.Tensor, peer_ptrs: torch.Tensor, rkeys: torch.Tensor, 
         _ptr(req), n, _ptr(peer_ptrs), _ptr(rkeys), world, n_qp, local_base, lkey, heap_size,
         _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(ctr), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def wqe_bucket_vmm(req: torch.Tensor, chunk_raddr: torch.Tensor, chunk_rkey: torch.Tensor,
+                   chunk_lkey: torch.Tensor, chunk_shift: int, world: int, n_qp: int,
+                   local_base: int, heap_size: int, rings: torch.Tensor, depth: int,
+                   head: torch.Tensor, count: torch.Tensor, ws: torch.Tensor,
+                   ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_wqe_bucket_vmm: puts on a chunked (VMM) heap, one WQE per chunk touched."""
+    n = _records(req, 16)
+    _check("db_wqe_bucket_vmm", _lib.db_wqe_bucket_vmm(
+        _ptr(req), n, _ptr(chunk_raddr), _ptr(chunk_rkey), _ptr(chunk_lkey), chunk_shift, world,
+        n_qp, local_base, heap_size, _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(ctr),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))

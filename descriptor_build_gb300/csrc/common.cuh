@@ -194,7 +194,11 @@ __device__ __forceinline__ void end_of_call(ScanHeader* h, unsigned long long* s
   __threadfence();
 }
 
-// Backoff for a bounded spin. Returns false once the wait has lasted kWaitLimitNs.
+// Backoff for a bounded spin: sleeps doubling from 32 ns up to
+// DB_BACKOFF_MAX_NS. Returns false once the wait has lasted kWaitLimitNs.
+#ifndef DB_BACKOFF_MAX_NS
+#define DB_BACKOFF_MAX_NS 2048
+#endif
 struct Backoff {
   uint64_t t0;
   uint32_t ns;
@@ -202,7 +206,7 @@ struct Backoff {
   __device__ __forceinline__ bool wait() {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     __nanosleep(ns);
-    if (ns < 2048) ns <<= 1;
+    if (ns < DB_BACKOFF_MAX_NS) ns <<= 1;
     return true;
   }
 };
@@ -245,6 +249,33 @@ __device__ __forceinline__ void block_excl_scan(uint32_t v, uint32_t& excl, uint
   }
   __syncthreads();
   excl = (warp ? s_warp[warp - 1] : 0u) + x - v;
+  total = s_warp[kWarps - 1];
+}
+
+// The same scan on 64-bit values.
+template <int kWarps>
+__device__ __forceinline__ void block_excl_scan64(uint64_t v, uint64_t& excl, uint64_t& total,
+                                                  uint64_t* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint64_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t w = lane < kWarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint64_t y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kWarps) s_warp[lane] = w;
+  }
+  __syncthreads();
+  excl = (warp ? s_warp[warp - 1] : 0ull) + x - v;
   total = s_warp[kWarps - 1];
 }
 

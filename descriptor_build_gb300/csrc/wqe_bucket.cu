@@ -84,6 +84,13 @@ struct Params {
   uint64_t* head_old;
   uint32_t* full;
   uint32_t* counts;  // [V][stride], first n_tiles of each column used
+  // VMM heap: chunks of 2^cshift bytes; a put makes one WQE per chunk.
+  bool vmm;
+  uint32_t cshift;
+  uint64_t n_chunks;
+  const uint64_t* chunk_raddr;  // [world][n_chunks]
+  const uint32_t* chunk_rkey;   // [world][n_chunks]
+  const uint32_t* chunk_lkey;   // [n_chunks]
 };
 
 // Ring of a put, or R for an invalid one.
@@ -95,6 +102,13 @@ __device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) 
   const bool ok = pe < p.world && qp < p.n_qp && bytes != 0 && off <= p.heap_size &&
                   (uint64_t)bytes <= p.heap_size - off;
   return ok ? pe * p.n_qp + qp : p.R;
+}
+
+// WQEs a valid put makes: one, or on a VMM heap one per chunk it touches.
+__device__ __forceinline__ uint32_t wqes_of(const Params& p, const ulonglong2 r) {
+  if (!p.vmm) return 1;
+  const uint64_t off = r.x, last = r.x + (uint32_t)r.y - 1;
+  return (uint32_t)((last >> p.cshift) - (off >> p.cshift)) + 1;
 }
 
 // ---------------------------------------------------------------- count pass
@@ -130,10 +144,16 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
         const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
         const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
         if (DB_WQE_COUNT_MODE == 1) {
-          if (bin < V) atomicAdd(&s_hist[bin], 1u);
+          if (bin < p.R) atomicAdd(&s_hist[bin], wqes_of(p, r[u]));
+          else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
         } else {
           const uint32_t peers = __match_any_sync(kFull, bin);
-          if (bin < V && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[bin], __popc(peers));
+          if (p.vmm) {  // weights differ per put
+            if (bin < p.R) atomicAdd(&s_hist[bin], wqes_of(p, r[u]));
+            else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
+          } else if (bin < V && (peers & lanemask_lt()) == 0) {
+            atomicAdd(&s_hist[bin], __popc(peers));
+          }
         }
       }
     }
@@ -145,14 +165,16 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
 
 // ----------------------------------------------------------------- scan pass
 // One CTA per bin: each thread takes 32 consecutive column entries (16-byte
-// loads and stores), so a column of up to 32768 tiles is one round.
+// loads and stores), so a column of up to 32768 tiles is one round. Sums are
+// 64-bit; the prefixes are stored in 32 bits, exact for any ring whose batch
+// total fits the ring (depth <= 2^31), which are the only ones written.
 constexpr int kScanThreads = 1024;
 constexpr int kScanPer = 32;
 constexpr uint64_t kScanSeg = (uint64_t)kScanThreads * kScanPer;
 
 __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) {
   constexpr int kW = kScanThreads / 32;
-  __shared__ uint32_t s_scan[kW];
+  __shared__ uint64_t s_scan[kW];
   __shared__ int s_last;
   const uint32_t v = blockIdx.x;
   uint32_t* col = p.counts + (uint64_t)v * p.stride;
@@ -174,12 +196,12 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
 #pragma unroll
       for (int j = 0; j < kScanPer; ++j) c[j] = b + j < T ? col[b + j] : 0u;
     }
-    uint32_t mine = 0;
+    uint64_t mine = 0;
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) mine += c[j];
-    uint32_t excl, seg_total;
-    block_excl_scan<kW>(mine, excl, seg_total, s_scan);
-    uint32_t run = (uint32_t)carry + excl;
+    uint64_t excl, seg_total;
+    block_excl_scan64<kW>(mine, excl, seg_total, s_scan);
+    uint32_t run = (uint32_t)(carry + excl);
 #pragma unroll
     for (int j = 0; j < kScanPer; ++j) {
       const uint32_t x = c[j];
@@ -203,7 +225,7 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
     if (v < p.R) {
       const uint64_t h = p.head[v];
       const bool over = total > p.depth;
-      p.count[v] = (uint32_t)total;
+      p.count[v] = total < 0xFFFFFFFFull ? (uint32_t)total : 0xFFFFFFFFu;
       p.head_old[v] = h;
       p.full[v] = over ? 1u : 0u;
       if (!over) p.head[v] = h + total;
@@ -362,14 +384,182 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
   }
 }
 
+// ------------------------------------------------------ scatter, VMM heap
+// As wqe_scatter_kernel, but a put makes one WQE per chunk it touches. The
+// tile's puts are put in ring order as before (a put-count permutation);
+// then an exclusive prefix of WQE counts over that order gives each put's
+// first WQE, and the write-out walks the tile's WQEs in that order (each
+// ring's WQEs contiguous in its ring), finding a WQE's put by binary search.
+// Per warp: puts, per-ring first sequence number, run start in puts and in
+// WQEs, per-row ring counts, the permutation and the WQE prefix.
+__host__ __device__ inline size_t vmm_warp_smem(uint32_t V) {
+  size_t b = (size_t)kTile * 16;      // puts
+  b += (size_t)V * 8;                 // first sequence number per ring
+  b += (size_t)V * 4 * 2;             // run start (puts), run start (WQEs)
+  b += (size_t)kRows * V * 2;         // per-row counts
+  b += (size_t)kTile * 2;             // permutation
+  b += (size_t)(kTile + 1) * 4;       // WQE prefix over the ring order
+  return (b + 15) & ~(size_t)15;
+}
+inline int vmm_scatter_warps(uint32_t V) {
+  const size_t fit = (kMaxSmem - cta_smem(V)) / vmm_warp_smem(V);
+  return (int)(fit < (size_t)kSWarps ? fit : (size_t)kSWarps);
+}
+inline size_t vmm_scatter_smem(uint32_t V) { return cta_smem(V) + vmm_scatter_warps(V) * vmm_warp_smem(V); }
+
+__global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const uint32_t V = p.V, R = p.R;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint64_t pol_first = policy_evict_first();
+  uint64_t* s_slots = reinterpret_cast<uint64_t*>(smem);
+  unsigned char* w = smem + cta_smem(V) + warp * vmm_warp_smem(V);
+  ulonglong2* s_put = reinterpret_cast<ulonglong2*>(w);
+  uint64_t* s_seq0 = reinterpret_cast<uint64_t*>(s_put + kTile);
+  uint32_t* s_run = reinterpret_cast<uint32_t*>(s_seq0 + V);
+  uint32_t* s_wrun = s_run + V;
+  uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_wrun + V);  // [kRows][V]
+  uint16_t* s_perm = s_cnt + kRows * V;
+  uint32_t* s_wstart = reinterpret_cast<uint32_t*>(s_perm + kTile);  // [kTile + 1]
+
+  for (uint32_t v = threadIdx.x; v < R; v += blockDim.x)
+    s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
+  __syncthreads();  // the only CTA-wide barrier
+  const uint64_t tile = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  if (tile >= p.n_tiles) return;
+  const uint64_t t0 = tile * kTile;
+
+  // 1. Load the tile; ring of each put; rank inside its row; per-row counts.
+  for (uint32_t x = lane; x < kRows * V; x += 32) s_cnt[x] = 0;
+  ulonglong2 r[kRows];
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
+    r[u] = i < p.n ? ld_stream16(p.req + i, pol_first) : make_ulonglong2(0, 0);
+  }
+  __syncwarp();
+  uint32_t bin_rank[kRows];  // ring | rank << 16
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
+    const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
+    s_put[u * 32 + lane] = r[u];
+    const uint32_t peers = __match_any_sync(kFull, bin);
+    const uint32_t before = peers & lanemask_lt();
+    if (bin < V && before == 0) s_cnt[u * V + bin] = (uint16_t)__popc(peers);
+    bin_rank[u] = bin | ((uint32_t)__popc(before) << 16);
+  }
+  __syncwarp();
+  // 2. Per ring: prefix of its put counts over the rows, where its run of
+  //    puts starts, and the tile's first sequence number.
+  uint32_t carry = 0;
+  for (uint32_t v0 = 0; v0 < R; v0 += 32) {
+    const uint32_t v = v0 + lane;
+    uint32_t tot = 0;
+    if (v < R) {
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        const uint32_t c = s_cnt[u * V + v];
+        s_cnt[u * V + v] = (uint16_t)tot;
+        tot += c;
+      }
+    }
+    uint32_t x = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (v < R) {
+      s_run[v] = carry + x - tot;
+      s_seq0[v] = p.head_old[v] + p.counts[(uint64_t)v * p.stride + tile];
+    }
+    carry += __shfl_sync(kFull, x, 31);
+  }
+  const uint32_t n_valid = carry;
+  __syncwarp();
+  // 3. Ring-order permutation of the valid puts.
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint32_t bin = bin_rank[u] & 0xFFFFu;
+    if (bin < R) s_perm[s_run[bin] + s_cnt[u * V + bin] + (bin_rank[u] >> 16)] = (uint16_t)(u * 32 + lane);
+  }
+  __syncwarp();
+  // 4. Exclusive prefix of WQE counts over the ring order (lane l takes
+  //    positions 8l .. 8l + 7), and where each ring's WQEs start.
+  constexpr int kPer = kTile / 32;
+  uint32_t kq[kPer], mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const uint32_t q = lane * kPer + j;
+    kq[j] = q < n_valid ? wqes_of(p, s_put[s_perm[q]]) : 0u;
+    mine += kq[j];
+  }
+  uint32_t x = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  uint32_t run = x - mine;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    s_wstart[lane * kPer + j] = run;
+    run += kq[j];
+  }
+  const uint32_t n_wqe = __shfl_sync(kFull, x, 31);
+  if (lane == 0) s_wstart[kTile] = n_wqe;
+  __syncwarp();
+  for (uint32_t v = lane; v < R; v += 32) s_wrun[v] = s_wstart[s_run[v]];
+  __syncwarp();
+  // 5. Write-out: lanes 2w and 2w + 1 write the two halves of the tile's
+  //    WQE w (ring order); its put is the last one whose first WQE is at or
+  //    before w.
+  const uint64_t C = 1ull << p.cshift;
+  const uint64_t slot_mask = p.depth - 1;
+  for (uint64_t f = lane; f < 2ull * n_wqe; f += 32) {
+    const uint32_t wq = (uint32_t)(f >> 1), h = (uint32_t)(f & 1);
+    uint32_t lo = 0, hi = n_valid;  // s_wstart[lo] <= wq < s_wstart[hi]
+    while (hi - lo > 1) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (s_wstart[mid] <= wq) lo = mid;
+      else hi = mid;
+    }
+    const uint32_t o = s_perm[lo];
+    const uint32_t frag = wq - s_wstart[lo];
+    const ulonglong2 pu = s_put[o];
+    const uint32_t pe = (uint32_t)(pu.y >> 32) & 0xFFFFu, qp = (uint32_t)(pu.y >> 48);
+    const uint32_t v = pe * p.n_qp + qp;
+    const uint64_t slots = s_slots[v];
+    if (!slots) continue;
+    const uint64_t seq = s_seq0[v] + (wq - s_wrun[v]);
+    const uint64_t c = (pu.x >> p.cshift) + frag;  // the fragment's chunk
+    const uint64_t start = frag == 0 ? pu.x : (c << p.cshift);
+    const uint64_t stop = pu.x + (uint32_t)pu.y;
+    const uint64_t end = ((c + 1) << p.cshift) < stop ? ((c + 1) << p.cshift) : stop;
+    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6)) + 32 * h;
+    if (h == 0) {
+      const uint64_t rc = (uint64_t)pe * p.n_chunks + c;
+      st_stream32(d, __ldg(p.chunk_raddr + rc) + (start & (C - 1)), p.local_base + start,
+                  (end - start) | ((uint64_t)__ldg(p.chunk_lkey + c) << 32),
+                  (uint64_t)__ldg(p.chunk_rkey + rc), pol_first);
+    } else {
+      st_stream32(d, seq, t0 + o, 0ull, 0ull, pol_first);
+    }
+  }
+}
+
 // Allow the scatter kernel its largest shared-memory footprint (once per device).
 int prepare_scatter() {
   static bool done_for[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (!done_for[dev & 63]) {
-    const cudaError_t e = cudaFuncSetAttribute(
+    cudaError_t e = cudaFuncSetAttribute(
         wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    if (e != cudaSuccess) return cuda_failure(e);
+    e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
   }
@@ -387,12 +577,14 @@ extern "C" int db_wqe_workspace_size(uint64_t n, uint32_t n_rings, size_t* bytes
   return 0;
 }
 
-extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
-                             const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
-                             uint64_t local_base, uint32_t lkey, uint64_t heap_size,
-                             db_wqe* rings, uint64_t depth, uint64_t* head, uint32_t* count,
-                             db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
-  cudaStream_t s = (cudaStream_t)stream;
+namespace {
+
+// Checks shared by both entry points; fills the common Params fields.
+// Returns 0, a negative errno, or 1 for an empty batch already handled.
+int setup(wqe::Params& p, const db_put_req* req, uint64_t n, uint32_t world, uint32_t n_qp,
+          uint64_t local_base, uint64_t heap_size, db_wqe* rings, uint64_t depth,
+          uint64_t* head, uint32_t* count, db_counters* ctr, void* ws, size_t ws_bytes,
+          cudaStream_t s) {
   if (world == 0 || n_qp == 0 || (uint64_t)world * n_qp > wqe::kMaxRings) return -EINVAL;
   if (depth == 0 || (depth & (depth - 1)) != 0) return -EINVAL;
   if (n >= (1ull << 32)) return -EINVAL;
@@ -402,29 +594,23 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   if (n == 0) {
     cudaMemsetAsync(count, 0, (size_t)R * 4, s);
     if (ctr) cudaMemsetAsync(ctr, 0, sizeof(db_counters), s);
-    return launch_result();
+    const int rc = launch_result();
+    return rc ? rc : 1;
   }
-  if (!req || !peer_ptrs || !rkeys || !rings || !head || !ws) return -EINVAL;
-  if (!aligned(req, 16) || !aligned(peer_ptrs, 8) || !aligned(rkeys, 4) || !aligned(rings, 64) ||
-      !aligned(head, 8) || !aligned(ws, 256))
+  if (!req || !rings || !head || !ws) return -EINVAL;
+  if (!aligned(req, 16) || !aligned(rings, 64) || !aligned(head, 8) || !aligned(ws, 256))
     return -EINVAL;
-  const uint64_t n_tiles = wqe::tiles_for(n);
   if (ws_bytes < wqe::ws_bytes_for(n, R)) return -ENOSPC;
-
   char* w = static_cast<char*>(ws);
-  wqe::Params p;
   p.req = reinterpret_cast<const ulonglong2*>(req);
   p.n = n;
-  p.n_tiles = n_tiles;
+  p.n_tiles = wqe::tiles_for(n);
   p.stride = wqe::stride_for(n);
-  p.peer_ptrs = peer_ptrs;
-  p.rkeys = rkeys;
   p.world = world;
   p.n_qp = n_qp;
   p.R = R;
   p.V = R + 1;
   p.local_base = local_base;
-  p.lkey = lkey;
   p.heap_size = heap_size;
   p.rings = reinterpret_cast<unsigned char*>(rings);
   p.depth = depth;
@@ -435,11 +621,15 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   p.head_old = reinterpret_cast<uint64_t*>(w + wqe::kHeadOldOff);
   p.full = reinterpret_cast<uint32_t*>(w + wqe::kFullOff);
   p.counts = reinterpret_cast<uint32_t*>(w + wqe::kCountsOff);
+  return 0;
+}
 
+// Count, scan, scatter.
+int run(const wqe::Params& p, cudaStream_t s) {
   int rc = wqe::prepare_scatter();
   if (rc) return rc;
   uint64_t count_grid = (uint64_t)num_sms() * 8;
-  const uint64_t count_need = (n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
+  const uint64_t count_need = (p.n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
   if (count_grid > count_need) count_grid = count_need;
   wqe::wqe_count_kernel<<<(unsigned)count_grid, wqe::kCountThreads,
                           (size_t)wqe::kCountWarps * p.V * 4, s>>>(p);
@@ -448,8 +638,62 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
-  const int sw = wqe::scatter_warps(p.V);  // at least 6 for the largest ring count
-  const uint64_t scatter_grid = (n_tiles + sw - 1) / sw;
-  wqe::wqe_scatter_kernel<<<(unsigned)scatter_grid, sw * 32, wqe::scatter_smem(p.V), s>>>(p);
+  if (!p.vmm) {
+    const int sw = wqe::scatter_warps(p.V);  // kSWarps, fewer when many rings
+    const uint64_t grid = (p.n_tiles + sw - 1) / sw;
+    wqe::wqe_scatter_kernel<<<(unsigned)grid, sw * 32, wqe::scatter_smem(p.V), s>>>(p);
+  } else {
+    const int sw = wqe::vmm_scatter_warps(p.V);
+    const uint64_t grid = (p.n_tiles + sw - 1) / sw;
+    wqe::wqe_scatter_vmm_kernel<<<(unsigned)grid, sw * 32, wqe::vmm_scatter_smem(p.V), s>>>(p);
+  }
   return launch_result();
+}
+
+}  // namespace
+
+extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
+                             const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
+                             uint64_t local_base, uint32_t lkey, uint64_t heap_size,
+                             db_wqe* rings, uint64_t depth, uint64_t* head, uint32_t* count,
+                             db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  wqe::Params p{};
+  const int rc = setup(p, req, n, world, n_qp, local_base, heap_size, rings, depth, head, count,
+                       ctr, ws, ws_bytes, s);
+  if (rc) return rc < 0 ? rc : 0;
+  if (!peer_ptrs || !rkeys || !aligned(peer_ptrs, 8) || !aligned(rkeys, 4)) return -EINVAL;
+  p.peer_ptrs = peer_ptrs;
+  p.rkeys = rkeys;
+  p.lkey = lkey;
+  p.vmm = false;
+  return run(p, s);
+}
+
+extern "C" int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64_t* chunk_raddr,
+                                 const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
+                                 uint32_t chunk_shift, uint32_t world, uint32_t n_qp,
+                                 uint64_t local_base, uint64_t heap_size, db_wqe* rings,
+                                 uint64_t depth, uint64_t* head, uint32_t* count,
+                                 db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (chunk_shift < 4 || chunk_shift > 48) return -EINVAL;
+  if (heap_size == 0) return -EINVAL;
+  if (depth > (1ull << 31)) return -EINVAL;
+  const uint64_t n_chunks = ((heap_size - 1) >> chunk_shift) + 1;
+  if (n_chunks > (1ull << 32)) return -EINVAL;
+  wqe::Params p{};
+  const int rc = setup(p, req, n, world, n_qp, local_base, heap_size, rings, depth, head, count,
+                       ctr, ws, ws_bytes, s);
+  if (rc) return rc < 0 ? rc : 0;
+  if (!chunk_raddr || !chunk_rkey || !chunk_lkey || !aligned(chunk_raddr, 8) ||
+      !aligned(chunk_rkey, 4) || !aligned(chunk_lkey, 4))
+    return -EINVAL;
+  p.vmm = true;
+  p.cshift = chunk_shift;
+  p.n_chunks = n_chunks;
+  p.chunk_raddr = chunk_raddr;
+  p.chunk_rkey = chunk_rkey;
+  p.chunk_lkey = chunk_lkey;
+  return run(p, s);
 }

@@ -228,6 +228,44 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
                   uint64_t* head, uint32_t* count, db_counters* ctr, void* ws,
                   size_t ws_bytes, void* stream);
 
+/* ---- put translation on a VMM heap ------------------------------------------
+ * Source: "mori communication library analysis (1)", the VMM-heap branch of
+ * the put path: while bytes remain, the WQE covers the rest of the chunk
+ * holding the current source address, the rest of the chunk holding the
+ * current destination address, or what remains, whichever is least, with the
+ * source chunk's lkey and the destination chunk's remote address and rkey.
+ *
+ * The heap is cut into chunks of C = 2^chunk_shift bytes at the same offsets
+ * on every PE (n_chunks = ceil(heap_size / C)). A valid put (as for
+ * db_wqe_bucket) covering [off, off + bytes) makes one WQE for each chunk c
+ * it touches, in address order; for the part [s, e) of chunk c:
+ *   raddr = chunk_raddr[pe * n_chunks + c] + (s - c * C)
+ *   rkey  = chunk_rkey[pe * n_chunks + c]
+ *   laddr = local_base + s,  lkey = chunk_lkey[c],  len = e - s
+ *   seq, req_index as for db_wqe_bucket; a put's WQEs take consecutive post
+ *   indices of its ring.
+ * count[r] is the WQEs ring r was asked for (saturating at 2^32 - 1); a ring
+ * asked for more than `depth` takes none. ctr: total = WQEs posted,
+ * n_invalid = invalid puts, n_overflow = WQEs of overflowing rings.
+ * With one chunk as large as the heap this is db_wqe_bucket with
+ * peer_ptrs[pe] = chunk_raddr[pe], rkeys[pe] = chunk_rkey[pe] and
+ * lkey = chunk_lkey[0].
+ *
+ * Arguments as for db_wqe_bucket, and
+ *   chunk_raddr  [world][n_chunks] remote address of each chunk (8-byte aligned)
+ *   chunk_rkey   [world][n_chunks]
+ *   chunk_lkey   [n_chunks]
+ *   chunk_shift  4 <= chunk_shift <= 48
+ * Limits: n < 2^32, depth <= 2^31, n_chunks <= 2^32, heap_size >= 1.
+ * Workspace: db_wqe_workspace_size(n, world * n_qp).
+ */
+int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64_t* chunk_raddr,
+                      const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
+                      uint32_t chunk_shift, uint32_t world, uint32_t n_qp, uint64_t local_base,
+                      uint64_t heap_size, db_wqe* rings, uint64_t depth, uint64_t* head,
+                      uint32_t* count, db_counters* ctr, void* ws, size_t ws_bytes,
+                      void* stream);
+
 /* ---- PRP build with no caller workspace ------------------------------------
  * The source pages have no counterpart to this entry point; it is an addition
  * for callers that must not allocate device memory on their submission path:

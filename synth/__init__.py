@@ -36,7 +36,7 @@ GiB = 1024 * MiB
 SEED_BASE = 0xDB5EED00
 
 # Workload names in the order of the study's configuration list.
-WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket")
+WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket", "put_bucket_vmm")
 
 
 def seed_of(name: str) -> int:
@@ -306,10 +306,32 @@ def put_bucket(seed: int | None = None, n: int = 8_388_608, world: int = 8,
                 head=np.zeros(world * n_qp, dtype=np.uint64))
 
 
+def put_bucket_vmm(seed: int | None = None, n: int = 8_388_608, world: int = 8,
+                   n_qp: int = 4, depth: int = 1 << 19, chunk_shift: int = 21) -> dict:
+    """The put_bucket batch on a heap of 2^chunk_shift-byte chunks.
+
+    The puts are those of put_bucket (same seed rule). Each chunk c of each PE
+    sits at a random 2^chunk_shift-aligned remote address in [2^40, 2^47)
+    with a random rkey; each local chunk has a random lkey.
+    """
+    p = put_bucket(seed, n, world, n_qp, depth)
+    rng = _rng((seed_of("put_bucket_vmm") if seed is None else seed) ^ 0x5A5A)
+    C = 1 << chunk_shift
+    n_chunks = -(-p["heap_size"] // C)
+    lo, hi = (1 << 40) // C, (1 << 47) // C
+    chunk_raddr = rng.integers(lo, hi, size=(world, n_chunks), dtype=np.uint64) * np.uint64(C)
+    chunk_rkey = rng.integers(0, 1 << 32, size=(world, n_chunks), dtype=np.uint64).astype(np.uint32)
+    chunk_lkey = rng.integers(0, 1 << 32, size=n_chunks, dtype=np.uint64).astype(np.uint32)
+    p.update(name="put_bucket_vmm", chunk_shift=chunk_shift, chunk_raddr=chunk_raddr,
+             chunk_rkey=chunk_rkey, chunk_lkey=chunk_lkey)
+    return p
+
+
 GENERATORS = {
     "prp_tiny": prp_tiny,
     "prp_small": prp_small,
     "prp_large": prp_large,
     "mr_lookup": mr_lookup,
     "put_bucket": put_bucket,
+    "put_bucket_vmm": put_bucket_vmm,
 }
