@@ -12,7 +12,9 @@ synthetic workload, all on one CUDA stream:
 batches), with inputs resident in HBM. Each kernel call is also timed alone
 with CUDA events on the launch stream; the dominant one (prp_large) gives the
 roofline line. ``e2e`` repeats the step through the same API with inputs in
-pinned host memory and every descriptor copied back to the host.
+pinned host memory and every descriptor copied back to the host. ``next``
+times, on its own and outside the step, the row built after the hot path:
+the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (the batches are independent);
@@ -48,6 +50,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the separately timed rows after the hot path")
     ap.add_argument("--only", choices=["prp_small", "prp_large", "mr_lookup", "put_bucket"],
                     help="profiling aid: run one workload only (not a bench line)")
     ap.add_argument("--fraction", type=float, default=1.0,
@@ -293,6 +297,55 @@ class Step:
                 assert int(b["ctr"][2].item()) == 0, "arena overflow in the benchmark"
 
 
+def run_next(args, device) -> dict:
+    """The row after the hot path, timed on its own (not part of a step):
+    the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm)."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    import synth
+    P = synth.put_bucket_vmm()
+    d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+    d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+    R = P["world"] * P["n_qp"]
+    n = P["req"].shape[0]
+    b = dict(req=d64(P["req"]), raddr=d64(P["chunk_raddr"]), rkey=d32(P["chunk_rkey"]),
+             lkey=d32(P["chunk_lkey"]),
+             rings=t.empty((R, P["depth"], 64), dtype=t.uint8, device=device),
+             head=d64(P["head"]), count=t.empty(R, dtype=t.int32, device=device),
+             ctr=t.zeros(4, dtype=t.int64, device=device),
+             ws=db.workspace(db.wqe_workspace_size(n, R), device))
+    stream = t.cuda.Stream(device=device)
+
+    def call():
+        db.wqe_bucket_vmm(b["req"], b["raddr"], b["rkey"], b["lkey"], P["chunk_shift"],
+                          P["world"], P["n_qp"], P["local_base"], P["heap_size"], b["rings"],
+                          P["depth"], b["head"], b["count"], b["ws"], ctr=b["ctr"], stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    t.cuda.synchronize(device)
+    evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, z in evs:
+        a.record(stream)
+        call()
+        z.record(stream)
+    t.cuda.synchronize(device)
+    ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+    wqes = int(b["ctr"][0].item())
+    if int(b["ctr"][3].item()):
+        raise RuntimeError("put_bucket_vmm: device error bits")
+    n_chunks = P["chunk_lkey"].shape[0]
+    alg = 16 * n + 64 * wqes + P["world"] * n_chunks * 12 + n_chunks * 4
+    peak, peak_kind = peak_gbs()
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"put_bucket_vmm": {
+        "ms": round(ms, 4), "M_req_per_s": round(n / ms / 1e3, 2), "wqes": wqes,
+        "chunk_bytes": 1 << P["chunk_shift"], "algorithmic_bytes": alg,
+        "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
+        "note": "not part of the step: timed alone, same stream discipline"}}
+
+
 def run_ours(args, inp, world, device, dist):
     import torch
     import descriptor_build_gb300 as db
@@ -521,6 +574,8 @@ def main():
             out["note"] = "profiling run on a subset: not a bench line"
         if not args.no_cpu and not args.only and args.fraction >= 1.0:
             out["cpu_baseline"] = cpu_baseline(inp)
+        if not args.only and args.fraction >= 1.0 and not args.no_next:
+            out["next"] = run_next(args, device)
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()

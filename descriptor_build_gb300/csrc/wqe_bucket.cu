@@ -519,7 +519,11 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   const uint64_t slot_mask = p.depth - 1;
   for (uint64_t f = lane; f < 2ull * n_wqe; f += 32) {
     const uint32_t wq = (uint32_t)(f >> 1), h = (uint32_t)(f & 1);
-    uint32_t lo = 0, hi = n_valid;  // s_wstart[lo] <= wq < s_wstart[hi]
+    // Every put makes at least one WQE, so WQE wq belongs to a put in
+    // [wq - (n_wqe - n_valid), wq]: search only there.
+    const uint32_t extra = n_wqe - n_valid;
+    uint32_t lo = wq > extra ? wq - extra : 0u;
+    uint32_t hi = (wq + 1 < n_valid ? wq + 1 : n_valid);  // s_wstart[lo] <= wq < s_wstart[hi]
     while (hi - lo > 1) {
       const uint32_t mid = (lo + hi) >> 1;
       if (s_wstart[mid] <= wq) lo = mid;
