@@ -65,7 +65,7 @@ def _load():
                                               vp, vp, vp]
             lib.oracle_wqe_bucket_vmm.restype = None
             lib.oracle_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64,
-                                                  vp, u64, vp, vp, vp]
+                                                  vp, u64, vp, u32, vp, vp, vp]
             _lib = lib
     return _lib
 
@@ -188,9 +188,11 @@ def wqe_bucket(req, peer_ptrs, rkeys, world: int, n_qp: int, local_base: int, lk
 
 def wqe_bucket_vmm(req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift: int, world: int,
                    n_qp: int, local_base: int, heap_size: int, depth: int, head,
-                   fill: int = 0, rings: np.ndarray | None = None) -> dict:
+                   fill: int = 0, rings: np.ndarray | None = None, mtu: int = 0,
+                   psn_head=None) -> dict:
     """Put translation on a VMM heap: one WQE per chunk a put touches.
-    chunk_raddr / chunk_rkey are [world, n_chunks], chunk_lkey [n_chunks]."""
+    chunk_raddr / chunk_rkey are [world, n_chunks], chunk_lkey [n_chunks].
+    With an mtu, each WQE gets its first PSN; psn_head is updated."""
     req = _u64(req).reshape(-1, 2)
     n_chunks = -(-heap_size // (1 << chunk_shift))
     chunk_raddr = _u64(chunk_raddr).reshape(-1)
@@ -204,9 +206,14 @@ def wqe_bucket_vmm(req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift: int, w
     else:
         assert rings.dtype == np.uint8 and rings.shape == (n_rings, depth, 64)
     head = _u64(head).copy()
+    psn = _u64(psn_head if psn_head is not None else np.zeros(n_rings)).copy()
     count = np.zeros(n_rings, dtype=np.uint32)
     ctr = np.zeros(4, dtype=np.uint64)
     _load().oracle_wqe_bucket_vmm(_p(req), req.shape[0], _p(chunk_raddr), _p(chunk_rkey),
                                   _p(chunk_lkey), chunk_shift, world, n_qp, local_base,
-                                  heap_size, _p(rings), depth, _p(head), _p(count), _p(ctr))
-    return dict(rings=rings, head=head, count=count, ctr=ctr)
+                                  heap_size, _p(rings), depth, _p(head), mtu, _p(psn),
+                                  _p(count), _p(ctr))
+    out = dict(rings=rings, head=head, count=count, ctr=ctr)
+    if mtu:
+        out["psn_head"] = psn
+    return out

@@ -392,24 +392,35 @@ void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptr
 //    those of the static heap;
 //  * a ring asked for more than `depth` WQEs by the batch takes none;
 //    counters: WQEs posted, invalid puts, WQEs of overflowing rings, err.
+// Packet sequence numbers (same page, the BNXT branch), when mtu != 0: a WQE
+// of `len` bytes uses psnCnt = ceil(len / mtu) PSNs; its first PSN is the
+// ring's PSN counter plus the psnCnt of the ring's earlier WQEs (the page's
+// exclusive prefix over active lanes, here over the batch in order), written
+// as a u32 at byte 44 of the WQE. The SQ index still advances by one per WQE
+// (the page's code adds the lane count to the MSN and the PSN total to the
+// PSN). A ring that takes its batch advances psn_head by its PSN total.
 void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chunk_raddr,
                            const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
                            uint32_t chunk_shift, uint32_t world, uint32_t n_qp,
                            uint64_t local_base, uint64_t heap_size, uint8_t* rings,
-                           uint64_t depth, uint64_t* head, uint32_t* count, uint64_t* ctr) {
+                           uint64_t depth, uint64_t* head, uint32_t mtu, uint64_t* psn_head,
+                           uint32_t* count, uint64_t* ctr) {
   const uint64_t C = 1ull << chunk_shift;
   const uint64_t n_chunks = (heap_size + C - 1) / C;
   uint64_t n_rings = (uint64_t)world * n_qp;
-  std::vector<uint64_t> demand(n_rings, 0);
+  std::vector<uint64_t> demand(n_rings, 0), psn_demand(n_rings, 0);
   std::vector<int> ring_of(n);
   uint64_t n_invalid = 0;
-  // One pass of the page's loop, emitting nothing: how many WQEs a put makes.
-  auto fragments = [&](uint64_t off, uint64_t bytes) {
+  // One pass of the page's loop, emitting nothing: how many WQEs a put makes
+  // (and, with an mtu, how many PSNs they use).
+  auto fragments = [&](uint64_t off, uint64_t bytes, uint64_t& psns) {
     uint64_t cur = 0, remaining = bytes, k = 0;
+    psns = 0;
     while (remaining > 0) {
       const uint64_t src = off + cur, dst = off + cur;
       const uint64_t src_left = C - (src % C), dst_left = C - (dst % C);
       const uint64_t t = std::min(std::min(src_left, dst_left), remaining);
+      if (mtu) psns += (t + mtu - 1) / mtu;
       cur += t;
       remaining -= t;
       k += 1;
@@ -432,7 +443,9 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
     }
     const int ring = (int)(pe * n_qp + qp);  // PE-major, as for the static heap
     ring_of[i] = ring;
-    demand[ring] += fragments(off, bytes);
+    uint64_t psns = 0;
+    demand[ring] += fragments(off, bytes, psns);
+    psn_demand[ring] += psns;
   }
   // 2. Overflowing rings take nothing.
   uint64_t n_overflow = 0, posted = 0, err = 0;
@@ -445,7 +458,7 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
     }
   }
   // 3. Post in request order, each put's fragments in address order.
-  std::vector<uint64_t> taken(n_rings, 0);
+  std::vector<uint64_t> taken(n_rings, 0), psn_taken(n_rings, 0);
   for (uint64_t i = 0; i < n; ++i) {
     int r = ring_of[i];
     if (r < 0 || full[r]) continue;
@@ -475,6 +488,10 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
       put_u32(wqe + 28, 0);
       put_u64(wqe + 32, post);
       put_u32(wqe + 40, (uint32_t)i);
+      if (mtu) {
+        put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));  // first PSN
+        psn_taken[r] += (t + mtu - 1) / mtu;
+      }
       posted += 1;
       cur += t;
       remaining -= t;
@@ -482,8 +499,9 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
   }
   // 4. Advance heads of the rings that took their batch.
   for (uint64_t r = 0; r < n_rings; ++r) {
-    count[r] = (uint32_t)demand[r];
+    count[r] = (uint32_t)std::min<uint64_t>(demand[r], 0xFFFFFFFFull);
     if (!full[r]) head[r] += demand[r];
+    if (mtu && !full[r]) psn_head[r] += psn_demand[r];
   }
   ctr[0] = posted;
   ctr[1] = n_invalid;

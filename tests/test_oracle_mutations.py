@@ -64,6 +64,11 @@ MUTANTS = [
      "const uint32_t rkey = chunk_rkey[pe * n_chunks];"),
     ("vmm laddr does not advance per fragment",
      "put_u64(wqe + 8, local_base + src);", "put_u64(wqe + 8, local_base + off);"),
+    ("psn counts round down",
+     "if (mtu) psns += (t + mtu - 1) / mtu;", "if (mtu) psns += t / mtu;"),
+    ("psn taken after its own WQE",
+     "put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));  // first PSN\n        psn_taken[r] += (t + mtu - 1) / mtu;",
+     "psn_taken[r] += (t + mtu - 1) / mtu;\n        put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));"),
     ("vmm fragment runs 16 bytes past its chunk",
      "const uint64_t t = std::min(std::min(src_left, dst_left), remaining);\n      const uint64_t post",
      "const uint64_t t = std::min(src_left + 16, remaining);\n      const uint64_t post"),

@@ -112,3 +112,54 @@ def test_fragments_cover_each_put_chunk_by_chunk(oracle, chunk_shift, depth):
         posted += total
     assert int(out["ctr"][0]) == posted
     assert int(out["ctr"][1]) == int((nbytes == 0).sum())
+
+
+@pytest.mark.parametrize("variant", ["depth8", "depth2"])
+def test_hand_cases_with_psns(oracle, variant):
+    fx = load_golden("wqe_vmm_hand_cases.json")
+    ps = fx["psn"]
+    raddr = np.array([[h(x) for x in row] for row in fx["chunk_raddr"]], dtype=np.uint64)
+    out = oracle.wqe_bucket_vmm(pack(fx["req"]), raddr, np.array(fx["chunk_rkey"]),
+                                np.array(fx["chunk_lkey"]), fx["chunk_shift"], fx["world"],
+                                fx["n_qp"], h(fx["local_base"]), fx["heap_size"],
+                                fx[variant]["depth"], fx["head"], fill=0xCD, mtu=ps["mtu"],
+                                psn_head=np.array(ps["psn_head"], dtype=np.uint64))
+    assert out["psn_head"].tolist() == ps[f"{variant}_psn_head"]
+    assert out["head"].tolist() == fx[variant]["head"]
+    if variant == "depth8":
+        w = out["rings"].reshape(out["rings"].shape[0], out["rings"].shape[1], 64)
+        psn = w.view(np.uint32).reshape(w.shape[0], w.shape[1], 16)[..., 11]
+        for e in ps["depth8_psn"]:
+            assert int(psn[e["ring"], e["slot"]]) == e["psn"], e
+
+
+def test_psn_chain_per_ring(oracle):
+    """Each WQE's first PSN is the previous WQE's plus ceil(len / mtu) of the
+    previous, from the old PSN head to the new one; without an mtu byte 44
+    stays zero."""
+    rng = np.random.default_rng(44)
+    world, n_qp, heap, cs, depth, mtu = 3, 2, 1 << 22, 12, 1 << 14, 1024
+    n = 2000
+    pe, qp = rng.integers(0, world, size=n), rng.integers(0, n_qp, size=n)
+    off = 16 * rng.integers(0, heap // 16, size=n)
+    nbytes = np.minimum(16 * rng.integers(1, 2000, size=n), heap - off)
+    from synth import pack_put_requests
+    req = pack_put_requests(off, nbytes, pe, qp)
+    raddr, rkey, lkey = chunk_tables(rng, world, heap >> cs)
+    head = rng.integers(0, 1 << 20, size=world * n_qp).astype(np.uint64)
+    psn0 = rng.integers(0, 1 << 33, size=world * n_qp).astype(np.uint64)
+    out = oracle.wqe_bucket_vmm(req, raddr, rkey, lkey, cs, world, n_qp, 0, heap, depth, head,
+                                mtu=mtu, psn_head=psn0)
+    f = wqe_fields(out["rings"])
+    psn = out["rings"].view(np.uint32).reshape(world * n_qp, depth, 16)[..., 11]
+    for r in range(world * n_qp):
+        cnt = int(out["count"][r])
+        want = int(psn0[r])
+        for k in range(cnt):
+            s = (int(head[r]) + k) % depth
+            assert int(psn[r, s]) == want % (1 << 32)
+            want += -(-int(f["len"][r, s]) // mtu)
+        assert int(out["psn_head"][r]) == want
+    plain = oracle.wqe_bucket_vmm(req, raddr, rkey, lkey, cs, world, n_qp, 0, heap, depth, head)
+    assert (plain["rings"].view(np.uint32).reshape(world * n_qp, depth, 16)[..., 11] == 0).all()
+    assert (plain["rings"] == np.where(np.arange(64) // 4 == 11, 0, out["rings"])).all()
