@@ -298,8 +298,9 @@ class Step:
 
 
 def run_next(args, device) -> dict:
-    """The row after the hot path, timed on its own (not part of a step):
-    the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm)."""
+    """The rows after the hot path, timed on their own (not part of a step):
+    the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm), without and
+    with packet sequence numbers (mtu 4096)."""
     import torch as t
     import descriptor_build_gb300 as db
     import synth
@@ -313,37 +314,41 @@ def run_next(args, device) -> dict:
              rings=t.empty((R, P["depth"], 64), dtype=t.uint8, device=device),
              head=d64(P["head"]), count=t.empty(R, dtype=t.int32, device=device),
              ctr=t.zeros(4, dtype=t.int64, device=device),
+             psn=t.zeros(R, dtype=t.int64, device=device),
              ws=db.workspace(db.wqe_workspace_size(n, R), device))
     stream = t.cuda.Stream(device=device)
+    out = {}
+    for name, mtu in (("put_bucket_vmm", 0), ("put_bucket_vmm_psn", 4096)):
+        def call():
+            db.wqe_bucket_vmm(b["req"], b["raddr"], b["rkey"], b["lkey"], P["chunk_shift"],
+                              P["world"], P["n_qp"], P["local_base"], P["heap_size"], b["rings"],
+                              P["depth"], b["head"], b["count"], b["ws"], ctr=b["ctr"],
+                              stream=stream, mtu=mtu, psn_head=b["psn"] if mtu else None)
 
-    def call():
-        db.wqe_bucket_vmm(b["req"], b["raddr"], b["rkey"], b["lkey"], P["chunk_shift"],
-                          P["world"], P["n_qp"], P["local_base"], P["heap_size"], b["rings"],
-                          P["depth"], b["head"], b["count"], b["ws"], ctr=b["ctr"], stream=stream)
-
-    for _ in range(args.warmup):
-        call()
-    t.cuda.synchronize(device)
-    evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for a, z in evs:
-        a.record(stream)
-        call()
-        z.record(stream)
-    t.cuda.synchronize(device)
-    ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
-    wqes = int(b["ctr"][0].item())
-    if int(b["ctr"][3].item()):
-        raise RuntimeError("put_bucket_vmm: device error bits")
-    n_chunks = P["chunk_lkey"].shape[0]
-    alg = 16 * n + 64 * wqes + P["world"] * n_chunks * 12 + n_chunks * 4
-    peak, peak_kind = peak_gbs()
-    gbs = alg / (ms * 1e-3) / 1e9
-    return {"put_bucket_vmm": {
-        "ms": round(ms, 4), "M_req_per_s": round(n / ms / 1e3, 2), "wqes": wqes,
-        "chunk_bytes": 1 << P["chunk_shift"], "algorithmic_bytes": alg,
-        "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
-        "note": "not part of the step: timed alone, same stream discipline"}}
+        for _ in range(args.warmup):
+            call()
+        t.cuda.synchronize(device)
+        evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, z in evs:
+            a.record(stream)
+            call()
+            z.record(stream)
+        t.cuda.synchronize(device)
+        ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+        wqes = int(b["ctr"][0].item())
+        if int(b["ctr"][3].item()):
+            raise RuntimeError(f"{name}: device error bits")
+        n_chunks = P["chunk_lkey"].shape[0]
+        alg = 16 * n + 64 * wqes + P["world"] * n_chunks * 12 + n_chunks * 4
+        peak, peak_kind = peak_gbs()
+        gbs = alg / (ms * 1e-3) / 1e9
+        out[name] = {
+            "ms": round(ms, 4), "M_req_per_s": round(n / ms / 1e3, 2), "wqes": wqes,
+            "chunk_bytes": 1 << P["chunk_shift"], "mtu": mtu, "algorithmic_bytes": alg,
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
+            "note": "not part of the step: timed alone, same stream discipline"}
+    return out
 
 
 def run_ours(args, inp, world, device, dist):

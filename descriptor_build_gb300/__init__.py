@@ -69,7 +69,7 @@ def _load():
     lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
                                   vp, sz, vp]
     lib.db_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64, vp, u64, vp,
-                                      vp, vp, vp, sz, vp]
+                                      vp, u32, vp, vp, vp, sz, vp]
     for name in ("db_prp_workspace_size", "db_prp_build", "db_prp_build_static",
                  "db_mr_workspace_size",
                  "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
@@ -201,10 +201,12 @@ def wqe_bucket_vmm(req: torch.Tensor, chunk_raddr: torch.Tensor, chunk_rkey: tor
                    chunk_lkey: torch.Tensor, chunk_shift: int, world: int, n_qp: int,
                    local_base: int, heap_size: int, rings: torch.Tensor, depth: int,
                    head: torch.Tensor, count: torch.Tensor, ws: torch.Tensor,
-                   ctr: torch.Tensor | None = None, stream=None) -> None:
-    """db_wqe_bucket_vmm: puts on a chunked (VMM) heap, one WQE per chunk touched."""
+                   ctr: torch.Tensor | None = None, stream=None, mtu: int = 0,
+                   psn_head: torch.Tensor | None = None) -> None:
+    """db_wqe_bucket_vmm: puts on a chunked (VMM) heap, one WQE per chunk
+    touched; with an mtu, each WQE also gets its first PSN."""
     n = _records(req, 16)
     _check("db_wqe_bucket_vmm", _lib.db_wqe_bucket_vmm(
         _ptr(req), n, _ptr(chunk_raddr), _ptr(chunk_rkey), _ptr(chunk_lkey), chunk_shift, world,
-        n_qp, local_base, heap_size, _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(ctr),
-        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        n_qp, local_base, heap_size, _ptr(rings), depth, _ptr(head), _ptr(count), mtu,
+        _ptr(psn_head), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))

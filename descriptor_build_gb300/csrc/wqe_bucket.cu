@@ -56,12 +56,18 @@ struct Header {
 };
 constexpr size_t kHeadOldOff = 256;
 constexpr size_t kFullOff = kHeadOldOff + 8 * kMaxRings;
-constexpr size_t kCountsOff = kFullOff + 4 * kMaxRings;
+constexpr size_t kPsnOldOff = kFullOff + 4 * kMaxRings;  // PSN heads before the call
+constexpr size_t kPsnTotOff = kPsnOldOff + 8 * kMaxRings;  // PSNs each ring was asked for
+constexpr size_t kCountsOff = kPsnTotOff + 8 * kMaxRings;
 inline uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
 // Column stride of counts: tiles rounded up to 8 (32-byte aligned columns).
 inline uint64_t stride_for(uint64_t n) { return (tiles_for(n) + 7) & ~7ull; }
+inline size_t column_bytes(uint64_t n, uint32_t R) {
+  return (stride_for(n) * ((uint64_t)R + 1) * 4 + 255) & ~(uint64_t)255;
+}
+// WQE counts, then PSN counts (used when PSNs are asked for).
 inline size_t ws_bytes_for(uint64_t n, uint32_t R) {
-  return kCountsOff + ((stride_for(n) * ((uint64_t)R + 1) * 4 + 255) & ~(uint64_t)255);
+  return kCountsOff + 2 * column_bytes(n, R);
 }
 
 struct Params {
@@ -91,6 +97,13 @@ struct Params {
   const uint64_t* chunk_raddr;  // [world][n_chunks]
   const uint32_t* chunk_rkey;   // [world][n_chunks]
   const uint32_t* chunk_lkey;   // [n_chunks]
+  // Packet sequence numbers (mtu != 0): one column of per-tile PSN counts
+  // per bin, the PSN heads before the call and each ring's PSN total.
+  uint32_t mtu;
+  uint64_t* psn_head;
+  uint32_t* psn_counts;  // [V][stride]
+  uint64_t* psn_old;
+  uint64_t* psn_tot;
 };
 
 // Ring of a put, or R for an invalid one.
@@ -111,6 +124,25 @@ __device__ __forceinline__ uint32_t wqes_of(const Params& p, const ulonglong2 r)
   return (uint32_t)((last >> p.cshift) - (off >> p.cshift)) + 1;
 }
 
+// PSNs a valid put's WQEs use: ceil(len / mtu) per WQE, summed over its
+// chunks (a first partial chunk, full chunks, a last partial one).
+__device__ __forceinline__ uint32_t psns_of(const Params& p, const ulonglong2 r) {
+  const uint64_t off = r.x, bytes = (uint32_t)r.y, m = p.mtu;
+  const uint32_t k = wqes_of(p, r);
+  if (k == 1) return (uint32_t)((bytes + m - 1) / m);
+  const uint64_t C = 1ull << p.cshift;
+  const uint64_t first = C - (off & (C - 1));
+  const uint64_t last = ((off + bytes - 1) & (C - 1)) + 1;
+  return (uint32_t)((first + m - 1) / m + (uint64_t)(k - 2) * ((C + m - 1) / m) + (last + m - 1) / m);
+}
+// PSNs of the fragments before fragment f of a put.
+__device__ __forceinline__ uint32_t psns_before(const Params& p, uint64_t off, uint32_t f) {
+  if (f == 0) return 0;
+  const uint64_t C = 1ull << p.cshift, m = p.mtu;
+  const uint64_t first = C - (off & (C - 1));
+  return (uint32_t)((first + m - 1) / m + (uint64_t)(f - 1) * ((C + m - 1) / m));
+}
+
 // ---------------------------------------------------------------- count pass
 // One warp counts a whole tile (8 rows of 32 puts) into its own shared
 // histogram; warps stride over tiles, so no block-wide barrier is needed.
@@ -122,15 +154,19 @@ constexpr int kCountWarps = kCountThreads / 32;
 constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at once
 
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
-  extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V]
+  extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V] WQEs, then PSNs if asked
   const uint32_t V = p.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* s_hist = s_hist_all + (size_t)warp * V;
+  uint32_t* s_psn = s_hist_all + (size_t)(kCountWarps + warp) * V;
   const uint64_t pol_first = policy_evict_first();
   const uint64_t n_warps = (uint64_t)gridDim.x * kCountWarps;
   for (uint64_t tile = (uint64_t)blockIdx.x * kCountWarps + warp; tile < p.n_tiles;
        tile += n_warps) {
-    for (uint32_t v = lane; v < V; v += 32) s_hist[v] = 0;
+    for (uint32_t v = lane; v < V; v += 32) {
+      s_hist[v] = 0;
+      if (p.mtu) s_psn[v] = 0;
+    }
     __syncwarp();
     for (int row = 0; row < kTile / 32; row += kCountUnroll) {
       ulonglong2 r[kCountUnroll];
@@ -143,6 +179,7 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
       for (int u = 0; u < kCountUnroll; ++u) {
         const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
         const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
+        if (p.mtu && bin < p.R) atomicAdd(&s_psn[bin], psns_of(p, r[u]));
         if (DB_WQE_COUNT_MODE == 1) {
           if (bin < p.R) atomicAdd(&s_hist[bin], wqes_of(p, r[u]));
           else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
@@ -158,7 +195,10 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
       }
     }
     __syncwarp();
-    for (uint32_t v = lane; v < V; v += 32) p.counts[v * p.stride + tile] = s_hist[v];
+    for (uint32_t v = lane; v < V; v += 32) {
+      p.counts[v * p.stride + tile] = s_hist[v];
+      if (p.mtu) p.psn_counts[v * p.stride + tile] = s_psn[v];
+    }
     __syncwarp();
   }
 }
@@ -176,8 +216,11 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
   constexpr int kW = kScanThreads / 32;
   __shared__ uint64_t s_scan[kW];
   __shared__ int s_last;
-  const uint32_t v = blockIdx.x;
-  uint32_t* col = p.counts + (uint64_t)v * p.stride;
+  // CTAs 0 .. V-1 scan the WQE columns, V .. 2V-1 (when PSNs are asked for)
+  // the PSN columns.
+  const bool psn_col = blockIdx.x >= p.V;
+  const uint32_t v = psn_col ? blockIdx.x - p.V : blockIdx.x;
+  uint32_t* col = (psn_col ? p.psn_counts : p.counts) + (uint64_t)v * p.stride;
   const uint64_t T = p.n_tiles;
   uint64_t carry = 0;
   for (uint64_t s0 = 0; s0 < T; s0 += kScanSeg) {
@@ -221,7 +264,14 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
     __syncthreads();  // s_scan is reused by the next round
   }
   const uint64_t total = carry;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && psn_col) {
+    if (v < p.R) {  // the head moves once the ring's overflow decision is known
+      p.psn_old[v] = p.psn_head[v];
+      p.psn_tot[v] = total;
+    }
+    __threadfence();
+    s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
+  } else if (threadIdx.x == 0) {
     if (v < p.R) {
       const uint64_t h = p.head[v];
       const bool over = total > p.depth;
@@ -251,6 +301,10 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
       p.ctr->n_overflow = overflow;
       p.ctr->err = overflow ? DB_ERR_RING_OVERFLOW : 0u;
     }
+    if (p.mtu)
+      for (uint32_t r = 0; r < p.R; ++r)
+        if (!*(volatile uint32_t*)&p.full[r])
+          p.psn_head[r] = *(volatile uint64_t*)&p.psn_old[r] + *(volatile uint64_t*)&p.psn_tot[r];
     p.hdr->done = 0;
     __threadfence();
   }
@@ -399,6 +453,8 @@ __host__ __device__ inline size_t vmm_warp_smem(uint32_t V) {
   b += (size_t)kRows * V * 2;         // per-row counts
   b += (size_t)kTile * 2;             // permutation
   b += (size_t)(kTile + 1) * 4;       // WQE prefix over the ring order
+  b += (size_t)(kTile + 1) * 4;       // PSN prefix over the ring order
+  b += (size_t)V * 4 * 2;             // first PSN of the tile, PSN run start
   return (b + 15) & ~(size_t)15;
 }
 inline int vmm_scatter_warps(uint32_t V) {
@@ -421,6 +477,9 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_wrun + V);  // [kRows][V]
   uint16_t* s_perm = s_cnt + kRows * V;
   uint32_t* s_wstart = reinterpret_cast<uint32_t*>(s_perm + kTile);  // [kTile + 1]
+  uint32_t* s_pstart = s_wstart + kTile + 1;                          // [kTile + 1]
+  uint32_t* s_psn0 = s_pstart + kTile + 1;                            // [V]
+  uint32_t* s_prun = s_psn0 + V;                                      // [V]
 
   for (uint32_t v = threadIdx.x; v < R; v += blockDim.x)
     s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
@@ -473,6 +532,7 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
     if (v < R) {
       s_run[v] = carry + x - tot;
       s_seq0[v] = p.head_old[v] + p.counts[(uint64_t)v * p.stride + tile];
+      if (p.mtu) s_psn0[v] = (uint32_t)(p.psn_old[v] + p.psn_counts[(uint64_t)v * p.stride + tile]);
     }
     carry += __shfl_sync(kFull, x, 31);
   }
@@ -510,7 +570,32 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   const uint32_t n_wqe = __shfl_sync(kFull, x, 31);
   if (lane == 0) s_wstart[kTile] = n_wqe;
   __syncwarp();
-  for (uint32_t v = lane; v < R; v += 32) s_wrun[v] = s_wstart[s_run[v]];
+  if (p.mtu) {  // the same over PSN counts (mod 2^32, as the WQE keeps 32 bits)
+    uint32_t pmine = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const uint32_t q = lane * kPer + j;
+      kq[j] = q < n_valid ? psns_of(p, s_put[s_perm[q]]) : 0u;
+      pmine += kq[j];
+    }
+    uint32_t px = pmine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, px, o);
+      if (lane >= o) px += y;
+    }
+    uint32_t prun = px - pmine;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      s_pstart[lane * kPer + j] = prun;
+      prun += kq[j];
+    }
+    __syncwarp();
+  }
+  for (uint32_t v = lane; v < R; v += 32) {
+    s_wrun[v] = s_wstart[s_run[v]];
+    if (p.mtu) s_prun[v] = s_pstart[s_run[v]];
+  }
   __syncwarp();
   // 5. Write-out: lanes 2w and 2w + 1 write the two halves of the tile's
   //    WQE w (ring order); its put is the last one whose first WQE is at or
@@ -548,7 +633,11 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
                   (end - start) | ((uint64_t)__ldg(p.chunk_lkey + c) << 32),
                   (uint64_t)__ldg(p.chunk_rkey + rc), pol_first);
     } else {
-      st_stream32(d, seq, t0 + o, 0ull, 0ull, pol_first);
+      // u32 batch index at byte 40, first PSN at byte 44
+      uint64_t w5 = t0 + o;
+      if (p.mtu)
+        w5 |= (uint64_t)(s_psn0[v] + (s_pstart[lo] - s_prun[v]) + psns_before(p, pu.x, frag)) << 32;
+      st_stream32(d, seq, w5, 0ull, 0ull, pol_first);
     }
   }
 }
@@ -564,6 +653,10 @@ int prepare_scatter() {
     if (e != cudaSuccess) return cuda_failure(e);
     e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kMaxSmem);
+    if (e != cudaSuccess) return cuda_failure(e);
+    // Two histograms (WQEs and PSNs) of up to 1025 bins per warp.
+    e = cudaFuncSetAttribute(wqe_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((size_t)kCountWarps * (kMaxRings + 1) * 4 * 2));
     if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
   }
@@ -625,6 +718,9 @@ int setup(wqe::Params& p, const db_put_req* req, uint64_t n, uint32_t world, uin
   p.head_old = reinterpret_cast<uint64_t*>(w + wqe::kHeadOldOff);
   p.full = reinterpret_cast<uint32_t*>(w + wqe::kFullOff);
   p.counts = reinterpret_cast<uint32_t*>(w + wqe::kCountsOff);
+  p.psn_counts = reinterpret_cast<uint32_t*>(w + wqe::kCountsOff + wqe::column_bytes(n, R));
+  p.psn_old = reinterpret_cast<uint64_t*>(w + wqe::kPsnOldOff);
+  p.psn_tot = reinterpret_cast<uint64_t*>(w + wqe::kPsnTotOff);
   return 0;
 }
 
@@ -636,10 +732,10 @@ int run(const wqe::Params& p, cudaStream_t s) {
   const uint64_t count_need = (p.n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
   if (count_grid > count_need) count_grid = count_need;
   wqe::wqe_count_kernel<<<(unsigned)count_grid, wqe::kCountThreads,
-                          (size_t)wqe::kCountWarps * p.V * 4, s>>>(p);
+                          (size_t)wqe::kCountWarps * p.V * 4 * (p.mtu ? 2 : 1), s>>>(p);
   rc = launch_result();
   if (rc) return rc;
-  wqe::wqe_scan_kernel<<<p.V, wqe::kScanThreads, 0, s>>>(p);
+  wqe::wqe_scan_kernel<<<p.V * (p.mtu ? 2 : 1), wqe::kScanThreads, 0, s>>>(p);
   rc = launch_result();
   if (rc) return rc;
   if (!p.vmm) {
@@ -678,10 +774,14 @@ extern "C" int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64
                                  const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
                                  uint32_t chunk_shift, uint32_t world, uint32_t n_qp,
                                  uint64_t local_base, uint64_t heap_size, db_wqe* rings,
-                                 uint64_t depth, uint64_t* head, uint32_t* count,
-                                 db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
+                                 uint64_t depth, uint64_t* head, uint32_t* count, uint32_t mtu,
+                                 uint64_t* psn_head, db_counters* ctr, void* ws, size_t ws_bytes,
+                                 void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   if (chunk_shift < 4 || chunk_shift > 48) return -EINVAL;
+  if (mtu != 0 && (mtu < 512 || mtu > (1u << 20) || chunk_shift < 12 || !psn_head ||
+                   !aligned(psn_head, 8)))
+    return -EINVAL;
   if (heap_size == 0) return -EINVAL;
   if (depth > (1ull << 31)) return -EINVAL;
   const uint64_t n_chunks = ((heap_size - 1) >> chunk_shift) + 1;
@@ -694,6 +794,8 @@ extern "C" int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64
       !aligned(chunk_rkey, 4) || !aligned(chunk_lkey, 4))
     return -EINVAL;
   p.vmm = true;
+  p.mtu = mtu;
+  p.psn_head = psn_head;
   p.cshift = chunk_shift;
   p.n_chunks = n_chunks;
   p.chunk_raddr = chunk_raddr;

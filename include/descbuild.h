@@ -251,11 +251,20 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
  * peer_ptrs[pe] = chunk_raddr[pe], rkeys[pe] = chunk_rkey[pe] and
  * lkey = chunk_lkey[0].
  *
+ * Packet sequence numbers (same page, the BNXT branch), when mtu != 0: a WQE
+ * of len bytes uses ceil(len / mtu) PSNs; its first PSN, psn_head[r] plus
+ * the PSNs of ring r's earlier WQEs in the batch, is stored as a u32 at byte
+ * 44 (rsvd[0]). A ring that takes its batch advances psn_head[r] by its PSN
+ * total. The post index still advances by one per WQE. With mtu == 0 byte
+ * 44 stays 0 and psn_head is not used.
+ *
  * Arguments as for db_wqe_bucket, and
  *   chunk_raddr  [world][n_chunks] remote address of each chunk (8-byte aligned)
  *   chunk_rkey   [world][n_chunks]
  *   chunk_lkey   [n_chunks]
  *   chunk_shift  4 <= chunk_shift <= 48
+ *   mtu          0, or 512 <= mtu <= 2^20 with chunk_shift >= 12
+ *   psn_head     [world * n_qp] in/out PSN counters (8-byte aligned); NULL if mtu == 0
  * Limits: n < 2^32, depth <= 2^31, n_chunks <= 2^32, heap_size >= 1.
  * Workspace: db_wqe_workspace_size(n, world * n_qp).
  */
@@ -263,8 +272,8 @@ int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64_t* chunk_r
                       const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
                       uint32_t chunk_shift, uint32_t world, uint32_t n_qp, uint64_t local_base,
                       uint64_t heap_size, db_wqe* rings, uint64_t depth, uint64_t* head,
-                      uint32_t* count, db_counters* ctr, void* ws, size_t ws_bytes,
-                      void* stream);
+                      uint32_t* count, uint32_t mtu, uint64_t* psn_head, db_counters* ctr,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* ---- PRP build with no caller workspace ------------------------------------
  * The source pages have no counterpart to this entry point; it is an addition

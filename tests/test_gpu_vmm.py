@@ -17,7 +17,7 @@ def db():
 
 
 def run_vmm(db, req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift, world, n_qp,
-            local_base, heap, depth, head, fill=0xCD):
+            local_base, heap, depth, head, fill=0xCD, mtu=0, psn_head=None):
     n = req.shape[0]
     R = world * n_qp
     rings = torch.full((R, depth, 64), fill, dtype=torch.uint8, device="cuda")
@@ -25,22 +25,30 @@ def run_vmm(db, req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift, world, n_
     count = torch.full((R,), -1, dtype=torch.int32, device="cuda")
     ctr = torch.full((4,), -1, dtype=torch.int64, device="cuda")
     ws = db.workspace(db.wqe_workspace_size(max(n, 1), R))
+    d_psn = dev64(np.asarray(psn_head, dtype=np.uint64)) if mtu else None
     d_req = dev64(req) if n else torch.zeros((0, 2), dtype=torch.int64, device="cuda")
     db.wqe_bucket_vmm(d_req, dev64(np.ascontiguousarray(chunk_raddr, dtype=np.uint64)),
                       dev32(np.ascontiguousarray(chunk_rkey, dtype=np.uint32)),
                       dev32(np.ascontiguousarray(chunk_lkey, dtype=np.uint32)), chunk_shift,
-                      world, n_qp, local_base, heap, rings, depth, d_head, count, ws, ctr=ctr)
+                      world, n_qp, local_base, heap, rings, depth, d_head, count, ws, ctr=ctr,
+                      mtu=mtu, psn_head=d_psn)
     torch.cuda.synchronize()
-    return dict(rings=rings, head=host64(d_head), count=host32(count), ctr=host64(ctr))
+    out = dict(rings=rings, head=host64(d_head), count=host32(count), ctr=host64(ctr))
+    if mtu:
+        out["psn_head"] = host64(d_psn)
+    return out
 
 
-def both(db, oracle, req, tables, chunk_shift, world, n_qp, local_base, heap, depth, head):
+def both(db, oracle, req, tables, chunk_shift, world, n_qp, local_base, heap, depth, head,
+         mtu=0, psn_head=None):
     raddr, rkey, lkey = tables
     want = oracle.wqe_bucket_vmm(req, raddr, rkey, lkey, chunk_shift, world, n_qp, local_base,
-                                 heap, depth, head, fill=0xCD)
+                                 heap, depth, head, fill=0xCD, mtu=mtu, psn_head=psn_head)
     got = run_vmm(db, req, raddr, rkey, lkey, chunk_shift, world, n_qp, local_base, heap, depth,
-                  head)
+                  head, mtu=mtu, psn_head=psn_head)
     check(got, want)
+    if mtu:
+        assert (got["psn_head"] == want["psn_head"]).all()
     return got, want
 
 
@@ -91,6 +99,44 @@ def test_random_batches(db, oracle, n, world, n_qp, chunk_shift, depth, max_byte
          n_qp, 0x7C0000000000, heap, depth, head)
 
 
+@pytest.mark.parametrize("variant", ["depth8", "depth2"])
+def test_golden_psn(db, oracle, variant):
+    fx = load_golden("wqe_vmm_hand_cases.json")
+    from test_oracle_wqe import pack
+    ps = fx["psn"]
+    raddr = np.array([[h(x) for x in row] for row in fx["chunk_raddr"]], dtype=np.uint64)
+    got, _ = both(db, oracle, pack(fx["req"]), (raddr, np.array(fx["chunk_rkey"]),
+                                                np.array(fx["chunk_lkey"])),
+                  fx["chunk_shift"], fx["world"], fx["n_qp"], h(fx["local_base"]),
+                  fx["heap_size"], fx[variant]["depth"], fx["head"], mtu=ps["mtu"],
+                  psn_head=np.array(ps["psn_head"], dtype=np.uint64))
+    assert got["psn_head"].tolist() == ps[f"{variant}_psn_head"]
+
+
+@pytest.mark.parametrize("n,world,n_qp,chunk_shift,depth,max_bytes,mtu", [
+    (257, 8, 4, 12, 256, 20000, 1024), (5000, 8, 4, 16, 1024, 200000, 4096),
+    (5000, 8, 4, 12, 128, 20000, 512), (20000, 1, 1, 12, 1 << 17, 100000, 2048),
+    (60000, 1024, 1, 13, 256, 30000, 1024), (3000, 2, 1, 12, 1 << 15, 1 << 20, 512),
+    (100000, 8, 4, 21, 1 << 14, 65536, 4096)])
+def test_random_batches_with_psns(db, oracle, n, world, n_qp, chunk_shift, depth, max_bytes,
+                                  mtu):
+    rng = np.random.default_rng(n + chunk_shift * 1000 + world + mtu)
+    heap = 1 << 30
+    while world * (heap >> chunk_shift) > (1 << 22):
+        heap >>= 1
+    pe = rng.integers(0, world, size=n)
+    qp = rng.integers(0, n_qp, size=n)
+    off = 16 * rng.integers(0, heap // 16, size=n)
+    nbytes = np.minimum(16 * rng.integers(1, max_bytes // 16 + 1, size=n), heap - off)
+    nbytes = np.where(rng.random(n) < 0.03, 0, nbytes)
+    from synth import pack_put_requests
+    req = pack_put_requests(off, nbytes, pe, qp)
+    head = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    psn0 = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    both(db, oracle, req, tables_for(rng, world, heap >> chunk_shift, chunk_shift), chunk_shift,
+         world, n_qp, 0x7C0000000000, heap, depth, head, mtu=mtu, psn_head=psn0)
+
+
 def test_one_chunk_matches_static_heap(db, oracle):
     import synth
     from test_gpu_wqe import run_gpu
@@ -117,6 +163,10 @@ def test_bad_arguments(db):
     for shift, depth in ((3, 8), (49, 8), (12, 6), (12, 1 << 32)):
         with pytest.raises(db.DescBuildError, match="invalid"):
             db.wqe_bucket_vmm(t, tab, t32, t32, shift, 2, 1, 0, 1 << 16, rings, depth, head, cnt, ws)
+    for shift, mtu, psn in ((12, 256, head), (11, 1024, head), (12, 1024, None)):
+        with pytest.raises(db.DescBuildError, match="invalid"):
+            db.wqe_bucket_vmm(t, tab, t32, t32, shift, 2, 1, 0, 1 << 16, rings, 8, head, cnt, ws,
+                              mtu=mtu, psn_head=psn)
 
 
 def test_full_size_workload(db, oracle):
