@@ -56,7 +56,7 @@ def _load():
                                              vp, i32]
             lib.oracle_mr_round.restype = None
             lib.oracle_mr_round.argtypes = [u64, u64, vp]
-            for name in ("oracle_mr_linear", "oracle_mr_bsearch"):
+            for name in ("oracle_mr_linear", "oracle_mr_bsearch", "oracle_mr_prefix_max"):
                 fn = getattr(lib, name)
                 fn.restype = None
                 fn.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp]
@@ -156,6 +156,11 @@ def _mr(fn_name, queries, start, end, lkey):
 def mr_linear(queries, start, end, lkey) -> dict:
     """The definition: first containing range by index, for every query."""
     return _mr("oracle_mr_linear", queries, start, end, lkey)
+
+
+def mr_prefix_max(queries, start, end, lkey) -> dict:
+    """Same result for tables sorted by start whose ranges may overlap."""
+    return _mr("oracle_mr_prefix_max", queries, start, end, lkey)
 
 
 def mr_bsearch(queries, start, end, lkey) -> dict:

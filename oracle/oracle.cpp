@@ -256,6 +256,35 @@ void oracle_mr_linear(const uint64_t* q, uint64_t n_q, const uint64_t* start,
   }
 }
 
+// For tables sorted by start whose ranges may overlap: the lowest index
+// containing [base, aend) has start <= base, so it lies in [0, j] with j the
+// last range starting at or below base; among those it is the first whose
+// end reaches aend, found by binary search on the prefix maximum of the ends
+// (non-decreasing). Pinned against oracle_mr_linear, the definition.
+void oracle_mr_prefix_max(const uint64_t* q, uint64_t n_q, const uint64_t* start,
+                          const uint64_t* end, const uint32_t* lkey, uint64_t n_mr,
+                          int32_t* idx, uint32_t* lkey_out, uint8_t* kind) {
+  std::vector<uint64_t> pm(n_mr);
+  for (uint64_t i = 0; i < n_mr; ++i) pm[i] = i ? std::max(pm[i - 1], end[i]) : end[i];
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t base, aend;
+    idx[k] = -1;
+    lkey_out[k] = 0;
+    if (!mr_round(q[2 * k], q[2 * k + 1], &base, &aend)) {
+      kind[k] = 3;
+      continue;
+    }
+    kind[k] = 0;
+    const uint64_t cnt = (uint64_t)(std::upper_bound(start, start + n_mr, base) - start);
+    if (cnt == 0) continue;
+    const uint64_t i = (uint64_t)(std::lower_bound(pm.begin(), pm.begin() + cnt, aend) - pm.begin());
+    if (i == cnt) continue;
+    idx[k] = (int32_t)i;
+    lkey_out[k] = lkey[i];
+    kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;
+  }
+}
+
 // For tables sorted by start with no two ranges overlapping: the only range
 // that can contain [base, aend) is the last one starting at or below base.
 void oracle_mr_bsearch(const uint64_t* q, uint64_t n_q, const uint64_t* start,

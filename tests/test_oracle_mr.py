@@ -123,3 +123,33 @@ def test_edges(oracle):
         assert out["idx"].tolist() == [0, 1, -1, -1, 0]
     empty = oracle.mr_linear(q, start[:0], end[:0], lkey[:0])
     assert (empty["kind"] == 0).all() and (empty["idx"] == -1).all()
+
+
+def overlapping_table(rng, n, span_pages, max_pages):
+    """Sorted-by-start ranges that may overlap (page-granular, non-empty)."""
+    start = np.sort(rng.integers(0, span_pages, size=n)).astype(np.uint64) * np.uint64(4096)
+    pages = rng.integers(1, max_pages + 1, size=n).astype(np.uint64)
+    end = start + pages * np.uint64(4096)
+    lkey = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    return start, end, lkey
+
+
+@pytest.mark.parametrize("n,span,maxp", [(1, 10, 3), (7, 20, 8), (50, 200, 40), (300, 2000, 400),
+                                          (2000, 100000, 30)])
+def test_prefix_max_equals_the_definition_on_overlapping_tables(oracle, n, span, maxp):
+    """The O(log N) search for sorted overlapping tables gives the lowest
+    containing index, as the linear definition does."""
+    rng = np.random.default_rng(n * 7 + span)
+    start, end, lkey = overlapping_table(rng, n, span, maxp)
+    m = 20000
+    a = rng.integers(0, (span + maxp) * 4096, size=m).astype(np.uint64)
+    sz = rng.integers(0, 8 * 4096, size=m).astype(np.uint64)
+    pick = rng.integers(0, n, size=m)
+    a = np.where(rng.random(m) < 0.4, start[pick], a)
+    sz = np.where(rng.random(m) < 0.3, end[pick] - start[pick], sz)
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    lin = oracle.mr_linear(q, start, end, lkey)
+    pm = oracle.mr_prefix_max(q, start, end, lkey)
+    for key in ("idx", "lkey", "kind"):
+        assert (lin[key] == pm[key]).all(), key
+    assert (lin["kind"] == 1).any() and (lin["kind"] == 2).any() and (lin["kind"] == 0).any()

@@ -42,6 +42,8 @@ MUTANTS = [
     ("mr exact compares one end only",
      "kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;",
      "kind[k] = (start[i] == base) ? 1 : 2;"),
+    ("mr prefix max keeps each end alone",
+     "pm[i] = i ? std::max(pm[i - 1], end[i]) : end[i];", "pm[i] = end[i];"),
     ("mr bsearch takes lower_bound",
      "std::upper_bound(start, start + n_mr, base);", "std::lower_bound(start, start + n_mr, base);"),
     ("wqe ring order is qp-major",
