@@ -281,7 +281,8 @@ void oracle_mr_prefix_max(const uint64_t* q, uint64_t n_q, const uint64_t* start
     if (i == cnt) continue;
     idx[k] = (int32_t)i;
     lkey_out[k] = lkey[i];
-    kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;
+    const bool same_ends = start[i] == base && end[i] == aend;
+    kind[k] = same_ends ? 1 : 2;
   }
 }
 

@@ -91,6 +91,24 @@ def test_overlapping_table_lowest_index_wins(oracle):
     assert out["idx"][0] == 0 and out["kind"][0] == 2 and out["lkey"][0] == 1
 
 
+def test_overlap_hand_cases(oracle):
+    """Hand-worked values on a table of overlapping records (a partial
+    overlap is registered anew), checked against page sets as well."""
+    fx = load_golden("mr_hand_cases.json")["overlap_after_partial_miss"]
+    table = [(h(r["start"]), h(r["end"])) for r in fx["table"]]
+    start = np.array([t[0] for t in table], dtype=np.uint64)
+    end = np.array([t[1] for t in table], dtype=np.uint64)
+    lkey = np.array([r["lkey"] for r in fx["table"]], dtype=np.uint32)
+    q = np.array([[h(x["off"]), x["size"]] for x in fx["queries"]], dtype=np.uint64)
+    for x in fx["queries"]:
+        assert brute_force_kind(h(x["off"]), x["size"], table) == (x["kind"], x["idx"])
+    for fn in (oracle.mr_linear, oracle.mr_prefix_max):
+        out = fn(q, start, end, lkey)
+        assert out["kind"].tolist() == [x["kind"] for x in fx["queries"]]
+        assert out["idx"].tolist() == [x["idx"] for x in fx["queries"]]
+        assert out["lkey"].tolist() == [x["lkey"] for x in fx["queries"]]
+
+
 def test_linear_equals_bsearch_medium(oracle):
     import synth
     rng = np.random.default_rng(11)

@@ -42,6 +42,12 @@ MUTANTS = [
     ("mr exact compares one end only",
      "kind[k] = (start[i] == base && end[i] == aend) ? 1 : 2;",
      "kind[k] = (start[i] == base) ? 1 : 2;"),
+    ("mr prefix max: exact compares one end only",
+     "const bool same_ends = start[i] == base && end[i] == aend;",
+     "const bool same_ends = start[i] == base;"),
+    ("mr prefix max searches past the last start at or below base",
+     "std::lower_bound(pm.begin(), pm.begin() + cnt, aend)",
+     "std::lower_bound(pm.begin(), pm.begin() + std::min<uint64_t>(cnt + 1, n_mr), aend)"),
     ("mr prefix max keeps each end alone",
      "pm[i] = i ? std::max(pm[i - 1], end[i]) : end[i];", "pm[i] = end[i];"),
     ("mr bsearch takes lower_bound",
