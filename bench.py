@@ -13,8 +13,10 @@ batches), with inputs resident in HBM. Each kernel call is also timed alone
 with CUDA events on the launch stream; the dominant one (prp_large) gives the
 roofline line. ``e2e`` repeats the step through the same API with inputs in
 pinned host memory and every descriptor copied back to the host. ``next``
-times, on its own and outside the step, the row built after the hot path:
-the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm).
+times, on its own and outside the step, the rows built after the hot path:
+the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm, without and
+with packet sequence numbers) and the MR lookup on a table whose records
+overlap (db_mr_lookup_overlap).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (the batches are independent);
@@ -300,7 +302,8 @@ class Step:
 def run_next(args, device) -> dict:
     """The rows after the hot path, timed on their own (not part of a step):
     the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm), without and
-    with packet sequence numbers (mtu 4096)."""
+    with packet sequence numbers (mtu 4096), and the MR lookup on a table
+    whose records overlap (db_mr_lookup_overlap)."""
     import torch as t
     import descriptor_build_gb300 as db
     import synth
@@ -348,7 +351,52 @@ def run_next(args, device) -> dict:
             "chunk_bytes": 1 << P["chunk_shift"], "mtu": mtu, "algorithmic_bytes": alg,
             "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
             "note": "not part of the step: timed alone, same stream discipline"}
+    out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
     return out
+
+
+def time_mr_overlap(args, device, stream) -> dict:
+    """db_mr_lookup_overlap on a registration table whose records overlap
+    (1,048,576 disjoint records plus 262,144 straddling ones), 16,777,216
+    queries; algorithmic bytes as for mr_lookup."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    import synth
+    m = synth.mr_lookup_overlap()
+    d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+    d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+    nq, nr = m["queries"].shape[0], m["mr_start"].shape[0]
+    b = dict(q=d64(m["queries"]), start=d64(m["mr_start"]), end=d64(m["mr_end"]),
+             lkey=d32(m["mr_lkey"]), idx=t.empty(nq, dtype=t.int32, device=device),
+             olkey=t.empty(nq, dtype=t.int32, device=device),
+             kind=t.empty(nq, dtype=t.uint8, device=device),
+             ctr=t.zeros(4, dtype=t.int64, device=device),
+             ws=db.workspace(db.mr_workspace_size(nr), device))
+
+    def call():
+        db.mr_lookup_overlap(b["q"], b["start"], b["end"], b["lkey"], b["idx"], b["olkey"],
+                             b["kind"], b["ws"], ctr=b["ctr"], stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    t.cuda.synchronize(device)
+    evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, z in evs:
+        a.record(stream)
+        call()
+        z.record(stream)
+    t.cuda.synchronize(device)
+    ms = statistics.mean(a.elapsed_time(z) for a, z in evs)
+    if int(b["ctr"][3].item()):
+        raise RuntimeError("mr_lookup_overlap: device error bits")
+    alg = 25 * nq + 20 * nr
+    peak, _ = peak_gbs()
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "M_req_per_s": round(nq / ms / 1e3, 2), "records": nr,
+            "hits": int(b["ctr"][0].item()), "algorithmic_bytes": alg,
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 5,
+            "note": "not part of the step: timed alone, same stream discipline"}
 
 
 def run_ours(args, inp, world, device, dist):

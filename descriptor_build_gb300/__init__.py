@@ -28,7 +28,7 @@ from . import build as _build
 __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
-    "mr_workspace_size", "mr_lookup", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
+    "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
     "strerror",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
@@ -65,6 +65,7 @@ def _load():
     lib.db_prp_build_static.argtypes = [vp, u64, vp, u64, u64, u64, vp, vp, vp, vp, vp, u32, vp]
     lib.db_mr_workspace_size.argtypes = [u64, psz]
     lib.db_mr_lookup.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp, vp, vp, sz, vp]
+    lib.db_mr_lookup_overlap.argtypes = lib.db_mr_lookup.argtypes
     lib.db_wqe_workspace_size.argtypes = [u64, u32, psz]
     lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
                                   vp, sz, vp]
@@ -72,7 +73,7 @@ def _load():
                                       vp, u32, vp, vp, vp, sz, vp]
     for name in ("db_prp_workspace_size", "db_prp_build", "db_prp_build_static",
                  "db_mr_workspace_size",
-                 "db_mr_lookup", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
+                 "db_mr_lookup", "db_mr_lookup_overlap", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
                  "db_last_cuda_error"):
         getattr(lib, name).restype = i32
     lib.db_strerror.argtypes = [i32]
@@ -176,6 +177,18 @@ def mr_lookup(q: torch.Tensor, mr_start: torch.Tensor, mr_end: torch.Tensor,
     n_q = _records(q, 16)
     n_mr = _records(mr_start, 8)
     _check("db_mr_lookup", _lib.db_mr_lookup(
+        _ptr(q), n_q, _ptr(mr_start), _ptr(mr_end), _ptr(mr_lkey), n_mr, _ptr(idx), _ptr(lkey),
+        _ptr(kind), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def mr_lookup_overlap(q: torch.Tensor, mr_start: torch.Tensor, mr_end: torch.Tensor,
+                      mr_lkey: torch.Tensor, idx: torch.Tensor, lkey: torch.Tensor,
+                      kind: torch.Tensor, ws: torch.Tensor, ctr: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """db_mr_lookup_overlap: the same on a start-sorted table whose ranges may overlap."""
+    n_q = _records(q, 16)
+    n_mr = _records(mr_start, 8)
+    _check("db_mr_lookup_overlap", _lib.db_mr_lookup_overlap(
         _ptr(q), n_q, _ptr(mr_start), _ptr(mr_end), _ptr(mr_lkey), n_mr, _ptr(idx), _ptr(lkey),
         _ptr(kind), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 

@@ -61,7 +61,7 @@ struct Header {        // first 256 bytes of the workspace
 struct alignas(32) Rec {
   uint64_t start, end;
   uint32_t lkey, pad0;
-  uint64_t pad1;
+  uint64_t before;  // tables that may overlap: the largest end of records 0 .. i-1 (0 for i = 0)
 };
 constexpr size_t kHeaderBytes = 256;
 
@@ -88,9 +88,14 @@ constexpr uint32_t kNoOff = 0xFFFFFFFFu;
 constexpr uint32_t kMaxOffsetShift = 43;  // bucket widths up to 2^43 bytes keep offsets in 32 bits
 inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * sizeof(Dir) + 255) & ~(size_t)255; }
 static_assert(sizeof(Dir) == 32, "one L2 sector per directory entry");
+// Tables that may overlap: Rec::before is built by a max-scan of the ends
+// in blocks of 1024 records, whose block maxima sit after the records.
+constexpr int kPmBlock = 1024;
+inline size_t pm_blocks(uint64_t n_mr) { return (n_mr + kPmBlock - 1) / kPmBlock; }
+inline size_t rec_bytes(uint64_t n_mr) { return ((size_t)n_mr * sizeof(Rec) + 255) & ~(size_t)255; }
 inline size_t ws_bytes_for(uint64_t n_mr) {
   const uint32_t nb = buckets_for(n_mr);
-  return kHeaderBytes + dir_bytes(nb) + (size_t)n_mr * sizeof(Rec);
+  return kHeaderBytes + dir_bytes(nb) + rec_bytes(n_mr) + pm_blocks(n_mr) * 8;
 }
 
 struct BuildParams {
@@ -103,6 +108,7 @@ struct BuildParams {
   Rec* rec;
   uint32_t nb;
   uint32_t log_nb;
+  bool overlap;  // ranges may overlap: only starts must be sorted
 };
 
 __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t shift,
@@ -173,9 +179,9 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
       r.end = e;
       r.lkey = p.lkey[i];
       r.pad0 = 0;
-      r.pad1 = 0;
+      r.before = 0;
       p.rec[i] = r;
-      if (!(s < e) || (i > 0 && p.end[i - 1] > s)) bad = true;
+      if (!(s < e) || (i > 0 && (p.overlap ? p.start[i - 1] > s : p.end[i - 1] > s))) bad = true;
       b0 = i == 0 ? 0 : bucket_of(p.start[i - 1], lo, shift, p.nb) + 1;
       b1 = bucket_of(s, lo, shift, p.nb);
     }
@@ -217,6 +223,28 @@ struct LookupParams {
   db_counters* ctr;
 };
 
+// Tables that may overlap: the first record i <= j whose prefix maximum of
+// ends, pm(i) = rec[i + 1].before, reaches aend, given pm(j - 1) >= aend.
+// Galloping back from j - 1 (overlaps are usually short), then a binary
+// search between the last miss and the first hit.
+__device__ __forceinline__ uint32_t first_reaching(const Rec* rec, uint32_t j, uint64_t aend,
+                                                   uint64_t pol) {
+  int64_t hi = (int64_t)j - 1, step = 1;  // pm(hi) >= aend
+  while (hi - step >= 0 && ld_table8(&rec[hi - step + 1].before, pol) >= aend) {
+    hi -= step;
+    step <<= 1;
+  }
+  int64_t lo = hi - step;  // pm(lo) < aend, or lo = -1
+  if (lo < -1) lo = -1;
+  while (hi - lo > 1) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (ld_table8(&rec[mid + 1].before, pol) >= aend) hi = mid;
+    else lo = mid;
+  }
+  return (uint32_t)hi;
+}
+
+template <bool kOverlap>
 __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(const LookupParams p) {
   const uint64_t pol_first = policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
@@ -339,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
         }
       }
     }
-    // The candidate is record a - 1: the last one starting at or below base.
+    // The candidate is record j = a - 1: the last one starting at or below
+    // base. On a table that may overlap, an earlier record whose end
+    // reaches aend (Rec::before of j says whether one exists) comes first.
 #pragma unroll
     for (int k = 0; k < kQPT; ++k) {
       const uint64_t i = first + (uint64_t)k * kThreads;
@@ -349,9 +379,13 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
       uint8_t out_kind = state[k] == 2 ? DB_MR_INVALID : DB_MR_MISS;
       invalid += state[k] == 2;
       if (state[k] == 1 && a[k] > 0) {
-        const uint32_t j = a[k] - 1;
-        uint64_t rs, re, rk, pad;
-        ld_table32(&p.rec[j], pol_last, rs, re, rk, pad);
+        uint32_t j = a[k] - 1;
+        uint64_t rs, re, rk, before;
+        ld_table32(&p.rec[j], pol_last, rs, re, rk, before);
+        if (kOverlap && before >= aend[k]) {
+          j = first_reaching(p.rec, j, aend[k], pol_last);
+          ld_table32(&p.rec[j], pol_last, rs, re, rk, before);
+        }
         if (rs <= base[k] && aend[k] <= re) {
           out_idx = (int32_t)j;
           out_lkey = (uint32_t)rk;
@@ -400,6 +434,63 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
   }
 }
 
+// ------------------------------------------------------ overlapping tables
+// Rec::before of record i + 1 is the prefix maximum of the ends,
+// pm(i) = max(end[0..i]): a block-local inclusive max-scan, a scan of the
+// block maxima (one CTA), then each block takes the maximum of the blocks
+// before it. A record read then says whether an earlier one may contain
+// the query, so the common case costs the same single 32-byte record load
+// as on a disjoint table.
+__device__ __forceinline__ uint64_t warp_max_scan(uint64_t x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o && y > x) x = y;
+  }
+  return x;
+}
+// Inclusive max-scan of one value per thread over a CTA of kPmBlock threads.
+__device__ __forceinline__ uint64_t block_max_scan(uint64_t x, uint64_t* s_w) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  x = warp_max_scan(x, lane);
+  if (lane == 31) s_w[warp] = x;
+  __syncthreads();
+  if (warp == 0) s_w[lane] = warp_max_scan(s_w[lane], lane);  // kPmBlock / 32 == 32 warps
+  __syncthreads();
+  const uint64_t before = warp ? s_w[warp - 1] : 0ull;
+  return before > x ? before : x;
+}
+__global__ void __launch_bounds__(kPmBlock) mr_pm_block_kernel(const uint64_t* end, uint64_t n,
+                                                               Rec* rec, uint64_t* bmax) {
+  __shared__ uint64_t s_w[32];
+  const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
+  const uint64_t x = block_max_scan(i < n ? end[i] : 0ull, s_w);
+  if (i + 1 < n) rec[i + 1].before = x;  // block-local for now
+  if (threadIdx.x == kPmBlock - 1) bmax[blockIdx.x] = x;
+}
+__global__ void __launch_bounds__(kPmBlock) mr_pm_scan_kernel(uint64_t* bmax, uint64_t nblk) {
+  __shared__ uint64_t s_w[32];
+  uint64_t carry = 0;
+  for (uint64_t b0 = 0; b0 < nblk; b0 += kPmBlock) {
+    const uint64_t b = b0 + threadIdx.x;
+    uint64_t x = block_max_scan(b < nblk ? bmax[b] : 0ull, s_w);
+    x = x > carry ? x : carry;
+    if (b < nblk) bmax[b] = x;
+    __syncthreads();  // block_max_scan's reads of s_w are done
+    if (threadIdx.x == kPmBlock - 1) s_w[0] = x;  // this round's maximum carries to the next
+    __syncthreads();
+    carry = s_w[0];
+    __syncthreads();
+  }
+}
+__global__ void __launch_bounds__(kPmBlock) mr_pm_apply_kernel(Rec* rec, uint64_t n,
+                                                               const uint64_t* bmax) {
+  const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
+  if (blockIdx.x == 0 || i + 1 >= n) return;
+  const uint64_t prior = bmax[blockIdx.x - 1];
+  if (prior > rec[i + 1].before) rec[i + 1].before = prior;
+}
+
 int lookup_ctas_per_sm() {
   static int per_sm[64] = {0};
   int dev = 0;
@@ -407,7 +498,7 @@ int lookup_ctas_per_sm() {
   int& occ = per_sm[dev & 63];
   if (occ == 0) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, mr_lookup_kernel, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, mr_lookup_kernel<false>, kThreads, 0) !=
             cudaSuccess ||
         o < 1)
       o = 1;
@@ -427,11 +518,11 @@ extern "C" int db_mr_workspace_size(uint64_t n_mr, size_t* bytes) {
   return 0;
 }
 
-extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
-                            const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr,
-                            int32_t* idx, uint32_t* lkey, uint8_t* kind, db_counters* ctr,
-                            void* ws, size_t ws_bytes, void* stream) {
-  cudaStream_t s = (cudaStream_t)stream;
+namespace {
+
+int mr_call(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint64_t* mr_end,
+            const uint32_t* mr_lkey, uint64_t n_mr, int32_t* idx, uint32_t* lkey, uint8_t* kind,
+            db_counters* ctr, void* ws, size_t ws_bytes, cudaStream_t s, bool overlap) {
   if (n_mr >= (1ull << 31)) return -EINVAL;
   if (ctr && !aligned(ctr, 8)) return -EINVAL;
   if (n_q == 0) {
@@ -453,16 +544,27 @@ extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_
   char* w = static_cast<char*>(ws);
   mr::Header* hdr = reinterpret_cast<mr::Header*>(w);
   mr::Dir* dir = reinterpret_cast<mr::Dir*>(w + mr::kHeaderBytes);
-  mr::Rec* rec = reinterpret_cast<mr::Rec*>(w + mr::kHeaderBytes + mr::dir_bytes(nb));
+  char* recs = w + mr::kHeaderBytes + mr::dir_bytes(nb);
+  mr::Rec* rec = reinterpret_cast<mr::Rec*>(recs);
+  uint64_t* bmax = reinterpret_cast<uint64_t*>(recs + mr::rec_bytes(n_mr));
 
   if (n_mr > 0) {
-    mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb};
+    mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb, overlap};
     uint64_t grid = (n_mr + mr::kBuildThreads - 1) / mr::kBuildThreads;
     const uint64_t cap = (uint64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
     int rc = launch_result();
     if (rc) return rc;
+    if (overlap) {
+      const uint64_t nblk = mr::pm_blocks(n_mr);
+      mr::mr_pm_block_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(mr_end, n_mr, rec, bmax);
+      if ((rc = launch_result())) return rc;
+      mr::mr_pm_scan_kernel<<<1, mr::kPmBlock, 0, s>>>(bmax, nblk);
+      if ((rc = launch_result())) return rc;
+      mr::mr_pm_apply_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(rec, n_mr, bmax);
+      if ((rc = launch_result())) return rc;
+    }
   }
   mr::LookupParams l{reinterpret_cast<const ulonglong2*>(q), n_q, n_mr, hdr, hdr, dir, rec,
                      idx, lkey, kind, ctr};
@@ -470,6 +572,27 @@ extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_
   uint64_t grid = (n_q + per_cta - 1) / per_cta;
   const uint64_t resident = (uint64_t)num_sms() * mr::lookup_ctas_per_sm();
   if (grid > resident) grid = resident;
-  mr::mr_lookup_kernel<<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+  if (overlap)
+    mr::mr_lookup_kernel<true><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+  else
+    mr::mr_lookup_kernel<false><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
   return launch_result();
+}
+
+}  // namespace
+
+extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
+                            const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr,
+                            int32_t* idx, uint32_t* lkey, uint8_t* kind, db_counters* ctr,
+                            void* ws, size_t ws_bytes, void* stream) {
+  return mr_call(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
+                 (cudaStream_t)stream, false);
+}
+
+extern "C" int db_mr_lookup_overlap(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
+                                    const uint64_t* mr_end, const uint32_t* mr_lkey,
+                                    uint64_t n_mr, int32_t* idx, uint32_t* lkey, uint8_t* kind,
+                                    db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
+  return mr_call(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
+                 (cudaStream_t)stream, true);
 }

@@ -6,7 +6,8 @@
  *   db_prp_build   NVMe PRP1/PRP2 and chained 4 KiB PRP lists from heap
  *                  offsets and a 64 KiB-granular bus-address LUT.
  *   db_mr_lookup   classify ranges against a sorted registration (MR) table
- *                  after rounding them to whole 4 KiB pages.
+ *                  after rounding them to whole 4 KiB pages
+ *                  (db_mr_lookup_overlap: records may overlap).
  *   db_wqe_bucket  translate symmetric-heap puts and stable-partition them
  *                  into per-queue rings of 64-byte work-queue entries.
  *
@@ -192,6 +193,29 @@ int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
                  const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr, int32_t* idx,
                  uint32_t* lkey, uint8_t* kind, db_counters* ctr, void* ws, size_t ws_bytes,
                  void* stream);
+
+/* db_mr_lookup_overlap: the same classification on a table whose records
+ * may overlap. Source: the same page, "IB Backend MR Cache": a range that
+ * only partly overlaps a cached MR is no hit and is registered anew, so the
+ * cache comes to hold MRs that overlap one another, and "Communicator User
+ * Registration Cache" inserts each new record in address order.
+ *
+ * The answer is the same as db_mr_lookup's rule above: the LOWEST i with
+ * mr_start[i] <= base and aend <= mr_end[i]. Records must be non-empty and
+ * sorted by start (mr_start[i] < mr_end[i], mr_start[i] <= mr_start[i+1]);
+ * ends are free. Every record at or after the last one starting at or
+ * below base starts too late, so the answer is the first i <= j whose
+ * prefix maximum of ends reaches aend (the prefix maximum is kept in the
+ * workspace, rebuilt on every call).
+ *
+ * Arguments, workspace (db_mr_workspace_size), counters and limits as for
+ * db_mr_lookup; err gets DB_ERR_TABLE_ORDER when starts are not sorted or
+ * a record is empty.
+ */
+int db_mr_lookup_overlap(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
+                         const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr,
+                         int32_t* idx, uint32_t* lkey, uint8_t* kind, db_counters* ctr,
+                         void* ws, size_t ws_bytes, void* stream);
 
 /* ---- put translation and WQE bucketing ------------------------------------
  * Source: "mori communication library analysis (1)". Static-heap put:

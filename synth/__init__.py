@@ -36,7 +36,8 @@ GiB = 1024 * MiB
 SEED_BASE = 0xDB5EED00
 
 # Workload names in the order of the study's configuration list.
-WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket", "put_bucket_vmm")
+WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket", "put_bucket_vmm",
+             "mr_lookup_overlap")
 
 
 def seed_of(name: str) -> int:
@@ -273,6 +274,67 @@ def mr_lookup(seed: int | None = None, n_mr: int = 1_048_576,
     stop[x] = np.where(in_gap, gap_stop, st_stop)
 
     return dict(name="mr_lookup", mr_start=start, mr_end=end, mr_lkey=lkey,
+                queries=pack_ranges(addr, stop - addr), query_mix=kind)
+
+
+def mr_lookup_overlap(seed: int | None = None, n_mr: int = 1_048_576,
+                      n_q: int = 16_777_216, extra: float = 0.25) -> dict:
+    """A registration table whose records overlap, plus query ranges.
+
+    The disjoint table of ``mr_table`` gets ``extra * n_mr`` more records,
+    each for a range that straddles an existing record's end (from 1 page
+    up to the whole record before it, 1 .. 64 pages after): the ranges a
+    cache registers anew after a partial-overlap miss. The merged table is
+    sorted by start (stably, so an original record precedes an extra one
+    with the same start). Queries pick a merged record uniformly: 40 % the
+    record itself (half with in-page slack), 40 % a page run inside it,
+    20 % a range straddling its end by 1 .. 128 pages. Which record answers
+    a query depends on the overlaps, so no kind is fixed by the mix.
+    """
+    rng = _rng(seed_of("mr_lookup_overlap") if seed is None else seed)
+    start, end, lkey, _ = mr_table(rng, n_mr)
+    P = np.uint64(4096)
+    pages = (end - start) // P
+    n_x = int(n_mr * extra)
+    m = rng.integers(0, n_mr, size=n_x)
+    back = 1 + (rng.random(n_x) * pages[m].astype(np.float64)).astype(np.uint64)
+    back = np.minimum(back, pages[m])
+    ahead = 1 + rng.integers(0, 64, size=n_x, dtype=np.uint64)
+    xs = end[m] - back * P
+    xe = end[m] + ahead * P
+    xk = rng.integers(0, 1 << 32, size=n_x, dtype=np.uint64).astype(np.uint32)
+    all_s = np.concatenate([start, xs])
+    order = np.argsort(all_s, kind="stable")
+    start = all_s[order]
+    end = np.concatenate([end, xe])[order]
+    lkey = np.concatenate([lkey, xk])[order]
+    n = start.shape[0]
+    pages = (end - start) // P
+
+    u = rng.random(n_q)
+    kind = np.where(u < 0.4, 0, np.where(u < 0.8, 1, 2))
+    r = rng.integers(0, n, size=n_q)
+    npg = pages[r]
+    a = rng.integers(0, 4096, size=n_q, dtype=np.uint64)
+    b = rng.integers(0, 4096, size=n_q, dtype=np.uint64)
+    b = np.where(a + b >= P, P - np.uint64(1) - a, b)
+    slack = rng.random(n_q) < 0.5
+    # 0: the record, with or without slack
+    addr0 = start[r] + np.where(slack, a, np.uint64(0))
+    stop0 = end[r] - np.where(slack, b, np.uint64(0))
+    # 1: a page run [p0, p1) inside the record
+    p0 = np.minimum((rng.random(n_q) * npg.astype(np.float64)).astype(np.uint64), npg - np.uint64(1))
+    p1 = p0 + np.uint64(1) + (rng.random(n_q) * (npg - p0).astype(np.float64)).astype(np.uint64)
+    p1 = np.minimum(p1, npg)
+    addr1 = start[r] + p0 * P + a
+    stop1 = start[r] + p1 * P - np.where(p1 - p0 == np.uint64(1), np.minimum(b, P - np.uint64(1) - a), b)
+    # 2: straddling the record's end
+    bk = np.minimum(np.uint64(1) + (rng.random(n_q) * npg.astype(np.float64)).astype(np.uint64), npg)
+    addr2 = end[r] - bk * P
+    stop2 = end[r] + (np.uint64(1) + rng.integers(0, 128, size=n_q, dtype=np.uint64)) * P
+    addr = np.where(kind == 0, addr0, np.where(kind == 1, addr1, addr2))
+    stop = np.where(kind == 0, stop0, np.where(kind == 1, stop1, stop2))
+    return dict(name="mr_lookup_overlap", mr_start=start, mr_end=end, mr_lkey=lkey,
                 queries=pack_ranges(addr, stop - addr), query_mix=kind)
 
 
