@@ -66,6 +66,10 @@ def _load():
             lib.oracle_wqe_bucket_vmm.restype = None
             lib.oracle_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64,
                                                   vp, u64, vp, u32, vp, vp, vp]
+            lib.oracle_cq_mirror_pass.restype = u32
+            lib.oracle_cq_mirror_pass.argtypes = [vp, u32, vp, vp, vp, u32]
+            lib.oracle_cq_ack.restype = u32
+            lib.oracle_cq_ack.argtypes = [u32, u32, u32]
             _lib = lib
     return _lib
 
@@ -222,3 +226,25 @@ def wqe_bucket_vmm(req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift: int, w
     if mtu:
         out["psn_head"] = psn
     return out
+
+
+# ------------------------------------------------------------------ CQ mirror
+def cq_mirror_pass(dev_cq: np.ndarray, head: int, phase: int, host_cq: np.ndarray,
+                   max_entries: int | None = None):
+    """One mirror pass over a completion queue ([depth, 4] uint32 entries):
+    copies the entries whose phase tag is the expected one into ``host_cq``
+    (in place). Returns (copied, head, phase)."""
+    assert dev_cq.dtype == np.uint32 and dev_cq.shape[1] == 4 and dev_cq.flags["C_CONTIGUOUS"]
+    assert host_cq.dtype == np.uint32 and host_cq.shape == dev_cq.shape
+    assert host_cq.flags["C_CONTIGUOUS"]
+    depth = dev_cq.shape[0]
+    h = np.array([head], dtype=np.uint32)
+    ph = np.array([phase], dtype=np.uint32)
+    n = _load().oracle_cq_mirror_pass(_p(dev_cq), depth, _p(h), _p(ph), _p(host_cq),
+                                      depth if max_entries is None else max_entries)
+    return int(n), int(h[0]), int(ph[0])
+
+
+def cq_ack(cur: int, now: int, keep: int) -> int:
+    """Acknowledgement after working under generation ``cur`` and finding ``now``."""
+    return int(_load().oracle_cq_ack(cur, now, keep))

@@ -24,6 +24,11 @@
 //    branch (one WQE per chunk: min of the source and destination chunk
 //    remainders and the bytes left) and the warp-level WQE slot reservation
 //    (a post index per send queue).
+//  * CQ mirror -- xNVMe "uPCIe CUDA" backend page, "Completions in device
+//    memory": a resident kernel watches each device-memory completion queue
+//    with one warp and copies completions into the host CQ as their phase
+//    bit turns; a slot per queue carries a generation (odd while attached)
+//    and an acknowledgement.
 //
 // Readings where the pages are silent are listed with each function.
 //
@@ -537,6 +542,45 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
   ctr[1] = n_invalid;
   ctr[2] = n_overflow;
   ctr[3] = err;
+}
+
+// ---------------------------------------------------------------- CQ mirror
+// Readings: a completion entry is 16 bytes (four dwords) in the NVMe layout,
+// whose phase tag is bit 16 of the fourth dword; a fresh queue expects
+// phase 1, and the expected phase flips each time the head wraps to 0; an
+// entry is copied whole to the same position of the host CQ.
+//
+// One pass of the mirror over one queue: starting at (head, phase), every
+// entry whose phase tag is the expected one is copied, in queue order,
+// stopping at the first entry that is not, or after `max` entries. Returns
+// how many were copied; head and phase are advanced past them.
+uint32_t oracle_cq_mirror_pass(const uint32_t* dev_cq, uint32_t depth, uint32_t* head,
+                               uint32_t* phase, uint32_t* host_cq, uint32_t max) {
+  uint32_t copied = 0;
+  while (copied < max) {
+    const uint32_t* entry = dev_cq + 4 * (uint64_t)*head;
+    const uint32_t tag = (entry[3] >> 16) & 1u;
+    if (tag != *phase) break;
+    for (int w = 0; w < 4; ++w) host_cq[4 * (uint64_t)*head + w] = entry[w];
+    copied += 1;
+    *head += 1;
+    if (*head == depth) {
+      *head = 0;
+      *phase ^= 1u;
+    }
+  }
+  return copied;
+}
+
+// The acknowledgement written by a warp that last worked under generation
+// `cur` (0 if under none) and now finds generation `now`: once the
+// generation has moved on from an odd value, that odd value; on finding an
+// even generation, the odd value before it (a queue detached before the
+// warp took it up has nothing to drain). Otherwise `keep` (no write).
+uint32_t oracle_cq_ack(uint32_t cur, uint32_t now, uint32_t keep) {
+  if ((cur & 1u) && now != cur) return cur;
+  if ((now & 1u) == 0 && now > 0) return now - 1;
+  return keep;
 }
 
 }  // extern "C"

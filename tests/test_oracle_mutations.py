@@ -77,6 +77,16 @@ MUTANTS = [
     ("psn taken after its own WQE",
      "put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));  // first PSN\n        psn_taken[r] += (t + mtu - 1) / mtu;",
      "psn_taken[r] += (t + mtu - 1) / mtu;\n        put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));"),
+    ("cq phase tag read from bit 15",
+     "const uint32_t tag = (entry[3] >> 16) & 1u;", "const uint32_t tag = (entry[3] >> 15) & 1u;"),
+    ("cq phase kept across the wrap",
+     "      *head = 0;\n      *phase ^= 1u;", "      *head = 0;"),
+    ("cq copies three dwords",
+     "for (int w = 0; w < 4; ++w) host_cq", "for (int w = 0; w < 3; ++w) host_cq"),
+    ("cq even generation acknowledged as itself",
+     "if ((now & 1u) == 0 && now > 0) return now - 1;", "if ((now & 1u) == 0 && now > 0) return now;"),
+    ("cq acknowledges the new generation",
+     "if ((cur & 1u) && now != cur) return cur;", "if ((cur & 1u) && now != cur) return now;"),
     ("vmm fragment runs 16 bytes past its chunk",
      "const uint64_t t = std::min(std::min(src_left, dst_left), remaining);\n      const uint64_t post",
      "const uint64_t t = std::min(src_left + 16, remaining);\n      const uint64_t post"),
@@ -95,7 +105,7 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     env = dict(os.environ, DB_ORACLE_LIB=str(lib))
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
-              "test_oracle_vmm.py")]
+              "test_oracle_vmm.py", "test_oracle_cq.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
