@@ -15,8 +15,9 @@ roofline line. ``e2e`` repeats the step through the same API with inputs in
 pinned host memory and every descriptor copied back to the host. ``next``
 times, on its own and outside the step, the rows built after the hot path:
 the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm, without and
-with packet sequence numbers) and the MR lookup on a table whose records
-overlap (db_mr_lookup_overlap).
+with packet sequence numbers), the MR lookup on a table whose records
+overlap (db_mr_lookup_overlap) and the completion-queue mirror
+(db_cq_mirror: drain rate over 64 queues, latency at queue depth 1).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (the batches are independent);
@@ -302,8 +303,8 @@ class Step:
 def run_next(args, device) -> dict:
     """The rows after the hot path, timed on their own (not part of a step):
     the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm), without and
-    with packet sequence numbers (mtu 4096), and the MR lookup on a table
-    whose records overlap (db_mr_lookup_overlap)."""
+    with packet sequence numbers (mtu 4096), the MR lookup on a table whose
+    records overlap (db_mr_lookup_overlap) and the CQ mirror (db_cq_mirror)."""
     import torch as t
     import descriptor_build_gb300 as db
     import synth
@@ -352,7 +353,131 @@ def run_next(args, device) -> dict:
             "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
             "note": "not part of the step: timed alone, same stream discipline"}
     out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
+    out["cq_mirror"] = time_cq_mirror(args, device)
     return out
+
+
+def time_cq_mirror(args, device) -> dict:
+    """db_cq_mirror with the host standing in for a controller.
+
+    drain: 64 queues of 4,096 entries, each with 4,095 completions already in
+    its device CQ; the time from attaching the queues (the kernel running)
+    until the kernel has copied all of them, averaged over --steps rounds.
+    qd1: one queue, one completion at a time: the round trip from the host
+    issuing the completion's two copies into the device CQ until its host CQ
+    shows the new phase tag, median over 2,000 completions; beside it the
+    same round trip with a copy engine (a 16-byte device-to-host copy queued
+    after the write) doing the mirror's job.
+    Every copied entry is checked against what was written."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    PHASE = np.uint32(1 << 16)
+    depth, nq, k = 4096, 64, 4095
+    rng = np.random.default_rng(0xC0FFEE)
+    copy_s, mir_s = t.cuda.Stream(device=device), t.cuda.Stream(device=device)
+    slots = db.cq_slots(nq)
+    f = db.cq_slot_fields(slots)
+    stop = t.zeros(1, dtype=t.int32).pin_memory()
+    ctr = t.zeros(4, dtype=t.int64, device=device)
+    devs = [t.zeros((depth, 4), dtype=t.int32, device=device) for _ in range(nq)]
+    hosts = [t.zeros((depth, 4), dtype=t.int32).pin_memory() for _ in range(nq)]
+    body = rng.integers(0, 2**32, size=(nq, depth, 4), dtype=np.uint64).astype(np.uint32)
+    body[:, :, 3] |= PHASE                       # first pass: tag 1
+    stage = t.from_numpy(body.view(np.int32)).pin_memory()
+    one_old = t.zeros((depth, 4), dtype=t.int32).pin_memory()
+    one_new = t.zeros((depth, 4), dtype=t.int32).pin_memory()
+    t.cuda.synchronize(device)
+    db.cq_mirror(slots, stop, 20.0, ctr=ctr, stream=mir_s)
+    rates, total = [], 0
+    try:
+        for rep in range(args.warmup + args.steps):
+            if rep:
+                gens = [db.cq_detach(slots, i) for i in range(nq)]
+                if not all(db.cq_wait_ack(slots, i, g, 5.0) for i, g in enumerate(gens)):
+                    raise RuntimeError("cq_mirror: no acknowledgement")
+            with t.cuda.stream(copy_s):
+                for i in range(nq):
+                    devs[i].zero_()
+                    hosts[i].zero_()
+                    devs[i][:k].copy_(stage[i, :k], non_blocking=True)
+            copy_s.synchronize()
+            t0 = time.perf_counter()
+            gnew = np.array([db.cq_attach(slots, i, devs[i], hosts[i]) for i in range(nq)])
+            # a warp writes copied = 0 before it publishes the generation it took up
+            while (not ((f["seen"] == gnew) & (f["copied"] == k)).all()
+                   and time.perf_counter() - t0 < 5.0):
+                pass
+            dt = time.perf_counter() - t0
+            for i in range(nq):
+                got, _, _ = db.cq_host_reap(hosts[i], 0, 1)
+                if got.shape[0] != k or not (got == body[i, :k]).all():
+                    raise RuntimeError("cq_mirror: host CQ differs from the device CQ")
+            total += nq * k
+            if rep >= args.warmup:
+                rates.append(nq * k / dt)
+        # QD1 on queue 0: host issues one completion, polls its host CQ until
+        # the tag shows. The same round trip with a copy engine in place of
+        # the mirror (a 16-byte device-to-host copy queued after the write)
+        # is timed beside it, on an unattached queue pair.
+        gens = [db.cq_detach(slots, i) for i in range(nq)]
+        if not all(db.cq_wait_ack(slots, i, g, 5.0) for i, g in enumerate(gens)):
+            raise RuntimeError("cq_mirror: no acknowledgement")
+        d, h, d2, h2 = devs[0], hosts[0], devs[1], hosts[1]
+        with t.cuda.stream(copy_s):
+            d.zero_()
+            d2.zero_()
+        h.zero_()
+        h2.zero_()
+        copy_s.synchronize()
+        db.cq_attach(slots, 0, d, h)
+        ov, nv = one_old.numpy().view(np.uint32), one_new.numpy().view(np.uint32)
+        rts = {"mirror": [], "copy_engine": []}
+        for i in range(4000):
+            leg = "mirror" if i % 2 == 0 else "copy_engine"
+            j = i // 2
+            pos, tag = j % depth, np.uint32(1 - (j // depth) % 2)
+            dq, hq = (d, h) if leg == "mirror" else (d2, h2)
+            hv = hq.numpy().view(np.uint32)
+            e = rng.integers(0, 2**32, size=4, dtype=np.uint64).astype(np.uint32)
+            e[3] = (e[3] & ~PHASE) | (tag << np.uint32(16))
+            nv[pos] = e
+            ov[pos] = e
+            ov[pos, 3] ^= PHASE
+            want = tag << np.uint32(16)
+            ta = time.perf_counter()
+            with t.cuda.stream(copy_s):
+                dq[pos:pos + 1].copy_(one_old[pos:pos + 1], non_blocking=True)
+                dq[pos:pos + 1].copy_(one_new[pos:pos + 1], non_blocking=True)
+                if leg == "copy_engine":
+                    hq[pos:pos + 1].copy_(dq[pos:pos + 1], non_blocking=True)
+            while (hv[pos, 3] & PHASE) != want and time.perf_counter() - ta < 1.0:
+                pass
+            tc = time.perf_counter()
+            copy_s.synchronize()
+            got, _, _ = db.cq_host_reap(hq, pos, int(tag), max_entries=1)
+            if got.shape[0] != 1 or not (got[0] == e).all():
+                raise RuntimeError(f"cq_mirror: QD1 entry differs ({leg})")
+            total += leg == "mirror"
+            rts[leg].append(tc - ta)
+        g = db.cq_detach(slots, 0)
+        db.cq_wait_ack(slots, 0, g, 5.0)
+    finally:
+        db.cq_request_stop(stop)
+        mir_s.synchronize()
+    c = ctr.cpu().numpy()
+    if int(c[0]) != total or int(c[3]):
+        raise RuntimeError(f"cq_mirror: counters {c.tolist()}, expected {total} copied")
+    rate = statistics.mean(rates)
+    return {"drain_M_cqe_per_s": round(rate / 1e6, 3), "queues": nq, "depth": depth,
+            "cqes_per_round": nq * k,
+            "ns_per_cqe_per_queue": round(nq / rate * 1e9, 1),
+            "qd1_roundtrip_us_median": round(statistics.median(rts["mirror"]) * 1e6, 2),
+            "qd1_roundtrip_us_copy_engine_median":
+                round(statistics.median(rts["copy_engine"]) * 1e6, 2),
+            "launches": 1, "bound": "latency: device CQ to host CQ over the CPU-GPU link",
+            "note": "not part of the step: the host writes the device CQs (two stream-ordered "
+                    "copies per batch) and polls host memory; times are host wall clock, "
+                    "round trips include the host's copy issue and polling"}
 
 
 def time_mr_overlap(args, device, stream) -> dict:

@@ -21,6 +21,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -29,7 +30,8 @@ __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
     "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
-    "strerror",
+    "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "cq_slots", "cq_slot_fields",
+    "cq_mirror", "cq_attach", "cq_detach", "cq_wait_ack", "cq_host_reap", "cq_request_stop",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
 ]
@@ -75,6 +77,17 @@ def _load():
                  "db_mr_workspace_size",
                  "db_mr_lookup", "db_mr_lookup_overlap", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
                  "db_last_cuda_error"):
+        getattr(lib, name).restype = i32
+    lib.db_cq_mirror.argtypes = [vp, u32, vp, u64, vp, vp]
+    lib.db_cq_attach.argtypes = [vp, u64, u64, u32, ctypes.POINTER(ctypes.c_uint32)]
+    lib.db_cq_detach.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.db_cq_wait_ack.argtypes = [vp, u32, u64]
+    lib.db_cq_host_reap.argtypes = [vp, u32, ctypes.POINTER(ctypes.c_uint32),
+                                    ctypes.POINTER(ctypes.c_uint32), vp, u32]
+    lib.db_cq_request_stop.argtypes = [vp]
+    lib.db_cq_request_stop.restype = None
+    for name in ("db_cq_mirror", "db_cq_attach", "db_cq_detach", "db_cq_wait_ack",
+                 "db_cq_host_reap"):
         getattr(lib, name).restype = i32
     lib.db_strerror.argtypes = [i32]
     lib.db_strerror.restype = ctypes.c_char_p
@@ -223,3 +236,80 @@ def wqe_bucket_vmm(req: torch.Tensor, chunk_raddr: torch.Tensor, chunk_rkey: tor
         _ptr(req), n, _ptr(chunk_raddr), _ptr(chunk_rkey), _ptr(chunk_lkey), chunk_shift, world,
         n_qp, local_base, heap_size, _ptr(rings), depth, _ptr(head), _ptr(count), mtu,
         _ptr(psn_head), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ CQ mirror
+CQ_MAX_SLOTS, CQ_MAX_DEPTH = 64, 65536
+# db_cq_slot, 64 bytes
+CQ_SLOT_DTYPE = np.dtype([("dev_cq", "<u8"), ("host_cq", "<u8"), ("depth", "<u4"),
+                          ("generation", "<u4"), ("ack", "<u4"), ("seen", "<u4"),
+                          ("head", "<u4"), ("phase", "<u4"), ("copied", "<u8"),
+                          ("rsvd", "<u8", (2,))])
+assert CQ_SLOT_DTYPE.itemsize == 64
+
+
+def _host(t: torch.Tensor) -> int:
+    if t.device.type != "cpu" or not t.is_contiguous():
+        raise ValueError("expected a contiguous host tensor")
+    return t.data_ptr()
+
+
+def cq_slots(n: int) -> torch.Tensor:
+    """A zero-filled slot table of n slots in pinned host memory."""
+    return torch.zeros((n, 64), dtype=torch.uint8).pin_memory()
+
+
+def cq_slot_fields(slots: torch.Tensor) -> np.ndarray:
+    """A live structured view of a slot table (reads see the kernel's writes)."""
+    return slots.numpy().view(CQ_SLOT_DTYPE).reshape(-1)
+
+
+def cq_mirror(slots: torch.Tensor, stop: torch.Tensor, limit_s: float,
+              ctr: torch.Tensor | None = None, stream=None, n_slots: int | None = None) -> None:
+    """db_cq_mirror: launch the bounded resident mirror over the slots."""
+    n = slots.shape[0] if n_slots is None else n_slots
+    _check("db_cq_mirror", _lib.db_cq_mirror(_host(slots), n, _host(stop),
+                                             int(limit_s * 1e9), _ptr(ctr), _stream(stream)))
+
+
+def cq_attach(slots: torch.Tensor, i: int, dev_cq: torch.Tensor, host_cq: torch.Tensor) -> int:
+    """db_cq_attach: serve the device CQ dev_cq ([depth, 4] int32, device)
+    into host_cq ([depth, 4] int32, pinned); returns the odd generation."""
+    depth = _records(dev_cq, 16)
+    if _records(host_cq, 16) != depth:
+        raise ValueError("device and host CQ differ in depth")
+    g = ctypes.c_uint32(0)
+    _check("db_cq_attach", _lib.db_cq_attach(_host(slots) + 64 * i, _ptr(dev_cq),
+                                             _host(host_cq), depth, ctypes.byref(g)))
+    return g.value
+
+
+def cq_detach(slots: torch.Tensor, i: int) -> int:
+    """db_cq_detach: returns the odd generation whose acknowledgement to wait for."""
+    g = ctypes.c_uint32(0)
+    _check("db_cq_detach", _lib.db_cq_detach(_host(slots) + 64 * i, ctypes.byref(g)))
+    return g.value
+
+
+def cq_wait_ack(slots: torch.Tensor, i: int, generation: int, timeout_s: float) -> bool:
+    rc = _lib.db_cq_wait_ack(_host(slots) + 64 * i, generation, int(timeout_s * 1e9))
+    if rc not in (0, -110):
+        _check("db_cq_wait_ack", rc)
+    return rc == 0
+
+
+def cq_host_reap(host_cq: torch.Tensor, head: int, phase: int, max_entries: int | None = None):
+    """db_cq_host_reap: returns (entries [n, 4] uint32, head, phase)."""
+    depth = _records(host_cq, 16)
+    m = depth if max_entries is None else max_entries
+    out = np.zeros((max(m, 1), 4), dtype=np.uint32)
+    h, ph = ctypes.c_uint32(head), ctypes.c_uint32(phase)
+    n = _lib.db_cq_host_reap(_host(host_cq), depth, ctypes.byref(h), ctypes.byref(ph),
+                             out.ctypes.data, m)
+    if n < 0:
+        _check("db_cq_host_reap", n)
+    return out[:n], h.value, ph.value
+
+
+def cq_request_stop(stop: torch.Tensor) -> None:
+    _lib.db_cq_request_stop(_host(stop))

@@ -48,6 +48,12 @@ extern "C" const char* db_strerror(int code) {
       return "CUDA launch failed (see db_last_cuda_error)";
     case -E2BIG:
       return "batch larger than the built-in workspace allows (DB_PRP_STATIC_MAX_REQUESTS)";
+    case -EBUSY:
+      return "slot busy (attached, or its previous generation not yet acknowledged)";
+    case -ETIMEDOUT:
+      return "timed out";
+    case -ENODEV:
+      return "no CUDA device, or memory of the wrong kind (pinned host or device memory expected)";
     default:
       return "unknown error";
   }
