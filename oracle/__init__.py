@@ -66,6 +66,15 @@ def _load():
             lib.oracle_wqe_bucket_vmm.restype = None
             lib.oracle_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64,
                                                   vp, u64, vp, u32, vp, vp, vp]
+            lib.oracle_mr_register.restype = None
+            lib.oracle_mr_register.argtypes = [vp, u64, vp, u32, vp, vp, vp, vp, u64, vp, vp, vp,
+                                               vp, u64, vp, vp, vp, vp]
+            lib.oracle_mr_register_seq.restype = None
+            lib.oracle_mr_register_seq.argtypes = [vp, u64, vp, u32, vp, vp, vp, vp, u64, vp, vp,
+                                                   vp, vp, vp, vp, vp, vp]
+            lib.oracle_mr_deregister.restype = None
+            lib.oracle_mr_deregister.argtypes = [vp, u64, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp,
+                                                 vp, vp]
             lib.oracle_cq_mirror_pass.restype = u32
             lib.oracle_cq_mirror_pass.argtypes = [vp, u32, vp, vp, vp, u32]
             lib.oracle_cq_ack.restype = u32
@@ -170,6 +179,66 @@ def mr_prefix_max(queries, start, end, lkey) -> dict:
 def mr_bsearch(queries, start, end, lkey) -> dict:
     """Same result for sorted non-overlapping tables, by binary search."""
     return _mr("oracle_mr_bsearch", queries, start, end, lkey)
+
+
+MR_HIT_EXACT, MR_HIT_CONTAINED, MR_NEW, MR_NEW_DUP = 1, 2, 4, 5
+DEREG_OK, DEREG_RELEASED, DEREG_STALE = 0, 1, 2
+
+
+def _table(start, end, lkey, refs):
+    return (_u64(start), _u64(end), np.ascontiguousarray(lkey, dtype=np.uint32),
+            np.ascontiguousarray(refs, dtype=np.uint32))
+
+
+def mr_register(queries, new_lkey, start, end, lkey, refs, granule_shift: int = 12,
+                out_cap: int | None = None, one_at_a_time: bool = False) -> dict:
+    """A batch of registrations against a table sorted by start (records may
+    overlap). Returns the table after the batch (start, end, lkey, refs,
+    trimmed to its size), handle / kind per request, remap per old record and
+    ctr [records after, invalid, overflow, error bits]. With one_at_a_time,
+    the pages' per-call definition instead of the batch reading."""
+    q = _u64(queries).reshape(-1, 2)
+    start, end, lkey, refs = _table(start, end, lkey, refs)
+    new_lkey = np.ascontiguousarray(new_lkey, dtype=np.uint32)
+    n_q, n = q.shape[0], start.shape[0]
+    cap = n + n_q if out_cap is None else out_cap
+    o = dict(start=np.zeros(max(cap, 1), np.uint64), end=np.zeros(max(cap, 1), np.uint64),
+             lkey=np.zeros(max(cap, 1), np.uint32), refs=np.zeros(max(cap, 1), np.uint32))
+    handle = np.full(max(n_q, 1), -1, dtype=np.int64)
+    kind = np.zeros(max(n_q, 1), dtype=np.uint8)
+    remap = np.full(max(n, 1), -1, dtype=np.int64)
+    ctr = np.zeros(4, dtype=np.uint64)
+    if one_at_a_time:
+        _load().oracle_mr_register_seq(_p(q), n_q, _p(new_lkey), granule_shift, _p(start),
+                                       _p(end), _p(lkey), _p(refs), n, _p(o["start"]),
+                                       _p(o["end"]), _p(o["lkey"]), _p(o["refs"]), _p(handle),
+                                       _p(kind), _p(remap), _p(ctr))
+    else:
+        _load().oracle_mr_register(_p(q), n_q, _p(new_lkey), granule_shift, _p(start), _p(end),
+                                   _p(lkey), _p(refs), n, _p(o["start"]), _p(o["end"]),
+                                   _p(o["lkey"]), _p(o["refs"]), cap, _p(handle), _p(kind),
+                                   _p(remap), _p(ctr))
+    m = int(ctr[0]) if int(ctr[2]) == 0 else 0
+    return dict(start=o["start"][:m], end=o["end"][:m], lkey=o["lkey"][:m], refs=o["refs"][:m],
+                handle=handle[:n_q], kind=kind[:n_q], remap=remap[:n], ctr=ctr)
+
+
+def mr_deregister(handles, start, end, lkey, refs) -> dict:
+    """A batch of deregistrations (record indices), applied in batch order."""
+    h = np.ascontiguousarray(handles, dtype=np.int64)
+    start, end, lkey, refs = _table(start, end, lkey, refs)
+    n = start.shape[0]
+    o = dict(start=np.zeros(max(n, 1), np.uint64), end=np.zeros(max(n, 1), np.uint64),
+             lkey=np.zeros(max(n, 1), np.uint32), refs=np.zeros(max(n, 1), np.uint32))
+    remap = np.full(max(n, 1), -1, dtype=np.int64)
+    status = np.zeros(max(h.shape[0], 1), dtype=np.uint8)
+    ctr = np.zeros(4, dtype=np.uint64)
+    _load().oracle_mr_deregister(_p(h), h.shape[0], _p(start), _p(end), _p(lkey), _p(refs), n,
+                                 _p(o["start"]), _p(o["end"]), _p(o["lkey"]), _p(o["refs"]),
+                                 _p(remap), _p(status), _p(ctr))
+    m = int(ctr[0])
+    return dict(start=o["start"][:m], end=o["end"][:m], lkey=o["lkey"][:m], refs=o["refs"][:m],
+                remap=remap[:n], status=status[:h.shape[0]], ctr=ctr)
 
 
 # ----------------------------------------------------------------------- WQE

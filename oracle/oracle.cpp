@@ -24,6 +24,14 @@
 //    branch (one WQE per chunk: min of the source and destination chunk
 //    remainders and the bytes left) and the warp-level WQE slot reservation
 //    (a post index per send queue).
+//  * MR cache mutation -- the same NCCL page: a hit takes one more
+//    reference, a miss is registered anew and inserted in address order,
+//    deregistration drops a reference and removes the MR at zero, a handle
+//    not in the cache is an error (the ncclCommRegister experiment: the same
+//    range twice and a range inside it share one record, refs 3; three
+//    deregistrations delete it; then a stale handle is invalid usage); and
+//    the xNVMe "uPCIe CUDA" page: xnvme_buf_register refcounts whole 64 KiB
+//    device pages.
 //  * CQ mirror -- xNVMe "uPCIe CUDA" backend page, "Completions in device
 //    memory": a resident kernel watches each device-memory completion queue
 //    with one warp and copies completions into the host CQ as their phase
@@ -41,6 +49,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <utility>
 #include <vector>
 
 namespace {
@@ -542,6 +552,224 @@ void oracle_wqe_bucket_vmm(const uint64_t* req, uint64_t n, const uint64_t* chun
   ctr[1] = n_invalid;
   ctr[2] = n_overflow;
   ctr[3] = err;
+}
+
+// ---------------------------------------------------------- MR cache mutation
+// Readings (a batch form of the pages' one-call-at-a-time operations):
+//  * Registration batch. Every request is rounded to whole granules (4 KiB,
+//    or 64 KiB for the xNVMe registry) and looked up in the table as it
+//    stood before the batch: a hit takes one more reference on the
+//    lowest-index record holding it. The requests that missed become one
+//    new record per distinct rounded range, with as many references as
+//    requests for it and the new_lkey of its first request. A new record
+//    goes after every old record with the same start; new records among
+//    themselves are in (start, end) order. This is one-at-a-time
+//    registration whenever no new range of the batch lies inside another
+//    one (then the later one would have been a hit).
+//  * Handles are record indices; remap[i] is old record i's index after the
+//    batch (-1 once removed). A handle of a request is its record's index in
+//    the table after the batch.
+//  * Deregistration batch: in batch order, each handle takes one reference
+//    off its record; the one that takes the last reference releases it; a
+//    handle naming no record, or a record already released, is stale. The
+//    records whose references reach 0 are removed.
+// Kinds: 1 hit (same range), 2 hit (contained), 3 invalid, 4 new record,
+// 5 same range as a new record of this batch. Deregistration status: 0 a
+// reference dropped, 1 released, 2 stale.
+
+// [base, aend): the range widened to whole granules of g bytes; false for an
+// empty range or one whose widened end would not fit in 64 bits.
+static bool round_to_granule(uint64_t addr, uint64_t size, uint64_t g, uint64_t* base,
+                             uint64_t* aend) {
+  if (size == 0) return false;
+  const u128 stop = (u128)addr + (u128)size;
+  if (stop > (u128)(UINT64_MAX - g + 1)) return false;
+  const uint64_t b = addr - addr % g;
+  const uint64_t units = (uint64_t)((stop - b + g - 1) / g);
+  *base = b;
+  *aend = b + units * g;
+  return true;
+}
+
+// Lowest index i with start[i] <= base and aend <= end[i] in a table sorted
+// by start, or -1: records after the last start <= base start too late, and
+// among the others the first whose prefix maximum of ends reaches aend.
+static int64_t lowest_holder(const uint64_t* start, const std::vector<uint64_t>& pm, uint64_t n,
+                             uint64_t base, uint64_t aend) {
+  const uint64_t cnt = (uint64_t)(std::upper_bound(start, start + n, base) - start);
+  const uint64_t i = (uint64_t)(std::lower_bound(pm.begin(), pm.begin() + cnt, aend) - pm.begin());
+  return i < cnt ? (int64_t)i : -1;
+}
+
+void oracle_mr_register(const uint64_t* q, uint64_t n_q, const uint32_t* new_lkey,
+                        uint32_t granule_shift, const uint64_t* start, const uint64_t* end,
+                        const uint32_t* lkey, const uint32_t* refs, uint64_t n,
+                        uint64_t* o_start, uint64_t* o_end, uint32_t* o_lkey, uint32_t* o_refs,
+                        uint64_t o_cap, int64_t* handle, uint8_t* kind, int64_t* remap,
+                        uint64_t* ctr) {
+  const uint64_t g = 1ull << granule_shift;
+  uint64_t err = 0;
+  for (uint64_t i = 0; i < n; ++i)
+    if (!(start[i] < end[i]) || (i > 0 && start[i - 1] > start[i])) err = 4;
+  std::vector<uint64_t> pm(n);
+  for (uint64_t i = 0; i < n; ++i) pm[i] = i ? std::max(pm[i - 1], end[i]) : end[i];
+  // 1. look every request up in the table as it stood before the batch
+  std::vector<uint64_t> more(n, 0);                 // references each old record gains
+  std::vector<int64_t> holder(n_q, -1);
+  std::vector<std::pair<uint64_t, uint64_t>> range(n_q);
+  std::map<std::pair<uint64_t, uint64_t>, std::pair<uint64_t, uint64_t>> fresh;  // -> (first, count)
+  uint64_t n_invalid = 0;
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t b, e;
+    if (!round_to_granule(q[2 * k], q[2 * k + 1], g, &b, &e)) {
+      kind[k] = 3;
+      n_invalid += 1;
+      continue;
+    }
+    range[k] = {b, e};
+    const int64_t i = lowest_holder(start, pm, n, b, e);
+    if (i >= 0) {
+      holder[k] = i;
+      more[i] += 1;
+      kind[k] = (start[i] == b && end[i] == e) ? 1 : 2;
+    } else {
+      auto it = fresh.find({b, e});
+      if (it == fresh.end()) {
+        fresh[{b, e}] = {k, 1};
+        kind[k] = 4;
+      } else {
+        it->second.second += 1;
+        kind[k] = 5;
+      }
+    }
+  }
+  const uint64_t n_out = n + fresh.size();
+  ctr[0] = n_out;
+  ctr[1] = n_invalid;
+  ctr[2] = n_out > o_cap ? 1 : 0;
+  ctr[3] = err;
+  if (n_out > o_cap) return;  // nothing else is written
+  // 2. merge: an old record goes before new records with the same start
+  std::map<std::pair<uint64_t, uint64_t>, uint64_t> placed;  // new range -> index after the batch
+  auto nit = fresh.begin();
+  uint64_t i = 0, w = 0;
+  while (i < n || nit != fresh.end()) {
+    const bool take_old = i < n && (nit == fresh.end() || start[i] <= nit->first.first);
+    if (take_old) {
+      o_start[w] = start[i];
+      o_end[w] = end[i];
+      o_lkey[w] = lkey[i];
+      o_refs[w] = (uint32_t)(refs[i] + more[i]);
+      remap[i] = (int64_t)w;
+      ++i;
+    } else {
+      o_start[w] = nit->first.first;
+      o_end[w] = nit->first.second;
+      o_lkey[w] = new_lkey[nit->second.first];
+      o_refs[w] = (uint32_t)nit->second.second;
+      placed[nit->first] = w;
+      ++nit;
+    }
+    ++w;
+  }
+  // 3. handles
+  for (uint64_t k = 0; k < n_q; ++k) {
+    if (kind[k] == 3) handle[k] = -1;
+    else if (kind[k] <= 2) handle[k] = remap[holder[k]];
+    else handle[k] = (int64_t)placed[range[k]];
+  }
+}
+
+// One registration at a time, as the pages describe it: look the range up
+// in the table as it is now (lowest index holding it); a hit takes a
+// reference, a miss inserts a record after every record starting at or
+// before it. Kind 5 marks a hit on a record this batch created. Handles and
+// remap are indices in the final table.
+void oracle_mr_register_seq(const uint64_t* q, uint64_t n_q, const uint32_t* new_lkey,
+                            uint32_t granule_shift, const uint64_t* start, const uint64_t* end,
+                            const uint32_t* lkey, const uint32_t* refs, uint64_t n,
+                            uint64_t* o_start, uint64_t* o_end, uint32_t* o_lkey,
+                            uint32_t* o_refs, int64_t* handle, uint8_t* kind, int64_t* remap,
+                            uint64_t* ctr) {
+  struct Rec { uint64_t s, e; uint32_t lk, refs; int64_t id; };  // id: old index, or -1 - request
+  const uint64_t g = 1ull << granule_shift;
+  std::vector<Rec> t;
+  for (uint64_t i = 0; i < n; ++i) t.push_back({start[i], end[i], lkey[i], refs[i], (int64_t)i});
+  std::vector<int64_t> got(n_q, 0);  // record id each request ends up on
+  uint64_t n_invalid = 0;
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t b, e;
+    if (!round_to_granule(q[2 * k], q[2 * k + 1], g, &b, &e)) {
+      kind[k] = 3;
+      n_invalid += 1;
+      continue;
+    }
+    bool hit = false;
+    for (auto& r : t) {
+      if (r.s <= b && e <= r.e) {
+        r.refs += 1;
+        got[k] = r.id;
+        kind[k] = r.id >= 0 ? ((r.s == b && r.e == e) ? 1 : 2) : 5;
+        hit = true;
+        break;
+      }
+    }
+    if (hit) continue;
+    size_t at = 0;
+    while (at < t.size() && t[at].s <= b) ++at;
+    t.insert(t.begin() + at, Rec{b, e, new_lkey[k], 1, -1 - (int64_t)k});
+    got[k] = -1 - (int64_t)k;
+    kind[k] = 4;
+  }
+  std::map<int64_t, int64_t> final_index;
+  for (size_t w = 0; w < t.size(); ++w) {
+    o_start[w] = t[w].s;
+    o_end[w] = t[w].e;
+    o_lkey[w] = t[w].lk;
+    o_refs[w] = t[w].refs;
+    final_index[t[w].id] = (int64_t)w;
+  }
+  for (uint64_t i = 0; i < n; ++i) remap[i] = final_index[(int64_t)i];
+  for (uint64_t k = 0; k < n_q; ++k) handle[k] = kind[k] == 3 ? -1 : final_index[got[k]];
+  ctr[0] = t.size();
+  ctr[1] = n_invalid;
+  ctr[2] = 0;
+  ctr[3] = 0;
+}
+
+void oracle_mr_deregister(const int64_t* h, uint64_t n_h, const uint64_t* start,
+                          const uint64_t* end, const uint32_t* lkey, const uint32_t* refs,
+                          uint64_t n, uint64_t* o_start, uint64_t* o_end, uint32_t* o_lkey,
+                          uint32_t* o_refs, int64_t* remap, uint8_t* status, uint64_t* ctr) {
+  std::vector<uint64_t> left(refs, refs + n);
+  uint64_t n_stale = 0;
+  for (uint64_t k = 0; k < n_h; ++k) {
+    const int64_t i = h[k];
+    if (i < 0 || (uint64_t)i >= n || left[i] == 0) {
+      status[k] = 2;
+      n_stale += 1;
+      continue;
+    }
+    left[i] -= 1;
+    status[k] = left[i] == 0 ? 1 : 0;
+  }
+  uint64_t w = 0;
+  for (uint64_t i = 0; i < n; ++i) {
+    if (left[i] == 0) {
+      remap[i] = -1;
+      continue;
+    }
+    o_start[w] = start[i];
+    o_end[w] = end[i];
+    o_lkey[w] = lkey[i];
+    o_refs[w] = (uint32_t)left[i];
+    remap[i] = (int64_t)w;
+    ++w;
+  }
+  ctr[0] = w;
+  ctr[1] = n_stale;
+  ctr[2] = 0;
+  ctr[3] = 0;
 }
 
 // ---------------------------------------------------------------- CQ mirror

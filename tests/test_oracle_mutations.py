@@ -77,6 +77,22 @@ MUTANTS = [
     ("psn taken after its own WQE",
      "put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));  // first PSN\n        psn_taken[r] += (t + mtu - 1) / mtu;",
      "psn_taken[r] += (t + mtu - 1) / mtu;\n        put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));"),
+    ("register: a hit takes no reference", "more[i] += 1;", "more[i] += 0;"),
+    ("register: new record before an old one with the same start",
+     "start[i] <= nit->first.first);", "start[i] < nit->first.first);"),
+    ("register: new record keyed by the wrong request",
+     "o_lkey[w] = new_lkey[nit->second.first];",
+     "o_lkey[w] = new_lkey[nit->second.first + nit->second.second - 1];"),
+    ("register: granule rounding drops the tail",
+     "const uint64_t units = (uint64_t)((stop - b + g - 1) / g);",
+     "const uint64_t units = (uint64_t)((stop - b) / g);"),
+    ("register: repeats are not merged", "if (it == fresh.end()) {", "if (true) {"),
+    ("register one at a time: insert before equal starts",
+     "while (at < t.size() && t[at].s <= b) ++at;", "while (at < t.size() && t[at].s < b) ++at;"),
+    ("deregister: released one reference early",
+     "status[k] = left[i] == 0 ? 1 : 0;", "status[k] = left[i] <= 1 ? 1 : 0;"),
+    ("deregister: a released record takes more",
+     "if (i < 0 || (uint64_t)i >= n || left[i] == 0) {", "if (i < 0 || (uint64_t)i >= n) {"),
     ("cq phase tag read from bit 15",
      "const uint32_t tag = (entry[3] >> 16) & 1u;", "const uint32_t tag = (entry[3] >> 15) & 1u;"),
     ("cq phase kept across the wrap",
@@ -105,7 +121,7 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     env = dict(os.environ, DB_ORACLE_LIB=str(lib))
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
-              "test_oracle_vmm.py", "test_oracle_cq.py")]
+              "test_oracle_vmm.py", "test_oracle_cq.py", "test_oracle_mr_cache.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
