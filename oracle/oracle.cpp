@@ -596,9 +596,10 @@ static bool round_to_granule(uint64_t addr, uint64_t size, uint64_t g, uint64_t*
 // among the others the first whose prefix maximum of ends reaches aend.
 static int64_t lowest_holder(const uint64_t* start, const std::vector<uint64_t>& pm, uint64_t n,
                              uint64_t base, uint64_t aend) {
-  const uint64_t cnt = (uint64_t)(std::upper_bound(start, start + n, base) - start);
-  const uint64_t i = (uint64_t)(std::lower_bound(pm.begin(), pm.begin() + cnt, aend) - pm.begin());
-  return i < cnt ? (int64_t)i : -1;
+  const uint64_t starting = (uint64_t)(std::upper_bound(start, start + n, base) - start);
+  const auto first_reach = std::lower_bound(pm.begin(), pm.begin() + (ptrdiff_t)starting, aend);
+  const uint64_t i = (uint64_t)(first_reach - pm.begin());
+  return i < starting ? (int64_t)i : -1;
 }
 
 void oracle_mr_register(const uint64_t* q, uint64_t n_q, const uint32_t* new_lkey,
@@ -611,8 +612,12 @@ void oracle_mr_register(const uint64_t* q, uint64_t n_q, const uint32_t* new_lke
   uint64_t err = 0;
   for (uint64_t i = 0; i < n; ++i)
     if (!(start[i] < end[i]) || (i > 0 && start[i - 1] > start[i])) err = 4;
-  std::vector<uint64_t> pm(n);
-  for (uint64_t i = 0; i < n; ++i) pm[i] = i ? std::max(pm[i - 1], end[i]) : end[i];
+  std::vector<uint64_t> pm(n);  // prefix maximum of the ends
+  uint64_t reach = 0;
+  for (uint64_t i = 0; i < n; ++i) {
+    reach = std::max(reach, end[i]);
+    pm[i] = reach;
+  }
   // 1. look every request up in the table as it stood before the batch
   std::vector<uint64_t> more(n, 0);                 // references each old record gains
   std::vector<int64_t> holder(n_q, -1);

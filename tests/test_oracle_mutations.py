@@ -77,6 +77,11 @@ MUTANTS = [
     ("psn taken after its own WQE",
      "put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));  // first PSN\n        psn_taken[r] += (t + mtu - 1) / mtu;",
      "psn_taken[r] += (t + mtu - 1) / mtu;\n        put_u32(wqe + 44, (uint32_t)(psn_head[r] + psn_taken[r]));"),
+    ("register: holder must start below the base, not at it",
+     "const uint64_t starting = (uint64_t)(std::upper_bound(start, start + n, base) - start);",
+     "const uint64_t starting = (uint64_t)(std::lower_bound(start, start + n, base) - start);"),
+    ("register: prefix maximum of the ends restarts", "reach = std::max(reach, end[i]);",
+     "reach = end[i];"),
     ("register: a hit takes no reference", "more[i] += 1;", "more[i] += 0;"),
     ("register: new record before an old one with the same start",
      "start[i] <= nit->first.first);", "start[i] < nit->first.first);"),
