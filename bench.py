@@ -16,7 +16,8 @@ pinned host memory and every descriptor copied back to the host. ``next``
 times, on its own and outside the step, the rows built after the hot path:
 the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm, without and
 with packet sequence numbers), the MR lookup on a table whose records
-overlap (db_mr_lookup_overlap) and the completion-queue mirror
+overlap (db_mr_lookup_overlap), the registration-cache batches
+(db_mr_register, db_mr_deregister) and the completion-queue mirror
 (db_cq_mirror: drain rate over 64 queues, latency at queue depth 1).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -59,6 +60,8 @@ def parse():
                     help="profiling aid: run one workload only (not a bench line)")
     ap.add_argument("--fraction", type=float, default=1.0,
                     help="profiling aid: keep this leading fraction of each batch")
+    ap.add_argument("--next-only", choices=["mr_register", "mr_deregister"],
+                    help="profiling aid: time one of the rows after the hot path, alone")
     return ap.parse_args()
 
 
@@ -304,7 +307,9 @@ def run_next(args, device) -> dict:
     """The rows after the hot path, timed on their own (not part of a step):
     the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm), without and
     with packet sequence numbers (mtu 4096), the MR lookup on a table whose
-    records overlap (db_mr_lookup_overlap) and the CQ mirror (db_cq_mirror)."""
+    records overlap (db_mr_lookup_overlap), the registration and
+    deregistration batches (db_mr_register, db_mr_deregister) and the CQ
+    mirror (db_cq_mirror)."""
     import torch as t
     import descriptor_build_gb300 as db
     import synth
@@ -353,8 +358,109 @@ def run_next(args, device) -> dict:
             "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
             "note": "not part of the step: timed alone, same stream discipline"}
     out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
+    out.update(time_mr_mutation(args, device, stream))
     out["cq_mirror"] = time_cq_mirror(args, device)
     return out
+
+
+def _event_ms(t, stream, call, warmup, steps) -> float:
+    for _ in range(warmup):
+        call()
+    t.cuda.synchronize()
+    evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, z in evs:
+        a.record(stream)
+        call()
+        z.record(stream)
+    t.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(z) for a, z in evs)
+
+
+def time_mr_mutation(args, device, stream, only=None) -> dict:
+    """db_mr_register on the mr_lookup table and queries taken as a
+    registration batch (16,777,216 requests, 1,048,576 records, a fifth of
+    the requests missing), and db_mr_deregister of 2,097,152 handles.
+    Algorithmic bytes: per request 16 B range + 4 B new lkey in, 8 B handle
+    + 1 B kind out; per record 24 B in and 24 B + 8 B remap out (registration
+    also writes 24 B per new record); per handle 8 B in, 1 B out."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    import synth
+    d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+    d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+    peak, _ = peak_gbs()
+    out = {}
+    if only == "mr_deregister":
+        return _time_dereg(args, device, stream, db, synth, t, d64, d32, peak)
+    r = synth.mr_register()
+    nq, n = r["queries"].shape[0], r["mr_start"].shape[0]
+    cap = n + nq
+    rb = dict(q=d64(r["queries"]), nl=d32(r["new_lkey"]), s=d64(r["mr_start"]),
+              e=d64(r["mr_end"]), lk=d32(r["mr_lkey"]), refs=d32(r["mr_refs"]),
+              os=t.empty(cap, dtype=t.int64, device=device),
+              oe=t.empty(cap, dtype=t.int64, device=device),
+              olk=t.empty(cap, dtype=t.int32, device=device),
+              orefs=t.empty(cap, dtype=t.int32, device=device),
+              h=t.empty(nq, dtype=t.int64, device=device),
+              k=t.empty(nq, dtype=t.uint8, device=device),
+              remap=t.empty(n, dtype=t.int64, device=device),
+              ctr=t.zeros(4, dtype=t.int64, device=device),
+              ws=db.workspace(db.mr_register_workspace_size(nq, n), device))
+    del r
+
+    def reg():
+        db.mr_register(rb["q"], rb["nl"], rb["s"], rb["e"], rb["lk"], rb["refs"], rb["os"],
+                       rb["oe"], rb["olk"], rb["orefs"], rb["h"], rb["k"], rb["remap"], rb["ws"],
+                       ctr=rb["ctr"], stream=stream)
+
+    ms = _event_ms(t, stream, reg, args.warmup, args.steps)
+    c = rb["ctr"].cpu().tolist()
+    if c[2] or c[3]:
+        raise RuntimeError(f"mr_register: counters {c}")
+    u = c[0] - n
+    alg = 29 * nq + 56 * n + 24 * u
+    gbs = alg / (ms * 1e-3) / 1e9
+    out["mr_register"] = {"ms": round(ms, 4), "M_req_per_s": round(nq / ms / 1e3, 2),
+                          "records_before": n, "new_records": u, "algorithmic_bytes": alg,
+                          "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                          "note": "not part of the step: timed alone; lookup + 14 radix passes "
+                                  "+ merge, about 70 launches"}
+    del rb
+    if only == "mr_register":
+        return out
+    return {**out, **_time_dereg(args, device, stream, db, synth, t, d64, d32, peak)}
+
+
+def _time_dereg(args, device, stream, db, synth, t, d64, d32, peak) -> dict:
+    g = synth.mr_deregister()
+    nh, n = g["handles"].shape[0], g["mr_start"].shape[0]
+    db_ = dict(hd=t.from_numpy(g["handles"]).to(device), s=d64(g["mr_start"]),
+               e=d64(g["mr_end"]), lk=d32(g["mr_lkey"]), refs=d32(g["mr_refs"]),
+               os=t.empty(n, dtype=t.int64, device=device),
+               oe=t.empty(n, dtype=t.int64, device=device),
+               olk=t.empty(n, dtype=t.int32, device=device),
+               orefs=t.empty(n, dtype=t.int32, device=device),
+               remap=t.empty(n, dtype=t.int64, device=device),
+               st=t.empty(nh, dtype=t.uint8, device=device),
+               ctr=t.zeros(4, dtype=t.int64, device=device),
+               ws=db.workspace(db.mr_deregister_workspace_size(nh, n), device))
+
+    def dereg():
+        db.mr_deregister(db_["hd"], db_["s"], db_["e"], db_["lk"], db_["refs"], db_["os"],
+                         db_["oe"], db_["olk"], db_["orefs"], db_["remap"], db_["st"], db_["ws"],
+                         ctr=db_["ctr"], stream=stream)
+
+    ms = _event_ms(t, stream, dereg, args.warmup, args.steps)
+    c = db_["ctr"].cpu().tolist()
+    alg = 9 * nh + 56 * n
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"mr_deregister": {"ms": round(ms, 4), "M_handles_per_s": round(nh / ms / 1e3, 2),
+                            "records_before": n, "records_after": c[0], "stale": c[1],
+                            "algorithmic_bytes": alg, "GB_per_s": round(gbs, 1),
+                            "frac_of_peak": round(gbs / peak, 4),
+                            "note": "not part of the step: timed alone; 3 radix passes + "
+                                    "runs + compaction"}}
 
 
 def time_cq_mirror(args, device) -> dict:
@@ -745,6 +851,14 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(device)
         dist.init_process_group("nccl", device_id=device)
+    if args.next_only:
+        if rank == 0:
+            import torch as t
+            res = time_mr_mutation(args, device, t.cuda.Stream(device=device),
+                                   only=args.next_only)
+            print(json.dumps({"next_only": args.next_only, **res,
+                              "note": "profiling aid: not a bench line"}), flush=True)
+        return
     inp = make_inputs(args.only, args.fraction)
     out = run_ours(args, inp, world, device, dist)
     if rank == 0:

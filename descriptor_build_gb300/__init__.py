@@ -31,6 +31,9 @@ __all__ = [
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
     "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
     "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "cq_slots", "cq_slot_fields",
+    "mr_capacity_for", "mr_register_workspace_size", "mr_register",
+    "mr_deregister_workspace_size", "mr_deregister", "MR_NEW", "MR_NEW_DUP", "DEREG_OK",
+    "DEREG_RELEASED", "DEREG_STALE",
     "cq_mirror", "cq_attach", "cq_detach", "cq_wait_ack", "cq_host_reap", "cq_request_stop",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
@@ -77,6 +80,17 @@ def _load():
                  "db_mr_workspace_size",
                  "db_mr_lookup", "db_mr_lookup_overlap", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
                  "db_last_cuda_error"):
+        getattr(lib, name).restype = i32
+    lib.db_mr_capacity_for.argtypes = [u64]
+    lib.db_mr_capacity_for.restype = u64
+    lib.db_mr_register_workspace_size.argtypes = [u64, u64, psz]
+    lib.db_mr_register.argtypes = [vp, u64, vp, u32, vp, vp, vp, vp, u64, vp, vp, vp, vp, u64,
+                                   vp, vp, vp, vp, vp, sz, vp]
+    lib.db_mr_deregister_workspace_size.argtypes = [u64, u64, psz]
+    lib.db_mr_deregister.argtypes = [vp, u64, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, sz, vp]
+    for name in ("db_mr_register_workspace_size", "db_mr_register",
+                 "db_mr_deregister_workspace_size", "db_mr_deregister"):
         getattr(lib, name).restype = i32
     lib.db_cq_mirror.argtypes = [vp, u32, vp, u64, vp, vp]
     lib.db_cq_attach.argtypes = [vp, u64, u64, u32, ctypes.POINTER(ctypes.c_uint32)]
@@ -204,6 +218,54 @@ def mr_lookup_overlap(q: torch.Tensor, mr_start: torch.Tensor, mr_end: torch.Ten
     _check("db_mr_lookup_overlap", _lib.db_mr_lookup_overlap(
         _ptr(q), n_q, _ptr(mr_start), _ptr(mr_end), _ptr(mr_lkey), n_mr, _ptr(idx), _ptr(lkey),
         _ptr(kind), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+# ------------------------------------------------------- MR cache mutation
+MR_NEW, MR_NEW_DUP = 4, 5
+DEREG_OK, DEREG_RELEASED, DEREG_STALE = 0, 1, 2
+
+
+def mr_capacity_for(n: int) -> int:
+    """Table capacity after growth to n records: 0, 32, then doubling."""
+    return int(_lib.db_mr_capacity_for(n))
+
+
+def mr_register_workspace_size(n_q: int, n_mr: int) -> int:
+    return _size(_lib.db_mr_register_workspace_size, n_q, n_mr)
+
+
+def mr_register(q: torch.Tensor, new_lkey: torch.Tensor, start: torch.Tensor, end: torch.Tensor,
+                lkey: torch.Tensor, refs: torch.Tensor, out_start: torch.Tensor,
+                out_end: torch.Tensor, out_lkey: torch.Tensor, out_refs: torch.Tensor,
+                handle: torch.Tensor, kind: torch.Tensor, remap: torch.Tensor, ws: torch.Tensor,
+                granule_shift: int = 12, ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_mr_register: a batch of registrations; the table after it goes to out_*."""
+    n_q = _records(q, 16)
+    n_mr = _records(start, 8)
+    out_cap = _records(out_start, 8)
+    _check("db_mr_register", _lib.db_mr_register(
+        _ptr(q), n_q, _ptr(new_lkey), granule_shift, _ptr(start), _ptr(end), _ptr(lkey),
+        _ptr(refs), n_mr, _ptr(out_start), _ptr(out_end), _ptr(out_lkey), _ptr(out_refs),
+        out_cap, _ptr(handle), _ptr(kind), _ptr(remap), _ptr(ctr), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def mr_deregister_workspace_size(n_h: int, n_mr: int) -> int:
+    return _size(_lib.db_mr_deregister_workspace_size, n_h, n_mr)
+
+
+def mr_deregister(handle: torch.Tensor, start: torch.Tensor, end: torch.Tensor,
+                  lkey: torch.Tensor, refs: torch.Tensor, out_start: torch.Tensor,
+                  out_end: torch.Tensor, out_lkey: torch.Tensor, out_refs: torch.Tensor,
+                  remap: torch.Tensor, status: torch.Tensor, ws: torch.Tensor,
+                  ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_mr_deregister: a batch of deregistrations, in batch order."""
+    n_h = _records(handle, 8)
+    n_mr = _records(start, 8)
+    _check("db_mr_deregister", _lib.db_mr_deregister(
+        _ptr(handle), n_h, _ptr(start), _ptr(end), _ptr(lkey), _ptr(refs), n_mr,
+        _ptr(out_start), _ptr(out_end), _ptr(out_lkey), _ptr(out_refs), _ptr(remap),
+        _ptr(status), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 # --------------------------------------------------------------- WQE bucketing

@@ -1,0 +1,761 @@
+// Registration-cache mutation batches (sm_103a).
+//
+// Sources: "NCCL expert course 26: GPUDirect RDMA, DMA-BUF, MR and the
+// registration cache" -- "IB Backend MR Cache" (a containing MR is reused
+// and takes a reference; partial overlap registers anew; deregistration
+// drops a reference and removes the MR at zero; an unknown handle is an
+// error), "Communicator User Registration Cache" (insert in address order),
+// the ncclCommRegister experiment; xNVMe "uPCIe CUDA" backend page
+// (xnvme_buf_register: whole 64 KiB device pages, refcounted).
+//
+// Registration, all on the caller's stream, no host round trip:
+//   1. the MR lookup (overlap path, 4 KiB or 64 KiB granules) classifies
+//      every request against the table before the batch;
+//   2. hits add to a per-record reference count (atomics); misses are
+//      flagged and compacted by an exclusive scan into (key, request) pairs;
+//   3. a stable LSD radix sort orders the misses by widened end, then by
+//      widened start (8-bit digits; reduce-then-scan over 4,096-key tiles,
+//      in-tile ranks from __match_any_sync), so equal ranges are adjacent
+//      and in request order;
+//   4. run starts give the new records (a scan numbers them); each old and
+//      new record finds its place in the merged table by a binary search in
+//      the other list (old records first on equal starts);
+//   5. handles, kinds, remap and counters.
+// Deregistration: handles are sorted by record (same radix sort, stable), so
+// a handle's rank among those naming its record is its batch-order rank; the
+// first refs of them drop references, the refs-th releases, the rest are
+// stale; survivors are compacted by a scan.
+#include <cerrno>
+
+#include "common.cuh"
+#include "mr_internal.h"
+#include "mrcache.h"
+
+namespace db {
+namespace mrc {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 8;
+constexpr uint64_t kScanChunk = (uint64_t)kScanThreads * kScanItems;
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;
+constexpr uint64_t kSortTile = (uint64_t)kSortThreads * kSortItems;
+constexpr int kThreads = 256;
+constexpr uint64_t kMaxItems = 1ull << 31;
+
+inline size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+inline unsigned grid_for(uint64_t n) {
+  uint64_t g = ceil_div(n, kThreads);
+  const uint64_t cap = (uint64_t)num_sms() * 16;
+  if (g > cap) g = cap;
+  return (unsigned)(g ? g : 1);
+}
+#define FOR_EACH(i, n) \
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (n); i += (uint64_t)gridDim.x * blockDim.x)
+
+// ------------------------------------------------------------------ scan
+// Exclusive scan of n u32 values (n known on the host): block sums, a scan
+// of the block sums by one CTA, then each block re-scans with its offset.
+__global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n,
+                                                            uint32_t* bsum) {
+  __shared__ uint32_t s_w[32];
+  const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
+  uint32_t v = 0;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j)
+    if (base + j < n) v += in[base + j];
+  uint32_t ex, tot;
+  block_excl_scan<32>(v, ex, tot, s_w);
+  if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
+}
+__global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint64_t nb,
+                                                           uint32_t* total) {
+  __shared__ uint32_t s_w[32];
+  uint32_t carry = 0;
+  for (uint64_t b0 = 0; b0 < nb; b0 += kScanThreads) {
+    const uint64_t b = b0 + threadIdx.x;
+    const uint32_t v = b < nb ? bsum[b] : 0u;
+    uint32_t ex, tot;
+    block_excl_scan<32>(v, ex, tot, s_w);
+    if (b < nb) bsum[b] = carry + ex;
+    carry += tot;
+    __syncthreads();  // s_w is written again by the next round
+  }
+  if (threadIdx.x == 0 && total) *total = carry;
+}
+__global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
+                                                           uint64_t n, const uint32_t* bsum) {
+  __shared__ uint32_t s_w[32];
+  const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
+  uint32_t x[kScanItems];
+  uint32_t v = 0;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    x[j] = base + j < n ? in[base + j] : 0u;
+    v += x[j];
+  }
+  uint32_t ex, tot;
+  block_excl_scan<32>(v, ex, tot, s_w);
+  uint32_t run = bsum[blockIdx.x] + ex;
+#pragma unroll
+  for (int j = 0; j < kScanItems; ++j) {
+    if (base + j < n) out[base + j] = run;
+    run += x[j];
+  }
+}
+inline size_t scan_tmp_words(uint64_t n) { return (size_t)ceil_div(n ? n : 1, kScanChunk); }
+int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_t* bsum,
+         cudaStream_t s) {
+  if (n == 0) {
+    if (total) cudaMemsetAsync(total, 0, 4, s);
+    return launch_result();
+  }
+  const uint64_t nb = ceil_div(n, kScanChunk);
+  scan_reduce<<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, bsum);
+  scan_bsums<<<1, kScanThreads, 0, s>>>(bsum, nb, total);
+  scan_apply<<<(unsigned)nb, kScanThreads, 0, s>>>(in, out, n, bsum);
+  return launch_result();
+}
+
+// ------------------------------------------------------------- radix sort
+// One stable pass on 8 bits of a u64 key (value u32 alongside), over the
+// first *n_dev items of arrays that hold up to n_max. counts is
+// [256][tiles], digit-major, so its exclusive scan gives each (digit, tile)
+// its first output position.
+__global__ void __launch_bounds__(kSortThreads) radix_count(const uint64_t* key,
+                                                            const uint32_t* n_dev, uint32_t shift,
+                                                            uint32_t* counts, uint32_t tiles) {
+  __shared__ uint32_t hist[256];
+  const uint64_t n = *n_dev;
+  const uint64_t t0 = (uint64_t)blockIdx.x * kSortTile;
+  if (t0 >= n) {  // past the items: an empty tile
+    counts[(uint64_t)threadIdx.x * tiles + blockIdx.x] = 0;
+    return;
+  }
+  hist[threadIdx.x] = 0;
+  __syncthreads();
+#pragma unroll 4
+  for (int j = 0; j < kSortItems; ++j) {
+    const uint64_t i = t0 + (uint64_t)j * kSortThreads + threadIdx.x;
+    if (i < n) atomicAdd(&hist[(uint32_t)(key[i] >> shift) & 255u], 1u);
+  }
+  __syncthreads();
+  counts[(uint64_t)threadIdx.x * tiles + blockIdx.x] = hist[threadIdx.x];
+}
+// A tile's items keep their index order: warp w ranks the 512 items
+// t0 + 512w .. t0 + 512w + 511 itself (rounds of 32, rank inside the round
+// from __match_any_sync, earlier rounds from a warp-private count), then one
+// prefix over the warps gives each item its place in the tile sorted by
+// digit. The tile is reordered in shared memory and written out run by run,
+// so consecutive threads write consecutive addresses.
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kWarpItems = (int)(kSortTile / kSortWarps);  // 512
+constexpr size_t kScatterSmem =
+    sizeof(uint32_t) * (kSortWarps * 256 + 256 + 256 + 32) + kSortTile * (8 + 4);
+__global__ void __launch_bounds__(kSortThreads) radix_scatter(
+    const uint64_t* key, const uint32_t* val, const uint32_t* n_dev, uint32_t shift,
+    const uint32_t* offs, uint32_t tiles, uint64_t* key_out, uint32_t* val_out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* s_key = reinterpret_cast<uint64_t*>(smem);                     // [kSortTile]
+  uint32_t* s_val = reinterpret_cast<uint32_t*>(s_key + kSortTile);        // [kSortTile]
+  uint32_t* s_hist = s_val + kSortTile;                                    // [warps][256]
+  uint32_t* s_tdig = s_hist + kSortWarps * 256;                            // [256]
+  uint32_t* s_goff = s_tdig + 256;                                         // [256]
+  uint32_t* s_w = s_goff + 256;                                            // [32]
+  const uint64_t n = *n_dev;
+  const uint64_t t0 = (uint64_t)blockIdx.x * kSortTile;
+  if (t0 >= n) return;  // no items: the tile's counts were all zero
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int w = 0; w < kSortWarps; ++w) s_hist[w * 256 + threadIdx.x] = 0;
+  s_goff[threadIdx.x] = offs[(uint64_t)threadIdx.x * tiles + blockIdx.x];
+  __syncthreads();
+  // 1. ranks inside each warp's chunk
+  constexpr int kRounds = kWarpItems / 32;
+  const uint64_t wbase = t0 + (uint64_t)warp * kWarpItems;
+  uint64_t k[kRounds];
+  uint32_t v[kRounds], r[kRounds];
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    const uint64_t i = wbase + (uint64_t)j * 32 + lane;
+    const bool ok = i < n;
+    k[j] = ok ? key[i] : 0ull;
+    v[j] = ok ? val[i] : 0u;
+    const uint32_t d = ok ? ((uint32_t)(k[j] >> shift) & 255u) : 256u + lane;
+    const uint32_t peers = __match_any_sync(kFull, d);
+    const uint32_t rank = __popc(peers & lanemask_lt());
+    const uint32_t before = ok ? s_hist[warp * 256 + d] : 0u;
+    r[j] = ok ? before + rank : 0xFFFFFFFFu;
+    __syncwarp();
+    if (ok && rank == 0) s_hist[warp * 256 + d] = before + __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // 2. per digit: counts of the earlier warps, and where the digit starts in the tile
+  uint32_t run = 0;
+#pragma unroll
+  for (int w = 0; w < kSortWarps; ++w) {
+    const uint32_t c = s_hist[w * 256 + threadIdx.x];
+    s_hist[w * 256 + threadIdx.x] = run;
+    run += c;
+  }
+  uint32_t ex, tot;
+  block_excl_scan<kSortWarps>(run, ex, tot, s_w);
+  s_tdig[threadIdx.x] = ex;
+  __syncthreads();
+  // 3. reorder the tile by digit in shared memory
+#pragma unroll
+  for (int j = 0; j < kRounds; ++j) {
+    if (r[j] == 0xFFFFFFFFu) continue;
+    const uint32_t d = (uint32_t)(k[j] >> shift) & 255u;
+    const uint32_t lp = s_tdig[d] + s_hist[warp * 256 + d] + r[j];
+    s_key[lp] = k[j];
+    s_val[lp] = v[j];
+  }
+  __syncthreads();
+  // 4. write the digit runs out
+  const uint64_t cnt = n - t0 < kSortTile ? n - t0 : kSortTile;
+  for (uint32_t i = threadIdx.x; i < cnt; i += kSortThreads) {
+    const uint64_t kk = s_key[i];
+    const uint32_t d = (uint32_t)(kk >> shift) & 255u;
+    const uint32_t pos = s_goff[d] + (i - s_tdig[d]);
+    key_out[pos] = kk;
+    val_out[pos] = s_val[i];
+  }
+}
+
+struct SortBufs {
+  uint64_t* key[2];
+  uint32_t* val[2];
+  uint32_t* counts;  // [256][tiles]
+  uint32_t* bsum;    // scan scratch
+  uint64_t n_max;
+};
+inline uint32_t sort_tiles(uint64_t n_max) { return (uint32_t)ceil_div(n_max ? n_max : 1, kSortTile); }
+inline size_t sort_count_words(uint64_t n_max) { return (size_t)256 * sort_tiles(n_max); }
+// The scatter's shared memory is above the default 48 KiB: opt in once per device.
+int prepare_scatter() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!done[dev & 63]) {
+    if (cudaFuncSetAttribute(radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kScatterSmem) != cudaSuccess)
+      return launch_result();
+    done[dev & 63] = true;
+  }
+  return 0;
+}
+// Sorts by bits [0, bits) of the key; the result is in buffer `cur` on return.
+int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, cudaStream_t s) {
+  if (int rc = prepare_scatter()) return rc;
+  const uint32_t tiles = sort_tiles(b.n_max);
+  const uint64_t nc = (uint64_t)256 * tiles;
+  for (int shift = 0; shift < bits; shift += 8) {
+    radix_count<<<tiles, kSortThreads, 0, s>>>(b.key[cur], n_dev, (uint32_t)shift, b.counts, tiles);
+    int rc = launch_result();
+    if (rc) return rc;
+    if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s))) return rc;
+    radix_scatter<<<tiles, kSortThreads, kScatterSmem, s>>>(
+        b.key[cur], b.val[cur], n_dev, (uint32_t)shift, b.counts, tiles, b.key[cur ^ 1],
+        b.val[cur ^ 1]);
+    if ((rc = launch_result())) return rc;
+    cur ^= 1;
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------- registration
+struct RegHeader {   // 256 bytes at the start of the registration workspace
+  uint32_t m;        // requests that missed
+  uint32_t u;        // distinct missed ranges (new records)
+  uint32_t pad[2];
+  db_counters lookup;  // counters of the lookup pass
+};
+
+__device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gshift,
+                                      uint64_t& base, uint64_t& aend) {
+  const uint64_t g = 1ull << gshift;
+  const uint64_t addr = q[k].addr, size = q[k].size;
+  base = addr & ~(g - 1);
+  aend = (addr + size + g - 1) & ~(g - 1);  // valid requests only: no wrap
+}
+
+__global__ void reg_mark(const uint8_t* kind0, const int32_t* idx, uint64_t n_q, uint32_t* more,
+                         uint32_t* flag) {
+  FOR_EACH(k, n_q) {
+    const uint8_t kd = kind0[k];
+    flag[k] = kd == DB_MR_MISS;
+    if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) atomicAdd(&more[idx[k]], 1u);
+  }
+}
+__global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint32_t* pos,
+                            uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val) {
+  FOR_EACH(k, n_q) {
+    if (!flag[k]) continue;
+    uint64_t b, e;
+    widen(q, k, gshift, b, e);
+    key[pos[k]] = e >> gshift;
+    val[pos[k]] = (uint32_t)k;
+  }
+}
+__global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
+                          const uint32_t* val, uint64_t* key) {
+  const uint64_t m = h->m;
+  FOR_EACH(i, n_max) {
+    if (i >= m) break;
+    uint64_t b, e;
+    widen(q, val[i], gshift, b, e);
+    key[i] = b >> gshift;
+  }
+}
+// Run starts of equal widened ranges over the sorted misses (0 past m).
+__global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
+                         const uint32_t* val, uint32_t* flag) {
+  const uint64_t m = h->m;
+  FOR_EACH(i, n_max) {
+    uint32_t f = 0;
+    if (i < m) {
+      if (i == 0) {
+        f = 1;
+      } else {
+        uint64_t b0, e0, b1, e1;
+        widen(q, val[i - 1], gshift, b0, e0);
+        widen(q, val[i], gshift, b1, e1);
+        f = (b0 != b1 || e0 != e1);
+      }
+    }
+    flag[i] = f;
+  }
+}
+// New record j from the run that starts at sorted position i; every miss
+// adds one reference to its run's record.
+__global__ void reg_new(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
+                        const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
+                        uint64_t* nstart, uint64_t* nend, uint32_t* nfirst, uint32_t* nrefs) {
+  const uint64_t m = h->m;
+  FOR_EACH(i, n_max) {
+    if (i >= m) break;
+    const uint32_t j = excl[i] + flag[i] - 1;
+    if (flag[i]) {
+      uint64_t b, e;
+      widen(q, val[i], gshift, b, e);
+      nstart[j] = b;
+      nend[j] = e;
+      nfirst[j] = val[i];
+    }
+    atomicAdd(&nrefs[j], 1u);
+  }
+}
+// Count of a[0..n) below x (strict) or at most x.
+__device__ __forceinline__ uint64_t count_below(const uint64_t* a, uint64_t n, uint64_t x,
+                                                bool or_equal) {
+  uint64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint64_t mid = (lo + hi) >> 1;
+    const uint64_t v = a[mid];
+    if (v < x || (or_equal && v == x)) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+struct PlaceParams {
+  const uint64_t *start, *end;
+  const uint32_t *lkey, *refs, *more;
+  uint64_t n;
+  const uint64_t *nstart, *nend;
+  const uint32_t *nfirst, *nrefs, *new_lkey;
+  uint64_t *o_start, *o_end;
+  uint32_t *o_lkey, *o_refs;
+  uint64_t o_cap;
+  int64_t* remap;
+  uint32_t* npos;
+  const RegHeader* h;
+};
+__global__ void reg_place_old(const PlaceParams p) {
+  const uint64_t u = p.h->u;
+  if (p.n + u > p.o_cap) return;
+  FOR_EACH(i, p.n) {
+    const uint64_t w = i + count_below(p.nstart, u, p.start[i], false);  // old first on ties
+    p.o_start[w] = p.start[i];
+    p.o_end[w] = p.end[i];
+    p.o_lkey[w] = p.lkey[i];
+    p.o_refs[w] = p.refs[i] + p.more[i];
+    p.remap[i] = (int64_t)w;
+  }
+}
+__global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
+  const uint64_t u = p.h->u;
+  if (p.n + u > p.o_cap) return;
+  FOR_EACH(j, n_max) {
+    if (j >= u) break;
+    const uint64_t w = j + count_below(p.start, p.n, p.nstart[j], true);
+    p.o_start[w] = p.nstart[j];
+    p.o_end[w] = p.nend[j];
+    p.o_lkey[w] = p.new_lkey[p.nfirst[j]];
+    p.o_refs[w] = p.nrefs[j];
+    p.npos[j] = (uint32_t)w;
+  }
+}
+__global__ void reg_handles_hit(const uint8_t* kind0, const int32_t* idx, uint64_t n_q,
+                                const int64_t* remap, const RegHeader* h, uint64_t n,
+                                uint64_t o_cap, int64_t* handle, uint8_t* kind) {
+  const bool fits = n + h->u <= o_cap;
+  FOR_EACH(k, n_q) {
+    const uint8_t kd = kind0[k];
+    if (kd == DB_MR_MISS) continue;
+    kind[k] = kd;
+    if (!fits) continue;
+    handle[k] = kd == DB_MR_INVALID ? -1 : remap[idx[k]];
+  }
+}
+__global__ void reg_handles_miss(const RegHeader* h, uint64_t n_max, uint64_t n, uint64_t o_cap,
+                                 const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
+                                 const uint32_t* npos, int64_t* handle, uint8_t* kind) {
+  const uint64_t m = h->m;
+  const bool fits = n + h->u <= o_cap;
+  FOR_EACH(i, n_max) {
+    if (i >= m) break;
+    const uint32_t k = val[i];
+    kind[k] = flag[i] ? DB_MR_NEW : DB_MR_NEW_DUP;
+    if (fits) handle[k] = npos[excl[i] + flag[i] - 1];
+  }
+}
+__global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_counters* ctr) {
+  const uint64_t total = n + h->u;
+  ctr->total = total;
+  ctr->n_invalid = h->lookup.n_invalid;
+  ctr->n_overflow = total > o_cap ? 1 : 0;
+  ctr->err = h->lookup.err;
+}
+
+struct RegLayout {
+  size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
+      nstart, nend, nfirst, nrefs, npos, total;
+};
+RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
+  RegLayout L;
+  const uint64_t q = n_q ? n_q : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
+  L.lookup = take(mr::workspace_bytes(n_mr));
+  L.hdr = take(sizeof(RegHeader));
+  L.idx = take(q * 4);
+  L.lk = take(q * 4);
+  L.kind0 = take(q);
+  L.more = take((n_mr ? n_mr : 1) * 4);
+  L.flag = take(q * 4);
+  L.pos = take(q * 4);
+  L.key0 = take(q * 8);
+  L.key1 = take(q * 8);
+  L.val0 = take(q * 4);
+  L.val1 = take(q * 4);
+  L.counts = take(sort_count_words(q) * 4);
+  L.bsum = take(scan_tmp_words(sort_count_words(q) > q ? sort_count_words(q) : q) * 4);
+  L.nstart = take(q * 8);
+  L.nend = take(q * 8);
+  L.nfirst = take(q * 4);
+  L.nrefs = take(q * 4);
+  L.npos = take(q * 4);
+  L.total = o;
+  return L;
+}
+
+// ----------------------------------------------------------- deregistration
+struct DeregHeader {
+  uint32_t n_h;      // items the sort covers (every handle)
+  uint32_t kept;     // records after the batch
+  unsigned long long stale;
+};
+__global__ void set_u32(uint32_t* p, uint32_t v) { *p = v; }
+__global__ void dereg_key(const int64_t* handle, uint64_t n_h, uint64_t n, uint64_t* key,
+                          uint32_t* val) {
+  FOR_EACH(k, n_h) {
+    const int64_t x = handle[k];
+    key[k] = (x >= 0 && (uint64_t)x < n) ? (uint64_t)x : n;  // n: no such record
+    val[k] = (uint32_t)k;
+  }
+}
+__global__ void dereg_runs(const uint64_t* key, uint64_t n_h, uint32_t* flag) {
+  FOR_EACH(i, n_h) flag[i] = i == 0 || key[i] != key[i - 1];
+}
+__global__ void dereg_run_start(const uint32_t* flag, const uint32_t* excl, uint64_t n_h,
+                                uint32_t* rs) {
+  FOR_EACH(i, n_h) if (flag[i]) rs[excl[i]] = (uint32_t)i;
+}
+__global__ void dereg_status(const uint64_t* key, const uint32_t* val, const uint32_t* flag,
+                             const uint32_t* excl, const uint32_t* rs, uint64_t n_h, uint64_t n,
+                             const uint32_t* refs, uint32_t* dec, uint8_t* status,
+                             DeregHeader* h) {
+  unsigned long long stale = 0;
+  FOR_EACH(i, n_h) {
+    const uint64_t r = key[i];
+    uint8_t st = DB_DEREG_STALE;
+    if (r < n) {
+      const uint32_t rank = (uint32_t)i - rs[excl[i] + flag[i] - 1];
+      const uint32_t have = refs[r];
+      if (rank < have) {
+        st = rank + 1 == have ? DB_DEREG_RELEASED : DB_DEREG_OK;
+        atomicAdd(&dec[r], 1u);
+      }
+    }
+    stale += st == DB_DEREG_STALE;
+    status[val[i]] = st;
+  }
+  stale = warp_sum64(stale);
+  if ((threadIdx.x & 31) == 0 && stale) atomicAdd(&h->stale, stale);
+}
+__global__ void dereg_keep(const uint32_t* refs, const uint32_t* dec, uint64_t n, uint32_t* keep) {
+  FOR_EACH(i, n) keep[i] = refs[i] > dec[i];
+}
+__global__ void dereg_place(const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
+                            const uint32_t* refs, const uint32_t* dec, const uint32_t* keep,
+                            const uint32_t* kpos, uint64_t n, uint64_t* o_start, uint64_t* o_end,
+                            uint32_t* o_lkey, uint32_t* o_refs, int64_t* remap) {
+  FOR_EACH(i, n) {
+    if (!keep[i]) {
+      remap[i] = -1;
+      continue;
+    }
+    const uint32_t w = kpos[i];
+    o_start[w] = start[i];
+    o_end[w] = end[i];
+    o_lkey[w] = lkey[i];
+    o_refs[w] = refs[i] - dec[i];
+    remap[i] = w;
+  }
+}
+__global__ void dereg_final(const DeregHeader* h, db_counters* ctr) {
+  ctr->total = h->kept;
+  ctr->n_invalid = h->stale;
+  ctr->n_overflow = 0;
+  ctr->err = 0;
+}
+
+struct DeregLayout {
+  size_t hdr, key0, key1, val0, val1, counts, bsum, flag, excl, rs, dec, keep, kpos, total;
+};
+DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
+  DeregLayout L;
+  const uint64_t q = n_h ? n_h : 1, n = n_mr ? n_mr : 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
+  L.hdr = take(sizeof(DeregHeader));
+  L.key0 = take(q * 8);
+  L.key1 = take(q * 8);
+  L.val0 = take(q * 4);
+  L.val1 = take(q * 4);
+  L.counts = take(sort_count_words(q) * 4);
+  const uint64_t scan_n = sort_count_words(q) > q ? sort_count_words(q) : q;
+  L.bsum = take(scan_tmp_words(scan_n > n ? scan_n : n) * 4);
+  L.flag = take(q * 4);
+  L.excl = take(q * 4);
+  L.rs = take(q * 4);
+  L.dec = take(n * 4);
+  L.keep = take(n * 4);
+  L.kpos = take(n * 4);
+  L.total = o;
+  return L;
+}
+
+}  // namespace mrc
+}  // namespace db
+
+using namespace db;
+
+extern "C" uint64_t db_mr_capacity_for(uint64_t n) {
+  if (n == 0) return 0;
+  uint64_t c = 32;
+  while (c < n) c <<= 1;
+  return c;
+}
+
+extern "C" int db_mr_register_workspace_size(uint64_t n_q, uint64_t n_mr, size_t* bytes) {
+  if (!bytes || n_q >= mrc::kMaxItems || n_mr >= mrc::kMaxItems) return -EINVAL;
+  *bytes = mrc::reg_layout(n_q, n_mr).total;
+  return 0;
+}
+
+extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* new_lkey,
+                              uint32_t granule_shift, const uint64_t* start, const uint64_t* end,
+                              const uint32_t* lkey, const uint32_t* refs, uint64_t n_mr,
+                              uint64_t* out_start, uint64_t* out_end, uint32_t* out_lkey,
+                              uint32_t* out_refs, uint64_t out_cap, int64_t* handle,
+                              uint8_t* kind, int64_t* remap, db_counters* ctr, void* ws,
+                              size_t ws_bytes, void* stream) {
+  using namespace mrc;
+  if (granule_shift != 12 && granule_shift != 16) return -EINVAL;
+  if (n_q >= kMaxItems || n_mr >= kMaxItems || out_cap >= kMaxItems) return -EINVAL;
+  if (!ws || !aligned(ws, 256) || (ctr && !aligned(ctr, 8))) return -EINVAL;
+  if (n_q && (!q || !new_lkey || !handle || !kind || !aligned(q, 16) || !aligned(new_lkey, 4) ||
+              !aligned(handle, 8)))
+    return -EINVAL;
+  if (n_mr && (!start || !end || !lkey || !refs || !remap || !aligned(start, 8) ||
+               !aligned(end, 8) || !aligned(lkey, 4) || !aligned(refs, 4) || !aligned(remap, 8)))
+    return -EINVAL;
+  if (out_cap && (!out_start || !out_end || !out_lkey || !out_refs || !aligned(out_start, 8) ||
+                  !aligned(out_end, 8) || !aligned(out_lkey, 4) || !aligned(out_refs, 4)))
+    return -EINVAL;
+  const RegLayout L = reg_layout(n_q, n_mr);
+  if (ws_bytes < L.total) return -ENOSPC;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = static_cast<char*>(ws);
+  auto at = [&](size_t off) { return static_cast<void*>(w + off); };
+  RegHeader* h = static_cast<RegHeader*>(at(L.hdr));
+  int32_t* idx = static_cast<int32_t*>(at(L.idx));
+  uint8_t* kind0 = static_cast<uint8_t*>(at(L.kind0));
+  uint32_t* more = static_cast<uint32_t*>(at(L.more));
+  uint32_t* flag = static_cast<uint32_t*>(at(L.flag));
+  uint32_t* pos = static_cast<uint32_t*>(at(L.pos));
+  uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
+  SortBufs sb{{static_cast<uint64_t*>(at(L.key0)), static_cast<uint64_t*>(at(L.key1))},
+              {static_cast<uint32_t*>(at(L.val0)), static_cast<uint32_t*>(at(L.val1))},
+              static_cast<uint32_t*>(at(L.counts)), bsum, n_q};
+  uint64_t* nstart = static_cast<uint64_t*>(at(L.nstart));
+  uint64_t* nend = static_cast<uint64_t*>(at(L.nend));
+  uint32_t* nfirst = static_cast<uint32_t*>(at(L.nfirst));
+  uint32_t* nrefs = static_cast<uint32_t*>(at(L.nrefs));
+  uint32_t* npos = static_cast<uint32_t*>(at(L.npos));
+
+  int rc = 0;
+  if (cudaMemsetAsync(h, 0, sizeof(RegHeader), s) != cudaSuccess ||
+      (n_mr && cudaMemsetAsync(more, 0, n_mr * 4, s) != cudaSuccess) ||
+      (n_q && cudaMemsetAsync(nrefs, 0, n_q * 4, s) != cudaSuccess))
+    return launch_result();
+  // 1. lookup against the table as it stands
+  if (n_q) {
+    rc = mr::lookup(q, n_q, start, end, lkey, n_mr, idx, static_cast<uint32_t*>(at(L.lk)), kind0,
+                    &h->lookup, at(L.lookup), mr::workspace_bytes(n_mr), s, true,
+                    (int)granule_shift);
+    if (rc) return rc;
+    // 2. hits and misses
+    reg_mark<<<grid_for(n_q), kThreads, 0, s>>>(kind0, idx, n_q, more, flag);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->m, bsum, s))) return rc;
+    reg_compact<<<grid_for(n_q), kThreads, 0, s>>>(q, flag, pos, n_q, granule_shift, sb.key[0],
+                                                   sb.val[0]);
+    if ((rc = launch_result())) return rc;
+    // 3. sort the misses by (start, end), stable in request order
+    const int bits = 64 - (int)granule_shift;
+    int cur = 0;
+    if ((rc = radix_sort(sb, cur, &h->m, bits, s))) return rc;
+    reg_rekey<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sb.val[cur],
+                                                 sb.key[cur]);
+    if ((rc = launch_result())) return rc;
+    if ((rc = radix_sort(sb, cur, &h->m, bits, s))) return rc;
+    // 4. runs of equal ranges are the new records
+    const uint32_t* sval = sb.val[cur];
+    reg_runs<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sval, flag);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->u, bsum, s))) return rc;
+    reg_new<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sval, flag, pos, nstart,
+                                               nend, nfirst, nrefs);
+    if ((rc = launch_result())) return rc;
+    PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
+    if (n_mr) {
+      reg_place_old<<<grid_for(n_mr), kThreads, 0, s>>>(pp);
+      if ((rc = launch_result())) return rc;
+    }
+    reg_place_new<<<grid_for(n_q), kThreads, 0, s>>>(pp, n_q);
+    if ((rc = launch_result())) return rc;
+    // 5. handles and kinds
+    reg_handles_hit<<<grid_for(n_q), kThreads, 0, s>>>(kind0, idx, n_q, remap, h, n_mr, out_cap,
+                                                       handle, kind);
+    if ((rc = launch_result())) return rc;
+    reg_handles_miss<<<grid_for(n_q), kThreads, 0, s>>>(h, n_q, n_mr, out_cap, sval, flag, pos,
+                                                        npos, handle, kind);
+    if ((rc = launch_result())) return rc;
+  } else if (n_mr) {
+    // no requests: the table is copied through (and checked like a lookup would)
+    rc = mr::lookup(nullptr, 0, start, end, lkey, n_mr, nullptr, nullptr, nullptr, &h->lookup,
+                    at(L.lookup), mr::workspace_bytes(n_mr), s, true, (int)granule_shift);
+    if (rc) return rc;
+    PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
+    reg_place_old<<<grid_for(n_mr), kThreads, 0, s>>>(pp);
+    if ((rc = launch_result())) return rc;
+  }
+  if (ctr) {
+    reg_final<<<1, 1, 0, s>>>(h, n_mr, out_cap, ctr);
+    return launch_result();
+  }
+  return 0;
+}
+
+extern "C" int db_mr_deregister_workspace_size(uint64_t n_h, uint64_t n_mr, size_t* bytes) {
+  if (!bytes || n_h >= mrc::kMaxItems || n_mr >= mrc::kMaxItems) return -EINVAL;
+  *bytes = mrc::dereg_layout(n_h, n_mr).total;
+  return 0;
+}
+
+extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint64_t* start,
+                                const uint64_t* end, const uint32_t* lkey, const uint32_t* refs,
+                                uint64_t n_mr, uint64_t* out_start, uint64_t* out_end,
+                                uint32_t* out_lkey, uint32_t* out_refs, int64_t* remap,
+                                uint8_t* status, db_counters* ctr, void* ws, size_t ws_bytes,
+                                void* stream) {
+  using namespace mrc;
+  if (n_h >= kMaxItems || n_mr >= kMaxItems) return -EINVAL;
+  if (!ws || !aligned(ws, 256) || (ctr && !aligned(ctr, 8))) return -EINVAL;
+  if (n_h && (!handle || !status || !aligned(handle, 8))) return -EINVAL;
+  if (n_mr && (!start || !end || !lkey || !refs || !remap || !out_start || !out_end ||
+               !out_lkey || !out_refs || !aligned(start, 8) || !aligned(end, 8) ||
+               !aligned(lkey, 4) || !aligned(refs, 4) || !aligned(remap, 8) ||
+               !aligned(out_start, 8) || !aligned(out_end, 8) || !aligned(out_lkey, 4) ||
+               !aligned(out_refs, 4)))
+    return -EINVAL;
+  const DeregLayout L = dereg_layout(n_h, n_mr);
+  if (ws_bytes < L.total) return -ENOSPC;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = static_cast<char*>(ws);
+  auto at = [&](size_t off) { return static_cast<void*>(w + off); };
+  DeregHeader* h = static_cast<DeregHeader*>(at(L.hdr));
+  uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
+  SortBufs sb{{static_cast<uint64_t*>(at(L.key0)), static_cast<uint64_t*>(at(L.key1))},
+              {static_cast<uint32_t*>(at(L.val0)), static_cast<uint32_t*>(at(L.val1))},
+              static_cast<uint32_t*>(at(L.counts)), bsum, n_h};
+  uint32_t* flag = static_cast<uint32_t*>(at(L.flag));
+  uint32_t* excl = static_cast<uint32_t*>(at(L.excl));
+  uint32_t* rs = static_cast<uint32_t*>(at(L.rs));
+  uint32_t* dec = static_cast<uint32_t*>(at(L.dec));
+  uint32_t* keep = static_cast<uint32_t*>(at(L.keep));
+  uint32_t* kpos = static_cast<uint32_t*>(at(L.kpos));
+  if (cudaMemsetAsync(h, 0, sizeof(DeregHeader), s) != cudaSuccess ||
+      (n_mr && cudaMemsetAsync(dec, 0, n_mr * 4, s) != cudaSuccess))
+    return launch_result();
+  set_u32<<<1, 1, 0, s>>>(&h->n_h, (uint32_t)n_h);  // the sort reads its length on the device
+  int rc = launch_result();
+  if (rc) return rc;
+  if (n_h) {
+    dereg_key<<<grid_for(n_h), kThreads, 0, s>>>(handle, n_h, n_mr, sb.key[0], sb.val[0]);
+    if ((rc = launch_result())) return rc;
+    int bits = 0;
+    while (bits < 64 && (n_mr >> bits)) ++bits;  // keys are at most n_mr
+    bits = (bits + 7) & ~7;
+    int cur = 0;
+    if ((rc = radix_sort(sb, cur, &h->n_h, bits, s))) return rc;
+    dereg_runs<<<grid_for(n_h), kThreads, 0, s>>>(sb.key[cur], n_h, flag);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, excl, n_h, nullptr, bsum, s))) return rc;
+    dereg_run_start<<<grid_for(n_h), kThreads, 0, s>>>(flag, excl, n_h, rs);
+    if ((rc = launch_result())) return rc;
+    dereg_status<<<grid_for(n_h), kThreads, 0, s>>>(sb.key[cur], sb.val[cur], flag, excl, rs, n_h,
+                                                    n_mr, refs, dec, status, h);
+    if ((rc = launch_result())) return rc;
+  }
+  if (n_mr) {
+    dereg_keep<<<grid_for(n_mr), kThreads, 0, s>>>(refs, dec, n_mr, keep);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(keep, kpos, n_mr, &h->kept, bsum, s))) return rc;
+    dereg_place<<<grid_for(n_mr), kThreads, 0, s>>>(start, end, lkey, refs, dec, keep, kpos, n_mr,
+                                                    out_start, out_end, out_lkey, out_refs, remap);
+    if ((rc = launch_result())) return rc;
+  }
+  if (ctr) {
+    dereg_final<<<1, 1, 0, s>>>(h, ctr);
+    return launch_result();
+  }
+  return 0;
+}

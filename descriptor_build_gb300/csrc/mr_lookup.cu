@@ -25,6 +25,7 @@
 // contain [base, aend) is the last one starting at or below base, so the
 // lowest containing index is that record or none.
 #include "common.cuh"
+#include "mr_internal.h"
 
 namespace db {
 namespace mr {
@@ -244,8 +245,12 @@ __device__ __forceinline__ uint32_t first_reaching(const Rec* rec, uint32_t j, u
   return (uint32_t)hi;
 }
 
-template <bool kOverlap>
+// kGranuleShift: queries are widened to whole granules of 2^kGranuleShift
+// bytes (12: 4 KiB pages; 16: the 64 KiB registry granule). The directory
+// works in 4 KiB pages either way, since every granule boundary is one.
+template <bool kOverlap, int kGranuleShift>
 __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(const LookupParams p) {
+  constexpr uint64_t kGran = 1ull << kGranuleShift;
   const uint64_t pol_first = policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
   const uint64_t lo = p.hdr_ro->lo;
@@ -281,13 +286,13 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
       if (i < p.n_q) {
         const uint64_t addr = nq[k].x, size = nq[k].y;
         // valid iff size >= 1 and addr + size <= 2^64 - 4096 (the widened end fits)
-        constexpr uint64_t kTop = ~0ull - 4095ull;
+        constexpr uint64_t kTop = ~0ull - (kGran - 1);
         const bool ok = size != 0 && size <= kTop && addr <= kTop - size;
         if (!ok) {
           state[k] = 2;
         } else {
-          base[k] = addr & ~4095ull;
-          aend[k] = (addr + size + 4095ull) & ~4095ull;
+          base[k] = addr & ~(kGran - 1);
+          aend[k] = (addr + size + kGran - 1) & ~(kGran - 1);
           state[k] = (n_mr == 0 || base[k] < lo) ? 0 : 1;
         }
       }
@@ -498,7 +503,7 @@ int lookup_ctas_per_sm() {
   int& occ = per_sm[dev & 63];
   if (occ == 0) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, mr_lookup_kernel<false>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, mr_lookup_kernel<false, 12>, kThreads, 0) !=
             cudaSuccess ||
         o < 1)
       o = 1;
@@ -518,11 +523,14 @@ extern "C" int db_mr_workspace_size(uint64_t n_mr, size_t* bytes) {
   return 0;
 }
 
-namespace {
+namespace db {
+namespace mr {
 
-int mr_call(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint64_t* mr_end,
-            const uint32_t* mr_lkey, uint64_t n_mr, int32_t* idx, uint32_t* lkey, uint8_t* kind,
-            db_counters* ctr, void* ws, size_t ws_bytes, cudaStream_t s, bool overlap) {
+int lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint64_t* mr_end,
+           const uint32_t* mr_lkey, uint64_t n_mr, int32_t* idx, uint32_t* lkey, uint8_t* kind,
+           db_counters* ctr, void* ws, size_t ws_bytes, cudaStream_t s, bool overlap,
+           int granule_shift) {
+  if (granule_shift != 12 && granule_shift != 16) return -EINVAL;
   if (n_mr >= (1ull << 31)) return -EINVAL;
   if (ctr && !aligned(ctr, 8)) return -EINVAL;
   if (n_q == 0) {
@@ -572,27 +580,32 @@ int mr_call(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uin
   uint64_t grid = (n_q + per_cta - 1) / per_cta;
   const uint64_t resident = (uint64_t)num_sms() * mr::lookup_ctas_per_sm();
   if (grid > resident) grid = resident;
-  if (overlap)
-    mr::mr_lookup_kernel<true><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+  if (granule_shift == 16)
+    mr::mr_lookup_kernel<true, 16><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+  else if (overlap)
+    mr::mr_lookup_kernel<true, 12><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
   else
-    mr::mr_lookup_kernel<false><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+    mr::mr_lookup_kernel<false, 12><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
   return launch_result();
 }
 
-}  // namespace
+size_t workspace_bytes(uint64_t n_mr) { return ws_bytes_for(n_mr); }
+
+}  // namespace mr
+}  // namespace db
 
 extern "C" int db_mr_lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
                             const uint64_t* mr_end, const uint32_t* mr_lkey, uint64_t n_mr,
                             int32_t* idx, uint32_t* lkey, uint8_t* kind, db_counters* ctr,
                             void* ws, size_t ws_bytes, void* stream) {
-  return mr_call(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
-                 (cudaStream_t)stream, false);
+  return mr::lookup(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
+                    (cudaStream_t)stream, false, 12);
 }
 
 extern "C" int db_mr_lookup_overlap(const db_range* q, uint64_t n_q, const uint64_t* mr_start,
                                     const uint64_t* mr_end, const uint32_t* mr_lkey,
                                     uint64_t n_mr, int32_t* idx, uint32_t* lkey, uint8_t* kind,
                                     db_counters* ctr, void* ws, size_t ws_bytes, void* stream) {
-  return mr_call(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
-                 (cudaStream_t)stream, true);
+  return mr::lookup(q, n_q, mr_start, mr_end, mr_lkey, n_mr, idx, lkey, kind, ctr, ws, ws_bytes,
+                    (cudaStream_t)stream, true, 12);
 }

@@ -37,7 +37,7 @@ SEED_BASE = 0xDB5EED00
 
 # Workload names in the order of the study's configuration list.
 WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket", "put_bucket_vmm",
-             "mr_lookup_overlap")
+             "mr_lookup_overlap", "mr_register", "mr_deregister")
 
 
 def seed_of(name: str) -> int:
@@ -336,6 +336,37 @@ def mr_lookup_overlap(seed: int | None = None, n_mr: int = 1_048_576,
     stop = np.where(kind == 0, stop0, np.where(kind == 1, stop1, stop2))
     return dict(name="mr_lookup_overlap", mr_start=start, mr_end=end, mr_lkey=lkey,
                 queries=pack_ranges(addr, stop - addr), query_mix=kind)
+
+
+def mr_register(seed: int | None = None, n_mr: int = 1_048_576,
+                n_q: int = 16_777_216) -> dict:
+    """A registration batch: the ``mr_lookup`` table and queries as requests
+    (40 % the same range as a record, 40 % inside one, 20 % missing), each
+    record holding 1..4 references, and the lkey a new registration for each
+    request would get (uniform u32)."""
+    d = mr_lookup(seed_of("mr_register") if seed is None else seed, n_mr, n_q)
+    rng = _rng((seed_of("mr_register") if seed is None else seed) + 1)
+    d["name"] = "mr_register"
+    d["mr_refs"] = rng.integers(1, 5, size=n_mr).astype(np.uint32)
+    d["new_lkey"] = rng.integers(0, 1 << 32, size=n_q, dtype=np.uint64).astype(np.uint32)
+    return d
+
+
+def mr_deregister(seed: int | None = None, n_mr: int = 1_048_576,
+                  n_h: int = 2_097_152) -> dict:
+    """A deregistration batch over the ``mr_lookup`` table with 1..4
+    references per record: 94 % of the handles name a record (uniform), 3 %
+    are -1 and 3 % lie past the table, so some records lose every reference
+    and some handles arrive after their record was released."""
+    s0 = seed_of("mr_deregister") if seed is None else seed
+    rng = _rng(s0)
+    start, end, lkey, _ = mr_table(rng, n_mr)
+    refs = rng.integers(1, 5, size=n_mr).astype(np.uint32)
+    h = rng.integers(0, n_mr, size=n_h).astype(np.int64)
+    u = rng.random(n_h)
+    h = np.where(u < 0.03, -1, np.where(u < 0.06, n_mr + rng.integers(0, n_mr, size=n_h), h))
+    return dict(name="mr_deregister", mr_start=start, mr_end=end, mr_lkey=lkey, mr_refs=refs,
+                handles=h.astype(np.int64))
 
 
 def put_bucket(seed: int | None = None, n: int = 8_388_608, world: int = 8,

@@ -1,0 +1,241 @@
+"""db_mr_register / db_mr_deregister on the GPU against the oracle, bit for
+bit ("NCCL expert course 26": IB Backend MR Cache, Communicator User
+Registration Cache, the ncclCommRegister experiment; xNVMe "uPCIe CUDA":
+xnvme_buf_register at 64 KiB)."""
+
+import numpy as np
+import pytest
+
+from conftest import h, load_golden
+from gpu_util import dev32, dev64, host32, host64, lib, need_gpu, torch
+
+pytestmark = pytest.mark.gpu
+
+EMPTY = (np.zeros(0, np.uint64), np.zeros(0, np.uint64), np.zeros(0, np.uint32),
+         np.zeros(0, np.uint32))
+
+
+@pytest.fixture(scope="module")
+def db():
+    need_gpu()
+    return lib()
+
+
+def d64(a):
+    return dev64(a) if a.shape[0] else torch.zeros(0, dtype=torch.int64, device="cuda")
+
+
+def d32(a):
+    return dev32(a) if a.shape[0] else torch.zeros(0, dtype=torch.int32, device="cuda")
+
+
+def register(db, q, new_lkey, start, end, lkey, refs, granule_shift=12, out_cap=None):
+    q = np.ascontiguousarray(q, np.uint64).reshape(-1, 2)
+    n_q, n = q.shape[0], start.shape[0]
+    cap = n + n_q if out_cap is None else out_cap
+    o = [torch.full((cap,), 0x55, dtype=torch.int64, device="cuda"),
+         torch.full((cap,), 0x55, dtype=torch.int64, device="cuda"),
+         torch.full((cap,), 0x55, dtype=torch.int32, device="cuda"),
+         torch.full((cap,), 0x55, dtype=torch.int32, device="cuda")]
+    handle = torch.full((n_q,), -7, dtype=torch.int64, device="cuda")
+    kind = torch.full((n_q,), 0xEE, dtype=torch.uint8, device="cuda")
+    remap = torch.full((n,), -7, dtype=torch.int64, device="cuda")
+    ctr = torch.full((4,), -1, dtype=torch.int64, device="cuda")
+    ws = db.workspace(db.mr_register_workspace_size(n_q, n))
+    db.mr_register(d64(q.reshape(-1)).view(-1, 2) if n_q else torch.zeros((0, 2), dtype=torch.int64, device="cuda"),
+                   d32(np.ascontiguousarray(new_lkey, np.uint32)), d64(start), d64(end), d32(lkey),
+                   d32(refs), *o, handle, kind, remap, ws, granule_shift=granule_shift, ctr=ctr)
+    torch.cuda.synchronize()
+    c = host64(ctr)
+    m = int(c[0]) if int(c[2]) == 0 else 0
+    return dict(start=host64(o[0])[:m], end=host64(o[1])[:m], lkey=host32(o[2])[:m],
+                refs=host32(o[3])[:m], handle=handle.cpu().numpy(), kind=kind.cpu().numpy(),
+                remap=remap.cpu().numpy(), ctr=c)
+
+
+def deregister(db, handles, start, end, lkey, refs):
+    hs = np.ascontiguousarray(handles, np.int64)
+    n = start.shape[0]
+    o = [torch.full((max(n, 1),), 0x55, dtype=torch.int64, device="cuda"),
+         torch.full((max(n, 1),), 0x55, dtype=torch.int64, device="cuda"),
+         torch.full((max(n, 1),), 0x55, dtype=torch.int32, device="cuda"),
+         torch.full((max(n, 1),), 0x55, dtype=torch.int32, device="cuda")]
+    remap = torch.full((n,), -7, dtype=torch.int64, device="cuda")
+    status = torch.full((hs.shape[0],), 0xEE, dtype=torch.uint8, device="cuda")
+    ctr = torch.full((4,), -1, dtype=torch.int64, device="cuda")
+    ws = db.workspace(db.mr_deregister_workspace_size(hs.shape[0], n))
+    hd = torch.from_numpy(hs).cuda() if hs.shape[0] else torch.zeros(0, dtype=torch.int64,
+                                                                      device="cuda")
+    db.mr_deregister(hd, d64(start), d64(end), d32(lkey), d32(refs), *o, remap, status, ws,
+                     ctr=ctr)
+    torch.cuda.synchronize()
+    c = host64(ctr)
+    m = int(c[0])
+    return dict(start=host64(o[0])[:m], end=host64(o[1])[:m], lkey=host32(o[2])[:m],
+                refs=host32(o[3])[:m], remap=remap.cpu().numpy(), status=status.cpu().numpy(),
+                ctr=c)
+
+
+def same(got, want, keys):
+    for k in keys:
+        assert got[k].shape == want[k].shape, k
+        assert (got[k].astype(np.int64) == want[k].astype(np.int64)).all(), k
+
+
+REG_KEYS = ("start", "end", "lkey", "refs", "handle", "kind", "remap", "ctr")
+DEREG_KEYS = ("start", "end", "lkey", "refs", "remap", "status", "ctr")
+
+
+def test_page_experiment(db, oracle):
+    fx = load_golden("mr_hand_cases.json")["mutation_experiment"]
+    base = h(fx["alloc_base"])
+    t = EMPTY
+    for c in fx["register_calls"]:
+        q = np.array([[base + h(c["off"]), c["size"]]], np.uint64)
+        r = register(db, q, [c["new_lkey"]], *t)
+        assert r["kind"].tolist() == [c["kind"]] and r["handle"].tolist() == [c["handle"]]
+        assert r["refs"].tolist() == c["refs_after"]
+        t = (r["start"], r["end"], r["lkey"], r["refs"])
+    dr = fx["deregister_batch"]
+    d = deregister(db, dr["handles"], *t)
+    assert d["status"].tolist() == dr["status"] and d["remap"].tolist() == dr["remap"]
+    assert d["refs"].tolist() == [1] and d["ctr"].tolist() == [1, 1, 0, 0]
+    one = fx["one_batch_reading"]
+    q = np.array([[base + h(c["off"]), c["size"]] for c in fx["register_calls"]], np.uint64)
+    r = register(db, q, [c["new_lkey"] for c in fx["register_calls"]], *EMPTY)
+    assert r["kind"].tolist() == one["kind"] and r["handle"].tolist() == one["handle"]
+    assert [int(x) - base for x in r["end"]] == [h(x["end"]) for x in one["table_after"]]
+
+
+def random_case(rng, n, m, span, granule_shift):
+    g = 1 << granule_shift
+    s = np.sort(rng.integers(0, span, size=n)).astype(np.uint64) * np.uint64(g)
+    e = s + rng.integers(1, 40, size=n).astype(np.uint64) * np.uint64(g)
+    lk = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    refs = rng.integers(1, 5, size=n).astype(np.uint32)
+    a = rng.integers(0, (span + 50) * g, size=m).astype(np.uint64)
+    sz = rng.integers(0, 30 * g, size=m).astype(np.uint64)
+    if n:
+        pick = rng.integers(0, n, size=m)
+        inside = rng.random(m) < 0.4
+        a = np.where(inside, s[pick] + rng.integers(0, g, size=m).astype(np.uint64), a)
+        sz = np.where(inside, (e[pick] - s[pick]) // np.uint64(2), sz)
+    rep = rng.random(m) < 0.25
+    src = rng.integers(0, max(m // 3, 1), size=m)
+    a = np.where(rep, a[src], a)
+    sz = np.where(rep, sz[src], sz)
+    sz[::17] = 0                                   # invalid requests
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = rng.integers(0, 2**32, size=m, dtype=np.uint64).astype(np.uint32)
+    return q, nl, s, e, lk, refs
+
+
+@pytest.mark.parametrize("n,m,span,granule_shift", [
+    (0, 1, 10, 12), (0, 500, 100, 12), (1, 300, 10, 12), (37, 2000, 300, 12),
+    (500, 20000, 5000, 12), (3000, 100000, 20000, 12), (20000, 300000, 400000, 12),
+    (40, 3000, 200, 16), (5000, 200000, 60000, 16),
+])
+def test_register_against_the_oracle(db, oracle, n, m, span, granule_shift):
+    """Overlapping tables; requests held by records, nested, partly
+    overlapping, repeated and invalid; several tiles of the sort."""
+    rng = np.random.default_rng(n * 7 + m + granule_shift)
+    q, nl, s, e, lk, refs = random_case(rng, n, m, span, granule_shift)
+    want = oracle.mr_register(q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    got = register(db, q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    same(got, want, REG_KEYS)
+    kinds = set(want["kind"].tolist())
+    if m >= 300:
+        assert {3, 4, 5} <= kinds and (n == 0 or {1, 2} & kinds)
+
+
+def test_register_empty_batch_and_capacity(db, oracle):
+    rng = np.random.default_rng(3)
+    q, nl, s, e, lk, refs = random_case(rng, 50, 400, 400, 12)
+    got = register(db, q[:0], nl[:0], s, e, lk, refs)
+    same(got, oracle.mr_register(q[:0], nl[:0], s, e, lk, refs), REG_KEYS)
+    want = oracle.mr_register(q, nl, s, e, lk, refs)
+    total = int(want["ctr"][0])
+    small = register(db, q, nl, s, e, lk, refs, out_cap=total - 1)
+    assert small["ctr"].tolist() == [total, int(want["ctr"][1]), 1, 0]
+    assert (small["kind"] == want["kind"]).all()
+    grown = register(db, q, nl, s, e, lk, refs, out_cap=db.mr_capacity_for(total))
+    same(grown, want, REG_KEYS)
+
+
+def test_register_unsorted_table_is_flagged(db):
+    s = np.array([0x3000, 0x1000], np.uint64)
+    e = np.array([0x4000, 0x2000], np.uint64)
+    r = register(db, np.array([[0x1000, 1]], np.uint64), [1], s, e, np.array([1, 2], np.uint32),
+                 np.array([1, 1], np.uint32))
+    assert int(r["ctr"][3]) & db.ERR_TABLE_ORDER
+
+
+def test_register_full_size(db, oracle):
+    """16,777,216 requests against 1,048,576 records (a fifth miss and
+    become about 3.35 M new records)."""
+    import synth
+    d = synth.mr_register()
+    args = (d["queries"], d["new_lkey"], d["mr_start"], d["mr_end"], d["mr_lkey"], d["mr_refs"])
+    got = register(db, *args)
+    want = oracle.mr_register(*args)
+    same(got, want, REG_KEYS)
+
+
+@pytest.mark.parametrize("n,m", [(0, 10), (1, 5), (10, 0), (30, 200), (1000, 5000),
+                                 (70000, 300000)])
+def test_deregister_against_the_oracle(db, oracle, n, m):
+    rng = np.random.default_rng(n + 3 * m)
+    s = np.arange(n, dtype=np.uint64) * np.uint64(0x10000)
+    e = s + np.uint64(0x8000)
+    lk = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    refs = rng.integers(1, 6, size=n).astype(np.uint32)
+    hs = rng.integers(-3, n + 3, size=m).astype(np.int64)
+    hs[: m // 10] = rng.integers(-(2**62), 2**62, size=m // 10)
+    same(deregister(db, hs, s, e, lk, refs), oracle.mr_deregister(hs, s, e, lk, refs),
+         DEREG_KEYS)
+
+
+def test_deregister_full_size(db, oracle):
+    import synth
+    d = synth.mr_deregister()
+    args = (d["handles"], d["mr_start"], d["mr_end"], d["mr_lkey"], d["mr_refs"])
+    want = oracle.mr_deregister(*args)
+    same(deregister(db, *args), want, DEREG_KEYS)
+    assert set(want["status"].tolist()) == {0, 1, 2}
+
+
+def test_a_cache_over_several_batches(db, oracle):
+    """Register, deregister and register again, each batch on the table the
+    previous one left, handles carried forward through remap."""
+    rng = np.random.default_rng(11)
+    q, nl, s, e, lk, refs = random_case(rng, 200, 5000, 3000, 12)
+    t_gpu = t_cpu = (s, e, lk, refs)
+    for step in range(3):
+        r = register(db, q, nl, *t_gpu)
+        w = oracle.mr_register(q, nl, *t_cpu)
+        same(r, w, REG_KEYS)
+        t_gpu = (r["start"], r["end"], r["lkey"], r["refs"])
+        t_cpu = (w["start"], w["end"], w["lkey"], w["refs"])
+        held = r["handle"][r["handle"] >= 0]
+        hs = np.concatenate([held, held[: held.shape[0] // 2]])
+        rng.shuffle(hs)
+        d = deregister(db, hs, *t_gpu)
+        v = oracle.mr_deregister(hs, *t_cpu)
+        same(d, v, DEREG_KEYS)
+        t_gpu = (d["start"], d["end"], d["lkey"], d["refs"])
+        t_cpu = (v["start"], v["end"], v["lkey"], v["refs"])
+        q, nl = q[::-1].copy(), nl[::-1].copy()
+
+
+def test_argument_checks(db):
+    z = torch.zeros(4, dtype=torch.int64, device="cuda")
+    z32 = torch.zeros(4, dtype=torch.int32, device="cuda")
+    q = torch.zeros((1, 2), dtype=torch.int64, device="cuda")
+    ws = db.workspace(db.mr_register_workspace_size(1, 4))
+    with pytest.raises(db.DescBuildError):             # granule neither 4 KiB nor 64 KiB
+        db.mr_register(q, z32[:1], z, z, z32, z32, z, z, z32, z32, z[:1],
+                       torch.zeros(1, dtype=torch.uint8, device="cuda"), z, ws, granule_shift=13)
+    with pytest.raises(db.DescBuildError) as e:        # workspace too small
+        db.mr_register(q, z32[:1], z, z, z32, z32, z, z, z32, z32, z[:1],
+                       torch.zeros(1, dtype=torch.uint8, device="cuda"), z, ws[:256])
+    assert e.value.code == -28
