@@ -767,45 +767,53 @@ def run_e2e(st, stream, inp, K, device, dist, world):
 
 
 # ------------------------------------------------------------ CPU baseline
-def cpu_baseline(inp, scale: int = 1) -> dict:
+def cpu_baseline(inp, repeats: int = 3) -> dict:
     """The oracle as it stands (single-threaded C++) on a bounded sample of
-    each workload; value in the same unit, scaled by the sample sizes.
-    ``scale`` divides the sample sizes. Output buffers that scale with the
-    ring or arena size are allocated outside the timed calls."""
+    each workload: every request of prp_small, mr_lookup and put_bucket and
+    the first 524,288 of prp_large (their lists, 2 GB, are written into a
+    host arena), each timed `repeats` times (median); the value is one full
+    step's requests over the time those rates give for it. Output buffers
+    that scale with the ring or arena size are allocated outside the timed
+    calls."""
     import oracle
     s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
-    samples = {"prp_small": 262_144 // scale, "prp_large": 65_536 // scale,
-               "mr_lookup": 1_048_576 // scale, "put_bucket": 1_048_576 // scale}
-    secs = {}
-    t = time.perf_counter()
-    oracle.prp_build(s["req"][:samples["prp_small"]], s["lut"], s["heap_size"],
-                     s["arena_base"], 1, lists=False)
-    secs["prp_small"] = time.perf_counter() - t
+    u = units(inp)
+    samples = {"prp_small": u["prp_small"], "prp_large": min(524_288, u["prp_large"]),
+               "mr_lookup": u["mr_lookup"], "put_bucket": u["put_bucket"]}
     req = l["req"][:samples["prp_large"]]
     need = int(oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], 1 << 40,
                                 lists=False)["ctr"][0])
     arena = np.zeros((need, 512), dtype=np.uint64)
-    t = time.perf_counter()
-    oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"], need, arena=arena)
-    secs["prp_large"] = time.perf_counter() - t
-    t = time.perf_counter()
-    oracle.mr_bsearch(m["queries"][:samples["mr_lookup"]], m["mr_start"], m["mr_end"],
-                      m["mr_lkey"])
-    secs["mr_lookup"] = time.perf_counter() - t
     rings = np.zeros((p["world"] * p["n_qp"], p["depth"], 64), dtype=np.uint8)
-    t = time.perf_counter()
-    oracle.wqe_bucket(p["req"][:samples["put_bucket"]], p["peer_ptrs"], p["rkeys"], p["world"],
-                      p["n_qp"], p["local_base"], p["lkey"], p["heap_size"], p["depth"],
-                      p["head"], rings=rings)
-    secs["put_bucket"] = time.perf_counter() - t
+    calls = {
+        "prp_small": lambda: oracle.prp_build(s["req"][:samples["prp_small"]], s["lut"],
+                                              s["heap_size"], s["arena_base"], 1, lists=False),
+        "prp_large": lambda: oracle.prp_build(req, l["lut"], l["heap_size"], l["arena_base"],
+                                              need, arena=arena),
+        "mr_lookup": lambda: oracle.mr_bsearch(m["queries"][:samples["mr_lookup"]], m["mr_start"],
+                                               m["mr_end"], m["mr_lkey"]),
+        "put_bucket": lambda: oracle.wqe_bucket(p["req"][:samples["put_bucket"]], p["peer_ptrs"],
+                                                p["rkeys"], p["world"], p["n_qp"], p["local_base"],
+                                                p["lkey"], p["heap_size"], p["depth"], p["head"],
+                                                rings=rings),
+    }
+    secs = {}
+    for k, fn in calls.items():
+        ts = []
+        for _ in range(repeats):
+            t = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t)
+        secs[k] = statistics.median(ts)
     # Time for one full step's requests at the sampled per-request rates.
-    u = units(inp)
     step_s = sum(secs[k] * u[k] / samples[k] for k in u)
     return {"value": round(sum(u.values()) / step_s / 1e6, 3), "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": "first %d prp_small, %d prp_large (lists written), %d mr_lookup "
-                      "(binary-search oracle), %d put_bucket requests; per-workload rates "
-                      "scaled to one full step" % tuple(samples[k] for k in u),
+            "sample": "all %d prp_small, the first %d prp_large (lists written), all %d "
+                      "mr_lookup (binary-search oracle) and all %d put_bucket requests, each "
+                      "timed %d times (median); per-workload rates scaled to one full step"
+                      % (samples["prp_small"], samples["prp_large"], samples["mr_lookup"],
+                         samples["put_bucket"], repeats),
             "seconds": {k: round(v, 4) for k, v in secs.items()}}
 
 
@@ -815,11 +823,11 @@ def run_reference(args):
     workload on the host cores, same metric and unit as our arm."""
     inp = make_inputs()
     for _ in range(args.warmup):
-        cpu_baseline(inp)
+        cpu_baseline(inp, repeats=1)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(inp))
+        vals.append(cpu_baseline(inp, repeats=1))
     wall = time.perf_counter() - t0
     v = round(statistics.median(x["value"] for x in vals), 3)
     reqs = sum(units(inp).values())

@@ -45,6 +45,9 @@ namespace mr {
 #ifndef DB_MR_BUCKET_SHIFT
 #define DB_MR_BUCKET_SHIFT 0
 #endif
+#ifndef DB_MR_BUCKET_DOWN
+#define DB_MR_BUCKET_DOWN 1  // log2 of records per bucket (measured best: two)
+#endif
 constexpr int kBuildThreads = 256;
 constexpr int kThreads = DB_MR_THREADS;
 constexpr int kQPT = DB_MR_QPT;
@@ -68,7 +71,7 @@ constexpr size_t kHeaderBytes = 256;
 
 inline uint32_t buckets_for(uint64_t n_mr) {
   uint64_t nb = 1024;
-  while (nb < (n_mr << DB_MR_BUCKET_SHIFT) && nb < (1u << 22)) nb <<= 1;
+  while (nb < ((n_mr << DB_MR_BUCKET_SHIFT) >> DB_MR_BUCKET_DOWN) && nb < (1u << 22)) nb <<= 1;
   return (uint32_t)nb;
 }
 // Directory entry of bucket b: the records starting below the bucket
