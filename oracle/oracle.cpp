@@ -160,8 +160,16 @@ uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_
     slot += 1;
   }
   if (page + 1 != n_list) fail("list page count mismatch");
-  if (zero_tail)
+  if (zero_tail) {
     for (; slot < kListSlots; ++slot) list[page * kListSlots + slot] = 0;
+  } else {
+    // Reading: the slots that share the last entry's 32-byte sector (four
+    // slots from the page start) are written as 0; the rest are untouched.
+    while (slot % 4 != 0) {
+      list[page * kListSlots + slot] = 0;
+      slot += 1;
+    }
+  }
   return n_list;
 }
 

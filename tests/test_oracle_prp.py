@@ -59,8 +59,10 @@ def brute_force_pages(off, length, lut):
 
 
 def data_entries(prp1, prp2, lst, n_list, arena_base, page_base, fill=0):
-    """The page entries a request describes, chain pointers removed. Slots
-    of the last list page holding ``fill`` were never written."""
+    """The page entries a request describes, chain pointers removed. On the
+    last list page the entries end at the first slot holding ``fill`` (never
+    written) or 0 (the padding of the last entry's 32-byte sector; no entry
+    is 0, since LUT values are non-zero)."""
     if n_list == 0:
         return [prp1] + ([prp2] if prp2 else [])
     out = [prp1]
@@ -70,7 +72,7 @@ def data_entries(prp1, prp2, lst, n_list, arena_base, page_base, fill=0):
             if s == 511 and j + 1 < n_list:
                 assert v == arena_base + (page_base + j + 1) * PAGE
                 continue
-            if j + 1 == n_list and v == fill:
+            if j + 1 == n_list and (v == fill or v == 0):
                 break
             out.append(v)
     return out
@@ -102,11 +104,14 @@ def test_brute_force_tiny_heaps(oracle):
         n = len(pages)
         if n >= 3:
             assert prp2 == A + pb * PAGE
-        # Unused slots of the last list page stay untouched.
+        # Unused slots of the last list page stay untouched, except those in
+        # the last entry's 32-byte sector, which are 0.
         if n_list:
             used = (n - 1) - 511 * (n_list - 1)
             assert 1 <= used <= 512
-            assert (lst[-1, used:] == 0xAAAAAAAAAAAAAAAA).all()
+            pad = -used % 4
+            assert (lst[-1, used:used + pad] == 0).all()
+            assert (lst[-1, used + pad:] == 0xAAAAAAAAAAAAAAAA).all()
 
 
 def test_page_count_boundaries(oracle):
@@ -172,6 +177,28 @@ def test_zero_tail(oracle):
     # request 1: n = 601, 600 entries -> 511 + ptr, then 89 entries + zeros
     assert (out["arena"][2, 89:] == 0).all() and (out["arena"][2, :89] != 0).all()
     assert (out["arena"][3:] == 7).all()
+
+
+def test_last_sector_padding(oracle):
+    """Without DB_PRP_ZERO_TAIL the slots after the last entry up to the end
+    of its 32-byte sector (a multiple of four slots) are 0; later slots keep
+    what the arena held."""
+    rng = np.random.default_rng(6)
+    heap = 8 * 1024 * 1024
+    lut = random_lut(rng, heap // 65536)
+    FILL = 7
+    req = np.array([[0, 20 * PAGE], [0, 21 * PAGE], [4, 600 * PAGE], [0, 5 * PAGE]],
+                   dtype=np.uint64)
+    out = oracle.prp_build(req, lut, heap, 0x1000000, 8, fill=FILL)
+    a = out["arena"]
+    # 19 entries: slot 19 completes the sector
+    assert (a[0, :19] != 0).all() and a[0, 19] == 0 and (a[0, 20:] == FILL).all()
+    # 20 entries: the sector ends with the list
+    assert (a[1, :20] != 0).all() and (a[1, 20:] == FILL).all()
+    # 600 entries: 511 + pointer, then 89 entries and three slots of padding
+    assert (a[3, :89] != 0).all() and (a[3, 89:92] == 0).all() and (a[3, 92:] == FILL).all()
+    # 4 entries: exactly one sector
+    assert (a[4, :4] != 0).all() and (a[4, 4:] == FILL).all()
 
 
 def test_empty_batch(oracle):
