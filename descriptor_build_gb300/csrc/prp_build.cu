@@ -180,7 +180,9 @@ __device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, u
                                           uint64_t pol_out) {
   uint64_t* const dst0 = p.arena + (it.pb << 9) + 4 * lane;
   const uint32_t W = it.words;
-  const uint32_t total = p.zero_tail ? (it.pages << 9) : W;
+  // Words written: the list, then 0 up to the end of its last 32-byte sector
+  // (no partial-sector writes), or the whole last page with zeroed tails.
+  const uint32_t total = p.zero_tail ? (it.pages << 9) : ((W + 3u) & ~3u);
   const uint64_t c0 = it.hb >> 16;
   const uint64_t c_last = last_chunk(it);
   const uint32_t p0 = first_pos(it);
@@ -277,7 +279,7 @@ __device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, 
   const int g = lane & 7, g0 = lane & ~7;
   const uint32_t p0 = first_pos(it);
   uint64_t* dst = p.arena + (it.pb << 9);
-  const uint32_t total = p.zero_tail ? 512u : it.words;
+  const uint32_t total = p.zero_tail ? 512u : ((it.words + 3u) & ~3u);  // whole sectors
   const uint32_t steps = p.zero_tail ? 16u : 1u;  // the same for every group of the warp
   for (uint32_t st = 0; st < steps; ++st) {
     const uint32_t w = st * 32 + 4 * g;

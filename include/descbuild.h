@@ -143,7 +143,10 @@ typedef struct db_counters {
  *   arena_base       bus address of list page 0; a multiple of 4096
  *   arena_cap_pages  pages the arena holds
  *   arena            [arena_cap_pages][512] uint64: the arena's contents (32-byte aligned).
- *                    Unused slots are left as they were unless DB_PRP_ZERO_TAIL.
+ *                    Unused slots of a list's last page are left as they were,
+ *                    except the ones sharing the last entry's 32-byte sector
+ *                    (at most three), which are written as 0, so that every
+ *                    list ends on a whole sector; DB_PRP_ZERO_TAIL zeroes them all.
  *   prp              [n] output (16-byte aligned)
  *   page_base        [n] output or NULL
  *   status           [n] output (DB_PRP_*) or NULL
