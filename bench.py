@@ -1,7 +1,9 @@
 """Throughput of batched GPU-range -> DMA-descriptor translation on one GB300.
 
 One step runs every part of the hot path once, each on its full-size seeded
-synthetic workload, all on one CUDA stream:
+synthetic workload. The four batches are independent: each runs on its own
+CUDA stream, forked together and joined at the end of the step (--serial:
+one stream, in turn):
 
   prp_small   db_prp_build, 1,048,576 small requests (1 GiB heap)
   prp_large   db_prp_build, 4,194,304 requests, chained lists (16 GiB heap)
@@ -9,9 +11,9 @@ synthetic workload, all on one CUDA stream:
   put_bucket  db_wqe_bucket, 8,388,608 puts into 32 rings of 2^19 WQEs
 
 ``value`` is requests translated per second over the whole step (all four
-batches), with inputs resident in HBM. Each kernel call is also timed alone
-with CUDA events on the launch stream; the dominant one (prp_large) gives the
-roofline line. ``e2e`` repeats the step through the same API with inputs in
+batches), with inputs resident in HBM. Each call is also timed with CUDA
+events alone on the stream, in the same steps run one call at a time after
+the timed region; the dominant one (prp_large) gives the roofline line. ``e2e`` repeats the step through the same API with inputs in
 pinned host memory and every descriptor copied back to the host. ``next``
 times, on its own and outside the step, the rows built after the hot path:
 the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm, without and
@@ -44,6 +46,8 @@ sys.path.insert(0, ROOT)
 METRIC = "M requests/s translated + achieved HBM GB/s as % of GB300 peak"
 UNIT = "M requests/s"
 WORKLOAD = "descriptor batch: prp_small + prp_large + mr_lookup + put_bucket (full sizes)"
+# Launch order of a step's calls on their own streams (measured best on GB300).
+SCHEDULE = ("mr_lookup", "prp_small", "put_bucket", "prp_large")
 
 
 def parse():
@@ -60,6 +64,9 @@ def parse():
                     help="profiling aid: run one workload only (not a bench line)")
     ap.add_argument("--fraction", type=float, default=1.0,
                     help="profiling aid: keep this leading fraction of each batch")
+    ap.add_argument("--serial", action="store_true",
+                    help="run a step's four calls one after another on one stream "
+                         "(default: each on its own stream, all at once)")
     ap.add_argument("--next-only", choices=["mr_register", "mr_deregister"],
                     help="profiling aid: time one of the rows after the hot path, alone")
     return ap.parse_args()
@@ -637,12 +644,33 @@ def run_ours(args, inp, world, device, dist):
     torch.cuda.set_device(device)
     st = Step(db, torch, inp, device)
     stream = torch.cuda.Stream(device=device)
-    calls = st.calls()
     ev = lambda: torch.cuda.Event(enable_timing=True)
+    # The four calls are independent batches with their own buffers and
+    # workspaces: each runs on its own stream and a step forks them together
+    # and joins them (the MR lookup, bound by L2 requests, and the latency-bound
+    # small PRP batch overlap the HBM-bound ones). --serial runs them in turn.
+    calls = st.calls()
+    if not args.serial:
+        rank_of = {k: i for i, k in enumerate(SCHEDULE)}
+        calls = sorted(calls, key=lambda c: rank_of[c[0]])
+    streams = [stream if args.serial else torch.cuda.Stream(device=device) for _ in calls]
+
+    def one_step(call_ev, fork, join):
+        fork.record(stream)
+        for j, (_, fn) in enumerate(calls):
+            s = streams[j]
+            if s is not stream:
+                s.wait_event(fork)
+            call_ev[j][0].record(s)
+            fn(s)
+            call_ev[j][1].record(s)
+        for j in range(len(calls)):
+            if streams[j] is not stream:
+                stream.wait_event(call_ev[j][1])
+        join.record(stream)
 
     for _ in range(args.warmup):
-        for _, fn in calls:
-            fn(stream)
+        one_step([(ev(), ev()) for _ in calls], ev(), ev())
     torch.cuda.synchronize(device)
     st.check_counters()
 
@@ -657,21 +685,32 @@ def run_ours(args, inp, world, device, dist):
         t1 = ev()
         t0.record(stream)
         for k in range(K):
-            step_ev[k][0].record(stream)
-            for j, (_, fn) in enumerate(calls):
-                evs[k][j][0].record(stream)
-                fn(stream)
-                evs[k][j][1].record(stream)
-            step_ev[k][1].record(stream)
+            one_step(evs[k], step_ev[k][0], step_ev[k][1])
         t1.record(stream)
         torch.cuda.synchronize(device)
     total_ms = max_over_ranks(dist, t0.elapsed_time(t1), device)
     if dist:
         dist.barrier()
     st.check_counters()
-    per_kernel_ms = {name: statistics.mean(evs[k][j][0].elapsed_time(evs[k][j][1])
-                                           for k in range(K))
-                     for j, (name, _) in enumerate(calls)}
+    span_ms = {name: statistics.mean(evs[k][j][0].elapsed_time(evs[k][j][1]) for k in range(K))
+               for j, (name, _) in enumerate(calls)}
+    if args.serial:
+        per_kernel_ms = span_ms
+    else:
+        # A concurrent call's span includes waiting for SMs the others hold, so
+        # each call's own time comes from the same steps run one call at a time.
+        sev = [[(ev(), ev()) for _ in calls] for _ in range(K)]
+        torch.cuda.synchronize(device)
+        for k in range(K):
+            for j, (_, fn) in enumerate(calls):
+                sev[k][j][0].record(stream)
+                fn(stream)
+                sev[k][j][1].record(stream)
+        torch.cuda.synchronize(device)
+        st.check_counters()
+        per_kernel_ms = {name: statistics.mean(sev[k][j][0].elapsed_time(sev[k][j][1])
+                                               for k in range(K))
+                         for j, (name, _) in enumerate(calls)}
 
     u = units(inp)
     alg = algorithmic_bytes(inp)
@@ -686,6 +725,8 @@ def run_ours(args, inp, world, device, dist):
         kernels[name] = {"ms": round(ms, 4), "M_req_per_s": round(u[name] / ms / 1e3, 2),
                          "algorithmic_bytes": alg[name], "GB_per_s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4), "launches": Step.LAUNCHES[name]}
+        if not args.serial:
+            kernels[name]["concurrent_span_ms"] = round(span_ms[name], 4)
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     traffic = recorded_traffic("prp_build.cu", "prp_build_kernel") if dom.startswith("prp") \
         else None
@@ -703,51 +744,91 @@ def run_ours(args, inp, world, device, dist):
                       "per_workload_requests": u,
                       "l2": "inputs larger than L2: each step streams ~6 GB, so every "
                             "kernel's inputs are evicted before its next launch",
-                      "parallelism": f"replicas x{world}"},
+                      "parallelism": f"replicas x{world}",
+                      "schedule": ("one stream, the four calls in turn" if args.serial else
+                                   "four streams, forked and joined each step; launch order "
+                                   + ", ".join(n for n, _ in calls)
+                                   + "; per-call times and the roofline from the same steps "
+                                     "run one call at a time after the timed region")},
            "kernels": kernels, "roofline": roof,
-           "gpu_launches": K * sum(Step.LAUNCHES[k] for k in u),
+           "gpu_launches": K * sum(Step.LAUNCHES[k] for k in u),  # in the timed region
            "clocks": clk.summary()}
     if not args.no_e2e:
-        out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world)
+        out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world,
+                             serial=args.serial)
     return out
 
 
-def run_e2e(st, stream, inp, K, device, dist, world):
+def run_e2e(st, stream, inp, K, device, dist, world, serial=False):
     """The same step through the API with host buffers: pinned host inputs are
-    copied in, every descriptor the step produces is copied back out."""
+    copied in, every descriptor the step produces is copied back out. Each
+    workload runs on its own stream (copy in, call, copy out), the four
+    forked together as in the device-resident step; an output above 1 GiB is
+    copied back in four pieces on streams of their own, so that more than one
+    copy engine moves it."""
     import torch
     t = torch
     pin = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).pin_memory()
     pin32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).pin_memory()
-    h_in, outs = [], []
+    groups = {}
     for k in ("prp_small", "prp_large"):
         if k in st.bufs:
             b, w = st.bufs[k], inp[k]
-            h_in += [(pin(w["req"]), b["req"]), (pin(w["lut"]), b["lut"])]
-            outs += [b["prp"], b["ctr"]] + ([b["arena"][:b["cap"]]] if b["cap"] else [])
+            groups[k] = ([(pin(w["req"]), b["req"]), (pin(w["lut"]), b["lut"])],
+                         [b["prp"], b["ctr"]] + ([b["arena"][:b["cap"]]] if b["cap"] else []))
     if "mr_lookup" in st.bufs:
         b, m = st.bufs["mr_lookup"], inp["mr_lookup"]
-        h_in += [(pin(m["queries"]), b["q"]), (pin(m["mr_start"]), b["start"]),
-                 (pin(m["mr_end"]), b["end"]), (pin32(m["mr_lkey"]), b["lkey"])]
-        outs += [b["idx"], b["olkey"], b["kind"], b["ctr"]]
+        groups["mr_lookup"] = ([(pin(m["queries"]), b["q"]), (pin(m["mr_start"]), b["start"]),
+                                (pin(m["mr_end"]), b["end"]), (pin32(m["mr_lkey"]), b["lkey"])],
+                               [b["idx"], b["olkey"], b["kind"], b["ctr"]])
     if "put_bucket" in st.bufs:
         b, p = st.bufs["put_bucket"], inp["put_bucket"]
-        h_in += [(pin(p["req"]), b["req"]), (pin(p["peer_ptrs"]), b["peer"]),
-                 (pin32(p["rkeys"]), b["rkeys"])]
-        outs += [b["rings"], b["head"], b["count"], b["ctr"]]
-    h_out = [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    bi = sum(h.numel() * h.element_size() for h, _ in h_in)
-    bo = sum(o.numel() * o.element_size() for o in outs)
-    calls = st.calls()
+        groups["put_bucket"] = ([(pin(p["req"]), b["req"]), (pin(p["peer_ptrs"]), b["peer"]),
+                                 (pin32(p["rkeys"]), b["rkeys"])],
+                                [b["rings"], b["head"], b["count"], b["ctr"]])
+    h_out = {k: [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+             for k, (_, outs) in groups.items()}
+    bi = sum(h.numel() * h.element_size() for h_in, _ in groups.values() for h, _ in h_in)
+    bo = sum(o.numel() * o.element_size() for _, outs in groups.values() for o in outs)
+    calls = dict(st.calls())
+    order = [k for k in SCHEDULE if k in groups]
+    streams = {k: (stream if serial else t.cuda.Stream(device=device)) for k in order}
+    pieces = [t.cuda.Stream(device=device) for _ in range(4)]
+    big = 1 << 30
 
     def one():
-        with t.cuda.stream(stream):
-            for h, d in h_in:
-                d.copy_(h, non_blocking=True)
-            for _, fn in calls:
-                fn(stream)
-            for o, h in zip(outs, h_out):
-                h.copy_(o, non_blocking=True)
+        fork = t.cuda.Event()
+        fork.record(stream)
+        done = []
+        for k in order:
+            s = streams[k]
+            if s is not stream:
+                s.wait_event(fork)
+            with t.cuda.stream(s):
+                for h, d in groups[k][0]:
+                    d.copy_(h, non_blocking=True)
+                calls[k](s)
+                for o, h in zip(groups[k][1], h_out[k]):
+                    n = o.numel() * o.element_size()
+                    if n < big or serial:
+                        h.copy_(o, non_blocking=True)
+                        continue
+                    ready = t.cuda.Event()
+                    ready.record(s)
+                    rows = o.shape[0]
+                    for i, ps in enumerate(pieces):
+                        lo, hi = rows * i // len(pieces), rows * (i + 1) // len(pieces)
+                        ps.wait_event(ready)
+                        with t.cuda.stream(ps):
+                            h[lo:hi].copy_(o[lo:hi], non_blocking=True)
+                        e = t.cuda.Event()
+                        e.record(ps)
+                        done.append(e)
+            e = t.cuda.Event()
+            e.record(s)
+            done.append(e)
+        for e in done:
+            stream.wait_event(e)
 
     one()
     t.cuda.synchronize(device)
