@@ -857,6 +857,7 @@ def cpu_baseline(inp, repeats: int = 3) -> dict:
     that scale with the ring or arena size are allocated outside the timed
     calls."""
     import oracle
+    oracle.build()  # compiled (if need be) before anything is timed
     s, l, m, p = inp["prp_small"], inp["prp_large"], inp["mr_lookup"], inp["put_bucket"]
     u = units(inp)
     samples = {"prp_small": u["prp_small"], "prp_large": min(524_288, u["prp_large"]),
@@ -866,6 +867,8 @@ def cpu_baseline(inp, repeats: int = 3) -> dict:
                                 lists=False)["ctr"][0])
     arena = np.zeros((need, 512), dtype=np.uint64)
     rings = np.zeros((p["world"] * p["n_qp"], p["depth"], 64), dtype=np.uint8)
+    arena.fill(0)  # fault the pages in before the timed calls
+    rings.fill(0)
     calls = {
         "prp_small": lambda: oracle.prp_build(s["req"][:samples["prp_small"]], s["lut"],
                                               s["heap_size"], s["arena_base"], 1, lists=False),
