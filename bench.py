@@ -67,7 +67,8 @@ def parse():
     ap.add_argument("--serial", action="store_true",
                     help="run a step's four calls one after another on one stream "
                          "(default: each on its own stream, all at once)")
-    ap.add_argument("--next-only", choices=["mr_register", "mr_deregister"],
+    ap.add_argument("--next-only", choices=["mr_register", "mr_deregister", "put_bucket_vmm",
+                                            "put_bucket_vmm_psn", "mr_lookup_overlap"],
                     help="profiling aid: time one of the rows after the hot path, alone")
     return ap.parse_args()
 
@@ -318,6 +319,18 @@ def run_next(args, device) -> dict:
     deregistration batches (db_mr_register, db_mr_deregister) and the CQ
     mirror (db_cq_mirror)."""
     import torch as t
+    stream = t.cuda.Stream(device=device)
+    out = time_vmm(args, device, stream)
+    out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
+    out.update(time_mr_mutation(args, device, stream))
+    out["cq_mirror"] = time_cq_mirror(args, device)
+    return out
+
+
+def time_vmm(args, device, stream, only=None) -> dict:
+    """db_wqe_bucket_vmm on the put batch over 2 MiB chunks, without and with
+    packet sequence numbers (mtu 4096)."""
+    import torch as t
     import descriptor_build_gb300 as db
     import synth
     P = synth.put_bucket_vmm()
@@ -331,10 +344,13 @@ def run_next(args, device) -> dict:
              head=d64(P["head"]), count=t.empty(R, dtype=t.int32, device=device),
              ctr=t.zeros(4, dtype=t.int64, device=device),
              psn=t.zeros(R, dtype=t.int64, device=device),
-             ws=db.workspace(db.wqe_workspace_size(n, R), device))
-    stream = t.cuda.Stream(device=device)
+             ws=db.workspace(db.wqe_vmm_workspace_size(n, P["world"], P["n_qp"],
+                                                       P["heap_size"], P["chunk_shift"]), device))
     out = {}
     for name, mtu in (("put_bucket_vmm", 0), ("put_bucket_vmm_psn", 4096)):
+        if only and name != only:
+            continue
+
         def call():
             db.wqe_bucket_vmm(b["req"], b["raddr"], b["rkey"], b["lkey"], P["chunk_shift"],
                               P["world"], P["n_qp"], P["local_base"], P["heap_size"], b["rings"],
@@ -362,11 +378,8 @@ def run_next(args, device) -> dict:
         out[name] = {
             "ms": round(ms, 4), "M_req_per_s": round(n / ms / 1e3, 2), "wqes": wqes,
             "chunk_bytes": 1 << P["chunk_shift"], "mtu": mtu, "algorithmic_bytes": alg,
-            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 3,
+            "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 4,
             "note": "not part of the step: timed alone, same stream discipline"}
-    out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
-    out.update(time_mr_mutation(args, device, stream))
-    out["cq_mirror"] = time_cq_mirror(args, device)
     return out
 
 
@@ -946,8 +959,13 @@ def main():
     if args.next_only:
         if rank == 0:
             import torch as t
-            res = time_mr_mutation(args, device, t.cuda.Stream(device=device),
-                                   only=args.next_only)
+            s = t.cuda.Stream(device=device)
+            if args.next_only.startswith("put_bucket_vmm"):
+                res = time_vmm(args, device, s, only=args.next_only)
+            elif args.next_only == "mr_lookup_overlap":
+                res = {"mr_lookup_overlap": time_mr_overlap(args, device, s)}
+            else:
+                res = time_mr_mutation(args, device, s, only=args.next_only)
             print(json.dumps({"next_only": args.next_only, **res,
                               "note": "profiling aid: not a bench line"}), flush=True)
         return

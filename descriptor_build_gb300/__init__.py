@@ -29,7 +29,7 @@ from . import build as _build
 __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
-    "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
+    "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_vmm_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
     "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "cq_slots", "cq_slot_fields",
     "mr_capacity_for", "mr_register_workspace_size", "mr_register",
     "mr_deregister_workspace_size", "mr_deregister", "MR_NEW", "MR_NEW_DUP", "DEREG_OK",
@@ -72,6 +72,8 @@ def _load():
     lib.db_mr_lookup.argtypes = [vp, u64, vp, vp, vp, u64, vp, vp, vp, vp, vp, sz, vp]
     lib.db_mr_lookup_overlap.argtypes = lib.db_mr_lookup.argtypes
     lib.db_wqe_workspace_size.argtypes = [u64, u32, psz]
+    lib.db_wqe_vmm_workspace_size.argtypes = [u64, u32, u32, u64, u32, psz]
+    lib.db_wqe_vmm_workspace_size.restype = i32
     lib.db_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64, vp, vp, vp,
                                   vp, sz, vp]
     lib.db_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64, vp, u64, vp,
@@ -271,6 +273,12 @@ def mr_deregister(handle: torch.Tensor, start: torch.Tensor, end: torch.Tensor,
 # --------------------------------------------------------------- WQE bucketing
 def wqe_workspace_size(n: int, n_rings: int) -> int:
     return _size(_lib.db_wqe_workspace_size, n, n_rings)
+
+
+def wqe_vmm_workspace_size(n: int, world: int, n_qp: int, heap_size: int,
+                           chunk_shift: int) -> int:
+    """Workspace bytes of db_wqe_bucket_vmm (columns plus the packed chunk tables)."""
+    return _size(_lib.db_wqe_vmm_workspace_size, n, world, n_qp, heap_size, chunk_shift)
 
 
 def wqe_bucket(req: torch.Tensor, peer_ptrs: torch.Tensor, rkeys: torch.Tensor, world: int,

@@ -69,6 +69,12 @@ inline size_t column_bytes(uint64_t n, uint32_t R) {
 inline size_t ws_bytes_for(uint64_t n, uint32_t R) {
   return kCountsOff + 2 * column_bytes(n, R);
 }
+// A VMM heap's chunk tables, packed after the columns: one 16-byte record
+// {remote address, rkey | lkey << 32} per (PE, chunk).
+inline size_t vmm_table_off(uint64_t n, uint32_t R) { return (ws_bytes_for(n, R) + 255) & ~(size_t)255; }
+inline size_t vmm_ws_bytes_for(uint64_t n, uint32_t R, uint32_t world, uint64_t n_chunks) {
+  return vmm_table_off(n, R) + (size_t)world * n_chunks * 16;
+}
 
 struct Params {
   const ulonglong2* req;
@@ -97,6 +103,7 @@ struct Params {
   const uint64_t* chunk_raddr;  // [world][n_chunks]
   const uint32_t* chunk_rkey;   // [world][n_chunks]
   const uint32_t* chunk_lkey;   // [n_chunks]
+  ulonglong2* chunk_pack;       // [world][n_chunks]: the three, one record each
   // Packet sequence numbers (mtu != 0): one column of per-tile PSN counts
   // per bin, the PSN heads before the call and each ring's PSN total.
   uint32_t mtu;
@@ -463,11 +470,25 @@ inline int vmm_scatter_warps(uint32_t V) {
 }
 inline size_t vmm_scatter_smem(uint32_t V) { return cta_smem(V) + vmm_scatter_warps(V) * vmm_warp_smem(V); }
 
+// The chunk tables packed per call: record (pe, c) = {chunk_raddr[pe][c],
+// chunk_rkey[pe][c] | chunk_lkey[c] << 32}, so a WQE reads its chunk's three
+// values with one L2 request instead of three.
+__global__ void vmm_pack_kernel(const Params p) {
+  const uint64_t total = (uint64_t)p.world * p.n_chunks;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t c = i % p.n_chunks;
+    p.chunk_pack[i] = make_ulonglong2(p.chunk_raddr[i],
+                                      (uint64_t)p.chunk_rkey[i] | ((uint64_t)p.chunk_lkey[c] << 32));
+  }
+}
+
 __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const uint32_t V = p.V, R = p.R;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint64_t pol_first = policy_evict_first();
+  const uint64_t pol_last = policy_evict_last();
   uint64_t* s_slots = reinterpret_cast<uint64_t*>(smem);
   unsigned char* w = smem + cta_smem(V) + warp * vmm_warp_smem(V);
   ulonglong2* s_put = reinterpret_cast<ulonglong2*>(w);
@@ -628,10 +649,11 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
     const uint64_t end = ((c + 1) << p.cshift) < stop ? ((c + 1) << p.cshift) : stop;
     unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6)) + 32 * h;
     if (h == 0) {
-      const uint64_t rc = (uint64_t)pe * p.n_chunks + c;
-      st_stream32(d, __ldg(p.chunk_raddr + rc) + (start & (C - 1)), p.local_base + start,
-                  (end - start) | ((uint64_t)__ldg(p.chunk_lkey + c) << 32),
-                  (uint64_t)__ldg(p.chunk_rkey + rc), pol_first);
+      // one 16-byte read for the chunk's remote address, rkey and lkey
+      const ulonglong2 ck = ld_table16(p.chunk_pack + (uint64_t)pe * p.n_chunks + c, pol_last);
+      st_stream32(d, ck.x + (start & (C - 1)), p.local_base + start,
+                  (end - start) | (ck.y & 0xFFFFFFFF00000000ull), ck.y & 0xFFFFFFFFull,
+                  pol_first);
     } else {
       // u32 batch index at byte 40, first PSN at byte 44
       uint64_t w5 = t0 + o;
@@ -667,6 +689,17 @@ int prepare_scatter() {
 }  // namespace db
 
 using namespace db;
+
+extern "C" int db_wqe_vmm_workspace_size(uint64_t n, uint32_t world, uint32_t n_qp,
+                                         uint64_t heap_size, uint32_t chunk_shift,
+                                         size_t* bytes) {
+  if (!bytes || world == 0 || n_qp == 0 || (uint64_t)world * n_qp > wqe::kMaxRings) return -EINVAL;
+  if (chunk_shift < 4 || chunk_shift > 48 || heap_size == 0 || n >= (1ull << 32)) return -EINVAL;
+  const uint64_t n_chunks = ((heap_size - 1) >> chunk_shift) + 1;
+  if (n_chunks > (1ull << 32)) return -EINVAL;
+  *bytes = wqe::vmm_ws_bytes_for(n, world * n_qp, world, n_chunks);
+  return 0;
+}
 
 extern "C" int db_wqe_workspace_size(uint64_t n, uint32_t n_rings, size_t* bytes) {
   if (!bytes || n_rings == 0 || n_rings > wqe::kMaxRings || n >= (1ull << 32)) return -EINVAL;
@@ -728,6 +761,14 @@ int setup(wqe::Params& p, const db_put_req* req, uint64_t n, uint32_t world, uin
 int run(const wqe::Params& p, cudaStream_t s) {
   int rc = wqe::prepare_scatter();
   if (rc) return rc;
+  if (p.vmm) {
+    const uint64_t total = (uint64_t)p.world * p.n_chunks;
+    uint64_t g = (total + 255) / 256;
+    const uint64_t cap = (uint64_t)num_sms() * 8;
+    if (g > cap) g = cap;
+    wqe::vmm_pack_kernel<<<(unsigned)g, 256, 0, s>>>(p);
+    if ((rc = launch_result())) return rc;
+  }
   uint64_t count_grid = (uint64_t)num_sms() * 8;
   const uint64_t count_need = (p.n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
   if (count_grid > count_need) count_grid = count_need;
@@ -793,6 +834,9 @@ extern "C" int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64
   if (!chunk_raddr || !chunk_rkey || !chunk_lkey || !aligned(chunk_raddr, 8) ||
       !aligned(chunk_rkey, 4) || !aligned(chunk_lkey, 4))
     return -EINVAL;
+  if (ws_bytes < wqe::vmm_ws_bytes_for(n, world * n_qp, world, n_chunks)) return -ENOSPC;
+  p.chunk_pack = reinterpret_cast<ulonglong2*>(static_cast<char*>(ws) +
+                                               wqe::vmm_table_off(n, world * n_qp));
   p.vmm = true;
   p.mtu = mtu;
   p.psn_head = psn_head;

@@ -293,8 +293,13 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
  *   mtu          0, or 512 <= mtu <= 2^20 with chunk_shift >= 12
  *   psn_head     [world * n_qp] in/out PSN counters (8-byte aligned); NULL if mtu == 0
  * Limits: n < 2^32, depth <= 2^31, n_chunks <= 2^32, heap_size >= 1.
- * Workspace: db_wqe_workspace_size(n, world * n_qp).
+ * Workspace: db_wqe_vmm_workspace_size(n, world, n_qp, heap_size, chunk_shift)
+ * bytes: the bucketing columns plus a per-call packed copy of the chunk tables
+ * (16 bytes per PE and chunk, so that a WQE reads its chunk's remote address,
+ * rkey and lkey at once); -ENOSPC below that.
  */
+int db_wqe_vmm_workspace_size(uint64_t n, uint32_t world, uint32_t n_qp, uint64_t heap_size,
+                              uint32_t chunk_shift, size_t* bytes);
 int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64_t* chunk_raddr,
                       const uint32_t* chunk_rkey, const uint32_t* chunk_lkey,
                       uint32_t chunk_shift, uint32_t world, uint32_t n_qp, uint64_t local_base,

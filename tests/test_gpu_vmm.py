@@ -24,7 +24,7 @@ def run_vmm(db, req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift, world, n_
     d_head = dev64(np.asarray(head, dtype=np.uint64))
     count = torch.full((R,), -1, dtype=torch.int32, device="cuda")
     ctr = torch.full((4,), -1, dtype=torch.int64, device="cuda")
-    ws = db.workspace(db.wqe_workspace_size(max(n, 1), R))
+    ws = db.workspace(db.wqe_vmm_workspace_size(max(n, 1), world, n_qp, heap, chunk_shift))
     d_psn = dev64(np.asarray(psn_head, dtype=np.uint64)) if mtu else None
     d_req = dev64(req) if n else torch.zeros((0, 2), dtype=torch.int64, device="cuda")
     db.wqe_bucket_vmm(d_req, dev64(np.ascontiguousarray(chunk_raddr, dtype=np.uint64)),
@@ -167,6 +167,11 @@ def test_bad_arguments(db):
         with pytest.raises(db.DescBuildError, match="invalid"):
             db.wqe_bucket_vmm(t, tab, t32, t32, shift, 2, 1, 0, 1 << 16, rings, 8, head, cnt, ws,
                               mtu=mtu, psn_head=psn)
+    # a workspace without room for the packed chunk tables
+    with pytest.raises(db.DescBuildError) as e:
+        db.wqe_bucket_vmm(t, tab, t32, t32, 12, 2, 1, 0, 1 << 16, rings, 8, head, cnt, ws)
+    assert e.value.code == -28
+    assert db.wqe_vmm_workspace_size(4, 2, 1, 1 << 16, 12) >= db.wqe_workspace_size(4, 2) + 2 * 16 * 16
 
 
 def test_full_size_workload(db, oracle):
