@@ -774,21 +774,32 @@ def run_ours(args, inp, world, device, dist):
 
 def run_e2e(st, stream, inp, K, device, dist, world, serial=False):
     """The same step through the API with host buffers: pinned host inputs are
-    copied in, every descriptor the step produces is copied back out. Each
-    workload runs on its own stream (copy in, call, copy out), the four
-    forked together as in the device-resident step; an output above 1 GiB is
-    copied back in four pieces on streams of their own, so that more than one
-    copy engine moves it."""
+    copied in, every descriptor the step produces ends in host memory. The
+    PRP lists are written by the kernel straight into a pinned host arena
+    (the host-memory list region of the source page), so only the words a
+    list holds cross the link; everything else is copied back. Each workload
+    runs on its own stream (copy in, call, copy out), the four forked together
+    as in the device-resident step; an output above 1 GiB is copied back in
+    four pieces on streams of their own, so that more than one copy engine
+    moves it."""
     import torch
     t = torch
     pin = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).pin_memory()
     pin32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).pin_memory()
-    groups = {}
+    groups, host_calls = {}, {}
+    list_bytes = 0
+    alg = algorithmic_bytes(inp)
     for k in ("prp_small", "prp_large"):
         if k in st.bufs:
             b, w = st.bufs[k], inp[k]
             groups[k] = ([(pin(w["req"]), b["req"]), (pin(w["lut"]), b["lut"])],
-                         [b["prp"], b["ctr"]] + ([b["arena"][:b["cap"]]] if b["cap"] else []))
+                         [b["prp"], b["ctr"]])
+            if b["cap"]:
+                hb = dict(b, arena=t.empty((b["cap"], 512), dtype=t.int64, pin_memory=True))
+                host_calls[k] = (lambda hb: lambda s_: st.prp(hb, s_))(hb)
+                # list words the kernel writes into host memory (algorithmic
+                # bytes less the 16-byte request and 16-byte PRP pair)
+                list_bytes += alg[k] - 32 * w["req"].shape[0] - w["lut"].shape[0] * 8
     if "mr_lookup" in st.bufs:
         b, m = st.bufs["mr_lookup"], inp["mr_lookup"]
         groups["mr_lookup"] = ([(pin(m["queries"]), b["q"]), (pin(m["mr_start"]), b["start"]),
@@ -804,6 +815,7 @@ def run_e2e(st, stream, inp, K, device, dist, world, serial=False):
     bi = sum(h.numel() * h.element_size() for h_in, _ in groups.values() for h, _ in h_in)
     bo = sum(o.numel() * o.element_size() for _, outs in groups.values() for o in outs)
     calls = dict(st.calls())
+    calls.update(host_calls)
     order = [k for k in SCHEDULE if k in groups]
     streams = {k: (stream if serial else t.cuda.Stream(device=device)) for k in order}
     pieces = [t.cuda.Stream(device=device) for _ in range(4)]
@@ -857,7 +869,8 @@ def run_e2e(st, stream, inp, K, device, dist, world, serial=False):
     reqs = sum(units(inp).values())
     return {"value": round(job_throughput(world, reqs, ms), 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "steps": K, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo}
+            "d2h_bytes_per_step": bo + list_bytes,
+            "d2h_detail": {"copied_back": bo, "lists_written_to_host_arena": list_bytes}}
 
 
 # ------------------------------------------------------------ CPU baseline

@@ -142,7 +142,10 @@ typedef struct db_counters {
  *   heap_size        bytes of device heap; a multiple of 65536
  *   arena_base       bus address of list page 0; a multiple of 4096
  *   arena_cap_pages  pages the arena holds
- *   arena            [arena_cap_pages][512] uint64: the arena's contents (32-byte aligned).
+ *   arena            [arena_cap_pages][512] uint64: the arena's contents (32-byte aligned),
+ *                    in device memory or in pinned host memory (the host-memory
+ *                    region the lists live in on the source page; the kernel
+ *                    then writes the lists across the CPU-GPU link).
  *                    Unused slots of a list's last page are left as they were,
  *                    except the ones sharing the last entry's 32-byte sector
  *                    (at most three), which are written as 0, so that every

@@ -20,11 +20,16 @@ def db():
     return lib()
 
 
-def run_gpu(db, req, lut, heap, arena_base, cap, flags=0, ws=None, with_arena=True):
+def run_gpu(db, req, lut, heap, arena_base, cap, flags=0, ws=None, with_arena=True,
+            host_arena=False):
     n = req.shape[0]
     d_req = dev64(req) if n else torch.zeros((0, 2), dtype=torch.int64, device="cuda")
-    arena = torch.full((max(cap, 1), 512), FILL, dtype=torch.int64, device="cuda") \
-        if with_arena else None
+    if not with_arena:
+        arena = None
+    elif host_arena:  # pinned host memory, written by the kernel across the link
+        arena = torch.full((max(cap, 1), 512), FILL, dtype=torch.int64).pin_memory()
+    else:
+        arena = torch.full((max(cap, 1), 512), FILL, dtype=torch.int64, device="cuda")
     prp = torch.full((max(n, 1), 2), FILL, dtype=torch.int64, device="cuda")
     pb = torch.full((max(n, 1),), FILL, dtype=torch.int64, device="cuda")
     st = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device="cuda")
@@ -112,6 +117,26 @@ def test_random_batches_ragged(db, oracle, n):
     want = oracle.prp_build(req, lut, heap, 0x7_0000_0000, cap, fill=FILL & (2**64 - 1))
     got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap)
     compare(oracle, got, want, cap, False)
+
+
+@pytest.mark.parametrize("zero_tail", [False, True])
+def test_arena_in_pinned_host_memory(db, oracle, zero_tail):
+    """The lists written straight into a pinned host arena equal the oracle's."""
+    rng = np.random.default_rng(77)
+    heap = 64 * 1024 * 1024
+    lut = (rng.choice(np.arange(1, 1 << 20, dtype=np.uint64), size=heap // 65536, replace=False)
+           << np.uint64(16))
+    n = 20000
+    off = 4 * rng.integers(0, heap // 4, size=n).astype(np.uint64)
+    ln = rng.integers(1, 3 * 1024 * 1024, size=n).astype(np.uint64)
+    ln = np.minimum(ln, np.uint64(heap) - off)
+    req = np.stack([off, ln], axis=1).astype(np.uint64)
+    cap = int(oracle.prp_build(req, lut, heap, 0x2_0000_0000, 1 << 40, lists=False)["ctr"][0])
+    want = oracle.prp_build(req, lut, heap, 0x2_0000_0000, cap, zero_tail=zero_tail,
+                            fill=FILL & (2**64 - 1))
+    got = run_gpu(db, req, lut, heap, 0x2_0000_0000, cap,
+                  flags=db.PRP_ZERO_TAIL if zero_tail else 0, host_arena=True)
+    compare(oracle, got, want, cap, zero_tail)
 
 
 def test_arena_overflow_and_capacity_edges(db, oracle):
