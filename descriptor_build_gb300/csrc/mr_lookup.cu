@@ -92,14 +92,16 @@ constexpr uint32_t kNoOff = 0xFFFFFFFFu;
 constexpr uint32_t kMaxOffsetShift = 43;  // bucket widths up to 2^43 bytes keep offsets in 32 bits
 inline size_t dir_bytes(uint32_t nb) { return (((size_t)nb + 1) * sizeof(Dir) + 255) & ~(size_t)255; }
 static_assert(sizeof(Dir) == 32, "one L2 sector per directory entry");
-// Tables that may overlap: Rec::before is built by a max-scan of the ends
-// in blocks of 1024 records, whose block maxima sit after the records.
+// Tables that may overlap: Rec::before is the prefix maximum of the ends of
+// the records before it, built first in an array of its own (blocks of 1024
+// records, whose maxima sit after the records).
 constexpr int kPmBlock = 1024;
 inline size_t pm_blocks(uint64_t n_mr) { return (n_mr + kPmBlock - 1) / kPmBlock; }
 inline size_t rec_bytes(uint64_t n_mr) { return ((size_t)n_mr * sizeof(Rec) + 255) & ~(size_t)255; }
 inline size_t ws_bytes_for(uint64_t n_mr) {
   const uint32_t nb = buckets_for(n_mr);
-  return kHeaderBytes + dir_bytes(nb) + rec_bytes(n_mr) + pm_blocks(n_mr) * 8;
+  return kHeaderBytes + dir_bytes(nb) + rec_bytes(n_mr) +
+         ((pm_blocks(n_mr) * 8 + 255) & ~(size_t)255) + (size_t)n_mr * 8;
 }
 
 struct BuildParams {
@@ -112,7 +114,8 @@ struct BuildParams {
   Rec* rec;
   uint32_t nb;
   uint32_t log_nb;
-  bool overlap;  // ranges may overlap: only starts must be sorted
+  bool overlap;        // ranges may overlap: only starts must be sorted
+  const uint64_t* pm;  // overlap: prefix maximum of the ends, pm[i] = max(end[0..i])
 };
 
 __device__ __forceinline__ uint64_t bucket_of(uint64_t x, uint64_t lo, uint32_t shift,
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildPara
       r.end = e;
       r.lkey = p.lkey[i];
       r.pad0 = 0;
-      r.before = 0;
+      r.before = (p.overlap && i > 0) ? p.pm[i - 1] : 0;
       p.rec[i] = r;
       if (!(s < e) || (i > 0 && (p.overlap ? p.start[i - 1] > s : p.end[i - 1] > s))) bad = true;
       b0 = i == 0 ? 0 : bucket_of(p.start[i - 1], lo, shift, p.nb) + 1;
@@ -443,10 +446,11 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
 }
 
 // ------------------------------------------------------ overlapping tables
-// Rec::before of record i + 1 is the prefix maximum of the ends,
-// pm(i) = max(end[0..i]): a block-local inclusive max-scan, a scan of the
-// block maxima (one CTA), then each block takes the maximum of the blocks
-// before it. A record read then says whether an earlier one may contain
+// The prefix maximum of the ends, pm(i) = max(end[0..i]), into an array of
+// its own: a block-local inclusive max-scan, a scan of the block maxima (one
+// CTA), then each block takes the maximum of the blocks before it. The index
+// build then writes Rec::before = pm(i - 1) with the rest of record i, in one
+// whole-sector store. A record read then says whether an earlier one may contain
 // the query, so the common case costs the same single 32-byte record load
 // as on a disjoint table.
 __device__ __forceinline__ uint64_t warp_max_scan(uint64_t x, int lane) {
@@ -469,11 +473,11 @@ __device__ __forceinline__ uint64_t block_max_scan(uint64_t x, uint64_t* s_w) {
   return before > x ? before : x;
 }
 __global__ void __launch_bounds__(kPmBlock) mr_pm_block_kernel(const uint64_t* end, uint64_t n,
-                                                               Rec* rec, uint64_t* bmax) {
+                                                               uint64_t* pm, uint64_t* bmax) {
   __shared__ uint64_t s_w[32];
   const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
   const uint64_t x = block_max_scan(i < n ? end[i] : 0ull, s_w);
-  if (i + 1 < n) rec[i + 1].before = x;  // block-local for now
+  if (i < n) pm[i] = x;  // block-local for now
   if (threadIdx.x == kPmBlock - 1) bmax[blockIdx.x] = x;
 }
 __global__ void __launch_bounds__(kPmBlock) mr_pm_scan_kernel(uint64_t* bmax, uint64_t nblk) {
@@ -491,12 +495,12 @@ __global__ void __launch_bounds__(kPmBlock) mr_pm_scan_kernel(uint64_t* bmax, ui
     __syncthreads();
   }
 }
-__global__ void __launch_bounds__(kPmBlock) mr_pm_apply_kernel(Rec* rec, uint64_t n,
+__global__ void __launch_bounds__(kPmBlock) mr_pm_apply_kernel(uint64_t* pm, uint64_t n,
                                                                const uint64_t* bmax) {
   const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
-  if (blockIdx.x == 0 || i + 1 >= n) return;
+  if (blockIdx.x == 0 || i >= n) return;
   const uint64_t prior = bmax[blockIdx.x - 1];
-  if (prior > rec[i + 1].before) rec[i + 1].before = prior;
+  if (prior > pm[i]) pm[i] = prior;
 }
 
 int lookup_ctas_per_sm() {
@@ -558,24 +562,26 @@ int lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint
   char* recs = w + mr::kHeaderBytes + mr::dir_bytes(nb);
   mr::Rec* rec = reinterpret_cast<mr::Rec*>(recs);
   uint64_t* bmax = reinterpret_cast<uint64_t*>(recs + mr::rec_bytes(n_mr));
+  uint64_t* pm = reinterpret_cast<uint64_t*>(
+      recs + mr::rec_bytes(n_mr) + ((mr::pm_blocks(n_mr) * 8 + 255) & ~(size_t)255));
 
   if (n_mr > 0) {
-    mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb, overlap};
+    int rc = 0;
+    if (overlap) {  // the prefix maximum first, so the index build writes whole records
+      const uint64_t nblk = mr::pm_blocks(n_mr);
+      mr::mr_pm_block_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(mr_end, n_mr, pm, bmax);
+      if ((rc = launch_result())) return rc;
+      mr::mr_pm_scan_kernel<<<1, mr::kPmBlock, 0, s>>>(bmax, nblk);
+      if ((rc = launch_result())) return rc;
+      mr::mr_pm_apply_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(pm, n_mr, bmax);
+      if ((rc = launch_result())) return rc;
+    }
+    mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb, overlap, pm};
     uint64_t grid = (n_mr + mr::kBuildThreads - 1) / mr::kBuildThreads;
     const uint64_t cap = (uint64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
-    int rc = launch_result();
-    if (rc) return rc;
-    if (overlap) {
-      const uint64_t nblk = mr::pm_blocks(n_mr);
-      mr::mr_pm_block_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(mr_end, n_mr, rec, bmax);
-      if ((rc = launch_result())) return rc;
-      mr::mr_pm_scan_kernel<<<1, mr::kPmBlock, 0, s>>>(bmax, nblk);
-      if ((rc = launch_result())) return rc;
-      mr::mr_pm_apply_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(rec, n_mr, bmax);
-      if ((rc = launch_result())) return rc;
-    }
+    if ((rc = launch_result())) return rc;
   }
   mr::LookupParams l{reinterpret_cast<const ulonglong2*>(q), n_q, n_mr, hdr, hdr, dir, rec,
                      idx, lkey, kind, ctr};
