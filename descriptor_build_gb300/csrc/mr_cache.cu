@@ -55,11 +55,25 @@ inline unsigned grid_for(uint64_t n) {
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (n); i += (uint64_t)gridDim.x * blockDim.x)
 
 // ------------------------------------------------------------------ scan
-// Exclusive scan of n u32 values (n known on the host): block sums, a scan
-// of the block sums by one CTA, then each block re-scans with its offset.
-__global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n,
-                                                            uint32_t* bsum) {
+// Exclusive scan of n u32 values: block sums, a scan of the block sums by
+// one CTA, then each block re-scans with its offset. n is known on the host,
+// or (Len::dev) worked out on the device as mul * ceil(*dev / div), at most
+// the host's n: the count columns of a sort cover only the tiles that hold
+// items, and the blocks past them return at once.
+struct Len {
+  const uint32_t* dev;
+  uint32_t mul, div;
+};
+__device__ __forceinline__ uint64_t live_len(uint64_t n, const Len& l) {
+  if (!l.dev) return n;
+  const uint64_t m = (uint64_t)l.mul * ((*l.dev + (uint64_t)l.div - 1) / l.div);
+  return m < n ? m : n;
+}
+__global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n_max,
+                                                            Len len, uint32_t* bsum) {
   __shared__ uint32_t s_w[32];
+  const uint64_t n = live_len(n_max, len);
+  if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
   const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
   uint32_t v = 0;
 #pragma unroll
@@ -69,9 +83,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, 
   block_excl_scan<32>(v, ex, tot, s_w);
   if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
 }
-__global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint64_t nb,
-                                                           uint32_t* total) {
+__global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint64_t n_max,
+                                                           Len len, uint32_t* total) {
   __shared__ uint32_t s_w[32];
+  const uint64_t n = live_len(n_max, len);
+  const uint64_t nb = n ? (n + kScanChunk - 1) / kScanChunk : 1;
   uint32_t carry = 0;
   for (uint64_t b0 = 0; b0 < nb; b0 += kScanThreads) {
     const uint64_t b = b0 + threadIdx.x;
@@ -85,8 +101,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint6
   if (threadIdx.x == 0 && total) *total = carry;
 }
 __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
-                                                           uint64_t n, const uint32_t* bsum) {
+                                                           uint64_t n_max, Len len,
+                                                           const uint32_t* bsum) {
   __shared__ uint32_t s_w[32];
+  const uint64_t n = live_len(n_max, len);
+  if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
   const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
   uint32_t x[kScanItems];
   uint32_t v = 0;
@@ -106,15 +125,15 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, u
 }
 inline size_t scan_tmp_words(uint64_t n) { return (size_t)ceil_div(n ? n : 1, kScanChunk); }
 int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_t* bsum,
-         cudaStream_t s) {
+         cudaStream_t s, Len len = Len{nullptr, 0, 1}) {
   if (n == 0) {
     if (total) cudaMemsetAsync(total, 0, 4, s);
     return launch_result();
   }
   const uint64_t nb = ceil_div(n, kScanChunk);
-  scan_reduce<<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, bsum);
-  scan_bsums<<<1, kScanThreads, 0, s>>>(bsum, nb, total);
-  scan_apply<<<(unsigned)nb, kScanThreads, 0, s>>>(in, out, n, bsum);
+  scan_reduce<<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, len, bsum);
+  scan_bsums<<<1, kScanThreads, 0, s>>>(bsum, n, len, total);
+  scan_apply<<<(unsigned)nb, kScanThreads, 0, s>>>(in, out, n, len, bsum);
   return launch_result();
 }
 
@@ -129,10 +148,8 @@ __global__ void __launch_bounds__(kSortThreads) radix_count(const uint64_t* key,
   __shared__ uint32_t hist[256];
   const uint64_t n = *n_dev;
   const uint64_t t0 = (uint64_t)blockIdx.x * kSortTile;
-  if (t0 >= n) {  // past the items: an empty tile
-    counts[(uint64_t)threadIdx.x * tiles + blockIdx.x] = 0;
-    return;
-  }
+  if (t0 >= n) return;  // past the items: not a column entry
+  tiles = (uint32_t)((n + kSortTile - 1) / kSortTile);  // columns over the live tiles only
   hist[threadIdx.x] = 0;
   __syncthreads();
 #pragma unroll 4
@@ -165,7 +182,8 @@ __global__ void __launch_bounds__(kSortThreads) radix_scatter(
   uint32_t* s_w = s_goff + 256;                                            // [32]
   const uint64_t n = *n_dev;
   const uint64_t t0 = (uint64_t)blockIdx.x * kSortTile;
-  if (t0 >= n) return;  // no items: the tile's counts were all zero
+  if (t0 >= n) return;  // no items in this tile
+  tiles = (uint32_t)((n + kSortTile - 1) / kSortTile);  // columns over the live tiles only
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int w = 0; w < kSortWarps; ++w) s_hist[w * 256 + threadIdx.x] = 0;
@@ -256,7 +274,8 @@ int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, cudaStrea
     radix_count<<<tiles, kSortThreads, 0, s>>>(b.key[cur], n_dev, (uint32_t)shift, b.counts, tiles);
     int rc = launch_result();
     if (rc) return rc;
-    if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s))) return rc;
+    if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s, Len{n_dev, 256u, (uint32_t)kSortTile})))
+      return rc;
     radix_scatter<<<tiles, kSortThreads, kScatterSmem, s>>>(
         b.key[cur], b.val[cur], n_dev, (uint32_t)shift, b.counts, tiles, b.key[cur ^ 1],
         b.val[cur ^ 1]);
