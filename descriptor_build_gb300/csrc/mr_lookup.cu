@@ -40,7 +40,7 @@ namespace mr {
 #define DB_MR_QPT 3
 #endif
 #ifndef DB_MR_MIN_CTAS
-#define DB_MR_MIN_CTAS 5
+#define DB_MR_MIN_CTAS 4
 #endif
 #ifndef DB_MR_BUCKET_SHIFT
 #define DB_MR_BUCKET_SHIFT 0
