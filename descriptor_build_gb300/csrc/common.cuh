@@ -102,14 +102,18 @@ __device__ __forceinline__ void st_stream8(void* p, uint64_t a, uint64_t pol) {
     asm volatile("st.global.u64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
 }
 
-__device__ __forceinline__ uint64_t ld_acquire(const unsigned long long* p) {
+// Tile status words. The flag and the value travel in one aligned 64-bit
+// word, so a reader that sees the flag sees its value, and no other memory
+// is published through the word: relaxed (not acquire / release) ordering is
+// enough, and it lets a lane's four lookback loads be in flight together.
+__device__ __forceinline__ uint64_t ld_relaxed(const unsigned long long* p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned long long* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

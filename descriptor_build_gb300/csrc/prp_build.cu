@@ -7,15 +7,17 @@
 // one page chain through slot 511 (NVMe convention).
 //
 // One persistent kernel, single pass over the requests:
-//   1. a CTA takes a tile of 512 requests by atomic ticket and loads one
-//      16-byte request per thread;
+//   1. a CTA takes a tile of 2,048 requests by atomic ticket and loads four
+//      16-byte requests per thread;
 //   2. page count n and list-page count L per request, block scan of L;
 //   3. decoupled lookback over the tiles before it (one status word per
 //      tile in the workspace, bounded wait) gives the tile's first list page;
+//      a tile with no list (and no page_base output) skips the wait;
 //   4. PRP1/PRP2, page_base and status go out as 16/8/1-byte stores;
 //   5. the tile's lists are written by warps that take one request at a time
 //      from a shared-memory queue: each list is a contiguous run of 8-byte
-//      words starting on a 4 KiB page, written as 16-byte stores.
+//      words starting on a 4 KiB page, written as 32-byte stores and ended on
+//      a whole 32-byte sector.
 // The last CTA to finish publishes the counters and readies the workspace
 // for the next call (new epoch, ticket back to 0).
 #include "common.cuh"
@@ -49,7 +51,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kItems = DB_PRP_ITEMS;       // requests per thread per tile
 constexpr int kTile = kThreads * kItems;   // requests per tile
 
-// Workspace: ScanHeader (acc[0] invalid, acc[1] overflow), then one status
+// Workspace: ScanHeader (acc[0] invalid, acc[1] overflow, acc[2] list pages), then one status
 // word per tile.
 constexpr uint64_t tiles_for(uint64_t n) { return (n + kTile - 1) / kTile; }
 constexpr uint64_t kMaxRequests = 1ull << 28;
@@ -355,11 +357,11 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
   unsigned long long* mine = p.tile_status + t;
   failed = false;
   if (t == 0) {
-    if (lane == 0) st_release(mine, status_word(kPrefix, epoch, agg));
+    if (lane == 0) st_relaxed(mine, status_word(kPrefix, epoch, agg));
     excl_out = 0;
     return;
   }
-  if (lane == 0) st_release(mine, status_word(kAggregate, epoch, agg));
+  if (lane == 0) st_relaxed(mine, status_word(kAggregate, epoch, agg));
   uint64_t excl = 0;
   int64_t top = (int64_t)t - 1;  // newest tile of the window
   Backoff backoff;
@@ -375,7 +377,7 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
       uint32_t flag = kPrefix;     // before tile 0: an inclusive prefix of 0
       uint64_t val = 0;
       if (u >= 0) {
-        const uint64_t w = ld_acquire(p.tile_status + u);
+        const uint64_t w = ld_relaxed(p.tile_status + u);
         flag = status_flag(w, epoch);
         val = w & kValueMask;
       }
@@ -407,7 +409,7 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
     top -= 128;
   }
   if (lane == 0)
-    st_release(mine, failed ? status_word(kFailed, epoch, 0)
+    st_relaxed(mine, failed ? status_word(kFailed, epoch, 0)
                             : status_word(kPrefix, epoch, excl + agg));
   excl_out = excl;
 }
@@ -425,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
   const uint64_t pol_last = policy_evict_last();
   const uint32_t epoch = *(volatile unsigned int*)&p.hdr->epoch;
   uint32_t my_invalid = 0, my_overflow = 0;
+  uint64_t my_pages = 0;  // list pages of this CTA's tiles (thread 0's count is used)
   bool any_failed = false;
 
   for (;;) {
@@ -477,11 +480,16 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     const uint32_t n_short = (uint32_t)(tile_v >> 23) & 4095u;
     const uint32_t n_long = (uint32_t)(tile_v >> 35) & 4095u;
 
-    // 3. First list page of this tile.
+    // 3. First list page of this tile. A tile that owns no list and writes
+    //    no page_base never uses it: it publishes its (zero) aggregate and
+    //    goes on without waiting for its predecessors.
     if (threadIdx.x < 32) {
-      uint64_t excl;
-      bool failed;
-      lookback(p, tile, epoch, tile_L, excl, failed);
+      uint64_t excl = 0;
+      bool failed = false;
+      if (tile_L != 0 || p.page_base)
+        lookback(p, tile, epoch, tile_L, excl, failed);
+      else if (lane == 0)
+        st_relaxed(p.tile_status + tile, status_word(tile == 0 ? kPrefix : kAggregate, epoch, 0));
       if (lane == 0) {
         s_excl = excl;
         s_failed = failed;
@@ -523,8 +531,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
         s_list[q] = pack_item(off[k] & ~4095ull, (ovf || failed) ? 0 : L[k], pb, npg[k]);
       }
     }
-    if (tile + 1 == p.n_tiles && threadIdx.x == 0 && p.ctr && !failed)
-      p.ctr->total = s_excl + tile_L;
+    my_pages += tile_L;
     __syncthreads();
 
     // 5. Lists. Long ones: a warp takes the next queued request and writes
@@ -605,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     atomicAdd(&p.hdr->acc[1], (unsigned long long)my_overflow);
   }
   if (threadIdx.x == 0 && any_failed) atomicOr(&p.hdr->err, DB_ERR_TIMEOUT);
+  if (threadIdx.x == 0 && my_pages) atomicAdd(&p.hdr->acc[2], (unsigned long long)my_pages);
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -616,12 +624,13 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     if (threadIdx.x == 0) {
       const unsigned long long inv = atomicExch(&p.hdr->acc[0], 0ull);
       const unsigned long long ovf = atomicExch(&p.hdr->acc[1], 0ull);
+      const unsigned long long pages = atomicExch(&p.hdr->acc[2], 0ull);
       const unsigned int err = atomicExch(&p.hdr->err, 0u);
       if (p.ctr) {
+        p.ctr->total = err ? 0 : pages;
         p.ctr->n_invalid = inv;
         p.ctr->n_overflow = ovf;
         p.ctr->err = err;
-        if (err) p.ctr->total = 0;
       }
     }
     end_of_call(p.hdr, p.tile_status, p.n_tiles, p.cap_tiles, true);

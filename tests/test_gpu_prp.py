@@ -21,7 +21,10 @@ def db():
 
 
 def run_gpu(db, req, lut, heap, arena_base, cap, flags=0, ws=None, with_arena=True,
-            host_arena=False):
+            host_arena=False, per_request=True):
+    """One db_prp_build call. per_request=False leaves page_base and status
+    out, as the benchmark's calls do (a tile with no list then skips its
+    lookback)."""
     n = req.shape[0]
     d_req = dev64(req) if n else torch.zeros((0, 2), dtype=torch.int64, device="cuda")
     if not with_arena:
@@ -36,17 +39,21 @@ def run_gpu(db, req, lut, heap, arena_base, cap, flags=0, ws=None, with_arena=Tr
     ctr = torch.full((4,), FILL, dtype=torch.int64, device="cuda")
     if ws is None:
         ws = db.workspace(db.prp_workspace_size(n))
-    db.prp_build(d_req, dev64(lut), heap, arena_base, cap, arena, prp, ws, page_base=pb,
-                 status=st, ctr=ctr, flags=flags)
+    db.prp_build(d_req, dev64(lut), heap, arena_base, cap, arena, prp, ws,
+                 page_base=pb if per_request else None, status=st if per_request else None,
+                 ctr=ctr, flags=flags)
     torch.cuda.synchronize()
-    return dict(prp=host64(prp)[:n], page_base=host64(pb)[:n], status=st.cpu().numpy()[:n],
+    return dict(prp=host64(prp)[:n], page_base=host64(pb)[:n] if per_request else None,
+                status=st.cpu().numpy()[:n] if per_request else None,
                 ctr=host64(ctr), arena=arena)
 
 
 def compare(oracle, got, want, cap, zero_tail):
     assert (got["prp"] == want["prp"]).all()
-    assert (got["page_base"] == want["page_base"]).all()
-    assert (got["status"] == want["status"]).all()
+    if got["page_base"] is not None:
+        assert (got["page_base"] == want["page_base"]).all()
+    if got["status"] is not None:
+        assert (got["status"] == want["status"]).all()
     assert (got["ctr"] == want["ctr"]).all(), (got["ctr"], want["ctr"])
     if got["arena"] is not None:
         used = min(int(want["ctr"][0]), cap)
@@ -104,8 +111,9 @@ def random_batch(rng, n, heap, max_len, invalid_frac=0.02):
     return np.stack([off, length], axis=1).astype(np.uint64)
 
 
+@pytest.mark.parametrize("per_request", [True, False])
 @pytest.mark.parametrize("n", [1, 2, 511, 512, 513, 2047, 2048, 2049, 4999, 70001])
-def test_random_batches_ragged(db, oracle, n):
+def test_random_batches_ragged(db, oracle, n, per_request):
     """Several tiles of 2048 and a ragged tail, lists of all lengths."""
     import synth
     rng = np.random.default_rng(1000 + n)
@@ -115,7 +123,42 @@ def test_random_batches_ragged(db, oracle, n):
     need = oracle.prp_build(req, lut, heap, 0x7_0000_0000, 1 << 40, lists=False)
     cap = max(1, int(need["ctr"][0]))
     want = oracle.prp_build(req, lut, heap, 0x7_0000_0000, cap, fill=FILL & (2**64 - 1))
-    got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap)
+    got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap, per_request=per_request)
+    compare(oracle, got, want, cap, False)
+
+
+@pytest.mark.parametrize("per_request", [True, False])
+@pytest.mark.parametrize("spacing", [1, 3, 129, 300])
+def test_sparse_lists(db, oracle, spacing, per_request):
+    """Lists in one tile of every `spacing`, the tiles between them holding
+    only one- and two-page requests. Without page_base those tiles skip their
+    lookback, so a list tile's lookback sums runs of zero aggregates (more
+    than one 128-tile window when spacing > 128)."""
+    import synth
+    rng = np.random.default_rng(7000 + spacing)
+    heap = 256 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    tiles = 2 * spacing + 5 if spacing > 3 else 40
+    n = tiles * 2048 - 777  # ragged last tile
+    off = 4 * rng.integers(0, (heap - 8192) // 4, size=n).astype(np.uint64)
+    length = rng.integers(1, 4097, size=n).astype(np.uint64)  # at most two pages
+    list_tiles = np.arange(spacing - 1, tiles, spacing)
+    for t in list_tiles:
+        rows = t * 2048 + rng.choice(2048, size=5, replace=False)
+        rows = rows[rows < n]
+        off[rows] = 4096 * rng.integers(0, heap // 4096 - 1024, size=rows.size).astype(np.uint64)
+        length[rows] = rng.integers(3 * 4096, 2 * 1024 * 1024, size=rows.size).astype(np.uint64)
+    req = np.stack([off, length], axis=1).astype(np.uint64)
+    need = oracle.prp_build(req, lut, heap, 0x7_0000_0000, 1 << 40, lists=False)
+    cap = max(1, int(need["ctr"][0]))
+    assert cap > 1
+    want = oracle.prp_build(req, lut, heap, 0x7_0000_0000, cap, fill=FILL & (2**64 - 1))
+    got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap, per_request=per_request)
+    compare(oracle, got, want, cap, False)
+    # A second call on the same workspace (next epoch) gives the same result.
+    ws = db.workspace(db.prp_workspace_size(n))
+    for _ in range(2):
+        got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap, ws=ws, per_request=per_request)
     compare(oracle, got, want, cap, False)
 
 
@@ -226,19 +269,24 @@ def test_lookback_timeout_is_reported(db, oracle):
     compare(oracle, got, want, 1 << 14, False)
 
 
-def test_small_io_workload_full(db, oracle):
-    """1,048,576 small requests: every output against the oracle."""
+@pytest.mark.parametrize("per_request", [True, False])
+def test_small_io_workload_full(db, oracle, per_request):
+    """1,048,576 small requests: every output against the oracle (without
+    page_base and status: the benchmark's call)."""
     import synth
     w = synth.prp_small()
     want = oracle.prp_build(w["req"], w["lut"], w["heap_size"], w["arena_base"], 1024)
     assert int(want["ctr"][0]) == 0  # the list path is never taken here
-    got = run_gpu(db, w["req"], w["lut"], w["heap_size"], w["arena_base"], 1024)
+    got = run_gpu(db, w["req"], w["lut"], w["heap_size"], w["arena_base"], 1024,
+                  per_request=per_request)
     compare(oracle, got, want, 1024, False)
 
 
-def test_large_workload_full_size(db, oracle):
+@pytest.mark.parametrize("per_request", [True, False])
+def test_large_workload_full_size(db, oracle, per_request):
     """4,194,304 requests on a 16 GiB heap: PRPs, page bases and counters of
-    every request against the oracle; list pages of a sample, one by one."""
+    every request against the oracle; list pages of a sample, one by one
+    (per_request=False is the benchmark's call)."""
     import synth
     w = synth.prp_large()
     req, lut = w["req"], w["lut"]
@@ -246,10 +294,11 @@ def test_large_workload_full_size(db, oracle):
     full = oracle.prp_build(req, lut, w["heap_size"], w["arena_base"], 1 << 40, lists=False)
     cap = int(full["ctr"][0])
     want = oracle.prp_build(req, lut, w["heap_size"], w["arena_base"], cap, lists=False)
-    got = run_gpu(db, req, lut, w["heap_size"], w["arena_base"], cap)
+    got = run_gpu(db, req, lut, w["heap_size"], w["arena_base"], cap, per_request=per_request)
     assert (got["prp"] == want["prp"]).all()
-    assert (got["page_base"] == want["page_base"]).all()
-    assert (got["status"] == want["status"]).all()
+    if per_request:
+        assert (got["page_base"] == want["page_base"]).all()
+        assert (got["status"] == want["status"]).all()
     assert (got["ctr"] == want["ctr"]).all()
     rng = np.random.default_rng(0)
     pages = np.diff(np.append(want["page_base"], np.uint64(cap))).astype(np.int64)
