@@ -211,13 +211,16 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
 }
 
 // ----------------------------------------------------------------- scan pass
-// One CTA per bin: each thread takes 32 consecutive column entries (16-byte
-// loads and stores), so a column of up to 32768 tiles is one round. Sums are
+// One CTA per bin column. A round covers 32,768 column entries: warp w takes
+// the 1,024 contiguous entries at w * 1,024 and its lane l the four at
+// j * 128 + 4 l (j = 0..7), so every load and store of a warp covers 512
+// contiguous bytes; a column of up to 32,768 tiles is one round. Sums are
 // 64-bit; the prefixes are stored in 32 bits, exact for any ring whose batch
 // total fits the ring (depth <= 2^31), which are the only ones written.
 constexpr int kScanThreads = 1024;
-constexpr int kScanPer = 32;
-constexpr uint64_t kScanSeg = (uint64_t)kScanThreads * kScanPer;
+constexpr int kScanGroups = 8;  // four-entry groups per thread per round
+constexpr uint64_t kScanWarpSpan = 32ull * 4 * kScanGroups;
+constexpr uint64_t kScanSeg = (uint64_t)(kScanThreads / 32) * kScanWarpSpan;
 
 __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) {
   constexpr int kW = kScanThreads / 32;
@@ -229,43 +232,54 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
   const uint32_t v = psn_col ? blockIdx.x - p.V : blockIdx.x;
   uint32_t* col = (psn_col ? p.psn_counts : p.counts) + (uint64_t)v * p.stride;
   const uint64_t T = p.n_tiles;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t carry = 0;
   for (uint64_t s0 = 0; s0 < T; s0 += kScanSeg) {
-    const uint64_t b = s0 + (uint64_t)threadIdx.x * kScanPer;
-    uint32_t c[kScanPer];
-    if (b + kScanPer <= T) {
-#pragma unroll
-      for (int j = 0; j < kScanPer; j += 4) {
-        const uint4 x = *reinterpret_cast<const uint4*>(col + b + j);
-        c[j] = x.x;
-        c[j + 1] = x.y;
-        c[j + 2] = x.z;
-        c[j + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kScanPer; ++j) c[j] = b + j < T ? col[b + j] : 0u;
-    }
+    const uint64_t wb = s0 + (uint64_t)warp * kScanWarpSpan + 4u * lane;
+    uint4 c[kScanGroups];
     uint64_t mine = 0;
 #pragma unroll
-    for (int j = 0; j < kScanPer; ++j) mine += c[j];
+    for (int j = 0; j < kScanGroups; ++j) {
+      const uint64_t b = wb + (uint64_t)j * 128;
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (b < T) {  // columns are padded to 8 entries, so b + 4 <= stride
+        x = *reinterpret_cast<const uint4*>(col + b);
+        if (b + 1 >= T) x.y = 0;
+        if (b + 2 >= T) x.z = 0;
+        if (b + 3 >= T) x.w = 0;
+      }
+      c[j] = x;
+      mine += (uint64_t)x.x + x.y + x.z + x.w;
+    }
+    // Lane 0's exclusive prefix (lanes in order) is the total of the warps
+    // before this one.
     uint64_t excl, seg_total;
     block_excl_scan64<kW>(mine, excl, seg_total, s_scan);
-    uint32_t run = (uint32_t)(carry + excl);
+    uint64_t run = carry + __shfl_sync(kFull, excl, 0);
 #pragma unroll
-    for (int j = 0; j < kScanPer; ++j) {
-      const uint32_t x = c[j];
-      c[j] = run;
-      run += x;
+    for (int j = 0; j < kScanGroups; ++j) {
+      const uint4 x = c[j];
+      const uint64_t g = (uint64_t)x.x + x.y + x.z + x.w;
+      uint64_t incl = g;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t e0 = (uint32_t)(run + incl - g);
+      c[j] = make_uint4(e0, e0 + x.x, e0 + x.x + x.y, e0 + x.x + x.y + x.z);
+      run += __shfl_sync(kFull, incl, 31);
     }
-    if (b + kScanPer <= T) {
 #pragma unroll
-      for (int j = 0; j < kScanPer; j += 4)
-        *reinterpret_cast<uint4*>(col + b + j) = make_uint4(c[j], c[j + 1], c[j + 2], c[j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < kScanPer; ++j)
-        if (b + j < T) col[b + j] = c[j];
+    for (int j = 0; j < kScanGroups; ++j) {
+      const uint64_t b = wb + (uint64_t)j * 128;
+      if (b + 4 <= T) {
+        *reinterpret_cast<uint4*>(col + b) = c[j];
+      } else if (b < T) {
+        col[b] = c[j].x;
+        if (b + 1 < T) col[b + 1] = c[j].y;
+        if (b + 2 < T) col[b + 2] = c[j].z;
+      }
     }
     carry += seg_total;
     __syncthreads();  // s_scan is reused by the next round

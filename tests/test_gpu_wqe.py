@@ -161,3 +161,19 @@ def test_full_size_workload(db, oracle):
     got = run_gpu(db, p["req"], p["peer_ptrs"], p["rkeys"], p["world"], p["n_qp"],
                   p["local_base"], p["lkey"], p["heap_size"], p["depth"], p["head"])
     check(got, want)
+
+
+def test_columns_longer_than_one_scan_round(db, oracle):
+    """33,072 tiles of 256 puts: the scan of each ring's column takes two
+    rounds of 32,768 entries, the second one ragged."""
+    rng = np.random.default_rng(4242)
+    n = 32768 * 256 + 77777
+    world, n_qp, depth, heap = 4, 2, 1 << 21, 1 << 32
+    req = random_puts(rng, n, world, n_qp, heap)
+    peer = (rng.integers(1 << 19, 1 << 26, size=world) << 21).astype(np.uint64)
+    rkeys = rng.integers(0, 2**32, size=world, dtype=np.uint64).astype(np.uint32)
+    head = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    lb, lk = 0x7F0000000000, 0xC0FFEE
+    want = oracle.wqe_bucket(req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head, fill=0xCD)
+    got = run_gpu(db, req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head)
+    check(got, want)
