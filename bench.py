@@ -13,8 +13,11 @@ one stream, in turn):
 ``value`` is requests translated per second over the whole step (all four
 batches), with inputs resident in HBM. Each call is also timed with CUDA
 events alone on the stream, in the same steps run one call at a time after
-the timed region; the dominant one (prp_large) gives the roofline line. ``e2e`` repeats the step through the same API with inputs in
-pinned host memory and every descriptor copied back to the host. ``next``
+the timed region; the dominant one (prp_large) gives the roofline line.
+``output_GB_per_s`` counts the descriptor bytes written (PRP pairs, list
+words, MR results, WQEs), for the step and per call. ``e2e`` repeats the
+step through the same API with inputs in pinned host memory and every
+descriptor copied back to the host. ``next``
 times, on its own and outside the step, the rows built after the hot path:
 the put batch on a heap of 2 MiB chunks (db_wqe_bucket_vmm, without and
 with packet sequence numbers), the MR lookup on a table whose records
@@ -112,6 +115,20 @@ def algorithmic_bytes(inp) -> dict:
         out["mr_lookup"] = 25 * m["queries"].shape[0] + 20 * m["mr_start"].shape[0]
     if "put_bucket" in inp:
         out["put_bucket"] = 80 * inp["put_bucket"]["req"].shape[0]
+    return out
+
+
+def output_bytes(inp) -> dict:
+    """Descriptor bytes each call writes: the 16 B PRP pair and 8 B per list
+    word; the 9 B MR result (index, lkey, kind); the 64 B WQE."""
+    out = {}
+    for k in ("prp_small", "prp_large"):
+        if k in inp:
+            out[k] = 16 * inp[k]["req"].shape[0] + 8 * list_words(inp[k]["req"])
+    if "mr_lookup" in inp:
+        out["mr_lookup"] = 9 * inp["mr_lookup"]["queries"].shape[0]
+    if "put_bucket" in inp:
+        out["put_bucket"] = 64 * inp["put_bucket"]["req"].shape[0]
     return out
 
 
@@ -727,6 +744,7 @@ def run_ours(args, inp, world, device, dist):
 
     u = units(inp)
     alg = algorithmic_bytes(inp)
+    outb = output_bytes(inp)
     peak, peak_kind = peak_gbs()
     reqs_per_step = sum(u.values())
     ms_per_step = total_ms / K
@@ -737,7 +755,10 @@ def run_ours(args, inp, world, device, dist):
         gbs = alg[name] / (ms * 1e-3) / 1e9
         kernels[name] = {"ms": round(ms, 4), "M_req_per_s": round(u[name] / ms / 1e3, 2),
                          "algorithmic_bytes": alg[name], "GB_per_s": round(gbs, 1),
-                         "frac_of_peak": round(gbs / peak, 4), "launches": Step.LAUNCHES[name]}
+                         "frac_of_peak": round(gbs / peak, 4),
+                         "output_bytes": outb[name],
+                         "output_GB_per_s": round(outb[name] / (ms * 1e-3) / 1e9, 1),
+                         "launches": Step.LAUNCHES[name]}
         if not args.serial:
             kernels[name]["concurrent_span_ms"] = round(span_ms[name], 4)
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -763,6 +784,7 @@ def run_ours(args, inp, world, device, dist):
                                    + ", ".join(n for n, _ in calls)
                                    + "; per-call times and the roofline from the same steps "
                                      "run one call at a time after the timed region")},
+           "output_GB_per_s": round(world * sum(outb.values()) / (ms_per_step * 1e-3) / 1e9, 1),
            "kernels": kernels, "roofline": roof,
            "gpu_launches": K * sum(Step.LAUNCHES[k] for k in u),  # in the timed region
            "clocks": clk.summary()}
