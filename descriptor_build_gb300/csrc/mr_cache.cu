@@ -69,16 +69,35 @@ __device__ __forceinline__ uint64_t live_len(uint64_t n, const Len& l) {
   const uint64_t m = (uint64_t)l.mul * ((*l.dev + (uint64_t)l.div - 1) / l.div);
   return m < n ? m : n;
 }
+// Within a block's chunk, warp w takes the kScanItems * 32 items at
+// w * kScanItems * 32 and its lane l the four at g * 128 + 4 l for each
+// group g, so every load and store of a warp covers 512 contiguous bytes.
+constexpr int kScanGroups = kScanItems / 4;
+static_assert(kScanItems % 4 == 0, "groups of four items");
+// Loads the four items at b (those at or past n read as 0).
+__device__ __forceinline__ uint4 scan_load4(const uint32_t* in, uint64_t b, uint64_t n) {
+  if (b + 4 <= n) return *reinterpret_cast<const uint4*>(in + b);
+  uint4 x = make_uint4(0u, 0u, 0u, 0u);
+  if (b < n) x.x = in[b];
+  if (b + 1 < n) x.y = in[b + 1];
+  if (b + 2 < n) x.z = in[b + 2];
+  return x;
+}
+__device__ __forceinline__ uint64_t scan_group_base(uint32_t g) {
+  return (uint64_t)blockIdx.x * kScanChunk + (uint64_t)(threadIdx.x >> 5) * (kScanItems * 32) +
+         (uint64_t)g * 128 + 4u * (threadIdx.x & 31);
+}
 __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n_max,
                                                             Len len, uint32_t* bsum) {
   __shared__ uint32_t s_w[32];
   const uint64_t n = live_len(n_max, len);
   if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
-  const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
   uint32_t v = 0;
 #pragma unroll
-  for (int j = 0; j < kScanItems; ++j)
-    if (base + j < n) v += in[base + j];
+  for (int g = 0; g < kScanGroups; ++g) {
+    const uint4 x = scan_load4(in, scan_group_base(g), n);
+    v += x.x + x.y + x.z + x.w;
+  }
   uint32_t ex, tot;
   block_excl_scan<32>(v, ex, tot, s_w);
   if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
@@ -100,27 +119,47 @@ __global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint6
   }
   if (threadIdx.x == 0 && total) *total = carry;
 }
+// in and out may be the same array: a block reads its whole chunk before
+// writing any of it.
 __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
                                                            uint64_t n_max, Len len,
                                                            const uint32_t* bsum) {
   __shared__ uint32_t s_w[32];
   const uint64_t n = live_len(n_max, len);
   if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
-  const uint64_t base = (uint64_t)blockIdx.x * kScanChunk + (uint64_t)threadIdx.x * kScanItems;
-  uint32_t x[kScanItems];
+  const uint32_t lane = threadIdx.x & 31;
+  uint4 x[kScanGroups];
   uint32_t v = 0;
 #pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    x[j] = base + j < n ? in[base + j] : 0u;
-    v += x[j];
+  for (int g = 0; g < kScanGroups; ++g) {
+    x[g] = scan_load4(in, scan_group_base(g), n);
+    v += x[g].x + x[g].y + x[g].z + x[g].w;
   }
+  // Lane 0's exclusive prefix (lanes in order) is the total of the warps
+  // before this one.
   uint32_t ex, tot;
   block_excl_scan<32>(v, ex, tot, s_w);
-  uint32_t run = bsum[blockIdx.x] + ex;
+  uint32_t run = bsum[blockIdx.x] + __shfl_sync(kFull, ex, 0);
 #pragma unroll
-  for (int j = 0; j < kScanItems; ++j) {
-    if (base + j < n) out[base + j] = run;
-    run += x[j];
+  for (int g = 0; g < kScanGroups; ++g) {
+    const uint32_t gs = x[g].x + x[g].y + x[g].z + x[g].w;
+    uint32_t incl = gs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= (uint32_t)o) incl += y;
+    }
+    const uint32_t e0 = run + incl - gs;
+    const uint4 r = make_uint4(e0, e0 + x[g].x, e0 + x[g].x + x[g].y, e0 + x[g].x + x[g].y + x[g].z);
+    run += __shfl_sync(kFull, incl, 31);
+    const uint64_t b = scan_group_base(g);
+    if (b + 4 <= n) {
+      *reinterpret_cast<uint4*>(out + b) = r;
+    } else if (b < n) {
+      out[b] = r.x;
+      if (b + 1 < n) out[b + 1] = r.y;
+      if (b + 2 < n) out[b + 2] = r.z;
+    }
   }
 }
 inline size_t scan_tmp_words(uint64_t n) { return (size_t)ceil_div(n ? n : 1, kScanChunk); }
@@ -142,10 +181,52 @@ int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_
 // first *n_dev items of arrays that hold up to n_max. counts is
 // [256][tiles], digit-major, so its exclusive scan gives each (digit, tile)
 // its first output position.
-__global__ void __launch_bounds__(kSortThreads) radix_count(const uint64_t* key,
+//
+// Passes on a digit that every key shares keep the order, so they are
+// skipped: `diff` (the OR of key ^ key[0] over the items, worked out on the
+// device before the first pass) says which digits vary. The host launches
+// every pass; a skipped one returns at once, and the others find their
+// input buffer from the number of passes run before them. A last kernel
+// moves the result into the buffer the host expects when the two differ.
+__device__ __forceinline__ bool pass_runs(uint64_t diff, uint32_t shift) {
+  return ((diff >> shift) & 255u) != 0;
+}
+__device__ __forceinline__ uint32_t passes_run_below(uint64_t diff, uint32_t shift) {
+  uint32_t c = 0;
+  for (uint32_t t = 0; t < shift; t += 8) c += pass_runs(diff, t) ? 1u : 0u;
+  return c;
+}
+// One atomic per CTA: the warps' ORs meet in shared memory first.
+__global__ void __launch_bounds__(kThreads) radix_diff(const uint64_t* key, const uint32_t* n_dev,
+                                                       unsigned long long* diff) {
+  __shared__ unsigned long long s_or;
+  const uint64_t n = *n_dev;
+  if (n == 0) return;
+  if (threadIdx.x == 0) s_or = 0;
+  __syncthreads();
+  const uint64_t k0 = key[0];
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  uint64_t d = 0;
+  uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n; i += 4 * stride)
+    d |= (key[i] ^ k0) | (key[i + stride] ^ k0) | (key[i + 2 * stride] ^ k0) |
+         (key[i + 3 * stride] ^ k0);
+  for (; i < n; i += stride) d |= key[i] ^ k0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d |= __shfl_xor_sync(kFull, d, o);
+  if ((threadIdx.x & 31) == 0 && d) atomicOr(&s_or, (unsigned long long)d);
+  __syncthreads();
+  if (threadIdx.x == 0 && s_or) atomicOr(diff, s_or);
+}
+__global__ void __launch_bounds__(kSortThreads) radix_count(const uint64_t* key0,
+                                                            const uint64_t* key1, uint32_t cur0,
+                                                            const unsigned long long* diff,
                                                             const uint32_t* n_dev, uint32_t shift,
                                                             uint32_t* counts, uint32_t tiles) {
   __shared__ uint32_t hist[256];
+  const uint64_t dv = *diff;
+  if (!pass_runs(dv, shift)) return;
+  const uint64_t* key = ((cur0 + passes_run_below(dv, shift)) & 1u) ? key1 : key0;
   const uint64_t n = *n_dev;
   const uint64_t t0 = (uint64_t)blockIdx.x * kSortTile;
   if (t0 >= n) return;  // past the items: not a column entry
@@ -170,10 +251,18 @@ constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kWarpItems = (int)(kSortTile / kSortWarps);  // 512
 constexpr size_t kScatterSmem =
     sizeof(uint32_t) * (kSortWarps * 256 + 256 + 256 + 32) + kSortTile * (8 + 4);
-__global__ void __launch_bounds__(kSortThreads) radix_scatter(
-    const uint64_t* key, const uint32_t* val, const uint32_t* n_dev, uint32_t shift,
-    const uint32_t* offs, uint32_t tiles, uint64_t* key_out, uint32_t* val_out) {
+__global__ void __launch_bounds__(kSortThreads, 2) radix_scatter(
+    uint64_t* key0, uint64_t* key1, uint32_t* val0, uint32_t* val1, uint32_t cur0,
+    const unsigned long long* diff, const uint32_t* n_dev, uint32_t shift, const uint32_t* offs,
+    uint32_t tiles) {
   extern __shared__ __align__(16) unsigned char smem[];
+  const uint64_t dv = *diff;
+  if (!pass_runs(dv, shift)) return;
+  const bool from1 = ((cur0 + passes_run_below(dv, shift)) & 1u) != 0;
+  const uint64_t* key = from1 ? key1 : key0;
+  const uint32_t* val = from1 ? val1 : val0;
+  uint64_t* key_out = from1 ? key0 : key1;
+  uint32_t* val_out = from1 ? val0 : val1;
   uint64_t* s_key = reinterpret_cast<uint64_t*>(smem);                     // [kSortTile]
   uint32_t* s_val = reinterpret_cast<uint32_t*>(s_key + kSortTile);        // [kSortTile]
   uint32_t* s_hist = s_val + kSortTile;                                    // [warps][256]
@@ -243,12 +332,34 @@ __global__ void __launch_bounds__(kSortThreads) radix_scatter(
   }
 }
 
+// After `passes` launched passes the host expects the result in buffer
+// cur0 ^ (passes & 1); it is in cur0 ^ (passes run & 1).
+__global__ void __launch_bounds__(kThreads) radix_settle(uint64_t* key0, uint64_t* key1,
+                                                         uint32_t* val0, uint32_t* val1,
+                                                         uint32_t cur0, uint32_t passes,
+                                                         const unsigned long long* diff,
+                                                         const uint32_t* n_dev) {
+  const uint32_t ran = passes_run_below(*diff, 8u * passes);
+  if (((ran ^ passes) & 1u) == 0) return;
+  const bool in1 = ((cur0 + ran) & 1u) != 0;
+  const uint64_t* ks = in1 ? key1 : key0;
+  const uint32_t* vs = in1 ? val1 : val0;
+  uint64_t* kd = in1 ? key0 : key1;
+  uint32_t* vd = in1 ? val0 : val1;
+  const uint64_t n = *n_dev;
+  FOR_EACH(i, n) {
+    kd[i] = ks[i];
+    vd[i] = vs[i];
+  }
+}
+
 struct SortBufs {
   uint64_t* key[2];
   uint32_t* val[2];
-  uint32_t* counts;  // [256][tiles]
-  uint32_t* bsum;    // scan scratch
+  uint32_t* counts;           // [256][tiles]
+  uint32_t* bsum;             // scan scratch
   uint64_t n_max;
+  unsigned long long* diff;   // OR of key ^ key[0] over the items
 };
 inline uint32_t sort_tiles(uint64_t n_max) { return (uint32_t)ceil_div(n_max ? n_max : 1, kSortTile); }
 inline size_t sort_count_words(uint64_t n_max) { return (size_t)256 * sort_tiles(n_max); }
@@ -266,23 +377,40 @@ int prepare_scatter() {
   return 0;
 }
 // Sorts by bits [0, bits) of the key; the result is in buffer `cur` on return.
-int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, cudaStream_t s) {
+// skip_shared: look for digits every key shares and skip their passes (a
+// sort whose key width is already tight runs every pass without looking).
+int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip_shared,
+               cudaStream_t s) {
   if (int rc = prepare_scatter()) return rc;
   const uint32_t tiles = sort_tiles(b.n_max);
   const uint64_t nc = (uint64_t)256 * tiles;
-  for (int shift = 0; shift < bits; shift += 8) {
-    radix_count<<<tiles, kSortThreads, 0, s>>>(b.key[cur], n_dev, (uint32_t)shift, b.counts, tiles);
-    int rc = launch_result();
-    if (rc) return rc;
+  const uint32_t cur0 = (uint32_t)cur;
+  if (cudaMemsetAsync(b.diff, skip_shared ? 0 : 0xFF, sizeof(*b.diff), s) != cudaSuccess)
+    return launch_result();
+  int rc = 0;
+  if (skip_shared) {
+    const unsigned dg = grid_for(b.n_max) < (unsigned)num_sms() * 4 ? grid_for(b.n_max)
+                                                                      : (unsigned)num_sms() * 4;
+    radix_diff<<<dg, kThreads, 0, s>>>(b.key[cur0], n_dev, b.diff);
+    if ((rc = launch_result())) return rc;
+  }
+  uint32_t passes = 0;
+  for (int shift = 0; shift < bits; shift += 8, ++passes) {
+    radix_count<<<tiles, kSortThreads, 0, s>>>(b.key[0], b.key[1], cur0, b.diff, n_dev,
+                                               (uint32_t)shift, b.counts, tiles);
+    if ((rc = launch_result())) return rc;
     if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s, Len{n_dev, 256u, (uint32_t)kSortTile})))
       return rc;
-    radix_scatter<<<tiles, kSortThreads, kScatterSmem, s>>>(
-        b.key[cur], b.val[cur], n_dev, (uint32_t)shift, b.counts, tiles, b.key[cur ^ 1],
-        b.val[cur ^ 1]);
+    radix_scatter<<<tiles, kSortThreads, kScatterSmem, s>>>(b.key[0], b.key[1], b.val[0], b.val[1],
+                                                            cur0, b.diff, n_dev, (uint32_t)shift,
+                                                            b.counts, tiles);
     if ((rc = launch_result())) return rc;
     cur ^= 1;
   }
-  return 0;
+  if (!skip_shared) return 0;
+  radix_settle<<<grid_for(b.n_max), kThreads, 0, s>>>(b.key[0], b.key[1], b.val[0], b.val[1], cur0,
+                                                      passes, b.diff, n_dev);
+  return launch_result();
 }
 
 // ------------------------------------------------------------- registration
@@ -451,7 +579,7 @@ __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_cou
 
 struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
-      nstart, nend, nfirst, nrefs, npos, total;
+      diff, nstart, nend, nfirst, nrefs, npos, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -472,6 +600,7 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.val1 = take(q * 4);
   L.counts = take(sort_count_words(q) * 4);
   L.bsum = take(scan_tmp_words(sort_count_words(q) > q ? sort_count_words(q) : q) * 4);
+  L.diff = take(8);
   L.nstart = take(q * 8);
   L.nend = take(q * 8);
   L.nfirst = take(q * 4);
@@ -553,7 +682,7 @@ __global__ void dereg_final(const DeregHeader* h, db_counters* ctr) {
 }
 
 struct DeregLayout {
-  size_t hdr, key0, key1, val0, val1, counts, bsum, flag, excl, rs, dec, keep, kpos, total;
+  size_t hdr, key0, key1, val0, val1, counts, bsum, diff, flag, excl, rs, dec, keep, kpos, total;
 };
 DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
   DeregLayout L;
@@ -568,6 +697,7 @@ DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
   L.counts = take(sort_count_words(q) * 4);
   const uint64_t scan_n = sort_count_words(q) > q ? sort_count_words(q) : q;
   L.bsum = take(scan_tmp_words(scan_n > n ? scan_n : n) * 4);
+  L.diff = take(8);
   L.flag = take(q * 4);
   L.excl = take(q * 4);
   L.rs = take(q * 4);
@@ -630,7 +760,8 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
   uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
   SortBufs sb{{static_cast<uint64_t*>(at(L.key0)), static_cast<uint64_t*>(at(L.key1))},
               {static_cast<uint32_t*>(at(L.val0)), static_cast<uint32_t*>(at(L.val1))},
-              static_cast<uint32_t*>(at(L.counts)), bsum, n_q};
+              static_cast<uint32_t*>(at(L.counts)), bsum, n_q,
+              static_cast<unsigned long long*>(at(L.diff))};
   uint64_t* nstart = static_cast<uint64_t*>(at(L.nstart));
   uint64_t* nend = static_cast<uint64_t*>(at(L.nend));
   uint32_t* nfirst = static_cast<uint32_t*>(at(L.nfirst));
@@ -658,11 +789,11 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     // 3. sort the misses by (start, end), stable in request order
     const int bits = 64 - (int)granule_shift;
     int cur = 0;
-    if ((rc = radix_sort(sb, cur, &h->m, bits, s))) return rc;
+    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
     reg_rekey<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sb.val[cur],
                                                  sb.key[cur]);
     if ((rc = launch_result())) return rc;
-    if ((rc = radix_sort(sb, cur, &h->m, bits, s))) return rc;
+    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
     // 4. runs of equal ranges are the new records
     const uint32_t* sval = sb.val[cur];
     reg_runs<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sval, flag);
@@ -734,7 +865,8 @@ extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint6
   uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
   SortBufs sb{{static_cast<uint64_t*>(at(L.key0)), static_cast<uint64_t*>(at(L.key1))},
               {static_cast<uint32_t*>(at(L.val0)), static_cast<uint32_t*>(at(L.val1))},
-              static_cast<uint32_t*>(at(L.counts)), bsum, n_h};
+              static_cast<uint32_t*>(at(L.counts)), bsum, n_h,
+              static_cast<unsigned long long*>(at(L.diff))};
   uint32_t* flag = static_cast<uint32_t*>(at(L.flag));
   uint32_t* excl = static_cast<uint32_t*>(at(L.excl));
   uint32_t* rs = static_cast<uint32_t*>(at(L.rs));
@@ -754,7 +886,7 @@ extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint6
     while (bits < 64 && (n_mr >> bits)) ++bits;  // keys are at most n_mr
     bits = (bits + 7) & ~7;
     int cur = 0;
-    if ((rc = radix_sort(sb, cur, &h->n_h, bits, s))) return rc;
+    if ((rc = radix_sort(sb, cur, &h->n_h, bits, false, s))) return rc;
     dereg_runs<<<grid_for(n_h), kThreads, 0, s>>>(sb.key[cur], n_h, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, excl, n_h, nullptr, bsum, s))) return rc;

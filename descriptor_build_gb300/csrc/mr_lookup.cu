@@ -155,7 +155,7 @@ __device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32
                : "memory");
 }
 
-__global__ void __launch_bounds__(kBuildThreads) mr_index_kernel(const BuildParams p) {
+__global__ void __launch_bounds__(kBuildThreads, 4) mr_index_kernel(const BuildParams p) {
   const uint64_t lo = p.start[0];
   const uint64_t hi = p.start[p.n_mr - 1];
   const uint64_t span = hi > lo ? hi - lo : 0;
