@@ -244,7 +244,10 @@ int db_mr_lookup_overlap(const db_range* q, uint64_t n_q, const uint64_t* mr_sta
  *   rkeys       [world]
  *   world, n_qp PEs and queue pairs per PE; 1 <= world * n_qp <= 1024
  *   local_base, lkey, heap_size  the local object
- *   rings       [world * n_qp][depth] db_wqe (64-byte aligned)
+ *   rings       [world * n_qp][depth] db_wqe (64-byte aligned), in device memory or
+ *               in pinned host memory (a send queue the NIC reads may sit in either;
+ *               the kernel then writes each WQE across the CPU-GPU link). Only the
+ *               entries of this batch are written; the kernel reads none.
  *   depth       entries per ring, a power of two
  *   head        [world * n_qp] in/out post indices
  *   count       [world * n_qp] output: valid puts per ring in this batch

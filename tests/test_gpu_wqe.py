@@ -177,3 +177,20 @@ def test_columns_longer_than_one_scan_round(db, oracle):
     want = oracle.wqe_bucket(req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head, fill=0xCD)
     got = run_gpu(db, req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head)
     check(got, want)
+
+
+@pytest.mark.parametrize("depth", [1 << 14, 256])  # 256: every ring overflows and stays untouched
+def test_rings_in_pinned_host_memory(db, oracle, depth):
+    """The WQEs written straight into rings in pinned host memory equal the
+    oracle's, and so do the slots the batch leaves alone."""
+    rng = np.random.default_rng(515 + depth)
+    n, world, n_qp, heap = 50000, 8, 4, 1 << 32
+    req = random_puts(rng, n, world, n_qp, heap)
+    peer = (rng.integers(1 << 19, 1 << 26, size=world) << 21).astype(np.uint64)
+    rkeys = rng.integers(0, 2**32, size=world, dtype=np.uint64).astype(np.uint32)
+    head = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    lb, lk = 0x7F0000000000, 0xC0FFEE
+    want = oracle.wqe_bucket(req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head, fill=0xCD)
+    rings = torch.full((world * n_qp, depth, 64), 0xCD, dtype=torch.uint8).pin_memory()
+    got = run_gpu(db, req, peer, rkeys, world, n_qp, lb, lk, heap, depth, head, rings=rings)
+    check(got, want)
