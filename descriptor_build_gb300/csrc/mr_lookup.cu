@@ -46,7 +46,7 @@ namespace mr {
 #define DB_MR_BUCKET_SHIFT 0
 #endif
 #ifndef DB_MR_BUCKET_DOWN
-#define DB_MR_BUCKET_DOWN 1  // log2 of records per bucket (measured best: two)
+#define DB_MR_BUCKET_DOWN 1  // log2 of the fewest records per bucket (measured best: two)
 #endif
 constexpr int kBuildThreads = 256;
 constexpr int kThreads = DB_MR_THREADS;
@@ -71,7 +71,10 @@ constexpr size_t kHeaderBytes = 256;
 
 inline uint32_t buckets_for(uint64_t n_mr) {
   uint64_t nb = 1024;
-  while (nb < ((n_mr << DB_MR_BUCKET_SHIFT) >> DB_MR_BUCKET_DOWN) && nb < (1u << 22)) nb <<= 1;
+  // The largest power of two at most n_mr / 2 (at least 1024): a directory
+  // rounded up instead can be nearly twice as large, and tables plus
+  // directory then no longer stay in L2.
+  while (nb * 2 <= ((n_mr << DB_MR_BUCKET_SHIFT) >> DB_MR_BUCKET_DOWN) && nb < (1u << 22)) nb <<= 1;
   return (uint32_t)nb;
 }
 // Directory entry of bucket b: the records starting below the bucket
