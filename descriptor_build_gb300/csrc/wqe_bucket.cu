@@ -12,15 +12,15 @@
 //   count    a warp per tile: a warp-private shared-memory histogram over
 //            the R rings plus one bin for invalid puts, written column-major:
 //            counts[ring][tile].
-//   scan     one CTA per ring: exclusive scan of its column in place (staged
-//            through shared memory), the ring's batch total, count[], the
+//   scan     one CTA per ring: exclusive scan of its column in place (each
+//            warp a contiguous span), the ring's batch total, count[], the
 //            overflow decision, the head; the last CTA publishes the counters.
 //   scatter  a warp per tile, with no CTA-wide barrier: the tile's puts go to
 //            warp-private shared memory; stable rank of each put inside its
 //            row with __match_any_sync and across the 8 rows by a per-ring
 //            prefix; a 2-byte permutation puts the tile in ring order, and
-//            each ring's run is written out contiguously, two 32-byte stores
-//            per WQE from a pair of lanes.
+//            each ring's run is written out contiguously, a lane writing a
+//            WQE's two 32-byte halves.
 // No kernel waits on another CTA.
 #include "common.cuh"
 
@@ -438,11 +438,9 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
   }
   __syncwarp();
   // 4. Write-out, each ring's run contiguous in its ring (up to one wrap):
-  //    lanes 2q and 2q + 1 write the two halves of the WQE of position q.
-  const uint32_t n_out = 2 * carry;
+  //    lane l writes the WQEs of positions l, l + 32, ..., both halves.
   const uint64_t slot_mask = p.depth - 1;
-  for (uint32_t f = lane; f < n_out; f += 32) {
-    const uint32_t q = f >> 1, h = f & 1;
+  for (uint32_t q = lane; q < carry; q += 32) {
     const uint32_t o = s_perm[q];
     const ulonglong2 x = s_put[o];
     const uint32_t pe = (uint32_t)(x.y >> 32) & 0xFFFFu, qp = (uint32_t)(x.y >> 48);
@@ -450,12 +448,10 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
     const uint64_t slots = s_slots[v];
     if (!slots) continue;
     const uint64_t seq = s_seq0[v] + (q - s_run[v]);
-    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6)) + 32 * h;
-    if (h == 0)
-      st_stream32(d, s_peer[pe] + x.x, p.local_base + x.x,
-                  (uint64_t)(uint32_t)x.y | ((uint64_t)p.lkey << 32), (uint64_t)s_rkey[pe], pol_first);
-    else
-      st_stream32(d, seq, t0 + o, 0ull, 0ull, pol_first);
+    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6));
+    st_stream32(d, s_peer[pe] + x.x, p.local_base + x.x,
+                (uint64_t)(uint32_t)x.y | ((uint64_t)p.lkey << 32), (uint64_t)s_rkey[pe], pol_first);
+    st_stream32(d + 32, seq, t0 + o, 0ull, 0ull, pol_first);
   }
 }
 
@@ -632,16 +628,15 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
     if (p.mtu) s_prun[v] = s_pstart[s_run[v]];
   }
   __syncwarp();
-  // 5. Write-out: lanes 2w and 2w + 1 write the two halves of the tile's
-  //    WQE w (ring order); its put is the last one whose first WQE is at or
-  //    before w.
+  // 5. Write-out: lane l writes the tile's WQEs l, l + 32, ... (ring order),
+  //    both halves; a WQE's put is the last one whose first WQE is at or
+  //    before it.
   const uint64_t C = 1ull << p.cshift;
   const uint64_t slot_mask = p.depth - 1;
-  for (uint64_t f = lane; f < 2ull * n_wqe; f += 32) {
-    const uint32_t wq = (uint32_t)(f >> 1), h = (uint32_t)(f & 1);
+  const uint32_t extra = n_wqe - n_valid;
+  for (uint32_t wq = lane; wq < n_wqe; wq += 32) {
     // Every put makes at least one WQE, so WQE wq belongs to a put in
-    // [wq - (n_wqe - n_valid), wq]: search only there.
-    const uint32_t extra = n_wqe - n_valid;
+    // [wq - extra, wq]: search only there.
     uint32_t lo = wq > extra ? wq - extra : 0u;
     uint32_t hi = (wq + 1 < n_valid ? wq + 1 : n_valid);  // s_wstart[lo] <= wq < s_wstart[hi]
     while (hi - lo > 1) {
@@ -661,20 +656,16 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
     const uint64_t start = frag == 0 ? pu.x : (c << p.cshift);
     const uint64_t stop = pu.x + (uint32_t)pu.y;
     const uint64_t end = ((c + 1) << p.cshift) < stop ? ((c + 1) << p.cshift) : stop;
-    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6)) + 32 * h;
-    if (h == 0) {
-      // one 16-byte read for the chunk's remote address, rkey and lkey
-      const ulonglong2 ck = ld_table16(p.chunk_pack + (uint64_t)pe * p.n_chunks + c, pol_last);
-      st_stream32(d, ck.x + (start & (C - 1)), p.local_base + start,
-                  (end - start) | (ck.y & 0xFFFFFFFF00000000ull), ck.y & 0xFFFFFFFFull,
-                  pol_first);
-    } else {
-      // u32 batch index at byte 40, first PSN at byte 44
-      uint64_t w5 = t0 + o;
-      if (p.mtu)
-        w5 |= (uint64_t)(s_psn0[v] + (s_pstart[lo] - s_prun[v]) + psns_before(p, pu.x, frag)) << 32;
-      st_stream32(d, seq, w5, 0ull, 0ull, pol_first);
-    }
+    unsigned char* d = reinterpret_cast<unsigned char*>(slots + ((seq & slot_mask) << 6));
+    // one 16-byte read for the chunk's remote address, rkey and lkey
+    const ulonglong2 ck = ld_table16(p.chunk_pack + (uint64_t)pe * p.n_chunks + c, pol_last);
+    st_stream32(d, ck.x + (start & (C - 1)), p.local_base + start,
+                (end - start) | (ck.y & 0xFFFFFFFF00000000ull), ck.y & 0xFFFFFFFFull, pol_first);
+    // u32 batch index at byte 40, first PSN at byte 44
+    uint64_t w5 = t0 + o;
+    if (p.mtu)
+      w5 |= (uint64_t)(s_psn0[v] + (s_pstart[lo] - s_prun[v]) + psns_before(p, pu.x, frag)) << 32;
+    st_stream32(d + 32, seq, w5, 0ull, 0ull, pol_first);
   }
 }
 
