@@ -160,6 +160,9 @@ constexpr int kCountWarps = kCountThreads / 32;
 #endif
 constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at once
 
+// kVmm / kPsn: the call's heap kind and whether PSNs are counted, fixed at
+// compile time so that the common static-heap pass carries no per-put tests.
+template <bool kVmm, bool kPsn>
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
   extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V] WQEs, then PSNs if asked
   const uint32_t V = p.V;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
        tile += n_warps) {
     for (uint32_t v = lane; v < V; v += 32) {
       s_hist[v] = 0;
-      if (p.mtu) s_psn[v] = 0;
+      if (kPsn) s_psn[v] = 0;
     }
     __syncwarp();
     for (int row = 0; row < kTile / 32; row += kCountUnroll) {
@@ -186,13 +189,13 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
       for (int u = 0; u < kCountUnroll; ++u) {
         const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
         const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
-        if (p.mtu && bin < p.R) atomicAdd(&s_psn[bin], psns_of(p, r[u]));
+        if (kPsn && bin < p.R) atomicAdd(&s_psn[bin], psns_of(p, r[u]));
         if (DB_WQE_COUNT_MODE == 1) {
-          if (bin < p.R) atomicAdd(&s_hist[bin], wqes_of(p, r[u]));
+          if (bin < p.R) atomicAdd(&s_hist[bin], kVmm ? wqes_of(p, r[u]) : 1u);
           else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
         } else {
           const uint32_t peers = __match_any_sync(kFull, bin);
-          if (p.vmm) {  // weights differ per put
+          if (kVmm) {  // weights differ per put
             if (bin < p.R) atomicAdd(&s_hist[bin], wqes_of(p, r[u]));
             else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
           } else if (bin < V && (peers & lanemask_lt()) == 0) {
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
     __syncwarp();
     for (uint32_t v = lane; v < V; v += 32) {
       p.counts[v * p.stride + tile] = s_hist[v];
-      if (p.mtu) p.psn_counts[v * p.stride + tile] = s_psn[v];
+      if (kPsn) p.psn_counts[v * p.stride + tile] = s_psn[v];
     }
     __syncwarp();
   }
@@ -682,8 +685,15 @@ int prepare_scatter() {
                              (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
     // Two histograms (WQEs and PSNs) of up to 1025 bins per warp.
-    e = cudaFuncSetAttribute(wqe_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kCountWarps * (kMaxRings + 1) * 4 * 2));
+    const int count_smem = (int)((size_t)kCountWarps * (kMaxRings + 1) * 4 * 2);
+    e = cudaFuncSetAttribute(wqe_count_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wqe_count_kernel<true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wqe_count_kernel<true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
     if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
   }
@@ -777,8 +787,15 @@ int run(const wqe::Params& p, cudaStream_t s) {
   uint64_t count_grid = (uint64_t)num_sms() * 8;
   const uint64_t count_need = (p.n_tiles + wqe::kCountWarps - 1) / wqe::kCountWarps;
   if (count_grid > count_need) count_grid = count_need;
-  wqe::wqe_count_kernel<<<(unsigned)count_grid, wqe::kCountThreads,
-                          (size_t)wqe::kCountWarps * p.V * 4 * (p.mtu ? 2 : 1), s>>>(p);
+  {
+    const size_t count_smem = (size_t)wqe::kCountWarps * p.V * 4 * (p.mtu ? 2 : 1);
+    if (!p.vmm)
+      wqe::wqe_count_kernel<false, false><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+    else if (!p.mtu)
+      wqe::wqe_count_kernel<true, false><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+    else
+      wqe::wqe_count_kernel<true, true><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+  }
   rc = launch_result();
   if (rc) return rc;
   wqe::wqe_scan_kernel<<<p.V * (p.mtu ? 2 : 1), wqe::kScanThreads, 0, s>>>(p);
