@@ -251,7 +251,7 @@ constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kWarpItems = (int)(kSortTile / kSortWarps);  // 512
 constexpr size_t kScatterSmem =
     sizeof(uint32_t) * (kSortWarps * 256 + 256 + 256 + 32) + kSortTile * (8 + 4);
-__global__ void __launch_bounds__(kSortThreads, 2) radix_scatter(
+__global__ void __launch_bounds__(kSortThreads, 3) radix_scatter(
     uint64_t* key0, uint64_t* key1, uint32_t* val0, uint32_t* val1, uint32_t cur0,
     const unsigned long long* diff, const uint32_t* n_dev, uint32_t shift, const uint32_t* offs,
     uint32_t tiles) {
