@@ -14,6 +14,9 @@ one stream, in turn):
 batches), with inputs resident in HBM. Each call is also timed with CUDA
 events alone on the stream, in the same steps run one call at a time after
 the timed region; the dominant one (prp_large) gives the roofline line.
+Beside each call, a plain device copy of the same algorithmic bytes timed the
+same way (``size_matched_copy_ms``): small batches cannot reach the peak copy
+rate, and the ratio shows how near a call is to a copy of its own size.
 ``output_GB_per_s`` counts the descriptor bytes written (PRP pairs, list
 words, MR results, WQEs), for the step and per call. ``e2e`` repeats the
 step through the same API with inputs in pinned host memory and every
@@ -746,6 +749,7 @@ def run_ours(args, inp, world, device, dist):
     alg = algorithmic_bytes(inp)
     outb = output_bytes(inp)
     peak, peak_kind = peak_gbs()
+    copy_ms = size_matched_copy_ms(torch, [n for n, _ in calls], alg, K, stream, device)
     reqs_per_step = sum(u.values())
     ms_per_step = total_ms / K
     value = job_throughput(world, reqs_per_step, ms_per_step)
@@ -758,7 +762,9 @@ def run_ours(args, inp, world, device, dist):
                          "frac_of_peak": round(gbs / peak, 4),
                          "output_bytes": outb[name],
                          "output_GB_per_s": round(outb[name] / (ms * 1e-3) / 1e9, 1),
-                         "launches": Step.LAUNCHES[name]}
+                         "launches": Step.LAUNCHES[name],
+                         "size_matched_copy_ms": round(copy_ms[name], 4),
+                         "frac_of_size_matched_copy": round(copy_ms[name] / ms, 4)}
         if not args.serial:
             kernels[name]["concurrent_span_ms"] = round(span_ms[name], 4)
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -792,6 +798,44 @@ def run_ours(args, inp, world, device, dist):
         out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world,
                              serial=args.serial)
     return out
+
+
+def size_matched_copy_ms(torch, names, alg, K, stream, device) -> dict:
+    """Per workload, the mean time of a plain device copy that moves the same
+    algorithmic bytes (half read, half written), timed like the calls: CUDA
+    events on the launching stream, the workloads' copies in the step's order
+    so that each one starts with the others' data in L2. A kernel cannot move
+    its bytes faster than such a copy, and for small batches the copy itself is
+    far below the peak copy rate (launch and DRAM latency dominate), so the
+    ratio says how close a call is to the HBM bound at its own size."""
+    half = {n: (alg[n] // 2 + 255) & ~255 for n in names}
+    off, o = {}, 0
+    for n in names:  # disjoint regions: no copy finds another's lines in L2
+        off[n] = o
+        o += half[n]
+    src = torch.empty(o, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    view = lambda b, n: b[off[n]: off[n] + half[n]]
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    t = {n: [] for n in names}
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm-up
+            for n in names:
+                view(dst, n).copy_(view(src, n))
+        pairs = []
+        for _ in range(K):
+            for n in names:
+                e0, e1 = ev(), ev()
+                e0.record(stream)
+                view(dst, n).copy_(view(src, n))
+                e1.record(stream)
+                pairs.append((n, e0, e1))
+    torch.cuda.synchronize(device)
+    for n, e0, e1 in pairs:
+        t[n].append(e0.elapsed_time(e1))
+    del src, dst
+    return {n: statistics.mean(v) for n, v in t.items()}
 
 
 def run_e2e(st, stream, inp, K, device, dist, world, serial=False):

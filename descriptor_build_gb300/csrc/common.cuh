@@ -292,4 +292,33 @@ int launch_result();
 int cuda_failure(cudaError_t e);
 int num_sms();
 
+// Programmatic dependent launch: the kernel may start once every CTA of the
+// kernel before it on `s` has started (or that kernel has ended), and must
+// execute `griddepcontrol.wait` before it reads what that kernel writes.
+// Every kernel launched this way waits before it exits, so the kernels after
+// it still see the whole stream before them complete.
+template <typename P>
+inline int launch_dependent(void (*kernel)(P), unsigned grid, unsigned block, size_t smem,
+                            cudaStream_t s, const P& params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, params);
+  if (e != cudaSuccess) return cuda_failure(e);
+  return launch_result();
+}
+__device__ __forceinline__ void dependents_may_launch() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+__device__ __forceinline__ void wait_for_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace db

@@ -48,6 +48,20 @@ namespace mr {
 #ifndef DB_MR_BUCKET_DOWN
 #define DB_MR_BUCKET_DOWN 1  // log2 of the fewest records per bucket (measured best: two)
 #endif
+// Directory and record reads of the lookup: 1 skips the L1 allocation (the
+// reads are random and never reused by the same SM).
+#ifndef DB_MR_GATHER_NOALLOC
+#define DB_MR_GATHER_NOALLOC 1
+#endif
+// 1: the lookup is launched as a programmatic dependent of the index build,
+// so its CTAs start and load their first queries while the build finishes.
+#ifndef DB_MR_PDL
+#define DB_MR_PDL 1
+#endif
+// Index build grid: at most this many CTAs per SM (threads loop over records).
+#ifndef DB_MR_BUILD_CTAS_PER_SM
+#define DB_MR_BUILD_CTAS_PER_SM 4
+#endif
 constexpr int kBuildThreads = 256;
 constexpr int kThreads = DB_MR_THREADS;
 constexpr int kQPT = DB_MR_QPT;
@@ -159,6 +173,7 @@ __device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32
 }
 
 __global__ void __launch_bounds__(kBuildThreads, 4) mr_index_kernel(const BuildParams p) {
+  if (DB_MR_PDL) dependents_may_launch();
   const uint64_t lo = p.start[0];
   const uint64_t hi = p.start[p.n_mr - 1];
   const uint64_t span = hi > lo ? hi - lo : 0;
@@ -254,6 +269,16 @@ __device__ __forceinline__ uint32_t first_reaching(const Rec* rec, uint32_t j, u
   return (uint32_t)hi;
 }
 
+__device__ __forceinline__ void ld_gather32(const void* a, uint64_t pol, uint64_t& x, uint64_t& y,
+                                            uint64_t& z, uint64_t& w) {
+  if (DB_MR_GATHER_NOALLOC)
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u64 {%0, %1, %2, %3}, [%4], %5;"
+        : "=l"(x), "=l"(y), "=l"(z), "=l"(w)
+        : "l"(a), "l"(pol));
+  else
+    ld_table32(a, pol, x, y, z, w);
+}
+
 // kGranuleShift: queries are widened to whole granules of 2^kGranuleShift
 // bytes (12: 4 KiB pages; 16: the 64 KiB registry granule). The directory
 // works in 4 KiB pages either way, since every granule boundary is one.
@@ -262,11 +287,7 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
   constexpr uint64_t kGran = 1ull << kGranuleShift;
   const uint64_t pol_first = policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
-  const uint64_t lo = p.hdr_ro->lo;
-  const uint32_t shift = p.hdr_ro->shift;
-  const uint32_t nb = p.hdr_ro->nb;
   const uint64_t n_mr = p.n_mr;
-  const bool offsets_kept = shift <= kMaxOffsetShift;
   constexpr uint64_t kGroup = (uint64_t)kThreads * kQPT;  // queries per CTA step
   const uint64_t n_groups = (p.n_q + kGroup - 1) / kGroup;
   uint32_t hits = 0, invalid = 0;
@@ -280,6 +301,15 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
     const uint64_t i = g * kGroup + (uint64_t)k * kThreads + threadIdx.x;
     nq[k] = (g < n_groups && i < p.n_q) ? ld_stream16(p.q + i, pol_first) : make_ulonglong2(0, 0);
   }
+  // Launched as a dependent of the index build: everything the build writes
+  // (header, directory, records) is read only after this wait. The queries
+  // above are the caller's input, complete before the build started. Without
+  // a programmatic launch the wait returns at once.
+  wait_for_prerequisites();
+  const uint64_t lo = p.hdr_ro->lo;
+  const uint32_t shift = p.hdr_ro->shift;
+  const uint32_t nb = p.hdr_ro->nb;
+  const bool offsets_kept = shift <= kMaxOffsetShift;
   for (; g < n_groups; g += gridDim.x) {
     const uint64_t first = g * kGroup + threadIdx.x;
     uint64_t base[kQPT], aend[kQPT];
@@ -319,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
         uint64_t b = (base[k] - lo) >> shift;
         b = b < nb ? b : nb;
         uint64_t w0, w1, w2, w3;
-        ld_table32(p.dir + b, pol_last, w0, w1, w2, w3);
+        ld_gather32(p.dir + b, pol_last, w0, w1, w2, w3);
         uint32_t x = (uint32_t)w0;
         x = x < n_mr ? x : (uint32_t)n_mr;
         // base's page offset in the bucket, capped below kNoOff
@@ -395,10 +425,10 @@ __global__ void __launch_bounds__(kThreads, DB_MR_MIN_CTAS) mr_lookup_kernel(con
       if (state[k] == 1 && a[k] > 0) {
         uint32_t j = a[k] - 1;
         uint64_t rs, re, rk, before;
-        ld_table32(&p.rec[j], pol_last, rs, re, rk, before);
+        ld_gather32(&p.rec[j], pol_last, rs, re, rk, before);
         if (kOverlap && before >= aend[k]) {
           j = first_reaching(p.rec, j, aend[k], pol_last);
-          ld_table32(&p.rec[j], pol_last, rs, re, rk, before);
+          ld_gather32(&p.rec[j], pol_last, rs, re, rk, before);
         }
         if (rs <= base[k] && aend[k] <= re) {
           out_idx = (int32_t)j;
@@ -581,7 +611,7 @@ int lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint
     }
     mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb, overlap, pm};
     uint64_t grid = (n_mr + mr::kBuildThreads - 1) / mr::kBuildThreads;
-    const uint64_t cap = (uint64_t)num_sms() * 8;
+    const uint64_t cap = (uint64_t)num_sms() * DB_MR_BUILD_CTAS_PER_SM;
     if (grid > cap) grid = cap;
     mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
     if ((rc = launch_result())) return rc;
@@ -592,12 +622,12 @@ int lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint
   uint64_t grid = (n_q + per_cta - 1) / per_cta;
   const uint64_t resident = (uint64_t)num_sms() * mr::lookup_ctas_per_sm();
   if (grid > resident) grid = resident;
-  if (granule_shift == 16)
-    mr::mr_lookup_kernel<true, 16><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
-  else if (overlap)
-    mr::mr_lookup_kernel<true, 12><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
-  else
-    mr::mr_lookup_kernel<false, 12><<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
+  void (*kern)(const mr::LookupParams) = granule_shift == 16 ? mr::mr_lookup_kernel<true, 16>
+                                         : overlap            ? mr::mr_lookup_kernel<true, 12>
+                                                              : mr::mr_lookup_kernel<false, 12>;
+  if (DB_MR_PDL && n_mr > 0)  // a dependent of the index build just launched on `s`
+    return launch_dependent(kern, (unsigned)grid, mr::kThreads, 0, s, l);
+  kern<<<(unsigned)grid, mr::kThreads, 0, s>>>(l);
   return launch_result();
 }
 

@@ -155,6 +155,12 @@ __device__ __forceinline__ uint32_t psns_before(const Params& p, uint64_t off, u
 // histogram; warps stride over tiles, so no block-wide barrier is needed.
 constexpr int kCountThreads = 256;
 constexpr int kCountWarps = kCountThreads / 32;
+// 1: the scan and scatter passes are launched as programmatic dependents of
+// the pass before them: their CTAs start while that pass finishes, and the
+// scatter loads its tile of puts (the caller's input) before it waits.
+#ifndef DB_WQE_PDL
+#define DB_WQE_PDL 1
+#endif
 #ifndef DB_WQE_COUNT_UNROLL
 #define DB_WQE_COUNT_UNROLL 8
 #endif
@@ -165,6 +171,7 @@ constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at 
 template <bool kVmm, bool kPsn>
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
   extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V] WQEs, then PSNs if asked
+  if (DB_WQE_PDL) dependents_may_launch();
   const uint32_t V = p.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* s_hist = s_hist_all + (size_t)warp * V;
@@ -231,6 +238,10 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
   __shared__ int s_last;
   // CTAs 0 .. V-1 scan the WQE columns, V .. 2V-1 (when PSNs are asked for)
   // the PSN columns.
+  if (DB_WQE_PDL) {
+    dependents_may_launch();
+    wait_for_prerequisites();  // the count pass's columns
+  }
   const bool psn_col = blockIdx.x >= p.V;
   const uint32_t v = psn_col ? blockIdx.x - p.V : blockIdx.x;
   uint32_t* col = (psn_col ? p.psn_counts : p.counts) + (uint64_t)v * p.stride;
@@ -371,6 +382,18 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
   uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_run + V);  // [kRows][V]
   uint16_t* s_perm = s_cnt + kRows * V;
 
+  // 1. Load the tile (all rows in flight at once): the puts are the
+  //    caller's input, so this comes before the wait for the scan pass.
+  const uint64_t tile = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  const uint64_t t0 = tile * kTile;
+  ulonglong2 r[kRows];
+#pragma unroll
+  for (int u = 0; u < kRows; ++u) {
+    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
+    r[u] = (tile < p.n_tiles && i < p.n) ? ld_stream16(p.req + i, pol_first)
+                                         : make_ulonglong2(0, 0);
+  }
+  if (DB_WQE_PDL) wait_for_prerequisites();  // slots, heads and prefixes of the scan pass
   for (uint32_t v = threadIdx.x; v < R; v += blockDim.x) {
     s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
     if (v < p.world) {
@@ -379,19 +402,11 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
     }
   }
   __syncthreads();  // the only CTA-wide barrier
-  const uint64_t tile = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
   if (tile >= p.n_tiles) return;
-  const uint64_t t0 = tile * kTile;
 
-  // 1. Load the tile (all rows in flight at once); ring of each put; rank
-  //    inside its row; per-row counts by the row's first put of each ring.
+  //    Ring of each put; rank inside its row; per-row counts by the row's
+  //    first put of each ring.
   for (uint32_t x = lane; x < kRows * V; x += 32) s_cnt[x] = 0;
-  ulonglong2 r[kRows];
-#pragma unroll
-  for (int u = 0; u < kRows; ++u) {
-    const uint64_t i = t0 + (uint64_t)u * 32 + lane;
-    r[u] = i < p.n ? ld_stream16(p.req + i, pol_first) : make_ulonglong2(0, 0);
-  }
   __syncwarp();
   uint32_t bin_rank[kRows];  // ring | rank << 16
 #pragma unroll
@@ -515,21 +530,24 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   uint32_t* s_psn0 = s_pstart + kTile + 1;                            // [V]
   uint32_t* s_prun = s_psn0 + V;                                      // [V]
 
-  for (uint32_t v = threadIdx.x; v < R; v += blockDim.x)
-    s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
-  __syncthreads();  // the only CTA-wide barrier
+  // 1. Load the tile (the caller's input: before the wait for the scan pass).
   const uint64_t tile = (uint64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  if (tile >= p.n_tiles) return;
   const uint64_t t0 = tile * kTile;
-
-  // 1. Load the tile; ring of each put; rank inside its row; per-row counts.
-  for (uint32_t x = lane; x < kRows * V; x += 32) s_cnt[x] = 0;
   ulonglong2 r[kRows];
 #pragma unroll
   for (int u = 0; u < kRows; ++u) {
     const uint64_t i = t0 + (uint64_t)u * 32 + lane;
-    r[u] = i < p.n ? ld_stream16(p.req + i, pol_first) : make_ulonglong2(0, 0);
+    r[u] = (tile < p.n_tiles && i < p.n) ? ld_stream16(p.req + i, pol_first)
+                                         : make_ulonglong2(0, 0);
   }
+  if (DB_WQE_PDL) wait_for_prerequisites();  // slots, heads, prefixes and chunk records
+  for (uint32_t v = threadIdx.x; v < R; v += blockDim.x)
+    s_slots[v] = p.full[v] ? 0ull : (uint64_t)(p.rings + (((uint64_t)v * p.depth) << 6));
+  __syncthreads();  // the only CTA-wide barrier
+  if (tile >= p.n_tiles) return;
+
+  //    Ring of each put; rank inside its row; per-row counts.
+  for (uint32_t x = lane; x < kRows * V; x += 32) s_cnt[x] = 0;
   __syncwarp();
   uint32_t bin_rank[kRows];  // ring | rank << 16
 #pragma unroll
@@ -798,18 +816,21 @@ int run(const wqe::Params& p, cudaStream_t s) {
   }
   rc = launch_result();
   if (rc) return rc;
-  wqe::wqe_scan_kernel<<<p.V * (p.mtu ? 2 : 1), wqe::kScanThreads, 0, s>>>(p);
-  rc = launch_result();
-  if (rc) return rc;
-  if (!p.vmm) {
-    const int sw = wqe::scatter_warps(p.V);  // kSWarps, fewer when many rings
-    const uint64_t grid = (p.n_tiles + sw - 1) / sw;
-    wqe::wqe_scatter_kernel<<<(unsigned)grid, sw * 32, wqe::scatter_smem(p.V), s>>>(p);
+  const unsigned scan_grid = p.V * (p.mtu ? 2 : 1);
+  if (DB_WQE_PDL) {
+    rc = launch_dependent(wqe::wqe_scan_kernel, scan_grid, wqe::kScanThreads, 0, s, p);
   } else {
-    const int sw = wqe::vmm_scatter_warps(p.V);
-    const uint64_t grid = (p.n_tiles + sw - 1) / sw;
-    wqe::wqe_scatter_vmm_kernel<<<(unsigned)grid, sw * 32, wqe::vmm_scatter_smem(p.V), s>>>(p);
+    wqe::wqe_scan_kernel<<<scan_grid, wqe::kScanThreads, 0, s>>>(p);
+    rc = launch_result();
   }
+  if (rc) return rc;
+  void (*scatter)(const wqe::Params) = p.vmm ? wqe::wqe_scatter_vmm_kernel : wqe::wqe_scatter_kernel;
+  const int sw = p.vmm ? wqe::vmm_scatter_warps(p.V)
+                       : wqe::scatter_warps(p.V);  // kSWarps, fewer when many rings
+  const size_t smem = p.vmm ? wqe::vmm_scatter_smem(p.V) : wqe::scatter_smem(p.V);
+  const unsigned grid = (unsigned)((p.n_tiles + sw - 1) / sw);
+  if (DB_WQE_PDL) return launch_dependent(scatter, grid, sw * 32, smem, s, p);
+  scatter<<<grid, sw * 32, smem, s>>>(p);
   return launch_result();
 }
 
