@@ -465,7 +465,8 @@ def time_mr_mutation(args, device, stream, only=None) -> dict:
                           "records_before": n, "new_records": u, "algorithmic_bytes": alg,
                           "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                           "note": "not part of the step: timed alone; lookup + 14 radix passes "
-                                  "+ merge, about 70 launches"}
+                                  "+ merge, 95 launches (each a programmatic dependent of the "
+                                  "one before)"}
     del rb
     if only == "mr_register":
         return out

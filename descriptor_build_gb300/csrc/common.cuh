@@ -314,6 +314,23 @@ inline int launch_dependent(void (*kernel)(P), unsigned grid, unsigned block, si
   if (e != cudaSuccess) return cuda_failure(e);
   return launch_result();
 }
+// The same for kernels of any signature, as a statement: a failed launch is
+// left for launch_result() like one made with <<< >>>.
+template <typename... K, typename... A>
+inline void launch_dep(void (*kernel)(K...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
 __device__ __forceinline__ void dependents_may_launch() {
   asm volatile("griddepcontrol.launch_dependents;");
 }

@@ -32,6 +32,15 @@
 #include "mrcache.h"
 
 namespace db {
+
+// Every kernel of a registration or deregistration batch is launched as a
+// programmatic dependent of the one before it (launch_dep): it starts by
+// waiting for that kernel (and so for the whole stream before it), then lets
+// the next kernel's CTAs be scheduled while it runs.
+__device__ __forceinline__ void kernel_prologue() {
+  wait_for_prerequisites();
+  dependents_may_launch();
+}
 namespace mrc {
 
 constexpr int kScanThreads = 1024;
@@ -89,6 +98,7 @@ __device__ __forceinline__ uint64_t scan_group_base(uint32_t g) {
 }
 __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n_max,
                                                             Len len, uint32_t* bsum) {
+  kernel_prologue();
   __shared__ uint32_t s_w[32];
   const uint64_t n = live_len(n_max, len);
   if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
@@ -104,6 +114,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, 
 }
 __global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint64_t n_max,
                                                            Len len, uint32_t* total) {
+  kernel_prologue();
   __shared__ uint32_t s_w[32];
   const uint64_t n = live_len(n_max, len);
   const uint64_t nb = n ? (n + kScanChunk - 1) / kScanChunk : 1;
@@ -124,6 +135,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint6
 __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
                                                            uint64_t n_max, Len len,
                                                            const uint32_t* bsum) {
+  kernel_prologue();
   __shared__ uint32_t s_w[32];
   const uint64_t n = live_len(n_max, len);
   if ((uint64_t)blockIdx.x * kScanChunk >= n && blockIdx.x > 0) return;
@@ -170,9 +182,9 @@ int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_
     return launch_result();
   }
   const uint64_t nb = ceil_div(n, kScanChunk);
-  scan_reduce<<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, len, bsum);
-  scan_bsums<<<1, kScanThreads, 0, s>>>(bsum, n, len, total);
-  scan_apply<<<(unsigned)nb, kScanThreads, 0, s>>>(in, out, n, len, bsum);
+  launch_dep(scan_reduce, (unsigned)nb, kScanThreads, 0, s, in, n, len, bsum);
+  launch_dep(scan_bsums, 1, kScanThreads, 0, s, bsum, n, len, total);
+  launch_dep(scan_apply, (unsigned)nb, kScanThreads, 0, s, in, out, n, len, bsum);
   return launch_result();
 }
 
@@ -199,6 +211,7 @@ __device__ __forceinline__ uint32_t passes_run_below(uint64_t diff, uint32_t shi
 // One atomic per CTA: the warps' ORs meet in shared memory first.
 __global__ void __launch_bounds__(kThreads) radix_diff(const uint64_t* key, const uint32_t* n_dev,
                                                        unsigned long long* diff) {
+  kernel_prologue();
   __shared__ unsigned long long s_or;
   const uint64_t n = *n_dev;
   if (n == 0) return;
@@ -223,6 +236,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_count(const uint64_t* key0
                                                             const unsigned long long* diff,
                                                             const uint32_t* n_dev, uint32_t shift,
                                                             uint32_t* counts, uint32_t tiles) {
+  kernel_prologue();
   __shared__ uint32_t hist[256];
   const uint64_t dv = *diff;
   if (!pass_runs(dv, shift)) return;
@@ -255,6 +269,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter(
     uint64_t* key0, uint64_t* key1, uint32_t* val0, uint32_t* val1, uint32_t cur0,
     const unsigned long long* diff, const uint32_t* n_dev, uint32_t shift, const uint32_t* offs,
     uint32_t tiles) {
+  kernel_prologue();
   extern __shared__ __align__(16) unsigned char smem[];
   const uint64_t dv = *diff;
   if (!pass_runs(dv, shift)) return;
@@ -339,6 +354,7 @@ __global__ void __launch_bounds__(kThreads) radix_settle(uint64_t* key0, uint64_
                                                          uint32_t cur0, uint32_t passes,
                                                          const unsigned long long* diff,
                                                          const uint32_t* n_dev) {
+  kernel_prologue();
   const uint32_t ran = passes_run_below(*diff, 8u * passes);
   if (((ran ^ passes) & 1u) == 0) return;
   const bool in1 = ((cur0 + ran) & 1u) != 0;
@@ -391,25 +407,27 @@ int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip
   if (skip_shared) {
     const unsigned dg = grid_for(b.n_max) < (unsigned)num_sms() * 4 ? grid_for(b.n_max)
                                                                       : (unsigned)num_sms() * 4;
-    radix_diff<<<dg, kThreads, 0, s>>>(b.key[cur0], n_dev, b.diff);
+    launch_dep(radix_diff, dg, kThreads, 0, s, b.key[cur0], n_dev, b.diff);
     if ((rc = launch_result())) return rc;
   }
   uint32_t passes = 0;
   for (int shift = 0; shift < bits; shift += 8, ++passes) {
-    radix_count<<<tiles, kSortThreads, 0, s>>>(b.key[0], b.key[1], cur0, b.diff, n_dev,
-                                               (uint32_t)shift, b.counts, tiles);
+    launch_dep(radix_count, tiles, kSortThreads, 0, s, b.key[0], b.key[1], cur0, b.diff, n_dev,
+               (uint32_t)shift, b.counts, tiles);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s, Len{n_dev, 256u, (uint32_t)kSortTile})))
       return rc;
-    radix_scatter<<<tiles, kSortThreads, kScatterSmem, s>>>(b.key[0], b.key[1], b.val[0], b.val[1],
-                                                            cur0, b.diff, n_dev, (uint32_t)shift,
-                                                            b.counts, tiles);
+    launch_dep(radix_scatter, tiles, kSortThreads, kScatterSmem, s,
+               b.key[0], b.key[1], b.val[0], b.val[1],
+               cur0, b.diff, n_dev, (uint32_t)shift,
+               b.counts, tiles);
     if ((rc = launch_result())) return rc;
     cur ^= 1;
   }
   if (!skip_shared) return 0;
-  radix_settle<<<grid_for(b.n_max), kThreads, 0, s>>>(b.key[0], b.key[1], b.val[0], b.val[1], cur0,
-                                                      passes, b.diff, n_dev);
+  launch_dep(radix_settle, grid_for(b.n_max), kThreads, 0, s,
+             b.key[0], b.key[1], b.val[0], b.val[1], cur0,
+             passes, b.diff, n_dev);
   return launch_result();
 }
 
@@ -431,6 +449,7 @@ __device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gs
 
 __global__ void reg_mark(const uint8_t* kind0, const int32_t* idx, uint64_t n_q, uint32_t* more,
                          uint32_t* flag) {
+  kernel_prologue();
   FOR_EACH(k, n_q) {
     const uint8_t kd = kind0[k];
     flag[k] = kd == DB_MR_MISS;
@@ -439,6 +458,7 @@ __global__ void reg_mark(const uint8_t* kind0, const int32_t* idx, uint64_t n_q,
 }
 __global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint32_t* pos,
                             uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val) {
+  kernel_prologue();
   FOR_EACH(k, n_q) {
     if (!flag[k]) continue;
     uint64_t b, e;
@@ -449,6 +469,7 @@ __global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint3
 }
 __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
                           const uint32_t* val, uint64_t* key) {
+  kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
@@ -460,6 +481,7 @@ __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max,
 // Run starts of equal widened ranges over the sorted misses (0 past m).
 __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
                          const uint32_t* val, uint32_t* flag) {
+  kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     uint32_t f = 0;
@@ -481,6 +503,7 @@ __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, 
 __global__ void reg_new(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
                         const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
                         uint64_t* nstart, uint64_t* nend, uint32_t* nfirst, uint32_t* nrefs) {
+  kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
@@ -521,6 +544,7 @@ struct PlaceParams {
   const RegHeader* h;
 };
 __global__ void reg_place_old(const PlaceParams p) {
+  kernel_prologue();
   const uint64_t u = p.h->u;
   if (p.n + u > p.o_cap) return;
   FOR_EACH(i, p.n) {
@@ -533,6 +557,7 @@ __global__ void reg_place_old(const PlaceParams p) {
   }
 }
 __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
+  kernel_prologue();
   const uint64_t u = p.h->u;
   if (p.n + u > p.o_cap) return;
   FOR_EACH(j, n_max) {
@@ -548,6 +573,7 @@ __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
 __global__ void reg_handles_hit(const uint8_t* kind0, const int32_t* idx, uint64_t n_q,
                                 const int64_t* remap, const RegHeader* h, uint64_t n,
                                 uint64_t o_cap, int64_t* handle, uint8_t* kind) {
+  kernel_prologue();
   const bool fits = n + h->u <= o_cap;
   FOR_EACH(k, n_q) {
     const uint8_t kd = kind0[k];
@@ -560,6 +586,7 @@ __global__ void reg_handles_hit(const uint8_t* kind0, const int32_t* idx, uint64
 __global__ void reg_handles_miss(const RegHeader* h, uint64_t n_max, uint64_t n, uint64_t o_cap,
                                  const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
                                  const uint32_t* npos, int64_t* handle, uint8_t* kind) {
+  kernel_prologue();
   const uint64_t m = h->m;
   const bool fits = n + h->u <= o_cap;
   FOR_EACH(i, n_max) {
@@ -570,6 +597,7 @@ __global__ void reg_handles_miss(const RegHeader* h, uint64_t n_max, uint64_t n,
   }
 }
 __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_counters* ctr) {
+  kernel_prologue();
   const uint64_t total = n + h->u;
   ctr->total = total;
   ctr->n_invalid = h->lookup.n_invalid;
@@ -616,9 +644,11 @@ struct DeregHeader {
   uint32_t kept;     // records after the batch
   unsigned long long stale;
 };
-__global__ void set_u32(uint32_t* p, uint32_t v) { *p = v; }
+__global__ void set_u32(uint32_t* p, uint32_t v) {
+  kernel_prologue(); *p = v; }
 __global__ void dereg_key(const int64_t* handle, uint64_t n_h, uint64_t n, uint64_t* key,
                           uint32_t* val) {
+  kernel_prologue();
   FOR_EACH(k, n_h) {
     const int64_t x = handle[k];
     key[k] = (x >= 0 && (uint64_t)x < n) ? (uint64_t)x : n;  // n: no such record
@@ -626,16 +656,19 @@ __global__ void dereg_key(const int64_t* handle, uint64_t n_h, uint64_t n, uint6
   }
 }
 __global__ void dereg_runs(const uint64_t* key, uint64_t n_h, uint32_t* flag) {
+  kernel_prologue();
   FOR_EACH(i, n_h) flag[i] = i == 0 || key[i] != key[i - 1];
 }
 __global__ void dereg_run_start(const uint32_t* flag, const uint32_t* excl, uint64_t n_h,
                                 uint32_t* rs) {
+  kernel_prologue();
   FOR_EACH(i, n_h) if (flag[i]) rs[excl[i]] = (uint32_t)i;
 }
 __global__ void dereg_status(const uint64_t* key, const uint32_t* val, const uint32_t* flag,
                              const uint32_t* excl, const uint32_t* rs, uint64_t n_h, uint64_t n,
                              const uint32_t* refs, uint32_t* dec, uint8_t* status,
                              DeregHeader* h) {
+  kernel_prologue();
   unsigned long long stale = 0;
   FOR_EACH(i, n_h) {
     const uint64_t r = key[i];
@@ -655,12 +688,14 @@ __global__ void dereg_status(const uint64_t* key, const uint32_t* val, const uin
   if ((threadIdx.x & 31) == 0 && stale) atomicAdd(&h->stale, stale);
 }
 __global__ void dereg_keep(const uint32_t* refs, const uint32_t* dec, uint64_t n, uint32_t* keep) {
+  kernel_prologue();
   FOR_EACH(i, n) keep[i] = refs[i] > dec[i];
 }
 __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
                             const uint32_t* refs, const uint32_t* dec, const uint32_t* keep,
                             const uint32_t* kpos, uint64_t n, uint64_t* o_start, uint64_t* o_end,
                             uint32_t* o_lkey, uint32_t* o_refs, int64_t* remap) {
+  kernel_prologue();
   FOR_EACH(i, n) {
     if (!keep[i]) {
       remap[i] = -1;
@@ -675,6 +710,7 @@ __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const ui
   }
 }
 __global__ void dereg_final(const DeregHeader* h, db_counters* ctr) {
+  kernel_prologue();
   ctr->total = h->kept;
   ctr->n_invalid = h->stale;
   ctr->n_overflow = 0;
@@ -780,42 +816,46 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                     (int)granule_shift);
     if (rc) return rc;
     // 2. hits and misses
-    reg_mark<<<grid_for(n_q), kThreads, 0, s>>>(kind0, idx, n_q, more, flag);
+    launch_dep(reg_mark, grid_for(n_q), kThreads, 0, s, kind0, idx, n_q, more, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->m, bsum, s))) return rc;
-    reg_compact<<<grid_for(n_q), kThreads, 0, s>>>(q, flag, pos, n_q, granule_shift, sb.key[0],
-                                                   sb.val[0]);
+    launch_dep(reg_compact, grid_for(n_q), kThreads, 0, s,
+               q, flag, pos, n_q, granule_shift, sb.key[0],
+               sb.val[0]);
     if ((rc = launch_result())) return rc;
     // 3. sort the misses by (start, end), stable in request order
     const int bits = 64 - (int)granule_shift;
     int cur = 0;
     if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
-    reg_rekey<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sb.val[cur],
-                                                 sb.key[cur]);
+    launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sb.val[cur],
+               sb.key[cur]);
     if ((rc = launch_result())) return rc;
     if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
     // 4. runs of equal ranges are the new records
     const uint32_t* sval = sb.val[cur];
-    reg_runs<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sval, flag);
+    launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->u, bsum, s))) return rc;
-    reg_new<<<grid_for(n_q), kThreads, 0, s>>>(q, h, n_q, granule_shift, sval, flag, pos, nstart,
-                                               nend, nfirst, nrefs);
+    launch_dep(reg_new, grid_for(n_q), kThreads, 0, s,
+               q, h, n_q, granule_shift, sval, flag, pos, nstart,
+               nend, nfirst, nrefs);
     if ((rc = launch_result())) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
                    out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
     if (n_mr) {
-      reg_place_old<<<grid_for(n_mr), kThreads, 0, s>>>(pp);
+      launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
       if ((rc = launch_result())) return rc;
     }
-    reg_place_new<<<grid_for(n_q), kThreads, 0, s>>>(pp, n_q);
+    launch_dep(reg_place_new, grid_for(n_q), kThreads, 0, s, pp, n_q);
     if ((rc = launch_result())) return rc;
     // 5. handles and kinds
-    reg_handles_hit<<<grid_for(n_q), kThreads, 0, s>>>(kind0, idx, n_q, remap, h, n_mr, out_cap,
-                                                       handle, kind);
+    launch_dep(reg_handles_hit, grid_for(n_q), kThreads, 0, s,
+               kind0, idx, n_q, remap, h, n_mr, out_cap,
+               handle, kind);
     if ((rc = launch_result())) return rc;
-    reg_handles_miss<<<grid_for(n_q), kThreads, 0, s>>>(h, n_q, n_mr, out_cap, sval, flag, pos,
-                                                        npos, handle, kind);
+    launch_dep(reg_handles_miss, grid_for(n_q), kThreads, 0, s,
+               h, n_q, n_mr, out_cap, sval, flag, pos,
+               npos, handle, kind);
     if ((rc = launch_result())) return rc;
   } else if (n_mr) {
     // no requests: the table is copied through (and checked like a lookup would)
@@ -824,11 +864,11 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     if (rc) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
                    out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
-    reg_place_old<<<grid_for(n_mr), kThreads, 0, s>>>(pp);
+    launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
     if ((rc = launch_result())) return rc;
   }
   if (ctr) {
-    reg_final<<<1, 1, 0, s>>>(h, n_mr, out_cap, ctr);
+    launch_dep(reg_final, 1, 1, 0, s, h, n_mr, out_cap, ctr);
     return launch_result();
   }
   return 0;
@@ -876,36 +916,39 @@ extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint6
   if (cudaMemsetAsync(h, 0, sizeof(DeregHeader), s) != cudaSuccess ||
       (n_mr && cudaMemsetAsync(dec, 0, n_mr * 4, s) != cudaSuccess))
     return launch_result();
-  set_u32<<<1, 1, 0, s>>>(&h->n_h, (uint32_t)n_h);  // the sort reads its length on the device
-  int rc = launch_result();
+  launch_dep(set_u32, 1, 1, 0, s,
+             &h->n_h, (uint32_t)n_h);  // the sort reads its length on the device
+             int rc = launch_result();
   if (rc) return rc;
   if (n_h) {
-    dereg_key<<<grid_for(n_h), kThreads, 0, s>>>(handle, n_h, n_mr, sb.key[0], sb.val[0]);
+    launch_dep(dereg_key, grid_for(n_h), kThreads, 0, s, handle, n_h, n_mr, sb.key[0], sb.val[0]);
     if ((rc = launch_result())) return rc;
     int bits = 0;
     while (bits < 64 && (n_mr >> bits)) ++bits;  // keys are at most n_mr
     bits = (bits + 7) & ~7;
     int cur = 0;
     if ((rc = radix_sort(sb, cur, &h->n_h, bits, false, s))) return rc;
-    dereg_runs<<<grid_for(n_h), kThreads, 0, s>>>(sb.key[cur], n_h, flag);
+    launch_dep(dereg_runs, grid_for(n_h), kThreads, 0, s, sb.key[cur], n_h, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, excl, n_h, nullptr, bsum, s))) return rc;
-    dereg_run_start<<<grid_for(n_h), kThreads, 0, s>>>(flag, excl, n_h, rs);
+    launch_dep(dereg_run_start, grid_for(n_h), kThreads, 0, s, flag, excl, n_h, rs);
     if ((rc = launch_result())) return rc;
-    dereg_status<<<grid_for(n_h), kThreads, 0, s>>>(sb.key[cur], sb.val[cur], flag, excl, rs, n_h,
-                                                    n_mr, refs, dec, status, h);
+    launch_dep(dereg_status, grid_for(n_h), kThreads, 0, s,
+               sb.key[cur], sb.val[cur], flag, excl, rs, n_h,
+               n_mr, refs, dec, status, h);
     if ((rc = launch_result())) return rc;
   }
   if (n_mr) {
-    dereg_keep<<<grid_for(n_mr), kThreads, 0, s>>>(refs, dec, n_mr, keep);
+    launch_dep(dereg_keep, grid_for(n_mr), kThreads, 0, s, refs, dec, n_mr, keep);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(keep, kpos, n_mr, &h->kept, bsum, s))) return rc;
-    dereg_place<<<grid_for(n_mr), kThreads, 0, s>>>(start, end, lkey, refs, dec, keep, kpos, n_mr,
-                                                    out_start, out_end, out_lkey, out_refs, remap);
+    launch_dep(dereg_place, grid_for(n_mr), kThreads, 0, s,
+               start, end, lkey, refs, dec, keep, kpos, n_mr,
+               out_start, out_end, out_lkey, out_refs, remap);
     if ((rc = launch_result())) return rc;
   }
   if (ctr) {
-    dereg_final<<<1, 1, 0, s>>>(h, ctr);
+    launch_dep(dereg_final, 1, 1, 0, s, h, ctr);
     return launch_result();
   }
   return 0;

@@ -173,7 +173,10 @@ __device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32
 }
 
 __global__ void __launch_bounds__(kBuildThreads, 4) mr_index_kernel(const BuildParams p) {
-  if (DB_MR_PDL) dependents_may_launch();
+  if (DB_MR_PDL) {
+    wait_for_prerequisites();  // launched as a dependent after the prefix-maximum kernels
+    dependents_may_launch();
+  }
   const uint64_t lo = p.start[0];
   const uint64_t hi = p.start[p.n_mr - 1];
   const uint64_t span = hi > lo ? hi - lo : 0;
@@ -507,6 +510,8 @@ __device__ __forceinline__ uint64_t block_max_scan(uint64_t x, uint64_t* s_w) {
 }
 __global__ void __launch_bounds__(kPmBlock) mr_pm_block_kernel(const uint64_t* end, uint64_t n,
                                                                uint64_t* pm, uint64_t* bmax) {
+  wait_for_prerequisites();
+  dependents_may_launch();
   __shared__ uint64_t s_w[32];
   const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
   const uint64_t x = block_max_scan(i < n ? end[i] : 0ull, s_w);
@@ -514,6 +519,8 @@ __global__ void __launch_bounds__(kPmBlock) mr_pm_block_kernel(const uint64_t* e
   if (threadIdx.x == kPmBlock - 1) bmax[blockIdx.x] = x;
 }
 __global__ void __launch_bounds__(kPmBlock) mr_pm_scan_kernel(uint64_t* bmax, uint64_t nblk) {
+  wait_for_prerequisites();
+  dependents_may_launch();
   __shared__ uint64_t s_w[32];
   uint64_t carry = 0;
   for (uint64_t b0 = 0; b0 < nblk; b0 += kPmBlock) {
@@ -530,6 +537,8 @@ __global__ void __launch_bounds__(kPmBlock) mr_pm_scan_kernel(uint64_t* bmax, ui
 }
 __global__ void __launch_bounds__(kPmBlock) mr_pm_apply_kernel(uint64_t* pm, uint64_t n,
                                                                const uint64_t* bmax) {
+  wait_for_prerequisites();
+  dependents_may_launch();
   const uint64_t i = (uint64_t)blockIdx.x * kPmBlock + threadIdx.x;
   if (blockIdx.x == 0 || i >= n) return;
   const uint64_t prior = bmax[blockIdx.x - 1];
@@ -604,16 +613,19 @@ int lookup(const db_range* q, uint64_t n_q, const uint64_t* mr_start, const uint
       const uint64_t nblk = mr::pm_blocks(n_mr);
       mr::mr_pm_block_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(mr_end, n_mr, pm, bmax);
       if ((rc = launch_result())) return rc;
-      mr::mr_pm_scan_kernel<<<1, mr::kPmBlock, 0, s>>>(bmax, nblk);
+      launch_dep(mr::mr_pm_scan_kernel, 1, mr::kPmBlock, 0, s, bmax, nblk);
       if ((rc = launch_result())) return rc;
-      mr::mr_pm_apply_kernel<<<(unsigned)nblk, mr::kPmBlock, 0, s>>>(pm, n_mr, bmax);
+      launch_dep(mr::mr_pm_apply_kernel, (unsigned)nblk, mr::kPmBlock, 0, s, pm, n_mr, bmax);
       if ((rc = launch_result())) return rc;
     }
     mr::BuildParams b{mr_start, mr_end, mr_lkey, n_mr, hdr, dir, rec, nb, log_nb, overlap, pm};
     uint64_t grid = (n_mr + mr::kBuildThreads - 1) / mr::kBuildThreads;
     const uint64_t cap = (uint64_t)num_sms() * DB_MR_BUILD_CTAS_PER_SM;
     if (grid > cap) grid = cap;
-    mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
+    if (DB_MR_PDL && overlap)
+      launch_dep(mr::mr_index_kernel, (unsigned)grid, mr::kBuildThreads, 0, s, b);
+    else
+      mr::mr_index_kernel<<<(unsigned)grid, mr::kBuildThreads, 0, s>>>(b);
     if ((rc = launch_result())) return rc;
   }
   mr::LookupParams l{reinterpret_cast<const ulonglong2*>(q), n_q, n_mr, hdr, hdr, dir, rec,
