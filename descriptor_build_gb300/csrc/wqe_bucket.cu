@@ -171,7 +171,10 @@ constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at 
 template <bool kVmm, bool kPsn>
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
   extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V] WQEs, then PSNs if asked
-  if (DB_WQE_PDL) dependents_may_launch();
+  if (DB_WQE_PDL) {
+    wait_for_prerequisites();  // a dependent of the chunk-record pack on a VMM heap
+    dependents_may_launch();
+  }
   const uint32_t V = p.V;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t* s_hist = s_hist_all + (size_t)warp * V;
@@ -502,6 +505,7 @@ inline size_t vmm_scatter_smem(uint32_t V) { return cta_smem(V) + vmm_scatter_wa
 // chunk_rkey[pe][c] | chunk_lkey[c] << 32}, so a WQE reads its chunk's three
 // values with one L2 request instead of three.
 __global__ void vmm_pack_kernel(const Params p) {
+  if (DB_WQE_PDL) dependents_may_launch();
   const uint64_t total = (uint64_t)p.world * p.n_chunks;
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (uint64_t)gridDim.x * blockDim.x) {
@@ -807,14 +811,20 @@ int run(const wqe::Params& p, cudaStream_t s) {
   if (count_grid > count_need) count_grid = count_need;
   {
     const size_t count_smem = (size_t)wqe::kCountWarps * p.V * 4 * (p.mtu ? 2 : 1);
-    if (!p.vmm)
+    if (!p.vmm) {
       wqe::wqe_count_kernel<false, false><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
-    else if (!p.mtu)
-      wqe::wqe_count_kernel<true, false><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
-    else
-      wqe::wqe_count_kernel<true, true><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+      rc = launch_result();
+    } else {
+      void (*count)(const wqe::Params) = p.mtu ? wqe::wqe_count_kernel<true, true>
+                                               : wqe::wqe_count_kernel<true, false>;
+      if (DB_WQE_PDL) {  // after the pack kernel just launched on `s`
+        rc = launch_dependent(count, (unsigned)count_grid, wqe::kCountThreads, count_smem, s, p);
+      } else {
+        count<<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+        rc = launch_result();
+      }
+    }
   }
-  rc = launch_result();
   if (rc) return rc;
   const unsigned scan_grid = p.V * (p.mtu ? 2 : 1);
   if (DB_WQE_PDL) {
