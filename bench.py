@@ -53,7 +53,7 @@ METRIC = "M requests/s translated + achieved HBM GB/s as % of GB300 peak"
 UNIT = "M requests/s"
 WORKLOAD = "descriptor batch: prp_small + prp_large + mr_lookup + put_bucket (full sizes)"
 # Launch order of a step's calls on their own streams (measured best on GB300).
-SCHEDULE = ("mr_lookup", "prp_small", "put_bucket", "prp_large")
+SCHEDULE = ("mr_lookup", "put_bucket", "prp_small", "prp_large")
 
 
 def parse():
