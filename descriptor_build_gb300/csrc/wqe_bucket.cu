@@ -107,6 +107,8 @@ struct Params {
   // Packet sequence numbers (mtu != 0): one column of per-tile PSN counts
   // per bin, the PSN heads before the call and each ring's PSN total.
   uint32_t mtu;
+  uint64_t mtu_magic;      // ceil(2^64 / mtu): floor(x / mtu) of a 32-bit x by one multiply
+  uint64_t psn_per_chunk;  // ceil(chunk bytes / mtu)
   uint64_t* psn_head;
   uint32_t* psn_counts;  // [V][stride]
   uint64_t* psn_old;
@@ -131,23 +133,35 @@ __device__ __forceinline__ uint32_t wqes_of(const Params& p, const ulonglong2 r)
   return (uint32_t)((last >> p.cshift) - (off >> p.cshift)) + 1;
 }
 
-// PSNs a valid put's WQEs use: ceil(len / mtu) per WQE, summed over its
-// chunks (a first partial chunk, full chunks, a last partial one).
-__device__ __forceinline__ uint32_t psns_of(const Params& p, const ulonglong2 r) {
-  const uint64_t off = r.x, bytes = (uint32_t)r.y, m = p.mtu;
-  const uint32_t k = wqes_of(p, r);
-  if (k == 1) return (uint32_t)((bytes + m - 1) / m);
-  const uint64_t C = 1ull << p.cshift;
-  const uint64_t first = C - (off & (C - 1));
-  const uint64_t last = ((off + bytes - 1) & (C - 1)) + 1;
-  return (uint32_t)((first + m - 1) / m + (uint64_t)(k - 2) * ((C + m - 1) / m) + (last + m - 1) / m);
+// ceil(x / mtu) for a 32-bit x: the quotient is the high half of the 96-bit
+// product x * ceil(2^64 / mtu), exact for every 32-bit x and divisor
+// (Lemire, Kaser and Kurz, "Faster remainder by direct computation", 2019),
+// then one up unless the remainder is zero. Every length divided here is at
+// most a put's byte count, so it fits in 32 bits.
+__device__ __forceinline__ uint32_t ceil_mtu(const Params& p, uint32_t x) {
+  const uint32_t q = (uint32_t)__umul64hi(p.mtu_magic, (uint64_t)x);
+  return q + (x != q * p.mtu ? 1u : 0u);
 }
-// PSNs of the fragments before fragment f of a put.
+// PSNs a valid put's WQEs use: ceil(len / mtu) per WQE, summed over its
+// chunks (a first partial chunk, full chunks, a last partial one; the two
+// partial ones are shorter than the put).
+__device__ __forceinline__ uint32_t psns_of(const Params& p, const ulonglong2 r) {
+  const uint64_t off = r.x;
+  const uint32_t bytes = (uint32_t)r.y;
+  const uint32_t k = wqes_of(p, r);
+  if (k == 1) return ceil_mtu(p, bytes);
+  const uint64_t C = 1ull << p.cshift;
+  const uint32_t first = (uint32_t)(C - (off & (C - 1)));
+  const uint32_t last = (uint32_t)(((off + bytes - 1) & (C - 1)) + 1);
+  return (uint32_t)(ceil_mtu(p, first) + (uint64_t)(k - 2) * p.psn_per_chunk + ceil_mtu(p, last));
+}
+// PSNs of the fragments before fragment f of a put (f >= 1: the put crosses
+// its first chunk's end, so that chunk's part is shorter than the put).
 __device__ __forceinline__ uint32_t psns_before(const Params& p, uint64_t off, uint32_t f) {
   if (f == 0) return 0;
-  const uint64_t C = 1ull << p.cshift, m = p.mtu;
-  const uint64_t first = C - (off & (C - 1));
-  return (uint32_t)((first + m - 1) / m + (uint64_t)(f - 1) * ((C + m - 1) / m));
+  const uint64_t C = 1ull << p.cshift;
+  const uint32_t first = (uint32_t)(C - (off & (C - 1)));
+  return (uint32_t)(ceil_mtu(p, first) + (uint64_t)(f - 1) * p.psn_per_chunk);
 }
 
 // ---------------------------------------------------------------- count pass
@@ -892,6 +906,10 @@ extern "C" int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64
                                                wqe::vmm_table_off(n, world * n_qp));
   p.vmm = true;
   p.mtu = mtu;
+  if (mtu) {
+    p.mtu_magic = ~0ull / mtu + 1;
+    p.psn_per_chunk = ((1ull << chunk_shift) + mtu - 1) / mtu;
+  }
   p.psn_head = psn_head;
   p.cshift = chunk_shift;
   p.n_chunks = n_chunks;

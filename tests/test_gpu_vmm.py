@@ -137,6 +137,30 @@ def test_random_batches_with_psns(db, oracle, n, world, n_qp, chunk_shift, depth
          world, n_qp, 0x7C0000000000, heap, depth, head, mtu=mtu, psn_head=psn0)
 
 
+@pytest.mark.parametrize("mtu", [777, 1500, 4000, 9000, (1 << 20) - 1])
+def test_psns_with_mtus_that_are_not_powers_of_two(db, oracle, mtu):
+    """PSN counts divide lengths by the MTU; besides random puts, a few puts
+    of nearly 4 GiB (the longest a put can be) on a heap of 2 MiB chunks."""
+    rng = np.random.default_rng(mtu)
+    world, n_qp, chunk_shift, depth = 2, 2, 21, 1 << 14
+    heap = 1 << 34
+    n = 3000
+    pe = rng.integers(0, world, size=n)
+    qp = rng.integers(0, n_qp, size=n)
+    off = 16 * rng.integers(0, (heap >> 1) // 16, size=n)
+    nbytes = 16 * rng.integers(1, (8 << 20) // 16, size=n)
+    big = rng.choice(n, size=3, replace=False)
+    nbytes[big] = (1 << 32) - 16 * rng.integers(1, 1 << 12, size=3)
+    from synth import pack_put_requests
+    req = pack_put_requests(off, nbytes, pe, qp)
+    head = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    psn0 = rng.integers(0, 2**40, size=world * n_qp).astype(np.uint64)
+    _, want = both(db, oracle, req, tables_for(rng, world, heap >> chunk_shift, chunk_shift),
+                   chunk_shift, world, n_qp, 0x7C0000000000, heap, depth, head, mtu=mtu,
+                   psn_head=psn0)
+    assert want["ctr"][0] > n + 3 * 2047  # the long puts took their WQEs
+
+
 def test_one_chunk_matches_static_heap(db, oracle):
     import synth
     from test_gpu_wqe import run_gpu
