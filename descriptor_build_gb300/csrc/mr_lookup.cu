@@ -172,7 +172,10 @@ __device__ __forceinline__ void set_dir(const BuildParams& p, uint64_t b, uint32
                : "memory");
 }
 
-__global__ void __launch_bounds__(kBuildThreads, 4) mr_index_kernel(const BuildParams p) {
+#ifndef DB_MR_BUILD_MIN_CTAS
+#define DB_MR_BUILD_MIN_CTAS 4
+#endif
+__global__ void __launch_bounds__(kBuildThreads, DB_MR_BUILD_MIN_CTAS) mr_index_kernel(const BuildParams p) {
   if (DB_MR_PDL) {
     wait_for_prerequisites();  // launched as a dependent after the prefix-maximum kernels
     dependents_may_launch();
