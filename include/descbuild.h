@@ -146,10 +146,11 @@ typedef struct db_counters {
  *                    in device memory or in pinned host memory (the host-memory
  *                    region the lists live in on the source page; the kernel
  *                    then writes the lists across the CPU-GPU link).
- *                    Unused slots of a list's last page are left as they were,
- *                    except the ones sharing the last entry's 32-byte sector
- *                    (at most three), which are written as 0, so that every
- *                    list ends on a whole sector; DB_PRP_ZERO_TAIL zeroes them all.
+ *                    Unused slots of a list's last page are undefined: the
+ *                    library leaves them as they were, except that it may write
+ *                    0 into the ones sharing the last entry's 32-byte sector (at
+ *                    most three; this kernel does, so that every list ends on a
+ *                    whole sector). DB_PRP_ZERO_TAIL writes 0 into all of them.
  *   prp              [n] output (16-byte aligned)
  *   page_base        [n] output or NULL
  *   status           [n] output (DB_PRP_*) or NULL
@@ -330,8 +331,12 @@ int db_wqe_bucket_vmm(const db_put_req* req, uint64_t n, const uint64_t* chunk_r
  *
  *  - n > DB_PRP_STATIC_MAX_REQUESTS returns -E2BIG before any GPU work.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture on the device.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it with the
+ *    ID of the device's current CUDA context; make that first call before
+ *    any stream capture on the device. Later calls compare the context ID
+ *    (one driver query) and look the address up again when it differs, as
+ *    after cudaDeviceReset, which unloads the array with its context. A new
+ *    context's copy of the array starts zeroed.
  *  - The array starts zeroed and every call leaves it ready for the next one,
  *    so no call has to clear it. All calls share it: calls whose work can
  *    overlap on the GPU (different streams without ordering between them, or

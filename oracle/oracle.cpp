@@ -33,10 +33,10 @@
 //    the xNVMe "uPCIe CUDA" page: xnvme_buf_register refcounts whole 64 KiB
 //    device pages.
 //  * CQ mirror -- xNVMe "uPCIe CUDA" backend page, "Completions in device
-//    memory": a resident kernel watches each device-memory completion queue
-//    with one warp and copies completions into the host CQ as their phase
-//    bit turns; a slot per queue carries a generation (odd while attached)
-//    and an acknowledgement.
+//    memory": completion queues live in device memory and a GPU kernel
+//    forwards each new completion (recognised by its flipped phase tag) to
+//    the host CQ, one warp per queue; each queue's slot holds a generation
+//    (odd while attached) and an acknowledgement.
 //
 // Readings where the pages are silent are listed with each function.
 //
@@ -160,15 +160,10 @@ uint64_t oracle_prp_one(uint64_t off, uint64_t len, const uint64_t* lut, uint64_
     slot += 1;
   }
   if (page + 1 != n_list) fail("list page count mismatch");
+  // Reading: the pages say nothing of the slots after a list's last entry,
+  // so they are left as they were; the zero-tail option clears them.
   if (zero_tail) {
     for (; slot < kListSlots; ++slot) list[page * kListSlots + slot] = 0;
-  } else {
-    // Reading: the slots that share the last entry's 32-byte sector (four
-    // slots from the page start) are written as 0; the rest are untouched.
-    while (slot % 4 != 0) {
-      list[page * kListSlots + slot] = 0;
-      slot += 1;
-    }
   }
   return n_list;
 }

@@ -43,3 +43,27 @@ def host64(t: "torch.Tensor") -> np.ndarray:
 
 def host32(t: "torch.Tensor") -> np.ndarray:
     return t.cpu().numpy().view(np.uint32)
+
+
+def assert_arena_equal(got: np.ndarray, want: np.ndarray, fill: int, where: str = ""):
+    """List pages from the GPU against the oracle's, word for word.
+
+    Both arenas started filled with ``fill``; no list word can equal it (list
+    words are 4 KiB-aligned bus addresses, ``fill`` is not). Slots the oracle
+    wrote must match. Slots it left as they were must still hold ``fill``,
+    except that the library may write 0 into the slots that share a list's
+    last entry's 32-byte sector (the header allows it: the kernel ends every
+    list on a whole sector)."""
+    got = np.ascontiguousarray(got).view(np.uint64).reshape(-1, 4)
+    want = np.ascontiguousarray(want).view(np.uint64).reshape(-1, 4)
+    assert got.shape == want.shape, where
+    f = np.uint64(fill & (2**64 - 1))
+    defined = want != f
+    ok = np.where(defined, got == want, got == f)
+    # a sector holding a list's last entry: its undefined slots may be 0
+    tail = defined.any(axis=1, keepdims=True) & ~defined & (got == 0)
+    bad = ~(ok | tail)
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{where}: arena word {4 * r + c}: got {int(got[r, c]):#x}, "
+                             f"want {int(want[r, c]):#x} ({int(bad.sum())} words differ)")

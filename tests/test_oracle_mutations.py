@@ -82,8 +82,10 @@ MUTANTS = [
      "const uint64_t starting = (uint64_t)(std::lower_bound(start, start + n, base) - start);"),
     ("register: prefix maximum of the ends restarts", "reach = std::max(reach, end[i]);",
      "reach = end[i];"),
-    ("prp: last sector padded to eight slots", "while (slot % 4 != 0) {", "while (slot % 8 != 0) {"),
-    ("prp: last sector not padded", "while (slot % 4 != 0) {", "while (false) {"),
+    ("prp: tail slots cleared without the zero-tail option", "  if (zero_tail) {\n    for (; slot",
+     "  if (true) {\n    for (; slot"),
+    ("prp: zero tail stops one slot short", "for (; slot < kListSlots; ++slot)",
+     "for (; slot + 1 < kListSlots; ++slot)"),
     ("register: a hit takes no reference", "more[i] += 1;", "more[i] += 0;"),
     ("register: new record before an old one with the same start",
      "start[i] <= nit->first.first);", "start[i] < nit->first.first);"),

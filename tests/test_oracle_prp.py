@@ -60,9 +60,8 @@ def brute_force_pages(off, length, lut):
 
 def data_entries(prp1, prp2, lst, n_list, arena_base, page_base, fill=0):
     """The page entries a request describes, chain pointers removed. On the
-    last list page the entries end at the first slot holding ``fill`` (never
-    written) or 0 (the padding of the last entry's 32-byte sector; no entry
-    is 0, since LUT values are non-zero)."""
+    last list page the entries end at the first slot still holding ``fill``
+    (never written)."""
     if n_list == 0:
         return [prp1] + ([prp2] if prp2 else [])
     out = [prp1]
@@ -72,7 +71,7 @@ def data_entries(prp1, prp2, lst, n_list, arena_base, page_base, fill=0):
             if s == 511 and j + 1 < n_list:
                 assert v == arena_base + (page_base + j + 1) * PAGE
                 continue
-            if j + 1 == n_list and (v == fill or v == 0):
+            if j + 1 == n_list and v == fill:
                 break
             out.append(v)
     return out
@@ -104,14 +103,11 @@ def test_brute_force_tiny_heaps(oracle):
         n = len(pages)
         if n >= 3:
             assert prp2 == A + pb * PAGE
-        # Unused slots of the last list page stay untouched, except those in
-        # the last entry's 32-byte sector, which are 0.
+        # Unused slots of the last list page stay untouched.
         if n_list:
             used = (n - 1) - 511 * (n_list - 1)
             assert 1 <= used <= 512
-            pad = -used % 4
-            assert (lst[-1, used:used + pad] == 0).all()
-            assert (lst[-1, used + pad:] == 0xAAAAAAAAAAAAAAAA).all()
+            assert (lst[-1, used:] == 0xAAAAAAAAAAAAAAAA).all()
 
 
 def test_page_count_boundaries(oracle):
@@ -179,10 +175,9 @@ def test_zero_tail(oracle):
     assert (out["arena"][3:] == 7).all()
 
 
-def test_last_sector_padding(oracle):
-    """Without DB_PRP_ZERO_TAIL the slots after the last entry up to the end
-    of its 32-byte sector (a multiple of four slots) are 0; later slots keep
-    what the arena held."""
+def test_unused_slots_untouched(oracle):
+    """Without DB_PRP_ZERO_TAIL every slot after a list's last entry keeps
+    what the arena held, whatever the entry count modulo a store width."""
     rng = np.random.default_rng(6)
     heap = 8 * 1024 * 1024
     lut = random_lut(rng, heap // 65536)
@@ -191,14 +186,16 @@ def test_last_sector_padding(oracle):
                    dtype=np.uint64)
     out = oracle.prp_build(req, lut, heap, 0x1000000, 8, fill=FILL)
     a = out["arena"]
-    # 19 entries: slot 19 completes the sector
-    assert (a[0, :19] != 0).all() and a[0, 19] == 0 and (a[0, 20:] == FILL).all()
-    # 20 entries: the sector ends with the list
-    assert (a[1, :20] != 0).all() and (a[1, 20:] == FILL).all()
-    # 600 entries: 511 + pointer, then 89 entries and three slots of padding
-    assert (a[3, :89] != 0).all() and (a[3, 89:92] == 0).all() and (a[3, 92:] == FILL).all()
-    # 4 entries: exactly one sector
-    assert (a[4, :4] != 0).all() and (a[4, 4:] == FILL).all()
+    # 19 entries
+    assert (a[0, :19] != FILL).all() and (a[0, 19:] == FILL).all()
+    # 20 entries
+    assert (a[1, :20] != FILL).all() and (a[1, 20:] == FILL).all()
+    # 600 entries: 511 + pointer, then 89 entries
+    assert (a[2] != FILL).all()
+    assert (a[3, :89] != FILL).all() and (a[3, 89:] == FILL).all()
+    # 4 entries
+    assert (a[4, :4] != FILL).all() and (a[4, 4:] == FILL).all()
+    assert (a[5:] == FILL).all()
 
 
 def test_empty_batch(oracle):
