@@ -1,17 +1,17 @@
 // Completion-queue mirror (sm_103a).
 //
-// Source: xNVMe "uPCIe CUDA" backend page, "Completions in device memory":
-// a kernel watches each device-memory completion queue with one warp and
-// copies completions into the host CQ as their phase bit turns; a slot per
-// queue carries the two CQ addresses, the depth, a generation (odd while
-// attached) and an acknowledgement.
+// Source: xNVMe "uPCIe CUDA" backend page, "Completions in device memory"
+// (completion queues kept in device memory, forwarded to the host CQ by a
+// GPU kernel). Here: one warp per queue forwards each entry whose phase tag
+// has turned; a per-queue slot holds the two CQ addresses, the depth, a
+// generation (odd while attached) and an acknowledgement.
 //
 // One CTA of one warp per slot. Each pass of a warp's loop:
 //   1. every kCheckNs: the stop flag, the time limit (the launch never
 //      outlives limit_ns) and the slot's generation (acquire, system
 //      scope), all in host memory. A generation change ends the current
 //      queue (acknowledge the odd value worked under) and takes up the new
-//      one; an even generation acknowledges the odd value before it. Between
+//      one; with no queue taken up, an even value g > 0 gets ack = g - 1. Between
 //      checks a pass touches only device memory, except for its copies;
 //   2. lane l reads the phase dword of entry head + l (a window of up to 32
 //      entries); the run of leading lanes whose tag is the expected one is

@@ -715,6 +715,8 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
 // ---------------------------------------------------------------------------
 // db_prp_build_static: the same build with its scratch in a static device
 // array instead of a caller workspace (for callers that must not allocate).
+#include <cuda.h>
+
 #include <mutex>
 
 namespace db {
@@ -725,24 +727,61 @@ constexpr size_t kStaticWsBytes = ws_bytes_for(DB_PRP_STATIC_MAX_REQUESTS);
 // Zero when the module loads; every call leaves it ready for the next call.
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
-// Device address of g_static_ws on the current device. Host code cannot use
+// Device address of g_static_ws in the current context. Host code cannot use
 // the symbol itself (on the host it names a stand-in, not device memory), so
-// the address is looked up once per device, with that device current.
+// the address is looked up with the device current and kept per device with
+// the ID of the context it belongs to. A device reset destroys that context
+// (the module, and the array, load again elsewhere in the next one), so a
+// call whose context ID differs looks the address up again. The context
+// queries come from the driver through the runtime's entry-point lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+int current_context_id(CtxGetCurrentFn get_current, CtxGetIdFn get_id, unsigned long long* id) {
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return -1;
+  return get_id(ctx, id) == CUDA_SUCCESS ? 0 : -1;
+}
+
 int static_ws_address(void** out) {
+  struct Entry {
+    unsigned long long ctx_id;
+    void* addr;
+  };
   static std::mutex mu;
-  static void* addr[64] = {nullptr};
+  static Entry cache[64] = {};
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_failure(e);
   if (dev < 0 || dev >= 64) return -EINVAL;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_ws);
+  if (!get_current || !get_id) {
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+    void *f1 = nullptr, *f2 = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
     if (e != cudaSuccess) return cuda_failure(e);
-    addr[dev] = p;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess) return cuda_failure(e);
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return -EIO;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    get_id = reinterpret_cast<CtxGetIdFn>(f2);
   }
-  *out = addr[dev];
+  unsigned long long id = 0;
+  if (cache[dev].addr && current_context_id(get_current, get_id, &id) == 0 &&
+      id == cache[dev].ctx_id) {
+    *out = cache[dev].addr;
+    return 0;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_ws);  // makes the device's context current if need be
+  if (e != cudaSuccess) return cuda_failure(e);
+  if (current_context_id(get_current, get_id, &id) != 0) return -EIO;
+  cache[dev].ctx_id = id;
+  cache[dev].addr = p;
+  *out = p;
   return 0;
 }
 

@@ -1,20 +1,29 @@
 /*
  * cqmirror.h -- the completion-queue mirror of libdescbuild.so (CUDA, sm_103a).
  *
- * Source: xNVMe "uPCIe CUDA" backend page, "Completions in device memory".
- * A controller that writes its payloads into the GPU and its completions into
- * host memory changes destination at every command. Placing the completion
- * queue (CQ) in device memory beside the data gives the controller one
- * destination again. The CPU still owns the queue and polls the host-memory
- * CQ exactly as before. A kernel on the GPU watches each device-memory CQ
- * with one warp and copies completions into the host CQ as their phase bit
- * turns. One kernel serves every queue, up to 64, on a stream of its own.
- * The host and the kernel share a table with a slot per queue: the two CQ
- * addresses, the depth, a generation and an acknowledgement. The host fills
- * a slot and raises its generation to an odd value. The warp copies until
- * the generation changes, then acknowledges the value it worked under, and
- * the host frees nothing before it sees that. A warp finding an even
- * generation acknowledges the odd value before it.
+ * Source: xNVMe "uPCIe CUDA" backend page, section "Completions in device
+ * memory". That section moves an NVMe completion queue (CQ) out of host
+ * memory into device memory, next to the data the controller writes, and
+ * has a GPU kernel forward each completion to the host CQ that the CPU keeps
+ * polling as before.
+ *
+ * This header's contract, as invariants the library keeps:
+ *  - One kernel launch serves up to 64 queues, one warp per queue, on a
+ *    stream of its own.
+ *  - Host and kernel share a table of 64-byte slots, one per queue: the
+ *    device CQ, the host CQ, the depth, a generation counter and an
+ *    acknowledgement.
+ *  - The generation is odd exactly while the slot describes a live queue.
+ *    db_cq_attach fills the slot first and bumps the generation to odd last;
+ *    db_cq_detach bumps it to even.
+ *  - The warp mirrors a queue only under the odd generation it read. When
+ *    it sees any other value, it stops touching that queue's CQs and stores
+ *    the odd generation it was serving into `ack`. A warp serving no queue
+ *    that sees an even, non-zero generation stores the odd value just below
+ *    it (the queue was detached before the warp took it up).
+ *  - The host reuses or releases a slot's CQ memory only after `ack` holds
+ *    the slot's last odd generation (db_cq_wait_ack); db_cq_attach refuses a
+ *    slot whose last generation is not acknowledged yet (-EBUSY).
  *
  * What differs from the page: the kernel is never resident without a limit.
  * A launch ends when the host raises `stop` or after `limit_ns`, whichever

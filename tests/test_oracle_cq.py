@@ -1,7 +1,7 @@
 """Pins for the CQ-mirror oracle.
 
 Follows xNVMe "uPCIe CUDA" backend page, "Completions in device memory":
-completions are copied into the host CQ as their phase bit turns, and a
+an entry is forwarded to the host CQ once its phase tag has flipped, and a
 slot's generation (odd while attached) is acknowledged by the warp that
 worked under it. The phase-tag rule restated here (completion i of a queue
 goes to entry i mod depth, with tag 1 on the first pass through the queue,
