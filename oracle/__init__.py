@@ -63,6 +63,9 @@ def _load():
             lib.oracle_wqe_bucket.restype = None
             lib.oracle_wqe_bucket.argtypes = [vp, u64, vp, vp, u32, u32, u64, u32, u64, vp, u64,
                                               vp, vp, vp]
+            lib.oracle_wqe_bucket_transport.restype = None
+            lib.oracle_wqe_bucket_transport.argtypes = [vp, u64, vp, vp, vp, u32, u32, u64, u32,
+                                                        u64, vp, u64, vp, vp, vp, vp, vp]
             lib.oracle_wqe_bucket_vmm.restype = None
             lib.oracle_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64,
                                                   vp, u64, vp, u32, vp, vp, vp]
@@ -262,6 +265,41 @@ def wqe_bucket(req, peer_ptrs, rkeys, world: int, n_qp: int, local_base: int, lk
                               local_base, lkey, heap_size, _p(rings), depth, _p(head),
                               _p(count), _p(ctr))
     return dict(rings=rings, head=head, count=count, ctr=ctr)
+
+
+DIRECT_DTYPE = np.dtype([("dst", "<u8"), ("src", "<u8"), ("len", "<u4"), ("req_index", "<u4"),
+                         ("pe", "<u2"), ("transport", "u1"), ("rsvd0", "u1"), ("rsvd1", "<u4")])
+XPORT_RDMA, XPORT_P2P, XPORT_SDMA = 0, 1, 2
+
+
+def wqe_bucket_transport(req, peer_ptrs, rkeys, transport, world: int, n_qp: int,
+                         local_base: int, lkey: int, heap_size: int, depth: int, head,
+                         fill: int = 0, rings: np.ndarray | None = None) -> dict:
+    """Puts dispatched on their target PE's transport: RDMA puts become WQEs
+    in their rings (as wqe_bucket), P2P and SDMA puts direct descriptors in
+    request order. Returns rings, head, count, ctr, direct [n_direct, 32] u8
+    and n_direct."""
+    req = _u64(req).reshape(-1, 2)
+    peer_ptrs = _u64(peer_ptrs)
+    rkeys = np.ascontiguousarray(rkeys, dtype=np.uint32)
+    transport = np.ascontiguousarray(transport, dtype=np.uint8)
+    assert transport.shape[0] >= world
+    n_rings = world * n_qp
+    if rings is None:
+        rings = np.full((n_rings, depth, 64), fill, dtype=np.uint8)
+    else:
+        assert rings.dtype == np.uint8 and rings.shape == (n_rings, depth, 64)
+    head = _u64(head).copy()
+    count = np.zeros(n_rings, dtype=np.uint32)
+    ctr = np.zeros(4, dtype=np.uint64)
+    n = req.shape[0]
+    direct = np.full((max(n, 1), 32), fill, dtype=np.uint8)
+    nd = np.zeros(1, dtype=np.uint64)
+    _load().oracle_wqe_bucket_transport(_p(req), n, _p(peer_ptrs), _p(rkeys), _p(transport),
+                                        world, n_qp, local_base, lkey, heap_size, _p(rings),
+                                        depth, _p(head), _p(count), _p(ctr), _p(direct), _p(nd))
+    k = int(nd[0])
+    return dict(rings=rings, head=head, count=count, ctr=ctr, direct=direct[:k], n_direct=k)
 
 
 def wqe_bucket_vmm(req, chunk_raddr, chunk_rkey, chunk_lkey, chunk_shift: int, world: int,

@@ -422,6 +422,119 @@ void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptr
   ctr[3] = err;
 }
 
+// Put translation with a transport per PE -- "mori communication library
+// analysis (1)", the transport dispatch of the put path and the symmetric
+// object set-up before it: every PE is marked once with a transport type
+// (RDMA, P2P or SDMA) and each put branches on its target's type; for a PE
+// that is not reached over RDMA the peer pointer is replaced by the address
+// at which this process maps that PE's heap, so the destination is always
+// peer_ptrs[pe] + offset.
+//
+// transport[pe]: 0 RDMA, 1 P2P, 2 SDMA. Readings:
+//  - An RDMA put is translated and bucketed exactly as by oracle_wqe_bucket
+//    (its ring, seq, slot, fields, overflow rule); puts to other PEs take no
+//    ring slot and do not count in any ring.
+//  - A P2P or SDMA put makes no WQE: it is a copy this process issues itself
+//    (loads/stores through the mapping, or a DMA engine). It becomes a
+//    32-byte direct descriptor, appended in request order to `direct`:
+//    +0 u64 dst = peer_ptrs[pe] + offset, +8 u64 src = local_base + offset,
+//    +16 u32 len, +20 u32 request index, +24 u16 pe, +26 u8 transport,
+//    +27..31 zero.
+//  - Validity is the same rule for every transport (pe < world, qp < n_qp,
+//    bytes >= 1, offset + bytes <= heap_size), and a PE whose transport code
+//    is none of the three makes its puts invalid.
+//  - ctr = {WQEs posted, invalid puts, puts of overflowing rings, error
+//    bits}; *n_direct = direct descriptors written.
+void oracle_wqe_bucket_transport(const uint64_t* req, uint64_t n, const uint64_t* peer_ptrs,
+                                 const uint32_t* rkeys, const uint8_t* transport,
+                                 uint32_t world, uint32_t n_qp, uint64_t local_base,
+                                 uint32_t lkey, uint64_t heap_size, uint8_t* rings,
+                                 uint64_t depth, uint64_t* head, uint32_t* count, uint64_t* ctr,
+                                 uint8_t* direct, uint64_t* n_direct) {
+  uint64_t n_rings = (uint64_t)world * n_qp;
+  std::vector<uint64_t> demand(n_rings, 0);
+  std::vector<int> ring_of(n);     // -1 invalid, -2 direct
+  uint64_t n_invalid = 0;
+  // 1. Validate, dispatch on the target's transport, count per ring.
+  for (uint64_t i = 0; i < n; ++i) {
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint64_t bytes = w1 & 0xFFFFFFFFull;
+    uint64_t pe = (w1 >> 32) & 0xFFFF;
+    uint64_t qp = (w1 >> 48) & 0xFFFF;
+    bool ok = pe < world && qp < n_qp && bytes >= 1 &&
+              (u128)off + (u128)bytes <= (u128)heap_size && transport[pe] <= 2;
+    if (!ok) {
+      ring_of[i] = -1;
+      n_invalid += 1;
+      continue;
+    }
+    if (transport[pe] != 0) {
+      ring_of[i] = -2;
+      continue;
+    }
+    ring_of[i] = (int)(pe * n_qp + qp);
+    demand[ring_of[i]] += 1;
+  }
+  // 2. Overflowing rings take nothing.
+  uint64_t n_overflow = 0, posted = 0, err = 0;
+  std::vector<bool> full(n_rings, false);
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    if (demand[r] > depth) {
+      full[r] = true;
+      n_overflow += demand[r];
+      err |= 2;
+    }
+  }
+  // 3. In request order: WQEs into their rings, direct descriptors appended.
+  std::vector<uint64_t> taken(n_rings, 0);
+  uint64_t nd = 0;
+  for (uint64_t i = 0; i < n; ++i) {
+    int r = ring_of[i];
+    if (r == -1) continue;
+    uint64_t off = req[2 * i];
+    uint64_t w1 = req[2 * i + 1];
+    uint32_t bytes = (uint32_t)(w1 & 0xFFFFFFFFull);
+    uint32_t pe = (uint32_t)((w1 >> 32) & 0xFFFF);
+    if (r == -2) {
+      uint8_t* d = direct + nd * 32;
+      std::memset(d, 0, 32);
+      put_u64(d + 0, peer_ptrs[pe] + off);
+      put_u64(d + 8, local_base + off);
+      put_u32(d + 16, bytes);
+      put_u32(d + 20, (uint32_t)i);
+      d[24] = (uint8_t)(pe & 0xFF);
+      d[25] = (uint8_t)(pe >> 8);
+      d[26] = transport[pe];
+      nd += 1;
+      continue;
+    }
+    if (full[r]) continue;
+    uint64_t seq = head[r] + taken[r];
+    taken[r] += 1;
+    uint8_t* wqe = rings + ((uint64_t)r * depth + (seq % depth)) * 64;
+    std::memset(wqe, 0, 64);
+    put_u64(wqe + 0, peer_ptrs[pe] + off);
+    put_u64(wqe + 8, local_base + off);
+    put_u32(wqe + 16, bytes);
+    put_u32(wqe + 20, lkey);
+    put_u32(wqe + 24, rkeys[pe]);
+    put_u64(wqe + 32, seq);
+    put_u32(wqe + 40, (uint32_t)i);
+    posted += 1;
+  }
+  // 4. Advance heads of the rings that took their batch.
+  for (uint64_t r = 0; r < n_rings; ++r) {
+    count[r] = (uint32_t)demand[r];
+    if (!full[r]) head[r] += demand[r];
+  }
+  ctr[0] = posted;
+  ctr[1] = n_invalid;
+  ctr[2] = n_overflow;
+  ctr[3] = err;
+  *n_direct = nd;
+}
+
 // Put translation on a VMM heap -- "mori communication library analysis
 // (1)", the VMM-heap branch of the put path: while bytes remain, look up the
 // chunk holding the current source address (its lkey and how many bytes of

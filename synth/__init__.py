@@ -37,7 +37,7 @@ SEED_BASE = 0xDB5EED00
 
 # Workload names in the order of the study's configuration list.
 WORKLOADS = ("prp_tiny", "prp_small", "prp_large", "mr_lookup", "put_bucket", "put_bucket_vmm",
-             "mr_lookup_overlap", "mr_register", "mr_deregister")
+             "mr_lookup_overlap", "mr_register", "mr_deregister", "put_bucket_transport")
 
 
 def seed_of(name: str) -> int:
@@ -420,6 +420,29 @@ def put_bucket_vmm(seed: int | None = None, n: int = 8_388_608, world: int = 8,
     return p
 
 
+def put_bucket_transport(seed: int | None = None, n: int = 8_388_608, world: int = 8,
+                         n_qp: int = 4, depth: int = 1 << 19, p2p=(1, 2), sdma=()) -> dict:
+    """The put_bucket batch with a transport per PE.
+
+    The puts are those of put_bucket (same seed rule). transport[pe] is 0
+    (RDMA) except for the PEs in ``p2p`` (1) and ``sdma`` (2): the PEs on
+    this node. Their peer pointers are replaced by the addresses at which
+    this process maps their heaps: random 2 MiB-aligned bases in [2^40, 2^47).
+    """
+    p = put_bucket(seed, n, world, n_qp, depth)
+    rng = _rng((seed_of("put_bucket_transport") if seed is None else seed) ^ 0x3C3C)
+    transport = np.zeros(world, dtype=np.uint8)
+    transport[list(p2p)] = 1
+    transport[list(sdma)] = 2
+    two_mib = 2 * MiB
+    mapped = rng.integers((1 << 40) // two_mib, (1 << 47) // two_mib,
+                          size=world, dtype=np.uint64) * np.uint64(two_mib)
+    peer = p["peer_ptrs"].copy()
+    peer[transport != 0] = mapped[transport != 0]
+    p.update(name="put_bucket_transport", transport=transport, peer_ptrs=peer)
+    return p
+
+
 GENERATORS = {
     "prp_tiny": prp_tiny,
     "prp_small": prp_small,
@@ -427,4 +450,5 @@ GENERATORS = {
     "mr_lookup": mr_lookup,
     "put_bucket": put_bucket,
     "put_bucket_vmm": put_bucket_vmm,
+    "put_bucket_transport": put_bucket_transport,
 }

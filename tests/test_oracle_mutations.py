@@ -86,6 +86,16 @@ MUTANTS = [
      "  if (true) {\n    for (; slot"),
     ("prp: zero tail stops one slot short", "for (; slot < kListSlots; ++slot)",
      "for (; slot + 1 < kListSlots; ++slot)"),
+    ("transport: direct dst from the local base", "put_u64(d + 0, peer_ptrs[pe] + off);",
+     "put_u64(d + 0, local_base + off);"),
+    ("transport: direct src from the peer", "put_u64(d + 8, local_base + off);",
+     "put_u64(d + 8, peer_ptrs[pe] + off);"),
+    ("transport: direct puts counted in their ring", "ring_of[i] = -2;\n      continue;",
+     "ring_of[i] = -2;\n      demand[pe * n_qp + qp] += 1;\n      continue;"),
+    ("transport: unknown codes taken as RDMA", " && transport[pe] <= 2;", ";"),
+    ("transport: direct index counts descriptors", "put_u32(d + 20, (uint32_t)i);",
+     "put_u32(d + 20, (uint32_t)nd);"),
+    ("transport: SDMA puts become WQEs", "if (transport[pe] != 0) {", "if (transport[pe] == 1) {"),
     ("register: a hit takes no reference", "more[i] += 1;", "more[i] += 0;"),
     ("register: new record before an old one with the same start",
      "start[i] <= nit->first.first);", "start[i] < nit->first.first);"),
@@ -130,7 +140,8 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     env = dict(os.environ, DB_ORACLE_LIB=str(lib))
     tests = [os.path.join(ROOT, "tests", f) for f in
              ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
-              "test_oracle_vmm.py", "test_oracle_cq.py", "test_oracle_mr_cache.py")]
+              "test_oracle_vmm.py", "test_oracle_cq.py", "test_oracle_mr_cache.py",
+              "test_oracle_transport.py")]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
