@@ -352,32 +352,35 @@ void oracle_mr_bsearch(const uint64_t* q, uint64_t n_q, const uint64_t* start,
 static void put_u64(uint8_t* p, uint64_t v) { std::memcpy(p, &v, 8); }
 static void put_u32(uint8_t* p, uint32_t v) { std::memcpy(p, &v, 4); }
 
-void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptrs,
-                       const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
-                       uint64_t local_base, uint32_t lkey, uint64_t heap_size,
-                       uint8_t* rings, uint64_t depth, uint64_t* head, uint32_t* count,
-                       uint64_t* ctr) {
-  uint64_t n_rings = (uint64_t)world * n_qp;
-  std::vector<uint64_t> demand(n_rings, 0);
-  std::vector<int> ring_of(n);
-  uint64_t n_invalid = 0;
-  // 1. Validate and count per ring.
-  for (uint64_t i = 0; i < n; ++i) {
-    uint64_t off = req[2 * i];
-    uint64_t w1 = req[2 * i + 1];
-    uint64_t bytes = w1 & 0xFFFFFFFFull;
-    uint64_t pe = (w1 >> 32) & 0xFFFF;
-    uint64_t qp = (w1 >> 48) & 0xFFFF;
-    bool ok = pe < world && qp < n_qp && bytes >= 1 &&
-              (u128)off + (u128)bytes <= (u128)heap_size;
-    if (!ok) {
-      ring_of[i] = -1;
-      n_invalid += 1;
-      continue;
-    }
-    ring_of[i] = (int)(pe * n_qp + qp);
-    demand[ring_of[i]] += 1;
-  }
+struct PutFields {
+  uint64_t off, bytes, pe, qp;
+};
+static PutFields put_fields(const uint64_t* req, uint64_t i) {
+  uint64_t w1 = req[2 * i + 1];
+  return PutFields{req[2 * i], w1 & 0xFFFFFFFFull, (w1 >> 32) & 0xFFFF, (w1 >> 48) & 0xFFFF};
+}
+
+// The validity rule of a put (the same for every transport).
+static bool put_valid(const PutFields& f, uint32_t world, uint32_t n_qp, uint64_t heap_size) {
+  return f.pe < world && f.qp < n_qp && f.bytes >= 1 &&
+         (u128)f.off + (u128)f.bytes <= (u128)heap_size;
+}
+
+// Ring of a valid put.
+static int ring_index(const PutFields& f, uint32_t world, uint32_t n_qp) {
+  (void)world;
+  return (int)(f.pe * n_qp + f.qp);
+}
+
+// Steps 2-4 of the bucketing, given each put's ring (negative: none) and
+// each ring's demand: overflowing rings take nothing, the others get their
+// puts in request order, heads advance. Fills ctr[0], ctr[2], ctr[3].
+static void post_into_rings(const uint64_t* req, uint64_t n, const std::vector<int>& ring_of,
+                            const std::vector<uint64_t>& demand, const uint64_t* peer_ptrs,
+                            const uint32_t* rkeys, uint64_t local_base, uint32_t lkey,
+                            uint8_t* rings, uint64_t depth, uint64_t* head, uint32_t* count,
+                            uint64_t* ctr) {
+  uint64_t n_rings = demand.size();
   // 2. Overflowing rings take nothing.
   uint64_t n_overflow = 0, posted = 0, err = 0;
   std::vector<bool> full(n_rings, false);
@@ -393,19 +396,16 @@ void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptr
   for (uint64_t i = 0; i < n; ++i) {
     int r = ring_of[i];
     if (r < 0 || full[r]) continue;
-    uint64_t off = req[2 * i];
-    uint64_t w1 = req[2 * i + 1];
-    uint32_t bytes = (uint32_t)(w1 & 0xFFFFFFFFull);
-    uint32_t pe = (uint32_t)((w1 >> 32) & 0xFFFF);
+    PutFields f = put_fields(req, i);
     uint64_t seq = head[r] + taken[r];
     taken[r] += 1;
     uint8_t* wqe = rings + ((uint64_t)r * depth + (seq % depth)) * 64;
     std::memset(wqe, 0, 64);
-    put_u64(wqe + 0, peer_ptrs[pe] + off);
-    put_u64(wqe + 8, local_base + off);
-    put_u32(wqe + 16, bytes);
+    put_u64(wqe + 0, peer_ptrs[f.pe] + f.off);
+    put_u64(wqe + 8, local_base + f.off);
+    put_u32(wqe + 16, (uint32_t)f.bytes);
     put_u32(wqe + 20, lkey);
-    put_u32(wqe + 24, rkeys[pe]);
+    put_u32(wqe + 24, rkeys[f.pe]);
     put_u32(wqe + 28, 0);
     put_u64(wqe + 32, seq);
     put_u32(wqe + 40, (uint32_t)i);
@@ -417,9 +417,33 @@ void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptr
     if (!full[r]) head[r] += demand[r];
   }
   ctr[0] = posted;
-  ctr[1] = n_invalid;
   ctr[2] = n_overflow;
   ctr[3] = err;
+}
+
+void oracle_wqe_bucket(const uint64_t* req, uint64_t n, const uint64_t* peer_ptrs,
+                       const uint32_t* rkeys, uint32_t world, uint32_t n_qp,
+                       uint64_t local_base, uint32_t lkey, uint64_t heap_size,
+                       uint8_t* rings, uint64_t depth, uint64_t* head, uint32_t* count,
+                       uint64_t* ctr) {
+  uint64_t n_rings = (uint64_t)world * n_qp;
+  std::vector<uint64_t> demand(n_rings, 0);
+  std::vector<int> ring_of(n);
+  uint64_t n_invalid = 0;
+  // 1. Validate and count per ring.
+  for (uint64_t i = 0; i < n; ++i) {
+    PutFields f = put_fields(req, i);
+    if (!put_valid(f, world, n_qp, heap_size)) {
+      ring_of[i] = -1;
+      n_invalid += 1;
+      continue;
+    }
+    ring_of[i] = ring_index(f, world, n_qp);
+    demand[ring_of[i]] += 1;
+  }
+  post_into_rings(req, n, ring_of, demand, peer_ptrs, rkeys, local_base, lkey, rings, depth,
+                  head, count, ctr);
+  ctr[1] = n_invalid;
 }
 
 // Put translation with a transport per PE -- "mori communication library
@@ -457,81 +481,39 @@ void oracle_wqe_bucket_transport(const uint64_t* req, uint64_t n, const uint64_t
   uint64_t n_invalid = 0;
   // 1. Validate, dispatch on the target's transport, count per ring.
   for (uint64_t i = 0; i < n; ++i) {
-    uint64_t off = req[2 * i];
-    uint64_t w1 = req[2 * i + 1];
-    uint64_t bytes = w1 & 0xFFFFFFFFull;
-    uint64_t pe = (w1 >> 32) & 0xFFFF;
-    uint64_t qp = (w1 >> 48) & 0xFFFF;
-    bool ok = pe < world && qp < n_qp && bytes >= 1 &&
-              (u128)off + (u128)bytes <= (u128)heap_size && transport[pe] <= 2;
-    if (!ok) {
+    PutFields f = put_fields(req, i);
+    if (!put_valid(f, world, n_qp, heap_size) || transport[f.pe] > 2) {
       ring_of[i] = -1;
       n_invalid += 1;
       continue;
     }
-    if (transport[pe] != 0) {
+    if (transport[f.pe] != 0) {
       ring_of[i] = -2;
       continue;
     }
-    ring_of[i] = (int)(pe * n_qp + qp);
+    ring_of[i] = ring_index(f, world, n_qp);
     demand[ring_of[i]] += 1;
   }
-  // 2. Overflowing rings take nothing.
-  uint64_t n_overflow = 0, posted = 0, err = 0;
-  std::vector<bool> full(n_rings, false);
-  for (uint64_t r = 0; r < n_rings; ++r) {
-    if (demand[r] > depth) {
-      full[r] = true;
-      n_overflow += demand[r];
-      err |= 2;
-    }
-  }
-  // 3. In request order: WQEs into their rings, direct descriptors appended.
-  std::vector<uint64_t> taken(n_rings, 0);
+  // 2-4. The RDMA puts, into their rings.
+  post_into_rings(req, n, ring_of, demand, peer_ptrs, rkeys, local_base, lkey, rings, depth,
+                  head, count, ctr);
+  ctr[1] = n_invalid;
+  // The direct puts, appended in request order.
   uint64_t nd = 0;
   for (uint64_t i = 0; i < n; ++i) {
-    int r = ring_of[i];
-    if (r == -1) continue;
-    uint64_t off = req[2 * i];
-    uint64_t w1 = req[2 * i + 1];
-    uint32_t bytes = (uint32_t)(w1 & 0xFFFFFFFFull);
-    uint32_t pe = (uint32_t)((w1 >> 32) & 0xFFFF);
-    if (r == -2) {
-      uint8_t* d = direct + nd * 32;
-      std::memset(d, 0, 32);
-      put_u64(d + 0, peer_ptrs[pe] + off);
-      put_u64(d + 8, local_base + off);
-      put_u32(d + 16, bytes);
-      put_u32(d + 20, (uint32_t)i);
-      d[24] = (uint8_t)(pe & 0xFF);
-      d[25] = (uint8_t)(pe >> 8);
-      d[26] = transport[pe];
-      nd += 1;
-      continue;
-    }
-    if (full[r]) continue;
-    uint64_t seq = head[r] + taken[r];
-    taken[r] += 1;
-    uint8_t* wqe = rings + ((uint64_t)r * depth + (seq % depth)) * 64;
-    std::memset(wqe, 0, 64);
-    put_u64(wqe + 0, peer_ptrs[pe] + off);
-    put_u64(wqe + 8, local_base + off);
-    put_u32(wqe + 16, bytes);
-    put_u32(wqe + 20, lkey);
-    put_u32(wqe + 24, rkeys[pe]);
-    put_u64(wqe + 32, seq);
-    put_u32(wqe + 40, (uint32_t)i);
-    posted += 1;
+    if (ring_of[i] != -2) continue;
+    PutFields f = put_fields(req, i);
+    uint8_t* d = direct + nd * 32;
+    std::memset(d, 0, 32);
+    put_u64(d + 0, peer_ptrs[f.pe] + f.off);
+    put_u64(d + 8, local_base + f.off);
+    put_u32(d + 16, (uint32_t)f.bytes);
+    put_u32(d + 20, (uint32_t)i);
+    d[24] = (uint8_t)(f.pe & 0xFF);
+    d[25] = (uint8_t)(f.pe >> 8);
+    d[26] = transport[f.pe];
+    nd += 1;
   }
-  // 4. Advance heads of the rings that took their batch.
-  for (uint64_t r = 0; r < n_rings; ++r) {
-    count[r] = (uint32_t)demand[r];
-    if (!full[r]) head[r] += demand[r];
-  }
-  ctr[0] = posted;
-  ctr[1] = n_invalid;
-  ctr[2] = n_overflow;
-  ctr[3] = err;
   *n_direct = nd;
 }
 

@@ -53,15 +53,15 @@ MUTANTS = [
     ("mr bsearch takes lower_bound",
      "std::upper_bound(start, start + n_mr, base);", "std::lower_bound(start, start + n_mr, base);"),
     ("wqe ring order is qp-major",
-     "ring_of[i] = (int)(pe * n_qp + qp);", "ring_of[i] = (int)(qp * world + pe);"),
+     "return (int)(f.pe * n_qp + f.qp);", "return (int)(f.qp * world + f.pe);"),
     ("wqe seq ignores the head",
      "uint64_t seq = head[r] + taken[r];", "uint64_t seq = taken[r];"),
     ("wqe rkey of the local PE",
-     "put_u32(wqe + 24, rkeys[pe]);", "put_u32(wqe + 24, rkeys[0]);"),
+     "put_u32(wqe + 24, rkeys[f.pe]);", "put_u32(wqe + 24, rkeys[0]);"),
     ("wqe ring full one early",
      "if (demand[r] > depth) {", "if (demand[r] >= depth) {"),
     ("wqe raddr from the local base",
-     "put_u64(wqe + 0, peer_ptrs[pe] + off);", "put_u64(wqe + 0, local_base + off);"),
+     "put_u64(wqe + 0, peer_ptrs[f.pe] + f.off);", "put_u64(wqe + 0, local_base + f.off);"),
     ("vmm raddr adds the heap offset, not the chunk offset",
      "chunk_raddr[pe * n_chunks + dst_chunk] + (dst % C);",
      "chunk_raddr[pe * n_chunks + dst_chunk] + dst;"),
@@ -86,16 +86,17 @@ MUTANTS = [
      "  if (true) {\n    for (; slot"),
     ("prp: zero tail stops one slot short", "for (; slot < kListSlots; ++slot)",
      "for (; slot + 1 < kListSlots; ++slot)"),
-    ("transport: direct dst from the local base", "put_u64(d + 0, peer_ptrs[pe] + off);",
-     "put_u64(d + 0, local_base + off);"),
-    ("transport: direct src from the peer", "put_u64(d + 8, local_base + off);",
-     "put_u64(d + 8, peer_ptrs[pe] + off);"),
+    ("transport: direct dst from the local base", "put_u64(d + 0, peer_ptrs[f.pe] + f.off);",
+     "put_u64(d + 0, local_base + f.off);"),
+    ("transport: direct src from the peer", "put_u64(d + 8, local_base + f.off);",
+     "put_u64(d + 8, peer_ptrs[f.pe] + f.off);"),
     ("transport: direct puts counted in their ring", "ring_of[i] = -2;\n      continue;",
-     "ring_of[i] = -2;\n      demand[pe * n_qp + qp] += 1;\n      continue;"),
-    ("transport: unknown codes taken as RDMA", " && transport[pe] <= 2;", ";"),
+     "ring_of[i] = -2;\n      demand[ring_index(f, world, n_qp)] += 1;\n      continue;"),
+    ("transport: unknown codes taken as RDMA", " || transport[f.pe] > 2) {", ") {"),
     ("transport: direct index counts descriptors", "put_u32(d + 20, (uint32_t)i);",
      "put_u32(d + 20, (uint32_t)nd);"),
-    ("transport: SDMA puts become WQEs", "if (transport[pe] != 0) {", "if (transport[pe] == 1) {"),
+    ("transport: SDMA puts become WQEs", "if (transport[f.pe] != 0) {",
+     "if (transport[f.pe] == 1) {"),
     ("register: a hit takes no reference", "more[i] += 1;", "more[i] += 0;"),
     ("register: new record before an old one with the same start",
      "start[i] <= nit->first.first);", "start[i] < nit->first.first);"),
