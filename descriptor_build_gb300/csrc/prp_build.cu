@@ -12,7 +12,8 @@
 //   2. page count n and list-page count L per request, block scan of L;
 //   3. decoupled lookback over the tiles before it (one status word per
 //      tile in the workspace, bounded wait) gives the tile's first list page;
-//      a tile with no list (and no page_base output) skips the wait;
+//      a tile with no list, in a call without page_base output, skips the
+//      scan and the wait and takes its next ticket at once;
 //   4. PRP1/PRP2, page_base and status go out as 16/8/1-byte stores;
 //   5. the tile's lists are written by warps that take one request at a time
 //      from a shared-memory queue: each list is a contiguous run of 8-byte
@@ -308,6 +309,14 @@ __device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, 
   }
 }
 
+// Whether any of a thread's requests owns list pages.
+__device__ __forceinline__ bool any_list_rows(const uint32_t (&L)[kItems]) {
+  uint32_t a = 0;
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) a |= L[k];
+  return a != 0;
+}
+
 // Exclusive scan over a tile held as kItems rows of kThreads values, in
 // request order (row-major: request k * kThreads + thread). s_scan holds
 // kItems * kWarps values.
@@ -415,11 +424,11 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
 }
 
 __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(const Params p) {
-  __shared__ unsigned long long s_ticket;
+  __shared__ unsigned long long s_ticket[2];  // this tile's ticket, the next one's
   __shared__ uint64_t s_scan[kItems * kWarps + 1];
   __shared__ unsigned long long s_excl;
   __shared__ int s_failed;
-  __shared__ uint32_t s_next, s_next_short;
+  __shared__ uint32_t s_next, s_next_short, s_warps_done;
   __shared__ ulonglong2 s_list[kTile];
 
   const int lane = threadIdx.x & 31;
@@ -430,10 +439,15 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
   uint64_t my_pages = 0;  // list pages of this CTA's tiles (thread 0's count is used)
   bool any_failed = false;
 
-  for (;;) {
-    if (threadIdx.x == 0) s_ticket = atomicAdd(&p.hdr->ticket, 1ull);
+  if (threadIdx.x == 0) {
+    s_ticket[0] = atomicAdd(&p.hdr->ticket, 1ull);
+    s_warps_done = 0;
+  }
+  for (uint32_t round = 0;; ++round) {
+    // Every thread is past the previous tile (its lists included) here, so
+    // the tile's shared memory is free again.
     __syncthreads();
-    const uint64_t tile = s_ticket;
+    const uint64_t tile = s_ticket[round & 1];
     if (tile >= p.n_tiles) break;
 
     // 1-2. Four requests per thread (rows of the tile): validity, pages
@@ -464,6 +478,36 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
       const bool is_short = L[k] != 0 && npg[k] - 1 <= kShortWords;  // then L = 1, words = n - 1
       v[k] = (uint64_t)L[k] | ((uint64_t)(is_short ? 1 : 0) << 23) |
              ((uint64_t)(L[k] != 0 && !is_short ? 1 : 0) << 35);
+    }
+    // A tile none of whose requests owns a list, in a call that writes no
+    // page_base, needs neither the scan nor its predecessors: it publishes a
+    // zero aggregate, takes its next ticket at once (the atomic's latency
+    // hides behind the tile's LUT gathers and stores; it holds that ticket
+    // only for this short tile, so no later tile waits on it for long) and
+    // writes its PRP pairs.
+    const bool lists = __syncthreads_or(any_list_rows(L)) != 0;
+    if (!lists && !p.page_base) {
+      unsigned long long next_ticket = 0;
+      if (threadIdx.x == 0) {
+        next_ticket = atomicAdd(&p.hdr->ticket, 1ull);
+        st_relaxed(p.tile_status + tile, status_word(tile == 0 ? kPrefix : kAggregate, epoch, 0));
+      }
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+        uint64_t prp1 = 0, prp2 = 0;
+        if (valid[k]) {
+          prp1 = bus(p.lut, off[k], pol_last);
+          if (npg[k] == 2) prp2 = bus(p.lut, (off[k] & ~4095ull) + 4096, pol_last);
+        }
+        if (i < p.n) {
+          st_stream16(p.prp + i, prp1, prp2, pol_first);
+          if (p.status) p.status[i] = valid[k] ? DB_PRP_OK : DB_PRP_INVALID;
+          my_invalid += !valid[k];
+        }
+      }
+      if (threadIdx.x == 0) s_ticket[(round + 1) & 1] = next_ticket;
+      continue;
     }
     // The PRP1 / PRP2 gathers do not depend on the scan: optionally start
     // them before it (DB_PRP_EARLY_LUT).
@@ -600,7 +644,12 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
       sv = nsv;
       swin = nswin;
     }
-    __syncthreads();
+    // The last warp to finish the tile's lists takes the next ticket, so no
+    // ticket is held while lists of this tile are still being written.
+    if (lane == 0 && atomicAdd(&s_warps_done, 1u) == kWarps - 1) {
+      s_warps_done = 0;
+      s_ticket[(round + 1) & 1] = atomicAdd(&p.hdr->ticket, 1ull);
+    }
   }
 
   // Counters and hand-off to the next call.
