@@ -74,7 +74,8 @@ def parse():
                     help="run a step's four calls one after another on one stream "
                          "(default: each on its own stream, all at once)")
     ap.add_argument("--next-only", choices=["mr_register", "mr_deregister", "put_bucket_vmm",
-                                            "put_bucket_vmm_psn", "mr_lookup_overlap"],
+                                            "put_bucket_vmm_psn", "mr_lookup_overlap",
+                                            "put_bucket_transport"],
                     help="profiling aid: time one of the rows after the hot path, alone")
     return ap.parse_args()
 
@@ -341,6 +342,7 @@ def run_next(args, device) -> dict:
     import torch as t
     stream = t.cuda.Stream(device=device)
     out = time_vmm(args, device, stream)
+    out["put_bucket_transport"] = time_transport(args, device, stream)
     out["mr_lookup_overlap"] = time_mr_overlap(args, device, stream)
     out.update(time_mr_mutation(args, device, stream))
     out["cq_mirror"] = time_cq_mirror(args, device)
@@ -401,6 +403,46 @@ def time_vmm(args, device, stream, only=None) -> dict:
             "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "launches": 4,
             "note": "not part of the step: timed alone, same stream discipline"}
     return out
+
+
+def time_transport(args, device, stream) -> dict:
+    """db_wqe_bucket_transport on the put batch with PEs 1 and 2 on P2P: RDMA
+    puts into the rings, the others as direct records."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    import synth
+    P = synth.put_bucket_transport()
+    d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+    d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+    R = P["world"] * P["n_qp"]
+    n = P["req"].shape[0]
+    b = dict(req=d64(P["req"]), peer=d64(P["peer_ptrs"]), rkeys=d32(P["rkeys"]),
+             transport=t.from_numpy(P["transport"]).to(device),
+             rings=t.empty((R, P["depth"], 64), dtype=t.uint8, device=device),
+             head=d64(P["head"]), count=t.empty(R, dtype=t.int32, device=device),
+             direct=t.empty((n, 32), dtype=t.uint8, device=device),
+             n_direct=t.zeros(1, dtype=t.int64, device=device),
+             ctr=t.zeros(4, dtype=t.int64, device=device),
+             ws=db.workspace(db.wqe_workspace_size(n, R), device))
+
+    def call():
+        db.wqe_bucket_transport(b["req"], b["peer"], b["rkeys"], b["transport"], P["world"],
+                                P["n_qp"], P["local_base"], P["lkey"], P["heap_size"],
+                                b["rings"], P["depth"], b["head"], b["count"], b["direct"],
+                                b["n_direct"], b["ws"], ctr=b["ctr"], stream=stream)
+
+    ms = _event_ms(t, stream, call, args.warmup, args.steps)
+    if int(b["ctr"][3].item()):
+        raise RuntimeError("put_bucket_transport: device error bits")
+    wqes, nd = int(b["ctr"][0].item()), int(b["n_direct"].item())
+    alg = 16 * n + 64 * wqes + 32 * nd
+    peak, _ = peak_gbs()
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "M_req_per_s": round(n / ms / 1e3, 2), "wqes": wqes,
+            "direct": nd, "p2p_pes": [int(x) for x in np.flatnonzero(P["transport"] == 1)],
+            "algorithmic_bytes": alg, "GB_per_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "launches": 3,
+            "note": "not part of the step: timed alone, same stream discipline"}
 
 
 def _event_ms(t, stream, call, warmup, steps) -> float:
@@ -1044,6 +1086,8 @@ def main():
                 res = time_vmm(args, device, s, only=args.next_only)
             elif args.next_only == "mr_lookup_overlap":
                 res = {"mr_lookup_overlap": time_mr_overlap(args, device, s)}
+            elif args.next_only == "put_bucket_transport":
+                res = {"put_bucket_transport": time_transport(args, device, s)}
             else:
                 res = time_mr_mutation(args, device, s, only=args.next_only)
             print(json.dumps({"next_only": args.next_only, **res,

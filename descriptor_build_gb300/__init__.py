@@ -29,7 +29,9 @@ from . import build as _build
 __all__ = [
     "DescBuildError", "lib_path", "workspace", "prp_workspace_size", "prp_build",
     "prp_build_static", "PRP_STATIC_MAX_REQUESTS",
-    "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size", "wqe_vmm_workspace_size", "wqe_bucket", "wqe_bucket_vmm",
+    "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size",
+    "wqe_vmm_workspace_size", "wqe_bucket", "wqe_bucket_vmm", "wqe_bucket_transport",
+    "XPORT_RDMA", "XPORT_P2P", "XPORT_SDMA",
     "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "cq_slots", "cq_slot_fields",
     "mr_capacity_for", "mr_register_workspace_size", "mr_register",
     "mr_deregister_workspace_size", "mr_deregister", "MR_NEW", "MR_NEW_DUP", "DEREG_OK",
@@ -43,6 +45,7 @@ PRP_OK, PRP_INVALID, PRP_OVERFLOW = 0, 1, 2
 MR_MISS, MR_EXACT, MR_CONTAINED, MR_INVALID = 0, 1, 2, 3
 ERR_TIMEOUT, ERR_RING_OVERFLOW, ERR_TABLE_ORDER = 1, 2, 4
 PRP_ZERO_TAIL = 1
+XPORT_RDMA, XPORT_P2P, XPORT_SDMA = 0, 1, 2
 
 lib_path = _build.LIB
 
@@ -78,9 +81,12 @@ def _load():
                                   vp, sz, vp]
     lib.db_wqe_bucket_vmm.argtypes = [vp, u64, vp, vp, vp, u32, u32, u32, u64, u64, vp, u64, vp,
                                       vp, u32, vp, vp, vp, sz, vp]
+    lib.db_wqe_bucket_transport.argtypes = [vp, u64, vp, vp, vp, u32, u32, u64, u32, u64, vp,
+                                            u64, vp, vp, vp, vp, vp, vp, sz, vp]
     for name in ("db_prp_workspace_size", "db_prp_build", "db_prp_build_static",
                  "db_mr_workspace_size",
-                 "db_mr_lookup", "db_mr_lookup_overlap", "db_wqe_workspace_size", "db_wqe_bucket", "db_wqe_bucket_vmm",
+                 "db_mr_lookup", "db_mr_lookup_overlap", "db_wqe_workspace_size", "db_wqe_bucket",
+                 "db_wqe_bucket_vmm", "db_wqe_bucket_transport",
                  "db_last_cuda_error"):
         getattr(lib, name).restype = i32
     lib.db_mr_capacity_for.argtypes = [u64]
@@ -291,6 +297,23 @@ def wqe_bucket(req: torch.Tensor, peer_ptrs: torch.Tensor, rkeys: torch.Tensor, 
         _ptr(req), n, _ptr(peer_ptrs), _ptr(rkeys), world, n_qp, local_base, lkey, heap_size,
         _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(ctr), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def wqe_bucket_transport(req: torch.Tensor, peer_ptrs: torch.Tensor, rkeys: torch.Tensor,
+                         transport: torch.Tensor, world: int, n_qp: int, local_base: int,
+                         lkey: int, heap_size: int, rings: torch.Tensor, depth: int,
+                         head: torch.Tensor, count: torch.Tensor, direct: torch.Tensor,
+                         n_direct: torch.Tensor, ws: torch.Tensor,
+                         ctr: torch.Tensor | None = None, stream=None) -> None:
+    """db_wqe_bucket_transport: puts dispatched on their PE's transport (uint8
+    [world] of XPORT_*): RDMA puts into WQE rings as wqe_bucket, P2P and SDMA
+    puts as 32-byte direct records (uint8 [n, 32]) in batch order; n_direct
+    (int64 [1]) gets their number."""
+    n = _records(req, 16)
+    _check("db_wqe_bucket_transport", _lib.db_wqe_bucket_transport(
+        _ptr(req), n, _ptr(peer_ptrs), _ptr(rkeys), _ptr(transport), world, n_qp, local_base,
+        lkey, heap_size, _ptr(rings), depth, _ptr(head), _ptr(count), _ptr(direct),
+        _ptr(n_direct), _ptr(ctr), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def wqe_bucket_vmm(req: torch.Tensor, chunk_raddr: torch.Tensor, chunk_rkey: torch.Tensor,

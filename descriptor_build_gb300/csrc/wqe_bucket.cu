@@ -113,6 +113,11 @@ struct Params {
   uint32_t* psn_counts;  // [V][stride]
   uint64_t* psn_old;
   uint64_t* psn_tot;
+  // Transport per PE (db_wqe_bucket_transport): bin R + 1 collects the puts
+  // to P2P and SDMA PEs, which become direct descriptors in batch order.
+  const uint8_t* transport;  // [world]
+  unsigned char* direct;     // [n] 32-byte descriptors
+  uint64_t* n_direct;
 };
 
 // Ring of a put, or R for an invalid one.
@@ -124,6 +129,17 @@ __device__ __forceinline__ uint32_t bin_of(const Params& p, const ulonglong2 r) 
   const bool ok = pe < p.world && qp < p.n_qp && bytes != 0 && off <= p.heap_size &&
                   (uint64_t)bytes <= p.heap_size - off;
   return ok ? pe * p.n_qp + qp : p.R;
+}
+
+// With a transport table: an RDMA put keeps its ring, a P2P or SDMA put goes
+// to the direct bin R + 1, and a PE with any other code makes its puts
+// invalid (bin R).
+template <bool kXport>
+__device__ __forceinline__ uint32_t bin_for(const Params& p, const ulonglong2 r) {
+  const uint32_t b = bin_of(p, r);
+  if (!kXport || b >= p.R) return b;
+  const uint32_t t = __ldg(p.transport + ((uint32_t)(r.y >> 32) & 0xFFFFu));
+  return t == 0 ? b : (t <= 2 ? p.R + 1 : p.R);
 }
 
 // WQEs a valid put makes: one, or on a VMM heap one per chunk it touches.
@@ -182,7 +198,7 @@ constexpr int kCountUnroll = DB_WQE_COUNT_UNROLL;  // rows of 32 puts loaded at 
 
 // kVmm / kPsn: the call's heap kind and whether PSNs are counted, fixed at
 // compile time so that the common static-heap pass carries no per-put tests.
-template <bool kVmm, bool kPsn>
+template <bool kVmm, bool kPsn, bool kXport = false>
 __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p) {
   extern __shared__ uint32_t s_hist_all[];  // [kCountWarps][V] WQEs, then PSNs if asked
   if (DB_WQE_PDL) {
@@ -212,11 +228,11 @@ __global__ void __launch_bounds__(kCountThreads) wqe_count_kernel(const Params p
 #pragma unroll
       for (int u = 0; u < kCountUnroll; ++u) {
         const uint64_t i = tile * kTile + (uint64_t)(row + u) * 32 + lane;
-        const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;
+        const uint32_t bin = i < p.n ? bin_for<kXport>(p, r[u]) : V;
         if (kPsn && bin < p.R) atomicAdd(&s_psn[bin], psns_of(p, r[u]));
         if (DB_WQE_COUNT_MODE == 1) {
           if (bin < p.R) atomicAdd(&s_hist[bin], kVmm ? wqes_of(p, r[u]) : 1u);
-          else if (bin == p.R) atomicAdd(&s_hist[bin], 1u);
+          else if (bin < V) atomicAdd(&s_hist[bin], 1u);
         } else {
           const uint32_t peers = __match_any_sync(kFull, bin);
           if (kVmm) {  // weights differ per put
@@ -335,8 +351,10 @@ __global__ void __launch_bounds__(kScanThreads) wqe_scan_kernel(const Params p) 
         atomicAdd(&p.hdr->overflow, (unsigned long long)total);
       else if (total)
         atomicAdd(&p.hdr->posted, (unsigned long long)total);
-    } else if (total) {
-      atomicAdd(&p.hdr->invalid, (unsigned long long)total);
+    } else if (v == p.R) {
+      if (total) atomicAdd(&p.hdr->invalid, (unsigned long long)total);
+    } else {  // the direct bin of a transport call
+      *p.n_direct = total;
     }
     __threadfence();
     s_last = atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1;
@@ -384,6 +402,7 @@ inline int scatter_warps(uint32_t V) {
 }
 inline size_t scatter_smem(uint32_t V) { return cta_smem(V) + scatter_warps(V) * warp_smem(V); }
 
+template <bool kXport>
 __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const uint32_t V = p.V, R = p.R;
@@ -429,7 +448,7 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
 #pragma unroll
   for (int u = 0; u < kRows; ++u) {
     const uint64_t i = t0 + (uint64_t)u * 32 + lane;
-    const uint32_t bin = i < p.n ? bin_of(p, r[u]) : V;  // outside the batch: no bin
+    const uint32_t bin = i < p.n ? bin_for<kXport>(p, r[u]) : V;  // outside the batch: no bin
     s_put[u * 32 + lane] = r[u];
     const uint32_t peers = __match_any_sync(kFull, bin);
     const uint32_t before = peers & lanemask_lt();
@@ -464,7 +483,32 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
     }
     carry += __shfl_sync(kFull, x, 31);
   }
+  if (kXport && lane == 0) {  // the direct bin: prefix of its counts over the rows
+    uint32_t tot = 0;
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const uint32_t c = s_cnt[u * V + R + 1];
+      s_cnt[u * V + R + 1] = (uint16_t)tot;
+      tot += c;
+    }
+  }
   __syncwarp();
+  if (kXport) {
+    // Direct descriptors, in batch order from the tile's first slot (the
+    // count pass's scan of the direct bin): one 32-byte store per put.
+    const uint64_t d0 = p.counts[(uint64_t)(R + 1) * p.stride + tile];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      if ((bin_rank[u] & 0xFFFFu) != R + 1) continue;
+      const ulonglong2 x = r[u];
+      const uint32_t pe = (uint32_t)(x.y >> 32) & 0xFFFFu;
+      const uint64_t at = d0 + s_cnt[u * V + R + 1] + (bin_rank[u] >> 16);
+      const uint32_t t = __ldg(p.transport + pe);
+      st_stream32(p.direct + (at << 5), s_peer[pe] + x.x, p.local_base + x.x,
+                  (uint64_t)(uint32_t)x.y | ((t0 + (uint64_t)u * 32 + lane) << 32),
+                  (uint64_t)pe | ((uint64_t)t << 16), pol_first);
+    }
+  }
   // 3. Ring-order permutation of the valid puts.
 #pragma unroll
   for (int u = 0; u < kRows; ++u) {
@@ -715,7 +759,10 @@ int prepare_scatter() {
   cudaGetDevice(&dev);
   if (!done_for[dev & 63]) {
     cudaError_t e = cudaFuncSetAttribute(
-        wqe_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+        wqe_scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wqe_scatter_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
     e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kMaxSmem);
@@ -729,6 +776,9 @@ int prepare_scatter() {
                                cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(wqe_count_kernel<true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wqe_count_kernel<false, false, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, count_smem);
     if (e != cudaSuccess) return cuda_failure(e);
     done_for[dev & 63] = true;
@@ -825,7 +875,10 @@ int run(const wqe::Params& p, cudaStream_t s) {
   if (count_grid > count_need) count_grid = count_need;
   {
     const size_t count_smem = (size_t)wqe::kCountWarps * p.V * 4 * (p.mtu ? 2 : 1);
-    if (!p.vmm) {
+    if (!p.vmm && p.transport) {
+      wqe::wqe_count_kernel<false, false, true><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
+      rc = launch_result();
+    } else if (!p.vmm) {
       wqe::wqe_count_kernel<false, false><<<(unsigned)count_grid, wqe::kCountThreads, count_smem, s>>>(p);
       rc = launch_result();
     } else {
@@ -848,7 +901,9 @@ int run(const wqe::Params& p, cudaStream_t s) {
     rc = launch_result();
   }
   if (rc) return rc;
-  void (*scatter)(const wqe::Params) = p.vmm ? wqe::wqe_scatter_vmm_kernel : wqe::wqe_scatter_kernel;
+  void (*scatter)(const wqe::Params) = p.vmm         ? wqe::wqe_scatter_vmm_kernel
+                                       : p.transport ? wqe::wqe_scatter_kernel<true>
+                                                     : wqe::wqe_scatter_kernel<false>;
   const int sw = p.vmm ? wqe::vmm_scatter_warps(p.V)
                        : wqe::scatter_warps(p.V);  // kSWarps, fewer when many rings
   const size_t smem = p.vmm ? wqe::vmm_scatter_smem(p.V) : wqe::scatter_smem(p.V);
@@ -875,6 +930,37 @@ extern "C" int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* 
   p.rkeys = rkeys;
   p.lkey = lkey;
   p.vmm = false;
+  return run(p, s);
+}
+
+extern "C" int db_wqe_bucket_transport(const db_put_req* req, uint64_t n,
+                                       const uint64_t* peer_ptrs, const uint32_t* rkeys,
+                                       const uint8_t* transport, uint32_t world, uint32_t n_qp,
+                                       uint64_t local_base, uint32_t lkey, uint64_t heap_size,
+                                       db_wqe* rings, uint64_t depth, uint64_t* head,
+                                       uint32_t* count, db_direct* direct, uint64_t* n_direct,
+                                       db_counters* ctr, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!n_direct || !aligned(n_direct, 8)) return -EINVAL;
+  wqe::Params p{};
+  const int rc = setup(p, req, n, world, n_qp, local_base, heap_size, rings, depth, head, count,
+                       ctr, ws, ws_bytes, s);
+  if (rc == 1) {  // empty batch: counts and counters already zeroed
+    cudaMemsetAsync(n_direct, 0, 8, s);
+    return launch_result();
+  }
+  if (rc) return rc;
+  if (!peer_ptrs || !rkeys || !transport || !direct) return -EINVAL;
+  if (!aligned(peer_ptrs, 8) || !aligned(rkeys, 4) || !aligned(direct, 32)) return -EINVAL;
+  p.peer_ptrs = peer_ptrs;
+  p.rkeys = rkeys;
+  p.lkey = lkey;
+  p.vmm = false;
+  p.transport = transport;
+  p.direct = reinterpret_cast<unsigned char*>(direct);
+  p.n_direct = n_direct;
+  p.V = p.R + 2;  // rings, invalid, direct
   return run(p, s);
 }
 

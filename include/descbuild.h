@@ -88,6 +88,19 @@ typedef struct db_wqe {
   uint32_t rsvd[5];   /* 0                                 */
 } db_wqe;             /* 64 bytes */
 
+/* A put to a PE reached without RDMA (db_wqe_bucket_transport): the copy
+ * this process issues itself, through its mapping of the peer's heap. */
+typedef struct db_direct {
+  uint64_t dst;       /* peer_ptrs[pe] + off (the mapped peer heap) */
+  uint64_t src;       /* local_base + off                           */
+  uint32_t len;       /* bytes                                      */
+  uint32_t req_index; /* position of the put in the batch           */
+  uint16_t pe;
+  uint8_t transport;  /* DB_XPORT_P2P or DB_XPORT_SDMA              */
+  uint8_t rsvd0;      /* 0                                          */
+  uint32_t rsvd1;     /* 0                                          */
+} db_direct;          /* 32 bytes */
+
 /* Batch counters, written by the device at the end of a call. */
 typedef struct db_counters {
   uint64_t total;      /* prp: list pages the batch needs; wqe: entries posted */
@@ -112,6 +125,10 @@ typedef struct db_counters {
 #define DB_ERR_TABLE_ORDER 4u   /* the MR table is not sorted and non-overlapping            */
 
 #define DB_PRP_ZERO_TAIL 1u     /* db_prp_build: zero the unused slots of each last list page */
+
+#define DB_XPORT_RDMA 0 /* db_wqe_bucket_transport: how each PE is reached */
+#define DB_XPORT_P2P 1
+#define DB_XPORT_SDMA 2
 
 /* ---- PRP build ------------------------------------------------------------
  * Source: xNVMe "uPCIe CUDA" backend page. Introduction: the CUDA driver
@@ -261,6 +278,40 @@ int db_wqe_bucket(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
                   uint32_t lkey, uint64_t heap_size, db_wqe* rings, uint64_t depth,
                   uint64_t* head, uint32_t* count, db_counters* ctr, void* ws,
                   size_t ws_bytes, void* stream);
+
+/* ---- put translation with a transport per PE --------------------------------
+ * Source: "mori communication library analysis (1)": the put path branches
+ * on its target PE's transport type (RDMA, P2P or SDMA), fixed per PE when
+ * the connections are set up; for a PE that is not reached over RDMA the
+ * symmetric object's peer pointer holds the address at which this process
+ * maps that PE's heap, so the destination is peer_ptrs[pe] + off whatever
+ * the transport.
+ *
+ * Put i is valid under db_wqe_bucket's rule and when transport[pe] is one of
+ * DB_XPORT_RDMA / _P2P / _SDMA (any other code makes the PE's puts invalid).
+ *   transport[pe] == DB_XPORT_RDMA: a WQE, exactly as db_wqe_bucket (ring
+ *     r = pe * n_qp + qp, seq = head[r] + earlier RDMA puts of ring r, the
+ *     overflow rule); puts to other PEs take no ring slot and do not count
+ *     in count[] or in any ring's overflow decision.
+ *   P2P or SDMA: no WQE; a db_direct record, the k-th valid such put of the
+ *     batch (batch order) at direct[k]: dst = peer_ptrs[pe] + off,
+ *     src = local_base + off, len = bytes, req_index, pe, transport.
+ *
+ * Arguments as for db_wqe_bucket, and
+ *   transport  [world] DB_XPORT_* per PE (device memory)
+ *   direct     [n] output, 32-byte aligned: room for every put of the batch
+ *   n_direct   one uint64_t output (8-byte aligned): records written
+ *   ctr        NULL or counters: total = WQEs posted, n_invalid, n_overflow
+ *              = puts of overflowing rings
+ * Workspace: db_wqe_workspace_size(n, world * n_qp) bytes, as for
+ * db_wqe_bucket. Only the static heap has this variant.
+ */
+int db_wqe_bucket_transport(const db_put_req* req, uint64_t n, const uint64_t* peer_ptrs,
+                            const uint32_t* rkeys, const uint8_t* transport, uint32_t world,
+                            uint32_t n_qp, uint64_t local_base, uint32_t lkey,
+                            uint64_t heap_size, db_wqe* rings, uint64_t depth, uint64_t* head,
+                            uint32_t* count, db_direct* direct, uint64_t* n_direct,
+                            db_counters* ctr, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- put translation on a VMM heap ------------------------------------------
  * Source: "mori communication library analysis (1)", the VMM-heap branch of

@@ -99,3 +99,17 @@ def test_argument_checks_need_no_gpu(libpath):
     # more than 1024 rings
     assert lib.db_wqe_bucket(fake, 5, fake, fake, 64, 32, 0, 0, 1 << 20, fake, 8, fake, fake,
                              None, fake, 1 << 20, None) == -22
+
+
+def test_transport_argument_checks_need_no_gpu(libpath):
+    lib = ctypes.CDLL(libpath)
+    vp, u32, u64 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64
+    lib.db_wqe_bucket_transport.argtypes = [vp, u64, vp, vp, vp, u32, u32, u64, u32, u64, vp,
+                                            u64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    fake = 1 << 20  # never dereferenced: the checks fail first
+    call = lambda direct, n_direct, transport=fake: lib.db_wqe_bucket_transport(
+        fake, 5, fake, fake, transport, 8, 4, 0, 0, 1 << 20, fake, 8, fake, fake, direct,
+        n_direct, None, fake, 1 << 20, None)
+    assert call(fake, None) == -22           # no n_direct
+    assert call(fake + 16, fake) == -22      # direct records not 32-byte aligned
+    assert call(fake, fake, transport=None) == -22
