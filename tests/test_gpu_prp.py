@@ -165,6 +165,29 @@ def test_sparse_lists(db, oracle, spacing, per_request):
     compare(oracle, got, want, cap, False)
 
 
+@pytest.mark.parametrize("per_request", [True, False])
+def test_more_tiles_than_resident_ctas(db, oracle, per_request):
+    """A batch of 700,001 requests (342 tiles of 2048, a ragged last one):
+    more tiles than CTAs run at once, so CTAs take second tiles by ticket
+    while others still write lists. One request in ten owns a list, so
+    nearly every tile takes the list path."""
+    import synth
+    rng = np.random.default_rng(4343)
+    n = 700_001
+    heap = 256 * 1024 * 1024
+    lut = synth.physical_lut(rng, heap // 65536)
+    off = 4 * rng.integers(0, (heap - (1 << 21)) // 4, size=n).astype(np.uint64)
+    length = rng.integers(1, 8193, size=n).astype(np.uint64)
+    big = rng.random(n) < 0.1
+    length[big] = rng.integers(3 * 4096, 1 << 21, size=int(big.sum())).astype(np.uint64)
+    req = np.stack([off, length], axis=1).astype(np.uint64)
+    need = oracle.prp_build(req, lut, heap, 0x7_0000_0000, 1 << 40, lists=False)
+    cap = int(need["ctr"][0])
+    want = oracle.prp_build(req, lut, heap, 0x7_0000_0000, cap, fill=FILL & (2**64 - 1))
+    got = run_gpu(db, req, lut, heap, 0x7_0000_0000, cap, per_request=per_request)
+    compare(oracle, got, want, cap, False)
+
+
 @pytest.mark.parametrize("zero_tail", [False, True])
 def test_arena_in_pinned_host_memory(db, oracle, zero_tail):
     """The lists written straight into a pinned host arena equal the oracle's."""
