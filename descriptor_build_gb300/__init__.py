@@ -39,12 +39,14 @@ __all__ = [
     "cq_mirror", "cq_attach", "cq_detach", "cq_wait_ack", "cq_host_reap", "cq_request_stop",
     "PRP_OK", "PRP_INVALID", "PRP_OVERFLOW", "MR_MISS", "MR_EXACT", "MR_CONTAINED",
     "MR_INVALID", "ERR_TIMEOUT", "ERR_RING_OVERFLOW", "ERR_TABLE_ORDER", "PRP_ZERO_TAIL",
+    "PRP_SCHED_SINGLE", "PRP_SCHED_SPLIT",
 ]
 
 PRP_OK, PRP_INVALID, PRP_OVERFLOW = 0, 1, 2
 MR_MISS, MR_EXACT, MR_CONTAINED, MR_INVALID = 0, 1, 2, 3
 ERR_TIMEOUT, ERR_RING_OVERFLOW, ERR_TABLE_ORDER = 1, 2, 4
 PRP_ZERO_TAIL = 1
+PRP_SCHED_SINGLE, PRP_SCHED_SPLIT = 2, 4
 XPORT_RDMA, XPORT_P2P, XPORT_SDMA = 0, 1, 2
 
 lib_path = _build.LIB

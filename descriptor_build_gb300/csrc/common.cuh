@@ -161,7 +161,9 @@ struct ScanHeader {
   unsigned int epoch;           // tag of the current call's status words
   unsigned int aux;             // kAuxFailed / kAuxClearPending
   unsigned long long hw_words;  // most status words any call has used
-  unsigned long long acc[5];    // per-kernel accumulators, zero between calls
+  unsigned long long acc[5];    // per-kernel accumulators, zero between calls (the PRP
+                                // build keeps in acc[4] the epoch of the last call its
+                                // pair kernel completed)
 };
 constexpr size_t kScanHeaderBytes = 256;
 constexpr unsigned int kAuxFailed = 1u;        // the first pass of a call failed

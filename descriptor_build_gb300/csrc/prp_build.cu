@@ -6,7 +6,10 @@
 // (512 entries per 4 KiB list page; 513 x 4 KiB with PRP1). Lists longer than
 // one page chain through slot 511 (NVMe convention).
 //
-// One persistent kernel, single pass over the requests:
+// Two schedules with the same results (the host picks one by batch size):
+//
+// Single kernel (large batches): one persistent kernel, one pass over the
+// requests:
 //   1. a CTA takes a tile of 2,048 requests by atomic ticket and loads four
 //      16-byte requests per thread;
 //   2. page count n and list-page count L per request, block scan of L;
@@ -21,6 +24,15 @@
 //      a whole 32-byte sector.
 // The last CTA to finish publishes the counters and readies the workspace
 // for the next call (new epoch, ticket back to 0).
+//
+// Two kernels (batches that fit one wave of the first): a light pair kernel,
+// one CTA per tile and four CTAs per SM, loads every request at once,
+// publishes each tile's list-page total, and writes the PRP pairs of the
+// tiles that own no list (when page_base is not asked for). The list kernel
+// then runs the steps above on the remaining tiles, taken by index, with the
+// tile's first list page summed from the published totals instead of a
+// lookback. A small-I/O batch so spends one wave of loads, gathers and
+// stores rather than two rounds of a latency chain per CTA.
 #include "common.cuh"
 
 namespace db {
@@ -74,6 +86,7 @@ struct Params {
   uint8_t* status;
   db_counters* ctr;
   uint32_t zero_tail;
+  uint32_t parts;  // list kernel of the two-kernel schedule: CTAs per tile (1..kWarps)
   ScanHeader* hdr;
   unsigned long long* tile_status;  // [cap_tiles]
   uint64_t cap_tiles;
@@ -272,6 +285,10 @@ __device__ __forceinline__ void emit_list(const Params& p, const ListItem& it, u
 // loaded by lanes 0..2 of the group. With zeroed tails every list fills its
 // whole page, 32 words per group step.
 constexpr uint32_t kShortWords = 32;
+// Marker a thread adds to its part of a prefix sum when one of its status
+// words is not what it should be. Real sums stay below 2^40 (list pages of at
+// most 2^28 requests); 512 markers stay below 2^60.
+constexpr uint64_t kSplitBad = 1ull << 50;
 __device__ __forceinline__ uint64_t short_window(const Params& p, const ListItem& it, bool valid,
                                                  int lane, uint64_t pol_lut) {
   return valid ? lut_window(p.lut, (it.hb >> 16) + (uint64_t)(lane & 7), last_chunk(it), pol_lut)
@@ -307,6 +324,16 @@ __device__ __forceinline__ void emit_short(const Params& p, const ListItem& it, 
       }
     }
   }
+}
+
+// Validity, pages touched (n) and list pages (L) of one request; the same
+// arithmetic in every kernel that reads requests.
+__device__ __forceinline__ void classify(const Params& p, uint64_t i, uint64_t off, uint32_t len,
+                                         bool& valid, uint32_t& npg, uint32_t& L) {
+  valid = i < p.n && len != 0 && (off & 3) == 0 && off <= p.heap_size &&
+          (uint64_t)len <= p.heap_size - off;
+  npg = valid ? (uint32_t)(((off & 4095) + len + 4095) >> 12) : 0;
+  L = npg >= 3 ? (npg - 2 + 510) / 511 : 0;  // ceil((list entries - 1) / 511)
 }
 
 // Whether any of a thread's requests owns list pages.
@@ -423,13 +450,30 @@ __device__ __forceinline__ void lookback(const Params& p, uint64_t t, uint32_t e
   excl_out = excl;
 }
 
+// kSplit: the list kernel of the two-kernel schedule (tiles by index, first
+// list pages from the pair kernel's totals); otherwise the single kernel.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(const Params p) {
   __shared__ unsigned long long s_ticket[2];  // this tile's ticket, the next one's
   __shared__ uint64_t s_scan[kItems * kWarps + 1];
   __shared__ unsigned long long s_excl;
   __shared__ int s_failed;
   __shared__ uint32_t s_next, s_next_short, s_warps_done;
+  __shared__ uint64_t s_split[kWarps];  // two-kernel schedule: list pages before the tile, by warp
   __shared__ ulonglong2 s_list[kTile];
+
+  // In the two-kernel schedule this kernel runs as a programmatic dependent
+  // of the pair kernel and reads what that kernel wrote: wait for it first.
+  // If the pair kernel completed the call (epoch E recorded in acc[4], epoch
+  // now E + 1, tile 0's word still tagged E), there is nothing to do. Every
+  // thread reads the same settled values, so the exit is uniform.
+  if (kSplit) {
+    wait_for_prerequisites();
+    const uint32_t now = *(volatile unsigned int*)&p.hdr->epoch;
+    const uint32_t done_epoch = (uint32_t)*(volatile unsigned long long*)&p.hdr->acc[4];
+    if (done_epoch + 1 == now && status_flag(ld_relaxed(p.tile_status), done_epoch) == kAggregate)
+      return;
+  }
 
   const int lane = threadIdx.x & 31;
   const uint64_t pol_first = policy_evict_first();
@@ -440,15 +484,36 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
   bool any_failed = false;
 
   if (threadIdx.x == 0) {
-    s_ticket[0] = atomicAdd(&p.hdr->ticket, 1ull);
+    if (!kSplit) s_ticket[0] = atomicAdd(&p.hdr->ticket, 1ull);
     s_warps_done = 0;
   }
   for (uint32_t round = 0;; ++round) {
     // Every thread is past the previous tile (its lists included) here, so
     // the tile's shared memory is free again.
     __syncthreads();
-    const uint64_t tile = s_ticket[round & 1];
+    // Two-kernel schedule: tiles by index (nothing waits on another tile),
+    // each split into p.parts parts taken by different CTAs (part `part`
+    // writes the requests of warps w with w % parts == part and the lists
+    // the tile queues at positions j with j % parts == part); otherwise by
+    // ticket, one part.
+    uint64_t tile;
+    uint32_t part = 0, parts = 1;
+    if (kSplit) {  // fewer than 2^32 parts in all: n < 2^28 requests, parts <= 16
+      const uint32_t vt = blockIdx.x + round * gridDim.x;
+      parts = p.parts;
+      tile = vt / parts;
+      part = vt % parts;
+    } else {
+      tile = s_ticket[round & 1];
+    }
     if (tile >= p.n_tiles) break;
+    if (kSplit) {
+      // The pair kernel published every tile's list-page total and wrote the
+      // tile in full unless it owns lists or page_base is asked for. Every
+      // thread reads the same settled word, so the skip is uniform.
+      const uint64_t w = ld_relaxed(p.tile_status + tile);
+      if (status_flag(w, epoch) == kAggregate && (w & kValueMask) == 0 && !p.page_base) continue;
+    }
 
     // 1-2. Four requests per thread (rows of the tile): validity, pages
     //      touched, list pages; one scan in request order of the list pages
@@ -471,10 +536,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
       const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
-      valid[k] = i < p.n && len[k] != 0 && (off[k] & 3) == 0 && off[k] <= p.heap_size &&
-                 (uint64_t)len[k] <= p.heap_size - off[k];
-      npg[k] = valid[k] ? (uint32_t)(((off[k] & 4095) + len[k] + 4095) >> 12) : 0;
-      L[k] = npg[k] >= 3 ? (npg[k] - 2 + 510) / 511 : 0;  // ceil((list entries - 1) / 511)
+      classify(p, i, off[k], len[k], valid[k], npg[k], L[k]);
       const bool is_short = L[k] != 0 && npg[k] - 1 <= kShortWords;  // then L = 1, words = n - 1
       v[k] = (uint64_t)L[k] | ((uint64_t)(is_short ? 1 : 0) << 23) |
              ((uint64_t)(L[k] != 0 && !is_short ? 1 : 0) << 35);
@@ -486,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     // only for this short tile, so no later tile waits on it for long) and
     // writes its PRP pairs.
     const bool lists = __syncthreads_or(any_list_rows(L)) != 0;
-    if (!lists && !p.page_base) {
+    if (!kSplit && !lists && !p.page_base) {
       unsigned long long next_ticket = 0;
       if (threadIdx.x == 0) {
         next_ticket = atomicAdd(&p.hdr->ticket, 1ull);
@@ -519,6 +581,20 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
                   ? lut_window(p.lut, ((off[k] & ~4095ull) + 4096) >> 16, ~0ull, pol_last)
                   : 0;
     }
+    // Two-kernel schedule: the tile's first list page is the sum of the
+    // totals the pair kernel published for the tiles before it (a word that
+    // is not this call's aggregate fails the tile).
+    if (kSplit) {
+      uint64_t psum = 0;
+      bool bad = false;
+      for (uint64_t u = threadIdx.x; u < tile; u += kThreads) {
+        const uint64_t w = ld_relaxed(p.tile_status + u);
+        bad |= status_flag(w, epoch) != kAggregate;
+        psum += w & kValueMask;
+      }
+      psum = warp_sum64(psum + (bad ? kSplitBad : 0));
+      if (lane == 0) s_split[threadIdx.x >> 5] = psum;  // read after the scan's barriers
+    }
     tile_excl_scan(v, ex, tile_v, s_scan);
     const uint64_t tile_L = tile_v & ((1ull << 23) - 1);
     const uint32_t n_short = (uint32_t)(tile_v >> 23) & 4095u;
@@ -530,7 +606,13 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     if (threadIdx.x < 32) {
       uint64_t excl = 0;
       bool failed = false;
-      if (tile_L != 0 || p.page_base)
+      if (kSplit) {
+        const uint64_t w = ld_relaxed(p.tile_status + tile);
+        excl = warp_sum64(lane < kWarps ? s_split[lane] : 0);
+        failed = excl >= kSplitBad || status_flag(w, epoch) != kAggregate ||
+                 (w & kValueMask) != tile_L;
+        if (failed) excl = 0;
+      } else if (tile_L != 0 || p.page_base)
         lookback(p, tile, epoch, tile_L, excl, failed);
       else if (lane == 0)
         st_relaxed(p.tile_status + tile, status_word(tile == 0 ? kPrefix : kAggregate, epoch, 0));
@@ -545,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     const bool failed = s_failed != 0;
     any_failed |= failed;
 
-    // 4. PRP1 / PRP2, page_base, status; queue the lists.
+    // 4. PRP1 / PRP2, page_base, status (this part's warps); queue the lists.
+    const bool mine = !kSplit || (uint32_t)(threadIdx.x >> 5) % parts == part;
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
       const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
@@ -560,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
         else if (npg[k] >= 3)
           prp2 = p.arena_base + (pb << 12);
       }
-      if (i < p.n) {
+      if (i < p.n && mine) {
         st_stream16(p.prp + i, prp1, prp2, pol_first);
         if (p.page_base) p.page_base[i] = pb;
         if (p.status)
@@ -575,14 +658,14 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
         s_list[q] = pack_item(off[k] & ~4095ull, (ovf || failed) ? 0 : L[k], pb, npg[k]);
       }
     }
-    my_pages += tile_L;
+    if (part == 0) my_pages += tile_L;
     __syncthreads();
 
     // 5. Lists. Long ones: a warp takes the next queued request and writes
     //    its run, with the LUT window of the request after it already in
     //    flight. Then short ones, four per warp.
     uint32_t j = 0;
-    if (lane == 0) j = atomicAdd(&s_next, 1u);
+    if (lane == 0) j = kSplit ? part + parts * atomicAdd(&s_next, 1u) : atomicAdd(&s_next, 1u);
     j = __shfl_sync(kFull, j, 0);
     ListItem it{};
     uint64_t win0 = 0, win1 = 0;
@@ -595,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     }
     while (j < n_long) {
       uint32_t jn = 0;
-      if (lane == 0) jn = atomicAdd(&s_next, 1u);
+      if (lane == 0) jn = kSplit ? part + parts * atomicAdd(&s_next, 1u) : atomicAdd(&s_next, 1u);
       jn = __shfl_sync(kFull, jn, 0);
       ListItem nx{};
       uint64_t nwin0 = 0, nwin1 = 0;
@@ -614,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     }
     // Short lists, four per warp step, the next four already loading.
     uint32_t q0 = 0;
-    if (lane == 0) q0 = atomicAdd(&s_next_short, 4u);
+    if (lane == 0)
+      q0 = kSplit ? 4u * (part + parts * atomicAdd(&s_next_short, 1u)) : atomicAdd(&s_next_short, 4u);
     q0 = __shfl_sync(kFull, q0, 0);
     ListItem sh{};
     bool sv = false;
@@ -627,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     }
     while (q0 < n_short) {
       uint32_t q1 = 0;
-      if (lane == 0) q1 = atomicAdd(&s_next_short, 4u);
+      if (lane == 0)
+        q1 = kSplit ? 4u * (part + parts * atomicAdd(&s_next_short, 1u))
+                    : atomicAdd(&s_next_short, 4u);
       q1 = __shfl_sync(kFull, q1, 0);
       ListItem nsh{};
       bool nsv = false;
@@ -646,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
     }
     // The last warp to finish the tile's lists takes the next ticket, so no
     // ticket is held while lists of this tile are still being written.
-    if (lane == 0 && atomicAdd(&s_warps_done, 1u) == kWarps - 1) {
+    if (!kSplit && lane == 0 && atomicAdd(&s_warps_done, 1u) == kWarps - 1) {
       s_warps_done = 0;
       s_ticket[(round + 1) & 1] = atomicAdd(&p.hdr->ticket, 1ull);
     }
@@ -686,6 +772,114 @@ __global__ void __launch_bounds__(kThreads, DB_PRP_MIN_CTAS) prp_build_kernel(co
   }
 }
 
+// Pair kernel of the two-kernel schedule (batches that fit one wave of it):
+// one CTA per tile, by index, with nothing to wait for; light enough for four
+// CTAs of 512 threads per SM, so a batch of up to 4 x 2048 x SMs requests has
+// all its requests in flight at once. A warp none of whose requests owns a
+// list writes their PRP pairs and statuses at once (when page_base is not
+// asked for). Each tile's list-page total is published; a tile with lists,
+// or every tile when page_base is asked for, is left to the list kernel,
+// which writes the whole tile again (the same values for these warps). The
+// last CTA to finish completes the call itself when no tile was left over:
+// it publishes the counters, records the call's epoch in acc[4] and
+// advances the epoch, and the list kernel, finding that record, exits.
+// (At an epoch wrap it leaves the call to the list kernel, which clears the
+// status words.)
+constexpr int kPairCtasPerSm = 4;
+__global__ void __launch_bounds__(kThreads, kPairCtasPerSm) prp_pairs_kernel(const Params p) {
+  __shared__ uint32_t s_part[kWarps], s_inv[kWarps];
+  dependents_may_launch();  // the list kernel may take SMs as these CTAs finish
+  const uint64_t tile = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const uint64_t pol_first = policy_evict_first();
+  const uint64_t pol_last = policy_evict_last();
+  uint64_t off[kItems];
+  uint32_t len[kItems];
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+    off[k] = 0;
+    len[k] = 0;
+    if (i < p.n) {
+      const ulonglong2 r = ld_stream16(p.req + i, pol_first);
+      off[k] = r.x;
+      len[k] = (uint32_t)r.y;
+    }
+  }
+  uint32_t my_L = 0, two = 0, ok = 0, my_invalid = 0;  // bit k: request k has two pages / is valid
+#pragma unroll
+  for (int k = 0; k < kItems; ++k) {
+    const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+    bool valid;
+    uint32_t npg, L;
+    classify(p, i, off[k], len[k], valid, npg, L);
+    my_L += L;  // at most 4 x 2053
+    ok |= (valid ? 1u : 0u) << k;
+    two |= (npg == 2 ? 1u : 0u) << k;
+    my_invalid += (i < p.n && !valid) ? 1u : 0u;
+  }
+  if (!p.page_base && !__any_sync(kFull, my_L != 0)) {
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const uint64_t i = tile * kTile + (uint64_t)k * kThreads + threadIdx.x;
+      const bool valid = (ok >> k) & 1u;
+      uint64_t prp1 = 0, prp2 = 0;
+      if (valid) {
+        prp1 = bus(p.lut, off[k], pol_last);
+        if ((two >> k) & 1u) prp2 = bus(p.lut, (off[k] & ~4095ull) + 4096, pol_last);
+      }
+      if (i < p.n) {
+        st_stream16(p.prp + i, prp1, prp2, pol_first);
+        if (p.status) p.status[i] = valid ? DB_PRP_OK : DB_PRP_INVALID;
+      }
+    }
+  }
+  my_L = warp_sum32(my_L);  // at most 2^23 per tile
+  my_invalid = warp_sum32(my_invalid);
+  if (lane == 0) {
+    s_part[threadIdx.x >> 5] = my_L;
+    s_inv[threadIdx.x >> 5] = my_invalid;
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  uint64_t agg = 0, inv = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    agg += s_part[w];
+    inv += s_inv[w];
+  }
+  const uint32_t epoch = *(volatile unsigned int*)&p.hdr->epoch;
+  st_relaxed(p.tile_status + tile, status_word(kAggregate, epoch, agg));
+  if (agg != 0 || p.page_base)
+    atomicAdd(&p.hdr->acc[3], 1ull);  // left to the list kernel
+  else if (inv)
+    atomicAdd(&p.hdr->acc[0], inv);
+  __threadfence();
+  if (atomicAdd(&p.hdr->done, 1u) != gridDim.x - 1) return;
+  // Last CTA: every other CTA's counts and words are in place.
+  __threadfence();
+  ScanHeader* h = p.hdr;
+  const unsigned long long left = atomicExch(&h->acc[3], 0ull);
+  const unsigned long long n_inv = atomicExch(&h->acc[0], 0ull);  // in the same round trip
+  if (left != 0 || ((epoch + 1) & kEpochMask) == 0) {
+    if (n_inv) atomicAdd(&h->acc[0], n_inv);  // the list kernel publishes it
+    h->done = 0;                              // and counts its own CTAs
+    return;
+  }
+  if (p.ctr) {
+    p.ctr->total = 0;
+    p.ctr->n_invalid = n_inv;
+    p.ctr->n_overflow = 0;
+    p.ctr->err = 0;
+  }
+  h->acc[4] = epoch;  // this call is complete
+  if (h->hw_words < p.n_tiles) h->hw_words = p.n_tiles;
+  h->epoch = epoch + 1;
+  h->ticket = 0;
+  h->done = 0;
+}
+
+template <bool kSplit>
 int grid_for(uint64_t n_tiles) {
   static int per_sm[64] = {0};
   int dev = 0;
@@ -693,7 +887,7 @@ int grid_for(uint64_t n_tiles) {
   int& occ = per_sm[dev & 63];
   if (occ == 0) {
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prp_build_kernel, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prp_build_kernel<kSplit>, kThreads, 0) !=
             cudaSuccess ||
         o < 1)
       o = 1;
@@ -701,6 +895,24 @@ int grid_for(uint64_t n_tiles) {
   }
   const uint64_t g = (uint64_t)num_sms() * (uint64_t)occ;
   return (int)(n_tiles < g ? n_tiles : g);
+}
+
+// Tiles one wave of the pair kernel holds on this device: batches of at most
+// this many tiles take the two-kernel schedule.
+uint64_t pair_wave_tiles() {
+  static int per_sm[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& occ = per_sm[dev & 63];
+  if (occ == 0) {
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prp_pairs_kernel, kThreads, 0) !=
+            cudaSuccess ||
+        o < 1)
+      o = 1;
+    occ = o;
+  }
+  return (uint64_t)num_sms() * (uint64_t)occ;
 }
 
 }  // namespace prp
@@ -726,7 +938,8 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
   if (arena_base % 4096 != 0) return -EINVAL;
   if (arena_cap_pages > ((~0ull - arena_base) >> 12)) return -EINVAL;  // bus addresses must not wrap
   if (arena_cap_pages > (1ull << 40)) return -EINVAL;
-  if (flags & ~DB_PRP_ZERO_TAIL) return -EINVAL;
+  if (flags & ~(DB_PRP_ZERO_TAIL | DB_PRP_SCHED_SINGLE | DB_PRP_SCHED_SPLIT)) return -EINVAL;
+  if ((flags & DB_PRP_SCHED_SINGLE) && (flags & DB_PRP_SCHED_SPLIT)) return -EINVAL;
   if (ctr && !aligned(ctr, 8)) return -EINVAL;
   if (n == 0) {
     if (ctr) cudaMemsetAsync(ctr, 0, sizeof(db_counters), s);
@@ -757,8 +970,26 @@ extern "C" int db_prp_build(const db_prp_req* req, uint64_t n, const uint64_t* l
   p.hdr = reinterpret_cast<ScanHeader*>(ws);
   p.tile_status = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + kScanHeaderBytes);
   p.cap_tiles = (ws_bytes - kScanHeaderBytes) / 8;
-  prp::prp_build_kernel<<<prp::grid_for(p.n_tiles), prp::kThreads, 0, s>>>(p);
-  return launch_result();
+  p.parts = 1;
+  bool split = p.n_tiles <= prp::pair_wave_tiles();
+  if (flags & DB_PRP_SCHED_SINGLE) split = false;
+  if (flags & DB_PRP_SCHED_SPLIT) split = true;
+  if (!split) {
+    prp::prp_build_kernel<false>
+        <<<prp::grid_for<false>(p.n_tiles), prp::kThreads, 0, s>>>(p);
+    return launch_result();
+  }
+  // List kernel: with few tiles, several CTAs share each tile's lists.
+  const uint64_t resident = (uint64_t)prp::grid_for<true>(~0ull);
+  uint64_t parts = resident / p.n_tiles;
+  parts = parts < 1 ? 1 : (parts > (uint64_t)prp::kWarps ? (uint64_t)prp::kWarps : parts);
+  p.parts = (uint32_t)parts;
+  prp::prp_pairs_kernel<<<(unsigned)p.n_tiles, prp::kThreads, 0, s>>>(p);
+  const int rc = launch_result();
+  if (rc) return rc;
+  return launch_dependent(prp::prp_build_kernel<true>,
+                          (unsigned)prp::grid_for<true>(p.n_tiles * parts), prp::kThreads, 0, s,
+                          p);
 }
 
 // ---------------------------------------------------------------------------

@@ -125,6 +125,10 @@ typedef struct db_counters {
 #define DB_ERR_TABLE_ORDER 4u   /* the MR table is not sorted and non-overlapping            */
 
 #define DB_PRP_ZERO_TAIL 1u     /* db_prp_build: zero the unused slots of each last list page */
+/* db_prp_build schedule (results are the same either way; by default a batch
+ * that one wave of the pair kernel holds takes two kernels, a larger one one): */
+#define DB_PRP_SCHED_SINGLE 2u  /* one persistent kernel, tiles by ticket, decoupled lookback */
+#define DB_PRP_SCHED_SPLIT 4u   /* a pair kernel, then a list kernel for the tiles with lists */
 
 #define DB_XPORT_RDMA 0 /* db_wqe_bucket_transport: how each PE is reached */
 #define DB_XPORT_P2P 1
@@ -174,7 +178,15 @@ typedef struct db_counters {
  *   ctr              output counters or NULL: total list pages (including
  *                    those of requests that did not fit), n_invalid,
  *                    n_overflow, err
- *   flags            0 or DB_PRP_ZERO_TAIL
+ *   flags            DB_PRP_ZERO_TAIL, and at most one of DB_PRP_SCHED_SINGLE /
+ *                    DB_PRP_SCHED_SPLIT (the schedule; the outputs do not depend
+ *                    on it). By default a batch of at most one wave of the pair
+ *                    kernel's tiles (4 CTAs x 2048 requests per SM) takes the
+ *                    two-kernel schedule: all its requests are loaded at once,
+ *                    and only tiles that own lists (or all, when page_base is
+ *                    asked for) go through the list kernel. Larger batches take
+ *                    the single persistent kernel, which overlaps the scan of
+ *                    later tiles with the lists of earlier ones.
  * A request that is invalid or whose list does not fit gets prp = {0, 0}
  * and writes no list; one that does not fit still advances page_base.
  * Limits: n <= 2^28, arena_cap_pages <= 2^40.
