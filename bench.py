@@ -70,6 +70,9 @@ def parse():
                     help="profiling aid: run one workload only (not a bench line)")
     ap.add_argument("--fraction", type=float, default=1.0,
                     help="profiling aid: keep this leading fraction of each batch")
+    ap.add_argument("--prp-sched", choices=["auto", "single", "split"], default="auto",
+                    help="profiling aid: force a PRP schedule (a leading fraction of the large "
+                         "batch would otherwise take the small-batch one)")
     ap.add_argument("--serial", action="store_true",
                     help="run a step's four calls one after another on one stream "
                          "(default: each on its own stream, all at once)")
@@ -178,18 +181,37 @@ def source_sha256(kernel_src: str) -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(kernel_src: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernel sources as they are now (else None)."""
+def recorded_traffic(workload: str):
+    """The committed ncu figures of one call (DRAM bytes per call, L2 sectors
+    and requests per request), if they were taken on the kernel sources as
+    they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)[kernel]
-        if source_sha256(kernel_src) != rec["source_sha256"]:
+            rec = json.load(f)[workload]
+        if source_sha256(rec["source"]) != rec["source_sha256"]:
             return None
-        return int(rec["dram_bytes_per_launch"])
+        return rec
     except Exception:
         return None
+
+
+def host_cpu() -> dict:
+    """Host cores and CPU model (lscpu), recorded beside the CPU baseline."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                if not model.isdigit():
+                    break
+    except Exception:
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu_model": model}
 
 
 # -------------------------------------------------------------- clock sampler
@@ -258,8 +280,23 @@ class Step:
 
     LAUNCHES = {"prp_small": 1, "prp_large": 1, "mr_lookup": 2, "put_bucket": 3}
 
-    def __init__(self, db, torch, inp, device):
-        self.db, self.torch, self.inp = db, torch, inp
+    def launches(self, name: str) -> int:
+        """Kernels one call launches. A PRP batch of at most one wave of the
+        pair kernel (4 CTAs of 2,048 requests per SM) takes the two-kernel
+        schedule unless a schedule is forced."""
+        if name.startswith("prp"):
+            n = self.inp[name]["req"].shape[0]
+            sms = self.torch.cuda.get_device_properties(self.device).multi_processor_count
+            split = -(-n // 2048) <= 4 * sms
+            if self.prp_flags:
+                split = self.prp_flags == self.db.PRP_SCHED_SPLIT
+            return 2 if split else 1
+        return self.LAUNCHES[name]
+
+    def __init__(self, db, torch, inp, device, prp_sched="auto"):
+        self.db, self.torch, self.inp, self.device = db, torch, inp, device
+        self.prp_flags = {"auto": 0, "single": db.PRP_SCHED_SINGLE,
+                          "split": db.PRP_SCHED_SPLIT}[prp_sched]
         t = torch
         d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
         d32 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
@@ -303,7 +340,7 @@ class Step:
 
     def prp(self, a, stream):
         self.db.prp_build(a["req"], a["lut"], a["heap"], a["base"], a["cap"], a["arena"],
-                          a["prp"], a["ws"], ctr=a["ctr"], stream=stream)
+                          a["prp"], a["ws"], ctr=a["ctr"], flags=self.prp_flags, stream=stream)
 
     def mr_call(self, stream):
         m = self.bufs["mr_lookup"]
@@ -718,7 +755,7 @@ def run_ours(args, inp, world, device, dist):
     import descriptor_build_gb300 as db
 
     torch.cuda.set_device(device)
-    st = Step(db, torch, inp, device)
+    st = Step(db, torch, inp, device, args.prp_sched)
     stream = torch.cuda.Stream(device=device)
     ev = lambda: torch.cuda.Event(enable_timing=True)
     # The four calls are independent batches with their own buffers and
@@ -805,42 +842,118 @@ def run_ours(args, inp, world, device, dist):
                          "frac_of_peak": round(gbs / peak, 4),
                          "output_bytes": outb[name],
                          "output_GB_per_s": round(outb[name] / (ms * 1e-3) / 1e9, 1),
-                         "launches": Step.LAUNCHES[name],
+                         "launches": st.launches(name),
                          "size_matched_copy_ms": round(copy_ms[name], 4),
                          "frac_of_size_matched_copy": round(copy_ms[name] / ms, 4)}
         if not args.serial:
             kernels[name]["concurrent_span_ms"] = round(span_ms[name], 4)
+    for name in kernels:
+        rec = recorded_traffic(name) if args.fraction >= 1.0 else None
+        kernels[name]["traffic"] = rec["dram_bytes_per_call"] if rec else None
+        kernels[name]["traffic_over_algorithmic"] = rec["traffic_over_algorithmic"] if rec else None
+        kernels[name]["l2_sectors_per_request"] = rec["l2_sectors_per_request"] if rec else None
+        kernels[name]["l2_requests_per_request"] = rec["l2_requests_per_request"] if rec else None
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
-    traffic = recorded_traffic("prp_build.cu", "prp_build_kernel") if dom.startswith("prp") \
-        else None
-    roof = {"bound": "hbm", "kernel": "prp_build_kernel" if dom.startswith("prp") else dom,
+    names = {"prp_small": "prp_pairs_kernel + prp_build_kernel<true>",
+             "prp_large": "prp_build_kernel<false>",
+             "mr_lookup": "mr_index_kernel + mr_lookup_kernel",
+             "put_bucket": "wqe_count_kernel + wqe_scan_kernel + wqe_scatter_kernel"}
+    roof = {"bound": "hbm", "kernel": names.get(dom, dom),
             "workload": dom, "achieved": kernels[dom]["GB_per_s"], "peak": peak,
             "peak_source": peak_kind, "unit": "GB/s",
-            "frac": round(kernels[dom]["GB_per_s"] / peak, 4), "traffic": traffic,
-            "algorithmic_bytes_per_launch": alg[dom]}
+            "frac": round(kernels[dom]["GB_per_s"] / peak, 4), "traffic": kernels[dom]["traffic"],
+            "algorithmic_bytes_per_launch": alg[dom],
+            # every call of the step, timed alone (the same figures as `kernels`)
+            "calls": {n: {"ms": k["ms"], "GB_per_s": k["GB_per_s"], "frac": k["frac_of_peak"],
+                          "frac_of_size_matched_copy": k["frac_of_size_matched_copy"],
+                          "traffic": k["traffic"],
+                          "traffic_over_algorithmic": k["traffic_over_algorithmic"],
+                          "l2_sectors_per_request": k["l2_sectors_per_request"]}
+                      for n, k in kernels.items()}}
+    if not args.only and args.fraction >= 1.0:
+        c1 = time_tiny(args, device)
+        kernels["c1_tiny"] = c1
+        roof["calls"]["c1_tiny"] = {"prp_us": c1["prp_us"], "mr_lookup_us": c1["mr_lookup_us"]}
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
            "data": "synthetic (seeded generators of the five study workloads)",
-           "config": {"workload": WORKLOAD, "requests_per_step": reqs_per_step,
-                      "per_workload_requests": u,
-                      "l2": "inputs larger than L2: each step streams ~6 GB, so every "
-                            "kernel's inputs are evicted before its next launch",
-                      "parallelism": f"replicas x{world}",
-                      "schedule": ("one stream, the four calls in turn" if args.serial else
-                                   "four streams, forked and joined each step; launch order "
-                                   + ", ".join(n for n, _ in calls)
-                                   + "; per-call times and the roofline from the same steps "
-                                     "run one call at a time after the timed region")},
+           "config": workload_config(u, world, args.serial),
            "output_GB_per_s": round(world * sum(outb.values()) / (ms_per_step * 1e-3) / 1e9, 1),
            "kernels": kernels, "roofline": roof,
-           "gpu_launches": K * sum(Step.LAUNCHES[k] for k in u),  # in the timed region
+           "gpu_launches": K * sum(st.launches(k) for k in u),  # in the timed region
            "clocks": clk.summary()}
     if not args.no_e2e:
         out["e2e"] = run_e2e(st, stream, inp, max(3, min(K, 5)), device, dist, world,
                              serial=args.serial)
     return out
+
+
+def workload_config(u: dict, world: int, serial: bool) -> dict:
+    """The `config` of a bench line; both arms print the same one."""
+    order = [n for n in SCHEDULE if n in u]
+    return {"workload": WORKLOAD, "requests_per_step": sum(u.values()),
+            "per_workload_requests": u,
+            "l2": "inputs larger than L2: each step streams ~6 GB, so every "
+                  "kernel's inputs are evicted before its next launch",
+            "parallelism": f"replicas x{world}",
+            "schedule": ("one stream, the four calls in turn" if serial else
+                         "four streams, forked and joined each step; launch order "
+                         + ", ".join(order)
+                         + "; per-call times and the roofline from the same steps "
+                           "run one call at a time after the timed region")}
+
+
+def time_tiny(args, device) -> dict:
+    """Latency of the tiny workload (4,096 requests): the PRP build and the
+    lookup of the same ranges against its 64-record table, each call timed
+    alone with CUDA events after an L2 flush, mean of 50 calls."""
+    import torch as t
+    import descriptor_build_gb300 as db
+    import synth
+    w = synth.prp_tiny()
+    n = w["req"].shape[0]
+    d64 = lambda a: t.from_numpy(np.ascontiguousarray(a).view(np.int64)).to(device)
+    req, lut = d64(w["req"]), d64(w["lut"])
+    prp = t.empty((n, 2), dtype=t.int64, device=device)
+    ctr = t.zeros(4, dtype=t.int64, device=device)
+    ws = db.workspace(db.prp_workspace_size(n), device)
+    stream = t.cuda.Stream(device=device)
+    db.prp_build(req, lut, w["heap_size"], w["arena_base"], 0, None, prp, ws, ctr=ctr,
+                 stream=stream)
+    stream.synchronize()
+    cap = int(ctr[0].item())
+    arena = t.empty((max(cap, 1), 512), dtype=t.int64, device=device)
+    q, ms_, me = d64(w["queries"]), d64(w["mr_start"]), d64(w["mr_end"])
+    mk = t.from_numpy(w["mr_lkey"].view(np.int32)).to(device)
+    idx = t.empty(n, dtype=t.int32, device=device)
+    lk = t.empty(n, dtype=t.int32, device=device)
+    kind = t.empty(n, dtype=t.uint8, device=device)
+    mws = db.workspace(db.mr_workspace_size(w["mr_start"].shape[0]), device)
+    flush = t.empty(256 << 20, dtype=t.uint8, device=device)
+    calls = {"prp_us": lambda: db.prp_build(req, lut, w["heap_size"], w["arena_base"], cap, arena,
+                                            prp, ws, ctr=ctr, stream=stream),
+             "mr_lookup_us": lambda: db.mr_lookup(q, ms_, me, mk, idx, lk, kind, mws,
+                                                  stream=stream)}
+    res = {}
+    for name, fn in calls.items():
+        evs = []
+        with t.cuda.stream(stream):
+            for r in range(55):
+                flush.fill_(r & 0xFF)
+                a, b = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                if r >= 5:
+                    evs.append((a, b))
+        stream.synchronize()
+        res[name] = round(1000 * statistics.mean(a.elapsed_time(b) for a, b in evs), 2)
+    assert int(ctr[3].item()) == 0 and int(ctr[0].item()) == cap
+    return {"requests": n, "mr_records": int(w["mr_start"].shape[0]), **res,
+            "note": "latency of one call, inputs resident; CUDA event intervals come in steps "
+                    "of about 2 us here, so these are means of 50 calls"}
 
 
 def size_matched_copy_ms(torch, names, alg, K, stream, device) -> dict:
@@ -1027,7 +1140,7 @@ def cpu_baseline(inp, repeats: int = 3) -> dict:
     # Time for one full step's requests at the sampled per-request rates.
     step_s = sum(secs[k] * u[k] / samples[k] for k in u)
     return {"value": round(sum(u.values()) / step_s / 1e6, 3), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
+            **host_cpu(), "kind": "oracle",
             "sample": "all %d prp_small, the first %d prp_large (lists written), all %d "
                       "mr_lookup (binary-search oracle) and all %d put_bucket requests, each "
                       "timed %d times (median); per-workload rates scaled to one full step"
@@ -1057,7 +1170,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
             "data": "synthetic (seeded generators of the five study workloads)",
-            "config": {"workload": WORKLOAD, "requests_per_step": reqs},
+            "config": workload_config(units(inp), int(os.environ.get("WORLD_SIZE", "1")), False),
             "cpu_baseline": cb, "wall_s": round(wall, 2),
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
