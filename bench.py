@@ -593,7 +593,10 @@ def time_cq_mirror(args, device) -> dict:
     issuing the completion's two copies into the device CQ until its host CQ
     shows the new phase tag, median over 2,000 completions; beside it the
     same round trip with a copy engine (a 16-byte device-to-host copy queued
-    after the write) doing the mirror's job.
+    after the write) doing the mirror's job. The queue is timed
+    (DB_CQ_TIMED), so the slot also gives each completion's latency on the
+    device: from the warp reading its new phase tag to its host-CQ writes
+    being performed at system scope.
     Every copied entry is checked against what was written."""
     import torch as t
     import descriptor_build_gb300 as db
@@ -655,9 +658,11 @@ def time_cq_mirror(args, device) -> dict:
         h.zero_()
         h2.zero_()
         copy_s.synchronize()
+        f["flags"][0] = db.CQ_TIMED  # the kernel records each batch's latency in the slot
         db.cq_attach(slots, 0, d, h)
         ov, nv = one_old.numpy().view(np.uint32), one_new.numpy().view(np.uint32)
         rts = {"mirror": [], "copy_engine": []}
+        dev_lat = []
         for i in range(4000):
             leg = "mirror" if i % 2 == 0 else "copy_engine"
             j = i // 2
@@ -685,6 +690,13 @@ def time_cq_mirror(args, device) -> dict:
                 raise RuntimeError(f"cq_mirror: QD1 entry differs ({leg})")
             total += leg == "mirror"
             rts[leg].append(tc - ta)
+            if leg == "mirror":
+                tl = time.perf_counter()
+                while int(f["lat_seq"][0]) != j + 1 and time.perf_counter() - tl < 1.0:
+                    pass
+                if int(f["lat_seq"][0]) != j + 1:
+                    raise RuntimeError("cq_mirror: no latency record")
+                dev_lat.append(int(f["lat_ns"][0]))
         g = db.cq_detach(slots, 0)
         db.cq_wait_ack(slots, 0, g, 5.0)
     finally:
@@ -700,6 +712,11 @@ def time_cq_mirror(args, device) -> dict:
             "qd1_roundtrip_us_median": round(statistics.median(rts["mirror"]) * 1e6, 2),
             "qd1_roundtrip_us_copy_engine_median":
                 round(statistics.median(rts["copy_engine"]) * 1e6, 2),
+            "qd1_device_latency_us_median": round(statistics.median(dev_lat) / 1e3, 3),
+            "qd1_device_latency_us_p99": round(float(np.percentile(dev_lat, 99)) / 1e3, 3),
+            "device_latency": "per completion at queue depth 1, %globaltimer on the GPU: the "
+                              "warp reads the new phase tag -> its host-CQ writes performed at "
+                              "system scope (slot lat_ns, DB_CQ_TIMED)",
             "launches": 1, "bound": "latency: device CQ to host CQ over the CPU-GPU link",
             "note": "not part of the step: the host writes the device CQs (two stream-ordered "
                     "copies per batch) and polls host memory; times are host wall clock, "

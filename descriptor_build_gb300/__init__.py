@@ -32,7 +32,8 @@ __all__ = [
     "mr_workspace_size", "mr_lookup", "mr_lookup_overlap", "wqe_workspace_size",
     "wqe_vmm_workspace_size", "wqe_bucket", "wqe_bucket_vmm", "wqe_bucket_transport",
     "XPORT_RDMA", "XPORT_P2P", "XPORT_SDMA",
-    "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "cq_slots", "cq_slot_fields",
+    "strerror", "CQ_SLOT_DTYPE", "CQ_MAX_SLOTS", "CQ_MAX_DEPTH", "CQ_TIMED", "cq_slots",
+    "cq_slot_fields",
     "mr_capacity_for", "mr_register_workspace_size", "mr_register",
     "mr_deregister_workspace_size", "mr_deregister", "MR_NEW", "MR_NEW_DUP", "DEREG_OK",
     "DEREG_RELEASED", "DEREG_STALE",
@@ -335,11 +336,12 @@ def wqe_bucket_vmm(req: torch.Tensor, chunk_raddr: torch.Tensor, chunk_rkey: tor
 
 # ------------------------------------------------------------------ CQ mirror
 CQ_MAX_SLOTS, CQ_MAX_DEPTH = 64, 65536
+CQ_TIMED = 1  # slot flag: record each batch's latency in lat_ns / lat_seq
 # db_cq_slot, 64 bytes
 CQ_SLOT_DTYPE = np.dtype([("dev_cq", "<u8"), ("host_cq", "<u8"), ("depth", "<u4"),
                           ("generation", "<u4"), ("ack", "<u4"), ("seen", "<u4"),
                           ("head", "<u4"), ("phase", "<u4"), ("copied", "<u8"),
-                          ("rsvd", "<u8", (2,))])
+                          ("flags", "<u4"), ("lat_ns", "<u4"), ("lat_seq", "<u8")])
 assert CQ_SLOT_DTYPE.itemsize == 64
 
 

@@ -88,12 +88,14 @@ struct Queue {
   uint32_t* host;
   uint32_t depth;
   bool ok;
+  bool timed;
 };
 
 __device__ __forceinline__ Queue read_queue(db_cq_slot* s) {
   Queue q;
   const uint64_t d = ld_volatile64(&s->dev_cq), h = ld_volatile64(&s->host_cq);
   q.depth = ld_volatile32(&s->depth);
+  q.timed = (ld_volatile32(&s->flags) & DB_CQ_TIMED) != 0;
   q.ok = d && h && !(d & 15) && !(h & 15) && q.depth >= 2 && q.depth <= DB_CQ_MAX_DEPTH;
   q.dev = reinterpret_cast<const uint32_t*>(d);
   q.host = reinterpret_cast<uint32_t*>(h);
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(32) cq_mirror_kernel(const Params p) {
 
   uint32_t cur = 0;          // the generation last taken up (0: none yet)
   bool active = false;       // cur is odd and its queue is being served
-  Queue q{nullptr, nullptr, 0, false};
+  Queue q{nullptr, nullptr, 0, false, false};
   uint32_t head = 0, phase = 1;
   uint64_t copied_gen = 0, copied_launch = 0;
   uint32_t last_ack = lane == 0 ? ld_volatile32(&s->ack) : 0;
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(32) cq_mirror_kernel(const Params p) {
           q.host = reinterpret_cast<uint32_t*>(
               __shfl_sync(kFull, reinterpret_cast<uintptr_t>(q.host), 0));
           q.depth = __shfl_sync(kFull, q.depth, 0);
+          q.timed = __shfl_sync(kFull, q.timed ? 1 : 0, 0) != 0;
           head = __shfl_sync(kFull, h, 0);
           phase = __shfl_sync(kFull, ph, 0);
           copied_gen = __shfl_sync(kFull, c, 0);
@@ -206,12 +209,14 @@ __global__ void __launch_bounds__(32) cq_mirror_kernel(const Params p) {
       continue;
     }
     idle_ns = 32;
+    const uint64_t t_seen = q.timed ? globaltimer_ns() : 0;  // the batch's tags are in
     __threadfence();  // the tags seen above before the bodies read below
     if (lane < run) {
       const uint4 e = ld_volatile128(q.dev + 4ull * pos);
       uint32_t* dst = q.host + 4ull * pos;
       st_body(dst, e.x, e.y, e.z);
       st_release_sys(dst + 3, e.w);
+      if (q.timed) asm volatile("fence.sc.sys;" ::: "memory");  // this lane's writes performed
     }
     // 3. advance and publish
     head += run;
@@ -223,6 +228,12 @@ __global__ void __launch_bounds__(32) cq_mirror_kernel(const Params p) {
     copied_launch += run;
     __syncwarp();
     if (lane == 0) {
+      if (q.timed) {
+        const uint64_t dt = globaltimer_ns() - t_seen;
+        st_volatile32(&s->lat_ns, dt < 0xFFFFFFFFull ? (uint32_t)dt : 0xFFFFFFFFu);
+        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(&s->lat_seq), "l"(copied_gen)
+                     : "memory");
+      }
       st_volatile32(&s->head, head);
       st_volatile32(&s->phase, phase);
       st_volatile64(&s->copied, copied_gen);

@@ -77,8 +77,21 @@ typedef struct db_cq_slot {
   uint32_t head;       /* next entry to copy */
   uint32_t phase;      /* phase tag expected at head */
   uint64_t copied;     /* completions copied under `seen` */
-  uint64_t rsvd[2];
+  /* Written by the host before db_cq_attach, read when the kernel takes the
+   * generation up. */
+  uint32_t flags;      /* 0, or DB_CQ_TIMED */
+  /* Written by the kernel, for a slot attached with DB_CQ_TIMED. */
+  uint32_t lat_ns;     /* the last batch: new tags seen -> its entries visible at system scope */
+  uint64_t lat_seq;    /* `copied` after that batch (written after lat_ns, release order) */
 } db_cq_slot;          /* 64 bytes */
+
+/* A timed slot: after each batch the warp waits for its host-CQ writes to
+ * be performed at system scope (a fence.sc.sys per lane) and records the
+ * time from reading the batch's new phase tags in the device CQ to that
+ * point (%globaltimer, ns) in lat_ns, then the batch's `copied` value in
+ * lat_seq. The wait costs the warp that time per batch, so only queues
+ * being measured should be timed. */
+#define DB_CQ_TIMED 1u
 
 /* Launch the mirror for slots[0 .. n_slots) on `stream`: warp i serves
  * slot i. The launch returns at once (the kernel stays resident).

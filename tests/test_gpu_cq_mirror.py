@@ -146,6 +146,47 @@ def test_one_queue_against_the_oracle(db, oracle, depth):
     assert ctr.tolist() == [c.produced, 0, 0, 0]
 
 
+def test_timed_slot_records_latency(db, oracle):
+    """A slot attached with DB_CQ_TIMED: the copies are the oracle's, and
+    after each batch the slot holds that batch's latency (lat_seq equal to
+    the completions copied so far, lat_ns between 0 and 10 ms). An untimed
+    slot served by the same launch leaves both fields as they were."""
+    m = Mirror(db, 2, limit_s=20.0)
+    cs = torch.cuda.Stream()
+    timed, plain = Controller(64, 71, cs), Controller(64, 72, cs)
+    o_host = np.zeros((64, 4), dtype=np.uint32)
+    o_head, o_phase = 0, 1
+    f = m.fields
+    f["flags"][0] = db.CQ_TIMED
+    m.launch()
+    try:
+        db.cq_attach(m.slots, 0, timed.dev, timed.host)
+        db.cq_attach(m.slots, 1, plain.dev, plain.host)
+        lat = []
+        for _ in range(30):
+            k = int(timed.rng.integers(1, 40))
+            timed.produce(k)
+            plain.produce(k)
+            assert timed.reap_until(db, timed.produced) == timed.produced
+            assert plain.reap_until(db, plain.produced) == plain.produced
+            n, o_head, o_phase = oracle.cq_mirror_pass(timed.replica, o_head, o_phase, o_host)
+            assert n == k
+            assert (timed.host.numpy().view(np.uint32) == o_host).all()
+            t0 = time.monotonic()  # the latency fields follow the host CQ writes
+            while int(m.fields[0]["lat_seq"]) != timed.produced and time.monotonic() - t0 < 5.0:
+                time.sleep(10e-6)
+            g = m.fields[0]
+            assert int(g["lat_seq"]) == timed.produced
+            assert 0 < int(g["lat_ns"]) < 10_000_000
+            lat.append(int(g["lat_ns"]))
+        assert int(m.fields[1]["lat_seq"]) == 0 and int(m.fields[1]["lat_ns"]) == 0
+        gens = [db.cq_detach(m.slots, i) for i in range(2)]
+        assert all(db.cq_wait_ack(m.slots, i, g, 5.0) for i, g in enumerate(gens))
+    finally:
+        ctr = m.finish()
+    assert int(ctr[0]) == timed.produced + plain.produced and int(ctr[3]) == 0
+
+
 def test_sixty_four_queues(db, oracle):
     """64 queues of different depths, batches on random subsets of them."""
     m = Mirror(db, 64, limit_s=30.0)
