@@ -72,9 +72,10 @@ def _load():
             lib.oracle_mr_register.restype = None
             lib.oracle_mr_register.argtypes = [vp, u64, vp, u32, vp, vp, vp, vp, u64, vp, vp, vp,
                                                vp, u64, vp, vp, vp, vp]
-            lib.oracle_mr_register_seq.restype = None
-            lib.oracle_mr_register_seq.argtypes = [vp, u64, vp, u32, vp, vp, vp, vp, u64, vp, vp,
-                                                   vp, vp, vp, vp, vp, vp]
+            for name in ("oracle_mr_register_seq", "oracle_mr_register_seq_indexed"):
+                fn = getattr(lib, name)
+                fn.restype = None
+                fn.argtypes = lib.oracle_mr_register.argtypes
             lib.oracle_mr_deregister.restype = None
             lib.oracle_mr_deregister.argtypes = [vp, u64, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp,
                                                  vp, vp]
@@ -194,12 +195,16 @@ def _table(start, end, lkey, refs):
 
 
 def mr_register(queries, new_lkey, start, end, lkey, refs, granule_shift: int = 12,
-                out_cap: int | None = None, one_at_a_time: bool = False) -> dict:
+                out_cap: int | None = None, one_at_a_time: bool = False,
+                indexed: bool = False) -> dict:
     """A batch of registrations against a table sorted by start (records may
     overlap). Returns the table after the batch (start, end, lkey, refs,
     trimmed to its size), handle / kind per request, remap per old record and
     ctr [records after, invalid, overflow, error bits]. With one_at_a_time,
-    the pages' per-call definition instead of the batch reading."""
+    the pages' per-call definition (each request looked up in the table as
+    the requests before it left it) instead of the batch reading; with
+    indexed as well, the same definition computed with an index (for large
+    batches; pinned equal to the scan)."""
     q = _u64(queries).reshape(-1, 2)
     start, end, lkey, refs = _table(start, end, lkey, refs)
     new_lkey = np.ascontiguousarray(new_lkey, dtype=np.uint32)
@@ -212,10 +217,10 @@ def mr_register(queries, new_lkey, start, end, lkey, refs, granule_shift: int = 
     remap = np.full(max(n, 1), -1, dtype=np.int64)
     ctr = np.zeros(4, dtype=np.uint64)
     if one_at_a_time:
-        _load().oracle_mr_register_seq(_p(q), n_q, _p(new_lkey), granule_shift, _p(start),
-                                       _p(end), _p(lkey), _p(refs), n, _p(o["start"]),
-                                       _p(o["end"]), _p(o["lkey"]), _p(o["refs"]), _p(handle),
-                                       _p(kind), _p(remap), _p(ctr))
+        fn = "oracle_mr_register_seq_indexed" if indexed else "oracle_mr_register_seq"
+        getattr(_load(), fn)(_p(q), n_q, _p(new_lkey), granule_shift, _p(start), _p(end),
+                             _p(lkey), _p(refs), n, _p(o["start"]), _p(o["end"]), _p(o["lkey"]),
+                             _p(o["refs"]), cap, _p(handle), _p(kind), _p(remap), _p(ctr))
     else:
         _load().oracle_mr_register(_p(q), n_q, _p(new_lkey), granule_shift, _p(start), _p(end),
                                    _p(lkey), _p(refs), n, _p(o["start"]), _p(o["end"]),

@@ -49,6 +49,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
 #include <map>
 #include <utility>
 #include <vector>
@@ -792,8 +793,8 @@ void oracle_mr_register_seq(const uint64_t* q, uint64_t n_q, const uint32_t* new
                             uint32_t granule_shift, const uint64_t* start, const uint64_t* end,
                             const uint32_t* lkey, const uint32_t* refs, uint64_t n,
                             uint64_t* o_start, uint64_t* o_end, uint32_t* o_lkey,
-                            uint32_t* o_refs, int64_t* handle, uint8_t* kind, int64_t* remap,
-                            uint64_t* ctr) {
+                            uint32_t* o_refs, uint64_t o_cap, int64_t* handle, uint8_t* kind,
+                            int64_t* remap, uint64_t* ctr) {
   struct Rec { uint64_t s, e; uint32_t lk, refs; int64_t id; };  // id: old index, or -1 - request
   const uint64_t g = 1ull << granule_shift;
   std::vector<Rec> t;
@@ -824,6 +825,14 @@ void oracle_mr_register_seq(const uint64_t* q, uint64_t n_q, const uint32_t* new
     got[k] = -1 - (int64_t)k;
     kind[k] = 4;
   }
+  uint64_t err = 0;
+  for (uint64_t i = 0; i < n; ++i)
+    if (!(start[i] < end[i]) || (i > 0 && start[i - 1] > start[i])) err = 4;
+  ctr[0] = t.size();
+  ctr[1] = n_invalid;
+  ctr[2] = t.size() > o_cap ? 1 : 0;
+  ctr[3] = err;
+  if (t.size() > o_cap) return;  // as in the batch reading: only counters and kinds
   std::map<int64_t, int64_t> final_index;
   for (size_t w = 0; w < t.size(); ++w) {
     o_start[w] = t[w].s;
@@ -834,10 +843,142 @@ void oracle_mr_register_seq(const uint64_t* q, uint64_t n_q, const uint32_t* new
   }
   for (uint64_t i = 0; i < n; ++i) remap[i] = final_index[(int64_t)i];
   for (uint64_t k = 0; k < n_q; ++k) handle[k] = kind[k] == 3 ? -1 : final_index[got[k]];
-  ctr[0] = t.size();
+}
+
+// The same one-at-a-time registration with an index, for batches too large
+// for the scan above (pinned equal to it by the tests). At request k the
+// table holds the old records and the records created by requests before k,
+// in start order (a record goes after every record starting at or before
+// it, so the old records come first on equal starts and created records of
+// equal start follow in creation order). The lowest-index record holding
+// [b, e) is then the old one found as in the batch reading, or the created
+// one of least start holding it, whichever comes first in that order. Two
+// created records of equal start hold no common later request in a
+// different order: the later one was created only because the earlier did
+// not hold it, so it ends later, and creation order is end order. So the
+// created records are kept at their (start, end) rank among every range
+// that could be created (the requests that miss the old table); the
+// created holder of least table index is the leftmost rank with start <= b
+// whose end reaches e (a max-tree over ranks).
+void oracle_mr_register_seq_indexed(const uint64_t* q, uint64_t n_q, const uint32_t* new_lkey,
+                                    uint32_t granule_shift, const uint64_t* start,
+                                    const uint64_t* end, const uint32_t* lkey,
+                                    const uint32_t* refs, uint64_t n, uint64_t* o_start,
+                                    uint64_t* o_end, uint32_t* o_lkey, uint32_t* o_refs,
+                                    uint64_t o_cap, int64_t* handle, uint8_t* kind,
+                                    int64_t* remap, uint64_t* ctr) {
+  const uint64_t g = 1ull << granule_shift;
+  uint64_t err = 0;
+  for (uint64_t i = 0; i < n; ++i)
+    if (!(start[i] < end[i]) || (i > 0 && start[i - 1] > start[i])) err = 4;
+  std::vector<uint64_t> pm(n);  // prefix maximum of the ends
+  for (uint64_t i = 0; i < n; ++i) pm[i] = (i && pm[i - 1] > end[i]) ? pm[i - 1] : end[i];
+  // 1. widen; the old holder of every request (the table before the batch)
+  std::vector<std::pair<uint64_t, uint64_t>> range(n_q);
+  std::vector<int64_t> old(n_q, -1);
+  std::vector<char> valid(n_q, 0);
+  std::vector<std::pair<uint64_t, uint64_t>> cand;  // ranges that miss the old table
+  for (uint64_t k = 0; k < n_q; ++k) {
+    uint64_t b, e;
+    if (!round_to_granule(q[2 * k], q[2 * k + 1], g, &b, &e)) continue;
+    valid[k] = 1;
+    range[k] = {b, e};
+    old[k] = lowest_holder(start, pm, n, b, e);
+    if (old[k] < 0) cand.push_back({b, e});
+  }
+  std::sort(cand.begin(), cand.end());
+  cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
+  const uint64_t nc = cand.size();
+  // max-tree over ranks: the end of the record created at that rank (0: none)
+  uint64_t size = 1;
+  while (size < nc) size <<= 1;
+  std::vector<uint64_t> tree(2 * size, 0);
+  auto set_end = [&](uint64_t r, uint64_t e) {
+    uint64_t x = r + size;
+    tree[x] = e;
+    for (x >>= 1; x > 0; x >>= 1) tree[x] = std::max(tree[2 * x], tree[2 * x + 1]);
+  };
+  // leftmost rank in [0, hi) whose end is >= e, or nc
+  std::function<uint64_t(uint64_t, uint64_t, uint64_t, uint64_t, uint64_t)> leftmost =
+      [&](uint64_t x, uint64_t lo, uint64_t width, uint64_t hi, uint64_t e) -> uint64_t {
+    if (lo >= hi || tree[x] < e) return nc;
+    if (width == 1) return lo;
+    const uint64_t half = width / 2;
+    const uint64_t a = leftmost(2 * x, lo, half, hi, e);
+    return a < nc ? a : leftmost(2 * x + 1, lo + half, half, hi, e);
+  };
+  // 2. the requests in order
+  std::vector<int64_t> creator(nc, -1);  // request that created the record at each rank
+  std::vector<uint64_t> crefs(nc, 0);
+  std::vector<uint64_t> more(n, 0);
+  std::vector<int64_t> got_old(n_q, -1), got_new(n_q, -1);
+  uint64_t n_invalid = 0, n_new = 0;
+  for (uint64_t k = 0; k < n_q; ++k) {
+    if (!valid[k]) {
+      kind[k] = 3;
+      n_invalid += 1;
+      continue;
+    }
+    const uint64_t b = range[k].first, e = range[k].second;
+    const uint64_t hi = (uint64_t)(std::upper_bound(cand.begin(), cand.end(),
+                                                    std::make_pair(b, UINT64_MAX)) -
+                                   cand.begin());
+    const uint64_t c = nc ? leftmost(1, 0, size, hi, e) : nc;
+    const int64_t o = old[k];
+    if (c < nc && (o < 0 || cand[c].first < start[o])) {
+      crefs[c] += 1;
+      got_new[k] = (int64_t)c;
+      kind[k] = 5;
+    } else if (o >= 0) {
+      more[o] += 1;
+      got_old[k] = o;
+      kind[k] = (start[o] == b && end[o] == e) ? 1 : 2;
+    } else {
+      const uint64_t r = (uint64_t)(std::lower_bound(cand.begin(), cand.end(), range[k]) -
+                                    cand.begin());
+      set_end(r, e);
+      creator[r] = (int64_t)k;
+      crefs[r] = 1;
+      got_new[k] = (int64_t)r;
+      kind[k] = 4;
+      n_new += 1;
+    }
+  }
+  const uint64_t n_out = n + n_new;
+  ctr[0] = n_out;
   ctr[1] = n_invalid;
-  ctr[2] = 0;
-  ctr[3] = 0;
+  ctr[2] = n_out > o_cap ? 1 : 0;
+  ctr[3] = err;
+  if (n_out > o_cap) return;
+  // 3. merge: old records first on equal starts; created ones in rank order
+  std::vector<int64_t> placed(nc, -1);
+  uint64_t i = 0, r = 0, w = 0;
+  while (r < nc && creator[r] < 0) ++r;
+  while (i < n || r < nc) {
+    const bool take_old = i < n && (r >= nc || start[i] <= cand[r].first);
+    if (take_old) {
+      o_start[w] = start[i];
+      o_end[w] = end[i];
+      o_lkey[w] = lkey[i];
+      o_refs[w] = (uint32_t)(refs[i] + more[i]);
+      remap[i] = (int64_t)w;
+      ++i;
+    } else {
+      o_start[w] = cand[r].first;
+      o_end[w] = cand[r].second;
+      o_lkey[w] = new_lkey[creator[r]];
+      o_refs[w] = (uint32_t)crefs[r];
+      placed[r] = (int64_t)w;
+      ++r;
+      while (r < nc && creator[r] < 0) ++r;
+    }
+    ++w;
+  }
+  for (uint64_t k = 0; k < n_q; ++k) {
+    if (kind[k] == 3) handle[k] = -1;
+    else if (got_new[k] >= 0) handle[k] = placed[got_new[k]];
+    else handle[k] = remap[got_old[k]];
+  }
 }
 
 void oracle_mr_deregister(const int64_t* h, uint64_t n_h, const uint64_t* start,

@@ -277,3 +277,88 @@ def test_partial_overlap_miss_with_the_same_start(oracle):
         # the third request is [0x1000, 0x3000) after rounding: the new range again
         assert r["kind"].tolist()[2] == 5 and r["handle"].tolist()[2] == 1
         assert r["refs"].tolist() == [2, 2, 1]
+
+
+def nested_batch(rng, n_old, n_q, pages, overlap):
+    """A table over a few pages (overlapping records when `overlap`) and
+    requests that nest in each other and in the records, in random order,
+    with repeats and invalid ones."""
+    if n_old:
+        s = np.sort(rng.integers(0, pages - 1, size=n_old)).astype(np.uint64)
+        if not overlap:
+            s = np.unique(s)
+        ln = rng.integers(1, 8 if overlap else 2, size=s.shape[0]).astype(np.uint64)
+        if not overlap:  # disjoint: each record ends before the next starts
+            nxt = np.append(s[1:], np.uint64(pages))
+            ln = np.minimum(ln, nxt - s)
+        e = s + ln
+        s, e = s * np.uint64(4096), e * np.uint64(4096)
+    else:
+        s = e = np.zeros(0, np.uint64)
+    lk = rng.integers(0, 2**32, size=s.shape[0], dtype=np.uint64).astype(np.uint32)
+    refs = rng.integers(1, 4, size=s.shape[0]).astype(np.uint32)
+    a = rng.integers(0, pages, size=n_q).astype(np.uint64) * np.uint64(4096)
+    a += rng.integers(0, 4096, size=n_q).astype(np.uint64) * (rng.random(n_q) < 0.3)
+    sz = rng.integers(1, 6 * 4096, size=n_q).astype(np.uint64)
+    rep = rng.random(n_q) < 0.15
+    for k in np.flatnonzero(rep):
+        if k:
+            j = int(rng.integers(0, k))
+            a[k], sz[k] = a[j], sz[j]
+    sz[rng.random(n_q) < 0.03] = 0  # invalid
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = rng.integers(0, 2**32, size=n_q, dtype=np.uint64).astype(np.uint32)
+    return q, nl, (s, e, lk, refs)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_indexed_one_at_a_time_equals_the_scan(oracle, seed):
+    """The indexed one-at-a-time registration gives exactly the scan's
+    result (table, handles, kinds, remap, counters) on batches whose new
+    ranges nest in each other and in old records, on disjoint and
+    overlapping tables, at 4 KiB and 64 KiB granules, and with too small an
+    output capacity."""
+    rng = np.random.default_rng(900 + seed)
+    q, nl, t = nested_batch(rng, int(rng.integers(0, 12)), int(rng.integers(1, 300)),
+                            int(rng.integers(4, 80)), overlap=seed % 2 == 1)
+    g = G64K if seed % 5 == 4 else G4K
+    if g == G64K:
+        q[:, 0] *= np.uint64(16)
+        q[:, 1] *= np.uint64(16)
+        t = (t[0] * np.uint64(16), t[1] * np.uint64(16), t[2], t[3])
+    for cap in (None, len(t[0]) + 1):
+        a = oracle.mr_register(q, nl, *t, granule_shift=g, out_cap=cap, one_at_a_time=True)
+        b = oracle.mr_register(q, nl, *t, granule_shift=g, out_cap=cap, one_at_a_time=True,
+                               indexed=True)
+        assert a["ctr"].tolist() == b["ctr"].tolist()
+        assert a["kind"].tolist() == b["kind"].tolist()
+        if int(a["ctr"][2]) == 0:
+            for key in ("start", "end", "lkey", "refs", "handle", "remap"):
+                assert a[key].tolist() == b[key].tolist(), key
+
+
+def test_one_at_a_time_nesting_hand_case(oracle):
+    """Worked by hand from the per-call definition (lowest-index holder in
+    the table as it stands; a new record after every record starting at or
+    before it), on the old table {[8K, 16K)}:
+      0: [4K, 8K)   misses           -> new record A
+      1: [4K, 6K)   inside A         -> hit on A (kind 5)
+      2: [0, 16K)   misses           -> new record B, before A (lower start)
+      3: [4K, 8K)   A and B hold it  -> B, the lower start (kind 5)
+      4: [8K, 12K)  old record and B -> B starts lower (kind 5)
+      5: [12K, 16K) inside B and old -> B
+      6: [8K, 16K)  same as the old  -> B still comes first (kind 5)
+    Final table: B [0, 16K) refs 5, A [4K, 8K) refs 2, old [8K, 16K) refs 1."""
+    K = 1024
+    t = (np.array([8 * K], np.uint64), np.array([16 * K], np.uint64), np.array([77], np.uint32),
+         np.array([1], np.uint32))
+    q = np.array([[4 * K, 4 * K], [4 * K, 2 * K], [0, 16 * K], [4 * K, 4 * K], [8 * K, 4 * K],
+                  [12 * K, 4 * K], [8 * K, 8 * K]], np.uint64)
+    for indexed in (False, True):
+        r = oracle.mr_register(q, [10, 11, 12, 13, 14, 15, 16], *t, one_at_a_time=True,
+                               indexed=indexed)
+        assert r["kind"].tolist() == [4, 5, 4, 5, 5, 5, 5]
+        assert rows_of(r) == [(0, 16 * K, 12, 5), (4 * K, 8 * K, 10, 2), (8 * K, 16 * K, 77, 1)]
+        assert r["handle"].tolist() == [1, 1, 0, 0, 0, 0, 0]
+        assert r["remap"].tolist() == [2]
+        assert r["ctr"].tolist() == [3, 0, 0, 0]

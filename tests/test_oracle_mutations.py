@@ -109,6 +109,17 @@ MUTANTS = [
     ("register: repeats are not merged", "if (it == fresh.end()) {", "if (true) {"),
     ("register one at a time: insert before equal starts",
      "while (at < t.size() && t[at].s <= b) ++at;", "while (at < t.size() && t[at].s < b) ++at;"),
+    ("register indexed: a created record beats an old one of equal start",
+     "if (c < nc && (o < 0 || cand[c].first < start[o])) {",
+     "if (c < nc && (o < 0 || cand[c].first <= start[o])) {"),
+    ("register indexed: created holders may start past the base",
+     "std::make_pair(b, UINT64_MAX)) -", "std::make_pair(b + g, UINT64_MAX)) -"),
+    ("register indexed: holder search ignores the end",
+     "if (lo >= hi || tree[x] < e) return nc;", "if (lo >= hi || tree[x] == 0) return nc;"),
+    ("register indexed: prefix maximum of the ends restarts",
+     "pm[i] = (i && pm[i - 1] > end[i]) ? pm[i - 1] : end[i];", "pm[i] = end[i];"),
+    ("register one at a time: overflow not reported",
+     "ctr[2] = t.size() > o_cap ? 1 : 0;", "ctr[2] = 0;"),
     ("deregister: released one reference early",
      "status[k] = left[i] == 0 ? 1 : 0;", "status[k] = left[i] <= 1 ? 1 : 0;"),
     ("deregister: a released record takes more",
