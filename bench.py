@@ -543,9 +543,10 @@ def time_mr_mutation(args, device, stream, only=None) -> dict:
     out["mr_register"] = {"ms": round(ms, 4), "M_req_per_s": round(nq / ms / 1e3, 2),
                           "records_before": n, "new_records": u, "algorithmic_bytes": alg,
                           "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                          "note": "not part of the step: timed alone; lookup + 14 radix passes "
-                                  "+ merge, 95 launches (each a programmatic dependent of the "
-                                  "one before)"}
+                          "note": "not part of the step: timed alone; the requests' one-at-a-time "
+                                  "result: lookup, 14 radix passes, two dominance passes (merge "
+                                  "sorts on the end), merge; 164 launches, each a programmatic "
+                                  "dependent of the one before"}
     del rb
     if only == "mr_register":
         return out

@@ -431,11 +431,432 @@ int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip
   return launch_result();
 }
 
+// ------------------------------------------------- dominance minimum (CDQ)
+// Over a sequence of n items (n read on the device, at most n_max), each
+// with an end e, an optional key (kNone: not a point) and an optional query
+// id (kNone: not a query): for every query item i, the least key over the
+// points j < i whose end is at least e_i, written to ans[query id] (kNone
+// if there is none). A merge sort on e, descending, carries the answers:
+// when two neighbouring runs merge, every query of the right run takes the
+// least key over the points of the left run that reach its end -- a prefix
+// of the left run in that order -- so each pair (j < i) is met exactly
+// once, at the merge of the two runs that first hold both. Runs of up to
+// kCdqTile items merge in shared memory; longer ones output tile by output
+// tile along the merge path. The prefix minima of the keys are kept per
+// tile (pm) with the minimum of the run's earlier tiles (cpm).
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+constexpr int kCdqTile = 2048;
+constexpr int kCdqThreads = 512;
+constexpr int kCdqPer = kCdqTile / kCdqThreads;  // 4
+struct CdqBufs {
+  uint64_t* e[2];
+  uint32_t* key[2];
+  uint32_t* qid[2];
+  uint32_t* ans[2];
+  uint32_t* pm[2];   // [n_max] prefix minimum of the keys within each tile
+  uint32_t* cmin;    // [tiles] minimum key of each tile
+  uint32_t* cpm[2];  // [tiles] minimum key of the run's tiles before each tile
+  uint64_t n_max;
+  unsigned int* err;  // DB_ERR_TABLE_ORDER if a merge finds unsorted input
+};
+__host__ __device__ inline uint64_t cdq_tiles(uint64_t n) {
+  return ((n ? n : 1) + kCdqTile - 1) / kCdqTile;
+}
+// Merge levels after the tile level: runs of kCdqTile << l merge for l = 0, 1, ...
+inline uint32_t cdq_levels(uint64_t n) {
+  uint32_t l = 0;
+  while (((uint64_t)kCdqTile << l) < n) ++l;
+  return l;
+}
+__device__ __forceinline__ uint32_t cdq_levels_dev(uint64_t n) {
+  uint32_t l = 0;
+  while (((uint64_t)kCdqTile << l) < n) ++l;
+  return l;
+}
+
+// pm[i] = the least key over positions [run start, i] of runs of `seg`
+// items (a power of two) in the order `ord`; a thread owns positions
+// 4t .. 4t + 3. Ends with every thread past a barrier after the writes.
+__device__ __forceinline__ void seg_prefix_min(const uint32_t* sk, const uint16_t* ord,
+                                               uint32_t nt, uint32_t seg, uint32_t* pm,
+                                               uint32_t* s_w) {
+  const uint32_t base = threadIdx.x * kCdqPer;
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t v[kCdqPer];
+#pragma unroll
+  for (int u = 0; u < kCdqPer; ++u) v[u] = base + u < nt ? sk[ord[base + u]] : kNone;
+  if (seg <= (uint32_t)kCdqPer) {  // runs inside the thread
+#pragma unroll
+    for (int u = 1; u < kCdqPer; ++u)
+      if ((u & (seg - 1)) != 0) v[u] = min(v[u], v[u - 1]);
+  } else {
+#pragma unroll
+    for (int u = 1; u < kCdqPer; ++u) v[u] = min(v[u], v[u - 1]);
+    const uint32_t tpr = seg / kCdqPer;               // threads per run
+    const uint32_t wseg = tpr < 32 ? tpr : 32u;       // its part inside a warp
+    uint32_t x = v[kCdqPer - 1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if ((lane & (wseg - 1)) >= (uint32_t)o) x = min(x, y);
+    }
+    const uint32_t prev = __shfl_up_sync(kFull, x, 1);
+    uint32_t before = (lane & (wseg - 1)) ? prev : kNone;
+    if (tpr > 32) {  // earlier warps of the same run
+      if (lane == 31) s_w[warp] = x;
+      __syncthreads();
+      const uint32_t wpr = tpr / 32;
+      for (uint32_t w = warp & ~(wpr - 1); w < warp; ++w) before = min(before, s_w[w]);
+    }
+#pragma unroll
+    for (int u = 0; u < kCdqPer; ++u) v[u] = min(v[u], before);
+  }
+#pragma unroll
+  for (int u = 0; u < kCdqPer; ++u)
+    if (base + u < nt) pm[base + u] = v[u];
+  __syncthreads();
+}
+
+// Tile level: items [t0, t0 + nt) sorted by end (descending, stable) in
+// shared memory, answers from the pairs inside the tile; out to buffer 0.
+constexpr size_t kCdqTileSmem = (size_t)kCdqTile * (8 + 4 * 4 + 2 * 2);
+__global__ void __launch_bounds__(kCdqThreads) cdq_tile(const uint64_t* e_in,
+                                                        const uint32_t* key_in,
+                                                        const uint32_t* qid_in,
+                                                        const uint32_t* n_dev, CdqBufs b) {
+  kernel_prologue();
+  extern __shared__ __align__(16) unsigned char cdq_smem[];
+  uint64_t* se = reinterpret_cast<uint64_t*>(cdq_smem);
+  uint32_t* sk = reinterpret_cast<uint32_t*>(se + kCdqTile);
+  uint32_t* sq = sk + kCdqTile;
+  uint32_t* sa = sq + kCdqTile;
+  uint32_t* pm = sa + kCdqTile;
+  uint16_t* const ord0 = reinterpret_cast<uint16_t*>(pm + kCdqTile);
+  uint16_t* const ord1 = ord0 + kCdqTile;
+  __shared__ uint32_t s_w[kCdqThreads / 32];
+  const uint64_t n = *n_dev;
+  for (uint64_t t0 = (uint64_t)blockIdx.x * kCdqTile; t0 < n;
+       t0 += (uint64_t)gridDim.x * kCdqTile) {
+  const uint32_t nt = (uint32_t)(n - t0 < kCdqTile ? n - t0 : kCdqTile);
+  for (uint32_t x = threadIdx.x; x < nt; x += kCdqThreads) {
+    se[x] = e_in[t0 + x];
+    sk[x] = key_in[t0 + x];
+    sq[x] = qid_in[t0 + x];
+    sa[x] = kNone;
+    ord0[x] = (uint16_t)x;
+    pm[x] = sk[x];
+  }
+  __syncthreads();
+  int cur = 0;
+  for (uint32_t s = 1; s < nt; s <<= 1) {
+    // place every item in the merge of its run with the neighbouring one
+    const uint16_t* oc = cur ? ord1 : ord0;
+    uint16_t* on = cur ? ord0 : ord1;
+#pragma unroll
+    for (int u = 0; u < kCdqPer; ++u) {
+      const uint32_t i = threadIdx.x * kCdqPer + u;
+      if (i >= nt) continue;
+      const uint32_t x = oc[i];
+      const uint64_t ex = se[x];
+      const uint32_t r = i / s, pb = (r & ~1u) * s;
+      uint32_t pos;
+      if ((r & 1u) == 0) {  // left run: after the right run's items with a greater end
+        uint32_t lo = pb + s < nt ? pb + s : nt, hi = pb + 2 * s < nt ? pb + 2 * s : nt;
+        const uint32_t base = lo;
+        while (lo < hi) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (se[oc[mid]] > ex) lo = mid + 1;
+          else hi = mid;
+        }
+        pos = (i - pb) + (lo - base);
+      } else {  // right run: after the left run's items with an end at least its own
+        uint32_t lo = pb, hi = pb + s;
+        while (lo < hi) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (se[oc[mid]] >= ex) lo = mid + 1;
+          else hi = mid;
+        }
+        const uint32_t cnt = lo - pb;
+        if (sq[x] != kNone && cnt > 0) sa[x] = min(sa[x], pm[pb + cnt - 1]);
+        pos = (i - pb - s) + cnt;
+      }
+      on[pb + pos] = (uint16_t)x;
+    }
+    __syncthreads();
+    cur ^= 1;
+    seg_prefix_min(sk, cur ? ord1 : ord0, nt, 2 * s, pm, s_w);
+  }
+  for (uint32_t i = threadIdx.x; i < nt; i += kCdqThreads) {
+    const uint32_t x = (cur ? ord1 : ord0)[i];
+    b.e[0][t0 + i] = se[x];
+    b.key[0][t0 + i] = sk[x];
+    b.qid[0][t0 + i] = sq[x];
+    b.ans[0][t0 + i] = sa[x];
+    b.pm[0][t0 + i] = pm[i];
+  }
+  if (threadIdx.x == 0) b.cpm[0][t0 / kCdqTile] = kNone;  // a tile is its whole run
+  __syncthreads();  // shared memory is reused by the next tile
+  }
+}
+
+// Merge level l: runs of len = kCdqTile << l, buffers (l & 1) to (l & 1) ^ 1.
+// A CTA makes tile c of the output: the merge of the slices of the two runs
+// that precede it in the merged order (found by a warp-parallel binary
+// search on the merge path), in shared memory, written out whole with the
+// tile's prefix minima of the keys. A right-run query takes the least key of
+// the left run's prefix reaching its end, from the input's prefix minima.
+//
+// The merge path: the first d items of the merge are i items of the left
+// run and d - i of the right run for the least i at which the right run's
+// (d - i)-th item is ahead of the left run's (i + 1)-th, R[d - i - 1] > L[i]
+// (a right item is ahead only with a strictly greater end); that test turns
+// from false to true as i grows, and with none, i is the largest possible.
+__device__ __forceinline__ uint64_t corank_warp(const uint64_t* L, uint64_t nL, const uint64_t* R,
+                                                uint64_t nR, uint64_t d) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint64_t lo = d > nR ? d - nR : 0, hi = d < nL ? d : nL;  // answer in [lo, hi]
+  // probe t(i) = R[d - i - 1] <= L[i] (true before the answer)
+  while (hi - lo > 32) {
+    const uint64_t step = (hi - lo + 31) / 32;
+    const uint64_t at = lo + lane * step;
+    bool t = false;
+    if (at < hi) t = R[d - at - 1] <= L[at];
+    const uint32_t k = __popc(__ballot_sync(kFull, t));
+    const uint64_t nlo = k ? lo + (k - 1) * step + 1 : lo;
+    const uint64_t nhi = lo + k * step < hi ? lo + k * step : hi;
+    lo = nlo;
+    hi = nhi;
+  }
+  bool t = false;
+  if (lo + lane < hi) t = R[d - (lo + lane) - 1] <= L[lo + lane];
+  return lo + __popc(__ballot_sync(kFull, t));
+}
+constexpr size_t kCdqMergeSmem = (size_t)kCdqTile * (8 + 8 + 4 * 3);
+__global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32_t* n_dev,
+                                                         uint32_t level) {
+  kernel_prologue();
+  extern __shared__ __align__(16) unsigned char cdq_smem[];
+  uint64_t* seg = reinterpret_cast<uint64_t*>(cdq_smem);  // left slice, then right slice
+  uint64_t* oe = seg + kCdqTile;
+  uint32_t* ok = reinterpret_cast<uint32_t*>(oe + kCdqTile);
+  uint32_t* oq = ok + kCdqTile;
+  uint32_t* oa = oq + kCdqTile;
+  __shared__ uint64_t s_i0, s_i1;
+  __shared__ uint32_t s_w[kCdqThreads / 32];
+  const uint64_t n = *n_dev;
+  const uint64_t len = (uint64_t)kCdqTile << level;
+  if (len >= n) return;  // this level is not needed
+  for (uint64_t o0 = (uint64_t)blockIdx.x * kCdqTile; o0 < n;
+       o0 += (uint64_t)gridDim.x * kCdqTile) {
+  const uint64_t o1 = o0 + kCdqTile < n ? o0 + kCdqTile : n;
+  const bool odd = (level & 1u) != 0;  // input buffer 1, output 0
+  const uint64_t* E = odd ? b.e[1] : b.e[0];
+  const uint32_t* Kin = odd ? b.key[1] : b.key[0];
+  const uint32_t* Qin = odd ? b.qid[1] : b.qid[0];
+  const uint32_t* Ain = odd ? b.ans[1] : b.ans[0];
+  const uint32_t* PMin = odd ? b.pm[1] : b.pm[0];
+  const uint32_t* CPMin = odd ? b.cpm[1] : b.cpm[0];
+  uint64_t* Eo = odd ? b.e[0] : b.e[1];
+  uint32_t* Ko = odd ? b.key[0] : b.key[1];
+  uint32_t* Qo = odd ? b.qid[0] : b.qid[1];
+  uint32_t* Ao = odd ? b.ans[0] : b.ans[1];
+  uint32_t* PMo = odd ? b.pm[0] : b.pm[1];
+  const uint64_t pb = o0 / (2 * len) * (2 * len);
+  const uint64_t nL = pb + len < n ? len : n - pb;
+  const uint64_t rb = pb + nL;
+  const uint64_t nR = pb + 2 * len < n ? len : n - rb;
+  const uint64_t d0 = o0 - pb, d1 = o1 - pb;
+  if (threadIdx.x < 32) {
+    const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d0);
+    if (threadIdx.x == 0) s_i0 = i;
+  } else if (threadIdx.x < 64) {
+    const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d1);
+    if (threadIdx.x == 32) s_i1 = i;
+  }
+  __syncthreads();
+  const uint64_t i0 = s_i0, i1 = s_i1, j0 = d0 - i0, j1 = d1 - i1;
+  // A slice pair that is not a split of this tile (impossible for sorted
+  // runs) is reported and the tile left unwritten.
+  if (i1 < i0 || i1 > nL || j0 > d0 || j1 < j0 || j1 > nR) {
+    if (threadIdx.x == 0) atomicOr(b.err, DB_ERR_TABLE_ORDER);
+    __syncthreads();
+    continue;
+  }
+  const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0);
+  for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads)
+    seg[x] = x < na ? E[pb + i0 + x] : E[rb + j0 + (x - na)];
+  __syncthreads();
+  const uint64_t* sl = seg;
+  const uint64_t* sr = seg + na;
+  for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads) {
+    const bool from_left = x < na;
+    const uint64_t ex = seg[x];
+    uint32_t lo = 0, hi = from_left ? nb : na;
+    const uint64_t* o = from_left ? sr : sl;
+    while (lo < hi) {  // other-slice items ahead of this one
+      const uint32_t mid = (lo + hi) >> 1;
+      const uint64_t v = o[mid];
+      if (v > ex || (!from_left && v == ex)) lo = mid + 1;
+      else hi = mid;
+    }
+    const uint64_t gi = from_left ? pb + i0 + x : rb + j0 + (x - na);
+    const uint32_t q = Qin[gi];
+    uint32_t a = Ain[gi];
+    if (!from_left && q != kNone) {
+      const uint64_t c = i0 + lo;  // left-run items with an end at least ex
+      if (c > 0) {
+        const uint64_t j = pb + c - 1;
+        a = min(a, min(PMin[j], CPMin[j / kCdqTile]));
+      }
+    }
+    const uint32_t pos = (from_left ? x : x - na) + lo;
+    if (pos >= na + nb) {  // impossible for sorted slices; reported, not written
+      atomicOr(b.err, DB_ERR_TABLE_ORDER);
+      continue;
+    }
+    oe[pos] = ex;
+    ok[pos] = Kin[gi];
+    oq[pos] = q;
+    oa[pos] = a;
+  }
+  __syncthreads();
+  // write the tile out with its prefix minima of the keys
+  const uint32_t nt = (uint32_t)(o1 - o0);
+  const uint32_t base = threadIdx.x * kCdqPer;
+  uint32_t v[kCdqPer];
+  uint32_t run = kNone;
+#pragma unroll
+  for (int u = 0; u < kCdqPer; ++u) {
+    run = min(run, base + u < nt ? ok[base + u] : kNone);
+    v[u] = run;
+  }
+  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= (uint32_t)o) x = min(x, y);
+  }
+  if (lane == 31) s_w[warp] = x;
+  const uint32_t up = __shfl_up_sync(kFull, x, 1);
+  __syncthreads();
+  uint32_t before = lane ? up : kNone;
+  for (uint32_t w = 0; w < warp; ++w) before = min(before, s_w[w]);
+  for (uint32_t t = threadIdx.x; t < nt; t += kCdqThreads) {
+    Eo[o0 + t] = oe[t];
+    Ko[o0 + t] = ok[t];
+    Qo[o0 + t] = oq[t];
+    Ao[o0 + t] = oa[t];
+  }
+#pragma unroll
+  for (int u = 0; u < kCdqPer; ++u)
+    if (base + u < nt) PMo[o0 + base + u] = min(before, v[u]);
+  if (threadIdx.x == kCdqThreads - 1) {
+    uint32_t all = kNone;
+    for (int w = 0; w < kCdqThreads / 32; ++w) all = min(all, s_w[w]);
+    b.cmin[o0 / kCdqTile] = all;
+  }
+  __syncthreads();  // shared memory is reused by the next tile
+  }
+}
+
+// cpm[t] = the least cmin over the tiles before t in its merged run (one
+// CTA, 1,024 tiles at a time): a segmented scan, a run's first tile a head.
+__global__ void __launch_bounds__(1024) cdq_cpm(CdqBufs b, const uint32_t* n_dev, uint32_t level) {
+  kernel_prologue();
+  __shared__ uint32_t s_v[1024];
+  __shared__ uint8_t s_f[1024];
+  const uint64_t n = *n_dev;
+  const uint64_t len2 = (uint64_t)kCdqTile << (level + 1);  // merged run length
+  if ((len2 >> 1) >= n) return;
+  const uint64_t tiles = cdq_tiles(n);
+  const uint64_t per = len2 / kCdqTile;  // tiles per merged run
+  const uint32_t tid = threadIdx.x;
+  uint32_t carry = kNone;  // inclusive minimum of the open run up to the last block
+  for (uint64_t t0 = 0; t0 < tiles; t0 += 1024) {
+    const uint64_t t = t0 + tid;
+    const bool head = (t % per) == 0;
+    s_v[tid] = t < tiles ? b.cmin[t] : kNone;
+    s_f[tid] = head ? 1 : 0;
+    __syncthreads();
+    for (uint32_t d = 1; d < 1024; d <<= 1) {
+      uint32_t v = s_v[tid];
+      uint8_t f = s_f[tid];
+      if (tid >= d && !f) {
+        v = min(v, s_v[tid - d]);
+        f = s_f[tid - d];
+      }
+      __syncthreads();
+      s_v[tid] = v;
+      s_f[tid] = f;
+      __syncthreads();
+    }
+    // s_v[tid]: minimum from the last head in the block (or its start) to tid
+    const uint32_t prev = tid ? (s_f[tid - 1] ? s_v[tid - 1] : min(s_v[tid - 1], carry)) : carry;
+    if (t < tiles) ((level & 1u) ? b.cpm[0] : b.cpm[1])[t] = head ? kNone : prev;
+    __syncthreads();
+    carry = s_f[1023] ? s_v[1023] : min(s_v[1023], carry);
+    __syncthreads();
+  }
+}
+
+// Answers to the queries, from the buffer the last level wrote.
+__global__ void cdq_out(CdqBufs b, const uint32_t* n_dev, uint32_t* ans) {
+  kernel_prologue();
+  const uint64_t n = *n_dev;
+  const bool fin1 = (cdq_levels_dev(n) & 1u) != 0;
+  const uint32_t* Q = fin1 ? b.qid[1] : b.qid[0];
+  const uint32_t* A = fin1 ? b.ans[1] : b.ans[0];
+  FOR_EACH(i, n) {
+    const uint32_t q = Q[i];
+    if (q != kNone) ans[q] = A[i];
+  }
+}
+
+// The whole computation on items e_in / key_in / qid_in (at most b.n_max,
+// *n_dev of them); every launch is a dependent of the one before.
+int cdq_dominance_min(const uint64_t* e_in, const uint32_t* key_in, const uint32_t* qid_in,
+                      const uint32_t* n_dev, CdqBufs& b, uint32_t* ans, cudaStream_t s) {
+  static bool ready[64] = {false};  // the tile kernel's shared memory is above 48 KiB
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!ready[dev & 63]) {
+    if (cudaFuncSetAttribute(cdq_tile, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kCdqTileSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(cdq_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kCdqMergeSmem) != cudaSuccess)
+      return launch_result();
+    ready[dev & 63] = true;
+  }
+  // Loops over the tiles of the device-side length: one wave of CTAs.
+  uint64_t tiles = cdq_tiles(b.n_max);
+  const uint64_t wave = (uint64_t)num_sms() * 3;
+  if (tiles > wave) tiles = wave;
+  int rc = 0;
+  launch_dep(cdq_tile, (unsigned)tiles, kCdqThreads, kCdqTileSmem, s, e_in, key_in, qid_in,
+             n_dev, b);
+  if ((rc = launch_result())) return rc;
+  const uint32_t levels = cdq_levels(b.n_max);
+  for (uint32_t l = 0; l < levels; ++l) {
+    launch_dep(cdq_merge, (unsigned)tiles, kCdqThreads, kCdqMergeSmem, s, b, n_dev, l);
+    if ((rc = launch_result())) return rc;
+    if (l + 1 < levels) {  // the last level's tile minima are never read
+      launch_dep(cdq_cpm, 1, 1024, 0, s, b, n_dev, l);
+      if ((rc = launch_result())) return rc;
+    }
+  }
+  launch_dep(cdq_out, grid_for(b.n_max), kThreads, 0, s, b, n_dev, ans);
+  return launch_result();
+}
+
 // ------------------------------------------------------------- registration
 struct RegHeader {   // 256 bytes at the start of the registration workspace
-  uint32_t m;        // requests that missed
-  uint32_t u;        // distinct missed ranges (new records)
-  uint32_t pad[2];
+  uint32_t m;        // requests that missed the table before the batch
+  uint32_t u;        // new records (requests no earlier request's range held)
+  uint32_t d;        // distinct ranges among the misses
+  uint32_t nb;       // items of the second dominance pass (new records and queries)
+  unsigned int err;  // an inconsistency the passes found (DB_ERR_TABLE_ORDER)
+  uint32_t pad[3];
   db_counters lookup;  // counters of the lookup pass
 };
 
@@ -447,14 +868,9 @@ __device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gs
   aend = (addr + size + g - 1) & ~(g - 1);  // valid requests only: no wrap
 }
 
-__global__ void reg_mark(const uint8_t* kind0, const int32_t* idx, uint64_t n_q, uint32_t* more,
-                         uint32_t* flag) {
+__global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* flag) {
   kernel_prologue();
-  FOR_EACH(k, n_q) {
-    const uint8_t kd = kind0[k];
-    flag[k] = kd == DB_MR_MISS;
-    if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) atomicAdd(&more[idx[k]], 1u);
-  }
+  FOR_EACH(k, n_q) flag[k] = kind0[k] == DB_MR_MISS;
 }
 __global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint32_t* pos,
                             uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val) {
@@ -463,7 +879,7 @@ __global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint3
     if (!flag[k]) continue;
     uint64_t b, e;
     widen(q, k, gshift, b, e);
-    key[pos[k]] = e >> gshift;
+    key[pos[k]] = ~e >> gshift;  // ends descending
     val[pos[k]] = (uint32_t)k;
   }
 }
@@ -498,24 +914,259 @@ __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, 
     flag[i] = f;
   }
 }
-// New record j from the run that starts at sorted position i; every miss
-// adds one reference to its run's record.
-__global__ void reg_new(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
-                        const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
-                        uint64_t* nstart, uint64_t* nend, uint32_t* nfirst, uint32_t* nrefs) {
+// The distinct missed ranges, in (start ascending, end descending) order,
+// as items of the first dominance pass: a range's end, and the request that
+// first asked for it (its key and first[]); each is a query for the least
+// first request among the ranges before it that reach its end -- the ranges
+// that hold it.
+__global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_max,
+                             uint32_t gshift, const uint32_t* val, const uint32_t* flag,
+                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first,
+                             uint64_t* ce_in, uint32_t* ck_in, uint32_t* cq_in) {
   kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
-    const uint32_t j = excl[i] + flag[i] - 1;
-    if (flag[i]) {
-      uint64_t b, e;
-      widen(q, val[i], gshift, b, e);
-      nstart[j] = b;
-      nend[j] = e;
-      nfirst[j] = val[i];
+    if (!flag[i]) continue;
+    const uint32_t p = excl[i];
+    uint64_t b, e;
+    widen(q, val[i], gshift, b, e);
+    db[p] = b;
+    de[p] = e;
+    first[p] = val[i];
+    ce_in[p] = e;
+    ck_in[p] = val[i];
+    cq_in[p] = p;
+  }
+}
+// A distinct range makes a new record when no range before it that holds it
+// was asked for earlier (then its first request finds no record holding it).
+__global__ void reg_creators(const RegHeader* h, uint64_t n_max, const uint32_t* first,
+                             const uint32_t* held_by, uint32_t* cflag) {
+  kernel_prologue();
+  const uint64_t d = h->d;
+  FOR_EACH(p, n_max) cflag[p] = p < d && held_by[p] > first[p];
+}
+// New records in (start ascending, end descending) order: c = cpos[p].
+__global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cflag,
+                          const uint32_t* cpos, const uint64_t* db, uint32_t* cp, uint64_t* cb) {
+  kernel_prologue();
+  const uint64_t d = h->d;
+  FOR_EACH(p, n_max) {
+    if (p >= d) break;
+    if (!cflag[p]) continue;
+    cp[cpos[p]] = (uint32_t)p;
+    cb[cpos[p]] = db[p];
+  }
+}
+// Table order of the new records: start ascending, then end ascending (a
+// later new record of the same start ends later: it was not held by the
+// earlier one). Within a run of equal starts the list above is in the
+// opposite order of ends, so record c of a run [gs, ge) goes to gs + ge - 1 - c.
+__global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* cp,
+                           const uint64_t* cb, const uint64_t* de, const uint32_t* first,
+                           uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
+                           uint32_t* creator_of, uint64_t* cend) {
+  kernel_prologue();
+  const uint64_t u = h->u;
+  FOR_EACH(c, n_max) {
+    if (c >= u) break;
+    const uint64_t b = cb[c];
+    uint64_t gs = c, ge = c + 1;
+    if ((c > 0 && cb[c - 1] == b) || (c + 1 < u && cb[c + 1] == b)) {
+      uint64_t lo = 0, hi = c;  // first with start b
+      while (lo < hi) {
+        const uint64_t mid = (lo + hi) >> 1;
+        if (cb[mid] < b) lo = mid + 1;
+        else hi = mid;
+      }
+      gs = lo;
+      lo = c + 1;
+      hi = u;  // first with a greater start
+      while (lo < hi) {
+        const uint64_t mid = (lo + hi) >> 1;
+        if (cb[mid] <= b) lo = mid + 1;
+        else hi = mid;
+      }
+      ge = lo;
     }
-    atomicAdd(&nrefs[j], 1u);
+    const uint64_t j = gs + ge - 1 - c;
+    const uint32_t p = cp[c];
+    const uint64_t e = de[p];
+    nstart[j] = b;
+    nend[j] = e;
+    nfirst[j] = first[p];
+    creator_of[first[p]] = (uint32_t)j;
+    cend[c] = e;
+  }
+}
+// reach[o] = the largest end of a new record starting before old record o
+// (a prefix maximum of cend over the list, which is in start order): a hit
+// on o can be taken by a new record only if its end is within that reach.
+__global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t* pmax,
+                          const uint64_t* start, uint64_t n, uint64_t* reach) {
+  kernel_prologue();
+  const uint64_t u = h->u;
+  FOR_EACH(o, n) {
+    const uint64_t s = start[o];
+    uint64_t lo = 0, hi = u;  // new records starting before s
+    while (lo < hi) {
+      const uint64_t mid = (lo + hi) >> 1;
+      if (cb[mid] < s) lo = mid + 1;
+      else hi = mid;
+    }
+    reach[o] = lo ? pmax[lo - 1] : 0;
+  }
+}
+// Items of the second dominance pass, in request order: the new records
+// (key: table position among the new records, end) and the requests whose
+// record is still open -- misses that made no record, and hits on an old
+// record that a new record may precede (query id: the request).
+__global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
+                          const int32_t* idx, const uint64_t* reach, uint32_t* role) {
+  kernel_prologue();
+  FOR_EACH(k, n_q) {
+    const uint8_t kd = kind0[k];
+    uint32_t r = 0;
+    if (kd == DB_MR_MISS) {
+      r = 1;
+    } else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) {
+      uint64_t b, e;
+      widen(q, k, gshift, b, e);
+      r = reach[idx[k]] >= e;  // a new record starting before the old one may hold it
+    }
+    role[k] = r;
+  }
+}
+
+// Inclusive prefix maximum of n u64 values (n on the device, at most n_max):
+// block maxima, their scan by one CTA, then each block with its carry.
+constexpr int kMaxScanThreads = 1024;
+__global__ void __launch_bounds__(kMaxScanThreads) pmax_reduce(const uint64_t* in,
+                                                               const uint32_t* n_dev,
+                                                               uint64_t* bmax) {
+  kernel_prologue();
+  __shared__ uint64_t s_w[32];
+  const uint64_t n = *n_dev;
+  const uint64_t i = (uint64_t)blockIdx.x * kMaxScanThreads + threadIdx.x;
+  if ((uint64_t)blockIdx.x * kMaxScanThreads >= n) return;
+  uint64_t v = i < n ? in[i] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t y = __shfl_xor_sync(kFull, v, o);
+    v = v > y ? v : y;
+  }
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t m = 0;
+    for (int w = 0; w < kMaxScanThreads / 32; ++w) m = m > s_w[w] ? m : s_w[w];
+    bmax[blockIdx.x] = m;
+  }
+}
+__global__ void __launch_bounds__(1024) pmax_blocks(uint64_t* bmax, const uint32_t* n_dev) {
+  kernel_prologue();
+  __shared__ uint64_t s_w[32];
+  const uint64_t nb = (*n_dev + kMaxScanThreads - 1) / kMaxScanThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t carry = 0;  // the maximum of the blocks before this round
+  for (uint64_t b0 = 0; b0 < nb; b0 += 1024) {
+    const uint64_t b = b0 + threadIdx.x;
+    const uint64_t v = b < nb ? bmax[b] : 0;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o && y > x) x = y;
+    }
+    if (lane == 31) s_w[warp] = x;
+    __syncthreads();
+    const uint64_t up = __shfl_up_sync(kFull, x, 1);
+    uint64_t ex = lane ? up : 0;  // exclusive within the warp
+    for (int w = 0; w < warp; ++w) ex = ex > s_w[w] ? ex : s_w[w];
+    ex = ex > carry ? ex : carry;
+    if (b < nb) bmax[b] = ex;
+    uint64_t all = carry;
+    for (int w = 0; w < 32; ++w) all = all > s_w[w] ? all : s_w[w];
+    __syncthreads();  // s_w is written again in the next round
+    carry = all;
+  }
+}
+__global__ void __launch_bounds__(kMaxScanThreads) pmax_apply(const uint64_t* in,
+                                                              const uint32_t* n_dev,
+                                                              const uint64_t* bmax,
+                                                              uint64_t* out) {
+  kernel_prologue();
+  __shared__ uint64_t s_w[32];
+  const uint64_t n = *n_dev;
+  if ((uint64_t)blockIdx.x * kMaxScanThreads >= n) return;
+  const uint64_t i = (uint64_t)blockIdx.x * kMaxScanThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = i < n ? in[i] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o && y > x) x = y;
+  }
+  if (lane == 31) s_w[warp] = x;
+  __syncthreads();
+  uint64_t before = bmax[blockIdx.x];
+  for (int w = 0; w < warp; ++w) before = before > s_w[w] ? before : s_w[w];
+  if (i < n) out[i] = before > x ? before : x;
+}
+__global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, const uint32_t* role,
+                          const uint32_t* rpos, const uint32_t* creator_of, uint64_t* ce_in,
+                          uint32_t* ck_in, uint32_t* cq_in) {
+  kernel_prologue();
+  FOR_EACH(k, n_q) {
+    if (!role[k]) continue;
+    uint64_t b, e;
+    widen(q, k, gshift, b, e);
+    const uint32_t at = rpos[k];
+    const uint32_t c = creator_of[k];
+    ce_in[at] = e;
+    ck_in[at] = c;                       // kNone unless k made a record
+    cq_in[at] = c == kNone ? (uint32_t)k : kNone;
+  }
+}
+// Every request's record and kind, and the references they add.
+__global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
+                            const int32_t* idx, const uint32_t* role, const uint32_t* creator_of,
+                            const uint32_t* held, const uint64_t* nstart, const uint64_t* start,
+                            uint32_t* more, uint32_t* nrefs, uint32_t* rec_new, uint8_t* kind1,
+                            RegHeader* h) {
+  kernel_prologue();
+  FOR_EACH(k, n_q) {
+    const uint8_t kd = kind0[k];
+    uint32_t rn = kNone;
+    uint8_t k1 = kd;
+    if (kd != DB_MR_INVALID) {
+      uint64_t b, e;
+      widen(q, k, gshift, b, e);
+      const uint32_t c = creator_of[k];
+      if (c != kNone) {
+        rn = c;
+        k1 = DB_MR_NEW;
+      } else if (role[k]) {
+        const uint32_t w = held[k];  // the least-positioned new record reaching e, made before k
+        const bool holds = w != kNone && nstart[w] <= b;
+        if (kd == DB_MR_MISS) {
+          if (holds) {
+            rn = w;
+            k1 = DB_MR_NEW_DUP;
+          } else {
+            atomicOr(&h->err, DB_ERR_TABLE_ORDER);  // cannot happen on a valid table
+          }
+        } else if (holds && nstart[w] < start[idx[k]]) {
+          rn = w;  // the new record comes before the old one in the table
+          k1 = DB_MR_NEW_DUP;
+        }
+      }
+      if (rn != kNone) atomicAdd(&nrefs[rn], 1u);
+      else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) atomicAdd(&more[idx[k]], 1u);
+    }
+    rec_new[k] = rn;
+    kind1[k] = k1;
   }
 }
 // Count of a[0..n) below x (strict) or at most x.
@@ -570,30 +1221,19 @@ __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
     p.npos[j] = (uint32_t)w;
   }
 }
-__global__ void reg_handles_hit(const uint8_t* kind0, const int32_t* idx, uint64_t n_q,
-                                const int64_t* remap, const RegHeader* h, uint64_t n,
-                                uint64_t o_cap, int64_t* handle, uint8_t* kind) {
+__global__ void reg_handles(const uint8_t* kind1, const int32_t* idx, const uint32_t* rec_new,
+                            uint64_t n_q, const int64_t* remap, const uint32_t* npos,
+                            const RegHeader* h, uint64_t n, uint64_t o_cap, int64_t* handle,
+                            uint8_t* kind) {
   kernel_prologue();
   const bool fits = n + h->u <= o_cap;
   FOR_EACH(k, n_q) {
-    const uint8_t kd = kind0[k];
-    if (kd == DB_MR_MISS) continue;
+    const uint8_t kd = kind1[k];
     kind[k] = kd;
     if (!fits) continue;
-    handle[k] = kd == DB_MR_INVALID ? -1 : remap[idx[k]];
-  }
-}
-__global__ void reg_handles_miss(const RegHeader* h, uint64_t n_max, uint64_t n, uint64_t o_cap,
-                                 const uint32_t* val, const uint32_t* flag, const uint32_t* excl,
-                                 const uint32_t* npos, int64_t* handle, uint8_t* kind) {
-  kernel_prologue();
-  const uint64_t m = h->m;
-  const bool fits = n + h->u <= o_cap;
-  FOR_EACH(i, n_max) {
-    if (i >= m) break;
-    const uint32_t k = val[i];
-    kind[k] = flag[i] ? DB_MR_NEW : DB_MR_NEW_DUP;
-    if (fits) handle[k] = npos[excl[i] + flag[i] - 1];
+    if (rec_new[k] != kNone) handle[k] = npos[rec_new[k]];
+    else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) handle[k] = remap[idx[k]];
+    else handle[k] = -1;  // invalid (or, on a table that breaks the order, unresolved)
   }
 }
 __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_counters* ctr) {
@@ -602,12 +1242,14 @@ __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_cou
   ctr->total = total;
   ctr->n_invalid = h->lookup.n_invalid;
   ctr->n_overflow = total > o_cap ? 1 : 0;
-  ctr->err = h->lookup.err;
+  ctr->err = h->lookup.err | h->err;
 }
 
 struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
-      diff, nstart, nend, nfirst, nrefs, npos, total;
+      diff, nstart, nend, nfirst, nrefs, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
+      ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, rec_new,
+      kind1, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -634,6 +1276,30 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.nfirst = take(q * 4);
   L.nrefs = take(q * 4);
   L.npos = take(q * 4);
+  L.first = take(q * 4);
+  L.cp = take(q * 4);
+  L.cb = take(q * 8);
+  L.creator_of = take(q * 4);
+  L.cend = take(q * 8);
+  L.pmax = take(q * 8);
+  L.bmax = take(ceil_div(q, kMaxScanThreads) * 8);
+  L.reach = take((n_mr ? n_mr : 1) * 8);
+  L.ce0 = take(q * 8);
+  L.ce1 = take(q * 8);
+  L.ck0 = take(q * 4);
+  L.ck1 = take(q * 4);
+  L.cq0 = take(q * 4);
+  L.cq1 = take(q * 4);
+  L.ca0 = take(q * 4);
+  L.ca1 = take(q * 4);
+  L.cpm_tile = take(q * 4);
+  L.cpm_tile1 = take(q * 4);
+  L.cmin = take(cdq_tiles(q) * 4);
+  L.cpm = take(cdq_tiles(q) * 4);
+  L.cpm1 = take(cdq_tiles(q) * 4);
+  L.held = take(q * 4);
+  L.rec_new = take(q * 4);
+  L.kind1 = take(q);
   L.total = o;
   return L;
 }
@@ -807,7 +1473,8 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
   int rc = 0;
   if (cudaMemsetAsync(h, 0, sizeof(RegHeader), s) != cudaSuccess ||
       (n_mr && cudaMemsetAsync(more, 0, n_mr * 4, s) != cudaSuccess) ||
-      (n_q && cudaMemsetAsync(nrefs, 0, n_q * 4, s) != cudaSuccess))
+      (n_q && cudaMemsetAsync(nrefs, 0, n_q * 4, s) != cudaSuccess) ||
+      (n_q && cudaMemsetAsync(at(L.creator_of), 0xFF, n_q * 4, s) != cudaSuccess))
     return launch_result();
   // 1. lookup against the table as it stands
   if (n_q) {
@@ -815,15 +1482,15 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                     &h->lookup, at(L.lookup), mr::workspace_bytes(n_mr), s, true,
                     (int)granule_shift);
     if (rc) return rc;
-    // 2. hits and misses
-    launch_dep(reg_mark, grid_for(n_q), kThreads, 0, s, kind0, idx, n_q, more, flag);
+    // 2. the misses, compacted in request order
+    launch_dep(reg_mark, grid_for(n_q), kThreads, 0, s, kind0, n_q, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->m, bsum, s))) return rc;
     launch_dep(reg_compact, grid_for(n_q), kThreads, 0, s,
                q, flag, pos, n_q, granule_shift, sb.key[0],
                sb.val[0]);
     if ((rc = launch_result())) return rc;
-    // 3. sort the misses by (start, end), stable in request order
+    // 3. sort the misses by (start ascending, end descending), stable in request order
     const int bits = 64 - (int)granule_shift;
     int cur = 0;
     if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
@@ -831,14 +1498,72 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                sb.key[cur]);
     if ((rc = launch_result())) return rc;
     if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
-    // 4. runs of equal ranges are the new records
+    // 4. distinct ranges; a range makes a record when no range that holds it
+    //    (one before it in this order reaching its end) was asked for earlier
     const uint32_t* sval = sb.val[cur];
+    uint64_t* db = sb.key[0];  // the sort keys are no longer needed
+    uint64_t* de = sb.key[1];
+    uint32_t* first = static_cast<uint32_t*>(at(L.first));
+    uint32_t* held = static_cast<uint32_t*>(at(L.held));
+    CdqBufs cb_{{static_cast<uint64_t*>(at(L.ce0)), static_cast<uint64_t*>(at(L.ce1))},
+                {static_cast<uint32_t*>(at(L.ck0)), static_cast<uint32_t*>(at(L.ck1))},
+                {static_cast<uint32_t*>(at(L.cq0)), static_cast<uint32_t*>(at(L.cq1))},
+                {static_cast<uint32_t*>(at(L.ca0)), static_cast<uint32_t*>(at(L.ca1))},
+                {static_cast<uint32_t*>(at(L.cpm_tile)), static_cast<uint32_t*>(at(L.cpm_tile1))},
+                static_cast<uint32_t*>(at(L.cmin)),
+                {static_cast<uint32_t*>(at(L.cpm)), static_cast<uint32_t*>(at(L.cpm1))}, n_q,
+                &h->err};
     launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag);
     if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->d, bsum, s))) return rc;
+    launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
+               pos, db, de, first, cb_.e[1], cb_.key[1], cb_.qid[1]);
+    if ((rc = launch_result())) return rc;
+    if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->d, cb_, held, s)))
+      return rc;
+    launch_dep(reg_creators, grid_for(n_q), kThreads, 0, s, h, n_q, first, held, flag);
+    if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->u, bsum, s))) return rc;
-    launch_dep(reg_new, grid_for(n_q), kThreads, 0, s,
-               q, h, n_q, granule_shift, sval, flag, pos, nstart,
-               nend, nfirst, nrefs);
+    uint32_t* cp = static_cast<uint32_t*>(at(L.cp));
+    uint64_t* cbs = static_cast<uint64_t*>(at(L.cb));
+    uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
+    uint64_t* cend = static_cast<uint64_t*>(at(L.cend));
+    uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
+    uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
+    uint64_t* reach = static_cast<uint64_t*>(at(L.reach));
+    launch_dep(reg_clist, grid_for(n_q), kThreads, 0, s, h, n_q, flag, pos, db, cp, cbs);
+    if ((rc = launch_result())) return rc;
+    // 5. the new records in table order; old records a new one may precede
+    launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, de, first, nstart,
+               nend, nfirst, creator_of, cend);
+    if ((rc = launch_result())) return rc;
+    const unsigned mblocks = (unsigned)ceil_div(n_q, kMaxScanThreads);
+    launch_dep(pmax_reduce, mblocks, kMaxScanThreads, 0, s, (const uint64_t*)cend,
+               (const uint32_t*)&h->u, bmax);
+    launch_dep(pmax_blocks, 1, 1024, 0, s, bmax, (const uint32_t*)&h->u);
+    launch_dep(pmax_apply, mblocks, kMaxScanThreads, 0, s, (const uint64_t*)cend,
+               (const uint32_t*)&h->u, (const uint64_t*)bmax, pmax);
+    if ((rc = launch_result())) return rc;
+    if (n_mr) {
+      launch_dep(reg_reach, grid_for(n_mr), kThreads, 0, s, (const RegHeader*)h,
+                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, reach);
+      if ((rc = launch_result())) return rc;
+    }
+    // 6. every request's record: the lowest-positioned one holding it when
+    //    it is made (an old one, or a new one made before it)
+    launch_dep(reg_roles, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
+               (const uint64_t*)reach, flag);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->nb, bsum, s))) return rc;
+    launch_dep(reg_items, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, flag, pos,
+               creator_of, cb_.e[1], cb_.key[1], cb_.qid[1]);
+    if ((rc = launch_result())) return rc;
+    if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->nb, cb_, held, s)))
+      return rc;
+    uint32_t* rec_new = static_cast<uint32_t*>(at(L.rec_new));
+    uint8_t* kind1 = static_cast<uint8_t*>(at(L.kind1));
+    launch_dep(reg_resolve, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
+               flag, creator_of, held, nstart, start, more, nrefs, rec_new, kind1, h);
     if ((rc = launch_result())) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
                    out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
@@ -848,14 +1573,9 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     }
     launch_dep(reg_place_new, grid_for(n_q), kThreads, 0, s, pp, n_q);
     if ((rc = launch_result())) return rc;
-    // 5. handles and kinds
-    launch_dep(reg_handles_hit, grid_for(n_q), kThreads, 0, s,
-               kind0, idx, n_q, remap, h, n_mr, out_cap,
-               handle, kind);
-    if ((rc = launch_result())) return rc;
-    launch_dep(reg_handles_miss, grid_for(n_q), kThreads, 0, s,
-               h, n_q, n_mr, out_cap, sval, flag, pos,
-               npos, handle, kind);
+    // 7. handles and kinds
+    launch_dep(reg_handles, grid_for(n_q), kThreads, 0, s, kind1, idx, rec_new, n_q, remap, npos,
+               h, n_mr, out_cap, handle, kind);
     if ((rc = launch_result())) return rc;
   } else if (n_mr) {
     // no requests: the table is copied through (and checked like a lookup would)

@@ -24,20 +24,20 @@
  * separate output arrays and `remap[i]`, the index record i has after the
  * batch (-1 once removed), so the caller can carry its handles forward.
  *
- * Batch reading of the pages' one-call-at-a-time operations:
+ * A batch gives the result of the pages' one-call-at-a-time operations
+ * applied to its requests in order:
  *  - Registration. Each request is widened to whole granules (4 KiB, or 64 KiB
- *    for the xNVMe registry) and looked up in the table as it stood before
- *    the batch. A hit takes one more reference on the lowest-index record
- *    holding it (kind DB_MR_EXACT or DB_MR_CONTAINED). The requests that miss
- *    become one new record per distinct widened range (DB_MR_NEW for the
- *    range's first request, DB_MR_NEW_DUP for its repeats), with as many
- *    references as requests and the new_lkey of its first request. A new
- *    record goes after every old record with the same start, and new records
- *    are in (start, end) order among themselves. This equals registering the
- *    requests one call at a time whenever no new range of the batch lies
- *    inside another new range or holds a hit's range ahead of its old record
- *    (then the later request would have been a hit); a caller that needs the
- *    per-call result for such requests issues them in separate batches.
+ *    for the xNVMe registry) and looked up in the table as the requests
+ *    before it in the batch left it: the old records and the records those
+ *    requests created, in table order (start; an old record before a new one
+ *    of the same start; new records of one start in the order they were
+ *    made). The lowest-index record holding it takes one more reference:
+ *    an old record (kind DB_MR_EXACT or DB_MR_CONTAINED) or one an earlier
+ *    request of the batch created (DB_MR_NEW_DUP, whether the same range, a
+ *    wider one, or one that starts before the old record that also holds
+ *    it). A request that no record holds creates a record with one
+ *    reference and its new_lkey (DB_MR_NEW), placed after every record
+ *    starting at or before it.
  *  - Deregistration, in batch order: each handle drops one reference of its
  *    record; the handle that drops the last one releases the record
  *    (DB_DEREG_RELEASED); a handle naming no record or a released one is
@@ -56,8 +56,8 @@
 extern "C" {
 #endif
 
-#define DB_MR_NEW 4u     /* the request made a new record                 */
-#define DB_MR_NEW_DUP 5u /* same range as an earlier new record of the batch */
+#define DB_MR_NEW 4u     /* the request made a new record                                 */
+#define DB_MR_NEW_DUP 5u /* a hit on a record an earlier request of the batch made        */
 
 #define DB_DEREG_OK 0u       /* one reference dropped                      */
 #define DB_DEREG_RELEASED 1u /* the last reference: the record is removed  */

@@ -83,6 +83,13 @@ def same(got, want, keys):
 
 
 REG_KEYS = ("start", "end", "lkey", "refs", "handle", "kind", "remap", "ctr")
+
+
+def one_at_a_time(oracle, *args, **kw):
+    """The oracle's one-at-a-time registration (the pages' definition),
+    computed with its index; the tests of the oracle pin that equal to the
+    plain scan."""
+    return oracle.mr_register(*args, one_at_a_time=True, indexed=True, **kw)
 DEREG_KEYS = ("start", "end", "lkey", "refs", "remap", "status", "ctr")
 
 
@@ -100,11 +107,15 @@ def test_page_experiment(db, oracle):
     d = deregister(db, dr["handles"], *t)
     assert d["status"].tolist() == dr["status"] and d["remap"].tolist() == dr["remap"]
     assert d["refs"].tolist() == [1] and d["ctr"].tolist() == [1, 1, 0, 0]
-    one = fx["one_batch_reading"]
+    # The same registrations as one batch give the page's table: one record
+    # with three references, and the disjoint one.
+    one = fx["one_batch"]
     q = np.array([[base + h(c["off"]), c["size"]] for c in fx["register_calls"]], np.uint64)
     r = register(db, q, [c["new_lkey"] for c in fx["register_calls"]], *EMPTY)
     assert r["kind"].tolist() == one["kind"] and r["handle"].tolist() == one["handle"]
-    assert [int(x) - base for x in r["end"]] == [h(x["end"]) for x in one["table_after"]]
+    assert [(int(a) - base, int(b) - base, int(k), int(n))
+            for a, b, k, n in zip(r["start"], r["end"], r["lkey"], r["refs"])] == \
+        [(h(x["start"]), h(x["end"]), x["lkey"], x["refs"]) for x in one["table_after"]]
 
 
 def random_case(rng, n, m, span, granule_shift):
@@ -140,12 +151,46 @@ def test_register_against_the_oracle(db, oracle, n, m, span, granule_shift):
     overlapping, repeated and invalid; several tiles of the sort."""
     rng = np.random.default_rng(n * 7 + m + granule_shift)
     q, nl, s, e, lk, refs = random_case(rng, n, m, span, granule_shift)
-    want = oracle.mr_register(q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs, granule_shift=granule_shift)
     got = register(db, q, nl, s, e, lk, refs, granule_shift=granule_shift)
     same(got, want, REG_KEYS)
     kinds = set(want["kind"].tolist())
     if m >= 300:
         assert {3, 4, 5} <= kinds and (n == 0 or {1, 2} & kinds)
+
+
+@pytest.mark.parametrize("m,pages,granule_shift", [(700, 40, 12), (5000, 300, 12),
+                                                    (150000, 3000, 12), (400000, 100000, 12),
+                                                    (60000, 2000, 16)])
+def test_register_nesting_in_one_batch(db, oracle, m, pages, granule_shift):
+    """Requests over a few pages, so that new ranges lie inside earlier new
+    ranges of the batch, repeat them, end where they end, and wrap old
+    records whose hits they then take (a new record that starts before the
+    old one): the one-at-a-time result, on every output."""
+    rng = np.random.default_rng(m + pages + granule_shift)
+    g = 1 << granule_shift
+    n = max(1, pages // 20)
+    s = np.sort(rng.integers(0, pages, size=n)).astype(np.uint64) * np.uint64(g)
+    e = s + rng.integers(1, 12, size=n).astype(np.uint64) * np.uint64(g)
+    lk = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    refs = rng.integers(1, 4, size=n).astype(np.uint32)
+    a = rng.integers(0, pages, size=m).astype(np.uint64) * np.uint64(g)
+    a += rng.integers(0, g, size=m).astype(np.uint64) * (rng.random(m) < 0.3)
+    sz = rng.integers(1, 16 * g, size=m).astype(np.uint64)
+    wide = rng.random(m) < 0.05            # a few wide ranges that hold many others
+    sz = np.where(wide, rng.integers(16 * g, 400 * g, size=m).astype(np.uint64), sz)
+    rep = rng.random(m) < 0.1
+    src = rng.integers(0, m, size=m)
+    a = np.where(rep & (src < np.arange(m)), a[src], a)
+    sz = np.where(rep & (src < np.arange(m)), sz[src], sz)
+    sz[::23] = 0
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = rng.integers(0, 2**32, size=m, dtype=np.uint64).astype(np.uint32)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    kinds = want["kind"]
+    assert (kinds == 5).sum() > 0 and (kinds == 4).sum() > 0
+    got = register(db, q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    same(got, want, REG_KEYS)
 
 
 @pytest.mark.parametrize("pattern", ["all_same", "digit_2", "digits_0_3", "digits_5_6",
@@ -183,7 +228,7 @@ def test_register_sort_digit_patterns(db, oracle, pattern, granule_shift):
     e = s + np.uint64(g)
     lk = np.arange(8, dtype=np.uint32)
     refs = np.ones(8, np.uint32)
-    want = oracle.mr_register(q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs, granule_shift=granule_shift)
     got = register(db, q, nl, s, e, lk, refs, granule_shift=granule_shift)
     same(got, want, REG_KEYS)
 
@@ -209,8 +254,8 @@ def test_register_empty_batch_and_capacity(db, oracle):
     rng = np.random.default_rng(3)
     q, nl, s, e, lk, refs = random_case(rng, 50, 400, 400, 12)
     got = register(db, q[:0], nl[:0], s, e, lk, refs)
-    same(got, oracle.mr_register(q[:0], nl[:0], s, e, lk, refs), REG_KEYS)
-    want = oracle.mr_register(q, nl, s, e, lk, refs)
+    same(got, one_at_a_time(oracle, q[:0], nl[:0], s, e, lk, refs), REG_KEYS)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs)
     total = int(want["ctr"][0])
     small = register(db, q, nl, s, e, lk, refs, out_cap=total - 1)
     assert small["ctr"].tolist() == [total, int(want["ctr"][1]), 1, 0]
@@ -228,13 +273,13 @@ def test_register_unsorted_table_is_flagged(db):
 
 
 def test_register_full_size(db, oracle):
-    """16,777,216 requests against 1,048,576 records (a fifth miss and
-    become about 3.35 M new records)."""
+    """16,777,216 requests against 1,048,576 records: a fifth miss the table,
+    and many of those lie inside an earlier one of the batch."""
     import synth
     d = synth.mr_register()
     args = (d["queries"], d["new_lkey"], d["mr_start"], d["mr_end"], d["mr_lkey"], d["mr_refs"])
     got = register(db, *args)
-    want = oracle.mr_register(*args)
+    want = one_at_a_time(oracle, *args)
     same(got, want, REG_KEYS)
 
 
@@ -269,7 +314,7 @@ def test_a_cache_over_several_batches(db, oracle):
     t_gpu = t_cpu = (s, e, lk, refs)
     for step in range(3):
         r = register(db, q, nl, *t_gpu)
-        w = oracle.mr_register(q, nl, *t_cpu)
+        w = one_at_a_time(oracle, q, nl, *t_cpu)
         same(r, w, REG_KEYS)
         t_gpu = (r["start"], r["end"], r["lkey"], r["refs"])
         t_cpu = (w["start"], w["end"], w["lkey"], w["refs"])

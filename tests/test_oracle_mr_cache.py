@@ -65,9 +65,12 @@ def test_page_experiment_as_one_batch(oracle):
     assert r["kind"].tolist() == one["kind"] and r["handle"].tolist() == one["handle"]
     assert rows_of(r, base) == [(h(x["start"]), h(x["end"]), x["lkey"], x["refs"])
                                 for x in one["table_after"]]
-    s = oracle.mr_register(q, lk, *EMPTY, one_at_a_time=True)
-    assert s["handle"].tolist() == [c["handle"] for c in calls[:3]] + [1]
-    assert s["refs"].tolist() == [3, 1]
+    want = fx["one_batch"]
+    for indexed in (False, True):
+        s = oracle.mr_register(q, lk, *EMPTY, one_at_a_time=True, indexed=indexed)
+        assert s["kind"].tolist() == want["kind"] and s["handle"].tolist() == want["handle"]
+        assert rows_of(s, base) == [(h(x["start"]), h(x["end"]), x["lkey"], x["refs"])
+                                    for x in want["table_after"]]
 
 
 @pytest.mark.parametrize("addr,size,base,end", [
