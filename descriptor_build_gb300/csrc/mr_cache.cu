@@ -537,65 +537,65 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_tile(const uint64_t* e_in,
   const uint64_t n = *n_dev;
   for (uint64_t t0 = (uint64_t)blockIdx.x * kCdqTile; t0 < n;
        t0 += (uint64_t)gridDim.x * kCdqTile) {
-  const uint32_t nt = (uint32_t)(n - t0 < kCdqTile ? n - t0 : kCdqTile);
-  for (uint32_t x = threadIdx.x; x < nt; x += kCdqThreads) {
-    se[x] = e_in[t0 + x];
-    sk[x] = key_in[t0 + x];
-    sq[x] = qid_in[t0 + x];
-    sa[x] = kNone;
-    ord0[x] = (uint16_t)x;
-    pm[x] = sk[x];
-  }
-  __syncthreads();
-  int cur = 0;
-  for (uint32_t s = 1; s < nt; s <<= 1) {
-    // place every item in the merge of its run with the neighbouring one
-    const uint16_t* oc = cur ? ord1 : ord0;
-    uint16_t* on = cur ? ord0 : ord1;
-#pragma unroll
-    for (int u = 0; u < kCdqPer; ++u) {
-      const uint32_t i = threadIdx.x * kCdqPer + u;
-      if (i >= nt) continue;
-      const uint32_t x = oc[i];
-      const uint64_t ex = se[x];
-      const uint32_t r = i / s, pb = (r & ~1u) * s;
-      uint32_t pos;
-      if ((r & 1u) == 0) {  // left run: after the right run's items with a greater end
-        uint32_t lo = pb + s < nt ? pb + s : nt, hi = pb + 2 * s < nt ? pb + 2 * s : nt;
-        const uint32_t base = lo;
-        while (lo < hi) {
-          const uint32_t mid = (lo + hi) >> 1;
-          if (se[oc[mid]] > ex) lo = mid + 1;
-          else hi = mid;
-        }
-        pos = (i - pb) + (lo - base);
-      } else {  // right run: after the left run's items with an end at least its own
-        uint32_t lo = pb, hi = pb + s;
-        while (lo < hi) {
-          const uint32_t mid = (lo + hi) >> 1;
-          if (se[oc[mid]] >= ex) lo = mid + 1;
-          else hi = mid;
-        }
-        const uint32_t cnt = lo - pb;
-        if (sq[x] != kNone && cnt > 0) sa[x] = min(sa[x], pm[pb + cnt - 1]);
-        pos = (i - pb - s) + cnt;
-      }
-      on[pb + pos] = (uint16_t)x;
+    const uint32_t nt = (uint32_t)(n - t0 < kCdqTile ? n - t0 : kCdqTile);
+    for (uint32_t x = threadIdx.x; x < nt; x += kCdqThreads) {
+      se[x] = e_in[t0 + x];
+      sk[x] = key_in[t0 + x];
+      sq[x] = qid_in[t0 + x];
+      sa[x] = kNone;
+      ord0[x] = (uint16_t)x;
+      pm[x] = sk[x];
     }
     __syncthreads();
-    cur ^= 1;
-    seg_prefix_min(sk, cur ? ord1 : ord0, nt, 2 * s, pm, s_w);
-  }
-  for (uint32_t i = threadIdx.x; i < nt; i += kCdqThreads) {
-    const uint32_t x = (cur ? ord1 : ord0)[i];
-    b.e[0][t0 + i] = se[x];
-    b.key[0][t0 + i] = sk[x];
-    b.qid[0][t0 + i] = sq[x];
-    b.ans[0][t0 + i] = sa[x];
-    b.pm[0][t0 + i] = pm[i];
-  }
-  if (threadIdx.x == 0) b.cpm[0][t0 / kCdqTile] = kNone;  // a tile is its whole run
-  __syncthreads();  // shared memory is reused by the next tile
+    int cur = 0;
+    for (uint32_t s = 1; s < nt; s <<= 1) {
+      // place every item in the merge of its run with the neighbouring one
+      const uint16_t* oc = cur ? ord1 : ord0;
+      uint16_t* on = cur ? ord0 : ord1;
+  #pragma unroll
+      for (int u = 0; u < kCdqPer; ++u) {
+        const uint32_t i = threadIdx.x * kCdqPer + u;
+        if (i >= nt) continue;
+        const uint32_t x = oc[i];
+        const uint64_t ex = se[x];
+        const uint32_t r = i / s, pb = (r & ~1u) * s;
+        uint32_t pos;
+        if ((r & 1u) == 0) {  // left run: after the right run's items with a greater end
+          uint32_t lo = pb + s < nt ? pb + s : nt, hi = pb + 2 * s < nt ? pb + 2 * s : nt;
+          const uint32_t base = lo;
+          while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (se[oc[mid]] > ex) lo = mid + 1;
+            else hi = mid;
+          }
+          pos = (i - pb) + (lo - base);
+        } else {  // right run: after the left run's items with an end at least its own
+          uint32_t lo = pb, hi = pb + s;
+          while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (se[oc[mid]] >= ex) lo = mid + 1;
+            else hi = mid;
+          }
+          const uint32_t cnt = lo - pb;
+          if (sq[x] != kNone && cnt > 0) sa[x] = min(sa[x], pm[pb + cnt - 1]);
+          pos = (i - pb - s) + cnt;
+        }
+        on[pb + pos] = (uint16_t)x;
+      }
+      __syncthreads();
+      cur ^= 1;
+      seg_prefix_min(sk, cur ? ord1 : ord0, nt, 2 * s, pm, s_w);
+    }
+    for (uint32_t i = threadIdx.x; i < nt; i += kCdqThreads) {
+      const uint32_t x = (cur ? ord1 : ord0)[i];
+      b.e[0][t0 + i] = se[x];
+      b.key[0][t0 + i] = sk[x];
+      b.qid[0][t0 + i] = sq[x];
+      b.ans[0][t0 + i] = sa[x];
+      b.pm[0][t0 + i] = pm[i];
+    }
+    if (threadIdx.x == 0) b.cpm[0][t0 / kCdqTile] = kNone;  // a tile is its whole run
+    __syncthreads();  // shared memory is reused by the next tile
   }
 }
 
@@ -648,115 +648,115 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
   if (len >= n) return;  // this level is not needed
   for (uint64_t o0 = (uint64_t)blockIdx.x * kCdqTile; o0 < n;
        o0 += (uint64_t)gridDim.x * kCdqTile) {
-  const uint64_t o1 = o0 + kCdqTile < n ? o0 + kCdqTile : n;
-  const bool odd = (level & 1u) != 0;  // input buffer 1, output 0
-  const uint64_t* E = odd ? b.e[1] : b.e[0];
-  const uint32_t* Kin = odd ? b.key[1] : b.key[0];
-  const uint32_t* Qin = odd ? b.qid[1] : b.qid[0];
-  const uint32_t* Ain = odd ? b.ans[1] : b.ans[0];
-  const uint32_t* PMin = odd ? b.pm[1] : b.pm[0];
-  const uint32_t* CPMin = odd ? b.cpm[1] : b.cpm[0];
-  uint64_t* Eo = odd ? b.e[0] : b.e[1];
-  uint32_t* Ko = odd ? b.key[0] : b.key[1];
-  uint32_t* Qo = odd ? b.qid[0] : b.qid[1];
-  uint32_t* Ao = odd ? b.ans[0] : b.ans[1];
-  uint32_t* PMo = odd ? b.pm[0] : b.pm[1];
-  const uint64_t pb = o0 / (2 * len) * (2 * len);
-  const uint64_t nL = pb + len < n ? len : n - pb;
-  const uint64_t rb = pb + nL;
-  const uint64_t nR = pb + 2 * len < n ? len : n - rb;
-  const uint64_t d0 = o0 - pb, d1 = o1 - pb;
-  if (threadIdx.x < 32) {
-    const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d0);
-    if (threadIdx.x == 0) s_i0 = i;
-  } else if (threadIdx.x < 64) {
-    const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d1);
-    if (threadIdx.x == 32) s_i1 = i;
-  }
-  __syncthreads();
-  const uint64_t i0 = s_i0, i1 = s_i1, j0 = d0 - i0, j1 = d1 - i1;
-  // A slice pair that is not a split of this tile (impossible for sorted
-  // runs) is reported and the tile left unwritten.
-  if (i1 < i0 || i1 > nL || j0 > d0 || j1 < j0 || j1 > nR) {
-    if (threadIdx.x == 0) atomicOr(b.err, DB_ERR_TABLE_ORDER);
+    const uint64_t o1 = o0 + kCdqTile < n ? o0 + kCdqTile : n;
+    const bool odd = (level & 1u) != 0;  // input buffer 1, output 0
+    const uint64_t* E = odd ? b.e[1] : b.e[0];
+    const uint32_t* Kin = odd ? b.key[1] : b.key[0];
+    const uint32_t* Qin = odd ? b.qid[1] : b.qid[0];
+    const uint32_t* Ain = odd ? b.ans[1] : b.ans[0];
+    const uint32_t* PMin = odd ? b.pm[1] : b.pm[0];
+    const uint32_t* CPMin = odd ? b.cpm[1] : b.cpm[0];
+    uint64_t* Eo = odd ? b.e[0] : b.e[1];
+    uint32_t* Ko = odd ? b.key[0] : b.key[1];
+    uint32_t* Qo = odd ? b.qid[0] : b.qid[1];
+    uint32_t* Ao = odd ? b.ans[0] : b.ans[1];
+    uint32_t* PMo = odd ? b.pm[0] : b.pm[1];
+    const uint64_t pb = o0 / (2 * len) * (2 * len);
+    const uint64_t nL = pb + len < n ? len : n - pb;
+    const uint64_t rb = pb + nL;
+    const uint64_t nR = pb + 2 * len < n ? len : n - rb;
+    const uint64_t d0 = o0 - pb, d1 = o1 - pb;
+    if (threadIdx.x < 32) {
+      const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d0);
+      if (threadIdx.x == 0) s_i0 = i;
+    } else if (threadIdx.x < 64) {
+      const uint64_t i = corank_warp(E + pb, nL, E + rb, nR, d1);
+      if (threadIdx.x == 32) s_i1 = i;
+    }
     __syncthreads();
-    continue;
-  }
-  const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0);
-  for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads)
-    seg[x] = x < na ? E[pb + i0 + x] : E[rb + j0 + (x - na)];
-  __syncthreads();
-  const uint64_t* sl = seg;
-  const uint64_t* sr = seg + na;
-  for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads) {
-    const bool from_left = x < na;
-    const uint64_t ex = seg[x];
-    uint32_t lo = 0, hi = from_left ? nb : na;
-    const uint64_t* o = from_left ? sr : sl;
-    while (lo < hi) {  // other-slice items ahead of this one
-      const uint32_t mid = (lo + hi) >> 1;
-      const uint64_t v = o[mid];
-      if (v > ex || (!from_left && v == ex)) lo = mid + 1;
-      else hi = mid;
-    }
-    const uint64_t gi = from_left ? pb + i0 + x : rb + j0 + (x - na);
-    const uint32_t q = Qin[gi];
-    uint32_t a = Ain[gi];
-    if (!from_left && q != kNone) {
-      const uint64_t c = i0 + lo;  // left-run items with an end at least ex
-      if (c > 0) {
-        const uint64_t j = pb + c - 1;
-        a = min(a, min(PMin[j], CPMin[j / kCdqTile]));
-      }
-    }
-    const uint32_t pos = (from_left ? x : x - na) + lo;
-    if (pos >= na + nb) {  // impossible for sorted slices; reported, not written
-      atomicOr(b.err, DB_ERR_TABLE_ORDER);
+    const uint64_t i0 = s_i0, i1 = s_i1, j0 = d0 - i0, j1 = d1 - i1;
+    // A slice pair that is not a split of this tile (impossible for sorted
+    // runs) is reported and the tile left unwritten.
+    if (i1 < i0 || i1 > nL || j0 > d0 || j1 < j0 || j1 > nR) {
+      if (threadIdx.x == 0) atomicOr(b.err, DB_ERR_TABLE_ORDER);
+      __syncthreads();
       continue;
     }
-    oe[pos] = ex;
-    ok[pos] = Kin[gi];
-    oq[pos] = q;
-    oa[pos] = a;
-  }
-  __syncthreads();
-  // write the tile out with its prefix minima of the keys
-  const uint32_t nt = (uint32_t)(o1 - o0);
-  const uint32_t base = threadIdx.x * kCdqPer;
-  uint32_t v[kCdqPer];
-  uint32_t run = kNone;
-#pragma unroll
-  for (int u = 0; u < kCdqPer; ++u) {
-    run = min(run, base + u < nt ? ok[base + u] : kNone);
-    v[u] = run;
-  }
-  const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = run;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, x, o);
-    if (lane >= (uint32_t)o) x = min(x, y);
-  }
-  if (lane == 31) s_w[warp] = x;
-  const uint32_t up = __shfl_up_sync(kFull, x, 1);
-  __syncthreads();
-  uint32_t before = lane ? up : kNone;
-  for (uint32_t w = 0; w < warp; ++w) before = min(before, s_w[w]);
-  for (uint32_t t = threadIdx.x; t < nt; t += kCdqThreads) {
-    Eo[o0 + t] = oe[t];
-    Ko[o0 + t] = ok[t];
-    Qo[o0 + t] = oq[t];
-    Ao[o0 + t] = oa[t];
-  }
-#pragma unroll
-  for (int u = 0; u < kCdqPer; ++u)
-    if (base + u < nt) PMo[o0 + base + u] = min(before, v[u]);
-  if (threadIdx.x == kCdqThreads - 1) {
-    uint32_t all = kNone;
-    for (int w = 0; w < kCdqThreads / 32; ++w) all = min(all, s_w[w]);
-    b.cmin[o0 / kCdqTile] = all;
-  }
-  __syncthreads();  // shared memory is reused by the next tile
+    const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0);
+    for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads)
+      seg[x] = x < na ? E[pb + i0 + x] : E[rb + j0 + (x - na)];
+    __syncthreads();
+    const uint64_t* sl = seg;
+    const uint64_t* sr = seg + na;
+    for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads) {
+      const bool from_left = x < na;
+      const uint64_t ex = seg[x];
+      uint32_t lo = 0, hi = from_left ? nb : na;
+      const uint64_t* o = from_left ? sr : sl;
+      while (lo < hi) {  // other-slice items ahead of this one
+        const uint32_t mid = (lo + hi) >> 1;
+        const uint64_t v = o[mid];
+        if (v > ex || (!from_left && v == ex)) lo = mid + 1;
+        else hi = mid;
+      }
+      const uint64_t gi = from_left ? pb + i0 + x : rb + j0 + (x - na);
+      const uint32_t q = Qin[gi];
+      uint32_t a = Ain[gi];
+      if (!from_left && q != kNone) {
+        const uint64_t c = i0 + lo;  // left-run items with an end at least ex
+        if (c > 0) {
+          const uint64_t j = pb + c - 1;
+          a = min(a, min(PMin[j], CPMin[j / kCdqTile]));
+        }
+      }
+      const uint32_t pos = (from_left ? x : x - na) + lo;
+      if (pos >= na + nb) {  // impossible for sorted slices; reported, not written
+        atomicOr(b.err, DB_ERR_TABLE_ORDER);
+        continue;
+      }
+      oe[pos] = ex;
+      ok[pos] = Kin[gi];
+      oq[pos] = q;
+      oa[pos] = a;
+    }
+    __syncthreads();
+    // write the tile out with its prefix minima of the keys
+    const uint32_t nt = (uint32_t)(o1 - o0);
+    const uint32_t base = threadIdx.x * kCdqPer;
+    uint32_t v[kCdqPer];
+    uint32_t run = kNone;
+  #pragma unroll
+    for (int u = 0; u < kCdqPer; ++u) {
+      run = min(run, base + u < nt ? ok[base + u] : kNone);
+      v[u] = run;
+    }
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = run;
+  #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= (uint32_t)o) x = min(x, y);
+    }
+    if (lane == 31) s_w[warp] = x;
+    const uint32_t up = __shfl_up_sync(kFull, x, 1);
+    __syncthreads();
+    uint32_t before = lane ? up : kNone;
+    for (uint32_t w = 0; w < warp; ++w) before = min(before, s_w[w]);
+    for (uint32_t t = threadIdx.x; t < nt; t += kCdqThreads) {
+      Eo[o0 + t] = oe[t];
+      Ko[o0 + t] = ok[t];
+      Qo[o0 + t] = oq[t];
+      Ao[o0 + t] = oa[t];
+    }
+  #pragma unroll
+    for (int u = 0; u < kCdqPer; ++u)
+      if (base + u < nt) PMo[o0 + base + u] = min(before, v[u]);
+    if (threadIdx.x == kCdqThreads - 1) {
+      uint32_t all = kNone;
+      for (int w = 0; w < kCdqThreads / 32; ++w) all = min(all, s_w[w]);
+      b.cmin[o0 / kCdqTile] = all;
+    }
+    __syncthreads();  // shared memory is reused by the next tile
   }
 }
 
