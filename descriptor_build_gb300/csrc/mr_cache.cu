@@ -856,7 +856,8 @@ struct RegHeader {   // 256 bytes at the start of the registration workspace
   uint32_t d;        // distinct ranges among the misses
   uint32_t nb;       // items of the second dominance pass (new records and queries)
   unsigned int err;  // an inconsistency the passes found (DB_ERR_TABLE_ORDER)
-  uint32_t pad[3];
+  uint32_t dk;       // distinct ranges the first dominance pass needs
+  uint32_t pad[2];
   db_counters lookup;  // counters of the lookup pass
 };
 
@@ -914,15 +915,11 @@ __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, 
     flag[i] = f;
   }
 }
-// The distinct missed ranges, in (start ascending, end descending) order,
-// as items of the first dominance pass: a range's end, and the request that
-// first asked for it (its key and first[]); each is a query for the least
-// first request among the ranges before it that reach its end -- the ranges
-// that hold it.
+// The distinct missed ranges, in (start ascending, end descending) order:
+// start, end and the request that first asked for it.
 __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_max,
                              uint32_t gshift, const uint32_t* val, const uint32_t* flag,
-                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first,
-                             uint64_t* ce_in, uint32_t* ck_in, uint32_t* cq_in) {
+                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first) {
   kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
@@ -934,9 +931,43 @@ __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_m
     db[p] = b;
     de[p] = e;
     first[p] = val[i];
-    ce_in[p] = e;
-    ck_in[p] = val[i];
-    cq_in[p] = p;
+  }
+}
+// Items of the first dominance pass: a distinct range is a query for the
+// least first request among the ranges before it that reach its end (the
+// ranges that hold it) and a point keyed by its own first request. A range
+// that nothing before it reaches (prefix maximum of the ends, pm) is held by
+// none; one before which the next range starts at or past its end holds
+// none: such a range takes no part (held[] = none), and the rest keep their
+// order. keep[] is 1 for the others.
+__global__ void reg_keep_a(const RegHeader* h, uint64_t n_max, const uint64_t* db,
+                           const uint64_t* de, const uint64_t* pm, uint32_t* held,
+                           uint32_t* keep) {
+  kernel_prologue();
+  const uint64_t d = h->d;
+  FOR_EACH(p, n_max) {
+    uint32_t k = 0;
+    if (p < d) {
+      const bool nested = p > 0 && pm[p - 1] >= de[p];
+      const bool holds = p + 1 < d && db[p + 1] < de[p];
+      k = (nested || holds) ? 1u : 0u;
+      held[p] = kNone;
+    }
+    keep[p] = k;
+  }
+}
+__global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* keep,
+                            const uint32_t* kpos, const uint64_t* de, const uint32_t* first,
+                            uint64_t* ce_in, uint32_t* ck_in, uint32_t* cq_in) {
+  kernel_prologue();
+  const uint64_t d = h->d;
+  FOR_EACH(p, n_max) {
+    if (p >= d) break;
+    if (!keep[p]) continue;
+    const uint32_t at = kpos[p];
+    ce_in[at] = de[p];
+    ck_in[at] = first[p];
+    cq_in[at] = (uint32_t)p;
   }
 }
 // A distinct range makes a new record when no range before it that holds it
@@ -1113,6 +1144,14 @@ __global__ void __launch_bounds__(kMaxScanThreads) pmax_apply(const uint64_t* in
   uint64_t before = bmax[blockIdx.x];
   for (int w = 0; w < warp; ++w) before = before > s_w[w] ? before : s_w[w];
   if (i < n) out[i] = before > x ? before : x;
+}
+int prefix_max(const uint64_t* in, const uint32_t* n_dev, uint64_t n_max, uint64_t* bmax,
+               uint64_t* out, cudaStream_t s) {
+  const unsigned blocks = (unsigned)ceil_div(n_max ? n_max : 1, kMaxScanThreads);
+  launch_dep(pmax_reduce, blocks, kMaxScanThreads, 0, s, in, n_dev, bmax);
+  launch_dep(pmax_blocks, 1, 1024, 0, s, bmax, n_dev);
+  launch_dep(pmax_apply, blocks, kMaxScanThreads, 0, s, in, n_dev, (const uint64_t*)bmax, out);
+  return launch_result();
 }
 __global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, const uint32_t* role,
                           const uint32_t* rpos, const uint32_t* creator_of, uint64_t* ce_in,
@@ -1517,9 +1556,20 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->d, bsum, s))) return rc;
     launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
-               pos, db, de, first, cb_.e[1], cb_.key[1], cb_.qid[1]);
+               pos, db, de, first);
     if ((rc = launch_result())) return rc;
-    if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->d, cb_, held, s)))
+    uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
+    uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
+    if ((rc = prefix_max(de, &h->d, n_q, bmax, pmax, s))) return rc;
+    launch_dep(reg_keep_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
+               (const uint64_t*)db, (const uint64_t*)de, (const uint64_t*)pmax, held, flag);
+    if ((rc = launch_result())) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->dk, bsum, s))) return rc;
+    launch_dep(reg_items_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
+               (const uint32_t*)flag, (const uint32_t*)pos, (const uint64_t*)de,
+               (const uint32_t*)first, cb_.e[1], cb_.key[1], cb_.qid[1]);
+    if ((rc = launch_result())) return rc;
+    if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->dk, cb_, held, s)))
       return rc;
     launch_dep(reg_creators, grid_for(n_q), kThreads, 0, s, h, n_q, first, held, flag);
     if ((rc = launch_result())) return rc;
@@ -1528,8 +1578,6 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     uint64_t* cbs = static_cast<uint64_t*>(at(L.cb));
     uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
     uint64_t* cend = static_cast<uint64_t*>(at(L.cend));
-    uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
-    uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
     uint64_t* reach = static_cast<uint64_t*>(at(L.reach));
     launch_dep(reg_clist, grid_for(n_q), kThreads, 0, s, h, n_q, flag, pos, db, cp, cbs);
     if ((rc = launch_result())) return rc;
@@ -1537,13 +1585,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, de, first, nstart,
                nend, nfirst, creator_of, cend);
     if ((rc = launch_result())) return rc;
-    const unsigned mblocks = (unsigned)ceil_div(n_q, kMaxScanThreads);
-    launch_dep(pmax_reduce, mblocks, kMaxScanThreads, 0, s, (const uint64_t*)cend,
-               (const uint32_t*)&h->u, bmax);
-    launch_dep(pmax_blocks, 1, 1024, 0, s, bmax, (const uint32_t*)&h->u);
-    launch_dep(pmax_apply, mblocks, kMaxScanThreads, 0, s, (const uint64_t*)cend,
-               (const uint32_t*)&h->u, (const uint64_t*)bmax, pmax);
-    if ((rc = launch_result())) return rc;
+    if ((rc = prefix_max(cend, &h->u, n_q, bmax, pmax, s))) return rc;
     if (n_mr) {
       launch_dep(reg_reach, grid_for(n_mr), kThreads, 0, s, (const RegHeader*)h,
                  (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, reach);
