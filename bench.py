@@ -580,8 +580,9 @@ def _time_dereg(args, device, stream, db, synth, t, d64, d32, peak) -> dict:
                             "records_before": n, "records_after": c[0], "stale": c[1],
                             "algorithmic_bytes": alg, "GB_per_s": round(gbs, 1),
                             "frac_of_peak": round(gbs / peak, 4),
-                            "note": "not part of the step: timed alone; 3 radix passes + "
-                                    "runs + compaction"}}
+                            "note": "not part of the step: timed alone; per-record counts, "
+                                    "buckets of the contested records, statuses, "
+                                    "compaction"}}
 
 
 def time_cq_mirror(args, device) -> dict:

@@ -8,23 +8,27 @@
 // the ncclCommRegister experiment; xNVMe "uPCIe CUDA" backend page
 // (xnvme_buf_register: whole 64 KiB device pages, refcounted).
 //
-// Registration, all on the caller's stream, no host round trip:
+// Registration, all on the caller's stream, no host round trip, gives the
+// result of the batch's requests made one at a time in batch order:
 //   1. the MR lookup (overlap path, 4 KiB or 64 KiB granules) classifies
 //      every request against the table before the batch;
-//   2. hits add to a per-record reference count (atomics); misses are
-//      flagged and compacted by an exclusive scan into (key, request) pairs;
-//   3. a stable LSD radix sort orders the misses by widened end, then by
-//      widened start (8-bit digits; reduce-then-scan over 4,096-key tiles,
-//      in-tile ranks from __match_any_sync), so equal ranges are adjacent
-//      and in request order;
-//   4. run starts give the new records (a scan numbers them); each old and
-//      new record finds its place in the merged table by a binary search in
-//      the other list (old records first on equal starts);
-//   5. handles, kinds, remap and counters.
-// Deregistration: handles are sorted by record (same radix sort, stable), so
-// a handle's rank among those naming its record is its batch-order rank; the
-// first refs of them drop references, the refs-th releases, the rest are
-// stale; survivors are compacted by a scan.
+//   2. the misses are flagged and compacted by an exclusive scan;
+//   3. a stable LSD radix sort (8-bit digits, reduce-then-scan over
+//      4,096-key tiles, in-tile ranks from __match_any_sync) orders them by
+//      widened start ascending, then end descending, so equal ranges are
+//      adjacent and in request order;
+//   4. a distinct range makes a new record unless a range before it in that
+//      order that reaches its end (one that holds it) was asked for earlier:
+//      a dominance pass (a merge sort on the end carrying prefix minima of
+//      the first request) gives each range the earliest request among the
+//      ranges that hold it;
+//   5. the new records are numbered in table order; a second dominance pass
+//      gives every request the lowest-positioned record holding it when it
+//      is made (an old one, or a new one made before it);
+//   6. old and new records are merged, handles, kinds, remap and counters.
+// Deregistration counts each record's handles; only a record whose last
+// reference the batch reaches needs its handles' batch order, found in a
+// bucket of its own (no sort); survivors are compacted by a scan.
 #include <cerrno>
 
 #include "common.cuh"
@@ -1344,60 +1348,128 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
 }
 
 // ----------------------------------------------------------- deregistration
+// A record's handles in batch order drop its references one by one: with c
+// handles and R references, all of them drop one when c < R; otherwise the
+// first R - 1 drop one, the R-th releases the record and the rest are stale
+// ("IB Backend MR Cache": the MR goes at zero; an unknown handle is an
+// error). Only a contested record (R >= 1, c >= R, c >= 2) needs its
+// handles' order: they go into a bucket of the record's own (slots from an
+// exclusive scan of the counts, in any order), and a handle's rank is the
+// number of smaller handle indices in the bucket -- counted by the handle
+// itself in a bucket of at most kSmallBucket, else compared with the
+// record's releasing handle, found by a radix select over the bucket.
 struct DeregHeader {
-  uint32_t n_h;      // items the sort covers (every handle)
+  uint32_t nbig;     // records with more than kSmallBucket handles
   uint32_t kept;     // records after the batch
   unsigned long long stale;
 };
-__global__ void set_u32(uint32_t* p, uint32_t v) {
-  kernel_prologue(); *p = v; }
-__global__ void dereg_key(const int64_t* handle, uint64_t n_h, uint64_t n, uint64_t* key,
-                          uint32_t* val) {
+constexpr uint32_t kSmallBucket = 16;
+constexpr int kSelectThreads = 256;
+__device__ __forceinline__ uint64_t dereg_record(const int64_t* handle, uint64_t k, uint64_t n) {
+  const int64_t x = handle[k];
+  return (x >= 0 && (uint64_t)x < n) ? (uint64_t)x : n;  // n: no such record
+}
+__device__ __forceinline__ bool contested(uint32_t c, uint32_t R) {
+  return R >= 1 && c >= R && c >= 2;
+}
+// Handles per record; the handle that counts a record's (kSmallBucket + 1)-th
+// puts it on the list of large buckets (once per record).
+__global__ void dereg_count(const int64_t* handle, uint64_t n_h, uint64_t n, uint32_t* cnt,
+                            uint32_t* big, DeregHeader* h) {
   kernel_prologue();
   FOR_EACH(k, n_h) {
-    const int64_t x = handle[k];
-    key[k] = (x >= 0 && (uint64_t)x < n) ? (uint64_t)x : n;  // n: no such record
-    val[k] = (uint32_t)k;
+    const uint64_t r = dereg_record(handle, k, n);
+    if (r < n && atomicAdd(&cnt[r], 1u) == kSmallBucket) big[atomicAdd(&h->nbig, 1u)] = (uint32_t)r;
   }
 }
-__global__ void dereg_runs(const uint64_t* key, uint64_t n_h, uint32_t* flag) {
+// cur[r] starts as the record's first bucket slot and ends one past its last.
+__global__ void dereg_fill(const int64_t* handle, uint64_t n_h, uint64_t n, const uint32_t* cnt,
+                           const uint32_t* refs, uint32_t* cur, uint32_t* bucket) {
   kernel_prologue();
-  FOR_EACH(i, n_h) flag[i] = i == 0 || key[i] != key[i - 1];
+  FOR_EACH(k, n_h) {
+    const uint64_t r = dereg_record(handle, k, n);
+    if (r < n && contested(cnt[r], refs[r])) bucket[atomicAdd(&cur[r], 1u)] = (uint32_t)k;
+  }
 }
-__global__ void dereg_run_start(const uint32_t* flag, const uint32_t* excl, uint64_t n_h,
-                                uint32_t* rs) {
+// The releasing handle of each contested large bucket: its R-th smallest
+// handle index, 8 bits at a time from the top (a CTA per record).
+__global__ void __launch_bounds__(kSelectThreads) dereg_select(
+    const DeregHeader* h, const uint32_t* big, const uint32_t* cnt, const uint32_t* refs,
+    const uint32_t* cur, const uint32_t* bucket, uint32_t* rel) {
   kernel_prologue();
-  FOR_EACH(i, n_h) if (flag[i]) rs[excl[i]] = (uint32_t)i;
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_w[kSelectThreads / 32];
+  __shared__ uint32_t s_digit, s_before;
+  const uint32_t nbig = h->nbig;
+  for (uint32_t b = blockIdx.x; b < nbig; b += gridDim.x) {
+    const uint32_t r = big[b];
+    const uint32_t c = cnt[r], R = refs[r];
+    if (!contested(c, R)) continue;  // the same for the whole CTA
+    const uint32_t* L = bucket + (cur[r] - c);
+    uint32_t prefix = 0, want = R - 1;  // rank of the releaser among the handles left
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      const uint32_t hi = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
+      hist[threadIdx.x] = 0;
+      __syncthreads();
+      for (uint32_t i = threadIdx.x; i < c; i += kSelectThreads) {
+        const uint32_t x = L[i];
+        if ((x & hi) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      const uint32_t v = hist[threadIdx.x];
+      uint32_t ex, tot;
+      block_excl_scan<kSelectThreads / 32>(v, ex, tot, s_w);
+      if (ex <= want && want < ex + v) {  // exactly one digit
+        s_digit = threadIdx.x;
+        s_before = ex;
+      }
+      __syncthreads();
+      prefix |= s_digit << shift;
+      want -= s_before;
+      __syncthreads();  // hist, s_w and s_digit are written again
+    }
+    if (threadIdx.x == 0) rel[r] = prefix;
+  }
 }
-__global__ void dereg_status(const uint64_t* key, const uint32_t* val, const uint32_t* flag,
-                             const uint32_t* excl, const uint32_t* rs, uint64_t n_h, uint64_t n,
-                             const uint32_t* refs, uint32_t* dec, uint8_t* status,
-                             DeregHeader* h) {
+__global__ void dereg_status(const int64_t* handle, uint64_t n_h, uint64_t n, const uint32_t* cnt,
+                             const uint32_t* refs, const uint32_t* cur, const uint32_t* bucket,
+                             const uint32_t* rel, uint8_t* status, DeregHeader* h) {
   kernel_prologue();
   unsigned long long stale = 0;
-  FOR_EACH(i, n_h) {
-    const uint64_t r = key[i];
+  FOR_EACH(k, n_h) {
+    const uint64_t r = dereg_record(handle, k, n);
     uint8_t st = DB_DEREG_STALE;
     if (r < n) {
-      const uint32_t rank = (uint32_t)i - rs[excl[i] + flag[i] - 1];
-      const uint32_t have = refs[r];
-      if (rank < have) {
-        st = rank + 1 == have ? DB_DEREG_RELEASED : DB_DEREG_OK;
-        atomicAdd(&dec[r], 1u);
+      const uint32_t c = cnt[r], R = refs[r];
+      if (c < R) {
+        st = DB_DEREG_OK;
+      } else if (R >= 1) {
+        uint32_t rank = 0;  // handles of the record before this one
+        if (c == 1) {
+          rank = 0;
+        } else if (c <= kSmallBucket) {
+          const uint32_t* L = bucket + (cur[r] - c);
+          for (uint32_t i = 0; i < c; ++i) rank += L[i] < (uint32_t)k;
+        } else {
+          const uint32_t x = rel[r];  // rank R - 1
+          rank = (uint32_t)k < x ? 0u : (uint32_t)k == x ? R - 1 : R;
+        }
+        st = rank + 1 < R ? DB_DEREG_OK : rank + 1 == R ? DB_DEREG_RELEASED : DB_DEREG_STALE;
       }
     }
     stale += st == DB_DEREG_STALE;
-    status[val[i]] = st;
+    status[k] = st;
   }
   stale = warp_sum64(stale);
   if ((threadIdx.x & 31) == 0 && stale) atomicAdd(&h->stale, stale);
 }
-__global__ void dereg_keep(const uint32_t* refs, const uint32_t* dec, uint64_t n, uint32_t* keep) {
+// A record survives when its handles leave a reference: c < R.
+__global__ void dereg_keep(const uint32_t* refs, const uint32_t* cnt, uint64_t n, uint32_t* keep) {
   kernel_prologue();
-  FOR_EACH(i, n) keep[i] = refs[i] > dec[i];
+  FOR_EACH(i, n) keep[i] = refs[i] > cnt[i];
 }
 __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
-                            const uint32_t* refs, const uint32_t* dec, const uint32_t* keep,
+                            const uint32_t* refs, const uint32_t* cnt, const uint32_t* keep,
                             const uint32_t* kpos, uint64_t n, uint64_t* o_start, uint64_t* o_end,
                             uint32_t* o_lkey, uint32_t* o_refs, int64_t* remap) {
   kernel_prologue();
@@ -1410,7 +1482,7 @@ __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const ui
     o_start[w] = start[i];
     o_end[w] = end[i];
     o_lkey[w] = lkey[i];
-    o_refs[w] = refs[i] - dec[i];
+    o_refs[w] = refs[i] - cnt[i];
     remap[i] = w;
   }
 }
@@ -1423,7 +1495,7 @@ __global__ void dereg_final(const DeregHeader* h, db_counters* ctr) {
 }
 
 struct DeregLayout {
-  size_t hdr, key0, key1, val0, val1, counts, bsum, diff, flag, excl, rs, dec, keep, kpos, total;
+  size_t hdr, cnt, cur, bucket, rel, big, bsum, keep, kpos, total;
 };
 DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
   DeregLayout L;
@@ -1431,18 +1503,12 @@ DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
   L.hdr = take(sizeof(DeregHeader));
-  L.key0 = take(q * 8);
-  L.key1 = take(q * 8);
-  L.val0 = take(q * 4);
-  L.val1 = take(q * 4);
-  L.counts = take(sort_count_words(q) * 4);
-  const uint64_t scan_n = sort_count_words(q) > q ? sort_count_words(q) : q;
-  L.bsum = take(scan_tmp_words(scan_n > n ? scan_n : n) * 4);
-  L.diff = take(8);
-  L.flag = take(q * 4);
-  L.excl = take(q * 4);
-  L.rs = take(q * 4);
-  L.dec = take(n * 4);
+  L.cnt = take(n * 4);
+  L.cur = take(n * 4);
+  L.bucket = take(q * 4);
+  L.rel = take(n * 4);
+  L.big = take(n * 4);
+  L.bsum = take(scan_tmp_words(n) * 4);
   L.keep = take(n * 4);
   L.kpos = take(n * 4);
   L.total = o;
@@ -1665,47 +1731,44 @@ extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint6
   auto at = [&](size_t off) { return static_cast<void*>(w + off); };
   DeregHeader* h = static_cast<DeregHeader*>(at(L.hdr));
   uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
-  SortBufs sb{{static_cast<uint64_t*>(at(L.key0)), static_cast<uint64_t*>(at(L.key1))},
-              {static_cast<uint32_t*>(at(L.val0)), static_cast<uint32_t*>(at(L.val1))},
-              static_cast<uint32_t*>(at(L.counts)), bsum, n_h,
-              static_cast<unsigned long long*>(at(L.diff))};
-  uint32_t* flag = static_cast<uint32_t*>(at(L.flag));
-  uint32_t* excl = static_cast<uint32_t*>(at(L.excl));
-  uint32_t* rs = static_cast<uint32_t*>(at(L.rs));
-  uint32_t* dec = static_cast<uint32_t*>(at(L.dec));
+  uint32_t* cnt = static_cast<uint32_t*>(at(L.cnt));
+  uint32_t* cur = static_cast<uint32_t*>(at(L.cur));
+  uint32_t* bucket = static_cast<uint32_t*>(at(L.bucket));
+  uint32_t* rel = static_cast<uint32_t*>(at(L.rel));
+  uint32_t* big = static_cast<uint32_t*>(at(L.big));
   uint32_t* keep = static_cast<uint32_t*>(at(L.keep));
   uint32_t* kpos = static_cast<uint32_t*>(at(L.kpos));
   if (cudaMemsetAsync(h, 0, sizeof(DeregHeader), s) != cudaSuccess ||
-      (n_mr && cudaMemsetAsync(dec, 0, n_mr * 4, s) != cudaSuccess))
+      (n_mr && cudaMemsetAsync(cnt, 0, n_mr * 4, s) != cudaSuccess))
     return launch_result();
-  launch_dep(set_u32, 1, 1, 0, s,
-             &h->n_h, (uint32_t)n_h);  // the sort reads its length on the device
-             int rc = launch_result();
-  if (rc) return rc;
+  int rc = 0;
   if (n_h) {
-    launch_dep(dereg_key, grid_for(n_h), kThreads, 0, s, handle, n_h, n_mr, sb.key[0], sb.val[0]);
+    launch_dep(dereg_count, grid_for(n_h), kThreads, 0, s, handle, n_h, n_mr, cnt, big, h);
     if ((rc = launch_result())) return rc;
-    int bits = 0;
-    while (bits < 64 && (n_mr >> bits)) ++bits;  // keys are at most n_mr
-    bits = (bits + 7) & ~7;
-    int cur = 0;
-    if ((rc = radix_sort(sb, cur, &h->n_h, bits, false, s))) return rc;
-    launch_dep(dereg_runs, grid_for(n_h), kThreads, 0, s, sb.key[cur], n_h, flag);
-    if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, excl, n_h, nullptr, bsum, s))) return rc;
-    launch_dep(dereg_run_start, grid_for(n_h), kThreads, 0, s, flag, excl, n_h, rs);
-    if ((rc = launch_result())) return rc;
-    launch_dep(dereg_status, grid_for(n_h), kThreads, 0, s,
-               sb.key[cur], sb.val[cur], flag, excl, rs, n_h,
-               n_mr, refs, dec, status, h);
+    if (n_mr) {
+      if ((rc = scan(cnt, cur, n_mr, nullptr, bsum, s))) return rc;
+      launch_dep(dereg_fill, grid_for(n_h), kThreads, 0, s, handle, n_h, n_mr,
+                 (const uint32_t*)cnt, refs, cur, bucket);
+      if ((rc = launch_result())) return rc;
+      uint64_t sel = n_h / (kSmallBucket + 1);  // at most this many large buckets
+      const uint64_t cap = (uint64_t)num_sms() * 4;
+      sel = sel < 1 ? 1 : sel > cap ? cap : sel;
+      launch_dep(dereg_select, (unsigned)sel, kSelectThreads, 0, s, (const DeregHeader*)h,
+                 (const uint32_t*)big, (const uint32_t*)cnt, refs, (const uint32_t*)cur,
+                 (const uint32_t*)bucket, rel);
+      if ((rc = launch_result())) return rc;
+    }
+    launch_dep(dereg_status, grid_for(n_h), kThreads, 0, s, handle, n_h, n_mr,
+               (const uint32_t*)cnt, refs, (const uint32_t*)cur, (const uint32_t*)bucket,
+               (const uint32_t*)rel, status, h);
     if ((rc = launch_result())) return rc;
   }
   if (n_mr) {
-    launch_dep(dereg_keep, grid_for(n_mr), kThreads, 0, s, refs, dec, n_mr, keep);
+    launch_dep(dereg_keep, grid_for(n_mr), kThreads, 0, s, refs, (const uint32_t*)cnt, n_mr, keep);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(keep, kpos, n_mr, &h->kept, bsum, s))) return rc;
     launch_dep(dereg_place, grid_for(n_mr), kThreads, 0, s,
-               start, end, lkey, refs, dec, keep, kpos, n_mr,
+               start, end, lkey, refs, (const uint32_t*)cnt, keep, kpos, n_mr,
                out_start, out_end, out_lkey, out_refs, remap);
     if ((rc = launch_result())) return rc;
   }

@@ -250,6 +250,31 @@ def test_deregister_sort_digit_patterns(db, oracle, pattern):
          DEREG_KEYS)
 
 
+@pytest.mark.parametrize("case", ["bucket_sizes", "one_huge_bucket", "zero_refs"])
+def test_deregister_bucket_sizes(db, oracle, case):
+    """Records named by 1..40 handles each (either side of the bucket size a
+    handle ranks itself in), references below, at and above the handle
+    count; one record named by 300,000 handles; records holding no
+    reference."""
+    rng = np.random.default_rng({"bucket_sizes": 1, "one_huge_bucket": 2, "zero_refs": 3}[case])
+    n = 2000
+    s = np.arange(n, dtype=np.uint64) * np.uint64(0x10000)
+    e = s + np.uint64(0x8000)
+    lk = np.arange(n, dtype=np.uint32)
+    c = np.arange(n) % 40 + 1
+    refs = (rng.integers(0, 3, size=n) + np.maximum(c - 1, 0)).astype(np.uint32)
+    hs = np.repeat(np.arange(n), c)
+    if case == "one_huge_bucket":
+        hs = np.concatenate([hs, np.full(300000, 7)])
+        refs[7] = 123457
+    if case == "zero_refs":
+        refs[::3] = 0
+    hs = rng.permutation(hs).astype(np.int64)
+    hs[::97] = -1
+    same(deregister(db, hs, s, e, lk, refs), oracle.mr_deregister(hs, s, e, lk, refs),
+         DEREG_KEYS)
+
+
 def test_register_empty_batch_and_capacity(db, oracle):
     rng = np.random.default_rng(3)
     q, nl, s, e, lk, refs = random_case(rng, 50, 400, 400, 12)
