@@ -8,6 +8,7 @@ the oracle pin tests against it in a subprocess: they must fail.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -140,20 +141,55 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_mutant(tmp_path, name, old, new):
+PIN_FILES = ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
+             "test_oracle_vmm.py", "test_oracle_cq.py", "test_oracle_mr_cache.py",
+             "test_oracle_transport.py")
+# The pin file a mutant's name points at runs first (every file still runs
+# until one fails), so most mutants stop after one file.
+FIRST = (("transport", "test_oracle_transport.py"), ("register", "test_oracle_mr_cache.py"),
+         ("deregister", "test_oracle_mr_cache.py"), ("vmm", "test_oracle_vmm.py"),
+         ("psn", "test_oracle_vmm.py"), ("wqe", "test_oracle_wqe.py"), ("cq", "test_oracle_cq.py"),
+         ("mr", "test_oracle_mr.py"))
+
+
+def pin_order(name):
+    first = next((f for key, f in FIRST if name.startswith(key)), PIN_FILES[0])
+    return [first] + [f for f in PIN_FILES if f != first]
+
+
+def run_mutant(workdir, name, old, new):
+    """Build the mutant and run the pins against it: (returncode, output tail)."""
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
-    mutated = tmp_path / "oracle_mutant.cpp"
-    mutated.write_text(src.replace(old, new))
-    lib = tmp_path / "liboracle_mutant.so"
-    subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-o", str(lib), str(mutated)],
+    if src.count(old) != 1:
+        return None, f"mutation anchor not unique: {old!r}"
+    mutated = os.path.join(workdir, "oracle_mutant.cpp")
+    with open(mutated, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(workdir, "liboracle_mutant.so")
+    subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-o", lib, mutated],
                    check=True)
-    env = dict(os.environ, DB_ORACLE_LIB=str(lib))
-    tests = [os.path.join(ROOT, "tests", f) for f in
-             ("test_oracle_prp.py", "test_oracle_mr.py", "test_oracle_wqe.py",
-              "test_oracle_vmm.py", "test_oracle_cq.py", "test_oracle_mr_cache.py",
-              "test_oracle_transport.py")]
+    env = dict(os.environ, DB_ORACLE_LIB=lib)
+    tests = [os.path.join(ROOT, "tests", f) for f in pin_order(name)]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *tests],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
+    return r.returncode, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def verdicts(tmp_path_factory):
+    """Every mutant built and run once, several at a time (each run is its
+    own process with its own library)."""
+    assert len({m[0] for m in MUTANTS}) == len(MUTANTS), "mutant names must be unique"
+    jobs = {}
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as pool:
+        for i, (name, old, new) in enumerate(MUTANTS):
+            d = str(tmp_path_factory.mktemp(f"mutant{i}"))
+            jobs[name] = pool.submit(run_mutant, d, name, old, new)
+        return {name: job.result() for name, job in jobs.items()}
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(verdicts, name, old, new):
+    rc, out = verdicts[name]
+    assert rc is not None, out
+    assert rc != 0, f"pins did not catch: {name}\n{out}"
