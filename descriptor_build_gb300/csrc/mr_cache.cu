@@ -919,11 +919,25 @@ __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, 
     flag[i] = f;
   }
 }
+// Count of a[0..n) below x (strict) or at most x.
+__device__ __forceinline__ uint64_t count_below(const uint64_t* a, uint64_t n, uint64_t x,
+                                                bool or_equal) {
+  uint64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint64_t mid = (lo + hi) >> 1;
+    const uint64_t v = a[mid];
+    if (v < x || (or_equal && v == x)) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
 // The distinct missed ranges, in (start ascending, end descending) order:
-// start, end and the request that first asked for it.
+// start, end, the request that first asked for it, and whether a later
+// request asked for it again.
 __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_max,
                              uint32_t gshift, const uint32_t* val, const uint32_t* flag,
-                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first) {
+                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first,
+                             uint8_t* again) {
   kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
@@ -935,6 +949,7 @@ __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_m
     db[p] = b;
     de[p] = e;
     first[p] = val[i];
+    again[p] = (i + 1 < m && !flag[i + 1]) ? 1 : 0;
   }
 }
 // Items of the first dominance pass: a distinct range is a query for the
@@ -998,12 +1013,21 @@ __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cf
 // later new record of the same start ends later: it was not held by the
 // earlier one). Within a run of equal starts the list above is in the
 // opposite order of ends, so record c of a run [gs, ge) goes to gs + ge - 1 - c.
+//
+// A new record can be the answer of a later request only when its range is
+// asked for again, or it holds another missed range (then the next distinct
+// range starts before its end), or it may take a hit from an old record that
+// starts inside it (an old start lies strictly between its start and end);
+// point[j] says so, and the other new records stay out of the second
+// dominance pass (a request they could answer has a holder that is in it at
+// a position no later, or keeps its old record either way).
 __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* cp,
-                           const uint64_t* cb, const uint64_t* de, const uint32_t* first,
-                           uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
-                           uint32_t* creator_of, uint64_t* cend) {
+                           const uint64_t* cb, const uint64_t* db, const uint64_t* de,
+                           const uint32_t* first, const uint8_t* again, const uint64_t* start,
+                           uint64_t n_mr, uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
+                           uint32_t* creator_of, uint64_t* cend, uint8_t* point) {
   kernel_prologue();
-  const uint64_t u = h->u;
+  const uint64_t u = h->u, d = h->d;
   FOR_EACH(c, n_max) {
     if (c >= u) break;
     const uint64_t b = cb[c];
@@ -1033,6 +1057,12 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
     nfirst[j] = first[p];
     creator_of[first[p]] = (uint32_t)j;
     cend[c] = e;
+    bool pt = again[p] || (p + 1 < d && db[p + 1] < e);
+    if (!pt) {
+      const uint64_t o = count_below(start, n_mr, b, true);  // first old record starting past b
+      pt = o < n_mr && start[o] < e;
+    }
+    point[j] = pt ? 1 : 0;
   }
 }
 // reach[o] = the largest end of a new record starting before old record o
@@ -1054,17 +1084,20 @@ __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t
   }
 }
 // Items of the second dominance pass, in request order: the new records
-// (key: table position among the new records, end) and the requests whose
+// that may answer a request (key: table position among the new records,
+// end) and the requests whose
 // record is still open -- misses that made no record, and hits on an old
 // record that a new record may precede (query id: the request).
 __global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
-                          const int32_t* idx, const uint64_t* reach, uint32_t* role) {
+                          const int32_t* idx, const uint64_t* reach, const uint32_t* creator_of,
+                          const uint8_t* point, uint32_t* role) {
   kernel_prologue();
   FOR_EACH(k, n_q) {
     const uint8_t kd = kind0[k];
     uint32_t r = 0;
     if (kd == DB_MR_MISS) {
-      r = 1;
+      const uint32_t c = creator_of[k];
+      r = c == kNone ? 1u : point[c];
     } else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) {
       uint64_t b, e;
       widen(q, k, gshift, b, e);
@@ -1212,18 +1245,6 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
     kind1[k] = k1;
   }
 }
-// Count of a[0..n) below x (strict) or at most x.
-__device__ __forceinline__ uint64_t count_below(const uint64_t* a, uint64_t n, uint64_t x,
-                                                bool or_equal) {
-  uint64_t lo = 0, hi = n;
-  while (lo < hi) {
-    const uint64_t mid = (lo + hi) >> 1;
-    const uint64_t v = a[mid];
-    if (v < x || (or_equal && v == x)) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
 struct PlaceParams {
   const uint64_t *start, *end;
   const uint32_t *lkey, *refs, *more;
@@ -1292,7 +1313,7 @@ struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
       diff, nstart, nend, nfirst, nrefs, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
       ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, rec_new,
-      kind1, total;
+      kind1, again, point, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -1343,6 +1364,8 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.held = take(q * 4);
   L.rec_new = take(q * 4);
   L.kind1 = take(q);
+  L.again = take(q);
+  L.point = take(q);
   L.total = o;
   return L;
 }
@@ -1621,8 +1644,10 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->d, bsum, s))) return rc;
+    uint8_t* again = static_cast<uint8_t*>(at(L.again));
+    uint8_t* point = static_cast<uint8_t*>(at(L.point));
     launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
-               pos, db, de, first);
+               pos, db, de, first, again);
     if ((rc = launch_result())) return rc;
     uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
     uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
@@ -1648,8 +1673,8 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_clist, grid_for(n_q), kThreads, 0, s, h, n_q, flag, pos, db, cp, cbs);
     if ((rc = launch_result())) return rc;
     // 5. the new records in table order; old records a new one may precede
-    launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, de, first, nstart,
-               nend, nfirst, creator_of, cend);
+    launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, db, de, first,
+               (const uint8_t*)again, start, n_mr, nstart, nend, nfirst, creator_of, cend, point);
     if ((rc = launch_result())) return rc;
     if ((rc = prefix_max(cend, &h->u, n_q, bmax, pmax, s))) return rc;
     if (n_mr) {
@@ -1660,7 +1685,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     // 6. every request's record: the lowest-positioned one holding it when
     //    it is made (an old one, or a new one made before it)
     launch_dep(reg_roles, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
-               (const uint64_t*)reach, flag);
+               (const uint64_t*)reach, (const uint32_t*)creator_of, (const uint8_t*)point, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan(flag, pos, n_q, &h->nb, bsum, s))) return rc;
     launch_dep(reg_items, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, flag, pos,
