@@ -250,6 +250,30 @@ def test_deregister_sort_digit_patterns(db, oracle, pattern):
          DEREG_KEYS)
 
 
+def test_register_new_record_takes_a_later_hit(db, oracle):
+    """A new range that starts before an old record and covers part of it
+    takes a later request inside both (it comes first in the table); a
+    later miss inside it is a hit on it; a lone new range that nothing
+    asks for again changes no other request."""
+    s = np.array([0x10000, 0x40000], np.uint64)
+    e = np.array([0x20000, 0x50000], np.uint64)
+    lk = np.array([11, 12], np.uint32)
+    refs = np.array([1, 1], np.uint32)
+    q = np.array([[0x8000, 0x10000],    # misses: new record from 0x8000, over the old start
+                  [0x11000, 0x1000],    # inside the old record and the new one
+                  [0x30000, 0x1000],    # a lone new record
+                  [0x9000, 0x1000],     # a miss inside the first new record
+                  [0x41000, 0x1000],    # an ordinary hit
+                  [0x30000, 0x1000]],   # the lone record asked for again
+                 np.uint64)
+    nl = np.arange(100, 106, dtype=np.uint32)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs)
+    got = register(db, q, nl, s, e, lk, refs)
+    same(got, want, REG_KEYS)
+    assert want["kind"].tolist()[:5] == [db.MR_NEW, db.MR_NEW_DUP, db.MR_NEW, db.MR_NEW_DUP,
+                                         db.MR_CONTAINED]
+
+
 @pytest.mark.parametrize("case", ["bucket_sizes", "one_huge_bucket", "zero_refs"])
 def test_deregister_bucket_sizes(db, oracle, case):
     """Records named by 1..40 handles each (either side of the bucket size a
