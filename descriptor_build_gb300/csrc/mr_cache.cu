@@ -687,12 +687,29 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
       continue;
     }
     const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0);
-    for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads)
-      seg[x] = x < na ? E[pb + i0 + x] : E[rb + j0 + (x - na)];
+    // Thread t owns items t, t + kCdqThreads, ... of the two slices: it loads
+    // their end into shared memory and their key, query id and answer into
+    // registers, all before the search, so no load waits on it.
+    uint32_t rk[kCdqPer], rq[kCdqPer], ra[kCdqPer];
+#pragma unroll
+    for (int u = 0; u < kCdqPer; ++u) {
+      const uint32_t x = threadIdx.x + u * kCdqThreads;
+      rk[u] = rq[u] = ra[u] = kNone;
+      if (x < na + nb) {
+        const uint64_t gi = x < na ? pb + i0 + x : rb + j0 + (x - na);
+        seg[x] = E[gi];
+        rk[u] = Kin[gi];
+        rq[u] = Qin[gi];
+        ra[u] = Ain[gi];
+      }
+    }
     __syncthreads();
     const uint64_t* sl = seg;
     const uint64_t* sr = seg + na;
-    for (uint32_t x = threadIdx.x; x < na + nb; x += kCdqThreads) {
+#pragma unroll
+    for (int u = 0; u < kCdqPer; ++u) {
+      const uint32_t x = threadIdx.x + u * kCdqThreads;
+      if (x >= na + nb) continue;
       const bool from_left = x < na;
       const uint64_t ex = seg[x];
       uint32_t lo = 0, hi = from_left ? nb : na;
@@ -703,9 +720,8 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
         if (v > ex || (!from_left && v == ex)) lo = mid + 1;
         else hi = mid;
       }
-      const uint64_t gi = from_left ? pb + i0 + x : rb + j0 + (x - na);
-      const uint32_t q = Qin[gi];
-      uint32_t a = Ain[gi];
+      const uint32_t q = rq[u];
+      uint32_t a = ra[u];
       if (!from_left && q != kNone) {
         const uint64_t c = i0 + lo;  // left-run items with an end at least ex
         if (c > 0) {
@@ -719,7 +735,7 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
         continue;
       }
       oe[pos] = ex;
-      ok[pos] = Kin[gi];
+      ok[pos] = rk[u];
       oq[pos] = q;
       oa[pos] = a;
     }
