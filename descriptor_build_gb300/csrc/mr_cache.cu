@@ -1036,12 +1036,14 @@ __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cf
 // starts inside it (an old start lies strictly between its start and end);
 // point[j] says so, and the other new records stay out of the second
 // dominance pass (a request they could answer has a holder that is in it at
-// a position no later, or keeps its old record either way).
+// a position no later, or keeps its old record either way). nold[j] is the
+// number of old records starting at or before it (its place in the merged
+// table is j + nold[j]).
 __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* cp,
                            const uint64_t* cb, const uint64_t* db, const uint64_t* de,
                            const uint32_t* first, const uint8_t* again, const uint64_t* start,
                            uint64_t n_mr, uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
-                           uint32_t* creator_of, uint64_t* cend, uint8_t* point) {
+                           uint32_t* creator_of, uint64_t* cend, uint8_t* point, uint32_t* nold) {
   kernel_prologue();
   const uint64_t u = h->u, d = h->d;
   FOR_EACH(c, n_max) {
@@ -1073,19 +1075,19 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
     nfirst[j] = first[p];
     creator_of[first[p]] = (uint32_t)j;
     cend[c] = e;
-    bool pt = again[p] || (p + 1 < d && db[p + 1] < e);
-    if (!pt) {
-      const uint64_t o = count_below(start, n_mr, b, true);  // first old record starting past b
-      pt = o < n_mr && start[o] < e;
-    }
+    const uint64_t o = count_below(start, n_mr, b, true);  // first old record starting past b
+    nold[j] = (uint32_t)o;
+    const bool pt = again[p] || (p + 1 < d && db[p + 1] < e) || (o < n_mr && start[o] < e);
     point[j] = pt ? 1 : 0;
   }
 }
 // reach[o] = the largest end of a new record starting before old record o
 // (a prefix maximum of cend over the list, which is in start order): a hit
 // on o can be taken by a new record only if its end is within that reach.
+// onew[o] = the number of new records starting before old record o (its
+// place in the merged table is o + onew[o]).
 __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t* pmax,
-                          const uint64_t* start, uint64_t n, uint64_t* reach) {
+                          const uint64_t* start, uint64_t n, uint64_t* reach, uint32_t* onew) {
   kernel_prologue();
   const uint64_t u = h->u;
   FOR_EACH(o, n) {
@@ -1097,6 +1099,7 @@ __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t
       else hi = mid;
     }
     reach[o] = lo ? pmax[lo - 1] : 0;
+    onew[o] = (uint32_t)lo;
   }
 }
 // Items of the second dominance pass, in request order: the new records
@@ -1273,13 +1276,15 @@ struct PlaceParams {
   int64_t* remap;
   uint32_t* npos;
   const RegHeader* h;
+  const uint32_t* nold;  // old records starting at or before each new one
+  const uint32_t* onew;  // new records starting before each old one (null: none)
 };
 __global__ void reg_place_old(const PlaceParams p) {
   kernel_prologue();
   const uint64_t u = p.h->u;
   if (p.n + u > p.o_cap) return;
   FOR_EACH(i, p.n) {
-    const uint64_t w = i + count_below(p.nstart, u, p.start[i], false);  // old first on ties
+    const uint64_t w = i + (p.onew ? p.onew[i] : 0u);  // old first on equal starts
     p.o_start[w] = p.start[i];
     p.o_end[w] = p.end[i];
     p.o_lkey[w] = p.lkey[i];
@@ -1293,7 +1298,7 @@ __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
   if (p.n + u > p.o_cap) return;
   FOR_EACH(j, n_max) {
     if (j >= u) break;
-    const uint64_t w = j + count_below(p.start, p.n, p.nstart[j], true);
+    const uint64_t w = j + p.nold[j];
     p.o_start[w] = p.nstart[j];
     p.o_end[w] = p.nend[j];
     p.o_lkey[w] = p.new_lkey[p.nfirst[j]];
@@ -1329,7 +1334,7 @@ struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
       diff, nstart, nend, nfirst, nrefs, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
       ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, rec_new,
-      kind1, again, point, total;
+      kind1, again, point, nold, onew, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -1382,6 +1387,8 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.kind1 = take(q);
   L.again = take(q);
   L.point = take(q);
+  L.nold = take(q * 4);
+  L.onew = take((n_mr ? n_mr : 1) * 4);
   L.total = o;
   return L;
 }
@@ -1686,16 +1693,19 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
     uint64_t* cend = static_cast<uint64_t*>(at(L.cend));
     uint64_t* reach = static_cast<uint64_t*>(at(L.reach));
+    uint32_t* onew = static_cast<uint32_t*>(at(L.onew));
     launch_dep(reg_clist, grid_for(n_q), kThreads, 0, s, h, n_q, flag, pos, db, cp, cbs);
     if ((rc = launch_result())) return rc;
     // 5. the new records in table order; old records a new one may precede
+    uint32_t* nold = static_cast<uint32_t*>(at(L.nold));
     launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, db, de, first,
-               (const uint8_t*)again, start, n_mr, nstart, nend, nfirst, creator_of, cend, point);
+               (const uint8_t*)again, start, n_mr, nstart, nend, nfirst, creator_of, cend, point,
+               nold);
     if ((rc = launch_result())) return rc;
     if ((rc = prefix_max(cend, &h->u, n_q, bmax, pmax, s))) return rc;
     if (n_mr) {
       launch_dep(reg_reach, grid_for(n_mr), kThreads, 0, s, (const RegHeader*)h,
-                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, reach);
+                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, reach, onew);
       if ((rc = launch_result())) return rc;
     }
     // 6. every request's record: the lowest-positioned one holding it when
@@ -1715,7 +1725,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                flag, creator_of, held, nstart, start, more, nrefs, rec_new, kind1, h);
     if ((rc = launch_result())) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h, nold, onew};
     if (n_mr) {
       launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
       if ((rc = launch_result())) return rc;
@@ -1732,7 +1742,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                     at(L.lookup), mr::workspace_bytes(n_mr), s, true, (int)granule_shift);
     if (rc) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h};
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h, nullptr, nullptr};
     launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
     if ((rc = launch_result())) return rc;
   }
