@@ -1104,9 +1104,9 @@ __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t
 }
 // Items of the second dominance pass, in request order: the new records
 // that may answer a request (key: table position among the new records,
-// end) and the requests whose
-// record is still open -- misses that made no record, and hits on an old
-// record that a new record may precede (query id: the request).
+// end) and the requests whose record is still open -- misses that made no
+// record, and hits on an old record that a new record may precede (query
+// id: the request).
 __global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
                           const int32_t* idx, const uint64_t* reach, const uint32_t* creator_of,
                           const uint8_t* point, uint32_t* role) {
