@@ -542,22 +542,25 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_kernel(const Params 
 // ring's WQEs contiguous in its ring), finding a WQE's put by binary search.
 // Per warp: puts, per-ring first sequence number, run start in puts and in
 // WQEs, per-row ring counts, the permutation and the WQE prefix.
-__host__ __device__ inline size_t vmm_warp_smem(uint32_t V) {
+// (With PSNs the two prefix arrays are padded to 16-byte multiples.)
+__host__ __device__ inline size_t vmm_warp_smem(uint32_t V, bool psn) {
   size_t b = (size_t)kTile * 16;      // puts
   b += (size_t)V * 8;                 // first sequence number per ring
   b += (size_t)V * 4 * 2;             // run start (puts), run start (WQEs)
   b += (size_t)kRows * V * 2;         // per-row counts
   b += (size_t)kTile * 2;             // permutation
-  b += (size_t)(kTile + 1) * 4;       // WQE prefix over the ring order
-  b += (size_t)(kTile + 1) * 4;       // PSN prefix over the ring order
+  b += (size_t)(kTile + (psn ? 4 : 1)) * 4;  // WQE prefix over the ring order
+  b += (size_t)(kTile + (psn ? 4 : 1)) * 4;  // PSN prefix over the ring order
   b += (size_t)V * 4 * 2;             // first PSN of the tile, PSN run start
   return (b + 15) & ~(size_t)15;
 }
-inline int vmm_scatter_warps(uint32_t V) {
-  const size_t fit = (kMaxSmem - cta_smem(V)) / vmm_warp_smem(V);
+inline int vmm_scatter_warps(uint32_t V, bool psn) {
+  const size_t fit = (kMaxSmem - cta_smem(V)) / vmm_warp_smem(V, psn);
   return (int)(fit < (size_t)kSWarps ? fit : (size_t)kSWarps);
 }
-inline size_t vmm_scatter_smem(uint32_t V) { return cta_smem(V) + vmm_scatter_warps(V) * vmm_warp_smem(V); }
+inline size_t vmm_scatter_smem(uint32_t V, bool psn) {
+  return cta_smem(V) + vmm_scatter_warps(V, psn) * vmm_warp_smem(V, psn);
+}
 
 // The chunk tables packed per call: record (pe, c) = {chunk_raddr[pe][c],
 // chunk_rkey[pe][c] | chunk_lkey[c] << 32}, so a WQE reads its chunk's three
@@ -573,6 +576,8 @@ __global__ void vmm_pack_kernel(const Params p) {
   }
 }
 
+// kPsn: the call asks for PSNs (p.mtu != 0), fixed at compile time.
+template <bool kPsn>
 __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const uint32_t V = p.V, R = p.R;
@@ -580,7 +585,7 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   const uint64_t pol_first = policy_evict_first();
   const uint64_t pol_last = policy_evict_last();
   uint64_t* s_slots = reinterpret_cast<uint64_t*>(smem);
-  unsigned char* w = smem + cta_smem(V) + warp * vmm_warp_smem(V);
+  unsigned char* w = smem + cta_smem(V) + warp * vmm_warp_smem(V, kPsn);
   ulonglong2* s_put = reinterpret_cast<ulonglong2*>(w);
   uint64_t* s_seq0 = reinterpret_cast<uint64_t*>(s_put + kTile);
   uint32_t* s_run = reinterpret_cast<uint32_t*>(s_seq0 + V);
@@ -588,8 +593,9 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
   uint16_t* s_cnt = reinterpret_cast<uint16_t*>(s_wrun + V);  // [kRows][V]
   uint16_t* s_perm = s_cnt + kRows * V;
   uint32_t* s_wstart = reinterpret_cast<uint32_t*>(s_perm + kTile);  // [kTile + 1]
-  uint32_t* s_pstart = s_wstart + kTile + 1;                          // [kTile + 1]
-  uint32_t* s_psn0 = s_pstart + kTile + 1;                            // [V]
+  constexpr uint32_t kPad = kPsn ? 4 : 1;                             // 16-byte multiples
+  uint32_t* s_pstart = s_wstart + kTile + kPad;                       // [kTile + 1]
+  uint32_t* s_psn0 = s_pstart + kTile + kPad;                         // [V]
   uint32_t* s_prun = s_psn0 + V;                                      // [V]
 
   // 1. Load the tile (the caller's input: before the wait for the scan pass).
@@ -646,69 +652,91 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
     if (v < R) {
       s_run[v] = carry + x - tot;
       s_seq0[v] = p.head_old[v] + p.counts[(uint64_t)v * p.stride + tile];
-      if (p.mtu) s_psn0[v] = (uint32_t)(p.psn_old[v] + p.psn_counts[(uint64_t)v * p.stride + tile]);
+      if (kPsn) s_psn0[v] = (uint32_t)(p.psn_old[v] + p.psn_counts[(uint64_t)v * p.stride + tile]);
     }
     carry += __shfl_sync(kFull, x, 31);
   }
   const uint32_t n_valid = carry;
   __syncwarp();
-  // 3. Ring-order permutation of the valid puts.
+  // 3. Ring-order permutation of the valid puts (with PSNs, each put's WQE
+  //    and PSN counts are stored at its ring-order position as well).
 #pragma unroll
   for (int u = 0; u < kRows; ++u) {
     const uint32_t bin = bin_rank[u] & 0xFFFFu;
-    if (bin < R) s_perm[s_run[bin] + s_cnt[u * V + bin] + (bin_rank[u] >> 16)] = (uint16_t)(u * 32 + lane);
+    if (bin < R) {
+      const uint32_t at = s_run[bin] + s_cnt[u * V + bin] + (bin_rank[u] >> 16);
+      s_perm[at] = (uint16_t)(u * 32 + lane);
+      if (kPsn) {
+        s_wstart[at] = wqes_of(p, r[u]);
+        s_pstart[at] = psns_of(p, r[u]);
+      }
+    }
   }
   __syncwarp();
   // 4. Exclusive prefix of WQE counts over the ring order (lane l takes
-  //    positions 8l .. 8l + 7), and where each ring's WQEs start.
+  //    positions 8l .. 8l + 7), and where each ring's WQEs start; with PSNs
+  //    the same over PSN counts (mod 2^32, as the WQE keeps 32 bits), both in
+  //    place from the counts of step 3, two 16-byte words a lane.
   constexpr int kPer = kTile / 32;
-  uint32_t kq[kPer], mine = 0;
+  static_assert(kPer == 8, "two 16-byte words per lane");
+  uint32_t n_wqe;
+  if (kPsn) {
+    auto prefix8 = [&](uint32_t* a) {  // returns the total
+      uint4* a4 = reinterpret_cast<uint4*>(a + lane * kPer);
+      const uint4 u0 = a4[0], u1 = a4[1];
+      uint32_t kq[kPer] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t mine = 0;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const uint32_t q = lane * kPer + j;
-    kq[j] = q < n_valid ? wqes_of(p, s_put[s_perm[q]]) : 0u;
-    mine += kq[j];
-  }
-  uint32_t x = mine;
+      for (int j = 0; j < kPer; ++j) {
+        if (lane * kPer + j >= n_valid) kq[j] = 0;
+        mine += kq[j];
+      }
+      uint32_t x = mine;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  uint32_t run = x - mine;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      uint32_t e[kPer];
+      uint32_t run = x - mine;
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    s_wstart[lane * kPer + j] = run;
-    run += kq[j];
-  }
-  const uint32_t n_wqe = __shfl_sync(kFull, x, 31);
-  if (lane == 0) s_wstart[kTile] = n_wqe;
-  __syncwarp();
-  if (p.mtu) {  // the same over PSN counts (mod 2^32, as the WQE keeps 32 bits)
-    uint32_t pmine = 0;
+      for (int j = 0; j < kPer; ++j) {
+        e[j] = run;
+        run += kq[j];
+      }
+      a4[0] = make_uint4(e[0], e[1], e[2], e[3]);
+      a4[1] = make_uint4(e[4], e[5], e[6], e[7]);
+      return __shfl_sync(kFull, x, 31);
+    };
+    n_wqe = prefix8(s_wstart);
+    prefix8(s_pstart);
+  } else {
+    uint32_t kq[kPer], mine = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const uint32_t q = lane * kPer + j;
-      kq[j] = q < n_valid ? psns_of(p, s_put[s_perm[q]]) : 0u;
-      pmine += kq[j];
+      kq[j] = q < n_valid ? wqes_of(p, s_put[s_perm[q]]) : 0u;
+      mine += kq[j];
     }
-    uint32_t px = pmine;
+    uint32_t x = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, px, o);
-      if (lane >= o) px += y;
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
     }
-    uint32_t prun = px - pmine;
+    uint32_t run = x - mine;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      s_pstart[lane * kPer + j] = prun;
-      prun += kq[j];
+      s_wstart[lane * kPer + j] = run;
+      run += kq[j];
     }
-    __syncwarp();
+    n_wqe = __shfl_sync(kFull, x, 31);
   }
+  if (lane == 0) s_wstart[kTile] = n_wqe;
+  __syncwarp();
   for (uint32_t v = lane; v < R; v += 32) {
     s_wrun[v] = s_wstart[s_run[v]];
-    if (p.mtu) s_prun[v] = s_pstart[s_run[v]];
+    if (kPsn) s_prun[v] = s_pstart[s_run[v]];
   }
   __syncwarp();
   // 5. Write-out: lane l writes the tile's WQEs l, l + 32, ... (ring order),
@@ -746,7 +774,7 @@ __global__ void __launch_bounds__(kSWarps * 32) wqe_scatter_vmm_kernel(const Par
                 (end - start) | (ck.y & 0xFFFFFFFF00000000ull), ck.y & 0xFFFFFFFFull, pol_first);
     // u32 batch index at byte 40, first PSN at byte 44
     uint64_t w5 = t0 + o;
-    if (p.mtu)
+    if (kPsn)
       w5 |= (uint64_t)(s_psn0[v] + (s_pstart[lo] - s_prun[v]) + psns_before(p, pu.x, frag)) << 32;
     st_stream32(d + 32, seq, w5, 0ull, 0ull, pol_first);
   }
@@ -764,8 +792,11 @@ int prepare_scatter() {
       e = cudaFuncSetAttribute(wqe_scatter_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
-    e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kMaxSmem);
+    e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(wqe_scatter_vmm_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     if (e != cudaSuccess) return cuda_failure(e);
     // Two histograms (WQEs and PSNs) of up to 1025 bins per warp.
     const int count_smem = (int)((size_t)kCountWarps * (kMaxRings + 1) * 4 * 2);
@@ -901,12 +932,13 @@ int run(const wqe::Params& p, cudaStream_t s) {
     rc = launch_result();
   }
   if (rc) return rc;
-  void (*scatter)(const wqe::Params) = p.vmm         ? wqe::wqe_scatter_vmm_kernel
-                                       : p.transport ? wqe::wqe_scatter_kernel<true>
-                                                     : wqe::wqe_scatter_kernel<false>;
-  const int sw = p.vmm ? wqe::vmm_scatter_warps(p.V)
+  void (*scatter)(const wqe::Params) =
+      p.vmm ? (p.mtu ? wqe::wqe_scatter_vmm_kernel<true> : wqe::wqe_scatter_vmm_kernel<false>)
+            : p.transport ? wqe::wqe_scatter_kernel<true>
+                          : wqe::wqe_scatter_kernel<false>;
+  const int sw = p.vmm ? wqe::vmm_scatter_warps(p.V, p.mtu != 0)
                        : wqe::scatter_warps(p.V);  // kSWarps, fewer when many rings
-  const size_t smem = p.vmm ? wqe::vmm_scatter_smem(p.V) : wqe::scatter_smem(p.V);
+  const size_t smem = p.vmm ? wqe::vmm_scatter_smem(p.V, p.mtu != 0) : wqe::scatter_smem(p.V);
   const unsigned grid = (unsigned)((p.n_tiles + sw - 1) / sw);
   if (DB_WQE_PDL) return launch_dependent(scatter, grid, sw * 32, smem, s, p);
   scatter<<<grid, sw * 32, smem, s>>>(p);
