@@ -69,8 +69,9 @@ inline unsigned grid_for(uint64_t n) {
 
 // ------------------------------------------------------------------ scan
 // Exclusive scan of n u32 values: block sums, then each block re-scans with
-// its offset, the sum of the earlier blocks' sums (at most 2,048 of them for
-// the largest batch, summed by the block itself). n is known on the host,
+// its offset, the sum of the earlier blocks' sums -- summed by the block
+// itself when there are at most kScanFusedBlocks blocks, else found first by
+// a one-CTA scan of the block sums. n is known on the host,
 // or (Len::dev) worked out on the device as mul * ceil(*dev / div), at most
 // the host's n: the count columns of a sort cover only the tiles that hold
 // items, and the blocks past them return at once.
@@ -117,14 +118,34 @@ __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, 
   block_excl_scan<32>(v, ex, tot, s_w);
   if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
 }
+__global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint64_t n_max,
+                                                           Len len, uint32_t* total) {
+  kernel_prologue();
+  __shared__ uint32_t s_w[32];
+  const uint64_t n = live_len(n_max, len);
+  const uint64_t nb = n ? (n + kScanChunk - 1) / kScanChunk : 1;
+  uint32_t carry = 0;
+  for (uint64_t b0 = 0; b0 < nb; b0 += kScanThreads) {
+    const uint64_t b = b0 + threadIdx.x;
+    const uint32_t v = b < nb ? bsum[b] : 0u;
+    uint32_t ex, tot;
+    block_excl_scan<32>(v, ex, tot, s_w);
+    if (b < nb) bsum[b] = carry + ex;
+    carry += tot;
+    __syncthreads();  // s_w is written again by the next round
+  }
+  if (threadIdx.x == 0 && total) *total = carry;
+}
 // in and out may be the same array: a block reads its whole chunk before
 // writing any of it.
-// The block whose chunk holds item n - 1 (block 0 when n is 0) writes the
-// total.
+// prefixed: bsum holds the blocks' exclusive prefixes (scan_bsums wrote the
+// total); else their sums, and the block whose chunk holds item n - 1 (block
+// 0 when n is 0) writes the total.
+constexpr uint64_t kScanFusedBlocks = 4096;
 __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
                                                            uint64_t n_max, Len len,
                                                            const uint32_t* bsum,
-                                                           uint32_t* total) {
+                                                           uint32_t* total, bool prefixed) {
   kernel_prologue();
   __shared__ uint32_t s_w[32];
   __shared__ uint32_t s_before;
@@ -139,7 +160,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, u
     v += x[g].x + x[g].y + x[g].z + x[g].w;
   }
   uint32_t before = 0;  // the earlier blocks' sums
-  for (uint32_t b = threadIdx.x; b < blockIdx.x; b += kScanThreads) before += bsum[b];
+  for (uint32_t b = threadIdx.x; b < blockIdx.x && !prefixed; b += kScanThreads) before += bsum[b];
   before = warp_sum32(before);
   if (lane == 0) s_w[threadIdx.x >> 5] = before;
   __syncthreads();
@@ -148,12 +169,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, u
     if (threadIdx.x == 0) s_before = y;
   }
   __syncthreads();  // s_w is written again by the scan below
-  const uint32_t block0 = s_before;
+  const uint32_t block0 = prefixed ? bsum[blockIdx.x] : s_before;
   // Lane 0's exclusive prefix (lanes in order) is the total of the warps
   // before this one.
   uint32_t ex, tot;
   block_excl_scan<32>(v, ex, tot, s_w);
-  if (total && threadIdx.x == 0 && blockIdx.x == (n ? (n - 1) / kScanChunk : 0))
+  if (!prefixed && total && threadIdx.x == 0 && blockIdx.x == (n ? (n - 1) / kScanChunk : 0))
     *total = block0 + tot;
   uint32_t run = block0 + __shfl_sync(kFull, ex, 0);
 #pragma unroll
@@ -187,8 +208,10 @@ int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_
   }
   const uint64_t nb = ceil_div(n, kScanChunk);
   launch_dep(scan_reduce, (unsigned)nb, kScanThreads, 0, s, in, n, len, bsum);
+  const bool prefixed = nb > kScanFusedBlocks;
+  if (prefixed) launch_dep(scan_bsums, 1, kScanThreads, 0, s, bsum, n, len, total);
   launch_dep(scan_apply, (unsigned)nb, kScanThreads, 0, s, in, out, n, len,
-             (const uint32_t*)bsum, total);
+             (const uint32_t*)bsum, total, prefixed);
   return launch_result();
 }
 

@@ -346,6 +346,21 @@ def test_deregister_against_the_oracle(db, oracle, n, m):
          DEREG_KEYS)
 
 
+def test_deregister_past_the_fused_scan_limit(db, oracle):
+    """40,000,000 records: the survivors' compaction scans more blocks than a
+    block sums the earlier blocks' totals for itself, so the block totals are
+    scanned first by one CTA."""
+    n, m = 40_000_000, 1_000_000
+    rng = np.random.default_rng(40)
+    s = np.arange(n, dtype=np.uint64) * np.uint64(0x10000)
+    e = s + np.uint64(0x8000)
+    lk = (np.arange(n, dtype=np.uint64) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    refs = rng.integers(1, 3, size=n).astype(np.uint32)
+    hs = rng.integers(-1, n, size=m).astype(np.int64)
+    same(deregister(db, hs, s, e, lk, refs), oracle.mr_deregister(hs, s, e, lk, refs),
+         DEREG_KEYS)
+
+
 def test_deregister_full_size(db, oracle):
     import synth
     d = synth.mr_deregister()
