@@ -173,3 +173,13 @@ def test_full_size_workload(db, oracle):
     last = np.searchsorted(d["mr_start"], base, side="right") - 1
     hit = got["idx"] >= 0
     assert (got["idx"][hit] != last[hit]).mean() > 0.02
+
+
+def test_five_million_overlapping_records(db, oracle):
+    """5,000,000 overlapping records (4,883 blocks of the prefix maximum of
+    the ends, more than one scan round of the block maxima) and 1,000,000
+    queries against the oracle."""
+    rng = np.random.default_rng(50)
+    start, end, lkey = overlapping_table(rng, 5_000_000, 40_000_000, 64)
+    q = queries_near(rng, start, end, 1_000_000, (40_000_000 + 64) * 4096)
+    check(run_gpu(db, q, start, end, lkey), oracle.mr_prefix_max(q, start, end, lkey))
