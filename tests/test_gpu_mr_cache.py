@@ -159,6 +159,32 @@ def test_register_against_the_oracle(db, oracle, n, m, span, granule_shift):
         assert {3, 4, 5} <= kinds and (n == 0 or {1, 2} & kinds)
 
 
+@pytest.mark.parametrize("order", ["shrinking", "growing", "one_range", "same_start"])
+def test_register_chains(db, oracle, order):
+    """3,000 requests on a chain of ranges: each nested in the one before
+    (every later one a hit on the first), each holding the one before (every
+    one a new record), one range asked for 3,000 times, and ranges of one
+    start and growing ends (a new record each, none holding the next)."""
+    m, g = 3000, 4096
+    i = np.arange(m, dtype=np.uint64)
+    if order == "shrinking":
+        a, sz = i * np.uint64(g), (np.uint64(2 * m) - i) * np.uint64(g)
+    elif order == "growing":
+        a, sz = (np.uint64(m) - i) * np.uint64(g), (np.uint64(1) + i * np.uint64(2)) * np.uint64(g)
+    elif order == "one_range":
+        a, sz = np.full(m, 5 * g, np.uint64), np.full(m, 7 * g, np.uint64)
+    else:
+        a, sz = np.full(m, 5 * g, np.uint64), (np.uint64(1) + i) * np.uint64(g)
+    q = np.stack([a + np.uint64(1 << 30), sz], axis=1).astype(np.uint64)
+    s = np.array([0x1000], np.uint64)
+    e = np.array([0x3000], np.uint64)
+    lk = np.array([9], np.uint32)
+    refs = np.array([2], np.uint32)
+    nl = np.arange(m, dtype=np.uint32) + np.uint32(100)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs)
+    same(register(db, q, nl, s, e, lk, refs), want, REG_KEYS)
+
+
 @pytest.mark.parametrize("m,pages,granule_shift", [(700, 40, 12), (5000, 300, 12),
                                                     (150000, 3000, 12), (400000, 100000, 12),
                                                     (60000, 2000, 16)])
