@@ -125,6 +125,12 @@ MUTANTS = [
      "status[k] = left[i] == 0 ? 1 : 0;", "status[k] = left[i] <= 1 ? 1 : 0;"),
     ("deregister: a released record takes more",
      "if (i < 0 || (uint64_t)i >= n || left[i] == 0) {", "if (i < 0 || (uint64_t)i >= n) {"),
+    ("deregister: survivors keep their old references",
+     "o_refs[w] = (uint32_t)left[i];", "o_refs[w] = refs[i];"),
+    ("deregister: a removed record keeps its place",
+     "      remap[i] = -1;\n      continue;", "      remap[i] = -1;\n      ++w;\n      continue;"),
+    ("deregister: stale handles not counted",
+     "      status[k] = 2;\n      n_stale += 1;", "      status[k] = 2;\n      n_stale += 0;"),
     ("cq phase tag read from bit 15",
      "const uint32_t tag = (entry[3] >> 16) & 1u;", "const uint32_t tag = (entry[3] >> 15) & 1u;"),
     ("cq phase kept across the wrap",
