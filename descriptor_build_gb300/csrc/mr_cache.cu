@@ -658,16 +658,22 @@ __device__ __forceinline__ uint64_t corank_warp(const uint64_t* L, uint64_t nL, 
   if (lo + lane < hi) t = R[d - (lo + lane) - 1] <= L[lo + lane];
   return lo + __popc(__ballot_sync(kFull, t));
 }
-constexpr size_t kCdqMergeSmem = (size_t)kCdqTile * (8 + 8 + 4 * 3);
-__global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32_t* n_dev,
+// The slices' ends, keys, query ids and answers are staged in shared memory;
+// thread t makes outputs 4t .. 4t + 3 of the tile: it finds how many of the
+// first 4t come from the left slice (a search on the merge path inside the
+// slices) and merges four from there, left first on equal ends. A right item
+// taken after c items of the left run (i0 before the slice) is a query over
+// the left run's prefix of length c.
+constexpr size_t kCdqMergeSmem = (size_t)kCdqTile * (8 + 4 * 3);
+// Three CTAs per SM (at most 42 registers a thread) measured faster than two.
+__global__ void __launch_bounds__(kCdqThreads, 3) cdq_merge(CdqBufs b, const uint32_t* n_dev,
                                                          uint32_t level) {
   kernel_prologue();
   extern __shared__ __align__(16) unsigned char cdq_smem[];
   uint64_t* seg = reinterpret_cast<uint64_t*>(cdq_smem);  // left slice, then right slice
-  uint64_t* oe = seg + kCdqTile;
-  uint32_t* ok = reinterpret_cast<uint32_t*>(oe + kCdqTile);
-  uint32_t* oq = ok + kCdqTile;
-  uint32_t* oa = oq + kCdqTile;
+  uint32_t* sk = reinterpret_cast<uint32_t*>(seg + kCdqTile);
+  uint32_t* sq = sk + kCdqTile;
+  uint32_t* sa = sq + kCdqTile;
   __shared__ uint64_t s_i0, s_i1;
   __shared__ uint32_t s_w[kCdqThreads / 32];
   const uint64_t n = *n_dev;
@@ -709,68 +715,61 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
       __syncthreads();
       continue;
     }
-    const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0);
-    // Thread t owns items t, t + kCdqThreads, ... of the two slices: it loads
-    // their end into shared memory and their key, query id and answer into
-    // registers, all before the search, so no load waits on it.
-    uint32_t rk[kCdqPer], rq[kCdqPer], ra[kCdqPer];
-#pragma unroll
-    for (int u = 0; u < kCdqPer; ++u) {
-      const uint32_t x = threadIdx.x + u * kCdqThreads;
-      rk[u] = rq[u] = ra[u] = kNone;
-      if (x < na + nb) {
-        const uint64_t gi = x < na ? pb + i0 + x : rb + j0 + (x - na);
-        seg[x] = E[gi];
-        rk[u] = Kin[gi];
-        rq[u] = Qin[gi];
-        ra[u] = Ain[gi];
-      }
+    const uint32_t na = (uint32_t)(i1 - i0), nb = (uint32_t)(j1 - j0), nt = na + nb;
+    for (uint32_t x = threadIdx.x; x < nt; x += kCdqThreads) {
+      const uint64_t gi = x < na ? pb + i0 + x : rb + j0 + (x - na);
+      seg[x] = E[gi];
+      sk[x] = Kin[gi];
+      sq[x] = Qin[gi];
+      sa[x] = Ain[gi];
     }
     __syncthreads();
     const uint64_t* sl = seg;
     const uint64_t* sr = seg + na;
-#pragma unroll
-    for (int u = 0; u < kCdqPer; ++u) {
-      const uint32_t x = threadIdx.x + u * kCdqThreads;
-      if (x >= na + nb) continue;
-      const bool from_left = x < na;
-      const uint64_t ex = seg[x];
-      uint32_t lo = 0, hi = from_left ? nb : na;
-      const uint64_t* o = from_left ? sr : sl;
-      while (lo < hi) {  // other-slice items ahead of this one
+    const uint32_t base = threadIdx.x * kCdqPer;
+    uint64_t oe[kCdqPer];
+    uint32_t ok[kCdqPer], oq[kCdqPer], oa[kCdqPer];
+    {
+      // left items among the first `base` outputs: the least ia in [lo, hi]
+      // with sr[base - ia - 1] > sl[ia] (a right item is ahead only with a
+      // strictly greater end), hi when there is none
+      uint32_t lo = base > nb ? base - nb : 0u, hi = base < na ? base : na;
+      while (lo < hi) {
         const uint32_t mid = (lo + hi) >> 1;
-        const uint64_t v = o[mid];
-        if (v > ex || (!from_left && v == ex)) lo = mid + 1;
+        if (sr[base - mid - 1] <= sl[mid]) lo = mid + 1;
         else hi = mid;
       }
-      const uint32_t q = rq[u];
-      uint32_t a = ra[u];
-      if (!from_left && q != kNone) {
-        const uint64_t c = i0 + lo;  // left-run items with an end at least ex
-        if (c > 0) {
-          const uint64_t j = pb + c - 1;
-          a = min(a, min(PMin[j], CPMin[j / kCdqTile]));
+      uint32_t ia = lo, ib = base - lo;
+#pragma unroll
+      for (int u = 0; u < kCdqPer; ++u) {
+        oe[u] = 0;
+        ok[u] = oq[u] = oa[u] = kNone;
+        if (base + u >= nt) continue;
+        const bool left = ib >= nb || (ia < na && sl[ia] >= sr[ib]);
+        const uint32_t x = left ? ia : na + ib;
+        uint32_t a = sa[x];
+        const uint32_t q = sq[x];
+        if (!left && q != kNone) {
+          const uint64_t c = i0 + ia;  // left-run items with an end at least this one's
+          if (c > 0) {
+            const uint64_t j = pb + c - 1;
+            a = min(a, min(PMin[j], CPMin[j / kCdqTile]));
+          }
         }
+        oe[u] = seg[x];
+        ok[u] = sk[x];
+        oq[u] = q;
+        oa[u] = a;
+        if (left) ++ia;
+        else ++ib;
       }
-      const uint32_t pos = (from_left ? x : x - na) + lo;
-      if (pos >= na + nb) {  // impossible for sorted slices; reported, not written
-        atomicOr(b.err, DB_ERR_TABLE_ORDER);
-        continue;
-      }
-      oe[pos] = ex;
-      ok[pos] = rk[u];
-      oq[pos] = q;
-      oa[pos] = a;
     }
-    __syncthreads();
-    // write the tile out with its prefix minima of the keys
-    const uint32_t nt = (uint32_t)(o1 - o0);
-    const uint32_t base = threadIdx.x * kCdqPer;
+    // prefix minima of the keys over the tile's outputs, and the write-out
     uint32_t v[kCdqPer];
     uint32_t run = kNone;
   #pragma unroll
     for (int u = 0; u < kCdqPer; ++u) {
-      run = min(run, base + u < nt ? ok[base + u] : kNone);
+      run = min(run, ok[u]);
       v[u] = run;
     }
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -778,22 +777,33 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_merge(CdqBufs b, const uint32
   #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(kFull, x, o);
-      if (lane >= (uint32_t)o) x = min(x, y);
+      if (lane >= o) x = min(x, y);
     }
     if (lane == 31) s_w[warp] = x;
     const uint32_t up = __shfl_up_sync(kFull, x, 1);
     __syncthreads();
     uint32_t before = lane ? up : kNone;
     for (uint32_t w = 0; w < warp; ++w) before = min(before, s_w[w]);
-    for (uint32_t t = threadIdx.x; t < nt; t += kCdqThreads) {
-      Eo[o0 + t] = oe[t];
-      Ko[o0 + t] = ok[t];
-      Qo[o0 + t] = oq[t];
-      Ao[o0 + t] = oa[t];
-    }
+    if (base + kCdqPer <= nt) {
+      uint64_t* ep = Eo + o0 + base;
+      reinterpret_cast<ulonglong2*>(ep)[0] = make_ulonglong2(oe[0], oe[1]);
+      reinterpret_cast<ulonglong2*>(ep)[1] = make_ulonglong2(oe[2], oe[3]);
+      *reinterpret_cast<uint4*>(Ko + o0 + base) = make_uint4(ok[0], ok[1], ok[2], ok[3]);
+      *reinterpret_cast<uint4*>(Qo + o0 + base) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+      *reinterpret_cast<uint4*>(Ao + o0 + base) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+      *reinterpret_cast<uint4*>(PMo + o0 + base) =
+          make_uint4(min(before, v[0]), min(before, v[1]), min(before, v[2]), min(before, v[3]));
+    } else {
   #pragma unroll
-    for (int u = 0; u < kCdqPer; ++u)
-      if (base + u < nt) PMo[o0 + base + u] = min(before, v[u]);
+      for (int u = 0; u < kCdqPer; ++u) {
+        if (base + u >= nt) break;
+        Eo[o0 + base + u] = oe[u];
+        Ko[o0 + base + u] = ok[u];
+        Qo[o0 + base + u] = oq[u];
+        Ao[o0 + base + u] = oa[u];
+        PMo[o0 + base + u] = min(before, v[u]);
+      }
+    }
     if (threadIdx.x == kCdqThreads - 1) {
       uint32_t all = kNone;
       for (int w = 0; w < kCdqThreads / 32; ++w) all = min(all, s_w[w]);
