@@ -576,38 +576,42 @@ __global__ void __launch_bounds__(kCdqThreads) cdq_tile(const uint64_t* e_in,
     __syncthreads();
     int cur = 0;
     for (uint32_t s = 1; s < nt; s <<= 1) {
-      // place every item in the merge of its run with the neighbouring one
+      // Outputs 4t .. 4t + 3 of the merge of each run with the neighbouring
+      // one: where they start on the merge path, then four steps, left first
+      // on equal ends. A right item taken after c left items takes the least
+      // key of the left run's first c (its prefix minima, pm).
       const uint16_t* oc = cur ? ord1 : ord0;
       uint16_t* on = cur ? ord0 : ord1;
-  #pragma unroll
-      for (int u = 0; u < kCdqPer; ++u) {
-        const uint32_t i = threadIdx.x * kCdqPer + u;
-        if (i >= nt) continue;
-        const uint32_t x = oc[i];
-        const uint64_t ex = se[x];
-        const uint32_t r = i / s, pb = (r & ~1u) * s;
-        uint32_t pos;
-        if ((r & 1u) == 0) {  // left run: after the right run's items with a greater end
-          uint32_t lo = pb + s < nt ? pb + s : nt, hi = pb + 2 * s < nt ? pb + 2 * s : nt;
-          const uint32_t base = lo;
-          while (lo < hi) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (se[oc[mid]] > ex) lo = mid + 1;
-            else hi = mid;
-          }
-          pos = (i - pb) + (lo - base);
-        } else {  // right run: after the left run's items with an end at least its own
-          uint32_t lo = pb, hi = pb + s;
-          while (lo < hi) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (se[oc[mid]] >= ex) lo = mid + 1;
-            else hi = mid;
-          }
-          const uint32_t cnt = lo - pb;
-          if (sq[x] != kNone && cnt > 0) sa[x] = min(sa[x], pm[pb + cnt - 1]);
-          pos = (i - pb - s) + cnt;
+      const uint32_t first = threadIdx.x * kCdqPer;
+      if (first < nt) {
+        uint32_t pb = first / (2 * s) * (2 * s);
+        uint32_t nl = nt - pb < s ? nt - pb : s;
+        uint32_t nr = pb + s < nt ? (nt - pb - s < s ? nt - pb - s : s) : 0u;
+        const uint32_t d = first - pb;
+        uint32_t lo = d > nr ? d - nr : 0u, hi = d < nl ? d : nl;
+        while (lo < hi) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (se[oc[pb + s + d - mid - 1]] <= se[oc[pb + mid]]) lo = mid + 1;
+          else hi = mid;
         }
-        on[pb + pos] = (uint16_t)x;
+        uint32_t ia = lo, ib = d - lo;
+  #pragma unroll
+        for (int u = 0; u < kCdqPer; ++u) {
+          const uint32_t o = first + u;
+          if (o >= nt) break;
+          if (o - pb == 2 * s) {  // runs of one or two: the next pair of runs
+            pb = o;
+            nl = nt - pb < s ? nt - pb : s;
+            nr = pb + s < nt ? (nt - pb - s < s ? nt - pb - s : s) : 0u;
+            ia = ib = 0;
+          }
+          const bool left = ib >= nr || (ia < nl && se[oc[pb + ia]] >= se[oc[pb + s + ib]]);
+          const uint32_t x = left ? oc[pb + ia] : oc[pb + s + ib];
+          if (!left && ia > 0 && sq[x] != kNone) sa[x] = min(sa[x], pm[pb + ia - 1]);
+          on[o] = (uint16_t)x;
+          if (left) ++ia;
+          else ++ib;
+        }
       }
       __syncthreads();
       cur ^= 1;
