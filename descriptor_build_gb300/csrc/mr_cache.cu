@@ -25,7 +25,9 @@
 //   5. the new records are numbered in table order; a second dominance pass
 //      gives every request the lowest-positioned record holding it when it
 //      is made (an old one, or a new one made before it);
-//   6. old and new records are merged, handles, kinds, remap and counters.
+//   6. every request's kind and handle are resolved in one pass (the
+//      places of the records in the merged table are known by then), then
+//      old and new records are merged into the output table.
 // Deregistration counts each record's handles; only a record whose last
 // reference the batch reaches needs its handles' batch order, found in a
 // bucket of its own (no sort); survivors are compacted by a scan.
@@ -1074,13 +1076,14 @@ __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cf
 // point[j] says so, and the other new records stay out of the second
 // dominance pass (a request they could answer has a holder that is in it at
 // a position no later, or keeps its old record either way). nold[j] is the
-// number of old records starting at or before it (its place in the merged
-// table is j + nold[j]).
+// number of old records starting at or before it, so its place in the merged
+// table is npos[j] = j + nold[j].
 __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* cp,
                            const uint64_t* cb, const uint64_t* db, const uint64_t* de,
                            const uint32_t* first, const uint8_t* again, const uint64_t* start,
                            uint64_t n_mr, uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
-                           uint32_t* creator_of, uint64_t* cend, uint8_t* point, uint32_t* nold) {
+                           uint32_t* creator_of, uint64_t* cend, uint8_t* point, uint32_t* nold,
+                           uint32_t* npos) {
   kernel_prologue();
   const uint64_t u = h->u, d = h->d;
   FOR_EACH(c, n_max) {
@@ -1114,6 +1117,7 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
     cend[c] = e;
     const uint64_t o = count_below(start, n_mr, b, true);  // first old record starting past b
     nold[j] = (uint32_t)o;
+    npos[j] = (uint32_t)(j + o);  // its place in the merged table
     const bool pt = again[p] || (p + 1 < d && db[p + 1] < e) || (o < n_mr && start[o] < e);
     point[j] = pt ? 1 : 0;
   }
@@ -1121,12 +1125,15 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
 // reach[o] = the largest end of a new record starting before old record o
 // (a prefix maximum of cend over the list, which is in start order): a hit
 // on o can be taken by a new record only if its end is within that reach.
-// onew[o] = the number of new records starting before old record o (its
-// place in the merged table is o + onew[o]).
+// onew[o] = the number of new records starting before old record o; its
+// place in the merged table is remap[o] = o + onew[o] (written when the
+// merged table fits out_cap).
 __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t* pmax,
-                          const uint64_t* start, uint64_t n, uint64_t* reach, uint32_t* onew) {
+                          const uint64_t* start, uint64_t n, uint64_t o_cap, uint64_t* reach,
+                          uint32_t* onew, int64_t* remap) {
   kernel_prologue();
   const uint64_t u = h->u;
+  const bool fits = n + u <= o_cap;
   FOR_EACH(o, n) {
     const uint64_t s = start[o];
     uint64_t lo = 0, hi = u;  // new records starting before s
@@ -1137,6 +1144,7 @@ __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t
     }
     reach[o] = lo ? pmax[lo - 1] : 0;
     onew[o] = (uint32_t)lo;
+    if (fits) remap[o] = (int64_t)(o + lo);
   }
 }
 // Items of the second dominance pass, in request order: the new records
@@ -1261,13 +1269,18 @@ __global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, cons
     cq_in[at] = c == kNone ? (uint32_t)k : kNone;
   }
 }
-// Every request's record and kind, and the references they add.
+// Every request's record and kind, the references they add, and (when the
+// merged table fits out_cap) its handle: the record's place in the merged
+// table (npos for a new record, remap for an old one), -1 for an invalid
+// request (or, on a table that breaks the order, an unresolved one).
 __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
                             const int32_t* idx, const uint32_t* role, const uint32_t* creator_of,
                             const uint32_t* held, const uint64_t* nstart, const uint64_t* start,
-                            uint32_t* more, uint32_t* nrefs, uint32_t* rec_new, uint8_t* kind1,
-                            RegHeader* h) {
+                            uint32_t* more, uint32_t* nrefs, const uint32_t* npos,
+                            const int64_t* remap, uint64_t n_mr, uint64_t o_cap, int64_t* handle,
+                            uint8_t* kind, RegHeader* h) {
   kernel_prologue();
+  const bool fits = n_mr + h->u <= o_cap;
   FOR_EACH(k, n_q) {
     const uint8_t kd = kind0[k];
     uint32_t rn = kNone;
@@ -1297,8 +1310,10 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
       if (rn != kNone) atomicAdd(&nrefs[rn], 1u);
       else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) atomicAdd(&more[idx[k]], 1u);
     }
-    rec_new[k] = rn;
-    kind1[k] = k1;
+    kind[k] = k1;
+    if (fits)
+      handle[k] = rn != kNone ? (int64_t)npos[rn]
+                  : (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) ? remap[idx[k]] : -1;
   }
 }
 struct PlaceParams {
@@ -1311,7 +1326,6 @@ struct PlaceParams {
   uint32_t *o_lkey, *o_refs;
   uint64_t o_cap;
   int64_t* remap;
-  uint32_t* npos;
   const RegHeader* h;
   const uint32_t* nold;  // old records starting at or before each new one
   const uint32_t* onew;  // new records starting before each old one (null: none)
@@ -1326,7 +1340,7 @@ __global__ void reg_place_old(const PlaceParams p) {
     p.o_end[w] = p.end[i];
     p.o_lkey[w] = p.lkey[i];
     p.o_refs[w] = p.refs[i] + p.more[i];
-    p.remap[i] = (int64_t)w;
+    if (!p.onew) p.remap[i] = (int64_t)w;  // with requests, reg_reach wrote it
   }
 }
 __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
@@ -1340,22 +1354,6 @@ __global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
     p.o_end[w] = p.nend[j];
     p.o_lkey[w] = p.new_lkey[p.nfirst[j]];
     p.o_refs[w] = p.nrefs[j];
-    p.npos[j] = (uint32_t)w;
-  }
-}
-__global__ void reg_handles(const uint8_t* kind1, const int32_t* idx, const uint32_t* rec_new,
-                            uint64_t n_q, const int64_t* remap, const uint32_t* npos,
-                            const RegHeader* h, uint64_t n, uint64_t o_cap, int64_t* handle,
-                            uint8_t* kind) {
-  kernel_prologue();
-  const bool fits = n + h->u <= o_cap;
-  FOR_EACH(k, n_q) {
-    const uint8_t kd = kind1[k];
-    kind[k] = kd;
-    if (!fits) continue;
-    if (rec_new[k] != kNone) handle[k] = npos[rec_new[k]];
-    else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) handle[k] = remap[idx[k]];
-    else handle[k] = -1;  // invalid (or, on a table that breaks the order, unresolved)
   }
 }
 __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_counters* ctr) {
@@ -1370,8 +1368,8 @@ __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_cou
 struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
       diff, nstart, nend, nfirst, nrefs, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
-      ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, rec_new,
-      kind1, again, point, nold, onew, total;
+      ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, again,
+      point, nold, onew, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -1420,8 +1418,6 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.cpm = take(cdq_tiles(q) * 4);
   L.cpm1 = take(cdq_tiles(q) * 4);
   L.held = take(q * 4);
-  L.rec_new = take(q * 4);
-  L.kind1 = take(q);
   L.again = take(q);
   L.point = take(q);
   L.nold = take(q * 4);
@@ -1737,12 +1733,13 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     uint32_t* nold = static_cast<uint32_t*>(at(L.nold));
     launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, db, de, first,
                (const uint8_t*)again, start, n_mr, nstart, nend, nfirst, creator_of, cend, point,
-               nold);
+               nold, npos);
     if ((rc = launch_result())) return rc;
     if ((rc = prefix_max(cend, &h->u, n_q, bmax, pmax, s))) return rc;
     if (n_mr) {
       launch_dep(reg_reach, grid_for(n_mr), kThreads, 0, s, (const RegHeader*)h,
-                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, reach, onew);
+                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, out_cap, reach, onew,
+                 remap);
       if ((rc = launch_result())) return rc;
     }
     // 6. every request's record: the lowest-positioned one holding it when
@@ -1756,22 +1753,18 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     if ((rc = launch_result())) return rc;
     if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->nb, cb_, held, s)))
       return rc;
-    uint32_t* rec_new = static_cast<uint32_t*>(at(L.rec_new));
-    uint8_t* kind1 = static_cast<uint8_t*>(at(L.kind1));
+    // 7. every request's kind and handle
     launch_dep(reg_resolve, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
-               flag, creator_of, held, nstart, start, more, nrefs, rec_new, kind1, h);
+               flag, creator_of, held, nstart, start, more, nrefs, (const uint32_t*)npos,
+               (const int64_t*)remap, n_mr, out_cap, handle, kind, h);
     if ((rc = launch_result())) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h, nold, onew};
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, h, nold, onew};
     if (n_mr) {
       launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
       if ((rc = launch_result())) return rc;
     }
     launch_dep(reg_place_new, grid_for(n_q), kThreads, 0, s, pp, n_q);
-    if ((rc = launch_result())) return rc;
-    // 7. handles and kinds
-    launch_dep(reg_handles, grid_for(n_q), kThreads, 0, s, kind1, idx, rec_new, n_q, remap, npos,
-               h, n_mr, out_cap, handle, kind);
     if ((rc = launch_result())) return rc;
   } else if (n_mr) {
     // no requests: the table is copied through (and checked like a lookup would)
@@ -1779,7 +1772,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                     at(L.lookup), mr::workspace_bytes(n_mr), s, true, (int)granule_shift);
     if (rc) return rc;
     PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, npos, h, nullptr, nullptr};
+                   out_start, out_end, out_lkey, out_refs, out_cap, remap, h, nullptr, nullptr};
     launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
     if ((rc = launch_result())) return rc;
   }
