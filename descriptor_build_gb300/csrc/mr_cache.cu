@@ -25,9 +25,10 @@
 //   5. the new records are numbered in table order; a second dominance pass
 //      gives every request the lowest-positioned record holding it when it
 //      is made (an old one, or a new one made before it);
-//   6. every request's kind and handle are resolved in one pass (the
-//      places of the records in the merged table are known by then), then
-//      old and new records are merged into the output table.
+//   6. each record is written to the merged table by the pass that finds
+//      its place there (old records keep their references; new ones start
+//      at none); one pass then gives every request its kind and handle and
+//      adds its reference to that record.
 // Deregistration counts each record's handles; only a record whose last
 // reference the batch reaches needs its handles' batch order, found in a
 // bucket of its own (no sort); survivors are compacted by a scan.
@@ -1075,17 +1076,20 @@ __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cf
 // starts inside it (an old start lies strictly between its start and end);
 // point[j] says so, and the other new records stay out of the second
 // dominance pass (a request they could answer has a holder that is in it at
-// a position no later, or keeps its old record either way). nold[j] is the
-// number of old records starting at or before it, so its place in the merged
-// table is npos[j] = j + nold[j].
+// a position no later, or keeps its old record either way). Its place in
+// the merged table is npos[j] = j + the old records starting at or before
+// it; when that table fits out_cap the record is written there, with no
+// references yet (reg_resolve adds them).
 __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* cp,
                            const uint64_t* cb, const uint64_t* db, const uint64_t* de,
                            const uint32_t* first, const uint8_t* again, const uint64_t* start,
-                           uint64_t n_mr, uint64_t* nstart, uint64_t* nend, uint32_t* nfirst,
-                           uint32_t* creator_of, uint64_t* cend, uint8_t* point, uint32_t* nold,
-                           uint32_t* npos) {
+                           uint64_t n_mr, const uint32_t* new_lkey, uint64_t o_cap,
+                           uint64_t* nstart, uint64_t* nend, uint32_t* creator_of, uint64_t* cend,
+                           uint8_t* point, uint32_t* npos, uint64_t* o_start, uint64_t* o_end,
+                           uint32_t* o_lkey, uint32_t* o_refs) {
   kernel_prologue();
   const uint64_t u = h->u, d = h->d;
+  const bool fits = n_mr + u <= o_cap;
   FOR_EACH(c, n_max) {
     if (c >= u) break;
     const uint64_t b = cb[c];
@@ -1110,14 +1114,20 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
     const uint64_t j = gs + ge - 1 - c;
     const uint32_t p = cp[c];
     const uint64_t e = de[p];
+    const uint32_t f = first[p];
     nstart[j] = b;
     nend[j] = e;
-    nfirst[j] = first[p];
-    creator_of[first[p]] = (uint32_t)j;
+    creator_of[f] = (uint32_t)j;
     cend[c] = e;
     const uint64_t o = count_below(start, n_mr, b, true);  // first old record starting past b
-    nold[j] = (uint32_t)o;
-    npos[j] = (uint32_t)(j + o);  // its place in the merged table
+    const uint64_t w = j + o;
+    npos[j] = (uint32_t)w;
+    if (fits) {
+      o_start[w] = b;
+      o_end[w] = e;
+      o_lkey[w] = new_lkey[f];
+      o_refs[w] = 0;
+    }
     const bool pt = again[p] || (p + 1 < d && db[p + 1] < e) || (o < n_mr && start[o] < e);
     point[j] = pt ? 1 : 0;
   }
@@ -1125,12 +1135,14 @@ __global__ void reg_cplace(const RegHeader* h, uint64_t n_max, const uint32_t* c
 // reach[o] = the largest end of a new record starting before old record o
 // (a prefix maximum of cend over the list, which is in start order): a hit
 // on o can be taken by a new record only if its end is within that reach.
-// onew[o] = the number of new records starting before old record o; its
-// place in the merged table is remap[o] = o + onew[o] (written when the
-// merged table fits out_cap).
+// Its place in the merged table is remap[o] = o + the new records starting
+// before it; when that table fits out_cap the record is written there with
+// its references before the batch (reg_resolve adds the batch's).
 __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t* pmax,
-                          const uint64_t* start, uint64_t n, uint64_t o_cap, uint64_t* reach,
-                          uint32_t* onew, int64_t* remap) {
+                          const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
+                          const uint32_t* refs, uint64_t n, uint64_t o_cap, uint64_t* reach,
+                          int64_t* remap, uint64_t* o_start, uint64_t* o_end, uint32_t* o_lkey,
+                          uint32_t* o_refs) {
   kernel_prologue();
   const uint64_t u = h->u;
   const bool fits = n + u <= o_cap;
@@ -1143,8 +1155,14 @@ __global__ void reg_reach(const RegHeader* h, const uint64_t* cb, const uint64_t
       else hi = mid;
     }
     reach[o] = lo ? pmax[lo - 1] : 0;
-    onew[o] = (uint32_t)lo;
-    if (fits) remap[o] = (int64_t)(o + lo);
+    if (fits) {
+      const uint64_t w = o + lo;  // old first on equal starts
+      remap[o] = (int64_t)w;
+      o_start[w] = s;
+      o_end[w] = end[o];
+      o_lkey[w] = lkey[o];
+      o_refs[w] = refs[o];
+    }
   }
 }
 // Items of the second dominance pass, in request order: the new records
@@ -1269,16 +1287,16 @@ __global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, cons
     cq_in[at] = c == kNone ? (uint32_t)k : kNone;
   }
 }
-// Every request's record and kind, the references they add, and (when the
-// merged table fits out_cap) its handle: the record's place in the merged
-// table (npos for a new record, remap for an old one), -1 for an invalid
-// request (or, on a table that breaks the order, an unresolved one).
+// Every request's record and kind and, when the merged table fits out_cap,
+// its handle (the record's place in that table: npos for a new record, remap
+// for an old one; -1 for an invalid request or, on a table that breaks the
+// order, an unresolved one) and the reference it adds there.
 __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, const uint8_t* kind0,
                             const int32_t* idx, const uint32_t* role, const uint32_t* creator_of,
                             const uint32_t* held, const uint64_t* nstart, const uint64_t* start,
-                            uint32_t* more, uint32_t* nrefs, const uint32_t* npos,
-                            const int64_t* remap, uint64_t n_mr, uint64_t o_cap, int64_t* handle,
-                            uint8_t* kind, RegHeader* h) {
+                            const uint32_t* npos, const int64_t* remap, uint64_t n_mr,
+                            uint64_t o_cap, int64_t* handle, uint8_t* kind, uint32_t* o_refs,
+                            RegHeader* h) {
   kernel_prologue();
   const bool fits = n_mr + h->u <= o_cap;
   FOR_EACH(k, n_q) {
@@ -1307,53 +1325,28 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
           k1 = DB_MR_NEW_DUP;
         }
       }
-      if (rn != kNone) atomicAdd(&nrefs[rn], 1u);
-      else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) atomicAdd(&more[idx[k]], 1u);
     }
     kind[k] = k1;
-    if (fits)
-      handle[k] = rn != kNone ? (int64_t)npos[rn]
-                  : (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) ? remap[idx[k]] : -1;
+    if (fits) {
+      const int64_t w = rn != kNone ? (int64_t)npos[rn]
+                        : (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) ? remap[idx[k]] : -1;
+      handle[k] = w;
+      if (w >= 0) atomicAdd(&o_refs[w], 1u);
+    }
   }
 }
-struct PlaceParams {
-  const uint64_t *start, *end;
-  const uint32_t *lkey, *refs, *more;
-  uint64_t n;
-  const uint64_t *nstart, *nend;
-  const uint32_t *nfirst, *nrefs, *new_lkey;
-  uint64_t *o_start, *o_end;
-  uint32_t *o_lkey, *o_refs;
-  uint64_t o_cap;
-  int64_t* remap;
-  const RegHeader* h;
-  const uint32_t* nold;  // old records starting at or before each new one
-  const uint32_t* onew;  // new records starting before each old one (null: none)
-};
-__global__ void reg_place_old(const PlaceParams p) {
+// No requests: the table is copied through.
+__global__ void reg_copy(const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
+                         const uint32_t* refs, uint64_t n, uint64_t o_cap, uint64_t* o_start,
+                         uint64_t* o_end, uint32_t* o_lkey, uint32_t* o_refs, int64_t* remap) {
   kernel_prologue();
-  const uint64_t u = p.h->u;
-  if (p.n + u > p.o_cap) return;
-  FOR_EACH(i, p.n) {
-    const uint64_t w = i + (p.onew ? p.onew[i] : 0u);  // old first on equal starts
-    p.o_start[w] = p.start[i];
-    p.o_end[w] = p.end[i];
-    p.o_lkey[w] = p.lkey[i];
-    p.o_refs[w] = p.refs[i] + p.more[i];
-    if (!p.onew) p.remap[i] = (int64_t)w;  // with requests, reg_reach wrote it
-  }
-}
-__global__ void reg_place_new(const PlaceParams p, uint64_t n_max) {
-  kernel_prologue();
-  const uint64_t u = p.h->u;
-  if (p.n + u > p.o_cap) return;
-  FOR_EACH(j, n_max) {
-    if (j >= u) break;
-    const uint64_t w = j + p.nold[j];
-    p.o_start[w] = p.nstart[j];
-    p.o_end[w] = p.nend[j];
-    p.o_lkey[w] = p.new_lkey[p.nfirst[j]];
-    p.o_refs[w] = p.nrefs[j];
+  if (n > o_cap) return;
+  FOR_EACH(i, n) {
+    o_start[i] = start[i];
+    o_end[i] = end[i];
+    o_lkey[i] = lkey[i];
+    o_refs[i] = refs[i];
+    remap[i] = (int64_t)i;
   }
 }
 __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_counters* ctr) {
@@ -1366,10 +1359,10 @@ __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_cou
 }
 
 struct RegLayout {
-  size_t lookup, hdr, idx, lk, kind0, more, flag, pos, key0, key1, val0, val1, counts, bsum,
-      diff, nstart, nend, nfirst, nrefs, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
+  size_t lookup, hdr, idx, lk, kind0, flag, pos, key0, key1, val0, val1, counts, bsum,
+      diff, nstart, nend, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
       ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, again,
-      point, nold, onew, total;
+      point, total;
 };
 RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   RegLayout L;
@@ -1381,7 +1374,6 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.idx = take(q * 4);
   L.lk = take(q * 4);
   L.kind0 = take(q);
-  L.more = take((n_mr ? n_mr : 1) * 4);
   L.flag = take(q * 4);
   L.pos = take(q * 4);
   L.key0 = take(q * 8);
@@ -1393,8 +1385,6 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.diff = take(8);
   L.nstart = take(q * 8);
   L.nend = take(q * 8);
-  L.nfirst = take(q * 4);
-  L.nrefs = take(q * 4);
   L.npos = take(q * 4);
   L.first = take(q * 4);
   L.cp = take(q * 4);
@@ -1420,8 +1410,6 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.held = take(q * 4);
   L.again = take(q);
   L.point = take(q);
-  L.nold = take(q * 4);
-  L.onew = take((n_mr ? n_mr : 1) * 4);
   L.total = o;
   return L;
 }
@@ -1640,7 +1628,6 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
   RegHeader* h = static_cast<RegHeader*>(at(L.hdr));
   int32_t* idx = static_cast<int32_t*>(at(L.idx));
   uint8_t* kind0 = static_cast<uint8_t*>(at(L.kind0));
-  uint32_t* more = static_cast<uint32_t*>(at(L.more));
   uint32_t* flag = static_cast<uint32_t*>(at(L.flag));
   uint32_t* pos = static_cast<uint32_t*>(at(L.pos));
   uint32_t* bsum = static_cast<uint32_t*>(at(L.bsum));
@@ -1650,14 +1637,10 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
               static_cast<unsigned long long*>(at(L.diff))};
   uint64_t* nstart = static_cast<uint64_t*>(at(L.nstart));
   uint64_t* nend = static_cast<uint64_t*>(at(L.nend));
-  uint32_t* nfirst = static_cast<uint32_t*>(at(L.nfirst));
-  uint32_t* nrefs = static_cast<uint32_t*>(at(L.nrefs));
   uint32_t* npos = static_cast<uint32_t*>(at(L.npos));
 
   int rc = 0;
   if (cudaMemsetAsync(h, 0, sizeof(RegHeader), s) != cudaSuccess ||
-      (n_mr && cudaMemsetAsync(more, 0, n_mr * 4, s) != cudaSuccess) ||
-      (n_q && cudaMemsetAsync(nrefs, 0, n_q * 4, s) != cudaSuccess) ||
       (n_q && cudaMemsetAsync(at(L.creator_of), 0xFF, n_q * 4, s) != cudaSuccess))
     return launch_result();
   // 1. lookup against the table as it stands
@@ -1726,20 +1709,19 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
     uint64_t* cend = static_cast<uint64_t*>(at(L.cend));
     uint64_t* reach = static_cast<uint64_t*>(at(L.reach));
-    uint32_t* onew = static_cast<uint32_t*>(at(L.onew));
     launch_dep(reg_clist, grid_for(n_q), kThreads, 0, s, h, n_q, flag, pos, db, cp, cbs);
     if ((rc = launch_result())) return rc;
-    // 5. the new records in table order; old records a new one may precede
-    uint32_t* nold = static_cast<uint32_t*>(at(L.nold));
+    // 5. the new records in table order, and both kinds of record in the
+    //    merged table; old records a new one may precede
     launch_dep(reg_cplace, grid_for(n_q), kThreads, 0, s, h, n_q, cp, cbs, db, de, first,
-               (const uint8_t*)again, start, n_mr, nstart, nend, nfirst, creator_of, cend, point,
-               nold, npos);
+               (const uint8_t*)again, start, n_mr, new_lkey, out_cap, nstart, nend, creator_of,
+               cend, point, npos, out_start, out_end, out_lkey, out_refs);
     if ((rc = launch_result())) return rc;
     if ((rc = prefix_max(cend, &h->u, n_q, bmax, pmax, s))) return rc;
     if (n_mr) {
       launch_dep(reg_reach, grid_for(n_mr), kThreads, 0, s, (const RegHeader*)h,
-                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, n_mr, out_cap, reach, onew,
-                 remap);
+                 (const uint64_t*)cbs, (const uint64_t*)pmax, start, end, lkey, refs, n_mr,
+                 out_cap, reach, remap, out_start, out_end, out_lkey, out_refs);
       if ((rc = launch_result())) return rc;
     }
     // 6. every request's record: the lowest-positioned one holding it when
@@ -1753,27 +1735,18 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     if ((rc = launch_result())) return rc;
     if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->nb, cb_, held, s)))
       return rc;
-    // 7. every request's kind and handle
+    // 7. every request's kind, handle and reference
     launch_dep(reg_resolve, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
-               flag, creator_of, held, nstart, start, more, nrefs, (const uint32_t*)npos,
-               (const int64_t*)remap, n_mr, out_cap, handle, kind, h);
-    if ((rc = launch_result())) return rc;
-    PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, h, nold, onew};
-    if (n_mr) {
-      launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
-      if ((rc = launch_result())) return rc;
-    }
-    launch_dep(reg_place_new, grid_for(n_q), kThreads, 0, s, pp, n_q);
+               flag, creator_of, held, nstart, start, (const uint32_t*)npos,
+               (const int64_t*)remap, n_mr, out_cap, handle, kind, out_refs, h);
     if ((rc = launch_result())) return rc;
   } else if (n_mr) {
     // no requests: the table is copied through (and checked like a lookup would)
     rc = mr::lookup(nullptr, 0, start, end, lkey, n_mr, nullptr, nullptr, nullptr, &h->lookup,
                     at(L.lookup), mr::workspace_bytes(n_mr), s, true, (int)granule_shift);
     if (rc) return rc;
-    PlaceParams pp{start, end, lkey, refs, more, n_mr, nstart, nend, nfirst, nrefs, new_lkey,
-                   out_start, out_end, out_lkey, out_refs, out_cap, remap, h, nullptr, nullptr};
-    launch_dep(reg_place_old, grid_for(n_mr), kThreads, 0, s, pp);
+    launch_dep(reg_copy, grid_for(n_mr), kThreads, 0, s, start, end, lkey, refs, n_mr, out_cap,
+               out_start, out_end, out_lkey, out_refs, remap);
     if ((rc = launch_result())) return rc;
   }
   if (ctr) {
