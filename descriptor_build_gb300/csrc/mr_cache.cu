@@ -955,22 +955,20 @@ __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max,
     key[i] = b >> gshift;
   }
 }
-// Run starts of equal widened ranges over the sorted misses (0 past m).
+// Run starts of equal widened ranges over the sorted misses (the m first
+// flags; their scan reads no further).
 __global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
                          const uint32_t* val, uint32_t* flag) {
   kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
-    uint32_t f = 0;
-    if (i < m) {
-      if (i == 0) {
-        f = 1;
-      } else {
-        uint64_t b0, e0, b1, e1;
-        widen(q, val[i - 1], gshift, b0, e0);
-        widen(q, val[i], gshift, b1, e1);
-        f = (b0 != b1 || e0 != e1);
-      }
+    if (i >= m) break;
+    uint32_t f = 1;
+    if (i > 0) {
+      uint64_t b0, e0, b1, e1;
+      widen(q, val[i - 1], gshift, b0, e0);
+      widen(q, val[i], gshift, b1, e1);
+      f = (b0 != b1 || e0 != e1);
     }
     flag[i] = f;
   }
@@ -1014,21 +1012,19 @@ __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_m
 // that nothing before it reaches (prefix maximum of the ends, pm) is held by
 // none; one before which the next range starts at or past its end holds
 // none: such a range takes no part (held[] = none), and the rest keep their
-// order. keep[] is 1 for the others.
+// order. keep[] is 1 for the others (the d first flags; their scan reads no
+// further).
 __global__ void reg_keep_a(const RegHeader* h, uint64_t n_max, const uint64_t* db,
                            const uint64_t* de, const uint64_t* pm, uint32_t* held,
                            uint32_t* keep) {
   kernel_prologue();
   const uint64_t d = h->d;
   FOR_EACH(p, n_max) {
-    uint32_t k = 0;
-    if (p < d) {
-      const bool nested = p > 0 && pm[p - 1] >= de[p];
-      const bool holds = p + 1 < d && db[p + 1] < de[p];
-      k = (nested || holds) ? 1u : 0u;
-      held[p] = kNone;
-    }
-    keep[p] = k;
+    if (p >= d) break;
+    const bool nested = p > 0 && pm[p - 1] >= de[p];
+    const bool holds = p + 1 < d && db[p + 1] < de[p];
+    held[p] = kNone;
+    keep[p] = (nested || holds) ? 1u : 0u;
   }
 }
 __global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* keep,
@@ -1047,11 +1043,15 @@ __global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* 
 }
 // A distinct range makes a new record when no range before it that holds it
 // was asked for earlier (then its first request finds no record holding it).
+// The d first flags; their scan reads no further.
 __global__ void reg_creators(const RegHeader* h, uint64_t n_max, const uint32_t* first,
                              const uint32_t* held_by, uint32_t* cflag) {
   kernel_prologue();
   const uint64_t d = h->d;
-  FOR_EACH(p, n_max) cflag[p] = p < d && held_by[p] > first[p];
+  FOR_EACH(p, n_max) {
+    if (p >= d) break;
+    cflag[p] = held_by[p] > first[p];
+  }
 }
 // New records in (start ascending, end descending) order: c = cpos[p].
 __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cflag,
@@ -1682,7 +1682,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                 &h->err};
     launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->d, bsum, s))) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->d, bsum, s, Len{&h->m, 1u, 1u}))) return rc;
     uint8_t* again = static_cast<uint8_t*>(at(L.again));
     uint8_t* point = static_cast<uint8_t*>(at(L.point));
     launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
@@ -1694,7 +1694,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_keep_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
                (const uint64_t*)db, (const uint64_t*)de, (const uint64_t*)pmax, held, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->dk, bsum, s))) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->dk, bsum, s, Len{&h->d, 1u, 1u}))) return rc;
     launch_dep(reg_items_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
                (const uint32_t*)flag, (const uint32_t*)pos, (const uint64_t*)de,
                (const uint32_t*)first, cb_.e[1], cb_.key[1], cb_.qid[1]);
@@ -1703,7 +1703,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
       return rc;
     launch_dep(reg_creators, grid_for(n_q), kThreads, 0, s, h, n_q, first, held, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->u, bsum, s))) return rc;
+    if ((rc = scan(flag, pos, n_q, &h->u, bsum, s, Len{&h->d, 1u, 1u}))) return rc;
     uint32_t* cp = static_cast<uint32_t*>(at(L.cp));
     uint64_t* cbs = static_cast<uint64_t*>(at(L.cb));
     uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
