@@ -105,6 +105,11 @@ __device__ __forceinline__ uint64_t scan_group_base(uint32_t g) {
   return (uint64_t)blockIdx.x * kScanChunk + (uint64_t)(threadIdx.x >> 5) * (kScanItems * 32) +
          (uint64_t)g * 128 + 4u * (threadIdx.x & 31);
 }
+// kPopc: the values are the set bits of each word (a scan of flag words).
+__device__ __forceinline__ uint4 popc4(uint4 x) {
+  return make_uint4(__popc(x.x), __popc(x.y), __popc(x.z), __popc(x.w));
+}
+template <bool kPopc>
 __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, uint64_t n_max,
                                                             Len len, uint32_t* bsum) {
   kernel_prologue();
@@ -114,7 +119,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_reduce(const uint32_t* in, 
   uint32_t v = 0;
 #pragma unroll
   for (int g = 0; g < kScanGroups; ++g) {
-    const uint4 x = scan_load4(in, scan_group_base(g), n);
+    uint4 x = scan_load4(in, scan_group_base(g), n);
+    if (kPopc) x = popc4(x);
     v += x.x + x.y + x.z + x.w;
   }
   uint32_t ex, tot;
@@ -145,6 +151,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_bsums(uint32_t* bsum, uint6
 // total); else their sums, and the block whose chunk holds item n - 1 (block
 // 0 when n is 0) writes the total.
 constexpr uint64_t kScanFusedBlocks = 4096;
+template <bool kPopc>
 __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, uint32_t* out,
                                                            uint64_t n_max, Len len,
                                                            const uint32_t* bsum,
@@ -160,6 +167,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, u
 #pragma unroll
   for (int g = 0; g < kScanGroups; ++g) {
     x[g] = scan_load4(in, scan_group_base(g), n);
+    if (kPopc) x[g] = popc4(x[g]);
     v += x[g].x + x[g].y + x[g].z + x[g].w;
   }
   uint32_t before = 0;  // the earlier blocks' sums
@@ -203,19 +211,56 @@ __global__ void __launch_bounds__(kScanThreads) scan_apply(const uint32_t* in, u
   }
 }
 inline size_t scan_tmp_words(uint64_t n) { return (size_t)ceil_div(n ? n : 1, kScanChunk); }
-int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_t* bsum,
-         cudaStream_t s, Len len = Len{nullptr, 0, 1}) {
+template <bool kPopc>
+int scan_t(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_t* bsum,
+           cudaStream_t s, Len len) {
   if (n == 0) {
     if (total) cudaMemsetAsync(total, 0, 4, s);
     return launch_result();
   }
   const uint64_t nb = ceil_div(n, kScanChunk);
-  launch_dep(scan_reduce, (unsigned)nb, kScanThreads, 0, s, in, n, len, bsum);
+  launch_dep(scan_reduce<kPopc>, (unsigned)nb, kScanThreads, 0, s, in, n, len, bsum);
   const bool prefixed = nb > kScanFusedBlocks;
   if (prefixed) launch_dep(scan_bsums, 1, kScanThreads, 0, s, bsum, n, len, total);
-  launch_dep(scan_apply, (unsigned)nb, kScanThreads, 0, s, in, out, n, len,
+  launch_dep(scan_apply<kPopc>, (unsigned)nb, kScanThreads, 0, s, in, out, n, len,
              (const uint32_t*)bsum, total, prefixed);
   return launch_result();
+}
+int scan(const uint32_t* in, uint32_t* out, uint64_t n, uint32_t* total, uint32_t* bsum,
+         cudaStream_t s, Len len = Len{nullptr, 0, 1}) {
+  return scan_t<false>(in, out, n, total, bsum, s, len);
+}
+
+// ------------------------------------------------------------ flag words
+// A flag pass writes one bit per item, 32 consecutive items per word (a
+// warp's ballot). The scan of the words' set bits gives each word the
+// number of flags set before it, so a flagged item's place among them is
+// wpos[i / 32] + the bits set below it in its word. Against a u32 flag and
+// a u32 place per item this moves a 32nd of the bytes.
+__device__ __forceinline__ bool flag_at(const uint32_t* bits, uint64_t i) {
+  return (bits[i >> 5] >> (i & 31)) & 1u;
+}
+__device__ __forceinline__ uint32_t flag_pos(const uint32_t* bits, const uint32_t* wpos,
+                                             uint64_t i) {
+  return wpos[i >> 5] + __popc(bits[i >> 5] & ((1u << (i & 31)) - 1u));
+}
+// Rounds of 32 consecutive items per warp over [0, n): every lane takes part
+// in every round (its item i0 + lane may lie past n), so a round can end in
+// a ballot. Block sizes are multiples of 32.
+#define FOR_EACH_WARP(i0, n)                                                                 \
+  for (uint64_t i0 = (uint64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); i0 < (n); \
+       i0 += (uint64_t)gridDim.x * blockDim.x)
+__device__ __forceinline__ void put_flags(uint32_t* bits, uint64_t i0, bool f) {
+  const uint32_t w = __ballot_sync(kFull, f);
+  if ((threadIdx.x & 31) == 0) bits[i0 >> 5] = w;
+}
+// Scan of the flag words of items [0, n_max), or of the first *n_dev items
+// when n_dev is given (the words past them are not read); *total = the
+// flags set.
+int scan_flags(const uint32_t* bits, uint32_t* wpos, uint64_t n_max, uint32_t* total,
+               uint32_t* bsum, cudaStream_t s, const uint32_t* n_dev = nullptr) {
+  return scan_t<true>(bits, wpos, ceil_div(n_max, 32), total, bsum, s,
+                      n_dev ? Len{n_dev, 1u, 32u} : Len{nullptr, 0, 1});
 }
 
 // ------------------------------------------------------------- radix sort
@@ -929,19 +974,23 @@ __device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gs
   aend = (addr + size + g - 1) & ~(g - 1);  // valid requests only: no wrap
 }
 
-__global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* flag) {
+__global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* bits) {
   kernel_prologue();
-  FOR_EACH(k, n_q) flag[k] = kind0[k] == DB_MR_MISS;
+  FOR_EACH_WARP(k0, n_q) {
+    const uint64_t k = k0 + (threadIdx.x & 31);
+    put_flags(bits, k0, k < n_q && kind0[k] == DB_MR_MISS);
+  }
 }
-__global__ void reg_compact(const db_range* q, const uint32_t* flag, const uint32_t* pos,
+__global__ void reg_compact(const db_range* q, const uint32_t* bits, const uint32_t* wpos,
                             uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val) {
   kernel_prologue();
   FOR_EACH(k, n_q) {
-    if (!flag[k]) continue;
+    if (!flag_at(bits, k)) continue;
     uint64_t b, e;
     widen(q, k, gshift, b, e);
-    key[pos[k]] = ~e >> gshift;  // ends descending
-    val[pos[k]] = (uint32_t)k;
+    const uint32_t at = flag_pos(bits, wpos, k);
+    key[at] = ~e >> gshift;  // ends descending
+    val[at] = (uint32_t)k;
   }
 }
 __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
@@ -955,22 +1004,22 @@ __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max,
     key[i] = b >> gshift;
   }
 }
-// Run starts of equal widened ranges over the sorted misses (the m first
-// flags; their scan reads no further).
-__global__ void reg_runs(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
-                         const uint32_t* val, uint32_t* flag) {
+// Run starts of equal widened ranges over the sorted misses (flags of the
+// m first items; their scan reads no further).
+__global__ void reg_runs(const db_range* q, const RegHeader* h, uint32_t gshift,
+                         const uint32_t* val, uint32_t* bits) {
   kernel_prologue();
   const uint64_t m = h->m;
-  FOR_EACH(i, n_max) {
-    if (i >= m) break;
-    uint32_t f = 1;
-    if (i > 0) {
+  FOR_EACH_WARP(i0, m) {
+    const uint64_t i = i0 + (threadIdx.x & 31);
+    bool f = i < m;
+    if (f && i > 0) {
       uint64_t b0, e0, b1, e1;
       widen(q, val[i - 1], gshift, b0, e0);
       widen(q, val[i], gshift, b1, e1);
       f = (b0 != b1 || e0 != e1);
     }
-    flag[i] = f;
+    put_flags(bits, i0, f);
   }
 }
 // Count of a[0..n) below x (strict) or at most x.
@@ -989,21 +1038,21 @@ __device__ __forceinline__ uint64_t count_below(const uint64_t* a, uint64_t n, u
 // start, end, the request that first asked for it, and whether a later
 // request asked for it again.
 __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_max,
-                             uint32_t gshift, const uint32_t* val, const uint32_t* flag,
-                             const uint32_t* excl, uint64_t* db, uint64_t* de, uint32_t* first,
+                             uint32_t gshift, const uint32_t* val, const uint32_t* bits,
+                             const uint32_t* wpos, uint64_t* db, uint64_t* de, uint32_t* first,
                              uint8_t* again) {
   kernel_prologue();
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
-    if (!flag[i]) continue;
-    const uint32_t p = excl[i];
+    if (!flag_at(bits, i)) continue;
+    const uint32_t p = flag_pos(bits, wpos, i);
     uint64_t b, e;
     widen(q, val[i], gshift, b, e);
     db[p] = b;
     de[p] = e;
     first[p] = val[i];
-    again[p] = (i + 1 < m && !flag[i + 1]) ? 1 : 0;
+    again[p] = (i + 1 < m && !flag_at(bits, i + 1)) ? 1 : 0;
   }
 }
 // Items of the first dominance pass: a distinct range is a query for the
@@ -1012,19 +1061,22 @@ __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_m
 // that nothing before it reaches (prefix maximum of the ends, pm) is held by
 // none; one before which the next range starts at or past its end holds
 // none: such a range takes no part (held[] = none), and the rest keep their
-// order. keep[] is 1 for the others (the d first flags; their scan reads no
-// further).
-__global__ void reg_keep_a(const RegHeader* h, uint64_t n_max, const uint64_t* db,
-                           const uint64_t* de, const uint64_t* pm, uint32_t* held,
-                           uint32_t* keep) {
+// order. The others are flagged (flags of the d first items; their scan
+// reads no further).
+__global__ void reg_keep_a(const RegHeader* h, const uint64_t* db, const uint64_t* de,
+                           const uint64_t* pm, uint32_t* held, uint32_t* keep) {
   kernel_prologue();
   const uint64_t d = h->d;
-  FOR_EACH(p, n_max) {
-    if (p >= d) break;
-    const bool nested = p > 0 && pm[p - 1] >= de[p];
-    const bool holds = p + 1 < d && db[p + 1] < de[p];
-    held[p] = kNone;
-    keep[p] = (nested || holds) ? 1u : 0u;
+  FOR_EACH_WARP(p0, d) {
+    const uint64_t p = p0 + (threadIdx.x & 31);
+    bool k = false;
+    if (p < d) {
+      const bool nested = p > 0 && pm[p - 1] >= de[p];
+      const bool holds = p + 1 < d && db[p + 1] < de[p];
+      held[p] = kNone;
+      k = nested || holds;
+    }
+    put_flags(keep, p0, k);
   }
 }
 __global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* keep,
@@ -1034,8 +1086,8 @@ __global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* 
   const uint64_t d = h->d;
   FOR_EACH(p, n_max) {
     if (p >= d) break;
-    if (!keep[p]) continue;
-    const uint32_t at = kpos[p];
+    if (!flag_at(keep, p)) continue;
+    const uint32_t at = flag_pos(keep, kpos, p);
     ce_in[at] = de[p];
     ck_in[at] = first[p];
     cq_in[at] = (uint32_t)p;
@@ -1043,14 +1095,14 @@ __global__ void reg_items_a(const RegHeader* h, uint64_t n_max, const uint32_t* 
 }
 // A distinct range makes a new record when no range before it that holds it
 // was asked for earlier (then its first request finds no record holding it).
-// The d first flags; their scan reads no further.
-__global__ void reg_creators(const RegHeader* h, uint64_t n_max, const uint32_t* first,
-                             const uint32_t* held_by, uint32_t* cflag) {
+// Flags of the d first items; their scan reads no further.
+__global__ void reg_creators(const RegHeader* h, const uint32_t* first, const uint32_t* held_by,
+                             uint32_t* cflag) {
   kernel_prologue();
   const uint64_t d = h->d;
-  FOR_EACH(p, n_max) {
-    if (p >= d) break;
-    cflag[p] = held_by[p] > first[p];
+  FOR_EACH_WARP(p0, d) {
+    const uint64_t p = p0 + (threadIdx.x & 31);
+    put_flags(cflag, p0, p < d && held_by[p] > first[p]);
   }
 }
 // New records in (start ascending, end descending) order: c = cpos[p].
@@ -1060,9 +1112,10 @@ __global__ void reg_clist(const RegHeader* h, uint64_t n_max, const uint32_t* cf
   const uint64_t d = h->d;
   FOR_EACH(p, n_max) {
     if (p >= d) break;
-    if (!cflag[p]) continue;
-    cp[cpos[p]] = (uint32_t)p;
-    cb[cpos[p]] = db[p];
+    if (!flag_at(cflag, p)) continue;
+    const uint32_t c = flag_pos(cflag, cpos, p);
+    cp[c] = (uint32_t)p;
+    cb[c] = db[p];
   }
 }
 // Table order of the new records: start ascending, then end ascending (a
@@ -1174,18 +1227,19 @@ __global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, cons
                           const int32_t* idx, const uint64_t* reach, const uint32_t* creator_of,
                           const uint8_t* point, uint32_t* role) {
   kernel_prologue();
-  FOR_EACH(k, n_q) {
-    const uint8_t kd = kind0[k];
-    uint32_t r = 0;
+  FOR_EACH_WARP(k0, n_q) {
+    const uint64_t k = k0 + (threadIdx.x & 31);
+    bool r = false;
+    const uint8_t kd = k < n_q ? kind0[k] : (uint8_t)DB_MR_INVALID;
     if (kd == DB_MR_MISS) {
       const uint32_t c = creator_of[k];
-      r = c == kNone ? 1u : point[c];
+      r = c == kNone || point[c];
     } else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) {
       uint64_t b, e;
       widen(q, k, gshift, b, e);
       r = reach[idx[k]] >= e;  // a new record starting before the old one may hold it
     }
-    role[k] = r;
+    put_flags(role, k0, r);
   }
 }
 
@@ -1277,10 +1331,10 @@ __global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, cons
                           uint32_t* ck_in, uint32_t* cq_in) {
   kernel_prologue();
   FOR_EACH(k, n_q) {
-    if (!role[k]) continue;
+    if (!flag_at(role, k)) continue;
     uint64_t b, e;
     widen(q, k, gshift, b, e);
-    const uint32_t at = rpos[k];
+    const uint32_t at = flag_pos(role, rpos, k);
     const uint32_t c = creator_of[k];
     ce_in[at] = e;
     ck_in[at] = c;                       // kNone unless k made a record
@@ -1310,7 +1364,7 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
       if (c != kNone) {
         rn = c;
         k1 = DB_MR_NEW;
-      } else if (role[k]) {
+      } else if (flag_at(role, k)) {
         const uint32_t w = held[k];  // the least-positioned new record reaching e, made before k
         const bool holds = w != kNone && nstart[w] <= b;
         if (kd == DB_MR_MISS) {
@@ -1374,8 +1428,8 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.idx = take(q * 4);
   L.lk = take(q * 4);
   L.kind0 = take(q);
-  L.flag = take(q * 4);
-  L.pos = take(q * 4);
+  L.flag = take(ceil_div(q, 32) * 4);  // flag words
+  L.pos = take(ceil_div(q, 32) * 4);   // their exclusive prefix
   L.key0 = take(q * 8);
   L.key1 = take(q * 8);
   L.val0 = take(q * 4);
@@ -1652,7 +1706,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     // 2. the misses, compacted in request order
     launch_dep(reg_mark, grid_for(n_q), kThreads, 0, s, kind0, n_q, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->m, bsum, s))) return rc;
+    if ((rc = scan_flags(flag, pos, n_q, &h->m, bsum, s))) return rc;
     launch_dep(reg_compact, grid_for(n_q), kThreads, 0, s,
                q, flag, pos, n_q, granule_shift, sb.key[0],
                sb.val[0]);
@@ -1680,9 +1734,10 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                 static_cast<uint32_t*>(at(L.cmin)),
                 {static_cast<uint32_t*>(at(L.cpm)), static_cast<uint32_t*>(at(L.cpm1))}, n_q,
                 &h->err};
-    launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag);
+    launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, granule_shift,
+               sval, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->d, bsum, s, Len{&h->m, 1u, 1u}))) return rc;
+    if ((rc = scan_flags(flag, pos, n_q, &h->d, bsum, s, &h->m))) return rc;
     uint8_t* again = static_cast<uint8_t*>(at(L.again));
     uint8_t* point = static_cast<uint8_t*>(at(L.point));
     launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
@@ -1691,19 +1746,20 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
     uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
     if ((rc = prefix_max(de, &h->d, n_q, bmax, pmax, s))) return rc;
-    launch_dep(reg_keep_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
+    launch_dep(reg_keep_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h,
                (const uint64_t*)db, (const uint64_t*)de, (const uint64_t*)pmax, held, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->dk, bsum, s, Len{&h->d, 1u, 1u}))) return rc;
+    if ((rc = scan_flags(flag, pos, n_q, &h->dk, bsum, s, &h->d))) return rc;
     launch_dep(reg_items_a, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h, n_q,
                (const uint32_t*)flag, (const uint32_t*)pos, (const uint64_t*)de,
                (const uint32_t*)first, cb_.e[1], cb_.key[1], cb_.qid[1]);
     if ((rc = launch_result())) return rc;
     if ((rc = cdq_dominance_min(cb_.e[1], cb_.key[1], cb_.qid[1], &h->dk, cb_, held, s)))
       return rc;
-    launch_dep(reg_creators, grid_for(n_q), kThreads, 0, s, h, n_q, first, held, flag);
+    launch_dep(reg_creators, grid_for(n_q), kThreads, 0, s, (const RegHeader*)h,
+               (const uint32_t*)first, (const uint32_t*)held, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->u, bsum, s, Len{&h->d, 1u, 1u}))) return rc;
+    if ((rc = scan_flags(flag, pos, n_q, &h->u, bsum, s, &h->d))) return rc;
     uint32_t* cp = static_cast<uint32_t*>(at(L.cp));
     uint64_t* cbs = static_cast<uint64_t*>(at(L.cb));
     uint32_t* creator_of = static_cast<uint32_t*>(at(L.creator_of));
@@ -1729,7 +1785,7 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_roles, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, kind0, idx,
                (const uint64_t*)reach, (const uint32_t*)creator_of, (const uint8_t*)point, flag);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(flag, pos, n_q, &h->nb, bsum, s))) return rc;
+    if ((rc = scan_flags(flag, pos, n_q, &h->nb, bsum, s))) return rc;
     launch_dep(reg_items, grid_for(n_q), kThreads, 0, s, q, n_q, granule_shift, flag, pos,
                creator_of, cb_.e[1], cb_.key[1], cb_.qid[1]);
     if ((rc = launch_result())) return rc;
