@@ -544,9 +544,10 @@ def time_mr_mutation(args, device, stream, only=None) -> dict:
                           "records_before": n, "new_records": u, "algorithmic_bytes": alg,
                           "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                           "note": "not part of the step: timed alone; the requests' one-at-a-time "
-                                  "result: lookup, 14 radix passes, two dominance passes (merge "
-                                  "sorts on the end), merge; 150 launches, each a programmatic "
-                                  "dependent of the one before"}
+                                  "result: lookup, one radix sort of the misses on a packed "
+                                  "(start, length) key, two dominance passes (merge sorts on the "
+                                  "end), merge; 150 launches, each a programmatic dependent of "
+                                  "the one before"}
     del rb
     if only == "mr_register":
         return out

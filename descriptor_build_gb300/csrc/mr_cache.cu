@@ -16,7 +16,10 @@
 //   3. a stable LSD radix sort (8-bit digits, reduce-then-scan over
 //      4,096-key tiles, in-tile ranks from __match_any_sync) orders them by
 //      widened start ascending, then end descending, so equal ranges are
-//      adjacent and in request order;
+//      adjacent and in request order: one sort on the start granule and the
+//      length in granules packed in one key, or, when a miss's start or
+//      length does not fit that key, a sort on the end and then a stable
+//      one on the start;
 //   4. a distinct range makes a new record unless a range before it in that
 //      order that reaches its end (one that holds it) was asked for earlier:
 //      a dominance pass (a merge sort on the end carrying prefix minima of
@@ -283,13 +286,15 @@ __device__ __forceinline__ uint32_t passes_run_below(uint64_t diff, uint32_t shi
   for (uint32_t t = 0; t < shift; t += 8) c += pass_runs(diff, t) ? 1u : 0u;
   return c;
 }
-// One atomic per CTA: the warps' ORs meet in shared memory first.
+// One atomic per CTA: the warps' ORs meet in shared memory first. With
+// only_if given and *only_if zero no digit is marked, so no pass runs.
 __global__ void __launch_bounds__(kThreads) radix_diff(const uint64_t* key, const uint32_t* n_dev,
+                                                       const uint32_t* only_if,
                                                        unsigned long long* diff) {
   kernel_prologue();
   __shared__ unsigned long long s_or;
   const uint64_t n = *n_dev;
-  if (n == 0) return;
+  if (n == 0 || (only_if && *only_if == 0)) return;
   if (threadIdx.x == 0) s_or = 0;
   __syncthreads();
   const uint64_t k0 = key[0];
@@ -470,8 +475,11 @@ int prepare_scatter() {
 // Sorts by bits [0, bits) of the key; the result is in buffer `cur` on return.
 // skip_shared: look for digits every key shares and skip their passes (a
 // sort whose key width is already tight runs every pass without looking).
+// only_if (with skip_shared): sort only when *only_if is nonzero on the
+// device; otherwise every pass returns at once (the result still lands in
+// buffer `cur`).
 int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip_shared,
-               cudaStream_t s) {
+               cudaStream_t s, const uint32_t* only_if = nullptr) {
   if (int rc = prepare_scatter()) return rc;
   const uint32_t tiles = sort_tiles(b.n_max);
   const uint64_t nc = (uint64_t)256 * tiles;
@@ -482,7 +490,7 @@ int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip
   if (skip_shared) {
     const unsigned dg = grid_for(b.n_max) < (unsigned)num_sms() * 4 ? grid_for(b.n_max)
                                                                       : (unsigned)num_sms() * 4;
-    launch_dep(radix_diff, dg, kThreads, 0, s, b.key[cur0], n_dev, b.diff);
+    launch_dep(radix_diff, dg, kThreads, 0, s, b.key[cur0], n_dev, only_if, b.diff);
     if ((rc = launch_result())) return rc;
   }
   uint32_t passes = 0;
@@ -962,7 +970,8 @@ struct RegHeader {   // 256 bytes at the start of the registration workspace
   uint32_t nb;       // items of the second dominance pass (new records and queries)
   unsigned int err;  // an inconsistency the passes found (DB_ERR_TABLE_ORDER)
   uint32_t dk;       // distinct ranges the first dominance pass needs
-  uint32_t pad[2];
+  uint32_t wide;     // a miss whose start or length does not fit the packed sort key
+  uint32_t pad;
   db_counters lookup;  // counters of the lookup pass
 };
 
@@ -981,27 +990,42 @@ __global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* bits) {
     put_flags(bits, k0, k < n_q && kind0[k] == DB_MR_MISS);
   }
 }
+// The packed sort key: the start granule above kLenBits bits that hold the
+// length in granules complemented, so one ascending sort orders the ranges
+// by start ascending, then end descending. It holds starts below
+// 2^(64 - kLenBits) granules and lengths below 2^kLenBits granules.
+constexpr uint32_t kLenBits = 24;
+constexpr uint64_t kLenMask = (1ull << kLenBits) - 1;
 __global__ void reg_compact(const db_range* q, const uint32_t* bits, const uint32_t* wpos,
-                            uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val) {
+                            uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val,
+                            RegHeader* h) {
   kernel_prologue();
+  bool wide = false;
   FOR_EACH(k, n_q) {
     if (!flag_at(bits, k)) continue;
     uint64_t b, e;
     widen(q, k, gshift, b, e);
+    const uint64_t g = b >> gshift, len = (e - b) >> gshift;
+    const bool fits = (g >> (64 - kLenBits)) == 0 && len <= kLenMask;
+    wide |= !fits;
     const uint32_t at = flag_pos(bits, wpos, k);
-    key[at] = ~e >> gshift;  // ends descending
+    key[at] = (g << kLenBits) | (kLenMask - len);  // rewritten when some miss does not fit
     val[at] = (uint32_t)k;
   }
+  if (__syncthreads_or(wide) && threadIdx.x == 0) atomicOr(&h->wide, 1u);
 }
+// Only when the packed key does not hold every miss: the key of the sort on
+// the end (descending) or, after it, of the stable sort on the start.
 __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max, uint32_t gshift,
-                          const uint32_t* val, uint64_t* key) {
+                          const uint32_t* val, uint64_t* key, bool by_end) {
   kernel_prologue();
+  if (!h->wide) return;
   const uint64_t m = h->m;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
     uint64_t b, e;
     widen(q, val[i], gshift, b, e);
-    key[i] = b >> gshift;
+    key[i] = by_end ? ~e >> gshift : b >> gshift;
   }
 }
 // Run starts of equal widened ranges over the sorted misses (flags of the
@@ -1587,7 +1611,10 @@ __global__ void dereg_status(const int64_t* handle, uint64_t n_h, uint64_t n, co
 // A record survives when its handles leave a reference: c < R.
 __global__ void dereg_keep(const uint32_t* refs, const uint32_t* cnt, uint64_t n, uint32_t* keep) {
   kernel_prologue();
-  FOR_EACH(i, n) keep[i] = refs[i] > cnt[i];
+  FOR_EACH_WARP(i0, n) {
+    const uint64_t i = i0 + (threadIdx.x & 31);
+    put_flags(keep, i0, i < n && refs[i] > cnt[i]);
+  }
 }
 __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const uint32_t* lkey,
                             const uint32_t* refs, const uint32_t* cnt, const uint32_t* keep,
@@ -1595,11 +1622,11 @@ __global__ void dereg_place(const uint64_t* start, const uint64_t* end, const ui
                             uint32_t* o_lkey, uint32_t* o_refs, int64_t* remap) {
   kernel_prologue();
   FOR_EACH(i, n) {
-    if (!keep[i]) {
+    if (!flag_at(keep, i)) {
       remap[i] = -1;
       continue;
     }
-    const uint32_t w = kpos[i];
+    const uint32_t w = flag_pos(keep, kpos, i);
     o_start[w] = start[i];
     o_end[w] = end[i];
     o_lkey[w] = lkey[i];
@@ -1630,8 +1657,8 @@ DeregLayout dereg_layout(uint64_t n_h, uint64_t n_mr) {
   L.rel = take(n * 4);
   L.big = take(n * 4);
   L.bsum = take(scan_tmp_words(n) * 4);
-  L.keep = take(n * 4);
-  L.kpos = take(n * 4);
+  L.keep = take(ceil_div(n, 32) * 4);  // flag words
+  L.kpos = take(ceil_div(n, 32) * 4);
   L.total = o;
   return L;
 }
@@ -1707,18 +1734,21 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_mark, grid_for(n_q), kThreads, 0, s, kind0, n_q, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan_flags(flag, pos, n_q, &h->m, bsum, s))) return rc;
-    launch_dep(reg_compact, grid_for(n_q), kThreads, 0, s,
-               q, flag, pos, n_q, granule_shift, sb.key[0],
-               sb.val[0]);
+    launch_dep(reg_compact, grid_for(n_q), kThreads, 0, s, q, (const uint32_t*)flag,
+               (const uint32_t*)pos, n_q, granule_shift, sb.key[0], sb.val[0], h);
     if ((rc = launch_result())) return rc;
-    // 3. sort the misses by (start ascending, end descending), stable in request order
+    // 3. sort the misses by (start ascending, end descending), stable in
+    //    request order: on the packed key, or on the end and then the start
     const int bits = 64 - (int)granule_shift;
     int cur = 0;
-    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
-    launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sb.val[cur],
-               sb.key[cur]);
+    launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, n_q,
+               granule_shift, (const uint32_t*)sb.val[cur], sb.key[cur], true);
     if ((rc = launch_result())) return rc;
-    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s))) return rc;
+    if ((rc = radix_sort(sb, cur, &h->m, 64, true, s))) return rc;
+    launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, n_q,
+               granule_shift, (const uint32_t*)sb.val[cur], sb.key[cur], false);
+    if ((rc = launch_result())) return rc;
+    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s, &h->wide))) return rc;
     // 4. distinct ranges; a range makes a record when no range that holds it
     //    (one before it in this order reaching its end) was asked for earlier
     const uint32_t* sval = sb.val[cur];
@@ -1876,7 +1906,7 @@ extern "C" int db_mr_deregister(const int64_t* handle, uint64_t n_h, const uint6
   if (n_mr) {
     launch_dep(dereg_keep, grid_for(n_mr), kThreads, 0, s, refs, (const uint32_t*)cnt, n_mr, keep);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(keep, kpos, n_mr, &h->kept, bsum, s))) return rc;
+    if ((rc = scan_flags(keep, kpos, n_mr, &h->kept, bsum, s))) return rc;
     launch_dep(dereg_place, grid_for(n_mr), kThreads, 0, s,
                start, end, lkey, refs, (const uint32_t*)cnt, keep, kpos, n_mr,
                out_start, out_end, out_lkey, out_refs, remap);

@@ -259,6 +259,48 @@ def test_register_sort_digit_patterns(db, oracle, pattern, granule_shift):
     same(got, want, REG_KEYS)
 
 
+@pytest.mark.parametrize("case", ["one_long_range", "one_high_start", "at_the_limits"])
+@pytest.mark.parametrize("granule_shift", [12, 16])
+def test_register_packed_sort_key_limits(db, oracle, case, granule_shift):
+    """The misses are sorted once on a key that packs the start granule
+    above 24 bits of the length in granules when every miss fits it, and
+    else on the end and then on the start: nested ordinary misses with one
+    range 2^24 granules long, or one starting at granule 2^40 (no packed
+    key), or ranges of 2^24 - 1 granules up to granule 2^40 - 1 (the
+    largest that fit)."""
+    rng = np.random.default_rng(len(case) * 31 + granule_shift)
+    m, g = 5000, 1 << granule_shift
+    pages = 3000
+    a = rng.integers(0, pages, size=m).astype(np.uint64) * np.uint64(g)
+    a += rng.integers(0, g, size=m).astype(np.uint64) * (rng.random(m) < 0.3)
+    sz = rng.integers(1, 40 * g, size=m).astype(np.uint64)
+    rep = rng.random(m) < 0.1
+    src = rng.integers(0, m, size=m)
+    a = np.where(rep & (src < np.arange(m)), a[src], a)
+    sz = np.where(rep & (src < np.arange(m)), sz[src], sz)
+    top = np.uint64(1 << 40)                 # the first start granule the key cannot hold
+    longest = np.uint64((1 << 24) - 1)       # the longest length it can
+    if case == "one_long_range":             # holds every other request
+        a[2500], sz[2500] = 0, (longest + np.uint64(1)) * np.uint64(g)
+    elif case == "one_high_start":
+        a[2500], sz[2500] = top * np.uint64(g), np.uint64(3 * g)
+    else:
+        k = np.arange(40, 80)
+        a[k] = (top - np.uint64(1) - np.arange(40, dtype=np.uint64) % np.uint64(3)) * np.uint64(g)
+        sz[k] = (longest - np.arange(40, dtype=np.uint64) % np.uint64(2)) * np.uint64(g)
+        a[4900], sz[4900] = 0, longest * np.uint64(g)
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = rng.integers(0, 2**32, size=m, dtype=np.uint64).astype(np.uint32)
+    s = np.array([0x40 * g, 0x900 * g], np.uint64)
+    e = s + np.uint64(8 * g)
+    lk = np.array([3, 4], np.uint32)
+    refs = np.array([1, 2], np.uint32)
+    want = one_at_a_time(oracle, q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    assert (want["kind"] == 4).sum() > 500 and (want["kind"] == 5).sum() > 500
+    got = register(db, q, nl, s, e, lk, refs, granule_shift=granule_shift)
+    same(got, want, REG_KEYS)
+
+
 @pytest.mark.parametrize("pattern", ["one_handle", "two_records"])
 def test_deregister_sort_digit_patterns(db, oracle, pattern):
     """Handles naming one record (no sort pass runs) or two records apart in
