@@ -996,6 +996,12 @@ __global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* bits) {
 // 2^(64 - kLenBits) granules and lengths below 2^kLenBits granules.
 constexpr uint32_t kLenBits = 24;
 constexpr uint64_t kLenMask = (1ull << kLenBits) - 1;
+// The range a packed key holds.
+__device__ __forceinline__ void unpack_key(uint64_t k, uint32_t gshift, uint64_t& b, uint64_t& e) {
+  const uint64_t g = k >> kLenBits, len = kLenMask - (k & kLenMask);
+  b = g << gshift;
+  e = (g + len) << gshift;
+}
 __global__ void reg_compact(const db_range* q, const uint32_t* bits, const uint32_t* wpos,
                             uint64_t n_q, uint32_t gshift, uint64_t* key, uint32_t* val,
                             RegHeader* h) {
@@ -1029,19 +1035,26 @@ __global__ void reg_rekey(const db_range* q, const RegHeader* h, uint64_t n_max,
   }
 }
 // Run starts of equal widened ranges over the sorted misses (flags of the
-// m first items; their scan reads no further).
+// m first items; their scan reads no further). Packed keys are equal
+// exactly when their ranges are; the end and start keys of the two-sort
+// path are not, so then the ranges are read again.
 __global__ void reg_runs(const db_range* q, const RegHeader* h, uint32_t gshift,
-                         const uint32_t* val, uint32_t* bits) {
+                         const uint32_t* val, const uint64_t* key, uint32_t* bits) {
   kernel_prologue();
   const uint64_t m = h->m;
+  const bool packed = !h->wide;
   FOR_EACH_WARP(i0, m) {
     const uint64_t i = i0 + (threadIdx.x & 31);
     bool f = i < m;
     if (f && i > 0) {
-      uint64_t b0, e0, b1, e1;
-      widen(q, val[i - 1], gshift, b0, e0);
-      widen(q, val[i], gshift, b1, e1);
-      f = (b0 != b1 || e0 != e1);
+      if (packed) {
+        f = key[i] != key[i - 1];
+      } else {
+        uint64_t b0, e0, b1, e1;
+        widen(q, val[i - 1], gshift, b0, e0);
+        widen(q, val[i], gshift, b1, e1);
+        f = (b0 != b1 || e0 != e1);
+      }
     }
     put_flags(bits, i0, f);
   }
@@ -1062,17 +1075,19 @@ __device__ __forceinline__ uint64_t count_below(const uint64_t* a, uint64_t n, u
 // start, end, the request that first asked for it, and whether a later
 // request asked for it again.
 __global__ void reg_distinct(const db_range* q, const RegHeader* h, uint64_t n_max,
-                             uint32_t gshift, const uint32_t* val, const uint32_t* bits,
-                             const uint32_t* wpos, uint64_t* db, uint64_t* de, uint32_t* first,
-                             uint8_t* again) {
+                             uint32_t gshift, const uint32_t* val, const uint64_t* key,
+                             const uint32_t* bits, const uint32_t* wpos, uint64_t* db,
+                             uint64_t* de, uint32_t* first, uint8_t* again) {
   kernel_prologue();
   const uint64_t m = h->m;
+  const bool packed = !h->wide;
   FOR_EACH(i, n_max) {
     if (i >= m) break;
     if (!flag_at(bits, i)) continue;
     const uint32_t p = flag_pos(bits, wpos, i);
     uint64_t b, e;
-    widen(q, val[i], gshift, b, e);
+    if (packed) unpack_key(key[i], gshift, b, e);
+    else widen(q, val[i], gshift, b, e);
     db[p] = b;
     de[p] = e;
     first[p] = val[i];
@@ -1438,7 +1453,7 @@ __global__ void reg_final(const RegHeader* h, uint64_t n, uint64_t o_cap, db_cou
 
 struct RegLayout {
   size_t lookup, hdr, idx, lk, kind0, flag, pos, key0, key1, val0, val1, counts, bsum,
-      diff, nstart, nend, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
+      diff, de, nstart, nend, npos, first, cp, cb, creator_of, cend, pmax, bmax, reach,
       ce0, ce1, ck0, ck1, cq0, cq1, ca0, ca1, cpm_tile, cpm_tile1, cmin, cpm, cpm1, held, again,
       point, total;
 };
@@ -1461,6 +1476,7 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.counts = take(sort_count_words(q) * 4);
   L.bsum = take(scan_tmp_words(sort_count_words(q) > q ? sort_count_words(q) : q) * 4);
   L.diff = take(8);
+  L.de = take(q * 8);
   L.nstart = take(q * 8);
   L.nend = take(q * 8);
   L.npos = take(q * 4);
@@ -1752,8 +1768,9 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     // 4. distinct ranges; a range makes a record when no range that holds it
     //    (one before it in this order reaching its end) was asked for earlier
     const uint32_t* sval = sb.val[cur];
-    uint64_t* db = sb.key[0];  // the sort keys are no longer needed
-    uint64_t* de = sb.key[1];
+    const uint64_t* skey = sb.key[cur];
+    uint64_t* db = sb.key[cur ^ 1];  // free once sorted
+    uint64_t* de = static_cast<uint64_t*>(at(L.de));
     uint32_t* first = static_cast<uint32_t*>(at(L.first));
     uint32_t* held = static_cast<uint32_t*>(at(L.held));
     CdqBufs cb_{{static_cast<uint64_t*>(at(L.ce0)), static_cast<uint64_t*>(at(L.ce1))},
@@ -1765,13 +1782,14 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
                 {static_cast<uint32_t*>(at(L.cpm)), static_cast<uint32_t*>(at(L.cpm1))}, n_q,
                 &h->err};
     launch_dep(reg_runs, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, granule_shift,
-               sval, flag);
+               sval, skey, flag);
     if ((rc = launch_result())) return rc;
     if ((rc = scan_flags(flag, pos, n_q, &h->d, bsum, s, &h->m))) return rc;
     uint8_t* again = static_cast<uint8_t*>(at(L.again));
     uint8_t* point = static_cast<uint8_t*>(at(L.point));
-    launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, h, n_q, granule_shift, sval, flag,
-               pos, db, de, first, again);
+    launch_dep(reg_distinct, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, n_q,
+               granule_shift, sval, skey, (const uint32_t*)flag, (const uint32_t*)pos, db, de,
+               first, again);
     if ((rc = launch_result())) return rc;
     uint64_t* pmax = static_cast<uint64_t*>(at(L.pmax));
     uint64_t* bmax = static_cast<uint64_t*>(at(L.bmax));
