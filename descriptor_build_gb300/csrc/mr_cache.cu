@@ -1282,35 +1282,62 @@ __global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, cons
   }
 }
 
-// Inclusive prefix maximum of n u64 values (n on the device, at most n_max):
-// block maxima, their scan by one CTA, then each block with its carry.
+// Inclusive prefix maximum of n u64 values (n on the device, at most n_max).
+// A thread takes kPmItems consecutive values; block maxima first, then each
+// block scans its chunk from the maximum of the blocks before it -- found by
+// the block itself when there are at most kScanFusedBlocks blocks, else by a
+// one-CTA scan of the block maxima.
 constexpr int kMaxScanThreads = 1024;
+constexpr int kPmItems = 8;
+constexpr uint64_t kPmChunk = (uint64_t)kMaxScanThreads * kPmItems;
+__device__ __forceinline__ void pm_load(const uint64_t* in, uint64_t b, uint64_t n,
+                                        uint64_t (&x)[kPmItems]) {
+  if (b + kPmItems <= n) {
+    const ulonglong2* p = reinterpret_cast<const ulonglong2*>(in + b);
+#pragma unroll
+    for (int j = 0; j < kPmItems / 2; ++j) {
+      const ulonglong2 v = p[j];
+      x[2 * j] = v.x;
+      x[2 * j + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPmItems; ++j) x[j] = b + j < n ? in[b + j] : 0;
+  }
+}
+__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+// The maximum over the block (every thread gets it).
+__device__ __forceinline__ uint64_t block_max(uint64_t v, uint64_t* s_w) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max64(v, __shfl_xor_sync(kFull, v, o));
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = s_w[threadIdx.x & 31];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max64(v, __shfl_xor_sync(kFull, v, o));
+  __syncthreads();  // s_w may be written again
+  return v;
+}
 __global__ void __launch_bounds__(kMaxScanThreads) pmax_reduce(const uint64_t* in,
                                                                const uint32_t* n_dev,
                                                                uint64_t* bmax) {
   kernel_prologue();
   __shared__ uint64_t s_w[32];
   const uint64_t n = *n_dev;
-  const uint64_t i = (uint64_t)blockIdx.x * kMaxScanThreads + threadIdx.x;
-  if ((uint64_t)blockIdx.x * kMaxScanThreads >= n) return;
-  uint64_t v = i < n ? in[i] : 0;
+  if ((uint64_t)blockIdx.x * kPmChunk >= n) return;
+  uint64_t x[kPmItems];
+  pm_load(in, (uint64_t)blockIdx.x * kPmChunk + (uint64_t)threadIdx.x * kPmItems, n, x);
+  uint64_t v = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t y = __shfl_xor_sync(kFull, v, o);
-    v = v > y ? v : y;
-  }
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint64_t m = 0;
-    for (int w = 0; w < kMaxScanThreads / 32; ++w) m = m > s_w[w] ? m : s_w[w];
-    bmax[blockIdx.x] = m;
-  }
+  for (int j = 0; j < kPmItems; ++j) v = max64(v, x[j]);
+  v = block_max(v, s_w);
+  if (threadIdx.x == 0) bmax[blockIdx.x] = v;
 }
+// More than kScanFusedBlocks blocks: bmax becomes the exclusive prefix maximum.
 __global__ void __launch_bounds__(1024) pmax_blocks(uint64_t* bmax, const uint32_t* n_dev) {
   kernel_prologue();
   __shared__ uint64_t s_w[32];
-  const uint64_t nb = (*n_dev + kMaxScanThreads - 1) / kMaxScanThreads;
+  const uint64_t nb = (*n_dev + kPmChunk - 1) / kPmChunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t carry = 0;  // the maximum of the blocks before this round
   for (uint64_t b0 = 0; b0 < nb; b0 += 1024) {
@@ -1326,43 +1353,68 @@ __global__ void __launch_bounds__(1024) pmax_blocks(uint64_t* bmax, const uint32
     __syncthreads();
     const uint64_t up = __shfl_up_sync(kFull, x, 1);
     uint64_t ex = lane ? up : 0;  // exclusive within the warp
-    for (int w = 0; w < warp; ++w) ex = ex > s_w[w] ? ex : s_w[w];
-    ex = ex > carry ? ex : carry;
+    for (int w = 0; w < warp; ++w) ex = max64(ex, s_w[w]);
+    ex = max64(ex, carry);
     if (b < nb) bmax[b] = ex;
     uint64_t all = carry;
-    for (int w = 0; w < 32; ++w) all = all > s_w[w] ? all : s_w[w];
+    for (int w = 0; w < 32; ++w) all = max64(all, s_w[w]);
     __syncthreads();  // s_w is written again in the next round
     carry = all;
   }
 }
 __global__ void __launch_bounds__(kMaxScanThreads) pmax_apply(const uint64_t* in,
                                                               const uint32_t* n_dev,
-                                                              const uint64_t* bmax,
+                                                              const uint64_t* bmax, bool prefixed,
                                                               uint64_t* out) {
   kernel_prologue();
   __shared__ uint64_t s_w[32];
   const uint64_t n = *n_dev;
-  if ((uint64_t)blockIdx.x * kMaxScanThreads >= n) return;
-  const uint64_t i = (uint64_t)blockIdx.x * kMaxScanThreads + threadIdx.x;
+  if ((uint64_t)blockIdx.x * kPmChunk >= n) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t x = i < n ? in[i] : 0;
+  const uint64_t b = (uint64_t)blockIdx.x * kPmChunk + (uint64_t)threadIdx.x * kPmItems;
+  uint64_t x[kPmItems];
+  pm_load(in, b, n, x);
+  uint64_t before = 0;  // the blocks before this one
+  if (prefixed) {
+    before = bmax[blockIdx.x];
+  } else {
+    for (uint32_t k = threadIdx.x; k < blockIdx.x; k += kMaxScanThreads)
+      before = max64(before, bmax[k]);
+    before = block_max(before, s_w);
+  }
+#pragma unroll
+  for (int j = 1; j < kPmItems; ++j) x[j] = max64(x[j], x[j - 1]);
+  uint64_t t = x[kPmItems - 1];  // inclusive over the threads up to this one
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o && y > x) x = y;
+    const uint64_t y = __shfl_up_sync(kFull, t, o);
+    if (lane >= o) t = max64(t, y);
   }
-  if (lane == 31) s_w[warp] = x;
+  if (lane == 31) s_w[warp] = t;
   __syncthreads();
-  uint64_t before = bmax[blockIdx.x];
-  for (int w = 0; w < warp; ++w) before = before > s_w[w] ? before : s_w[w];
-  if (i < n) out[i] = before > x ? before : x;
+  uint64_t ex = __shfl_up_sync(kFull, t, 1);
+  ex = lane ? ex : 0;
+  for (int w = 0; w < warp; ++w) ex = max64(ex, s_w[w]);
+  ex = max64(ex, before);
+  if (b + kPmItems <= n) {
+    ulonglong2* p = reinterpret_cast<ulonglong2*>(out + b);
+#pragma unroll
+    for (int j = 0; j < kPmItems / 2; ++j)
+      p[j] = make_ulonglong2(max64(ex, x[2 * j]), max64(ex, x[2 * j + 1]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPmItems; ++j)
+      if (b + j < n) out[b + j] = max64(ex, x[j]);
+  }
 }
 int prefix_max(const uint64_t* in, const uint32_t* n_dev, uint64_t n_max, uint64_t* bmax,
                uint64_t* out, cudaStream_t s) {
-  const unsigned blocks = (unsigned)ceil_div(n_max ? n_max : 1, kMaxScanThreads);
-  launch_dep(pmax_reduce, blocks, kMaxScanThreads, 0, s, in, n_dev, bmax);
-  launch_dep(pmax_blocks, 1, 1024, 0, s, bmax, n_dev);
-  launch_dep(pmax_apply, blocks, kMaxScanThreads, 0, s, in, n_dev, (const uint64_t*)bmax, out);
+  const uint64_t nb = ceil_div(n_max ? n_max : 1, kPmChunk);
+  launch_dep(pmax_reduce, (unsigned)nb, kMaxScanThreads, 0, s, in, n_dev, bmax);
+  const bool prefixed = nb > kScanFusedBlocks;
+  if (prefixed) launch_dep(pmax_blocks, 1, 1024, 0, s, bmax, n_dev);
+  launch_dep(pmax_apply, (unsigned)nb, kMaxScanThreads, 0, s, in, n_dev, (const uint64_t*)bmax,
+             prefixed, out);
   return launch_result();
 }
 __global__ void reg_items(const db_range* q, uint64_t n_q, uint32_t gshift, const uint32_t* role,
@@ -1397,13 +1449,13 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
     uint32_t rn = kNone;
     uint8_t k1 = kd;
     if (kd != DB_MR_INVALID) {
-      uint64_t b, e;
-      widen(q, k, gshift, b, e);
       const uint32_t c = creator_of[k];
       if (c != kNone) {
         rn = c;
         k1 = DB_MR_NEW;
       } else if (flag_at(role, k)) {
+        uint64_t b, e;
+        widen(q, k, gshift, b, e);
         const uint32_t w = held[k];  // the least-positioned new record reaching e, made before k
         const bool holds = w != kNone && nstart[w] <= b;
         if (kd == DB_MR_MISS) {
@@ -1486,7 +1538,7 @@ RegLayout reg_layout(uint64_t n_q, uint64_t n_mr) {
   L.creator_of = take(q * 4);
   L.cend = take(q * 8);
   L.pmax = take(q * 8);
-  L.bmax = take(ceil_div(q, kMaxScanThreads) * 8);
+  L.bmax = take(ceil_div(q, kPmChunk) * 8);
   L.reach = take((n_mr ? n_mr : 1) * 8);
   L.ce0 = take(q * 8);
   L.ce1 = take(q * 8);

@@ -415,9 +415,9 @@ def test_deregister_against_the_oracle(db, oracle, n, m):
 
 
 def test_deregister_past_the_fused_scan_limit(db, oracle):
-    """40,000,000 records: the survivors' compaction scans more blocks than a
-    block sums the earlier blocks' totals for itself, so the block totals are
-    scanned first by one CTA."""
+    """40,000,000 records: the scan of the per-record handle counts runs over
+    more blocks than a block sums the earlier blocks' totals for itself, so
+    the block totals are scanned first by one CTA."""
     n, m = 40_000_000, 1_000_000
     rng = np.random.default_rng(40)
     s = np.arange(n, dtype=np.uint64) * np.uint64(0x10000)
@@ -427,6 +427,39 @@ def test_deregister_past_the_fused_scan_limit(db, oracle):
     hs = rng.integers(-1, n, size=m).astype(np.int64)
     same(deregister(db, hs, s, e, lk, refs), oracle.mr_deregister(hs, s, e, lk, refs),
          DEREG_KEYS)
+
+
+def test_register_past_the_fused_scan_limit(db):
+    """34,000,000 requests: the prefix maxima of the ends run over more blocks
+    than a block takes the earlier blocks' maximum for itself, so the block
+    maxima are scanned first by one CTA. The first request asks for a range
+    holding every later one (and two old records), so the one-at-a-time
+    result is plain: it makes the only new record, at the head of the table,
+    and every later request is a hit on it. A range whose only holder lies
+    blocks away in the sorted order (most of them) would make a record of
+    its own if a block's carry were wrong."""
+    m, g = 34_000_000, 4096
+    assert m > 8192 * 4096
+    rng = np.random.default_rng(34)
+    pages = 10_000_000
+    a = rng.integers(1, pages, size=m).astype(np.uint64) * np.uint64(g)
+    a += rng.integers(0, g, size=m).astype(np.uint64) * (rng.random(m) < 0.3)
+    sz = rng.integers(1, 16 * g, size=m).astype(np.uint64)
+    a[0], sz[0] = 0, np.uint64((pages + 32) * g)
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = (np.arange(m, dtype=np.uint64) * np.uint64(7) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    s = np.array([0x4000 * g, 0x9000 * g], np.uint64)  # inside the first range
+    e = s + np.uint64(8 * g)
+    lk = np.array([3, 4], np.uint32)
+    refs = np.array([1, 2], np.uint32)
+    got = register(db, q, nl, s, e, lk, refs)
+    assert got["ctr"].tolist() == [3, 0, 0, 0]
+    assert got["kind"][0] == 4 and (got["kind"][1:] == 5).all()
+    assert (got["handle"] == 0).all() and got["remap"].tolist() == [1, 2]
+    assert got["start"].tolist() == [0, int(s[0]), int(s[1])]
+    assert got["end"].tolist() == [(pages + 32) * g, int(e[0]), int(e[1])]
+    assert got["lkey"].tolist() == [int(nl[0]), 3, 4]
+    assert got["refs"].tolist() == [m, 1, 2]
 
 
 def test_deregister_full_size(db, oracle):
