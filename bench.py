@@ -546,7 +546,7 @@ def time_mr_mutation(args, device, stream, only=None) -> dict:
                           "note": "not part of the step: timed alone; the requests' one-at-a-time "
                                   "result: lookup, one radix sort of the misses on a packed "
                                   "(start, length) key, two dominance passes (merge sorts on the "
-                                  "end), merge; 150 launches, each a programmatic dependent of "
+                                  "end), merge; 153 launches, each a programmatic dependent of "
                                   "the one before"}
     del rb
     if only == "mr_register":
