@@ -80,13 +80,18 @@ inline unsigned grid_for(uint64_t n) {
 // a one-CTA scan of the block sums. n is known on the host,
 // or (Len::dev) worked out on the device as mul * ceil(*dev / div), at most
 // the host's n: the count columns of a sort cover only the tiles that hold
-// items, and the blocks past them return at once.
+// items, and the blocks past them return at once. With Len::diff given the
+// length is 0 unless bits [shift, shift + 8) of *diff are set (the counts of
+// a sort pass that does not run are not scanned).
 struct Len {
   const uint32_t* dev;
   uint32_t mul, div;
+  const unsigned long long* diff = nullptr;
+  uint32_t shift = 0;
 };
 __device__ __forceinline__ uint64_t live_len(uint64_t n, const Len& l) {
   if (!l.dev) return n;
+  if (l.diff && ((*l.diff >> l.shift) & 255u) == 0) return 0;
   const uint64_t m = (uint64_t)l.mul * ((*l.dev + (uint64_t)l.div - 1) / l.div);
   return m < n ? m : n;
 }
@@ -498,7 +503,8 @@ int radix_sort(SortBufs& b, int& cur, const uint32_t* n_dev, int bits, bool skip
     launch_dep(radix_count, tiles, kSortThreads, 0, s, b.key[0], b.key[1], cur0, b.diff, n_dev,
                (uint32_t)shift, b.counts, tiles);
     if ((rc = launch_result())) return rc;
-    if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s, Len{n_dev, 256u, (uint32_t)kSortTile})))
+    if ((rc = scan(b.counts, b.counts, nc, nullptr, b.bsum, s,
+                   Len{n_dev, 256u, (uint32_t)kSortTile, b.diff, (uint32_t)shift})))
       return rc;
     launch_dep(radix_scatter, tiles, kSortThreads, kScatterSmem, s,
                b.key[0], b.key[1], b.val[0], b.val[1],
@@ -983,11 +989,28 @@ __device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gs
   aend = (addr + size + g - 1) & ~(g - 1);  // valid requests only: no wrap
 }
 
+// Four kinds a lane (one u32 load; kind0 is 4-byte aligned and padded), so
+// a warp round covers 128 requests, four flag words: lanes 8w .. 8w + 7 hold
+// word w's 32 bits, four each, gathered by three shuffles.
 __global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* bits) {
   kernel_prologue();
-  FOR_EACH_WARP(k0, n_q) {
-    const uint64_t k = k0 + (threadIdx.x & 31);
-    put_flags(bits, k0, k < n_q && kind0[k] == DB_MR_MISS);
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x * 4;
+  for (uint64_t b0 = ((uint64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) * 4; b0 < n_q;
+       b0 += stride) {
+    const uint64_t k = b0 + 4 * lane;
+    uint32_t nib = 0;
+    if (k < n_q) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(kind0 + k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k + j < n_q && ((w >> (8 * j)) & 255u) == DB_MR_MISS) nib |= 1u << j;
+    }
+    uint32_t x = nib << (4 * (lane & 7));
+    x |= __shfl_xor_sync(kFull, x, 1);
+    x |= __shfl_xor_sync(kFull, x, 2);
+    x |= __shfl_xor_sync(kFull, x, 4);
+    if ((lane & 7) == 0 && b0 + 4 * lane < n_q) bits[(b0 >> 5) + (lane >> 3)] = x;
   }
 }
 // The packed sort key: the start granule above kLenBits bits that hold the
@@ -1807,7 +1830,6 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     if ((rc = launch_result())) return rc;
     // 3. sort the misses by (start ascending, end descending), stable in
     //    request order: on the packed key, or on the end and then the start
-    const int bits = 64 - (int)granule_shift;
     int cur = 0;
     launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, n_q,
                granule_shift, (const uint32_t*)sb.val[cur], sb.key[cur], true);
@@ -1816,7 +1838,9 @@ extern "C" int db_mr_register(const db_range* q, uint64_t n_q, const uint32_t* n
     launch_dep(reg_rekey, grid_for(n_q), kThreads, 0, s, q, (const RegHeader*)h, n_q,
                granule_shift, (const uint32_t*)sb.val[cur], sb.key[cur], false);
     if ((rc = launch_result())) return rc;
-    if ((rc = radix_sort(sb, cur, &h->m, bits, true, s, &h->wide))) return rc;
+    // 64 bits: an even number of passes, so a sort that does not run leaves
+    // the items where the host expects them (no move back)
+    if ((rc = radix_sort(sb, cur, &h->m, 64, true, s, &h->wide))) return rc;
     // 4. distinct ranges; a range makes a record when no range that holds it
     //    (one before it in this order reaching its end) was asked for earlier
     const uint32_t* sval = sb.val[cur];
