@@ -252,9 +252,9 @@ __device__ __forceinline__ uint32_t flag_pos(const uint32_t* bits, const uint32_
                                              uint64_t i) {
   return wpos[i >> 5] + __popc(bits[i >> 5] & ((1u << (i & 31)) - 1u));
 }
-// Rounds of 32 consecutive items per warp over [0, n): every lane takes part
-// in every round (its item i0 + lane may lie past n), so a round can end in
-// a ballot. Block sizes are multiples of 32.
+// Steps of 32 consecutive items per warp over [0, n): every lane takes part
+// in every step (its item i0 + lane may lie past n), so a step can end in a
+// ballot. Block sizes are multiples of 32.
 #define FOR_EACH_WARP(i0, n)                                                                 \
   for (uint64_t i0 = (uint64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); i0 < (n); \
        i0 += (uint64_t)gridDim.x * blockDim.x)
@@ -990,7 +990,7 @@ __device__ __forceinline__ void widen(const db_range* q, uint64_t k, uint32_t gs
 }
 
 // Four kinds a lane (one u32 load; kind0 is 4-byte aligned and padded), so
-// a warp round covers 128 requests, four flag words: lanes 8w .. 8w + 7 hold
+// a warp step covers 128 requests, four flag words: lanes 8w .. 8w + 7 hold
 // word w's 32 bits, four each, gathered by three shuffles.
 __global__ void reg_mark(const uint8_t* kind0, uint64_t n_q, uint32_t* bits) {
   kernel_prologue();
