@@ -1289,19 +1289,42 @@ __global__ void reg_roles(const db_range* q, uint64_t n_q, uint32_t gshift, cons
                           const int32_t* idx, const uint64_t* reach, const uint32_t* creator_of,
                           const uint8_t* point, uint32_t* role) {
   kernel_prologue();
-  FOR_EACH_WARP(k0, n_q) {
-    const uint64_t k = k0 + (threadIdx.x & 31);
-    bool r = false;
-    const uint8_t kd = k < n_q ? kind0[k] : (uint8_t)DB_MR_INVALID;
-    if (kd == DB_MR_MISS) {
-      const uint32_t c = creator_of[k];
-      r = c == kNone || point[c];
-    } else if (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) {
-      uint64_t b, e;
-      widen(q, k, gshift, b, e);
-      r = reach[idx[k]] >= e;  // a new record starting before the old one may hold it
+  // Two warp steps at a time, so that both steps' dependent loads (the
+  // creator or the old record, then its point flag or reach) are in flight
+  // together.
+  const uint64_t step = (uint64_t)gridDim.x * blockDim.x;
+  const uint32_t lane = threadIdx.x & 31;
+  for (uint64_t k0 = (uint64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); k0 < n_q;
+       k0 += 2 * step) {
+    uint64_t k[2] = {k0 + lane, k0 + step + lane};
+    uint8_t kd[2];
+    uint32_t c[2];
+    int32_t o[2];
+    uint64_t e[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      kd[u] = k[u] < n_q ? kind0[k[u]] : (uint8_t)DB_MR_INVALID;
+      c[u] = kNone;
+      o[u] = 0;
+      e[u] = 0;
+      if (kd[u] == DB_MR_MISS) {
+        c[u] = creator_of[k[u]];
+      } else if (kd[u] == DB_MR_EXACT || kd[u] == DB_MR_CONTAINED) {
+        uint64_t b;
+        widen(q, k[u], gshift, b, e[u]);
+        o[u] = idx[k[u]];
+      }
     }
-    put_flags(role, k0, r);
+    bool r[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      r[u] = false;
+      if (kd[u] == DB_MR_MISS) r[u] = c[u] == kNone || point[c[u]];
+      else if (kd[u] == DB_MR_EXACT || kd[u] == DB_MR_CONTAINED)
+        r[u] = reach[o[u]] >= e[u];  // a new record starting before the old one may hold it
+    }
+    put_flags(role, k0, r[0]);
+    if (k0 + step < n_q) put_flags(role, k0 + step, r[1]);
   }
 }
 
