@@ -1490,39 +1490,64 @@ __global__ void reg_resolve(const db_range* q, uint64_t n_q, uint32_t gshift, co
                             RegHeader* h) {
   kernel_prologue();
   const bool fits = n_mr + h->u <= o_cap;
-  FOR_EACH(k, n_q) {
-    const uint8_t kd = kind0[k];
-    uint32_t rn = kNone;
-    uint8_t k1 = kd;
-    if (kd != DB_MR_INVALID) {
-      const uint32_t c = creator_of[k];
-      if (c != kNone) {
-        rn = c;
-        k1 = DB_MR_NEW;
-      } else if (flag_at(role, k)) {
-        uint64_t b, e;
-        widen(q, k, gshift, b, e);
-        const uint32_t w = held[k];  // the least-positioned new record reaching e, made before k
-        const bool holds = w != kNone && nstart[w] <= b;
-        if (kd == DB_MR_MISS) {
-          if (holds) {
-            rn = w;
-            k1 = DB_MR_NEW_DUP;
-          } else {
-            atomicOr(&h->err, DB_ERR_TABLE_ORDER);  // cannot happen on a valid table
-          }
-        } else if (holds && nstart[w] < start[idx[k]]) {
-          rn = w;  // the new record comes before the old one in the table
-          k1 = DB_MR_NEW_DUP;
-        }
+  // Two requests a thread at a time, their loads in phases (the request,
+  // then its creator or holder, then that record's start and place), so
+  // that both requests' dependent loads are in flight together.
+  const uint64_t step = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t k0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; k0 < n_q; k0 += 2 * step) {
+    uint64_t k[2] = {k0, k0 + step};
+    uint8_t kd[2];
+    uint32_t c[2], w[2];
+    int32_t o[2];
+    bool rl[2];
+    uint64_t b[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      kd[u] = k[u] < n_q ? kind0[k[u]] : (uint8_t)DB_MR_INVALID;
+      const bool valid = kd[u] != DB_MR_INVALID;
+      const bool hit = kd[u] == DB_MR_EXACT || kd[u] == DB_MR_CONTAINED;
+      c[u] = valid ? creator_of[k[u]] : kNone;
+      rl[u] = valid && flag_at(role, k[u]);
+      o[u] = hit ? idx[k[u]] : 0;
+      w[u] = kNone;
+      b[u] = 0;
+      if (rl[u]) {
+        uint64_t e;
+        widen(q, k[u], gshift, b[u], e);
+        w[u] = held[k[u]];  // the least-positioned new record reaching e, made before k
       }
     }
-    kind[k] = k1;
-    if (fits) {
-      const int64_t w = rn != kNone ? (int64_t)npos[rn]
-                        : (kd == DB_MR_EXACT || kd == DB_MR_CONTAINED) ? remap[idx[k]] : -1;
-      handle[k] = w;
-      if (w >= 0) atomicAdd(&o_refs[w], 1u);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (k[u] >= n_q) continue;
+      uint32_t rn = kNone;
+      uint8_t k1 = kd[u];
+      if (kd[u] != DB_MR_INVALID) {
+        if (c[u] != kNone) {
+          rn = c[u];
+          k1 = DB_MR_NEW;
+        } else if (rl[u]) {
+          const bool holds = w[u] != kNone && nstart[w[u]] <= b[u];
+          if (kd[u] == DB_MR_MISS) {
+            if (holds) {
+              rn = w[u];
+              k1 = DB_MR_NEW_DUP;
+            } else {
+              atomicOr(&h->err, DB_ERR_TABLE_ORDER);  // cannot happen on a valid table
+            }
+          } else if (holds && nstart[w[u]] < start[o[u]]) {
+            rn = w[u];  // the new record comes before the old one in the table
+            k1 = DB_MR_NEW_DUP;
+          }
+        }
+      }
+      kind[k[u]] = k1;
+      if (fits) {
+        const int64_t pw = rn != kNone ? (int64_t)npos[rn]
+                           : (kd[u] == DB_MR_EXACT || kd[u] == DB_MR_CONTAINED) ? remap[o[u]] : -1;
+        handle[k[u]] = pw;
+        if (pw >= 0) atomicAdd(&o_refs[pw], 1u);
+      }
     }
   }
 }
