@@ -12,7 +12,8 @@
 // result of the batch's requests made one at a time in batch order:
 //   1. the MR lookup (overlap path, 4 KiB or 64 KiB granules) classifies
 //      every request against the table before the batch;
-//   2. the misses are flagged and compacted by an exclusive scan;
+//   2. the misses are flagged, one bit each in flag words, and compacted by
+//      an exclusive scan of the words' set bits;
 //   3. a stable LSD radix sort (8-bit digits, reduce-then-scan over
 //      4,096-key tiles, in-tile ranks from __match_any_sync) orders them by
 //      widened start ascending, then end descending, so equal ranges are
