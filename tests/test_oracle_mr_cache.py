@@ -365,3 +365,31 @@ def test_one_at_a_time_nesting_hand_case(oracle):
         assert r["handle"].tolist() == [1, 1, 0, 0, 0, 0, 0]
         assert r["remap"].tolist() == [2]
         assert r["ctr"].tolist() == [3, 0, 0, 0]
+
+
+@pytest.mark.parametrize("g", [G4K, G64K])
+def test_one_at_a_time_first_range_holds_the_rest(oracle, g):
+    """A closed form from the per-call definition: the first request asks for
+    a range holding every later request and both old records, so it makes
+    the only new record, first in the table (lowest start), and every later
+    request -- a miss, a repeat, or a range inside an old record, which the
+    new record precedes -- is a hit on it. Its references are the batch's
+    size; the old records keep theirs and move up by one."""
+    rng = np.random.default_rng(70 + g)
+    unit = 1 << g
+    m, pages = 4000, 3000
+    a = rng.integers(1, pages, size=m).astype(np.uint64) * np.uint64(unit)
+    a += rng.integers(0, unit, size=m).astype(np.uint64) * (rng.random(m) < 0.3)
+    sz = rng.integers(1, 16 * unit, size=m).astype(np.uint64)
+    a[0], sz[0] = 0, np.uint64((pages + 32) * unit)
+    q = np.stack([a, sz], axis=1).astype(np.uint64)
+    nl = np.arange(m, dtype=np.uint32) + np.uint32(5)
+    s = np.array([40 * unit, 900 * unit], np.uint64)
+    t = (s, s + np.uint64(8 * unit), np.array([3, 4], np.uint32), np.array([1, 2], np.uint32))
+    for indexed in (False, True):
+        r = oracle.mr_register(q, nl, *t, granule_shift=g, one_at_a_time=True, indexed=indexed)
+        assert r["kind"][0] == 4 and (r["kind"][1:] == 5).all()
+        assert (r["handle"] == 0).all() and r["remap"].tolist() == [1, 2]
+        assert rows_of(r) == [(0, (pages + 32) * unit, 5, m), (40 * unit, 48 * unit, 3, 1),
+                              (900 * unit, 908 * unit, 4, 2)]
+        assert r["ctr"].tolist() == [3, 0, 0, 0]
